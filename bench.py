@@ -1,0 +1,435 @@
+"""Benchmark: routed FP4 MoE expert-FFN decode on one GB300 (or N replicas).
+
+Workload (default `layer_b1`): one MoE layer with 384 resident experts
+(H=4096, I=2880, FP4 E2M1 + ue8m0 per 32, 7.2 GB), top-6 routing, decode batch
+1.  Each step is one moe_ffn_forward call for a fresh token; routings are
+pre-drawn so that consecutive steps share no expert (every step streams its 6
+experts, 112.8 MB, from HBM: inputs far larger than L2).  Steps are replayed
+from CUDA graphs of up to 500 calls.
+
+One JSON line on rank 0.  `value` is tokens/s of the layer summed over ranks
+(each rank an independent replica: "scaling": "weak").  `--impl reference`
+times the CPU oracle instead (on this host's cores).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    "layer_b1": dict(E=384, H=4096, I=2880, k=6, T=1),
+}
+METRIC = "MoE expert-FFN decode tokens/s per layer-stack & HBM GB/s (% of GB300 roofline)"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def expert_bytes(H, I):
+    return 3 * H * I // 2 + 3 * H * I // 32
+
+
+def gate_up_bytes(H, I):
+    return 2 * (H * I // 2 + H * I // 32)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([s.strip() for s in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm = [float(r[1]) for r in self.rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            if len(r) >= 9:
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def draw_routings(R, E, k, T, seed):
+    import numpy as np
+
+    import synth
+
+    idx = np.zeros((R, T, k), np.int32)
+    prev = None
+    for r in range(R):
+        cur = synth.routing_uniform(T, E, k, seed=seed, stream=synth.S_ROUTE + 1000 * (r + 1),
+                                    avoid=prev)
+        idx[r] = cur
+        prev = set(int(v) for v in cur.reshape(-1))
+    w = np.stack([synth.routing_weights(T, k, seed=seed, stream=synth.S_LOGIT + 1000 * (r + 1))
+                  for r in range(R)])
+    return idx, w
+
+
+def traffic_record(kernel):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    rec = d.get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return rec["dram_bytes_per_launch"] if sha == rec["source_sha256"] else None
+
+
+# --------------------------------------------------------------- CPU oracle
+
+def cpu_sample(wl, budget_s=12.0, seed=0):
+    """The oracle, as it stands, on whole tokens of the workload until the
+    budget is used (at least one token).  Returns (tokens/s, threads, sample)."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    E, H, I, k = wl["E"], wl["H"], wl["I"], wl["k"]
+    n = cores()
+    threads = min(n, k)
+    done, spent = 0, 0.0
+    t_tok = []
+    while spent < budget_s and done < 64:
+        idx = synth.routing_uniform(1, E, k, seed=seed + 17, stream=synth.S_ROUTE + 7 * done)
+        w = synth.routing_weights(1, k, seed=seed + 17, stream=synth.S_LOGIT + 7 * done)
+        x = synth.activations_bf16(1, H, seed=seed + 17, n0=H * done)
+        codes, scales = [None] * E, [None] * E
+        for e in set(int(v) for v in idx.reshape(-1)):
+            codes[e], scales[e] = synth.expert_canonical(H, I, e)
+        t0 = time.perf_counter()
+        oracle.moe_ffn(codes, scales, H, I, x, idx, w, nthreads=threads)
+        dt = time.perf_counter() - t0
+        t_tok.append(dt)
+        spent += dt
+        done += 1
+    return done / spent, threads, f"{done} whole tokens of the layer (top-{k} of {E}, H={H}, I={I}), fp64 oracle, {threads} threads over slots"
+
+
+def run_reference(args, wl):
+    """--impl reference: the CPU oracle on this host's cores, same metric."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    E, H, I, k = wl["E"], wl["H"], wl["I"], wl["k"]
+    threads = min(cores(), k)
+    per_token_weights = k * 3 * H * I
+    # calibrate one token
+    idx = synth.routing_uniform(1, E, k, seed=3)
+    w = synth.routing_weights(1, k, seed=3)
+    x = synth.activations_bf16(1, H, seed=3)
+    codes, scales = [None] * E, [None] * E
+    used = set(int(v) for v in idx.reshape(-1))
+    for e in used:
+        codes[e], scales[e] = synth.expert_canonical(H, I, e)
+    t0 = time.perf_counter()
+    oracle.moe_ffn(codes, scales, H, I, x, idx, w, nthreads=threads)
+    t_token = time.perf_counter() - t0
+    budget = 90.0
+    nsteps = args.steps + args.warmup
+    if nsteps * t_token <= budget:
+        mode, rows = "token", None
+        sample = f"one whole token per step (top-{k} of {E}, H={H}, I={I}), {threads} threads"
+    else:
+        mode = "rows"
+        # rows of one gate matrix per step, single thread, sized to the budget
+        t_row = t_token * threads / (k * 3 * I)          # seconds per H-long row, one thread
+        rows = max(1, min(I, int(budget / nsteps / t_row)))
+        threads = 1
+        sample = (f"{rows} gate rows (K={H}) of one expert per step, 1 thread, scaled to "
+                  f"tokens by weights processed")
+    e0 = sorted(used)[0]
+    gc = I * H // 2
+    xr = synth.bf16_bits_to_f32(x[0]).astype(np.float64)
+
+    def step():
+        if mode == "token":
+            oracle.moe_ffn(codes, scales, H, I, x, idx, w, nthreads=threads)
+        else:
+            oracle.matvec(codes[e0][:rows * H // 2], scales[e0][:rows * H // 32], rows, H, xr)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    if mode == "token":
+        value = args.steps / dt
+    else:
+        value = args.steps * rows * H / dt / per_token_weights
+    ms = dt * 1000.0 / args.steps
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "experts": E, "hidden": H, "inter": I, "topk": k,
+                   "tokens_per_step": 1, "l2": "cpu run"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- GPU arm
+
+def run_ours(args, wl):
+    import numpy as np
+    import torch
+
+    import fp4_block_scaled_gb300 as moe
+    import synth
+    from fp4_block_scaled_gb300.experts import ExpertSet
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    E, H, I, k, T = wl["E"], wl["H"], wl["I"], wl["k"], wl["T"]
+    cfg = moe.config(E, H, I, k, T, out_dtype=moe.MOE_OUT_F32)
+    h = moe.moe_ffn_create(cfg, local)
+    es = ExpertSet(h, cfg, device=local)
+    nc, ns = synth.expert_sizes(H, I)
+    tc = torch.empty(nc, dtype=torch.uint8, device="cuda")
+    ts = torch.empty(ns, dtype=torch.uint8, device="cuda")
+    for e in range(E):
+        synth.device_fill_expert(tc.data_ptr(), ts.data_ptr(), H, I, e, seed=0)
+        es.load(e, tc, ts)
+    torch.cuda.synchronize()
+    del tc, ts
+
+    R = 500
+    idx_np, w_np = draw_routings(R, E, k, T, seed=rank)
+    x_np = synth.activations_bf16(R * T, H, seed=rank).reshape(R, T, H)
+    idx_d = torch.from_numpy(idx_np).cuda()
+    w_d = torch.from_numpy(w_np).cuda()
+    x_d = torch.from_numpy(x_np.view(np.int16)).cuda()
+    y_d = torch.empty((R, T, H), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def fwd(i, s):
+        moe.moe_ffn_forward(h, x_d[i], idx_d[i], w_d[i], es.table, y_d[i], T, s)
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                fwd(i % R, torch.cuda.current_stream())
+        return g
+
+    K, W = args.steps, args.warmup
+    chunk = min(K, R)
+    g_full = capture(chunk)
+    rem = K % chunk
+    g_rem = capture(rem) if rem else None
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            fwd(i % R, stream)
+    stream.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps
+    barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(K // chunk):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
+    stream.synchronize()
+    clocks = sampler.stop()
+    barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    if dist is not None:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / K
+    value = world * T * K / (ms_total / 1000.0)
+
+    # algorithmic bytes: distinct experts per step x bytes per expert + activations
+    distinct = [len(set(int(v) for v in idx_np[i % R].reshape(-1))) for i in range(K)]
+    act_io = T * H * 2 + T * H * 4 + 2 * T * k * 4
+    bytes_step = sum(distinct) / K * expert_bytes(H, I) + act_io
+    gbs_step = bytes_step / (ms_step / 1000.0) / 1e9
+
+    # ---- dominant kernel (gate/up) timed with CUDA events on its stream
+    peak, peak_kind = peaks()
+    moe.moe_ffn_profile_enable(h, True)
+    nprof = min(K, 2000)
+    with torch.cuda.stream(stream):
+        for i in range(nprof):
+            fwd(i % R, stream)
+    stream.synchronize()
+    ms_ph, n_ph = moe.moe_ffn_profile_read(h)
+    moe.moe_ffn_profile_enable(h, False)
+    gu_ms = ms_ph[moe.MOE_PHASE_GATE_UP] / max(1, n_ph[moe.MOE_PHASE_GATE_UP])
+    dn_ms = ms_ph[moe.MOE_PHASE_DOWN] / max(1, n_ph[moe.MOE_PHASE_DOWN])
+    pr_ms = ms_ph[moe.MOE_PHASE_PREP] / max(1, n_ph[moe.MOE_PHASE_PREP])
+    gu_dist = sum(len(set(int(v) for v in idx_np[i % R].reshape(-1))) for i in range(nprof)) / nprof
+    gu_bytes = gu_dist * gate_up_bytes(H, I)
+    achieved = gu_bytes / (gu_ms / 1000.0) / 1e9
+    traffic = traffic_record("k_gate_up")
+
+    # ---- end to end through the host-buffer entry point (copies in the timed region)
+    ne2e = min(K, 2000)
+    xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
+    ih = torch.from_numpy(idx_np).pin_memory()
+    wh = torch.from_numpy(w_np).pin_memory()
+    yh = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    for i in range(3):
+        moe.moe_ffn_forward_host(h, xh[i], ih[i], wh[i], es.table, yh, T, stream)
+    t0 = time.perf_counter()
+    for i in range(ne2e):
+        moe.moe_ffn_forward_host(h, xh[i % R], ih[i % R], wh[i % R], es.table, yh, T, stream)
+    e2e_s = time.perf_counter() - t0
+    e2e_value = world * T * ne2e / e2e_s
+    status = moe.moe_ffn_status(h, stream)
+    assert status == moe.MOE_OK, moe.strerror(status)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        v, thr, sample = cpu_sample(wl)
+        cpu = {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16xe2m1->f32", "data": "synthetic",
+            "config": {"workload": args.workload, "experts": E, "hidden": H, "inter": I, "topk": k,
+                       "tokens_per_step": T, "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2: 7.2 GB resident experts, consecutive steps "
+                             "share no expert", "graph_chunk": chunk},
+            "hbm_gbs": gbs_step, "hbm_frac": gbs_step / peak,
+            "bytes_per_step": bytes_step,
+            "phase_us": {"prep": pr_ms * 1e3, "gate_up": gu_ms * 1e3, "down": dn_ms * 1e3},
+            "roofline": {"bound": "hbm", "kernel": "k_gate_up", "achieved": achieved,
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": gu_bytes},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "tokens/s",
+                    "h2d_bytes_per_step": T * H * 2 + 2 * T * k * 4,
+                    "d2h_bytes_per_step": T * H * 4},
+            "gpu_launches": 3 * K,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    moe.moe_ffn_destroy(h)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="layer_b1")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+"""Python binding of libmoe_ffn.so (the GB300 routed FP4 MoE expert-FFN library).
+
+Argument marshalling only: every function forwards to the C entry point of the
+same name in include/moe_ffn.h.  Pointers may be given as ints or as torch
+tensors (their data_ptr() is passed); streams as ints, torch streams or None
+(the legacy default stream).  A nonzero return code raises MoeError.  There is
+no fallback: if the CUDA library cannot be built or loaded, importing the
+binding's functions raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_CUDA = -2
+MOE_ERR_OOM = -3
+MOE_ERR_UNSUPPORTED = -4
+MOE_ERR_BAD_INDEX = -5
+MOE_ERR_DEVICE_TIMEOUT = -6
+
+MOE_ACT_BF16 = 0
+MOE_ACT_E4M3_UE8M0_128 = 1
+MOE_OUT_BF16 = 0
+MOE_OUT_F32 = 1
+
+EXPORTS = [
+    "moe_ffn_packed_codes_bytes", "moe_ffn_packed_scales_bytes", "moe_ffn_create",
+    "moe_ffn_pack_expert", "moe_ffn_forward", "moe_ffn_forward_host", "moe_ffn_route",
+    "moe_ffn_act_quant", "moe_stack_forward", "moe_ffn_profile_enable", "moe_ffn_profile_read",
+    "moe_ffn_status", "moe_ffn_strerror", "moe_ffn_destroy",
+]
+
+MOE_PHASE_PREP = 0
+MOE_PHASE_GATE_UP = 1
+MOE_PHASE_DOWN = 2
+MOE_PHASE_ROUTE = 3
+MOE_PHASE_ACT_QUANT = 4
+MOE_NUM_PHASES = 8
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} ({code})")
+
+
+class moe_ffn_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "num_experts", "hidden", "inter", "topk", "max_tokens", "act_mode", "out_dtype",
+        "gemm_min_tokens")]
+
+
+class moe_expert_table(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile libmoe_ffn.so for sm_103a (in-tree)."""
+    return _build.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        cfgp = ctypes.POINTER(moe_ffn_config)
+        tblp = ctypes.POINTER(moe_expert_table)
+        sig = {
+            "moe_ffn_packed_codes_bytes": (S, [cfgp]),
+            "moe_ffn_packed_scales_bytes": (S, [cfgp]),
+            "moe_ffn_create": (I, [ctypes.POINTER(P), cfgp, I]),
+            "moe_ffn_pack_expert": (I, [P, P, P, P, P, P]),
+            "moe_ffn_forward": (I, [P, P, P, P, tblp, P, I, P]),
+            "moe_ffn_forward_host": (I, [P, P, P, P, tblp, P, I, P]),
+            "moe_ffn_route": (I, [P, P, I, P, P, P, P, P]),
+            "moe_ffn_act_quant": (I, [P, P, I, I, P, P, P]),
+            "moe_stack_forward": (I, [P, P, tblp, P, P, I, I, P]),
+            "moe_ffn_profile_enable": (I, [P, I]),
+            "moe_ffn_profile_read": (I, [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I)]),
+            "moe_ffn_status": (I, [P, P]),
+            "moe_ffn_strerror": (ctypes.c_char_p, [I]),
+            "moe_ffn_destroy": (None, [P]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def library_path() -> str:
+    return os.path.abspath(_build.LIB)
+
+
+def _p(x) -> int | None:
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if isinstance(x, ctypes.Array):
+        return ctypes.addressof(x)
+    return int(x)
+
+
+def _s(stream) -> int | None:
+    if stream is None:
+        return None
+    if hasattr(stream, "cuda_stream"):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != MOE_OK:
+        raise MoeError(rc, where)
+
+
+def strerror(code: int) -> str:
+    return lib().moe_ffn_strerror(int(code)).decode()
+
+
+moe_ffn_strerror = strerror
+
+
+def config(num_experts, hidden, inter, topk, max_tokens, act_mode=MOE_ACT_BF16,
+           out_dtype=MOE_OUT_F32, gemm_min_tokens=0) -> moe_ffn_config:
+    return moe_ffn_config(num_experts, hidden, inter, topk, max_tokens, act_mode, out_dtype,
+                          gemm_min_tokens)
+
+
+def moe_ffn_packed_codes_bytes(cfg: moe_ffn_config) -> int:
+    return lib().moe_ffn_packed_codes_bytes(ctypes.byref(cfg))
+
+
+def moe_ffn_packed_scales_bytes(cfg: moe_ffn_config) -> int:
+    return lib().moe_ffn_packed_scales_bytes(ctypes.byref(cfg))
+
+
+def moe_ffn_create(cfg: moe_ffn_config, device: int = 0) -> int:
+    h = ctypes.c_void_p()
+    _check(lib().moe_ffn_create(ctypes.byref(h), ctypes.byref(cfg), int(device)), "moe_ffn_create")
+    return h.value
+
+
+def moe_ffn_pack_expert(h, canon_codes, canon_scales, packed_codes, packed_scales, stream=None):
+    _check(lib().moe_ffn_pack_expert(h, _p(canon_codes), _p(canon_scales), _p(packed_codes),
+                                     _p(packed_scales), _s(stream)), "moe_ffn_pack_expert")
+
+
+def expert_table(codes_ptrs, scales_ptrs) -> moe_expert_table:
+    """codes_ptrs / scales_ptrs: device arrays (e.g. torch int64 tensors on the
+    GPU) holding one device pointer per expert."""
+    return moe_expert_table(_p(codes_ptrs), _p(scales_ptrs))
+
+
+def moe_ffn_forward(h, x, topk_idx, topk_w, table: moe_expert_table, y, T: int, stream=None):
+    _check(lib().moe_ffn_forward(h, _p(x), _p(topk_idx), _p(topk_w), ctypes.byref(table), _p(y),
+                                 int(T), _s(stream)), "moe_ffn_forward")
+
+
+def moe_ffn_forward_host(h, x, topk_idx, topk_w, table: moe_expert_table, y, T: int, stream=None):
+    _check(lib().moe_ffn_forward_host(h, _p(x), _p(topk_idx), _p(topk_w), ctypes.byref(table),
+                                      _p(y), int(T), _s(stream)), "moe_ffn_forward_host")
+
+
+def moe_ffn_route(h, topk_idx, T: int, counts, offsets, perm, inv, stream=None):
+    _check(lib().moe_ffn_route(h, _p(topk_idx), int(T), _p(counts), _p(offsets), _p(perm), _p(inv),
+                               _s(stream)), "moe_ffn_route")
+
+
+def moe_ffn_act_quant(h, x, rows: int, n: int, codes, scales, stream=None):
+    _check(lib().moe_ffn_act_quant(h, _p(x), int(rows), int(n), _p(codes), _p(scales), _s(stream)),
+           "moe_ffn_act_quant")
+
+
+def moe_stack_forward(h, x, tables, topk_idx, topk_w, L: int, T: int, stream=None):
+    """tables: a sequence of moe_expert_table, one per layer."""
+    arr = (moe_expert_table * len(tables))(*tables)
+    _check(lib().moe_stack_forward(h, _p(x), arr, _p(topk_idx), _p(topk_w), int(L), int(T),
+                                   _s(stream)), "moe_stack_forward")
+
+
+def moe_ffn_profile_enable(h, on: bool = True) -> None:
+    _check(lib().moe_ffn_profile_enable(h, 1 if on else 0), "moe_ffn_profile_enable")
+
+
+def moe_ffn_profile_read(h):
+    """Returns (ms, launches): per-phase summed milliseconds and launch counts."""
+    ms = (ctypes.c_double * MOE_NUM_PHASES)()
+    n = (ctypes.c_int * MOE_NUM_PHASES)()
+    _check(lib().moe_ffn_profile_read(h, ms, n), "moe_ffn_profile_read")
+    return list(ms), list(n)
+
+
+def moe_ffn_status(h, stream=None) -> int:
+    """Returns the (cleared) sticky device status code; does not raise."""
+    return lib().moe_ffn_status(h, _s(stream))
+
+
+def moe_ffn_destroy(h) -> None:
+    lib().moe_ffn_destroy(h)

@@ -1,0 +1,423 @@
+// api.cu -- the C ABI: validation, workspace, launches, graphs, status.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "../../include/moe_ffn.h"
+#include "internal.h"
+
+using namespace moe;
+
+namespace {
+
+struct StackGraph {
+    float* x;
+    const int32_t* idx;
+    const float* w;
+    int L, T;
+    std::vector<const void*> tables;  // codes/scales array pointers per layer
+    cudaGraphExec_t exec;
+    unsigned long long last_use;
+};
+
+}  // namespace
+
+struct moe_ffn {
+    moe_ffn_config cfg;
+    int device;
+    int kc_gu;
+    void* ws;
+    size_t ws_bytes;
+    GemvArgs base;              // workspace pointers, problem sizes
+    int* status;
+    uint16_t* x_stage;          // staging for moe_ffn_forward_host
+    int32_t* idx_stage;
+    float* w_stage;
+    void* y_stage;
+    cudaStream_t cap_stream;    // private stream used only for graph capture
+    std::vector<StackGraph> graphs;
+    unsigned long long use_clock;
+    Profiler* prof;             // non-null while moe_ffn_profile_enable(h, 1)
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int check_cfg(const moe_ffn_config* c)
+{
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->num_experts <= 0 || c->hidden <= 0 || c->inter <= 0 || c->topk <= 0 ||
+        c->max_tokens < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (c->topk > 16 || c->topk > c->num_experts) return MOE_ERR_INVALID_ARG;
+    if (c->act_mode != MOE_ACT_BF16 && c->act_mode != MOE_ACT_E4M3_UE8M0_128)
+        return MOE_ERR_INVALID_ARG;
+    if (c->out_dtype != MOE_OUT_BF16 && c->out_dtype != MOE_OUT_F32) return MOE_ERR_INVALID_ARG;
+    if (c->hidden % 64 || c->inter % 64) return MOE_ERR_UNSUPPORTED;
+    if ((long long)c->hidden * c->inter > (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+    if (c->max_tokens > (1 << 16)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) cudaSetDevice(dev);
+    }
+    ~DeviceGuard()
+    {
+        int cur;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+GemvArgs layer_args(const moe_ffn* h, int T, const int32_t* idx, const float* w,
+                    const moe_expert_table* tbl)
+{
+    GemvArgs a = h->base;
+    a.T = T;
+    a.idx = idx;
+    a.w = w;
+    a.codes = tbl->codes;
+    a.scales = tbl->scales;
+    return a;
+}
+
+int check_forward(const moe_ffn* h, const void* x, const int32_t* idx, const float* w,
+                  const moe_expert_table* tbl, const void* y, int T)
+{
+    if (!h) return MOE_ERR_INVALID_ARG;
+    if (T < 0 || T > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !idx || !w || !y || !tbl || !tbl->codes || !tbl->scales) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(idx, 4) || !aligned(w, 4) ||
+        !aligned(tbl->codes, 8) || !aligned(tbl->scales, 8))
+        return MOE_ERR_INVALID_ARG;
+    if (x == y) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+int run_forward(moe_ffn* h, const void* x, const int32_t* idx, const float* w,
+                const moe_expert_table* tbl, void* y, int T, cudaStream_t s)
+{
+    if (h->cfg.act_mode != MOE_ACT_BF16) return MOE_ERR_UNSUPPORTED;
+    GemvArgs a = layer_args(h, T, idx, w, tbl);
+    a.x_bf16 = (const uint16_t*)x;
+    a.x_resid = nullptr;
+    a.y = y;
+    return cuda_rc(launch_gemv_layer(a, s, true, h->prof));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_ffn_packed_codes_bytes(const moe_ffn_config* cfg)
+{
+    if (check_cfg(cfg) != MOE_OK) return 0;
+    return make_expert_layout(cfg->hidden, cfg->inter).code_bytes;
+}
+
+size_t moe_ffn_packed_scales_bytes(const moe_ffn_config* cfg)
+{
+    if (check_cfg(cfg) != MOE_OK) return 0;
+    return make_expert_layout(cfg->hidden, cfg->inter).scale_bytes;
+}
+
+int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
+{
+    if (!out) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    int rc = check_cfg(cfg);
+    if (rc) return rc;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev)
+        return ndev ? MOE_ERR_INVALID_ARG : MOE_ERR_CUDA;
+    DeviceGuard guard(device);
+
+    moe_ffn* h = new (std::nothrow) moe_ffn();
+    if (!h) return MOE_ERR_OOM;
+    h->cfg = *cfg;
+    h->device = device;
+    h->kc_gu = gemv_default_kc(cfg->hidden);
+    const int T = cfg->max_tokens > 0 ? cfg->max_tokens : 1;
+    const int H = cfg->hidden, I = cfg->inter, k = cfg->topk;
+    GemvWorkspaceSizes g = gemv_workspace_sizes(T, k, H, I, h->kc_gu);
+
+    // one allocation, carved into aligned pieces
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off = align_up(off + bytes, kAlign);
+        return o;
+    };
+    size_t o_status = take(sizeof(int));
+    size_t o_xh = take(g.xh * 2), o_xs = take(g.xs * 4);
+    size_t o_pgu = take(g.part_gu * 4), o_cgu = take(g.cnt_gu * 4);
+    size_t o_hh = take(g.hh * 2), o_hs = take(g.hs * 4);
+    size_t o_pdn = take(g.part_dn * 4), o_cdn = take(g.cnt_dn * 4);
+    size_t o_xst = take((size_t)T * H * 2), o_ist = take((size_t)T * k * 4);
+    size_t o_wst = take((size_t)T * k * 4), o_yst = take((size_t)T * H * 4);
+    h->ws_bytes = off;
+    if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return MOE_ERR_OOM;
+    }
+    if (cudaMemset(h->ws, 0, h->ws_bytes) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
+        cudaFree(h->ws);
+        delete h;
+        return MOE_ERR_CUDA;
+    }
+    char* b = (char*)h->ws;
+    h->status = (int*)(b + o_status);
+    GemvArgs& a = h->base;
+    memset(&a, 0, sizeof(a));
+    a.topk = k;
+    a.E = cfg->num_experts;
+    a.H = H;
+    a.I = I;
+    a.kc_gu = h->kc_gu;
+    a.xs_stride = (H / 32 + 3) / 4 * 4;
+    a.hs_stride = (I / 32 + 3) / 4 * 4;
+    a.eps = 1e-6f;
+    a.xh = (uint16_t*)(b + o_xh);
+    a.xs = (float*)(b + o_xs);
+    a.part_gu = (float*)(b + o_pgu);
+    a.cnt_gu = (int*)(b + o_cgu);
+    a.hh = (uint16_t*)(b + o_hh);
+    a.hs = (float*)(b + o_hs);
+    a.part_dn = (float*)(b + o_pdn);
+    a.cnt_dn = (int*)(b + o_cdn);
+    a.status = h->status;
+    a.out_f32 = cfg->out_dtype == MOE_OUT_F32;
+    h->x_stage = (uint16_t*)(b + o_xst);
+    h->idx_stage = (int32_t*)(b + o_ist);
+    h->w_stage = (float*)(b + o_wst);
+    h->y_stage = (void*)(b + o_yst);
+    *out = h;
+    return MOE_OK;
+}
+
+int moe_ffn_pack_expert(moe_ffn_t h, const void* canon_codes, const void* canon_scales,
+                        void* packed_codes, void* packed_scales, void* stream)
+{
+    if (!h || !canon_codes || !canon_scales || !packed_codes || !packed_scales)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(canon_codes, 16) || !aligned(packed_codes, 16) || !aligned(packed_scales, 16))
+        return MOE_ERR_INVALID_ARG;
+    ExpertLayout L = make_expert_layout(h->cfg.hidden, h->cfg.inter);
+    const char* cc = (const char*)canon_codes;
+    const char* pc = (const char*)packed_codes;
+    if (cc < pc + L.code_bytes && pc < cc + L.code_bytes) return MOE_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    return cuda_rc(launch_pack_expert((const uint8_t*)canon_codes, (const uint8_t*)canon_scales,
+                                      (uint8_t*)packed_codes, (uint8_t*)packed_scales,
+                                      h->cfg.hidden, h->cfg.inter, (cudaStream_t)stream));
+}
+
+int moe_ffn_forward(moe_ffn_t h, const void* x, const int32_t* topk_idx, const float* topk_w,
+                    const moe_expert_table* tbl, void* y, int T, void* stream)
+{
+    int rc = check_forward(h, x, topk_idx, topk_w, tbl, y, T);
+    if (rc || T == 0) return rc;
+    DeviceGuard guard(h->device);
+    return run_forward(h, x, topk_idx, topk_w, tbl, y, T, (cudaStream_t)stream);
+}
+
+int moe_ffn_forward_host(moe_ffn_t h, const void* x_host, const int32_t* idx_host,
+                         const float* w_host, const moe_expert_table* tbl, void* y_host, int T,
+                         void* stream)
+{
+    if (!h) return MOE_ERR_INVALID_ARG;
+    if (T < 0 || T > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x_host || !idx_host || !w_host || !y_host || !tbl || !tbl->codes || !tbl->scales)
+        return MOE_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    cudaStream_t s = (cudaStream_t)stream;
+    const int H = h->cfg.hidden, k = h->cfg.topk;
+    size_t ybytes = (size_t)T * H * (h->cfg.out_dtype == MOE_OUT_F32 ? 4 : 2);
+    cudaError_t e;
+    e = cudaMemcpyAsync(h->x_stage, x_host, (size_t)T * H * 2, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(h->idx_stage, idx_host, (size_t)T * k * 4, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(h->w_stage, w_host, (size_t)T * k * 4, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    int rc = run_forward(h, h->x_stage, h->idx_stage, h->w_stage, tbl, h->y_stage, T, s);
+    if (rc) return rc;
+    e = cudaMemcpyAsync(y_host, h->y_stage, ybytes, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return cuda_rc(e);
+}
+
+int moe_ffn_route(moe_ffn_t h, const int32_t* topk_idx, int T, int32_t* counts, int32_t* offsets,
+                  int32_t* perm, int32_t* inv, void* stream)
+{
+    (void)topk_idx; (void)T; (void)counts; (void)offsets; (void)perm; (void)inv; (void)stream;
+    return h ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
+}
+
+int moe_ffn_act_quant(moe_ffn_t h, const void* x, int rows, int n, uint8_t* codes,
+                      uint8_t* scales, void* stream)
+{
+    (void)x; (void)rows; (void)n; (void)codes; (void)scales; (void)stream;
+    return h ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
+}
+
+int moe_stack_forward(moe_ffn_t h, float* x, const moe_expert_table* tbls,
+                      const int32_t* topk_idx, const float* topk_w, int L, int T, void* stream)
+{
+    if (!h || L < 0 || T < 0 || T > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+    if (L == 0 || T == 0) return MOE_OK;
+    if (!x || !tbls || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(topk_idx, 4) || !aligned(topk_w, 4)) return MOE_ERR_INVALID_ARG;
+    for (int l = 0; l < L; l++)
+        if (!tbls[l].codes || !tbls[l].scales) return MOE_ERR_INVALID_ARG;
+    if (h->cfg.act_mode != MOE_ACT_BF16) return MOE_ERR_UNSUPPORTED;
+    DeviceGuard guard(h->device);
+    cudaStream_t s = (cudaStream_t)stream;
+
+    std::vector<const void*> key(2 * (size_t)L);
+    for (int l = 0; l < L; l++) {
+        key[2 * l] = tbls[l].codes;
+        key[2 * l + 1] = tbls[l].scales;
+    }
+    h->use_clock++;
+    for (auto& gph : h->graphs) {
+        if (gph.x == x && gph.idx == topk_idx && gph.w == topk_w && gph.L == L && gph.T == T &&
+            gph.tables == key) {
+            gph.last_use = h->use_clock;
+            return cuda_rc(cudaGraphLaunch(gph.exec, s));
+        }
+    }
+    // capture the L layers on the private stream, then replay on the caller's
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    cudaError_t le = cudaSuccess;
+    for (int l = 0; l < L && le == cudaSuccess; l++) {
+        GemvArgs a = layer_args(h, T, topk_idx + (size_t)l * T * h->cfg.topk,
+                                topk_w + (size_t)l * T * h->cfg.topk, &tbls[l]);
+        a.x_bf16 = nullptr;
+        a.x_resid = x;
+        a.y = nullptr;
+        le = launch_gemv_layer(a, h->cap_stream, true, nullptr);
+    }
+    e = cudaStreamEndCapture(h->cap_stream, &graph);
+    if (le != cudaSuccess || e != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (h->graphs.size() >= 8) {  // evict the least recently used graph
+        size_t v = 0;
+        for (size_t i = 1; i < h->graphs.size(); i++)
+            if (h->graphs[i].last_use < h->graphs[v].last_use) v = i;
+        cudaGraphExecDestroy(h->graphs[v].exec);
+        h->graphs.erase(h->graphs.begin() + (long)v);
+    }
+    h->graphs.push_back(StackGraph{x, topk_idx, topk_w, L, T, key, exec, h->use_clock});
+    return cuda_rc(cudaGraphLaunch(exec, s));
+}
+
+int moe_ffn_status(moe_ffn_t h, void* stream)
+{
+    if (!h) return MOE_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    cudaStream_t s = (cudaStream_t)stream;
+    int v = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemcpy(&v, h->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (v && cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (v & kStatusTimeout) return MOE_ERR_DEVICE_TIMEOUT;
+    if (v & kStatusBadIndex) return MOE_ERR_BAD_INDEX;
+    return MOE_OK;
+}
+
+int moe_ffn_profile_enable(moe_ffn_t h, int on)
+{
+    if (!h) return MOE_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    if (on && !h->prof) {
+        h->prof = new (std::nothrow) Profiler();
+        if (!h->prof) return MOE_ERR_OOM;
+    } else if (!on && h->prof) {
+        if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+        delete h->prof;
+        h->prof = nullptr;
+    }
+    return MOE_OK;
+}
+
+int moe_ffn_profile_read(moe_ffn_t h, double* ms, int* launches)
+{
+    if (!h || !ms || !launches) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < MOE_NUM_PHASES; i++) {
+        ms[i] = 0.0;
+        launches[i] = 0;
+    }
+    if (!h->prof) return MOE_OK;
+    DeviceGuard guard(h->device);
+    Profiler* p = h->prof;
+    int rc = MOE_OK;
+    for (auto& r : p->recs) {
+        float t = 0.0f;
+        if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+            rc = MOE_ERR_CUDA;
+        if (r.phase >= 0 && r.phase < MOE_NUM_PHASES) {
+            ms[r.phase] += t;
+            launches[r.phase] += 1;
+        }
+        p->pool.push_back(r.a);
+        p->pool.push_back(r.b);
+    }
+    p->recs.clear();
+    return rc;
+}
+
+const char* moe_ffn_strerror(int code)
+{
+    switch (code) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_CUDA: return "CUDA runtime error";
+        case MOE_ERR_OOM: return "out of device memory";
+        case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+        case MOE_ERR_BAD_INDEX: return "expert index out of range (slot contributed zero)";
+        case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        default: return "unknown error code";
+    }
+}
+
+void moe_ffn_destroy(moe_ffn_t h)
+{
+    if (!h) return;
+    DeviceGuard guard(h->device);
+    for (auto& g : h->graphs) cudaGraphExecDestroy(g.exec);
+    delete h->prof;
+    if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+    cudaFree(h->ws);
+    delete h;
+}
+
+}  // extern "C"

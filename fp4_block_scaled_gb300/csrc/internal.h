@@ -1,0 +1,90 @@
+// internal.h -- interfaces between the C ABI (api.cu) and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "layout.h"
+
+namespace moe {
+
+// bits of the sticky device status word
+enum : int { kStatusBadIndex = 1, kStatusTimeout = 2 };
+
+// Arguments of one MoE layer on the GEMV (slot-major) path.
+struct GemvArgs {
+    int T, topk, E, H, I;
+    int kc_gu;                          // K chunks per gate/up unit
+    // inputs: bf16 x (forward) or fp32 residual x (stack, rmsnorm fused)
+    const uint16_t* x_bf16;
+    float* x_resid;
+    float eps;
+    const int32_t* idx;
+    const float* w;
+    const uint8_t* const* codes;
+    const uint8_t* const* scales;
+    // workspace
+    uint16_t* xh;                       // [T][H] f16, block-scaled
+    float* xs;                          // [T][xs_stride] block scales (H/32 used)
+    int xs_stride, hs_stride;           // H/32 and I/32 rounded up to a multiple of 4
+    float* part_gu;                     // [T*k][I/32][kc_gu][64]
+    int* cnt_gu;                        // [T*k][I/32]
+    uint16_t* hh;                       // [T*k][I/32][2][32] f16 hi|lo
+    float* hs;                          // [T*k][hs_stride]
+    float* part_dn;                     // [T][H/16][k][16]
+    int* cnt_dn;                        // [T][H/16]
+    int* status;
+    // output (forward): y [T][H] fp32 or bf16
+    void* y;
+    int out_f32;
+};
+
+// Workspace element counts of the GEMV path for up to T tokens.
+struct GemvWorkspaceSizes {
+    size_t xh, xs, part_gu, cnt_gu, hh, hs, part_dn, cnt_dn;
+};
+GemvWorkspaceSizes gemv_workspace_sizes(int T, int topk, int H, int I, int kc_gu);
+int gemv_default_kc(int H);
+
+// Optional per-phase event recorder (moe_ffn_profile_*); nullptr = off.
+struct Profiler {
+    struct Rec { int phase; cudaEvent_t a, b; };
+    std::vector<Rec> recs;
+    std::vector<cudaEvent_t> pool;
+    cudaEvent_t get()
+    {
+        if (!pool.empty()) {
+            cudaEvent_t e = pool.back();
+            pool.pop_back();
+            return e;
+        }
+        cudaEvent_t e = nullptr;
+        cudaEventCreate(&e);
+        return e;
+    }
+    void begin(int phase, cudaStream_t s)
+    {
+        Rec r{phase, get(), get()};
+        cudaEventRecord(r.a, s);
+        recs.push_back(r);
+    }
+    void end(cudaStream_t s) { cudaEventRecord(recs.back().b, s); }
+    ~Profiler()
+    {
+        for (auto& r : recs) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
+        for (auto e : pool) cudaEventDestroy(e);
+    }
+};
+
+enum { kPhasePrep = 0, kPhaseGateUp = 1, kPhaseDown = 2, kPhaseRoute = 3, kPhaseActQuant = 4,
+       kNumPhases = 8 };
+
+cudaError_t launch_gemv_layer(const GemvArgs& a, cudaStream_t s, bool pdl, Profiler* prof);
+
+cudaError_t launch_pack_expert(const uint8_t* canon_codes, const uint8_t* canon_scales,
+                               uint8_t* packed_codes, uint8_t* packed_scales, int H, int I,
+                               cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,195 @@
+/*
+ * moe_ffn.h -- C ABI of the GB300 (sm_103a) routed FP4 MoE expert-FFN library.
+ *
+ * The operation is the routed expert FFN of an LLM decode step as described by
+ *   [8GB]  "在 8 GB 显卡上运行 510 GB 的 DeepSeek-V4.1-Flash——以及三个从不抛错的 Bug"
+ *   [A100] "把不支持 FP4 的 A100 拉到 673 tok/s，回过神来发现比官方 API 还快"
+ * Each token chooses top-k experts of a layer ([8GB] §每 token 字节数决定一切:
+ * 6 of 384); each expert is a SwiGLU block o = Wd (silu(Wg x) (.) (Wu x)) whose
+ * weights are FP4 E2M1 codes with one ue8m0 power-of-two scale per 32 weights
+ * ([A100] §质疑「不支持 FP4」这句话 for E2M1; [8GB] §RTX 50xx 上的三个从不抛错的
+ * Bug for ue8m0); the token's output is y = sum_k w_k o_k.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device pointers must be CUDA device (or managed)
+ *    memory of the handle's device; host pointers are plain host memory.
+ *  - Tensors are C-contiguous, with the shapes given, and their base addresses
+ *    16-byte aligned; no strides are accepted.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *    except the *_host variants and moe_ffn_status is asynchronous: it only
+ *    enqueues work and never waits for the device.
+ *  - The caller owns every buffer it passes and must keep it alive until the
+ *    stream has executed the call.  The handle owns its workspace.
+ *  - Calls on one handle must be ordered (one stream, or externally
+ *    synchronized): they share the handle's workspace.
+ *  - Return value: MOE_OK (0) or a negative MOE_ERR_* code.  Argument errors
+ *    are found on the host before anything is enqueued.  Errors that only the
+ *    device can see (an expert id out of range, a NULL expert pointer) do not
+ *    trap: the affected slot contributes zero and a sticky status word is set,
+ *    read and cleared by moe_ffn_status().
+ */
+#ifndef MOE_FFN_H
+#define MOE_FFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK                   0
+#define MOE_ERR_INVALID_ARG     (-1)  /* bad pointer, size, alignment or config   */
+#define MOE_ERR_CUDA            (-2)  /* a CUDA runtime call failed               */
+#define MOE_ERR_OOM             (-3)  /* workspace allocation failed              */
+#define MOE_ERR_UNSUPPORTED     (-4)  /* valid request this build does not serve  */
+#define MOE_ERR_BAD_INDEX       (-5)  /* device saw an expert id outside [0, E)   */
+#define MOE_ERR_DEVICE_TIMEOUT  (-6)  /* a bounded device-side wait gave up       */
+
+/* Activation numerics (chosen explicitly; no hidden heuristic). */
+enum {
+    /* x (bf16) and the SwiGLU output h are carried at (better than) fp32
+     * accuracy: products of exact E2M1 weights and activations, fp32 sums. */
+    MOE_ACT_BF16 = 0,
+    /* x and h are quantized to FP8 E4M3 with one ue8m0 scale per 128
+     * consecutive elements (the last block of h may be shorter) before each
+     * projection; the scale is 2^k with k the least integer such that
+     * amax <= 448 * 2^k, and codes round to nearest even, saturating. */
+    MOE_ACT_E4M3_UE8M0_128 = 1
+};
+
+enum { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 };
+
+typedef struct moe_ffn* moe_ffn_t;
+
+typedef struct {
+    int num_experts;      /* E, experts of one layer                         */
+    int hidden;           /* H, model width; multiple of 64                  */
+    int inter;            /* I, expert intermediate width; multiple of 64    */
+    int topk;             /* k, experts per token, 1..16                     */
+    int max_tokens;       /* largest T passed to forward calls               */
+    int act_mode;         /* MOE_ACT_*                                       */
+    int out_dtype;        /* MOE_OUT_*                                       */
+    int gemm_min_tokens;  /* T >= this uses the grouped (expert-major) path;
+                             0 selects the library default                   */
+} moe_ffn_config;
+
+/* One layer's experts.  codes / scales are DEVICE arrays of E DEVICE pointers,
+ * each to one expert's blob in the packed layout made by moe_ffn_pack_expert.
+ * A NULL entry is allowed for an expert that is never routed to. */
+typedef struct {
+    const uint8_t* const* codes;
+    const uint8_t* const* scales;
+} moe_expert_table;
+
+/* Bytes of one expert's packed codes (3*I*H/2) and packed scales (3*I*H/32):
+ * the same sizes as the published layout ([8GB] §方案：不重写模型，只迁移其存储:
+ * 17.7 MB of codes and 1.1 MB of scales at H = 4096, I = 2880).
+ * Returns 0 for an invalid config. */
+size_t moe_ffn_packed_codes_bytes(const moe_ffn_config* cfg);
+size_t moe_ffn_packed_scales_bytes(const moe_ffn_config* cfg);
+
+/* Validate cfg, select `device`, allocate the workspace (sized from
+ * max_tokens) and return a handle in *out.  Errors: INVALID_ARG (config),
+ * UNSUPPORTED (shape outside what the kernels serve), OOM, CUDA. */
+int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device);
+
+/* Re-lay one expert once, at load time, into the order the kernels stream
+ * ([A100] §但 CPU 也没那么快: reorder weights at load time into the order the
+ * compute unit consumes).  Input: the published layout, device memory:
+ *   canon_codes : gate [I][H/2] | up [I][H/2] | down [H][I/2]   (low nibble =
+ *                 even element), canon_scales: gate [I][H/32] | up [I][H/32] |
+ *                 down [H][I/32] (one ue8m0 byte per 32 weights of a row).
+ * Output: packed_codes (moe_ffn_packed_codes_bytes) and packed_scales, device
+ * memory, not overlapping the inputs.  A pure byte permutation. */
+int moe_ffn_pack_expert(moe_ffn_t h, const void* canon_codes, const void* canon_scales,
+                        void* packed_codes, void* packed_scales, void* stream);
+
+/* One MoE layer for T tokens (0 <= T <= max_tokens):
+ *   x        device bf16 [T][H]
+ *   topk_idx device int32 [T][k]   expert ids (repeats in a row are allowed)
+ *   topk_w   device fp32  [T][k]   combine weights, used as given
+ *   tbl      host struct of device pointer arrays (see moe_expert_table)
+ *   y        device [T][H], bf16 or fp32 per cfg.out_dtype; y must not alias x
+ * y[t] = sum_{k} topk_w[t,k] * FFN_{topk_idx[t,k]}(x[t]).  Deterministic:
+ * repeated calls give bitwise identical y. */
+int moe_ffn_forward(moe_ffn_t h, const void* x, const int32_t* topk_idx, const float* topk_w,
+                    const moe_expert_table* tbl, void* y, int T, void* stream);
+
+/* moe_ffn_forward with HOST x / topk_idx / topk_w / y (any host memory;
+ * pinned memory makes the copies asynchronous with respect to the host
+ * thread).  Copies the inputs into the workspace, runs the layer and copies y
+ * back, all on `stream`, then waits for `stream`.  The expert table stays in
+ * device memory. */
+int moe_ffn_forward_host(moe_ffn_t h, const void* x_host, const int32_t* topk_idx_host,
+                         const float* topk_w_host, const moe_expert_table* tbl, void* y_host,
+                         int T, void* stream);
+
+/* Token -> expert grouping on the device ([8GB] §提速之路：v1 到 v4: the
+ * per-expert token search, done without a host round trip).  Device outputs:
+ *   counts  int32 [E]      slots routed to each expert
+ *   offsets int32 [E+1]    exclusive prefix sum of counts
+ *   perm    int32 [T*k]    slot ids j = t*k + kk ordered by (expert, t, kk)
+ *   inv     int32 [T*k]    inv[perm[p]] = p
+ * Bit-exact and deterministic.  Out-of-range ids set MOE_ERR_BAD_INDEX in the
+ * status word and are left out of every output (their inv entry is -1). */
+int moe_ffn_route(moe_ffn_t h, const int32_t* topk_idx, int T, int32_t* counts,
+                  int32_t* offsets, int32_t* perm, int32_t* inv, void* stream);
+
+/* Activation quantizer of the MOE_ACT_E4M3_UE8M0_128 mode ([8GB] §RTX 50xx
+ * 上的三个从不抛错的 Bug, item 2: the ue8m0 act_quant step).  Device in/out:
+ *   x       bf16 [rows][n]
+ *   codes   uint8 [rows][n]          E4M3 codes
+ *   scales  uint8 [rows][ceil(n/128)] ue8m0 bytes (2^(s-127))
+ * Bit-exact and deterministic. n must be a multiple of 32. */
+int moe_ffn_act_quant(moe_ffn_t h, const void* x, int rows, int n, uint8_t* codes,
+                      uint8_t* scales, void* stream);
+
+/* L-layer decode step on a residual stream ([A100] §然后又发现每 token 启动
+ * 2000 次内核: RMSNorm and the MoE per layer, launched as a handful of
+ * dispatches): for l = 0..L-1,
+ *   u = bf16(x / sqrt(mean(x^2) + 1e-6))   (unit norm weight)
+ *   x = x + moe_l(u)
+ *   x        device fp32 [T][H], updated in place
+ *   tbls     host array [L] of expert tables (one per layer)
+ *   topk_idx device int32 [L][T][k];  topk_w device fp32 [L][T][k]
+ * The whole step is captured once into a CUDA graph per (T, L, pointer set)
+ * and replayed; later calls with the same pointers only replay it. */
+int moe_stack_forward(moe_ffn_t h, float* x, const moe_expert_table* tbls,
+                      const int32_t* topk_idx, const float* topk_w, int L, int T,
+                      void* stream);
+
+/* Per-kernel timing, a tracing aid.  While enabled, forward calls record a
+ * CUDA event pair around each of their kernel launches on the call's stream
+ * (this also stops a kernel's prologue from overlapping the previous kernel).
+ * moe_ffn_profile_read waits for the recorded events, writes the summed
+ * milliseconds and launch counts per phase (MOE_PHASE_*; arrays of
+ * MOE_NUM_PHASES entries, host memory) and resets the record.  The stack
+ * entry point is not traced.  Errors: INVALID_ARG, CUDA. */
+enum {
+    MOE_PHASE_PREP = 0,      /* activation prep (and fused RMSNorm)         */
+    MOE_PHASE_GATE_UP = 1,   /* gate/up projections + SwiGLU                */
+    MOE_PHASE_DOWN = 2,      /* down projection + combine                   */
+    MOE_PHASE_ROUTE = 3,     /* token -> expert grouping                    */
+    MOE_PHASE_ACT_QUANT = 4, /* E4M3 activation quantizer                   */
+    MOE_NUM_PHASES = 8
+};
+int moe_ffn_profile_enable(moe_ffn_t h, int on);
+int moe_ffn_profile_read(moe_ffn_t h, double* ms, int* launches);
+
+/* Wait for `stream`, then return and clear the sticky device status:
+ * MOE_OK, MOE_ERR_BAD_INDEX or MOE_ERR_DEVICE_TIMEOUT (or MOE_ERR_CUDA if the
+ * read itself failed). */
+int moe_ffn_status(moe_ffn_t h, void* stream);
+
+/* Static message for a MOE_* code. */
+const char* moe_ffn_strerror(int code);
+
+/* Free the workspace and cached graphs.  The caller must first make sure no
+ * enqueued call on the handle is still pending.  NULL is a no-op. */
+void moe_ffn_destroy(moe_ffn_t h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_FFN_H */

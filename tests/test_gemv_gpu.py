@@ -1,0 +1,282 @@
+"""GPU parity of the batch-1 / small-batch path against the CPU oracle, through
+the C ABI.  Float outputs: max|err| <= 2e-3 * rms(ref), cosine >= 0.99999."""
+import numpy as np
+import pytest
+import torch
+
+import fp4_block_scaled_gb300 as moe
+import oracle
+import synth
+from moe_setup import assert_close, bf16_to_f64, errors, fill_layer, host_experts
+
+pytestmark = pytest.mark.gpu
+
+TINY = dict(E=8, H=256, I=128, k=2)
+MID = dict(E=16, H=1024, I=448, k=6)      # down K = 448: 3 full k-groups + a 64-wide tail
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    moe.lib()
+    yield
+
+
+class Layer:
+    def __init__(self, E, H, I, k, max_tokens=8, out=moe.MOE_OUT_F32, seed=0, layer=0):
+        self.E, self.H, self.I, self.k = E, H, I, k
+        self.cfg = moe.config(E, H, I, k, max_tokens, out_dtype=out)
+        self.h = moe.moe_ffn_create(self.cfg, 0)
+        self.es = fill_layer(self.h, self.cfg, layer=layer, seed=seed)
+        self.seed, self.layer = seed, layer
+        self.out = out
+
+    def run(self, x_bits, idx, w):
+        T = x_bits.shape[0]
+        x = torch.from_numpy(x_bits.view(np.int16)).cuda()
+        it = torch.from_numpy(np.ascontiguousarray(idx, np.int32)).cuda()
+        wt = torch.from_numpy(np.ascontiguousarray(w, np.float32)).cuda()
+        dt = torch.float32 if self.out == moe.MOE_OUT_F32 else torch.bfloat16
+        y = torch.empty((T, self.H), dtype=dt, device="cuda")
+        moe.moe_ffn_forward(self.h, x, it, wt, self.es.table, y, T)
+        torch.cuda.synchronize()
+        return y
+
+    def oracle(self, x_bits, idx, w):
+        codes, scales = host_experts(self.H, self.I, idx.reshape(-1), layer=self.layer,
+                                     seed=self.seed, E=self.E)
+        return oracle.moe_ffn(codes, scales, self.H, self.I, x_bits, idx, w, nthreads=8)
+
+    def close(self):
+        moe.moe_ffn_destroy(self.h)
+
+
+def inputs(T, E, H, k, seed=0):
+    return (synth.activations_bf16(T, H, seed=seed), synth.routing_uniform(T, E, k, seed=seed),
+            synth.routing_weights(T, k, seed=seed))
+
+
+def test_device_fill_matches_host_generator():
+    n = 1000003
+    t = torch.empty(n, dtype=torch.uint8, device="cuda")
+    synth.device_fill_bytes(t.data_ptr(), n, 5, 77)
+    assert np.array_equal(t.cpu().numpy(), synth.random_bytes(5, 77, n))
+    synth.device_fill_bytes(t.data_ptr() + 3, 1000, 5, 77, offset=3)
+    assert np.array_equal(t[3:1003].cpu().numpy(), synth.random_bytes(5, 77, 1000, offset=3))
+    synth.device_fill_range(t.data_ptr(), n, 1, 9, 119, 127)
+    assert np.array_equal(t.cpu().numpy(), synth.random_range_bytes(1, 9, n, 119, 127))
+
+
+def _pack_reference(codes, scales, H, I):
+    """Independent numpy statement of the packed layout (tile / k-group /
+    lane order) used to check moe_ffn_pack_expert byte for byte."""
+    def section(cmat, smat, K, rows_of_tile, ntiles):
+        out_c, out_s = [], []
+        kgf, half = K // 128, (K % 128) // 64
+        for t in range(ntiles):
+            rows = rows_of_tile(t)
+            for kg in range(kgf + half):
+                nb = 4 if kg < kgf else 2
+                for lane in range(32):
+                    g, c = lane // 4, lane % 4
+                    for hf in range(2):
+                        r = rows[g + 8 * hf]
+                        for j in range(nb):
+                            b = kg * 4 + j
+                            out_c.append(cmat[r, b * 16 + 4 * c: b * 16 + 4 * c + 4])
+                for g in range(8):
+                    for hf in range(2):
+                        for j in range(nb):
+                            out_s.append(smat[rows[g + 8 * hf], kg * 4 + j: kg * 4 + j + 1])
+        return np.concatenate(out_c), np.concatenate(out_s)
+
+    gc, gs = I * H // 2, I * H // 32
+    cg = codes[:gc].reshape(I, H // 2)
+    cu = codes[gc:2 * gc].reshape(I, H // 2)
+    cd = codes[2 * gc:].reshape(H, I // 2)
+    sg = scales[:gs].reshape(I, H // 32)
+    su = scales[gs:2 * gs].reshape(I, H // 32)
+    sd = scales[2 * gs:].reshape(H, I // 32)
+    cgu = np.concatenate([cg, cu])            # rows 0..I-1 gate, I..2I-1 up
+    sgu = np.concatenate([sg, su])
+    pc1, ps1 = section(cgu, sgu, H, lambda t: [8 * t + r for r in range(8)] + [I + 8 * t + r for r in range(8)], I // 8)
+    pc2, ps2 = section(cd, sd, I, lambda t: [16 * t + r for r in range(16)], H // 16)
+    return np.concatenate([pc1, pc2]), np.concatenate([ps1, ps2])
+
+
+@pytest.mark.parametrize("dims", [TINY, dict(E=2, H=192, I=192, k=1)])
+def test_pack_is_the_documented_permutation(dims):
+    H, I = dims["H"], dims["I"]
+    cfg = moe.config(dims["E"], H, I, dims["k"], 1)
+    h = moe.moe_ffn_create(cfg, 0)
+    try:
+        es = fill_layer(h, cfg, experts=[1])
+        codes, scales = synth.expert_canonical(H, I, 1)
+        rc, rs = _pack_reference(codes, scales, H, I)
+        got_c = es.codes[es.code_stride: es.code_stride + es.code_bytes].cpu().numpy()
+        got_s = es.scales[es.scale_stride: es.scale_stride + es.scale_bytes].cpu().numpy()
+        assert np.array_equal(got_c, rc)
+        assert np.array_equal(got_s, rs)
+    finally:
+        moe.moe_ffn_destroy(h)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 5])
+def test_tiny_layer_matches_oracle(T):
+    L = Layer(**TINY)
+    try:
+        x, idx, w = inputs(T, TINY["E"], TINY["H"], TINY["k"], seed=T)
+        y = L.run(x, idx, w).cpu().numpy()
+        assert_close(y, L.oracle(x, idx, w), f"tiny T={T}")
+    finally:
+        L.close()
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_mid_layer_ragged_k_tail_matches_oracle(T):
+    L = Layer(**MID)
+    try:
+        x, idx, w = inputs(T, MID["E"], MID["H"], MID["k"], seed=10 + T)
+        y = L.run(x, idx, w).cpu().numpy()
+        assert_close(y, L.oracle(x, idx, w), f"mid T={T}")
+    finally:
+        L.close()
+
+
+def test_full_size_layer_batch1_matches_oracle():
+    """384 experts, H=4096, I=2880, top-6: the single-layer decode shape."""
+    L = Layer(E=384, H=4096, I=2880, k=6, max_tokens=1)
+    try:
+        for seed in (0, 1):
+            x, idx, w = inputs(1, 384, 4096, 6, seed=seed)
+            y = L.run(x, idx, w).cpu().numpy()
+            assert_close(y, L.oracle(x, idx, w), f"full-size seed={seed}")
+    finally:
+        L.close()
+
+
+def test_bf16_output_is_rounded_fp32_output():
+    Lf = Layer(**TINY)
+    Lb = Layer(**TINY, out=moe.MOE_OUT_BF16)
+    try:
+        x, idx, w = inputs(3, TINY["E"], TINY["H"], TINY["k"], seed=4)
+        yf = Lf.run(x, idx, w)
+        yb = Lb.run(x, idx, w)
+        assert torch.equal(yf.to(torch.bfloat16).view(torch.int16), yb.view(torch.int16))
+        ref = Lf.oracle(x, idx, w)
+        yb64 = bf16_to_f64(yb).reshape(ref.shape)
+        rms = np.sqrt(np.mean(ref ** 2))
+        half_ulp = np.ldexp(1.0, np.floor(np.log2(np.abs(ref) + 1e-300)).astype(int) - 8)
+        assert np.all(np.abs(yb64 - ref) <= 2e-3 * rms + half_ulp)
+    finally:
+        Lf.close()
+        Lb.close()
+
+
+def test_deterministic_across_repeats():
+    L = Layer(**MID)
+    try:
+        x, idx, w = inputs(2, MID["E"], MID["H"], MID["k"], seed=3)
+        ys = [L.run(x, idx, w).view(torch.int32).clone() for _ in range(5)]
+        assert all(torch.equal(ys[0], y) for y in ys[1:])
+    finally:
+        L.close()
+
+
+def test_zero_input_gives_zero_and_one_hot_weight_picks_expert():
+    L = Layer(**TINY)
+    try:
+        T = 2
+        x, idx, w = inputs(T, TINY["E"], TINY["H"], TINY["k"], seed=6)
+        y0 = L.run(np.zeros_like(x), idx, w)
+        assert torch.count_nonzero(y0).item() == 0
+        onehot = np.zeros_like(w)
+        onehot[:, 0] = 1.0
+        y = L.run(x, idx, onehot).cpu().numpy()
+        ref = L.oracle(x, idx, onehot)
+        assert_close(y, ref, "one-hot weight")
+    finally:
+        L.close()
+
+
+def test_out_of_range_expert_contributes_zero_and_sets_status():
+    L = Layer(**TINY)
+    try:
+        x, idx, w = inputs(2, TINY["E"], TINY["H"], TINY["k"], seed=8)
+        bad = idx.copy()
+        bad[1, 1] = TINY["E"] + 3
+        assert moe.moe_ffn_status(L.h) == moe.MOE_OK
+        y = L.run(x, bad, w).cpu().numpy()
+        assert moe.moe_ffn_status(L.h) == moe.MOE_ERR_BAD_INDEX
+        assert moe.moe_ffn_status(L.h) == moe.MOE_OK          # cleared by the read
+        w0 = w.copy()
+        w0[1, 1] = 0.0
+        ok = bad.copy()
+        ok[1, 1] = 0
+        assert_close(y, L.oracle(x, ok, w0), "bad index slot dropped")
+    finally:
+        L.close()
+
+
+def test_forward_host_equals_forward():
+    L = Layer(**TINY)
+    try:
+        T = 3
+        x, idx, w = inputs(T, TINY["E"], TINY["H"], TINY["k"], seed=2)
+        y_dev = L.run(x, idx, w).cpu().numpy()
+        y_host = np.zeros((T, TINY["H"]), np.float32)
+        moe.moe_ffn_forward_host(L.h, x.ctypes.data, idx.ctypes.data, w.ctypes.data, L.es.table,
+                                 y_host.ctypes.data, T)
+        assert np.array_equal(y_dev, y_host)
+    finally:
+        L.close()
+
+
+def test_forward_rejects_bad_arguments():
+    L = Layer(**TINY, max_tokens=2)
+    try:
+        x = torch.zeros((3, TINY["H"]), dtype=torch.bfloat16, device="cuda")
+        idx = torch.zeros((3, 2), dtype=torch.int32, device="cuda")
+        w = torch.zeros((3, 2), dtype=torch.float32, device="cuda")
+        y = torch.zeros((3, TINY["H"]), dtype=torch.float32, device="cuda")
+        with pytest.raises(moe.MoeError):
+            moe.moe_ffn_forward(L.h, x, idx, w, L.es.table, y, 3)       # T > max_tokens
+        with pytest.raises(moe.MoeError):
+            moe.moe_ffn_forward(L.h, x.data_ptr() + 2, idx, w, L.es.table, y, 1)  # misaligned
+        with pytest.raises(moe.MoeError):
+            moe.moe_ffn_forward(L.h, x, idx, w, L.es.table, x, 1)       # y aliases x
+        moe.moe_ffn_forward(L.h, x, idx, w, L.es.table, y, 0)           # T = 0 is a no-op
+    finally:
+        L.close()
+
+
+def test_stack_matches_oracle():
+    E, H, I, k, Lnum = 8, 256, 128, 2, 4
+    for T in (1, 3):
+        cfg = moe.config(E, H, I, k, T)
+        h = moe.moe_ffn_create(cfg, 0)
+        try:
+            sets = [fill_layer(h, cfg, layer=l) for l in range(Lnum)]
+            idx = np.stack([synth.routing_uniform(T, E, k, seed=100 + l) for l in range(Lnum)])
+            w = np.stack([synth.routing_weights(T, k, seed=100 + l) for l in range(Lnum)])
+            x0 = synth.activations_f32(T, H, seed=7)
+            x = torch.from_numpy(x0.copy()).cuda()
+            it, wt = torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda()
+            moe.moe_stack_forward(h, x, [s.table for s in sets], it, wt, Lnum, T)
+            torch.cuda.synchronize()
+            layers = []
+            for l in range(Lnum):
+                c, s = host_experts(H, I, idx[l].reshape(-1), layer=l, E=E)
+                layers.append((c, s, H, I))
+            ref = oracle.moe_stack(layers, x0.astype(np.float64), idx, w)
+            assert_close(x.cpu().numpy(), ref, f"stack T={T}")
+            # the update itself (x_L - x_0) is also within tolerance
+            assert_close(x.cpu().numpy() - x0, ref - x0, f"stack delta T={T}")
+            # a second call replays the cached graph on the updated residual
+            moe.moe_stack_forward(h, x, [s.table for s in sets], it, wt, Lnum, T)
+            torch.cuda.synchronize()
+            ref2 = oracle.moe_stack(layers, ref, idx, w)
+            assert_close(x.cpu().numpy(), ref2, f"stack replay T={T}")
+        finally:
+            moe.moe_ffn_destroy(h)
