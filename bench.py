@@ -29,6 +29,9 @@ sys.path.insert(0, ROOT)
 
 WORKLOADS = {
     "layer_b1": dict(E=384, H=4096, I=2880, k=6, T=1),
+    # same step (6 experts streamed per token) with 64 resident experts (1.2 GB,
+    # still far above L2): the size used for ncu captures
+    "layer_b1_e64": dict(E=64, H=4096, I=2880, k=6, T=1),
 }
 METRIC = "MoE expert-FFN decode tokens/s per layer-stack & HBM GB/s (% of GB300 roofline)"
 FALLBACK_HBM_GBS = 6800.0

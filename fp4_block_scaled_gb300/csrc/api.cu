@@ -28,7 +28,7 @@ struct StackGraph {
 struct moe_ffn {
     moe_ffn_config cfg;
     int device;
-    int kc_gu;
+    int sms;
     void* ws;
     size_t ws_bytes;
     GemvArgs base;              // workspace pointers, problem sizes
@@ -151,10 +151,14 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     if (!h) return MOE_ERR_OOM;
     h->cfg = *cfg;
     h->device = device;
-    h->kc_gu = gemv_default_kc(cfg->hidden);
+    if (cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        gemv_init_device() != cudaSuccess || route_init_device() != cudaSuccess) {
+        delete h;
+        return MOE_ERR_CUDA;
+    }
     const int T = cfg->max_tokens > 0 ? cfg->max_tokens : 1;
     const int H = cfg->hidden, I = cfg->inter, k = cfg->topk;
-    GemvWorkspaceSizes g = gemv_workspace_sizes(T, k, H, I, h->kc_gu);
+    GemvWorkspaceSizes g = gemv_workspace_sizes(T, k, H, I, h->sms);
 
     // one allocation, carved into aligned pieces
     size_t off = 0;
@@ -190,7 +194,7 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     a.E = cfg->num_experts;
     a.H = H;
     a.I = I;
-    a.kc_gu = h->kc_gu;
+    a.sms = h->sms;
     a.xs_stride = (H / 32 + 3) / 4 * 4;
     a.hs_stride = (I / 32 + 3) / 4 * 4;
     a.eps = 1e-6f;
@@ -268,15 +272,35 @@ int moe_ffn_forward_host(moe_ffn_t h, const void* x_host, const int32_t* idx_hos
 int moe_ffn_route(moe_ffn_t h, const int32_t* topk_idx, int T, int32_t* counts, int32_t* offsets,
                   int32_t* perm, int32_t* inv, void* stream)
 {
-    (void)topk_idx; (void)T; (void)counts; (void)offsets; (void)perm; (void)inv; (void)stream;
-    return h ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
+    if (!h || T < 0 || T > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+    if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !perm || !inv)) return MOE_ERR_INVALID_ARG;
+    if (!aligned(topk_idx, 4) || !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(perm, 4) ||
+        !aligned(inv, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (h->cfg.num_experts > route_max_experts()) return MOE_ERR_UNSUPPORTED;
+    DeviceGuard guard(h->device);
+    RouteArgs a{topk_idx, T * h->cfg.topk, h->cfg.num_experts, counts, offsets, perm, inv, h->status};
+    cudaStream_t s = (cudaStream_t)stream;
+    if (h->prof) h->prof->begin(kPhaseRoute, s);
+    cudaError_t e = launch_route(a, s);
+    if (h->prof) h->prof->end(s);
+    return cuda_rc(e);
 }
 
 int moe_ffn_act_quant(moe_ffn_t h, const void* x, int rows, int n, uint8_t* codes,
                       uint8_t* scales, void* stream)
 {
-    (void)x; (void)rows; (void)n; (void)codes; (void)scales; (void)stream;
-    return h ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
+    if (!h || rows < 0 || n <= 0 || n % 32) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 4)) return MOE_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    ActQuantArgs a{(const uint16_t*)x, nullptr, rows, n, codes, scales};
+    cudaStream_t s = (cudaStream_t)stream;
+    if (h->prof) h->prof->begin(kPhaseActQuant, s);
+    cudaError_t e = launch_act_quant(a, s, false);
+    if (h->prof) h->prof->end(s);
+    return cuda_rc(e);
 }
 
 int moe_stack_forward(moe_ffn_t h, float* x, const moe_expert_table* tbls,

@@ -16,7 +16,7 @@ enum : int { kStatusBadIndex = 1, kStatusTimeout = 2 };
 // Arguments of one MoE layer on the GEMV (slot-major) path.
 struct GemvArgs {
     int T, topk, E, H, I;
-    int kc_gu;                          // K chunks per gate/up unit
+    int sms;                            // CTAs of the streaming kernels (SM count)
     // inputs: bf16 x (forward) or fp32 residual x (stack, rmsnorm fused)
     const uint16_t* x_bf16;
     float* x_resid;
@@ -29,12 +29,12 @@ struct GemvArgs {
     uint16_t* xh;                       // [T][H] f16, block-scaled
     float* xs;                          // [T][xs_stride] block scales (H/32 used)
     int xs_stride, hs_stride;           // H/32 and I/32 rounded up to a multiple of 4
-    float* part_gu;                     // [T*k][I/32][kc_gu][64]
-    int* cnt_gu;                        // [T*k][I/32]
+    float* part_gu;                     // [sms][2][64] partial sums of split groups
+    int* cnt_gu;                        // [T*k][I/32] units done per group
     uint16_t* hh;                       // [T*k][I/32][2][32] f16 hi|lo
     float* hs;                          // [T*k][hs_stride]
-    float* part_dn;                     // [T][H/16][k][16]
-    int* cnt_dn;                        // [T][H/16]
+    float* part_dn;                     // [sms][2][64]
+    int* cnt_dn;                        // [T][H/64]
     int* status;
     // output (forward): y [T][H] fp32 or bf16
     void* y;
@@ -45,8 +45,9 @@ struct GemvArgs {
 struct GemvWorkspaceSizes {
     size_t xh, xs, part_gu, cnt_gu, hh, hs, part_dn, cnt_dn;
 };
-GemvWorkspaceSizes gemv_workspace_sizes(int T, int topk, int H, int I, int kc_gu);
-int gemv_default_kc(int H);
+GemvWorkspaceSizes gemv_workspace_sizes(int T, int topk, int H, int I, int sms);
+cudaError_t gemv_init_device();   // per device, before the first launch
+size_t gemv_stream_smem();
 
 // Optional per-phase event recorder (moe_ffn_profile_*); nullptr = off.
 struct Profiler {
@@ -82,6 +83,27 @@ enum { kPhasePrep = 0, kPhaseGateUp = 1, kPhaseDown = 2, kPhaseRoute = 3, kPhase
        kNumPhases = 8 };
 
 cudaError_t launch_gemv_layer(const GemvArgs& a, cudaStream_t s, bool pdl, Profiler* prof);
+
+// Token -> expert grouping (route.cu).
+struct RouteArgs {
+    const int32_t* idx;     // [n] expert ids of the slots
+    int n, E;
+    int32_t *counts, *offsets, *perm, *inv;
+    int* status;
+};
+int route_max_experts();
+cudaError_t route_init_device();
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+
+// E4M3 / ue8m0-per-128 activation quantizer (actquant.cu).
+struct ActQuantArgs {
+    const uint16_t* x;      // bf16 [src rows][n]
+    const int32_t* src_row; // optional gather: output row r reads x row src_row[r] (-1: zeros)
+    int rows, n;            // output rows; n % 32 == 0
+    uint8_t* codes;         // [rows][n]
+    uint8_t* scales;        // [rows][ceil(n/128)]
+};
+cudaError_t launch_act_quant(const ActQuantArgs& a, cudaStream_t s, bool pdl);
 
 cudaError_t launch_pack_expert(const uint8_t* canon_codes, const uint8_t* canon_scales,
                                uint8_t* packed_codes, uint8_t* packed_scales, int H, int I,

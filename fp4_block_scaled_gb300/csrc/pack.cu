@@ -1,9 +1,9 @@
 // pack.cu -- load-time re-layout of one expert (a pure byte permutation).
 //
 // Reorders the published layout (gate | up | down, row-major, two E2M1 codes
-// per byte, one ue8m0 byte per 32 weights) into the tile / k-group order of
-// layout.h, so that the decode kernels stream each tile with wide, fully
-// coalesced loads and find every mma fragment already in place.
+// per byte, one ue8m0 byte per 32 weights) into the tile-group / k-group /
+// tile / lane order of layout.h, so that the decode kernels stream contiguous
+// units with bulk copies and find every mma fragment already in place.
 #include "internal.h"
 
 namespace moe {
@@ -38,28 +38,34 @@ __device__ inline void canon_row(const SectionMap& s, int tile, int m, int k, co
 // One thread per packed 4-byte code word.
 __global__ void pack_codes_kernel(SectionMap s, MatLayout L, uint8_t* out)
 {
-    size_t words_per_tile = L.tile_code_bytes() / 4;
-    size_t total = words_per_tile * L.tiles;
+    size_t words_per_group = L.group_code_bytes() / 4;
+    size_t total = words_per_group * L.groups;
     size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t wi = (size_t)blockIdx.x * blockDim.x + threadIdx.x; wi < total; wi += stride) {
-        int tile = (int)(wi / words_per_tile);
-        int wt = (int)(wi % words_per_tile);
-        int kg = wt / 256, w = wt % 256;
-        int lane, half, j, block;
-        if (kg < L.kg_full) {
-            lane = w / 8;
-            half = (w / 4) & 1;
-            j = w & 3;
+        int grp = (int)(wi / words_per_group);
+        int wg = (int)(wi % words_per_group);
+        int kg = wg / 1024;
+        int q, half, lane, j, block;
+        if (kg < L.kg_full) {          // [tile q][half][lane][block 0..3][4 B]
+            int r = wg % 1024;
+            q = r / 256;
+            r %= 256;
+            half = r / 128;
+            lane = (r % 128) / 4;
+            j = r % 4;
             block = kg * 4 + j;
-        } else {                       // half k-group: 128 words
-            lane = w / 4;
-            half = (w / 2) & 1;
-            j = w & 1;
+        } else {                       // half k-group: [tile q][half][lane][block 0..1][4 B]
+            int r = wg - L.kg_full * 1024;
+            q = r / 128;
+            r %= 128;
+            half = r / 64;
+            lane = (r % 64) / 2;
+            j = r % 2;
             block = L.kg_full * 4 + j;
         }
         int g = lane >> 2, c = lane & 3;
         const uint8_t *crow, *srow;
-        canon_row(s, tile, g + 8 * half, L.k, crow, srow);
+        canon_row(s, grp * kTilesPerGroup + q, g + 8 * half, L.k, crow, srow);
         uint32_t v = *reinterpret_cast<const uint32_t*>(crow + block * 16 + 4 * c);
         reinterpret_cast<uint32_t*>(out)[wi] = v;
     }
@@ -68,25 +74,31 @@ __global__ void pack_codes_kernel(SectionMap s, MatLayout L, uint8_t* out)
 // One thread per packed scale byte.
 __global__ void pack_scales_kernel(SectionMap s, MatLayout L, uint8_t* out)
 {
-    size_t per_tile = L.tile_scale_bytes();
-    size_t total = per_tile * L.tiles;
+    size_t per_group = L.group_scale_bytes();
+    size_t total = per_group * L.groups;
     size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t bi = (size_t)blockIdx.x * blockDim.x + threadIdx.x; bi < total; bi += stride) {
-        int tile = (int)(bi / per_tile);
-        int bt = (int)(bi % per_tile);
-        int kg = bt / 64, w = bt % 64;
-        int g, half, block;
-        if (kg < L.kg_full) {
-            g = w / 8;
-            half = (w / 4) & 1;
-            block = kg * 4 + (w & 3);
-        } else {                       // half k-group: 32 bytes
-            g = w / 4;
-            half = (w / 2) & 1;
-            block = L.kg_full * 4 + (w & 1);
+        int grp = (int)(bi / per_group);
+        int sg = (int)(bi % per_group);
+        int kg = sg / 256;
+        int q, g, half, block;
+        if (kg < L.kg_full) {          // [tile q][g][half][block 0..3]
+            int r = sg % 256;
+            q = r / 64;
+            r %= 64;
+            g = r / 8;
+            half = (r / 4) & 1;
+            block = kg * 4 + (r & 3);
+        } else {                       // half k-group: [tile q][g][half][block 0..1]
+            int r = sg - L.kg_full * 256;
+            q = r / 32;
+            r %= 32;
+            g = r / 4;
+            half = (r / 2) & 1;
+            block = L.kg_full * 4 + (r & 1);
         }
         const uint8_t *crow, *srow;
-        canon_row(s, tile, g + 8 * half, L.k, crow, srow);
+        canon_row(s, grp * kTilesPerGroup + q, g + 8 * half, L.k, crow, srow);
         out[bi] = srow[block];
     }
 }
@@ -107,13 +119,13 @@ cudaError_t launch_pack_expert(const uint8_t* cc, const uint8_t* cs, uint8_t* pc
     SectionMap gu{cc, cs, 1, gu_c, gu_s};
     SectionMap dn{cc + 2 * gu_c, cs + 2 * gu_s, 0, 0, 0};
     size_t n;
-    n = E.gu.tiles * E.gu.tile_code_bytes() / 4;
+    n = E.gu.groups * E.gu.group_code_bytes() / 4;
     pack_codes_kernel<<<grid_for(n), 256, 0, st>>>(gu, E.gu, pc + E.gu_code_off);
-    n = E.dn.tiles * E.dn.tile_code_bytes() / 4;
+    n = E.dn.groups * E.dn.group_code_bytes() / 4;
     pack_codes_kernel<<<grid_for(n), 256, 0, st>>>(dn, E.dn, pc + E.dn_code_off);
-    n = E.gu.tiles * E.gu.tile_scale_bytes();
+    n = E.gu.groups * E.gu.group_scale_bytes();
     pack_scales_kernel<<<grid_for(n), 256, 0, st>>>(gu, E.gu, ps + E.gu_scale_off);
-    n = E.dn.tiles * E.dn.tile_scale_bytes();
+    n = E.dn.groups * E.dn.group_scale_bytes();
     pack_scales_kernel<<<grid_for(n), 256, 0, st>>>(dn, E.dn, ps + E.dn_scale_off);
     return cudaGetLastError();
 }

@@ -1,0 +1,131 @@
+// route.cu -- token -> expert grouping on the device (no host round trip).
+//
+// A stable counting sort of the T*k routing slots by expert id, in one CTA:
+//   1. histogram of expert ids in shared memory (order-free integer counts);
+//   2. exclusive prefix sum over the E counts (offsets);
+//   3. one warp walks the slots in order, 32 at a time: lanes that carry the
+//      same expert find each other with match.any, the lowest of them reserves
+//      a run of positions from that expert's cursor, and each lane takes
+//      cursor + (rank among the earlier equal lanes).  Slot order is kept
+//      within an expert, so perm is unique and the result bit-exact.
+// Out-of-range ids are left out (inv = -1, status "bad index"); perm entries
+// past the number of valid slots are -1.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kRouteThreads = 1024;
+
+__global__ void __launch_bounds__(kRouteThreads) k_route(RouteArgs a)
+{
+    extern __shared__ int s_cur[];          // E counters, then cursors
+    __shared__ int s_warp[kRouteThreads / 32];
+    __shared__ int s_bad;
+    const int n = a.n, E = a.E;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    pdl_wait();
+    for (int e = tid; e < E; e += blockDim.x) s_cur[e] = 0;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    for (int j = tid; j < n; j += blockDim.x) {
+        const int e = a.idx[j];
+        if (e >= 0 && e < E) atomicAdd(&s_cur[e], 1);
+        else s_bad = 1;
+    }
+    __syncthreads();
+
+    // exclusive scan over E: each thread owns a contiguous run of experts
+    const int per = (E + blockDim.x - 1) / blockDim.x;
+    const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+    int local = 0;
+    for (int e = e0; e < e1; e++) local += s_cur[e];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+        int v = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xFFFFFFFFu, v, o);
+            if (lane >= o) v += u;
+        }
+        if (lane < nw) s_warp[lane] = v;   // inclusive warp totals
+    }
+    __syncthreads();
+    int run = incl - local + (warp ? s_warp[warp - 1] : 0);   // exclusive start of my run
+    for (int e = e0; e < e1; e++) {
+        const int c = s_cur[e];
+        a.counts[e] = c;
+        a.offsets[e] = run;
+        s_cur[e] = run;                     // becomes the placement cursor
+        run += c;
+    }
+    const int total = s_warp[(blockDim.x >> 5) - 1];
+    if (tid == 0) {
+        a.offsets[E] = total;
+        if (s_bad) atomicOr(a.status, kStatusBadIndex);
+    }
+    __syncthreads();
+
+    // stable placement, one warp, slots in order
+    if (warp == 0) {
+        for (int base = 0; base < n; base += 32) {
+            const int j = base + lane;
+            const int e = j < n ? a.idx[j] : -1;
+            const bool valid = j < n && e >= 0 && e < E;
+            const int key = valid ? e : E + lane;          // invalid lanes match nobody
+            const unsigned mask = __match_any_sync(0xFFFFFFFFu, key);
+            const int leader = __ffs(mask) - 1;
+            const int rank = __popc(mask & ((1u << lane) - 1u));
+            int start = 0;
+            if (valid && lane == leader) {
+                start = s_cur[e];
+                s_cur[e] = start + __popc(mask);
+            }
+            start = __shfl_sync(0xFFFFFFFFu, start, leader);
+            if (valid) {
+                const int pos = start + rank;
+                a.perm[pos] = j;
+                a.inv[j] = pos;
+            } else if (j < n) {
+                a.inv[j] = -1;
+            }
+            __syncwarp();
+        }
+    }
+    for (int p = total + tid; p < n; p += blockDim.x) a.perm[p] = -1;
+    pdl_trigger();
+}
+
+}  // namespace
+
+int route_max_experts() { return 32768; }
+
+cudaError_t route_init_device()
+{
+    return cudaFuncSetAttribute((const void*)k_route, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                route_max_experts() * (int)sizeof(int));
+}
+
+cudaError_t launch_route(const RouteArgs& a0, cudaStream_t s)
+{
+    RouteArgs a = a0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kRouteThreads);
+    cfg.dynamicSmemBytes = (size_t)a.E * sizeof(int);
+    cfg.stream = s;
+    void* args[] = {&a};
+    return cudaLaunchKernelExC(&cfg, (const void*)k_route, args);
+}
+
+}  // namespace moe

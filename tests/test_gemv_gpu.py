@@ -72,23 +72,28 @@ def _pack_reference(codes, scales, H, I):
     """Independent numpy statement of the packed layout (tile / k-group /
     lane order) used to check moe_ffn_pack_expert byte for byte."""
     def section(cmat, smat, K, rows_of_tile, ntiles):
+        # tile groups of 4 tiles; per group: k-group, then tile, then
+        # [half][lane][block][4 bytes] codes and [g][half][block] scales
         out_c, out_s = [], []
         kgf, half = K // 128, (K % 128) // 64
-        for t in range(ntiles):
-            rows = rows_of_tile(t)
+        for grp in range(ntiles // 4):
             for kg in range(kgf + half):
                 nb = 4 if kg < kgf else 2
-                for lane in range(32):
-                    g, c = lane // 4, lane % 4
+                for q in range(4):
+                    rows = rows_of_tile(4 * grp + q)
                     for hf in range(2):
-                        r = rows[g + 8 * hf]
-                        for j in range(nb):
-                            b = kg * 4 + j
-                            out_c.append(cmat[r, b * 16 + 4 * c: b * 16 + 4 * c + 4])
-                for g in range(8):
-                    for hf in range(2):
-                        for j in range(nb):
-                            out_s.append(smat[rows[g + 8 * hf], kg * 4 + j: kg * 4 + j + 1])
+                        for lane in range(32):
+                            g, c = lane // 4, lane % 4
+                            r = rows[g + 8 * hf]
+                            for j in range(nb):
+                                b = kg * 4 + j
+                                out_c.append(cmat[r, b * 16 + 4 * c: b * 16 + 4 * c + 4])
+                for q in range(4):
+                    rows = rows_of_tile(4 * grp + q)
+                    for g in range(8):
+                        for hf in range(2):
+                            for j in range(nb):
+                                out_s.append(smat[rows[g + 8 * hf], kg * 4 + j: kg * 4 + j + 1])
         return np.concatenate(out_c), np.concatenate(out_s)
 
     gc, gs = I * H // 2, I * H // 32
