@@ -31,7 +31,7 @@ EXPORTS = [
     "moe_ffn_packed_codes_bytes", "moe_ffn_packed_scales_bytes", "moe_ffn_create",
     "moe_ffn_pack_expert", "moe_ffn_forward", "moe_ffn_forward_host", "moe_ffn_route",
     "moe_ffn_act_quant", "moe_stack_forward", "moe_ffn_profile_enable", "moe_ffn_profile_read",
-    "moe_ffn_status", "moe_ffn_strerror", "moe_ffn_destroy",
+    "moe_ffn_status", "moe_ffn_strerror", "moe_ffn_destroy", "moe_ffn_forward_noalloc",
 ]
 
 MOE_PHASE_PREP = 0
@@ -89,6 +89,7 @@ def lib() -> ctypes.CDLL:
             "moe_ffn_status": (I, [P, P]),
             "moe_ffn_strerror": (ctypes.c_char_p, [I]),
             "moe_ffn_destroy": (None, [P]),
+            "moe_ffn_forward_noalloc": (I, [cfgp, I, P, P, P, tblp, P, I, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -205,6 +206,15 @@ def moe_ffn_profile_read(h):
 def moe_ffn_status(h, stream=None) -> int:
     """Returns the (cleared) sticky device status code; does not raise."""
     return lib().moe_ffn_status(h, _s(stream))
+
+
+def moe_ffn_forward_noalloc(cfg: moe_ffn_config, device: int, x, topk_idx, topk_w,
+                            table: moe_expert_table, y, T: int, status=None, stream=None):
+    """The layer without a handle, using the library's fixed device scratch
+    array instead of allocating (see include/moe_ffn.h)."""
+    _check(lib().moe_ffn_forward_noalloc(ctypes.byref(cfg), int(device), _p(x), _p(topk_idx),
+                                         _p(topk_w), ctypes.byref(table), _p(y), int(T),
+                                         _p(status), _s(stream)), "moe_ffn_forward_noalloc")
 
 
 def moe_ffn_destroy(h) -> None:

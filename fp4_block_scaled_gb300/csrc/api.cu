@@ -122,6 +122,8 @@ int run_forward(moe_ffn* h, const void* x, const int32_t* idx, const float* w,
 
 }  // namespace
 
+int moe::check_config(const moe_ffn_config* cfg) { return check_cfg(cfg); }
+
 extern "C" {
 
 size_t moe_ffn_packed_codes_bytes(const moe_ffn_config* cfg)

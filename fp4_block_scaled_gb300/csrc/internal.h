@@ -6,6 +6,7 @@
 
 #include <vector>
 
+#include "../../include/moe_ffn.h"
 #include "layout.h"
 
 namespace moe {
@@ -104,6 +105,9 @@ struct ActQuantArgs {
     uint8_t* scales;        // [rows][ceil(n/128)]
 };
 cudaError_t launch_act_quant(const ActQuantArgs& a, cudaStream_t s, bool pdl);
+
+// Host-side config validation shared by the entry points (api.cu).
+int check_config(const moe_ffn_config* cfg);
 
 cudaError_t launch_pack_expert(const uint8_t* canon_codes, const uint8_t* canon_scales,
                                uint8_t* packed_codes, uint8_t* packed_scales, int H, int I,

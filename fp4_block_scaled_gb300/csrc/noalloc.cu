@@ -1,0 +1,154 @@
+// noalloc.cu -- moe_ffn_forward_noalloc: the batch-1 / small-batch layer
+// with its scratch memory in a fixed, file-scope device array.
+//
+// For callers that may not allocate device memory on their call path: hosts
+// that own every device allocation and give a library no allocator of its own
+// (embedded inference runtimes, plugin hosts with a fixed memory budget, code
+// that must never fail on an out-of-memory at call time).  moe_ffn_create
+// needs cudaMalloc for its workspace; this entry point needs no handle and
+// calls no cudaMalloc, cudaFree or allocating library routine.  It runs the
+// same kernels as moe_ffn_forward; their scratch (f16 activations, h, split-K
+// partial sums and counters) lives in g_scratch below.
+//
+// g_scratch is a static __device__ array: every GPU that loads this library
+// holds its kNoAllocScratchBytes until the process exits, and all calls share
+// it.  In host code the name g_scratch is only a host-side stand-in for the
+// symbol, not a device address; its device address is obtained once per
+// device with cudaGetSymbolAddress (with that device current) and passed to
+// the kernels.  That set-up runs during the first call on each device, so the
+// first call on a device should come before any stream capture.  Each call
+// clears the counters that must start at zero (cudaMemsetAsync on the call's
+// stream), but the array keeps the rest of the previous call's contents, and
+// two calls whose work overlaps on the GPU (different streams, or different
+// threads without ordering) race on it.
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 4u << 20;   // 4 MiB
+constexpr int kMaxDevices = 64;
+
+__device__ __align__(256) unsigned char g_scratch[kNoAllocScratchBytes];
+
+struct DeviceScratch {
+    void* ptr = nullptr;   // device address of g_scratch on that device
+    int sms = 0;
+    bool ready = false;
+};
+
+DeviceScratch g_devices[kMaxDevices];
+std::mutex g_setup_mutex;
+
+// Once per device, with the device current: resolve g_scratch's address and
+// prepare the kernels' shared-memory limits.
+int setup_device(int device, DeviceScratch** out)
+{
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    DeviceScratch& d = g_devices[device];
+    if (!d.ready) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_scratch) != cudaSuccess || !ptr) return MOE_ERR_CUDA;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (gemv_init_device() != cudaSuccess) return MOE_ERR_CUDA;
+        d.ptr = ptr;
+        d.sms = sms;
+        d.ready = true;
+    }
+    *out = &d;
+    return MOE_OK;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" int moe_ffn_forward_noalloc(const moe_ffn_config* cfg, int device, const void* x,
+                                       const int32_t* topk_idx, const float* topk_w,
+                                       const moe_expert_table* tbl, void* y, int T,
+                                       int* status, void* stream)
+{
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    if (cfg->act_mode != MOE_ACT_BF16) return MOE_ERR_UNSUPPORTED;
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !topk_idx || !topk_w || !y || !tbl || !tbl->codes || !tbl->scales || x == y)
+        return MOE_ERR_INVALID_ARG;
+    if (((uintptr_t)x | (uintptr_t)y) % 16 || ((uintptr_t)topk_idx | (uintptr_t)topk_w) % 4 ||
+        ((uintptr_t)status) % 4)
+        return MOE_ERR_INVALID_ARG;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (device < 0 || device >= ndev || device >= kMaxDevices) return MOE_ERR_INVALID_ARG;
+
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (prev != device && cudaSetDevice(device) != cudaSuccess) return MOE_ERR_CUDA;
+    struct Restore {
+        int prev, dev;
+        ~Restore() { if (prev >= 0 && prev != dev) cudaSetDevice(prev); }
+    } restore{prev, device};
+
+    DeviceScratch* d = nullptr;
+    rc = setup_device(device, &d);
+    if (rc) return rc;
+
+    // carve the scratch: counters and status first (cleared every call), then the rest
+    const int H = cfg->hidden, I = cfg->inter, k = cfg->topk;
+    const GemvWorkspaceSizes g = gemv_workspace_sizes(T, k, H, I, d->sms);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    const size_t o_status = take(sizeof(int));
+    const size_t o_cgu = take(g.cnt_gu * 4), o_cdn = take(g.cnt_dn * 4);
+    const size_t zero_bytes = off;
+    const size_t o_xh = take(g.xh * 2), o_xs = take(g.xs * 4);
+    const size_t o_pgu = take(g.part_gu * 4), o_hh = take(g.hh * 2), o_hs = take(g.hs * 4);
+    const size_t o_pdn = take(g.part_dn * 4);
+    if (off > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;   // problem too large for the array
+
+    cudaStream_t s = (cudaStream_t)stream;
+    char* b = (char*)d->ptr;
+    if (cudaMemsetAsync(b, 0, zero_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+    GemvArgs a;
+    memset(&a, 0, sizeof(a));
+    a.T = T;
+    a.topk = k;
+    a.E = cfg->num_experts;
+    a.H = H;
+    a.I = I;
+    a.sms = d->sms;
+    a.xs_stride = (H / 32 + 3) / 4 * 4;
+    a.hs_stride = (I / 32 + 3) / 4 * 4;
+    a.eps = 1e-6f;
+    a.x_bf16 = (const uint16_t*)x;
+    a.idx = topk_idx;
+    a.w = topk_w;
+    a.codes = tbl->codes;
+    a.scales = tbl->scales;
+    a.xh = (uint16_t*)(b + o_xh);
+    a.xs = (float*)(b + o_xs);
+    a.part_gu = (float*)(b + o_pgu);
+    a.cnt_gu = (int*)(b + o_cgu);
+    a.hh = (uint16_t*)(b + o_hh);
+    a.hs = (float*)(b + o_hs);
+    a.part_dn = (float*)(b + o_pdn);
+    a.cnt_dn = (int*)(b + o_cdn);
+    a.status = status ? status : (int*)(b + o_status);
+    a.y = y;
+    a.out_f32 = cfg->out_dtype == MOE_OUT_F32;
+    return launch_gemv_layer(a, s, true, nullptr) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

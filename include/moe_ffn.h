@@ -177,6 +177,34 @@ enum {
 int moe_ffn_profile_enable(moe_ffn_t h, int on);
 int moe_ffn_profile_read(moe_ffn_t h, double* ms, int* launches);
 
+/* moe_ffn_forward without a handle and without allocating.  The sources have
+ * no counterpart of this call; it serves callers that may not allocate device
+ * memory on their call path -- hosts that own every device allocation and give
+ * a library no allocator of its own (embedded inference runtimes, plugin hosts
+ * with a fixed memory budget), where moe_ffn_create's cudaMalloc is not
+ * allowed.  It calls no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * Same arguments and result as moe_ffn_forward (x, topk_idx, topk_w, y are
+ * device pointers; cfg is read on the host; only MOE_ACT_BF16), plus:
+ *   device  the CUDA device to run on (made current for the call)
+ *   status  optional DEVICE int; when non-NULL the kernels OR the device-side
+ *           status bits into it (1 = expert id out of range, 2 = a bounded
+ *           wait timed out); the caller clears it.  NULL: not reported.
+ * Scratch memory is one fixed 4 MiB array in this library's device code,
+ * present on every GPU that loads the library until the process exits and
+ * shared by all calls.  A call whose scratch need (for T tokens: activations,
+ * h, split-K partial sums and counters; about 240 KB per token at H = 4096,
+ * I = 2880, top-6) exceeds it returns MOE_ERR_UNSUPPORTED before enqueuing
+ * anything.  Each call clears the counters that must start at zero on
+ * `stream`; the array otherwise keeps the previous call's contents, and calls
+ * whose work overlaps on the GPU race on it, so calls must be ordered on one
+ * stream.  The first call on a device resolves the array's device address and
+ * sets kernel attributes; make that first call before any stream capture. */
+int moe_ffn_forward_noalloc(const moe_ffn_config* cfg, int device, const void* x,
+                            const int32_t* topk_idx, const float* topk_w,
+                            const moe_expert_table* tbl, void* y, int T, int* status,
+                            void* stream);
+
 /* Wait for `stream`, then return and clear the sticky device status:
  * MOE_OK, MOE_ERR_BAD_INDEX or MOE_ERR_DEVICE_TIMEOUT (or MOE_ERR_CUDA if the
  * read itself failed). */
