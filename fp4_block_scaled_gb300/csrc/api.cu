@@ -61,7 +61,7 @@ int check_cfg(const moe_ffn_config* c)
     if (c->act_mode != MOE_ACT_BF16 && c->act_mode != MOE_ACT_E4M3_UE8M0_128)
         return MOE_ERR_INVALID_ARG;
     if (c->out_dtype != MOE_OUT_BF16 && c->out_dtype != MOE_OUT_F32) return MOE_ERR_INVALID_ARG;
-    if (c->hidden % 64 || c->inter % 64) return MOE_ERR_UNSUPPORTED;
+    if (c->hidden % 128 || c->inter % 64) return MOE_ERR_UNSUPPORTED;
     if ((long long)c->hidden * c->inter > (1LL << 30)) return MOE_ERR_UNSUPPORTED;
     if (c->max_tokens > (1 << 16)) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
@@ -135,7 +135,7 @@ size_t moe_ffn_packed_codes_bytes(const moe_ffn_config* cfg)
 size_t moe_ffn_packed_scales_bytes(const moe_ffn_config* cfg)
 {
     if (check_cfg(cfg) != MOE_OK) return 0;
-    return make_expert_layout(cfg->hidden, cfg->inter).scale_bytes;
+    return make_expert_layout(cfg->hidden, cfg->inter).sf_bytes;
 }
 
 int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
@@ -170,9 +170,8 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
         return o;
     };
     size_t o_status = take(sizeof(int));
-    size_t o_xh = take(g.xh * 2), o_xs = take(g.xs * 4);
+    size_t o_xq = take(g.xq), o_xsf = take(g.xsf), o_hq = take(g.hq), o_hsf = take(g.hsf);
     size_t o_pgu = take(g.part_gu * 4), o_cgu = take(g.cnt_gu * 4);
-    size_t o_hh = take(g.hh * 2), o_hs = take(g.hs * 4);
     size_t o_pdn = take(g.part_dn * 4), o_cdn = take(g.cnt_dn * 4);
     size_t o_xst = take((size_t)T * H * 2), o_ist = take((size_t)T * k * 4);
     size_t o_wst = take((size_t)T * k * 4), o_yst = take((size_t)T * H * 4);
@@ -197,15 +196,13 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     a.H = H;
     a.I = I;
     a.sms = h->sms;
-    a.xs_stride = (H / 32 + 3) / 4 * 4;
-    a.hs_stride = (I / 32 + 3) / 4 * 4;
     a.eps = 1e-6f;
-    a.xh = (uint16_t*)(b + o_xh);
-    a.xs = (float*)(b + o_xs);
+    a.xq = (uint8_t*)(b + o_xq);
+    a.xsf = (uint8_t*)(b + o_xsf);
+    a.hq = (uint8_t*)(b + o_hq);
+    a.hsf = (uint8_t*)(b + o_hsf);
     a.part_gu = (float*)(b + o_pgu);
     a.cnt_gu = (int*)(b + o_cgu);
-    a.hh = (uint16_t*)(b + o_hh);
-    a.hs = (float*)(b + o_hs);
     a.part_dn = (float*)(b + o_pdn);
     a.cnt_dn = (int*)(b + o_cdn);
     a.status = h->status;

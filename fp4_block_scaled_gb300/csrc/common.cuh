@@ -175,6 +175,134 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// ---------------------------------------------------------------- tcgen05
+
+// Shared-memory matrix descriptor, K-major, no swizzle: core matrices of 8
+// rows x 16 bytes stored contiguously (128 B); lbo = byte distance between
+// core matrices adjacent along K, sbo = between adjacent 8-row groups.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;     // descriptor version of this MMA generation
+    return d;                   // base offset 0, no swizzle
+}
+
+// Instruction descriptor of kind::mxf4 block-scaled MMA: E2M1 x E2M1, ue8m0
+// scales, fp32 accumulate, both operands K-major.
+__host__ __device__ constexpr uint32_t mxf4_idesc(uint32_t M, uint32_t N)
+{
+    return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);
+}
+
+// scale-factor byte selectors (which two bytes of the 32-bit TMEM word)
+__device__ __forceinline__ uint32_t mxf4_idesc_sf(uint32_t idesc, uint32_t sf_id)
+{
+    return idesc | (sf_id << 29) | (sf_id << 4);
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 lanes x 128 bits from shared memory (a 512-byte scale-factor atom) to
+// TMEM, replicated to all four lane quadrants.
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread
+// has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Warp-collective: 16 consecutive 32-bit TMEM columns of this warp's 32 lanes.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// Two fp32 values to one byte of two E2M1 codes (lo -> low nibble),
+// round to nearest even, saturating at +-6.
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// E2M1 pair (low byte of w) back to two fp32 values.
+__device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t w)
+{
+    uint32_t h;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
+        : "=r"(h)
+        : "r"(w));
+    __half2 hv = *reinterpret_cast<__half2*>(&h);
+    return __half22float2(hv);
+}
+
+// Smallest e with amax <= 6 * 2^e (the ue8m0 scale of an E2M1 piece),
+// returned as the scale byte e + 127, clamped to [1, 254].  amax = m * 2^E,
+// m in [1, 2): e = E - 2 if m <= 1.5, else E - 1.
+__device__ __forceinline__ int e2m1_scale_byte(float amax)
+{
+    const uint32_t b = __float_as_uint(amax);
+    int ef = (int)((b >> 23) & 0xFF);
+    if (amax == 0.0f || ef == 0xFF) return 127;
+    int E;
+    uint32_t mant;
+    if (ef == 0) {
+        const uint32_t m = b & 0x7FFFFF;
+        const int p = 31 - __clz(m);
+        E = p - 149;
+        mant = (m << (23 - p)) & 0x7FFFFF;
+    } else {
+        E = ef - 127;
+        mant = b & 0x7FFFFF;
+    }
+    int e = (mant <= 0x400000u) ? E - 2 : E - 1;
+    int s = e + 127;
+    return s < 1 ? 1 : (s > 254 ? 254 : s);
+}
+
 // Named barrier over the first `threads` threads of the CTA (id 1..15).
 __device__ __forceinline__ void named_sync(int id, int threads)
 {

@@ -27,24 +27,24 @@ struct GemvArgs {
     const uint8_t* const* codes;
     const uint8_t* const* scales;
     // workspace
-    uint16_t* xh;                       // [T][H] f16, block-scaled
-    float* xs;                          // [T][xs_stride] block scales (H/32 used)
-    int xs_stride, hs_stride;           // H/32 and I/32 rounded up to a multiple of 4
-    float* part_gu;                     // [sms][2][64] partial sums of split groups
-    int* cnt_gu;                        // [T*k][I/32] units done per group
-    uint16_t* hh;                       // [T*k][I/32][2][32] f16 hi|lo
-    float* hs;                          // [T*k][hs_stride]
-    float* part_dn;                     // [sms][2][64]
-    int* cnt_dn;                        // [T][H/64]
+    uint8_t* xq;                        // [T][act_bytes(H)] activation pieces (B operand)
+    uint8_t* xsf;                       // [T][act_sf_bytes(H)] their scale atoms
+    uint8_t* hq;                        // [T*k][act_bytes(I)] pieces of w_k * h
+    uint8_t* hsf;                       // [T*k][act_sf_bytes(I)]
+    float* part_gu;                     // [sms][2][128] partial sums of split groups
+    int* cnt_gu;                        // [T*k][I/64] units done per group
+    float* part_dn;                     // [sms][2][128]
+    int* cnt_dn;                        // [T][H/128]
     int* status;
     // output (forward): y [T][H] fp32 or bf16
     void* y;
     int out_f32;
 };
 
-// Workspace element counts of the GEMV path for up to T tokens.
+// Workspace of the GEMV path for up to T tokens: bytes for xq, xsf, hq, hsf;
+// element counts for part_* (float) and cnt_* (int).
 struct GemvWorkspaceSizes {
-    size_t xh, xs, part_gu, cnt_gu, hh, hs, part_dn, cnt_dn;
+    size_t xq, xsf, hq, hsf, part_gu, cnt_gu, part_dn, cnt_dn;
 };
 GemvWorkspaceSizes gemv_workspace_sizes(int T, int topk, int H, int I, int sms);
 cudaError_t gemv_init_device();   // per device, before the first launch

@@ -1,58 +1,47 @@
 // layout.h -- packed expert layout shared by the packer and the kernels.
 //
-// An expert is three row-major matrices, each cut into "mma tiles" of 16
-// rows.  In the gate/up section tile t holds gate rows 8t..8t+7 followed by up
-// rows 8t..8t+7 (so one mma tile yields both SwiGLU inputs of 8 outputs); in
-// the down section tile t holds down rows 16t..16t+15.  Along K a tile is cut
-// into k-groups of 128 elements (4 scale blocks of 32) plus, when K % 128 == 64,
-// one half group of 64 elements at the end.
+// Each expert matrix is cut into tiles of 128 rows, the M of one tensor-core
+// MMA: a gate/up tile t holds gate rows 64t..64t+63 followed by up rows
+// 64t..64t+63 (so one accumulator holds both SwiGLU inputs of 64 outputs); a
+// down tile t holds down rows 128t..128t+127.  Along K a tile is cut into
+// units of 128 elements (two MMAs of K = 64, four ue8m0 blocks of 32), plus one
+// half unit of 64 when K % 128 == 64.
 //
-// Four consecutive tiles form a tile group (64 rows: 32 SwiGLU outputs in the
-// gate/up section, 64 output rows in the down section).  A tile group is
-// stored k-group by k-group, and within a k-group tile by tile, so one
-// "unit" = (tile group, k-group) is a contiguous 4 KB span of codes (2 KB for
-// the half group) and 256 B of scales (128 B), and consecutive units of a tile
-// group are adjacent.  The kernels stream units with bulk copies.
-//
-// Codes of one tile's full k-group (1024 bytes) are ordered [half 0..1]
-// [lane 0..31][block 0..3][4 bytes]: lane (g = lane/4, c = lane%4) finds, for
-// mma row g + 8*half, bytes 4c..4c+3 of each of the 4 blocks -- exactly the
-// E2M1 pairs its mma.m16n8k16 A fragments need -- in two conflict-free 16-byte
-// shared-memory reads.  A half group (512 bytes) is [half][lane][block 0..1]
-// [4 bytes].  Scales of a tile's full group (64 bytes) are [g 0..7][half]
-// [block 0..3], of a half group (32 bytes) [g][half][block 0..1].  The packing
-// is a pure permutation: sizes equal the published layout's.
+// Codes of a unit (8 KB; 4 KB for a half unit) are stored as the MMA reads
+// them from shared memory: per MMA m (4 KB), 16 row groups of 8 rows, each
+// holding two "core matrices" of 8 rows x 16 bytes (the two 32-element blocks
+// of that MMA's K range), i.e. offset = m*4096 + (row/8)*256 + c*128 +
+// (row%8)*16 for block 2m+c of the unit.  Scales of a unit are one 512-byte
+// atom: byte (row%32)*16 + (row/32)*4 + kb holds the scale of block kb of row
+// `row` -- the order in which tcgen05.cp moves 32 lanes x 128 bits into the
+// tensor memory for 128 rows.  A half unit's atom leaves bytes kb = 2, 3 at
+// 127 (scale 1, never read).  Tiles are stored one after another and units of
+// a tile are adjacent, so a run of units is one contiguous span of codes and
+// one of scales.  Codes are a pure permutation of the published layout; the
+// scales of a half unit are padded from 256 to 512 bytes.
 #pragma once
 #include <stddef.h>
 #include <stdint.h>
 
 namespace moe {
 
-constexpr int kTilesPerGroup = 4;
-constexpr int kUnitCodeBytes = 4096;   // full k-group of a tile group
-constexpr int kUnitScaleBytes = 256;
+constexpr int kTileRows = 128;
+constexpr int kUnitCodeBytes = 8192;   // 128 rows x 128 E2M1 codes
+constexpr int kMmaCodeBytes = 4096;    // one MMA (K = 64)
+constexpr int kUnitSfBytes = 512;      // scale atom of a unit
 
 struct MatLayout {
-    int rows;      // matrix rows (mma rows)
-    int k;         // reduction length (multiple of 64)
-    int tiles;     // rows / 16
-    int groups;    // tiles / 4
+    int rows;      // matrix rows
+    int k;         // reduction length
+    int tiles;     // rows / 128
     int kg_full;   // k / 128
     int kg_half;   // 1 if k % 128 == 64
     __host__ __device__ int kgt() const { return kg_full + kg_half; }
-    __host__ __device__ size_t tile_code_bytes() const { return (size_t)16 * k / 2; }
-    __host__ __device__ size_t tile_scale_bytes() const { return (size_t)16 * k / 32; }
-    __host__ __device__ size_t group_code_bytes() const { return kTilesPerGroup * tile_code_bytes(); }
-    __host__ __device__ size_t group_scale_bytes() const { return kTilesPerGroup * tile_scale_bytes(); }
-    // offset of unit (tile group, k-group) inside the section
-    __host__ __device__ size_t unit_code_off(int grp, int kg) const
+    __host__ __device__ size_t tile_code_bytes() const
     {
-        return (size_t)grp * group_code_bytes() + (size_t)kg * kUnitCodeBytes;
+        return (size_t)kg_full * kUnitCodeBytes + (size_t)kg_half * kMmaCodeBytes;
     }
-    __host__ __device__ size_t unit_scale_off(int grp, int kg) const
-    {
-        return (size_t)grp * group_scale_bytes() + (size_t)kg * kUnitScaleBytes;
-    }
+    __host__ __device__ size_t tile_sf_bytes() const { return (size_t)kgt() * kUnitSfBytes; }
 };
 
 __host__ __device__ inline MatLayout make_layout(int rows, int k)
@@ -60,18 +49,17 @@ __host__ __device__ inline MatLayout make_layout(int rows, int k)
     MatLayout m;
     m.rows = rows;
     m.k = k;
-    m.tiles = rows / 16;
-    m.groups = m.tiles / kTilesPerGroup;
+    m.tiles = rows / kTileRows;
     m.kg_full = k / 128;
     m.kg_half = (k % 128) ? 1 : 0;
     return m;
 }
 
 struct ExpertLayout {
-    MatLayout gu;   // 2*I rows (gate and up interleaved per 8), K = H
+    MatLayout gu;   // 2*I rows (gate / up halves per tile), K = H
     MatLayout dn;   // H rows, K = I
     size_t gu_code_off, dn_code_off, code_bytes;
-    size_t gu_scale_off, dn_scale_off, scale_bytes;
+    size_t gu_sf_off, dn_sf_off, sf_bytes;
 };
 
 __host__ __device__ inline ExpertLayout make_expert_layout(int hidden, int inter)
@@ -82,10 +70,31 @@ __host__ __device__ inline ExpertLayout make_expert_layout(int hidden, int inter
     L.gu_code_off = 0;
     L.dn_code_off = (size_t)L.gu.tiles * L.gu.tile_code_bytes();
     L.code_bytes = L.dn_code_off + (size_t)L.dn.tiles * L.dn.tile_code_bytes();
-    L.gu_scale_off = 0;
-    L.dn_scale_off = (size_t)L.gu.tiles * L.gu.tile_scale_bytes();
-    L.scale_bytes = L.dn_scale_off + (size_t)L.dn.tiles * L.dn.tile_scale_bytes();
+    L.gu_sf_off = 0;
+    L.dn_sf_off = (size_t)L.gu.tiles * L.gu.tile_sf_bytes();
+    L.sf_bytes = L.dn_sf_off + (size_t)L.dn.tiles * L.dn.tile_sf_bytes();
     return L;
+}
+
+// Activation operand ("pieces"): a vector v of length K is carried as 8
+// E2M1 vectors p_0..p_7 with one ue8m0 scale per (piece, 32-block), so that
+// v = sum_p p_p * scale; p_0 is v rounded to E2M1 under its block scale and
+// each next piece encodes what is left.  As the MMA's B operand it is 16 rows
+// (pieces 0..7, then 8 zero rows) per unit: per MMA m, 512 bytes laid out like
+// the A codes (2 row groups x 2 core matrices x 8 rows x 16 bytes), and a
+// 512-byte scale atom per unit (rows 0..15 used).
+constexpr int kPieces = 8;
+constexpr int kBRows = 16;
+constexpr int kMmaBBytes = 512;
+constexpr int kUnitBBytes = 1024;
+
+__host__ __device__ inline size_t act_bytes(int k)       // B codes of one vector
+{
+    return (size_t)(k / 128) * kUnitBBytes + (size_t)((k % 128) ? kMmaBBytes : 0);
+}
+__host__ __device__ inline size_t act_sf_bytes(int k)    // B scale atoms of one vector
+{
+    return (size_t)((k + 127) / 128) * kUnitSfBytes;
 }
 
 }  // namespace moe

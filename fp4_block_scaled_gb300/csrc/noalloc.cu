@@ -7,7 +7,7 @@
 // that must never fail on an out-of-memory at call time).  moe_ffn_create
 // needs cudaMalloc for its workspace; this entry point needs no handle and
 // calls no cudaMalloc, cudaFree or allocating library routine.  It runs the
-// same kernels as moe_ffn_forward; their scratch (f16 activations, h, split-K
+// same kernels as moe_ffn_forward; their scratch (activation pieces, h, split-K
 // partial sums and counters) lives in g_scratch below.
 //
 // g_scratch is a static __device__ array: every GPU that loads this library
@@ -114,9 +114,8 @@ extern "C" int moe_ffn_forward_noalloc(const moe_ffn_config* cfg, int device, co
     const size_t o_status = take(sizeof(int));
     const size_t o_cgu = take(g.cnt_gu * 4), o_cdn = take(g.cnt_dn * 4);
     const size_t zero_bytes = off;
-    const size_t o_xh = take(g.xh * 2), o_xs = take(g.xs * 4);
-    const size_t o_pgu = take(g.part_gu * 4), o_hh = take(g.hh * 2), o_hs = take(g.hs * 4);
-    const size_t o_pdn = take(g.part_dn * 4);
+    const size_t o_xq = take(g.xq), o_xsf = take(g.xsf), o_hq = take(g.hq), o_hsf = take(g.hsf);
+    const size_t o_pgu = take(g.part_gu * 4), o_pdn = take(g.part_dn * 4);
     if (off > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;   // problem too large for the array
 
     cudaStream_t s = (cudaStream_t)stream;
@@ -131,20 +130,18 @@ extern "C" int moe_ffn_forward_noalloc(const moe_ffn_config* cfg, int device, co
     a.H = H;
     a.I = I;
     a.sms = d->sms;
-    a.xs_stride = (H / 32 + 3) / 4 * 4;
-    a.hs_stride = (I / 32 + 3) / 4 * 4;
     a.eps = 1e-6f;
     a.x_bf16 = (const uint16_t*)x;
     a.idx = topk_idx;
     a.w = topk_w;
     a.codes = tbl->codes;
     a.scales = tbl->scales;
-    a.xh = (uint16_t*)(b + o_xh);
-    a.xs = (float*)(b + o_xs);
+    a.xq = (uint8_t*)(b + o_xq);
+    a.xsf = (uint8_t*)(b + o_xsf);
+    a.hq = (uint8_t*)(b + o_hq);
+    a.hsf = (uint8_t*)(b + o_hsf);
     a.part_gu = (float*)(b + o_pgu);
     a.cnt_gu = (int*)(b + o_cgu);
-    a.hh = (uint16_t*)(b + o_hh);
-    a.hs = (float*)(b + o_hs);
     a.part_dn = (float*)(b + o_pdn);
     a.cnt_dn = (int*)(b + o_cdn);
     a.status = status ? status : (int*)(b + o_status);

@@ -29,7 +29,9 @@ def test_packed_sizes_equal_published_sizes():
     cfg = moe.config(384, 4096, 2880, 6, 1)
     nc, ns = synth.expert_sizes(4096, 2880)
     assert moe.moe_ffn_packed_codes_bytes(cfg) == nc == 17694720
-    assert moe.moe_ffn_packed_scales_bytes(cfg) == ns == 1105920
+    # scale atoms of the 64-wide half unit of each 128-row down tile are padded to 512 B
+    assert ns == 1105920
+    assert moe.moe_ffn_packed_scales_bytes(cfg) == ns + (4096 // 128) * 256
     cfg = moe.config(8, 256, 128, 2, 1)
     assert moe.moe_ffn_packed_codes_bytes(cfg) == 3 * 256 * 128 // 2
 
@@ -39,7 +41,8 @@ def test_invalid_configs_are_rejected_on_the_host():
         moe.config(0, 4096, 2880, 6, 1),
         moe.config(8, 4096, 2880, 0, 1),
         moe.config(8, 4096, 2880, 9, 1),        # topk > E
-        moe.config(8, 4000, 2880, 6, 1),        # H % 64
+        moe.config(8, 4000, 2880, 6, 1),        # H % 128
+        moe.config(8, 4160, 2880, 6, 1),        # H % 128 (a multiple of 64)
         moe.config(8, 4096, 2850, 6, 1),        # I % 64
         moe.config(8, 4096, 2880, 6, -1),
         moe.config(8, 4096, 2880, 6, 1, act_mode=7),

@@ -12,7 +12,7 @@ from moe_setup import assert_close, bf16_to_f64, errors, fill_layer, host_expert
 pytestmark = pytest.mark.gpu
 
 TINY = dict(E=8, H=256, I=128, k=2)
-MID = dict(E=16, H=1024, I=448, k=6)      # down K = 448: 3 full k-groups + a 64-wide tail
+MID = dict(E=16, H=1024, I=448, k=6)      # down K = 448: 3 full units + a 64-wide half unit
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -69,31 +69,26 @@ def test_device_fill_matches_host_generator():
 
 
 def _pack_reference(codes, scales, H, I):
-    """Independent numpy statement of the packed layout (tile / k-group /
-    lane order) used to check moe_ffn_pack_expert byte for byte."""
+    """Independent numpy statement of the packed layout (tiles of 128 rows,
+    units of 128 K, per MMA 16 row groups x 2 core matrices x 8 rows x 16 B;
+    one 512-byte scale atom per unit) used to check moe_ffn_pack_expert."""
     def section(cmat, smat, K, rows_of_tile, ntiles):
-        # tile groups of 4 tiles; per group: k-group, then tile, then
-        # [half][lane][block][4 bytes] codes and [g][half][block] scales
         out_c, out_s = [], []
         kgf, half = K // 128, (K % 128) // 64
-        for grp in range(ntiles // 4):
+        for t in range(ntiles):
+            rows = rows_of_tile(t)
             for kg in range(kgf + half):
-                nb = 4 if kg < kgf else 2
-                for q in range(4):
-                    rows = rows_of_tile(4 * grp + q)
-                    for hf in range(2):
-                        for lane in range(32):
-                            g, c = lane // 4, lane % 4
-                            r = rows[g + 8 * hf]
-                            for j in range(nb):
-                                b = kg * 4 + j
-                                out_c.append(cmat[r, b * 16 + 4 * c: b * 16 + 4 * c + 4])
-                for q in range(4):
-                    rows = rows_of_tile(4 * grp + q)
-                    for g in range(8):
-                        for hf in range(2):
-                            for j in range(nb):
-                                out_s.append(smat[rows[g + 8 * hf], kg * 4 + j: kg * 4 + j + 1])
+                for m in range(1 if kg == kgf else 2):
+                    for rg in range(16):
+                        for c in range(2):
+                            for r8 in range(8):
+                                b = kg * 4 + m * 2 + c
+                                out_c.append(cmat[rows[rg * 8 + r8], b * 16:b * 16 + 16])
+                atom = np.full(512, 127, np.uint8)
+                for r in range(128):
+                    for kb in range(2 if kg == kgf else 4):
+                        atom[(r % 32) * 16 + (r // 32) * 4 + kb] = smat[rows[r], kg * 4 + kb]
+                out_s.append(atom)
         return np.concatenate(out_c), np.concatenate(out_s)
 
     gc, gs = I * H // 2, I * H // 32
@@ -105,12 +100,12 @@ def _pack_reference(codes, scales, H, I):
     sd = scales[2 * gs:].reshape(H, I // 32)
     cgu = np.concatenate([cg, cu])            # rows 0..I-1 gate, I..2I-1 up
     sgu = np.concatenate([sg, su])
-    pc1, ps1 = section(cgu, sgu, H, lambda t: [8 * t + r for r in range(8)] + [I + 8 * t + r for r in range(8)], I // 8)
-    pc2, ps2 = section(cd, sd, I, lambda t: [16 * t + r for r in range(16)], H // 16)
+    pc1, ps1 = section(cgu, sgu, H, lambda t: [64 * t + r for r in range(64)] + [I + 64 * t + r for r in range(64)], I // 64)
+    pc2, ps2 = section(cd, sd, I, lambda t: [128 * t + r for r in range(128)], H // 128)
     return np.concatenate([pc1, pc2]), np.concatenate([ps1, ps2])
 
 
-@pytest.mark.parametrize("dims", [TINY, dict(E=2, H=192, I=192, k=1)])
+@pytest.mark.parametrize("dims", [TINY, dict(E=2, H=256, I=192, k=1)])
 def test_pack_is_the_documented_permutation(dims):
     H, I = dims["H"], dims["I"]
     cfg = moe.config(dims["E"], H, I, dims["k"], 1)
