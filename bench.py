@@ -57,10 +57,6 @@ def expert_bytes(H, I):
     return 3 * H * I // 2 + 3 * H * I // 32
 
 
-def gate_up_bytes(H, I):
-    return 2 * (H * I // 2 + H * I // 32)
-
-
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
 
@@ -348,7 +344,7 @@ def run_ours(args, wl):
     bytes_step = sum(distinct) / K * expert_bytes(H, I) + act_io
     gbs_step = bytes_step / (ms_step / 1000.0) / 1e9
 
-    # ---- dominant kernel (gate/up) timed with CUDA events on its stream
+    # ---- dominant kernel (k_layer: both projections) timed with CUDA events on its stream
     peak, peak_kind = peaks()
     moe.moe_ffn_profile_enable(h, True)
     nprof = min(K, 2000)
@@ -358,13 +354,12 @@ def run_ours(args, wl):
     stream.synchronize()
     ms_ph, n_ph = moe.moe_ffn_profile_read(h)
     moe.moe_ffn_profile_enable(h, False)
-    gu_ms = ms_ph[moe.MOE_PHASE_GATE_UP] / max(1, n_ph[moe.MOE_PHASE_GATE_UP])
-    dn_ms = ms_ph[moe.MOE_PHASE_DOWN] / max(1, n_ph[moe.MOE_PHASE_DOWN])
+    ly_ms = ms_ph[moe.MOE_PHASE_GATE_UP] / max(1, n_ph[moe.MOE_PHASE_GATE_UP])
     pr_ms = ms_ph[moe.MOE_PHASE_PREP] / max(1, n_ph[moe.MOE_PHASE_PREP])
-    gu_dist = sum(len(set(int(v) for v in idx_np[i % R].reshape(-1))) for i in range(nprof)) / nprof
-    gu_bytes = gu_dist * gate_up_bytes(H, I)
-    achieved = gu_bytes / (gu_ms / 1000.0) / 1e9
-    traffic = traffic_record("k_gate_up")
+    ly_dist = sum(len(set(int(v) for v in idx_np[i % R].reshape(-1))) for i in range(nprof)) / nprof
+    ly_bytes = ly_dist * expert_bytes(H, I) + act_io
+    achieved = ly_bytes / (ly_ms / 1000.0) / 1e9
+    traffic = traffic_record("k_layer")
 
     # ---- end to end through the host-buffer entry point (copies in the timed region)
     ne2e = min(K, 2000)
@@ -398,16 +393,16 @@ def run_ours(args, wl):
                              "share no expert", "graph_chunk": chunk},
             "hbm_gbs": gbs_step, "hbm_frac": gbs_step / peak,
             "bytes_per_step": bytes_step,
-            "phase_us": {"prep": pr_ms * 1e3, "gate_up": gu_ms * 1e3, "down": dn_ms * 1e3},
-            "roofline": {"bound": "hbm", "kernel": "k_gate_up", "achieved": achieved,
+            "phase_us": {"prep": pr_ms * 1e3, "layer": ly_ms * 1e3},
+            "roofline": {"bound": "hbm", "kernel": "k_layer", "achieved": achieved,
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "algorithmic_bytes_per_launch": gu_bytes},
+                         "algorithmic_bytes_per_launch": ly_bytes},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": T * H * 2 + 2 * T * k * 4,
                     "d2h_bytes_per_step": T * H * 4},
-            "gpu_launches": 3 * K,
+            "gpu_launches": 2 * K,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -169,10 +169,9 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
         off = align_up(off + bytes, kAlign);
         return o;
     };
-    size_t o_status = take(sizeof(int));
+    size_t o_status = take(sizeof(int)), o_sync = take(kGemvSyncInts * sizeof(int));
     size_t o_xq = take(g.xq), o_xsf = take(g.xsf), o_hq = take(g.hq), o_hsf = take(g.hsf);
-    size_t o_pgu = take(g.part_gu * 4), o_cgu = take(g.cnt_gu * 4);
-    size_t o_pdn = take(g.part_dn * 4), o_cdn = take(g.cnt_dn * 4);
+    size_t o_pgu = take(g.part_gu * 8), o_pdn = take(g.part_dn * 8);
     size_t o_xst = take((size_t)T * H * 2), o_ist = take((size_t)T * k * 4);
     size_t o_wst = take((size_t)T * k * 4), o_yst = take((size_t)T * H * 4);
     h->ws_bytes = off;
@@ -201,10 +200,9 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     a.xsf = (uint8_t*)(b + o_xsf);
     a.hq = (uint8_t*)(b + o_hq);
     a.hsf = (uint8_t*)(b + o_hsf);
-    a.part_gu = (float*)(b + o_pgu);
-    a.cnt_gu = (int*)(b + o_cgu);
-    a.part_dn = (float*)(b + o_pdn);
-    a.cnt_dn = (int*)(b + o_cdn);
+    a.part_gu = (uint64_t*)(b + o_pgu);
+    a.part_dn = (uint64_t*)(b + o_pdn);
+    a.sync = (int*)(b + o_sync);
     a.status = h->status;
     a.out_f32 = cfg->out_dtype == MOE_OUT_F32;
     h->x_stage = (uint16_t*)(b + o_xst);

@@ -164,6 +164,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return true;
 }
 
+// As mbar_wait_bounded, but also gives up as soon as *abort is set.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, const int* abort,
+                                                   uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (*(const volatile int*)abort || globaltimer_ns() - t0 > limit_ns) return false;
+    return true;
+}
+
 // Bulk copy global -> this CTA's shared memory, completing tx bytes on `bar`.
 // dst, src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)

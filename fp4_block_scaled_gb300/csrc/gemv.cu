@@ -1,21 +1,29 @@
 // gemv.cu -- batch-1 / small-batch path of one routed FP4 MoE layer on the
 // fifth-generation tensor cores (tcgen05, block-scaled E2M1 MMA).
 //
-// Three launches per layer, chained with programmatic dependent launch (PDL):
-//   k_prep        x (bf16, or the fp32 residual through a fused RMSNorm) ->
-//                 8 E2M1 "pieces" per element with one ue8m0 scale per
-//                 (piece, 32-block): the MMA's B operand (see layout.h).
-//   k_tc<gate/up> per slot (t, k): Wg x and Wu x for 64 outputs per tile,
-//                 then h = w_k * silu(g) * u, written back as pieces.
-//   k_tc<down>    y[t] = sum_k Wd_k h_(t,k), or x += that in a stack.
+// Two launches per layer, chained with programmatic dependent launch (PDL):
+//   k_prep   x (bf16, or the fp32 residual through a fused RMSNorm) -> 16
+//            E2M1 "pieces" per element with one ue8m0 scale per (piece,
+//            32-block): the MMA's B operand (see layout.h).
+//   k_layer  both projections in one persistent grid, one CTA per SM:
+//            gate/up: per slot (t, k), Wg x and Wu x for 64 outputs per tile,
+//                     then h = w_k * silu(g) * u, written back as pieces;
+//            down:    y[t] = sum_k Wd_k h_(t,k), or x += that in a stack.
 //
-// k_tc is persistent, one CTA per SM.  A projection is a sequence of units --
-// one 128-K slice of one 128-row tile of one expert matrix: 8 KB of E2M1
-// codes + a 512 B scale atom -- and each CTA takes an equal contiguous range
-// of it (stream-K split), so every SM streams the same number of bytes.
-//   warp 0 (one thread)  bulk-copies chunks of 4 units, with the matching
-//                        activation pieces, from HBM into a ring of shared-
-//                        memory stages (cp.async.bulk, mbarrier tx counts);
+// A projection is a sequence of units -- one 128-K slice of one 128-row tile
+// of one expert matrix: 8 KB of E2M1 codes + a 512 B scale atom -- and each
+// CTA takes an equal contiguous range of it (stream-K split), so every SM
+// streams the same number of bytes.  Per CTA:
+//   warp 0 (one thread)  streams the weights: bulk-copies chunks of 4 units
+//                        (codes + scale atoms) from HBM into a ring of
+//                        shared-memory stages (cp.async.bulk, mbarrier tx
+//                        counts), gate/up then down without a pause, and
+//                        prefetches the rest of its down range into L2 at the
+//                        boundary;
+//   warp 9 (one thread)  copies the matching activation pieces into each
+//                        stage: x's once the previous kernel is done (PDL),
+//                        h's once every gate/up group of the grid has been
+//                        finalized (a grid-wide counter, bounded wait);
 //   warps 1-4            one MMA-issuing thread each (tcgen05 issue from a
 //                        single thread is serial; from several it overlaps):
 //                        issuer i moves the scale atoms of unit i of every
@@ -24,11 +32,13 @@
 //                        scale_vec 2X) into its own TMEM accumulator;
 //                        tcgen05.commit releases its part of the stage;
 //   warps 5-8            at the end of each reduction group read the issuers'
-//                        accumulators (tcgen05.ld), add the 8 piece columns
+//                        accumulators (tcgen05.ld), add the 16 piece columns
 //                        and the issuers in a fixed order, and finish the
-//                        group: directly when the CTA covered all of it, else
-//                        by the last contributor, which adds the CTAs' partial
-//                        sums in CTA order.
+//                        group.  A group split over several CTAs is finished
+//                        by the one holding its first unit, which reaches it
+//                        last; the others leave launch-tagged partial sums
+//                        that it adds in CTA order (no fences or counters on
+//                        the way, and mostly read before its own sum is done).
 // The tensor core does the E2M1 decoding, the per-(row, 32-block) scaling and
 // the fp32 accumulation; the CUDA cores only touch 128 values per group.
 // Results are bitwise reproducible on a given GPU.  Every wait is bounded
@@ -48,10 +58,10 @@ namespace {
 #define MOE_TC_STAGES 5
 #endif
 constexpr int kCU = MOE_TC_CU;
-constexpr int kStageCodes = kCU * kUnitCodeBytes;            // 16 KB
-constexpr int kStageSfa = kCU * kUnitSfBytes;                // 1 KB
-constexpr int kStageB = kCU * kUnitBBytes;                   // 2 KB
-constexpr int kStageSfb = kCU * kUnitSfBytes;                // 1 KB
+constexpr int kStageCodes = kCU * kUnitCodeBytes;            // 32 KB
+constexpr int kStageSfa = kCU * kUnitSfBytes;                // 2 KB
+constexpr int kStageB = kCU * kUnitBBytes;                   // 4 KB
+constexpr int kStageSfb = kCU * kUnitSfBytes;                // 2 KB
 constexpr int kOffSfa = kStageCodes;
 constexpr int kOffB = kOffSfa + kStageSfa;
 constexpr int kOffSfb = kOffB + kStageB;
@@ -60,29 +70,43 @@ constexpr int kStages = MOE_TC_STAGES;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 16;                                 // N = 16 fp32 columns
 constexpr int kIssuers = kCU;                                // MMA-issuing warps, one unit of a stage each
-constexpr int kSfCol0 = kIssuers * 2 * 16;                  // scale atoms after the accumulators
+constexpr int kSfCol0 = kIssuers * 2 * kAccCols;             // scale atoms after the accumulators
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr int kThreads = (1 + kIssuers + 4) * 32;     // producer, issuers, epilogue
+constexpr int kWarpEpi0 = 1 + kIssuers;                      // first of the 4 epilogue warps
+constexpr int kWarpLoader = kWarpEpi0 + 4;                   // activation copies
+constexpr int kThreads = (kWarpLoader + 1) * 32;
 constexpr int kJobWindow = 32;
+constexpr int kSlotCache = 256;                              // routing weights kept in shared memory
 
 #ifdef MOE_TC_TRACE
-// debug builds only: per-event timestamps of CTA 0 ([role][event], ns)
+// debug builds only: per-event timestamps of CTA 0 ([phase][role][idx], ns)
+// and per-CTA milestones
 }  // namespace
 __device__ long long g_tc_trace[2][4][4096];
-__device__ long long g_tc_cta[2][2][1024];   // per-CTA start / end
+__device__ long long g_tc_cta[8][1024];
 namespace {
-#define TC_TRACE(role, idx)                                                         \
+#define TC_TRACE(ph, role, idx)                                                     \
     do {                                                                            \
-        if (blockIdx.x == 0 && (idx) < 4096) g_tc_trace[PHASE][role][idx] = (long long)globaltimer_ns(); \
+        if (blockIdx.x == 0 && (idx) < 4096) g_tc_trace[ph][role][idx] = (long long)globaltimer_ns(); \
     } while (0)
+#define TC_CTA(slot) (g_tc_cta[slot][blockIdx.x] = (long long)globaltimer_ns())
 #else
-#define TC_TRACE(role, idx) \
-    do {                    \
+#define TC_TRACE(ph, role, idx) \
+    do {                        \
+    } while (0)
+#define TC_CTA(slot) \
+    do {             \
     } while (0)
 #endif
 
 static_assert(kStageBytes % 1024 == 0, "stage alignment");
 static_assert(kSfCol0 + kStages * kCU * 8 <= kTmemCols, "tensor memory budget");
+static_assert(kPieces == kAccCols && kBRows == kAccCols, "one accumulator column per piece");
+// k_layer's CTAs wait on one another (the down projection needs every h), so
+// two of them must never share an SM, where the second would block in the
+// tensor-memory allocation: the dynamic shared memory asked for is at least
+// more than half of an SM's.
+constexpr size_t kOneCtaPerSmSmem = 116 * 1024;
 
 struct JobInfo {
     const uint8_t* code;    // unit 0 of this job's tile
@@ -92,14 +116,26 @@ struct JobInfo {
     bool ok;
 };
 
+// Activation copy of one stage, posted by the weight producer.
+struct BSrc {
+    const uint8_t* B;       // nullptr: the stage multiplies nothing
+    const uint8_t* Bsf;
+    uint32_t nb, nsf;
+    int phase;
+};
+
 struct TcSmem {
     uint8_t stage[kStages][kStageBytes];
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[kStages];      // weights + activations of the stage landed
+    uint64_t empty[kStages];     // the issuers are done with the stage
+    uint64_t posted[kStages];    // the producer issued the stage's weights and posted bsrc
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
-    float comb[kTileRows];
-    JobInfo jobs[kJobWindow];
+    uint64_t drain[kIssuers];    // the issuers' last MMAs are done
+    BSrc bsrc[kStages];
+    float comb[2][kTileRows];
+    float slot_w[kSlotCache];    // w of each slot, 0 where its expert index is invalid
+    JobInfo jobs[2][kJobWindow]; // first jobs of the gate/up and down streams
     uint32_t tmem;
     int abort;
     int last;
@@ -118,37 +154,43 @@ struct StreamPlan {
 
 // ----------------------------------------------------------------- pieces
 
-// Write the 8 E2M1 pieces of one 32-element block held one value per lane:
-// piece p = round(r_p / 2^e_p) with e_p the smallest exponent such that
-// max|r_p| <= 6 * 2^e_p, and r_{p+1} = r_p - piece_p * 2^e_p (exact in fp32).
-// Bunit: the unit's B codes, Bsf: its scale atom, bu: block index in the unit.
-__device__ __forceinline__ void write_pieces(float v, int lane, uint8_t* Bunit, uint8_t* Bsf, int bu)
+// Pieces of 64 consecutive elements of a vector -- the 32-blocks blk0 and
+// blk0 + 1, blk0 even, so both lie in one MMA's K range -- held two per lane
+// (lane l: elements 2l and 2l + 1 of the span).  With e_0 the smallest
+// exponent such that the block's max|v| <= 6 * 2^e_0, piece p is the E2M1
+// rounding of the residual r_p at the scale 2^(e_0 - 2p), and r_(p+1) = r_p -
+// piece_p * 2^(e_0 - 2p), exact in fp32.  Rounding to E2M1 leaves at most
+// 2^(e_0 - 2p) of residual, inside the next piece's range 6 * 2^(e_0 - 2p - 2),
+// so the 16 pieces carry every element to within 2^(e_0 - 30) while only the
+// first scale needs a reduction across lanes.
+// Bunit: the unit's B codes, Bsf: its scale atom.
+__device__ __forceinline__ void write_pieces64(float v0, float v1, int lane, uint8_t* Bunit, uint8_t* Bsf,
+                                               int blk0)
 {
-    const int m = bu >> 1, c = bu & 1;
-    uint8_t* rows = Bunit + m * kMmaBBytes + c * 128;
-    float r = v;
-#pragma unroll 1
+    const int bu = (blk0 & 3) + (lane >> 4);       // block within the unit
+    const int i = lane & 15;                       // byte within the block's row
+    uint8_t* rows = Bunit + (bu >> 1) * kMmaBBytes + (bu & 1) * 128 + i;
+    float amax = fmaxf(fabsf(v0), fabsf(v1));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const int s0 = e2m1_scale_byte(amax);
+    float r0 = v0, r1 = v1;
+#pragma unroll
     for (int p = 0; p < kPieces; p++) {
-        const float amax = warp_max(fabsf(r));
-        const int s = e2m1_scale_byte(amax);
+        const int s = max(s0 - 2 * p, 1);
         const float down = exp2i(127 - s), up = exp2i(s - 127);
-        const float q = r * down;
-        const float qn = __shfl_xor_sync(0xFFFFFFFFu, q, 1);
-        const bool even = (lane & 1) == 0;
-        const uint32_t byte = f32x2_to_e2m1x2(even ? q : qn, even ? qn : q);
-        const float2 dec = e2m1x2_to_f32x2(byte);
-        r -= (even ? dec.x : dec.y) * up;
-        if (even) rows[p * 16 + (lane >> 1)] = (uint8_t)byte;
-        if (lane == 0) Bsf[p * 16 + bu] = (uint8_t)s;
+        const uint32_t byte = f32x2_to_e2m1x2(r0 * down, r1 * down);
+        const float2 d = e2m1x2_to_f32x2(byte);
+        r0 = fmaf(-d.x, up, r0);
+        r1 = fmaf(-d.y, up, r1);
+        rows[(p >> 3) * 256 + (p & 7) * 16] = (uint8_t)byte;
+        if (i == 0) Bsf[p * 16 + bu] = (uint8_t)s;
     }
-    // rows 8..15 of the operand are zero, with a finite scale
-    reinterpret_cast<uint32_t*>(rows + 256)[lane] = 0u;
-    if (lane < 8) Bsf[(kPieces + lane) * 16 + bu] = 127;
 }
 
 // ------------------------------------------------------------------ k_prep
 
-// grid (T, ceil(H/32 / 8)), 256 threads: one warp per 32-element block.
+// grid (T, ceil(H/64 / 8)), 256 threads: one warp per 64 elements.
 __global__ void __launch_bounds__(256) k_prep(GemvArgs a)
 {
     const int t = blockIdx.x;
@@ -176,21 +218,25 @@ __global__ void __launch_bounds__(256) k_prep(GemvArgs a)
         den = s_den;
     }
     pdl_trigger();
-    const int b = blockIdx.y * (blockDim.x >> 5) + warp;      // 32-element block
-    if (b >= H / 32) return;
-    const int i = b * 32 + lane;
-    float v;
-    if (a.x_resid)  // the MoE input is the bf16 rounding of the norm
-        v = __bfloat162float(__float2bfloat16_rn(a.x_resid[(size_t)t * H + i] / den));
-    else
-        v = __uint_as_float((uint32_t)a.x_bf16[(size_t)t * H + i] << 16);
-    const size_t ab = act_bytes(H), asb = act_sf_bytes(H);
-    uint8_t* Bunit = a.xq + (size_t)t * ab + (size_t)(b / 4) * kUnitBBytes;
-    uint8_t* Bsf = a.xsf + (size_t)t * asb + (size_t)(b / 4) * kUnitSfBytes;
-    write_pieces(v, lane, Bunit, Bsf, b % 4);
+    const int b = blockIdx.y * (blockDim.x >> 5) + warp;      // 64-element span
+    if (b >= H / 64) return;
+    const int i = b * 64 + 2 * lane;
+    float v0, v1;
+    if (a.x_resid) {  // the MoE input is the bf16 rounding of the norm
+        const float* xr = a.x_resid + (size_t)t * H + i;
+        v0 = __bfloat162float(__float2bfloat16_rn(xr[0] / den));
+        v1 = __bfloat162float(__float2bfloat16_rn(xr[1] / den));
+    } else {
+        const uint16_t* xb = a.x_bf16 + (size_t)t * H + i;   // only 2-byte alignment is assumed
+        v0 = __uint_as_float((uint32_t)xb[0] << 16);
+        v1 = __uint_as_float((uint32_t)xb[1] << 16);
+    }
+    uint8_t* Bunit = a.xq + (size_t)t * act_bytes(H) + (size_t)(b / 2) * kUnitBBytes;
+    uint8_t* Bsf = a.xsf + (size_t)t * act_sf_bytes(H) + (size_t)(b / 2) * kUnitSfBytes;
+    write_pieces64(v0, v1, lane, Bunit, Bsf, 2 * b);
 }
 
-// ------------------------------------------------------------------- k_tc
+// ----------------------------------------------------------------- k_layer
 
 template <int PHASE>
 __device__ __forceinline__ JobInfo job_info(const GemvArgs& a, const StreamPlan& p, long long job)
@@ -238,10 +284,36 @@ __device__ __forceinline__ int cta_of_unit(const StreamPlan& p, long long x)
     return (int)(((x + 1) * p.G - 1) / p.U);
 }
 
+// A CTA's unit range of one projection.
+struct Range {
+    uint32_t u0, u1, j0, jlast;
+};
+
+__device__ __forceinline__ Range cta_range(const StreamPlan& p)
+{
+    Range r;
+    r.u0 = (uint32_t)range_start(p, blockIdx.x);
+    r.u1 = (uint32_t)range_start(p, blockIdx.x + 1);
+    r.j0 = r.u0 / (uint32_t)p.kgt;
+    r.jlast = (r.u1 - 1) / (uint32_t)p.kgt;
+    return r;
+}
+
 // Walks a CTA's unit range in chunks (never crossing a job), as every role
 // must see the same sequence.
 struct Walk {
     uint32_t u, u1, kgt, job, kg, jg, jpg, group;
+    __device__ Walk(const StreamPlan& p, const Range& r)
+    {
+        u = r.u0;
+        u1 = r.u1;
+        kgt = (uint32_t)p.kgt;
+        job = r.j0;
+        kg = r.u0 - r.j0 * kgt;
+        jpg = (uint32_t)p.jobs_per_group;
+        jg = r.j0 % jpg;
+        group = r.j0 / jpg;
+    }
     __device__ uint32_t chunk() const { return min(min(kgt - kg, u1 - u), (uint32_t)kCU); }
     // advance past a chunk of n units; returns true when a group ended
     __device__ bool advance(uint32_t n, bool& next_job)
@@ -264,65 +336,419 @@ struct Walk {
     }
 };
 
-template <int PHASE>
-__device__ __forceinline__ void finalize_group(const GemvArgs& a, const StreamPlan& p, uint32_t group,
-                                               const float* comb, int row, int lane, TcSmem& sm)
+__device__ __forceinline__ int count_chunks(const StreamPlan& p, const Range& r)
 {
-    if (PHASE == 0) {
-        // group = (slot j, tile): rows 0..63 gate, 64..127 up of h indices 64*tile + i;
-        // the two warps holding rows 0..63 each turn one 32-block of h into pieces
-        if (row >= 64) return;
-        const int j = (int)(group / p.ntiles), tile = (int)(group % p.ntiles);
-        const int e = a.idx[j];
-        const bool ok = e >= 0 && e < a.E;
-        const float h = ok ? silu(comb[row]) * comb[64 + row] * a.w[j] : 0.0f;
-        const int hb = tile * 2 + (row >> 5);                 // 32-block of h
-        uint8_t* Bunit = a.hq + (size_t)j * act_bytes(a.I) + (size_t)(hb / 4) * kUnitBBytes;
-        uint8_t* Bsf = a.hsf + (size_t)j * act_sf_bytes(a.I) + (size_t)(hb / 4) * kUnitSfBytes;
-        write_pieces(h, lane, Bunit, Bsf, hb % 4);
-    } else {
-        // group = (token t, tile): 128 output rows, one per thread
-        const int t = (int)(group / p.ntiles), tile = (int)(group % p.ntiles);
-        const size_t o = (size_t)t * a.H + (size_t)tile * kTileRows + row;
-        const float val = comb[row];
-        if (a.x_resid) a.x_resid[o] += val;
-        else if (a.out_f32) reinterpret_cast<float*>(a.y)[o] = val;
-        else reinterpret_cast<__nv_bfloat16*>(a.y)[o] = __float2bfloat16_rn(val);
+    Walk wk(p, r);
+    int n = 0;
+    while (wk.u < wk.u1) {
+        bool nj;
+        wk.advance(wk.chunk(), nj);
+        n++;
     }
+    return n;
 }
 
 template <int PHASE>
-__global__ void __launch_bounds__(kThreads, 1) k_tc(GemvArgs a, StreamPlan p)
+__device__ __forceinline__ JobInfo job_at(const GemvArgs& a, const StreamPlan& p, const Range& r, TcSmem& sm,
+                                          uint32_t job)
+{
+    const uint32_t d = job - r.j0;
+    if (d < (uint32_t)kJobWindow) return sm.jobs[PHASE][d];
+    const JobInfo ji = job_info<PHASE>(a, p, job);
+    if (!ji.ok) atomicOr(a.status, kStatusBadIndex);
+    return ji;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const int* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void set_abort(const GemvArgs& a, TcSmem& sm)
+{
+    atomicOr(a.status, kStatusTimeout);
+    sm.abort = 1;
+}
+
+// ------------------------------------------------------------------ producer
+
+// Streams the weights of one projection's range into the ring and posts each
+// stage's activation source to the loader.  n: chunks so far (both phases).
+template <int PHASE>
+__device__ bool produce(const GemvArgs& a, const StreamPlan& p, const Range& r, TcSmem& sm, int& n)
+{
+    Walk wk(p, r);
+    const uint32_t kgt = wk.kgt;
+    JobInfo ji = job_at<PHASE>(a, p, r, sm, wk.job);
+    while (wk.u < wk.u1) {
+        const uint32_t nun = wk.chunk();
+        const bool has_half = p.kg_half && (wk.kg + nun == kgt);
+        const uint32_t nfull = nun - (has_half ? 1u : 0u);
+        const uint32_t cb = nfull * kUnitCodeBytes + (has_half ? kMmaCodeBytes : 0);
+        const uint32_t sb = nun * kUnitSfBytes;
+        const uint32_t bb = nfull * kUnitBBytes + (has_half ? kMmaBBytes : 0);
+        const uint32_t bsb = nun * kUnitSfBytes;
+        const int s = n % kStages;
+        if (n >= kStages && !mbar_wait_or_abort(&sm.empty[s], ((n / kStages) & 1) ^ 1, &sm.abort, kWaitLimitNs)) {
+            set_abort(a, sm);
+            return false;
+        }
+        uint8_t* stg = sm.stage[s];
+        if (ji.ok) {
+            mbar_arrive_expect_tx(&sm.full[s], cb + sb + bb + bsb);
+            bulk_g2s(stg, ji.code + (size_t)wk.kg * kUnitCodeBytes, cb, &sm.full[s]);
+            bulk_g2s(stg + kOffSfa, ji.sf + (size_t)wk.kg * kUnitSfBytes, sb, &sm.full[s]);
+            sm.bsrc[s] = BSrc{ji.B + (size_t)wk.kg * kUnitBBytes, ji.Bsf + (size_t)wk.kg * kUnitSfBytes, bb, bsb,
+                              PHASE};
+        } else {
+            mbar_arrive(&sm.full[s]);      // an empty stage: nothing to multiply
+            sm.bsrc[s].B = nullptr;
+        }
+        mbar_arrive(&sm.posted[s]);        // release: bsrc is visible to the loader
+        TC_TRACE(PHASE, 0, n);
+        bool nj;
+        wk.advance(nun, nj);
+        n++;
+        if (nj && wk.u < wk.u1) ji = job_at<PHASE>(a, p, r, sm, wk.job);
+    }
+    return true;
+}
+
+// The down weights beyond the first ring's worth go to L2 now, so that HBM
+// keeps streaming while the grid finishes h.
+__device__ void prefetch_down(const GemvArgs& a, const StreamPlan& p, const Range& r, TcSmem& sm)
+{
+    Walk wk(p, r);
+    const uint32_t kgt = wk.kgt;
+    JobInfo ji = job_at<1>(a, p, r, sm, wk.job);
+    for (int c = 0; wk.u < wk.u1; c++) {
+        const uint32_t nun = wk.chunk();
+        const bool has_half = p.kg_half && (wk.kg + nun == kgt);
+        const uint32_t cb = (nun - (has_half ? 1u : 0u)) * kUnitCodeBytes + (has_half ? kMmaCodeBytes : 0);
+        if (c >= kStages && ji.ok) {
+            prefetch_l2_bulk(ji.code + (size_t)wk.kg * kUnitCodeBytes, cb);
+            prefetch_l2_bulk(ji.sf + (size_t)wk.kg * kUnitSfBytes, nun * kUnitSfBytes);
+        }
+        bool nj;
+        wk.advance(nun, nj);
+        if (nj && wk.u < wk.u1) ji = job_at<1>(a, p, r, sm, wk.job);
+    }
+}
+
+// ------------------------------------------------------------------ loader
+
+// Issues the activation copies of every stage the producer posted, in order.
+// x's pieces wait for the previous kernel (PDL); h's for the grid-wide count
+// of finalized gate/up groups.  Once a stage is posted its copies are always
+// issued, even after a timeout, so that every transaction count completes.
+__device__ void load_b(const GemvArgs& a, int nchunks, uint32_t gu_groups, TcSmem& sm)
+{
+    bool pdl_done = false, h_done = false;
+    for (int n = 0; n < nchunks; n++) {
+        const int s = n % kStages;
+        if (!mbar_wait_or_abort(&sm.posted[s], (n / kStages) & 1, &sm.abort, kWaitLimitNs)) {
+            set_abort(a, sm);
+            return;
+        }
+        const BSrc q = sm.bsrc[s];
+        if (!q.B) continue;
+        if (!pdl_done) {
+            pdl_wait();
+            pdl_done = true;
+        }
+        if (q.phase == 1 && !h_done) {
+            bool ok = ld_acquire_u32(a.sync) >= gu_groups;
+            if (!ok) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!(ok = ld_acquire_u32(a.sync) >= gu_groups))
+                    if (*(volatile int*)&sm.abort || globaltimer_ns() - t0 > kWaitLimitNs) break;
+            }
+            TC_CTA(3);
+            // h was written with generic stores; the copies read it through the async proxy
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            if (!ok) set_abort(a, sm);
+            h_done = true;
+        }
+        uint8_t* stg = sm.stage[s];
+        bulk_g2s(stg + kOffB, q.B, q.nb, &sm.full[s]);
+        bulk_g2s(stg + kOffSfb, q.Bsf, q.nsf, &sm.full[s]);
+    }
+}
+
+// ------------------------------------------------------------------ MMA issue
+
+struct IssState {
+    int n, buf;
+    uint32_t use[2];
+    bool abort;
+};
+
+// Issuer ii takes unit ii of every stage into its own accumulator.
+template <int PHASE>
+__device__ void issue(const GemvArgs& a, const StreamPlan& p, const Range& r, TcSmem& sm, uint32_t tmem, int ii,
+                      IssState& is)
+{
+    const uint32_t idesc = mxf4_idesc(kTileRows, kBRows);
+    Walk wk(p, r);
+    const uint32_t kgt = wk.kgt;
+    bool ok = job_at<PHASE>(a, p, r, sm, wk.job).ok;
+    bool any = false;               // this issuer wrote its accumulator in this group
+    bool group_start = true;
+    while (wk.u < wk.u1) {
+        const uint32_t nun = wk.chunk();
+        const int s = is.n % kStages;
+        if (group_start) {
+            // the epilogue must have read this accumulator's previous group
+            if (!is.abort && is.use[is.buf] > 0 &&
+                !mbar_wait_or_abort(&sm.acc_empty[is.buf], (is.use[is.buf] - 1) & 1, &sm.abort, kWaitLimitNs)) {
+                set_abort(a, sm);
+                is.abort = true;
+            }
+            group_start = false;
+        }
+        if (!is.abort && !mbar_wait_or_abort(&sm.full[s], (is.n / kStages) & 1, &sm.abort, kWaitLimitNs)) {
+            set_abort(a, sm);
+            is.abort = true;
+        }
+        if (ii == 0) TC_TRACE(PHASE, 1, is.n);
+        if (!is.abort && ok && (uint32_t)ii < nun) {
+            tc_fence_after();
+            const uint8_t* st = sm.stage[s];
+            const uint32_t col = tmem + kSfCol0 + (uint32_t)(s * kCU + ii) * 8;
+            tc_cp_sf(col, umma_desc(smem_u32(st + kOffSfa + ii * kUnitSfBytes), 16, 128));
+            tc_cp_sf(col + 4, umma_desc(smem_u32(st + kOffSfb + ii * kUnitSfBytes), 16, 128));
+            const bool half = p.kg_half && (wk.kg + (uint32_t)ii == kgt - 1);
+            for (int m = 0; m < (half ? 1 : 2); m++) {
+                const uint64_t ad = umma_desc(smem_u32(st + ii * kUnitCodeBytes + m * kMmaCodeBytes), 128, 256);
+                const uint64_t bd = umma_desc(smem_u32(st + kOffB + ii * kUnitBBytes + m * kMmaBBytes), 128, 256);
+                tc_mma_mxf4(tmem + (uint32_t)(ii * 2 + is.buf) * kAccCols, ad, bd, mxf4_idesc_sf(idesc, 2 * m), col,
+                            col + 4, any ? 1u : 0u);
+                any = true;
+            }
+        }
+        tc_commit(&sm.empty[s]);           // this issuer's part of the stage is consumed
+        if (ii == 0) TC_TRACE(PHASE, 2, is.n);
+        bool nj;
+        const bool gend = wk.advance(nun, nj);
+        is.n++;
+        if (nj && wk.u < wk.u1) ok = job_at<PHASE>(a, p, r, sm, wk.job).ok;
+        if (gend) {
+            tc_commit(&sm.acc_full[is.buf]);   // this issuer's accumulator is final
+            is.use[is.buf]++;
+            is.buf ^= 1;
+            any = false;
+            group_start = true;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ epilogue
+
+__device__ __forceinline__ float slot_weight(const GemvArgs& a, const TcSmem& sm, int j)
+{
+    if (j < kSlotCache) return sm.slot_w[j];
+    const int e = a.idx[j];
+    return (e >= 0 && e < a.E) ? a.w[j] : 0.0f;
+}
+
+// Gate/up group (slot j, tile) -> the 64 values h = w_j * silu(g) * u, as
+// pieces, by one warp; then one more finished group on the grid-wide count.
+__device__ __forceinline__ void finalize_gate_up(const GemvArgs& a, const StreamPlan& p, const TcSmem& sm,
+                                                 uint32_t group, const float* comb, int lane)
+{
+    const int j = (int)(group / p.ntiles), tile = (int)(group % p.ntiles);
+    const float w = slot_weight(a, sm, j);
+    const float2 g = *reinterpret_cast<const float2*>(comb + 2 * lane);
+    const float2 u = *reinterpret_cast<const float2*>(comb + 64 + 2 * lane);
+    const float h0 = silu(g.x) * u.x * w, h1 = silu(g.y) * u.y * w;
+    uint8_t* Bunit = a.hq + (size_t)j * act_bytes(a.I) + (size_t)(tile / 2) * kUnitBBytes;
+    uint8_t* Bsf = a.hsf + (size_t)j * act_sf_bytes(a.I) + (size_t)(tile / 2) * kUnitSfBytes;
+    write_pieces64(h0, h1, lane, Bunit, Bsf, 2 * tile);
+    // the down projection reads these with bulk copies (async proxy), in other CTAs
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+        __threadfence();
+        atomicAdd(a.sync, 1);
+    }
+}
+
+struct EpiState {
+    int buf, cb;
+    uint32_t use[2];
+    uint32_t tag;               // this launch's tag of the partial sums
+};
+
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Partial sums of a split group from the CTAs after its owner, added in CTA
+// order into *acc; returns the first CTA not yet folded in.  With spin, waits
+// (bounded) for each; without, stops at the first that is not there yet.
+__device__ __forceinline__ int fold_partials(const uint64_t* part, int c, int c1, int row, uint32_t tag,
+                                             bool spin, float* acc, bool* timed_out)
+{
+    uint64_t t0 = 0;
+    while (c <= c1) {
+        const uint64_t e = ld_relaxed_u64(part + (size_t)c * kTileRows + row);
+        if ((uint32_t)(e >> 32) == tag) {
+            *acc += __uint_as_float((uint32_t)e);
+            c++;
+            continue;
+        }
+        if (!spin) break;
+        if (t0 == 0) t0 = globaltimer_ns();
+        else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *timed_out = true;
+            break;
+        }
+    }
+    return c;
+}
+
+template <int PHASE>
+__device__ void epilogue(const GemvArgs& a, const StreamPlan& p, const Range& r, TcSmem& sm, uint32_t tmem,
+                         int quad, int lane, int et, EpiState& es)
+{
+    uint64_t* part = PHASE == 0 ? a.part_gu : a.part_dn;
+    const int row = quad * 32 + lane;                      // accumulator row of this thread
+    const uint32_t gunits = (uint32_t)p.kgt * (uint32_t)p.jobs_per_group;
+    Walk wk(p, r);
+    uint32_t mask = 0;                                     // issuers that accumulated into this group
+    bool cur_ok = job_at<PHASE>(a, p, r, sm, wk.job).ok;
+    while (wk.u < wk.u1) {
+        bool nj;
+        const uint32_t group = wk.group;
+        const uint32_t nun = wk.chunk();
+        if (cur_ok) mask |= (1u << nun) - 1u;
+        const bool gend = wk.advance(nun, nj);
+        if (nj && wk.u < wk.u1) cur_ok = job_at<PHASE>(a, p, r, sm, wk.job).ok;
+        if (!gend) continue;
+
+        // ------------------------------------------- end of a reduction group
+        // A group split over CTAs c0..c1 is finished by c0, the CTA holding its
+        // first unit, which reaches it last (at the end of its range); the others
+        // leave their sums, tagged with the launch, in their partial vector.
+        const long long gs = (long long)group * gunits, ge = gs + gunits;
+        const bool owner = gs >= r.u0;
+        const int c1 = owner && ge > r.u1 ? cta_of_unit(p, ge - 1) : (int)blockIdx.x;
+        float pacc = 0.0f;
+        bool late = false;
+        int cnext = blockIdx.x + 1;
+        if (c1 > (int)blockIdx.x)   // while the last MMAs run: the partials that are there already
+            cnext = fold_partials(part, cnext, c1, row, es.tag, false, &pacc, &late);
+
+        const int buf = es.buf;
+        const bool ready = !*(volatile int*)&sm.abort &&
+                           mbar_wait_or_abort(&sm.acc_full[buf], es.use[buf] & 1, &sm.abort, kWaitLimitNs);
+        if (et == 0) TC_TRACE(PHASE, 3, es.use[0] + es.use[1]);
+        es.use[buf]++;
+        if (!ready) set_abort(a, sm);
+        tc_fence_after();
+        float v = 0.0f;
+        if (ready) {
+#pragma unroll
+            for (int ii = 0; ii < kIssuers; ii++) {
+                if (!((mask >> ii) & 1u)) continue;
+                float acc[16];
+                tc_ld16(tmem + (uint32_t)(ii * 2 + buf) * kAccCols + ((uint32_t)(quad * 32) << 16), acc);
+#pragma unroll
+                for (int c = 0; c < kPieces; c++) v += acc[c];
+            }
+        }
+        mask = 0;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);
+        es.buf ^= 1;
+
+        if (!owner) {
+            // a later part of a group owned by an earlier CTA
+            st_relaxed_u64(part + (size_t)blockIdx.x * kTileRows + row,
+                           ((uint64_t)es.tag << 32) | __float_as_uint(v));
+            continue;
+        }
+        if (cnext <= c1) {
+            const bool abort = *(volatile int*)&sm.abort;
+            fold_partials(part, cnext, c1, row, es.tag, !abort, &pacc, &late);
+            if (late) set_abort(a, sm);
+        }
+        v += pacc;
+        if (PHASE == 0) {
+            float* comb = sm.comb[es.cb];
+            comb[row] = v;
+            named_sync(1, 128);
+            if (et < 32) finalize_gate_up(a, p, sm, group, comb, lane);
+            es.cb ^= 1;
+        } else {
+            // group = (token t, tile): 128 output rows, one per thread
+            const int t = (int)(group / p.ntiles), tile = (int)(group % p.ntiles);
+            const size_t o = (size_t)t * a.H + (size_t)tile * kTileRows + row;
+            if (a.x_resid) a.x_resid[o] += v;
+            else if (a.out_f32) reinterpret_cast<float*>(a.y)[o] = v;
+            else reinterpret_cast<__nv_bfloat16*>(a.y)[o] = __float2bfloat16_rn(v);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+
+// One MoE layer: the gate/up projection then the down projection, in one
+// persistent grid.  The producer streams the down weights right after the
+// gate/up weights; only the copies of h wait until the last h piece is
+// written.
+__global__ void __launch_bounds__(kThreads, 1) k_layer(GemvArgs a, StreamPlan p0, StreamPlan p1)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     TcSmem& sm = *reinterpret_cast<TcSmem*>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t kgt = (uint32_t)p.kgt;
-    const uint32_t u0 = (uint32_t)range_start(p, blockIdx.x);
-    const uint32_t u1 = (uint32_t)range_start(p, blockIdx.x + 1);
-    const uint32_t j0 = u0 / kgt, jlast = (u1 - 1) / kgt;
-    const uint32_t jpg = (uint32_t)p.jobs_per_group;
-    const uint32_t gunits = kgt * jpg;
-    float* part = PHASE == 0 ? a.part_gu : a.part_dn;
-    int* cnt = PHASE == 0 ? a.cnt_gu : a.cnt_dn;
+    const Range r0 = cta_range(p0), r1 = cta_range(p1);
+    const uint32_t gu_groups = (uint32_t)(p0.U / ((long long)p0.kgt * p0.jobs_per_group));
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; s++) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], kIssuers);
+            mbar_init(&sm.posted[s], 1);
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(&sm.acc_full[b], kIssuers);
             mbar_init(&sm.acc_empty[b], 4);
         }
+        for (int i = 0; i < kIssuers; i++) mbar_init(&sm.drain[i], 1);
         sm.abort = 0;
         mbar_fence_init();
     }
-    if (warp == 0 && j0 + lane <= jlast && lane < kJobWindow) {
-        // resolve the CTA's first jobs (expert pointers) in parallel
-        const JobInfo ji = job_info<PHASE>(a, p, j0 + lane);
-        sm.jobs[lane] = ji;
-        if (!ji.ok) atomicOr(a.status, kStatusBadIndex);
+    if (warp == 0) {
+        // resolve the CTA's first jobs of both projections (expert pointers) in parallel
+        if (r0.j0 + lane <= r0.jlast && lane < kJobWindow) {
+            const JobInfo ji = job_info<0>(a, p0, r0.j0 + lane);
+            sm.jobs[0][lane] = ji;
+            if (!ji.ok) atomicOr(a.status, kStatusBadIndex);
+        }
+        if (r1.j0 + lane <= r1.jlast && lane < kJobWindow) {
+            const JobInfo ji = job_info<1>(a, p1, r1.j0 + lane);
+            sm.jobs[1][lane] = ji;
+            if (!ji.ok) atomicOr(a.status, kStatusBadIndex);
+        }
+    } else {
+        // routing weights of the slots (inputs of the layer, not of the previous kernel)
+        const int slots = min(a.T * a.topk, kSlotCache);
+        for (int j = threadIdx.x - 32; j < slots; j += kThreads - 32) {
+            const int e = a.idx[j];
+            sm.slot_w[j] = (e >= 0 && e < a.E) ? a.w[j] : 0.0f;
+        }
     }
     if (warp == 1) tmem_alloc(&sm.tmem, kTmemCols);
     tc_fence_before();
@@ -330,240 +756,65 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(GemvArgs a, StreamPlan p)
     tc_fence_after();
     pdl_trigger();
     const uint32_t tmem = sm.tmem;
-    if (threadIdx.x == 0) TC_TRACE(0, 4095);
-#ifdef MOE_TC_TRACE
-    if (threadIdx.x == 0) g_tc_cta[PHASE][0][blockIdx.x] = (long long)globaltimer_ns();
-#endif
-    auto job_at = [&](uint32_t job) -> JobInfo {
-        const uint32_t d = job - j0;
-        if (d < (uint32_t)kJobWindow) return sm.jobs[d];
-        const JobInfo ji = job_info<PHASE>(a, p, job);
-        if (!ji.ok) atomicOr(a.status, kStatusBadIndex);
-        return ji;
-    };
-    Walk w0{u0, u1, kgt, j0, u0 - j0 * kgt, j0 % jpg, jpg, j0 / jpg};
+    if (threadIdx.x == 0) TC_CTA(0);
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- producer
-        if (lane != 0) return;
-        struct Pend { int s; const uint8_t *B, *Bsf; uint32_t nb, nsf; };
-        Pend pend[kStages];
-        int npend = 0, n = 0;
-        bool pdl_done = false;
-        Walk wk = w0;
-        JobInfo ji = job_at(wk.job);
-        while (wk.u < wk.u1) {
-            const uint32_t nun = wk.chunk();
-            const bool has_half = p.kg_half && (wk.kg + nun == kgt);
-            const uint32_t nfull = nun - (has_half ? 1u : 0u);
-            const uint32_t cb = nfull * kUnitCodeBytes + (has_half ? kMmaCodeBytes : 0);
-            const uint32_t sb = nun * kUnitSfBytes;
-            const uint32_t bb = nfull * kUnitBBytes + (has_half ? kMmaBBytes : 0);
-            const uint32_t bsb = nun * kUnitSfBytes;
-            const int s = n % kStages;
-            if (n >= kStages) {
-                if (!pdl_done) {
-                    pdl_wait();
-                    for (int i = 0; i < npend; i++) {
-                        uint8_t* st = sm.stage[pend[i].s];
-                        bulk_g2s(st + kOffB, pend[i].B, pend[i].nb, &sm.full[pend[i].s]);
-                        bulk_g2s(st + kOffSfb, pend[i].Bsf, pend[i].nsf, &sm.full[pend[i].s]);
-                    }
-                    npend = 0;
-                    pdl_done = true;
-                }
-                if (*(volatile int*)&sm.abort ||
-                    !mbar_wait_bounded(&sm.empty[s], ((n / kStages) & 1) ^ 1, kWaitLimitNs)) {
-                    atomicOr(a.status, kStatusTimeout);
-                    sm.abort = 1;
-                    break;
-                }
+        if (lane == 0) {
+            int n = 0;
+            const bool ok = produce<0>(a, p0, r0, sm, n);
+            TC_CTA(2);
+            if (ok) {
+                prefetch_down(a, p1, r1, sm);
+                produce<1>(a, p1, r1, sm, n);
             }
-            uint8_t* st = sm.stage[s];
-            if (ji.ok) {
-                mbar_arrive_expect_tx(&sm.full[s], cb + sb + bb + bsb);
-                bulk_g2s(st, ji.code + (size_t)wk.kg * kUnitCodeBytes, cb, &sm.full[s]);
-                bulk_g2s(st + kOffSfa, ji.sf + (size_t)wk.kg * kUnitSfBytes, sb, &sm.full[s]);
-                const uint8_t* Bsrc = ji.B + (size_t)wk.kg * kUnitBBytes;
-                const uint8_t* Bsfsrc = ji.Bsf + (size_t)wk.kg * kUnitSfBytes;
-                if (pdl_done) {
-                    bulk_g2s(st + kOffB, Bsrc, bb, &sm.full[s]);
-                    bulk_g2s(st + kOffSfb, Bsfsrc, bsb, &sm.full[s]);
-                } else {
-                    pend[npend++] = Pend{s, Bsrc, Bsfsrc, bb, bsb};
-                }
-            } else {
-                mbar_arrive(&sm.full[s]);      // an empty stage: nothing to multiply
-            }
-            TC_TRACE(0, n);
-            bool nj;
-            wk.advance(nun, nj);
-            n++;
-            if (nj && wk.u < wk.u1) ji = job_at(wk.job);
+            // no copy may still be in flight into this CTA's memory at exit
+            for (int m = n > kStages ? n - kStages : 0; m < n; m++)
+                mbar_wait_bounded(&sm.full[m % kStages], (m / kStages) & 1, kWaitLimitNs);
         }
-        if (!pdl_done) {
-            pdl_wait();
-            for (int i = 0; i < npend; i++) {
-                uint8_t* st = sm.stage[pend[i].s];
-                bulk_g2s(st + kOffB, pend[i].B, pend[i].nb, &sm.full[pend[i].s]);
-                bulk_g2s(st + kOffSfb, pend[i].Bsf, pend[i].nsf, &sm.full[pend[i].s]);
-            }
-        }
-        // no copy may still be in flight into this CTA's memory at exit
-        for (int m = n > kStages ? n - kStages : 0; m < n; m++)
-            mbar_wait_bounded(&sm.full[m % kStages], (m / kStages) & 1, kWaitLimitNs);
         return;
     }
-
-    if (warp >= 1 && warp <= kIssuers) {
-        // ------------------------------------------------------------ MMA issue
-        // Issuer ii takes unit ii of every stage into its own accumulator:
-        // tcgen05 issue from one thread is serial, from several it overlaps.
+    if (warp == kWarpLoader) {
+        if (lane == 0) load_b(a, count_chunks(p0, r0) + count_chunks(p1, r1), gu_groups, sm);
+        return;
+    }
+    if (warp < kWarpEpi0) {
         if (lane == 0) {
-            const int ii = warp - 1;
-            const uint32_t idesc = mxf4_idesc(kTileRows, kBRows);
-            Walk wk = w0;
-            bool ok = job_at(wk.job).ok;
-            bool any = false;               // this issuer wrote its accumulator in this group
-            int n = 0, buf = 0;
-            uint32_t use[2] = {0, 0};
-            bool abort = false, group_start = true;
-            while (wk.u < wk.u1) {
-                const uint32_t nun = wk.chunk();
-                const int s = n % kStages;
-                if (group_start) {
-                    // the epilogue must have read this accumulator's previous group
-                    if (!abort && use[buf] > 0 &&
-                        !mbar_wait_bounded(&sm.acc_empty[buf], (use[buf] - 1) & 1, kWaitLimitNs)) {
-                        atomicOr(a.status, kStatusTimeout);
-                        sm.abort = 1;
-                        abort = true;
-                    }
-                    group_start = false;
-                }
-                if (!abort && (*(volatile int*)&sm.abort ||
-                               !mbar_wait_bounded(&sm.full[s], (n / kStages) & 1, kWaitLimitNs))) {
-                    atomicOr(a.status, kStatusTimeout);
-                    sm.abort = 1;
-                    abort = true;
-                }
-                if (ii == 0) TC_TRACE(1, n);
-                if (!abort && ok && (uint32_t)ii < nun) {
-                    tc_fence_after();
-                    const uint8_t* st = sm.stage[s];
-                    const uint32_t col = tmem + kSfCol0 + (uint32_t)(s * kCU + ii) * 8;
-                    tc_cp_sf(col, umma_desc(smem_u32(st + kOffSfa + ii * kUnitSfBytes), 16, 128));
-                    tc_cp_sf(col + 4, umma_desc(smem_u32(st + kOffSfb + ii * kUnitSfBytes), 16, 128));
-                    const bool half = p.kg_half && (wk.kg + (uint32_t)ii == kgt - 1);
-                    for (int m = 0; m < (half ? 1 : 2); m++) {
-                        const uint64_t ad = umma_desc(smem_u32(st + ii * kUnitCodeBytes + m * kMmaCodeBytes), 128, 256);
-                        const uint64_t bd = umma_desc(smem_u32(st + kOffB + ii * kUnitBBytes + m * kMmaBBytes), 128, 256);
-                        tc_mma_mxf4(tmem + (uint32_t)(ii * 2 + buf) * kAccCols, ad, bd, mxf4_idesc_sf(idesc, 2 * m),
-                                    col, col + 4, any ? 1u : 0u);
-                        any = true;
-                    }
-                }
-                tc_commit(&sm.empty[s]);       // this issuer's part of the stage is consumed
-                if (ii == 0) TC_TRACE(2, n);
-                bool nj;
-                const bool gend = wk.advance(nun, nj);
-                n++;
-                if (nj && wk.u < wk.u1) ok = job_at(wk.job).ok;
-                if (gend) {
-                    tc_commit(&sm.acc_full[buf]);  // this issuer's accumulator is final
-                    use[buf]++;
-                    buf ^= 1;
-                    any = false;
-                    group_start = true;
-                }
-            }
+            IssState is;
+            is.n = 0;
+            is.buf = 0;
+            is.use[0] = is.use[1] = 0;
+            is.abort = false;
+            issue<0>(a, p0, r0, sm, tmem, warp - 1, is);
+            if (warp == 1) TC_CTA(4);
+            issue<1>(a, p1, r1, sm, tmem, warp - 1, is);
+            // none of this thread's MMAs may be in flight when TMEM is freed (after
+            // an abort the epilogue no longer waits for the accumulators)
+            tc_commit(&sm.drain[warp - 1]);
+            mbar_wait_bounded(&sm.drain[warp - 1], 0, kWaitLimitNs);
         }
         __syncwarp();
     } else {
-        // ---------------------------------------------------------------- epilogue
         pdl_wait();
-        const int quad = warp & 3;                 // TMEM lane quadrant of this warp
-        const int row = quad * 32 + lane;          // accumulator row of this thread
-        const int et = threadIdx.x - (kIssuers + 1) * 32;   // 0..127 among the epilogue threads
-        Walk wk = w0;
-        uint32_t mask = 0;                         // issuers that accumulated into this group
-        bool cur_ok = job_at(wk.job).ok;
-        int buf = 0;
-        uint32_t use[2] = {0, 0};
-        uint32_t gstart = u0;
-        while (wk.u < wk.u1) {
-            bool nj;
-            const uint32_t group = wk.group;
-            const uint32_t nun = wk.chunk();
-            if (cur_ok) mask |= (1u << nun) - 1u;
-            const bool gend = wk.advance(nun, nj);
-            if (nj && wk.u < wk.u1) cur_ok = job_at(wk.job).ok;
-            if (!gend) continue;
-
-            // ------------------------------------------- end of a reduction group
-            const bool ready = mbar_wait_bounded(&sm.acc_full[buf], use[buf] & 1, kWaitLimitNs);
-            if (et == 0) TC_TRACE(3, use[0] + use[1]);
-            use[buf]++;
-            if (!ready) {
-                atomicOr(a.status, kStatusTimeout);
-                sm.abort = 1;
-            }
-            tc_fence_after();
-            float v = 0.0f;
-            if (ready && !*(volatile int*)&sm.abort) {
-#pragma unroll
-                for (int ii = 0; ii < kIssuers; ii++) {
-                    if (!((mask >> ii) & 1u)) continue;
-                    float acc[16];
-                    tc_ld16(tmem + (uint32_t)(ii * 2 + buf) * kAccCols + ((uint32_t)(quad * 32) << 16), acc);
-#pragma unroll
-                    for (int c = 0; c < kPieces; c++) v += acc[c];
-                }
-            }
-            mask = 0;
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);
-            buf ^= 1;
-
-            const bool complete = group * gunits >= u0 && (group + 1) * gunits <= u1;
-            if (!complete) {
-                const int slot = (group == u0 / gunits) ? 0 : 1;
-                float* mine = part + ((size_t)blockIdx.x * 2 + slot) * kTileRows;
-                mine[row] = v;
+        const int et = threadIdx.x - kWarpEpi0 * 32;     // 0..127 among the epilogue threads
+        EpiState es;
+        es.buf = 0;
+        es.cb = 0;
+        es.use[0] = es.use[1] = 0;
+        es.tag = 1u + (ld_acquire_u32(a.sync + 2) & 0x3FFFFFFFu);   // never 0, the cleared value
+        epilogue<0>(a, p0, r0, sm, tmem, warp & 3, lane, et, es);
+        if (et == 0) TC_CTA(5);
+        epilogue<1>(a, p1, r1, sm, tmem, warp & 3, lane, et, es);
+        if (et == 0) TC_CTA(6);
+        if (et == 0) {
+            // the last CTA to finish resets the layer's counters for the next launch
+            __threadfence();
+            const int done = atomicAdd(a.sync + 1, 1);
+            if (done == (int)gridDim.x - 1) {
+                a.sync[0] = 0;
+                a.sync[1] = 0;
+                a.sync[2] += 1;      // the next launch tags its partial sums differently
                 __threadfence();
-                named_sync(1, 128);
-                if (et == 0) {
-                    const int add = (int)(wk.u - gstart);
-                    const int old = atomicAdd(cnt + group, add);
-                    sm.last = (old + add == (int)gunits);
-                }
-                named_sync(1, 128);
-                const bool last = sm.last;
-                if (last) {
-                    __threadfence();
-                    const long long gs = (long long)group * gunits, ge = gs + gunits;
-                    const int c0 = cta_of_unit(p, gs), c1 = cta_of_unit(p, ge - 1);
-                    v = 0.0f;
-                    for (int c = c0; c <= c1; c++) {
-                        const int sl = (group == (uint32_t)(range_start(p, c) / gunits)) ? 0 : 1;
-                        v += __ldcg(part + ((size_t)c * 2 + sl) * kTileRows + row);
-                    }
-                    if (et == 0) cnt[group] = 0;       // ready for the next launch
-                }
-                if (last) {
-                    sm.comb[row] = v;
-                    named_sync(1, 128);
-                    finalize_group<PHASE>(a, p, group, sm.comb, row, lane, sm);
-                }
-                named_sync(1, 128);
-            } else {
-                sm.comb[row] = v;
-                named_sync(1, 128);
-                finalize_group<PHASE>(a, p, group, sm.comb, row, lane, sm);
-                named_sync(1, 128);
             }
-            gstart = wk.u;
         }
     }
     // the issuer and epilogue warps meet here before the tensor memory is released
@@ -571,9 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(GemvArgs a, StreamPlan p)
     named_sync(2, (kIssuers + 4) * 32);
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
-#ifdef MOE_TC_TRACE
-    if (threadIdx.x == 32) g_tc_cta[PHASE][1][blockIdx.x] = (long long)globaltimer_ns();
-#endif
+    if (threadIdx.x == 32) TC_CTA(1);
 }
 
 cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
@@ -592,7 +841,7 @@ cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, size_t smem, cudaSt
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-StreamPlan make_plan(const GemvArgs& a, int phase, int sms)
+StreamPlan make_plan(const GemvArgs& a, int phase)
 {
     StreamPlan p{};
     ExpertLayout E = make_expert_layout(a.H, a.I);
@@ -617,9 +866,10 @@ StreamPlan make_plan(const GemvArgs& a, int phase, int sms)
         p.act_bytes = act_bytes(a.I);
         p.act_sf_bytes = act_sf_bytes(a.I);
     }
-    p.G = (int)(p.U < sms ? p.U : sms);
     return p;
 }
+
+size_t layer_smem() { return sizeof(TcSmem) > kOneCtaPerSmSmem ? sizeof(TcSmem) : kOneCtaPerSmSmem; }
 
 }  // namespace
 
@@ -631,23 +881,18 @@ GemvWorkspaceSizes gemv_workspace_sizes(int T, int topk, int H, int I, int sms)
     s.xsf = (size_t)T * act_sf_bytes(H);
     s.hq = slots * act_bytes(I);
     s.hsf = slots * act_sf_bytes(I);
-    s.part_gu = (size_t)sms * 2 * kTileRows;
-    s.part_dn = (size_t)sms * 2 * kTileRows;
-    s.cnt_gu = slots * (size_t)(I / 64);
-    s.cnt_dn = (size_t)T * (size_t)(H / kTileRows);
+    s.part_gu = (size_t)sms * kTileRows;
+    s.part_dn = (size_t)sms * kTileRows;
     return s;
 }
 
 cudaError_t gemv_init_device()
 {
-    const int smem = (int)sizeof(TcSmem);
-    cudaError_t e = cudaFuncSetAttribute((const void*)k_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute((const void*)k_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    return e;
+    return cudaFuncSetAttribute((const void*)k_layer, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)layer_smem());
 }
 
-size_t gemv_stream_smem() { return sizeof(TcSmem); }
+size_t gemv_stream_smem() { return layer_smem(); }
 
 cudaError_t launch_gemv_layer(const GemvArgs& a0, cudaStream_t s, bool pdl, Profiler* prof)
 {
@@ -657,20 +902,20 @@ cudaError_t launch_gemv_layer(const GemvArgs& a0, cudaStream_t s, bool pdl, Prof
     {
         void* args[] = {&a};
         if (prof) prof->begin(kPhasePrep, s);
-        err = launch_ex((const void*)k_prep, dim3(a.T, (a.H / 32 + 7) / 8), dim3(256), 0, s, pdl && !prof, args);
+        err = launch_ex((const void*)k_prep, dim3(a.T, (a.H / 64 + 7) / 8), dim3(256), 0, s, pdl && !prof, args);
         if (prof) prof->end(s);
         if (err != cudaSuccess) return err;
     }
-    for (int phase = 0; phase < 2; phase++) {
-        StreamPlan p = make_plan(a, phase, a.sms);
-        void* args[] = {&a, &p};
-        const void* fn = phase == 0 ? (const void*)k_tc<0> : (const void*)k_tc<1>;
-        if (prof) prof->begin(phase == 0 ? kPhaseGateUp : kPhaseDown, s);
-        err = launch_ex(fn, dim3(p.G), dim3(kThreads), sizeof(TcSmem), s, pdl && !prof, args);
-        if (prof) prof->end(s);
-        if (err != cudaSuccess) return err;
-    }
-    return cudaSuccess;
+    StreamPlan p0 = make_plan(a, 0), p1 = make_plan(a, 1);
+    long long G = a.sms;
+    if (p0.U < G) G = p0.U;
+    if (p1.U < G) G = p1.U;
+    p0.G = p1.G = (int)G;     // every CTA has units of both projections
+    void* args[] = {&a, &p0, &p1};
+    if (prof) prof->begin(kPhaseGateUp, s);
+    err = launch_ex((const void*)k_layer, dim3((unsigned)G), dim3(kThreads), layer_smem(), s, pdl && !prof, args);
+    if (prof) prof->end(s);
+    return err;
 }
 
 }  // namespace moe

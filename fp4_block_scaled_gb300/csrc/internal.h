@@ -31,10 +31,13 @@ struct GemvArgs {
     uint8_t* xsf;                       // [T][act_sf_bytes(H)] their scale atoms
     uint8_t* hq;                        // [T*k][act_bytes(I)] pieces of w_k * h
     uint8_t* hsf;                       // [T*k][act_sf_bytes(I)]
-    float* part_gu;                     // [sms][2][128] partial sums of split groups
-    int* cnt_gu;                        // [T*k][I/64] units done per group
-    float* part_dn;                     // [sms][2][128]
-    int* cnt_dn;                        // [T][H/128]
+    // partial sums of split reduction groups, one 128-row vector per CTA and
+    // projection: entries are (fp32 bits | tag << 32), the tag naming the launch
+    uint64_t* part_gu;                  // [sms][128]
+    uint64_t* part_dn;                  // [sms][128]
+    int* sync;                          // [3]: gate/up groups finished, CTAs finished (both
+                                        // zero between launches: the last CTA resets them),
+                                        // launches so far (the partials' tag)
     int* status;
     // output (forward): y [T][H] fp32 or bf16
     void* y;
@@ -42,10 +45,11 @@ struct GemvArgs {
 };
 
 // Workspace of the GEMV path for up to T tokens: bytes for xq, xsf, hq, hsf;
-// element counts for part_* (float) and cnt_* (int).
+// entry counts for part_* (uint64); the sync words are kGemvSyncInts ints.
 struct GemvWorkspaceSizes {
-    size_t xq, xsf, hq, hsf, part_gu, cnt_gu, part_dn, cnt_dn;
+    size_t xq, xsf, hq, hsf, part_gu, part_dn;
 };
+constexpr int kGemvSyncInts = 3;
 GemvWorkspaceSizes gemv_workspace_sizes(int T, int topk, int H, int I, int sms);
 cudaError_t gemv_init_device();   // per device, before the first launch
 size_t gemv_stream_smem();

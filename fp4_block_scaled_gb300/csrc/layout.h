@@ -76,14 +76,14 @@ __host__ __device__ inline ExpertLayout make_expert_layout(int hidden, int inter
     return L;
 }
 
-// Activation operand ("pieces"): a vector v of length K is carried as 8
-// E2M1 vectors p_0..p_7 with one ue8m0 scale per (piece, 32-block), so that
-// v = sum_p p_p * scale; p_0 is v rounded to E2M1 under its block scale and
-// each next piece encodes what is left.  As the MMA's B operand it is 16 rows
-// (pieces 0..7, then 8 zero rows) per unit: per MMA m, 512 bytes laid out like
-// the A codes (2 row groups x 2 core matrices x 8 rows x 16 bytes), and a
-// 512-byte scale atom per unit (rows 0..15 used).
-constexpr int kPieces = 8;
+// Activation operand ("pieces"): a vector v of length K is carried as 16
+// E2M1 vectors p_0..p_15 with one ue8m0 scale per (piece, 32-block), so that
+// v = sum_p p_p * scale_p; p_0 is v rounded to E2M1 under its block scale and
+// each next piece encodes what is left.  As the MMA's B operand the pieces are
+// its N = 16 rows: per MMA m, 512 bytes laid out like the A codes (2 row groups
+// x 2 core matrices x 8 rows x 16 bytes), and a 512-byte scale atom per unit
+// (rows 0..15 used).
+constexpr int kPieces = 16;
 constexpr int kBRows = 16;
 constexpr int kMmaBBytes = 512;
 constexpr int kUnitBBytes = 1024;

@@ -102,7 +102,8 @@ extern "C" int moe_ffn_forward_noalloc(const moe_ffn_config* cfg, int device, co
     rc = setup_device(device, &d);
     if (rc) return rc;
 
-    // carve the scratch: counters and status first (cleared every call), then the rest
+    // carve the scratch: status and counters first (cleared every call, except
+    // the launch count that tags the partial sums), then the rest
     const int H = cfg->hidden, I = cfg->inter, k = cfg->topk;
     const GemvWorkspaceSizes g = gemv_workspace_sizes(T, k, H, I, d->sms);
     size_t off = 0;
@@ -111,11 +112,10 @@ extern "C" int moe_ffn_forward_noalloc(const moe_ffn_config* cfg, int device, co
         off = align_up(off + bytes, 256);
         return o;
     };
-    const size_t o_status = take(sizeof(int));
-    const size_t o_cgu = take(g.cnt_gu * 4), o_cdn = take(g.cnt_dn * 4);
-    const size_t zero_bytes = off;
+    const size_t o_status = take(sizeof(int)), o_sync = take(kGemvSyncInts * sizeof(int));
+    const size_t zero_bytes = o_sync + 2 * sizeof(int);
     const size_t o_xq = take(g.xq), o_xsf = take(g.xsf), o_hq = take(g.hq), o_hsf = take(g.hsf);
-    const size_t o_pgu = take(g.part_gu * 4), o_pdn = take(g.part_dn * 4);
+    const size_t o_pgu = take(g.part_gu * 8), o_pdn = take(g.part_dn * 8);
     if (off > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;   // problem too large for the array
 
     cudaStream_t s = (cudaStream_t)stream;
@@ -140,10 +140,9 @@ extern "C" int moe_ffn_forward_noalloc(const moe_ffn_config* cfg, int device, co
     a.xsf = (uint8_t*)(b + o_xsf);
     a.hq = (uint8_t*)(b + o_hq);
     a.hsf = (uint8_t*)(b + o_hsf);
-    a.part_gu = (float*)(b + o_pgu);
-    a.cnt_gu = (int*)(b + o_cgu);
-    a.part_dn = (float*)(b + o_pdn);
-    a.cnt_dn = (int*)(b + o_cdn);
+    a.part_gu = (uint64_t*)(b + o_pgu);
+    a.part_dn = (uint64_t*)(b + o_pdn);
+    a.sync = (int*)(b + o_sync);
     a.status = status ? status : (int*)(b + o_status);
     a.y = y;
     a.out_f32 = cfg->out_dtype == MOE_OUT_F32;
