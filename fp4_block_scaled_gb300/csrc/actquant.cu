@@ -16,33 +16,6 @@
 
 namespace moe {
 
-__device__ __forceinline__ int ue8m0_for_amax_bits(float amax)
-{
-    if (amax == 0.0f) return 127;
-    const uint32_t b = __float_as_uint(amax);
-    const int ef = (int)((b >> 23) & 0xFF);
-    if (ef == 0xFF) return 255;
-    int E;
-    uint32_t mant;
-    if (ef == 0) {                       // subnormal: amax = m * 2^-149
-        const uint32_t m = b & 0x7FFFFF;
-        const int p = 31 - __clz(m);     // leading one
-        E = p - 149;
-        mant = (m << (23 - p)) & 0x7FFFFF;
-    } else {
-        E = ef - 127;
-        mant = b & 0x7FFFFF;
-    }
-    int k = (mant <= 0x600000u) ? E - 8 : E - 7;
-    k = k < -127 ? -127 : (k > 127 ? 127 : k);
-    return k + 127;
-}
-
-__device__ __forceinline__ uint8_t e4m3_rn_sat(float v)
-{
-    return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
-}
-
 // x: [rows][n] bf16, codes [rows][n], scales [rows][nb]; optional row gather
 // (src_row[r] selects the input row of output row r; -1 writes zeros).
 __global__ void __launch_bounds__(256) k_act_quant(ActQuantArgs a)

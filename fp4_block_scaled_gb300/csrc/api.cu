@@ -112,7 +112,6 @@ int check_forward(const moe_ffn* h, const void* x, const int32_t* idx, const flo
 int run_forward(moe_ffn* h, const void* x, const int32_t* idx, const float* w,
                 const moe_expert_table* tbl, void* y, int T, cudaStream_t s)
 {
-    if (h->cfg.act_mode != MOE_ACT_BF16) return MOE_ERR_UNSUPPORTED;
     GemvArgs a = layer_args(h, T, idx, w, tbl);
     a.x_bf16 = (const uint16_t*)x;
     a.x_resid = nullptr;
@@ -160,7 +159,8 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     }
     const int T = cfg->max_tokens > 0 ? cfg->max_tokens : 1;
     const int H = cfg->hidden, I = cfg->inter, k = cfg->topk;
-    GemvWorkspaceSizes g = gemv_workspace_sizes(T, k, H, I, h->sms);
+    const bool e4m3 = cfg->act_mode == MOE_ACT_E4M3_UE8M0_128;
+    GemvWorkspaceSizes g = gemv_workspace_sizes(T, k, H, I, h->sms, e4m3);
 
     // one allocation, carved into aligned pieces
     size_t off = 0;
@@ -172,6 +172,7 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     size_t o_status = take(sizeof(int)), o_sync = take(kGemvSyncInts * sizeof(int));
     size_t o_xq = take(g.xq), o_xsf = take(g.xsf), o_hq = take(g.hq), o_hsf = take(g.hsf);
     size_t o_pgu = take(g.part_gu * 8), o_pdn = take(g.part_dn * 8);
+    size_t o_hraw = take(g.hraw), o_hpair = take(g.hpair);
     size_t o_xst = take((size_t)T * H * 2), o_ist = take((size_t)T * k * 4);
     size_t o_wst = take((size_t)T * k * 4), o_yst = take((size_t)T * H * 4);
     h->ws_bytes = off;
@@ -205,6 +206,9 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     a.sync = (int*)(b + o_sync);
     a.status = h->status;
     a.out_f32 = cfg->out_dtype == MOE_OUT_F32;
+    a.act_e4m3 = e4m3;
+    a.hraw = e4m3 ? (float*)(b + o_hraw) : nullptr;
+    a.hpair = e4m3 ? (int*)(b + o_hpair) : nullptr;
     h->x_stage = (uint16_t*)(b + o_xst);
     h->idx_stage = (int32_t*)(b + o_ist);
     h->w_stage = (float*)(b + o_wst);
@@ -309,7 +313,6 @@ int moe_stack_forward(moe_ffn_t h, float* x, const moe_expert_table* tbls,
     if (!aligned(x, 16) || !aligned(topk_idx, 4) || !aligned(topk_w, 4)) return MOE_ERR_INVALID_ARG;
     for (int l = 0; l < L; l++)
         if (!tbls[l].codes || !tbls[l].scales) return MOE_ERR_INVALID_ARG;
-    if (h->cfg.act_mode != MOE_ACT_BF16) return MOE_ERR_UNSUPPORTED;
     DeviceGuard guard(h->device);
     cudaStream_t s = (cudaStream_t)stream;
 

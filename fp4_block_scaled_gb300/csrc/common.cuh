@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace moe {
@@ -288,6 +289,48 @@ __device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t w)
         : "r"(w));
     __half2 hv = *reinterpret_cast<__half2*>(&h);
     return __half22float2(hv);
+}
+
+// The ue8m0 scale byte of an E4M3 block: k + 127 with k the least integer
+// such that amax <= 448 * 2^k, read off amax's bits (amax = m * 2^E, m in
+// [1, 2): k = E - 8 if m <= 1.75, else E - 7; 448 = 1.75 * 2^8).  A zero
+// maximum gives k = 0, a non-finite one the NaN byte 255.
+__device__ __forceinline__ int ue8m0_for_amax_bits(float amax)
+{
+    if (amax == 0.0f) return 127;
+    const uint32_t b = __float_as_uint(amax);
+    const int ef = (int)((b >> 23) & 0xFF);
+    if (ef == 0xFF) return 255;
+    int E;
+    uint32_t mant;
+    if (ef == 0) {                       // subnormal: amax = m * 2^-149
+        const uint32_t m = b & 0x7FFFFF;
+        const int p = 31 - __clz(m);     // leading one
+        E = p - 149;
+        mant = (m << (23 - p)) & 0x7FFFFF;
+    } else {
+        E = ef - 127;
+        mant = b & 0x7FFFFF;
+    }
+    int k = (mant <= 0x600000u) ? E - 8 : E - 7;
+    k = k < -127 ? -127 : (k > 127 ? 127 : k);
+    return k + 127;
+}
+
+// E4M3, round to nearest even, saturating at +-448.
+__device__ __forceinline__ uint8_t e4m3_rn_sat(float v)
+{
+    return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+
+// v quantized to E4M3 under the scale byte s (1 <= s <= 254) and taken back:
+// code(v * 2^(127 - s)) * 2^(s - 127), both scalings exact.
+__device__ __forceinline__ float e4m3_quant_dequant(float v, int s)
+{
+    const float down = __uint_as_float((uint32_t)(254 - s) << 23);     // 2^(127 - s)
+    const __half_raw hr = __nv_cvt_fp8_to_halfraw(e4m3_rn_sat(v * down), __NV_E4M3);
+    const float up = s > 0 ? __uint_as_float((uint32_t)s << 23) : __uint_as_float(0x00400000u);  // 2^(s-127)
+    return __half2float(__half(hr)) * up;
 }
 
 // Smallest e with amax <= 6 * 2^e (the ue8m0 scale of an E2M1 piece),

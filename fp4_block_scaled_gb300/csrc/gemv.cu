@@ -218,6 +218,28 @@ __global__ void __launch_bounds__(256) k_prep(GemvArgs a)
         den = s_den;
     }
     pdl_trigger();
+    if (a.act_e4m3) {
+        // x quantized to E4M3 under one ue8m0 scale per 128 elements (lane l holds
+        // elements 2l, 2l + 1 of each half), and the dequantized values as pieces
+        const int b = blockIdx.y * (blockDim.x >> 5) + warp;  // 128-element block
+        if (b >= H / 128) return;
+        float v[4];
+        for (int hh = 0; hh < 2; hh++)
+            for (int e = 0; e < 2; e++) {
+                const int i = b * 128 + hh * 64 + 2 * lane + e;
+                v[2 * hh + e] = a.x_resid ? __bfloat162float(__float2bfloat16_rn(a.x_resid[(size_t)t * H + i] / den))
+                                          : __uint_as_float((uint32_t)a.x_bf16[(size_t)t * H + i] << 16);
+            }
+        const float amax = warp_max(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+        const int s = ue8m0_for_amax_bits(amax);
+        for (int hh = 0; hh < 2; hh++) {
+            uint8_t* Bunit = a.xq + (size_t)t * act_bytes(H) + (size_t)b * kUnitBBytes;
+            uint8_t* Bsf = a.xsf + (size_t)t * act_sf_bytes(H) + (size_t)b * kUnitSfBytes;
+            write_pieces64(e4m3_quant_dequant(v[2 * hh], s), e4m3_quant_dequant(v[2 * hh + 1], s), lane, Bunit,
+                           Bsf, 2 * hh);
+        }
+        return;
+    }
     const int b = blockIdx.y * (blockDim.x >> 5) + warp;      // 64-element span
     if (b >= H / 64) return;
     const int i = b * 64 + 2 * lane;
@@ -562,16 +584,52 @@ __device__ __forceinline__ void finalize_gate_up(const GemvArgs& a, const Stream
     const float w = slot_weight(a, sm, j);
     const float2 g = *reinterpret_cast<const float2*>(comb + 2 * lane);
     const float2 u = *reinterpret_cast<const float2*>(comb + 64 + 2 * lane);
-    const float h0 = silu(g.x) * u.x * w, h1 = silu(g.y) * u.y * w;
+    float h0 = silu(g.x) * u.x, h1 = silu(g.y) * u.y;
+    int done = 1;                         // tiles of h whose pieces this call writes
+    if (a.act_e4m3) {
+        // h is quantized to E4M3 per 128 along I (tiles 2b, 2b + 1; a last block
+        // of 64 is one tile), before w.  The second tile of a block to finish
+        // quantizes both, from the first one's raw h.
+        const int blk = tile / 2, nblk = (p.ntiles + 1) / 2;
+        const bool pair = (tile | 1) < p.ntiles;
+        float o0 = 0.0f, o1 = 0.0f;
+        if (pair) {
+            float* mine = a.hraw + (size_t)j * a.I + (size_t)tile * 64 + 2 * lane;
+            mine[0] = h0;
+            mine[1] = h1;
+            __threadfence();
+            __syncwarp();
+            int old = 0;
+            if (lane == 0) old = atomicAdd(a.hpair + (size_t)j * nblk + blk, 1);
+            old = __shfl_sync(0xFFFFFFFFu, old, 0);
+            if (old == 0) return;         // the other tile finishes the block
+            __threadfence();
+            const float* other = a.hraw + (size_t)j * a.I + (size_t)(tile ^ 1) * 64 + 2 * lane;
+            o0 = __ldcg(other);
+            o1 = __ldcg(other + 1);
+            if (lane == 0) a.hpair[(size_t)j * nblk + blk] = 0;     // ready for the next launch
+            done = 2;
+        }
+        const float amax = warp_max(fmaxf(fmaxf(fabsf(h0), fabsf(h1)), fmaxf(fabsf(o0), fabsf(o1))));
+        const int s = ue8m0_for_amax_bits(amax);
+        h0 = e4m3_quant_dequant(h0, s);
+        h1 = e4m3_quant_dequant(h1, s);
+        if (pair) {
+            const int ot = tile ^ 1;
+            uint8_t* Bunit = a.hq + (size_t)j * act_bytes(a.I) + (size_t)(ot / 2) * kUnitBBytes;
+            uint8_t* Bsf = a.hsf + (size_t)j * act_sf_bytes(a.I) + (size_t)(ot / 2) * kUnitSfBytes;
+            write_pieces64(e4m3_quant_dequant(o0, s) * w, e4m3_quant_dequant(o1, s) * w, lane, Bunit, Bsf, 2 * ot);
+        }
+    }
     uint8_t* Bunit = a.hq + (size_t)j * act_bytes(a.I) + (size_t)(tile / 2) * kUnitBBytes;
     uint8_t* Bsf = a.hsf + (size_t)j * act_sf_bytes(a.I) + (size_t)(tile / 2) * kUnitSfBytes;
-    write_pieces64(h0, h1, lane, Bunit, Bsf, 2 * tile);
+    write_pieces64(h0 * w, h1 * w, lane, Bunit, Bsf, 2 * tile);
     // the down projection reads these with bulk copies (async proxy), in other CTAs
     asm volatile("fence.proxy.async.global;" ::: "memory");
     __syncwarp();
     if (lane == 0) {
         __threadfence();
-        atomicAdd(a.sync, 1);
+        atomicAdd(a.sync, done);
     }
 }
 
@@ -873,7 +931,7 @@ size_t layer_smem() { return sizeof(TcSmem) > kOneCtaPerSmSmem ? sizeof(TcSmem) 
 
 }  // namespace
 
-GemvWorkspaceSizes gemv_workspace_sizes(int T, int topk, int H, int I, int sms)
+GemvWorkspaceSizes gemv_workspace_sizes(int T, int topk, int H, int I, int sms, bool e4m3)
 {
     GemvWorkspaceSizes s;
     const size_t slots = (size_t)T * topk;
@@ -883,6 +941,8 @@ GemvWorkspaceSizes gemv_workspace_sizes(int T, int topk, int H, int I, int sms)
     s.hsf = slots * act_sf_bytes(I);
     s.part_gu = (size_t)sms * kTileRows;
     s.part_dn = (size_t)sms * kTileRows;
+    s.hraw = e4m3 ? slots * I * sizeof(float) : 0;
+    s.hpair = e4m3 ? slots * (size_t)((I + 127) / 128) * sizeof(int) : 0;
     return s;
 }
 
@@ -902,7 +962,8 @@ cudaError_t launch_gemv_layer(const GemvArgs& a0, cudaStream_t s, bool pdl, Prof
     {
         void* args[] = {&a};
         if (prof) prof->begin(kPhasePrep, s);
-        err = launch_ex((const void*)k_prep, dim3(a.T, (a.H / 64 + 7) / 8), dim3(256), 0, s, pdl && !prof, args);
+        const int spans = a.act_e4m3 ? a.H / 128 : a.H / 64;      // one warp each
+        err = launch_ex((const void*)k_prep, dim3(a.T, (spans + 7) / 8), dim3(256), 0, s, pdl && !prof, args);
         if (prof) prof->end(s);
         if (err != cudaSuccess) return err;
     }

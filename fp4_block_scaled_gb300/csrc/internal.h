@@ -35,6 +35,10 @@ struct GemvArgs {
     // projection: entries are (fp32 bits | tag << 32), the tag naming the launch
     uint64_t* part_gu;                  // [sms][128]
     uint64_t* part_dn;                  // [sms][128]
+    // E4M3 activation mode (x and h quantized to E4M3, one ue8m0 scale per 128)
+    int act_e4m3;
+    float* hraw;                        // [T*k][I] h before quantization
+    int* hpair;                         // [T*k][ceil(I/128)] tiles of each 128-block of h done
     int* sync;                          // [3]: gate/up groups finished, CTAs finished (both
                                         // zero between launches: the last CTA resets them),
                                         // launches so far (the partials' tag)
@@ -48,9 +52,10 @@ struct GemvArgs {
 // entry counts for part_* (uint64); the sync words are kGemvSyncInts ints.
 struct GemvWorkspaceSizes {
     size_t xq, xsf, hq, hsf, part_gu, part_dn;
+    size_t hraw, hpair;                 // bytes, E4M3 activation mode only
 };
 constexpr int kGemvSyncInts = 3;
-GemvWorkspaceSizes gemv_workspace_sizes(int T, int topk, int H, int I, int sms);
+GemvWorkspaceSizes gemv_workspace_sizes(int T, int topk, int H, int I, int sms, bool e4m3);
 cudaError_t gemv_init_device();   // per device, before the first launch
 size_t gemv_stream_smem();
 

@@ -105,7 +105,7 @@ extern "C" int moe_ffn_forward_noalloc(const moe_ffn_config* cfg, int device, co
     // carve the scratch: status and counters first (cleared every call, except
     // the launch count that tags the partial sums), then the rest
     const int H = cfg->hidden, I = cfg->inter, k = cfg->topk;
-    const GemvWorkspaceSizes g = gemv_workspace_sizes(T, k, H, I, d->sms);
+    const GemvWorkspaceSizes g = gemv_workspace_sizes(T, k, H, I, d->sms, false);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t o = off;

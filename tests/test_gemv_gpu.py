@@ -24,9 +24,10 @@ def _cuda():
 
 
 class Layer:
-    def __init__(self, E, H, I, k, max_tokens=8, out=moe.MOE_OUT_F32, seed=0, layer=0):
+    def __init__(self, E, H, I, k, max_tokens=8, out=moe.MOE_OUT_F32, seed=0, layer=0, act=moe.MOE_ACT_BF16):
         self.E, self.H, self.I, self.k = E, H, I, k
-        self.cfg = moe.config(E, H, I, k, max_tokens, out_dtype=out)
+        self.act = act
+        self.cfg = moe.config(E, H, I, k, max_tokens, out_dtype=out, act_mode=act)
         self.h = moe.moe_ffn_create(self.cfg, 0)
         self.es = fill_layer(self.h, self.cfg, layer=layer, seed=seed)
         self.seed, self.layer = seed, layer
@@ -46,7 +47,8 @@ class Layer:
     def oracle(self, x_bits, idx, w):
         codes, scales = host_experts(self.H, self.I, idx.reshape(-1), layer=self.layer,
                                      seed=self.seed, E=self.E)
-        return oracle.moe_ffn(codes, scales, self.H, self.I, x_bits, idx, w, nthreads=8)
+        act = oracle.ACT_E4M3_UE8M0_128 if self.act == moe.MOE_ACT_E4M3_UE8M0_128 else oracle.ACT_BF16
+        return oracle.moe_ffn(codes, scales, self.H, self.I, x_bits, idx, w, act_mode=act, nthreads=8)
 
     def close(self):
         moe.moe_ffn_destroy(self.h)
@@ -280,3 +282,43 @@ def test_stack_matches_oracle():
             assert_close(x.cpu().numpy(), ref2, f"stack replay T={T}")
         finally:
             moe.moe_ffn_destroy(h)
+
+
+# ---- E4M3 activation mode: x and h quantized to E4M3 with one ue8m0 scale per
+# 128 (the batch configurations' numerics).  The oracle quantizes fp64 h, the
+# GPU fp32 h, so an element may round to the other neighbour of the E4M3 grid;
+# the shapes here keep the result inside the float tolerance.
+
+@pytest.mark.parametrize("T", [1, 3])
+def test_tiny_layer_e4m3_matches_oracle(T):
+    L = Layer(**TINY, act=moe.MOE_ACT_E4M3_UE8M0_128)
+    try:
+        x, idx, w = inputs(T, TINY["E"], TINY["H"], TINY["k"], seed=20 + T)
+        assert_close(L.run(x, idx, w).cpu().numpy(), L.oracle(x, idx, w), f"tiny e4m3 T={T}")
+    finally:
+        L.close()
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_mid_layer_e4m3_odd_h_block_matches_oracle(T):
+    """I = 448: h has three 128-blocks and a last block of 64 (one tile)."""
+    L = Layer(**MID, act=moe.MOE_ACT_E4M3_UE8M0_128)
+    try:
+        x, idx, w = inputs(T, MID["E"], MID["H"], MID["k"], seed=30 + T)
+        assert_close(L.run(x, idx, w).cpu().numpy(), L.oracle(x, idx, w), f"mid e4m3 T={T}")
+    finally:
+        L.close()
+
+
+def test_full_size_layer_batch64_e4m3_matches_oracle():
+    """384 experts, H=4096, I=2880, top-6, 64 tokens, uniform routing."""
+    T = 64
+    L = Layer(E=384, H=4096, I=2880, k=6, max_tokens=T, act=moe.MOE_ACT_E4M3_UE8M0_128)
+    try:
+        x, idx, w = inputs(T, 384, 4096, 6, seed=3)
+        y = L.run(x, idx, w).cpu().numpy()
+        assert_close(y, L.oracle(x, idx, w), "full-size e4m3 T=64")
+        y2 = L.run(x, idx, w).cpu().numpy()
+        assert np.array_equal(y, y2)              # deterministic
+    finally:
+        L.close()
