@@ -7,9 +7,15 @@ pre-drawn so that consecutive steps share no expert (every step streams its 6
 experts, 112.8 MB, from HBM: inputs far larger than L2).  Steps are replayed
 from CUDA graphs of up to 500 calls.
 
-One JSON line on rank 0.  `value` is tokens/s of the layer summed over ranks
-(each rank an independent replica: "scaling": "weak").  `--impl reference`
-times the CPU oracle instead (on this host's cores).
+Other workloads (`--workload`): the same layer at batch 64 (uniform routing)
+and 512 (Zipf expert popularity) with E4M3 activations, and a 40-layer stack
+of 128-expert layers (residual + RMSNorm per layer, one CUDA graph per step)
+at batch 1 and 32.
+
+One JSON line on rank 0.  `value` is tokens/s of the layer (or of the whole
+stack) summed over ranks (each rank an independent replica: "scaling":
+"weak").  `--impl reference` times the CPU oracle instead (on this host's
+cores).
 """
 from __future__ import annotations
 
@@ -28,10 +34,19 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOADS = {
-    "layer_b1": dict(E=384, H=4096, I=2880, k=6, T=1),
+    # one MoE layer, decode batch 1 (the default: the headline workload)
+    "layer_b1": dict(E=384, H=4096, I=2880, k=6, T=1, L=1, act="bf16", dist="uniform", steps=20000),
     # same step (6 experts streamed per token) with 64 resident experts (1.2 GB,
     # still far above L2): the size used for ncu captures
-    "layer_b1_e64": dict(E=64, H=4096, I=2880, k=6, T=1),
+    "layer_b1_e64": dict(E=64, H=4096, I=2880, k=6, T=1, L=1, act="bf16", dist="uniform", steps=20000),
+    # the 384-expert layer at decode batch 64 (uniform) and 512 (Zipf 1.1 expert
+    # popularity), activations quantized to E4M3 with ue8m0 per 128
+    "layer_b64": dict(E=384, H=4096, I=2880, k=6, T=64, L=1, act="e4m3", dist="uniform", steps=1000),
+    "layer_b512": dict(E=384, H=4096, I=2880, k=6, T=512, L=1, act="e4m3", dist="zipf", steps=100),
+    # 40-layer stack of 128-expert layers (96 GB resident), residual + RMSNorm,
+    # the whole step as one CUDA graph, at batch 1 and 32
+    "stack_b1": dict(E=128, H=4096, I=2880, k=6, T=1, L=40, act="bf16", dist="uniform", steps=500),
+    "stack_b32": dict(E=128, H=4096, I=2880, k=6, T=32, L=40, act="bf16", dist="uniform", steps=50),
 }
 METRIC = "MoE expert-FFN decode tokens/s per layer-stack & HBM GB/s (% of GB300 roofline)"
 FALLBACK_HBM_GBS = 6800.0
@@ -108,7 +123,9 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def draw_routings(R, E, k, T, seed):
+def draw_routings(R, E, k, T, seed, dist="uniform", layer=0):
+    """R pre-drawn routings of T tokens.  At batch 1 consecutive ones share no
+    expert, so every step streams its experts from HBM."""
     import numpy as np
 
     import synth
@@ -116,11 +133,14 @@ def draw_routings(R, E, k, T, seed):
     idx = np.zeros((R, T, k), np.int32)
     prev = None
     for r in range(R):
-        cur = synth.routing_uniform(T, E, k, seed=seed, stream=synth.S_ROUTE + 1000 * (r + 1),
-                                    avoid=prev)
+        st = synth.S_ROUTE + 1000 * (r + 1) + 7 * layer
+        if dist == "zipf":
+            cur = synth.routing_zipf(T, E, k, s=1.1, seed=seed, stream=st)
+        else:
+            cur = synth.routing_uniform(T, E, k, seed=seed, stream=st, avoid=prev if T == 1 else None)
         idx[r] = cur
         prev = set(int(v) for v in cur.reshape(-1))
-    w = np.stack([synth.routing_weights(T, k, seed=seed, stream=synth.S_LOGIT + 1000 * (r + 1))
+    w = np.stack([synth.routing_weights(T, k, seed=seed, stream=synth.S_LOGIT + 1000 * (r + 1) + 7 * layer)
                   for r in range(R)])
     return idx, w
 
@@ -145,33 +165,53 @@ def traffic_record(kernel):
 
 # --------------------------------------------------------------- CPU oracle
 
-def cpu_sample(wl, budget_s=12.0, seed=0):
-    """The oracle, as it stands, on whole tokens of the workload until the
-    budget is used (at least one token).  Returns (tokens/s, threads, sample)."""
-    import numpy as np
-
+def _act_mode(wl):
     import oracle
+
+    return oracle.ACT_E4M3_UE8M0_128 if wl["act"] == "e4m3" else oracle.ACT_BF16
+
+
+def _oracle_token(wl, n, seed):
+    """Inputs of the n-th sampled (token, layer) of the workload: the oracle's
+    cost is per token and layer, so whole tokens of single layers are the unit
+    of every CPU sample (a stack token costs L of them)."""
     import synth
 
-    E, H, I, k = wl["E"], wl["H"], wl["I"], wl["k"]
-    n = cores()
-    threads = min(n, k)
+    E, H, I, k, L = wl["E"], wl["H"], wl["I"], wl["k"], wl["L"]
+    layer = n % L
+    if wl["dist"] == "zipf":
+        idx = synth.routing_zipf(1, E, k, s=1.1, seed=seed + 17, stream=synth.S_ROUTE + 7 * n)
+    else:
+        idx = synth.routing_uniform(1, E, k, seed=seed + 17, stream=synth.S_ROUTE + 7 * n)
+    w = synth.routing_weights(1, k, seed=seed + 17, stream=synth.S_LOGIT + 7 * n)
+    x = synth.activations_bf16(1, H, seed=seed + 17, n0=H * n)
+    codes, scales = [None] * E, [None] * E
+    for e in set(int(v) for v in idx.reshape(-1)):
+        codes[e], scales[e] = synth.expert_canonical(H, I, e, layer=layer)
+    return codes, scales, x, idx, w
+
+
+def cpu_sample(wl, budget_s=12.0, seed=0):
+    """The oracle, as it stands, on whole tokens of single layers of the
+    workload until the budget is used (at least one).  Returns (tokens/s of the
+    workload, threads, sample)."""
+    import oracle
+
+    E, H, I, k, L = wl["E"], wl["H"], wl["I"], wl["k"], wl["L"]
+    act = _act_mode(wl)
+    threads = min(cores(), k)
     done, spent = 0, 0.0
-    t_tok = []
     while spent < budget_s and done < 64:
-        idx = synth.routing_uniform(1, E, k, seed=seed + 17, stream=synth.S_ROUTE + 7 * done)
-        w = synth.routing_weights(1, k, seed=seed + 17, stream=synth.S_LOGIT + 7 * done)
-        x = synth.activations_bf16(1, H, seed=seed + 17, n0=H * done)
-        codes, scales = [None] * E, [None] * E
-        for e in set(int(v) for v in idx.reshape(-1)):
-            codes[e], scales[e] = synth.expert_canonical(H, I, e)
+        codes, scales, x, idx, w = _oracle_token(wl, done, seed)
         t0 = time.perf_counter()
-        oracle.moe_ffn(codes, scales, H, I, x, idx, w, nthreads=threads)
-        dt = time.perf_counter() - t0
-        t_tok.append(dt)
-        spent += dt
+        oracle.moe_ffn(codes, scales, H, I, x, idx, w, act_mode=act, nthreads=threads)
+        spent += time.perf_counter() - t0
         done += 1
-    return done / spent, threads, f"{done} whole tokens of the layer (top-{k} of {E}, H={H}, I={I}), fp64 oracle, {threads} threads over slots"
+    per_layer = done / spent
+    what = f"{done} whole tokens of one layer (top-{k} of {E}, H={H}, I={I}, {wl['act']} activations, {wl['dist']} routing)"
+    if L > 1:
+        what += f", scaled to the {L}-layer stack as 1/{L} of the per-layer rate"
+    return per_layer / L, threads, what + f", fp64 oracle, {threads} threads over slots"
 
 
 def run_reference(args, wl):
@@ -184,25 +224,22 @@ def run_reference(args, wl):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    E, H, I, k = wl["E"], wl["H"], wl["I"], wl["k"]
+    E, H, I, k, L = wl["E"], wl["H"], wl["I"], wl["k"], wl["L"]
+    act = _act_mode(wl)
     threads = min(cores(), k)
     per_token_weights = k * 3 * H * I
-    # calibrate one token
-    idx = synth.routing_uniform(1, E, k, seed=3)
-    w = synth.routing_weights(1, k, seed=3)
-    x = synth.activations_bf16(1, H, seed=3)
-    codes, scales = [None] * E, [None] * E
-    used = set(int(v) for v in idx.reshape(-1))
-    for e in used:
-        codes[e], scales[e] = synth.expert_canonical(H, I, e)
+    # calibrate one token of one layer
+    codes, scales, x, idx, w = _oracle_token(wl, 0, 3)
+    used = sorted(set(int(v) for v in idx.reshape(-1)))
     t0 = time.perf_counter()
-    oracle.moe_ffn(codes, scales, H, I, x, idx, w, nthreads=threads)
+    oracle.moe_ffn(codes, scales, H, I, x, idx, w, act_mode=act, nthreads=threads)
     t_token = time.perf_counter() - t0
     budget = 90.0
     nsteps = args.steps + args.warmup
     if nsteps * t_token <= budget:
         mode, rows = "token", None
-        sample = f"one whole token per step (top-{k} of {E}, H={H}, I={I}), {threads} threads"
+        sample = (f"one whole token of one layer per step (top-{k} of {E}, H={H}, I={I}, "
+                  f"{wl['act']} activations), {threads} threads")
     else:
         mode = "rows"
         # rows of one gate matrix per step, single thread, sized to the budget
@@ -211,13 +248,14 @@ def run_reference(args, wl):
         threads = 1
         sample = (f"{rows} gate rows (K={H}) of one expert per step, 1 thread, scaled to "
                   f"tokens by weights processed")
-    e0 = sorted(used)[0]
-    gc = I * H // 2
+    if L > 1:
+        sample += f"; a stack token costs {L} layer-tokens, the rate is divided by {L}"
+    e0 = used[0]
     xr = synth.bf16_bits_to_f32(x[0]).astype(np.float64)
 
     def step():
         if mode == "token":
-            oracle.moe_ffn(codes, scales, H, I, x, idx, w, nthreads=threads)
+            oracle.moe_ffn(codes, scales, H, I, x, idx, w, act_mode=act, nthreads=threads)
         else:
             oracle.matvec(codes[e0][:rows * H // 2], scales[e0][:rows * H // 32], rows, H, xr)
 
@@ -228,17 +266,18 @@ def run_reference(args, wl):
         step()
     dt = time.perf_counter() - t0
     if mode == "token":
-        value = args.steps / dt
+        value = args.steps / dt / L
     else:
-        value = args.steps * rows * H / dt / per_token_weights
+        value = args.steps * rows * H / dt / per_token_weights / L
     ms = dt * 1000.0 / args.steps
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.workload, "experts": E, "hidden": H, "inter": I, "topk": k,
-                   "tokens_per_step": 1, "l2": "cpu run"},
+        "config": {"workload": args.workload, "layers": L, "experts": E, "hidden": H, "inter": I,
+                   "topk": k, "tokens_per_step": wl["T"], "routing": wl["dist"],
+                   "activations": wl["act"], "l2": "cpu run"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -267,45 +306,75 @@ def run_ours(args, wl):
 
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    E, H, I, k, T = wl["E"], wl["H"], wl["I"], wl["k"], wl["T"]
-    cfg = moe.config(E, H, I, k, T, out_dtype=moe.MOE_OUT_F32)
+    E, H, I, k, T, L = wl["E"], wl["H"], wl["I"], wl["k"], wl["T"], wl["L"]
+    act = moe.MOE_ACT_E4M3_UE8M0_128 if wl["act"] == "e4m3" else moe.MOE_ACT_BF16
+    cfg = moe.config(E, H, I, k, T, act_mode=act, out_dtype=moe.MOE_OUT_F32)
     h = moe.moe_ffn_create(cfg, local)
-    es = ExpertSet(h, cfg, device=local)
     nc, ns = synth.expert_sizes(H, I)
     tc = torch.empty(nc, dtype=torch.uint8, device="cuda")
     ts = torch.empty(ns, dtype=torch.uint8, device="cuda")
-    for e in range(E):
-        synth.device_fill_expert(tc.data_ptr(), ts.data_ptr(), H, I, e, seed=0)
-        es.load(e, tc, ts)
+    sets = []
+    for l in range(L):
+        es = ExpertSet(h, cfg, device=local)
+        for e in range(E):
+            synth.device_fill_expert(tc.data_ptr(), ts.data_ptr(), H, I, e, layer=l, seed=0)
+            es.load(e, tc, ts)
+        sets.append(es)
     torch.cuda.synchronize()
     del tc, ts
 
-    R = 500
-    idx_np, w_np = draw_routings(R, E, k, T, seed=rank)
+    # pre-drawn routings and inputs: R steps (x L layers)
+    R = min(500, max(4, 2048 // T)) if L == 1 else 4
+    draws = [draw_routings(R, E, k, T, seed=rank, dist=wl["dist"], layer=l) for l in range(L)]
+    idx_np = np.stack([d[0] for d in draws], axis=1)          # [R][L][T][k]
+    w_np = np.stack([d[1] for d in draws], axis=1)
     x_np = synth.activations_bf16(R * T, H, seed=rank).reshape(R, T, H)
     idx_d = torch.from_numpy(idx_np).cuda()
     w_d = torch.from_numpy(w_np).cuda()
     x_d = torch.from_numpy(x_np.view(np.int16)).cuda()
-    y_d = torch.empty((R, T, H), dtype=torch.float32, device="cuda")
     stream = torch.cuda.Stream()
-
-    def fwd(i, s):
-        moe.moe_ffn_forward(h, x_d[i], idx_d[i], w_d[i], es.table, y_d[i], T, s)
-
-    def capture(n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
-                fwd(i % R, torch.cuda.current_stream())
-        return g
-
     K, W = args.steps, args.warmup
-    chunk = min(K, R)
-    g_full = capture(chunk)
-    rem = K % chunk
-    g_rem = capture(rem) if rem else None
+    if L == 1:
+        y_d = torch.empty((R, T, H), dtype=torch.float32, device="cuda")
+
+        def fwd(i, s):
+            moe.moe_ffn_forward(h, x_d[i], idx_d[i, 0], w_d[i, 0], sets[0].table, y_d[i], T, s)
+
+        def capture(n):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    fwd(i % R, torch.cuda.current_stream())
+            return g
+
+        chunk = min(K, R)
+        g_full = capture(chunk)
+        rem = K % chunk
+        g_rem = capture(rem) if rem else None
+
+        def timed_steps():
+            for _ in range(K // chunk):
+                g_full.replay()
+            if g_rem is not None:
+                g_rem.replay()
+    else:
+        # the residual: each step starts again from the step's own input
+        x0 = x_d.view(torch.bfloat16).float()                  # [R][T][H]
+        xs = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        tables = [es.table for es in sets]
+
+        def fwd(i, s):
+            xs.copy_(x0[i])
+            moe.moe_stack_forward(h, xs, tables, idx_d[i], w_d[i], L, T, s)
+
+        chunk = None
+
+        def timed_steps():
+            for i in range(K):
+                fwd(i % R, stream)
+
     with torch.cuda.stream(stream):
-        for i in range(W):
+        for i in range(max(W, R if L > 1 else 0)):       # the stack captures one graph per routing
             fwd(i % R, stream)
     stream.synchronize()
 
@@ -322,10 +391,7 @@ def run_ours(args, wl):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        for _ in range(K // chunk):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
+        timed_steps()
         ev1.record(stream)
     stream.synchronize()
     clocks = sampler.stop()
@@ -338,40 +404,65 @@ def run_ours(args, wl):
     ms_step = ms_total / K
     value = world * T * K / (ms_total / 1000.0)
 
-    # algorithmic bytes: distinct experts per step x bytes per expert + activations
-    distinct = [len(set(int(v) for v in idx_np[i % R].reshape(-1))) for i in range(K)]
+    # algorithmic bytes: distinct experts per layer per step x bytes per expert + activations
+    def distinct(i, l):
+        return len(set(int(v) for v in idx_np[i % R, l].reshape(-1)))
+
     act_io = T * H * 2 + T * H * 4 + 2 * T * k * 4
-    bytes_step = sum(distinct) / K * expert_bytes(H, I) + act_io
+    bytes_step = sum(distinct(i, l) for i in range(K) for l in range(L)) / K * expert_bytes(H, I) + L * act_io
     gbs_step = bytes_step / (ms_step / 1000.0) / 1e9
 
-    # ---- dominant kernel (k_layer: both projections) timed with CUDA events on its stream
+    # ---- dominant kernel (k_layer: both projections) timed with CUDA events on its
+    # stream: single-layer forwards (layer 0 of the workload) in profiling mode
     peak, peak_kind = peaks()
+    yp = torch.empty((T, H), dtype=torch.float32, device="cuda")
     moe.moe_ffn_profile_enable(h, True)
-    nprof = min(K, 2000)
+    nprof = min(K * L, 2000 if T == 1 else 50)
     with torch.cuda.stream(stream):
         for i in range(nprof):
-            fwd(i % R, stream)
+            moe.moe_ffn_forward(h, x_d[i % R], idx_d[i % R, 0], w_d[i % R, 0], sets[0].table, yp, T, stream)
     stream.synchronize()
     ms_ph, n_ph = moe.moe_ffn_profile_read(h)
     moe.moe_ffn_profile_enable(h, False)
     ly_ms = ms_ph[moe.MOE_PHASE_GATE_UP] / max(1, n_ph[moe.MOE_PHASE_GATE_UP])
     pr_ms = ms_ph[moe.MOE_PHASE_PREP] / max(1, n_ph[moe.MOE_PHASE_PREP])
-    ly_dist = sum(len(set(int(v) for v in idx_np[i % R].reshape(-1))) for i in range(nprof)) / nprof
-    ly_bytes = ly_dist * expert_bytes(H, I) + act_io
+    ly_bytes = sum(distinct(i, 0) for i in range(nprof)) / nprof * expert_bytes(H, I) + act_io
     achieved = ly_bytes / (ly_ms / 1000.0) / 1e9
-    traffic = traffic_record("k_layer")
+    traffic = traffic_record("k_layer") if args.workload in ("layer_b1", "layer_b1_e64") else None
 
-    # ---- end to end through the host-buffer entry point (copies in the timed region)
-    ne2e = min(K, 2000)
+    # ---- end to end through the public API from host buffers: every step copies
+    # its inputs in from pinned host memory and its result back
+    ne2e = min(K, 2000 if T * L == 1 else 20)
     xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
     ih = torch.from_numpy(idx_np).pin_memory()
     wh = torch.from_numpy(w_np).pin_memory()
     yh = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    if L == 1:
+        def e2e_step(i):
+            moe.moe_ffn_forward_host(h, xh[i], ih[i, 0], wh[i, 0], sets[0].table, yh, T, stream)
+        h2d = T * H * 2 + 2 * T * k * 4
+    else:
+        xin = torch.empty((T, H), dtype=torch.int16, device="cuda")
+        idev = torch.empty((L, T, k), dtype=torch.int32, device="cuda")
+        wdev = torch.empty((L, T, k), dtype=torch.float32, device="cuda")
+        xf = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        tables = [es.table for es in sets]
+
+        def e2e_step(i):
+            with torch.cuda.stream(stream):
+                xin.copy_(xh[i], non_blocking=True)
+                idev.copy_(ih[i], non_blocking=True)
+                wdev.copy_(wh[i], non_blocking=True)
+                xf.copy_(xin.view(torch.bfloat16))
+                moe.moe_stack_forward(h, xf, tables, idev, wdev, L, T, stream)
+                yh.copy_(xf, non_blocking=True)
+            stream.synchronize()
+        h2d = T * H * 2 + 2 * L * T * k * 4
     for i in range(3):
-        moe.moe_ffn_forward_host(h, xh[i], ih[i], wh[i], es.table, yh, T, stream)
+        e2e_step(i % R)
     t0 = time.perf_counter()
     for i in range(ne2e):
-        moe.moe_ffn_forward_host(h, xh[i % R], ih[i % R], wh[i % R], es.table, yh, T, stream)
+        e2e_step(i % R)
     e2e_s = time.perf_counter() - t0
     e2e_value = world * T * ne2e / e2e_s
     status = moe.moe_ffn_status(h, stream)
@@ -383,14 +474,19 @@ def run_ours(args, wl):
         cpu = {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle", "sample": sample}
 
     if rank == 0:
+        resident = L * E * expert_bytes(H, I) / 1e9
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f16xe2m1->f32", "data": "synthetic",
-            "config": {"workload": args.workload, "experts": E, "hidden": H, "inter": I, "topk": k,
-                       "tokens_per_step": T, "parallelism": f"replicas{world}",
-                       "l2": "inputs larger than L2: 7.2 GB resident experts, consecutive steps "
-                             "share no expert", "graph_chunk": chunk},
+            "vs_baseline": None,
+            "dtype": "e4m3xe2m1->f32" if wl["act"] == "e4m3" else "f16xe2m1->f32",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "layers": L, "experts": E, "hidden": H, "inter": I,
+                       "topk": k, "tokens_per_step": T, "routing": wl["dist"], "activations": wl["act"],
+                       "parallelism": f"replicas{world}",
+                       "l2": f"inputs larger than L2: {resident:.1f} GB resident experts"
+                             + (", consecutive steps share no expert" if T == 1 and L == 1 else ""),
+                       "graph_chunk": chunk},
             "hbm_gbs": gbs_step, "hbm_frac": gbs_step / peak,
             "bytes_per_step": bytes_step,
             "phase_us": {"prep": pr_ms * 1e3, "layer": ly_ms * 1e3},
@@ -399,10 +495,9 @@ def run_ours(args, wl):
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes_per_launch": ly_bytes},
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "tokens/s",
-                    "h2d_bytes_per_step": T * H * 2 + 2 * T * k * 4,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": T * H * 4},
-            "gpu_launches": 2 * K,
+            "gpu_launches": 2 * K * L,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -414,15 +509,19 @@ def run_ours(args, wl):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default: per workload)")
+    ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="layer_b1")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
     args = ap.parse_args()
+    wl = WORKLOADS[args.workload]
+    if args.steps is None:
+        args.steps = wl["steps"] if args.impl == "ours" else 10
+    if args.warmup is None:
+        args.warmup = 50 if args.impl == "ours" else 3
     if args.warmup < 3:
         args.warmup = 3
-    wl = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, wl)
     else:
