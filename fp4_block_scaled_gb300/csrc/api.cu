@@ -31,7 +31,9 @@ struct moe_ffn {
     int sms;
     void* ws;
     size_t ws_bytes;
-    GemvArgs base;              // workspace pointers, problem sizes
+    GemvArgs base;              // workspace pointers, problem sizes (slot-major path)
+    GroupArgs gbase;            // the same for the expert-major path
+    int gemm_min_tokens;        // T >= this takes the expert-major path
     int* status;
     uint16_t* x_stage;          // staging for moe_ffn_forward_host
     int32_t* idx_stage;
@@ -109,14 +111,42 @@ int check_forward(const moe_ffn* h, const void* x, const int32_t* idx, const flo
     return MOE_OK;
 }
 
+GroupArgs group_args(const moe_ffn* h, int T, const int32_t* idx, const float* w,
+                     const moe_expert_table* tbl)
+{
+    GroupArgs a = h->gbase;
+    a.T = T;
+    a.idx = idx;
+    a.w = w;
+    a.codes = tbl->codes;
+    a.scales = tbl->scales;
+    return a;
+}
+
+// One layer, on the path the config selects for T tokens: x_bf16 -> y, or
+// (x_bf16 == nullptr) the residual x_resid += moe(rmsnorm(x_resid)).
+cudaError_t launch_layer(const moe_ffn* h, const uint16_t* x_bf16, float* x_resid, const int32_t* idx,
+                         const float* w, const moe_expert_table* tbl, void* y, int T, cudaStream_t s,
+                         Profiler* prof)
+{
+    if (T >= h->gemm_min_tokens) {
+        GroupArgs a = group_args(h, T, idx, w, tbl);
+        a.x_bf16 = x_bf16;
+        a.x_resid = x_resid;
+        a.y = y;
+        return launch_group_layer(a, s, true, prof);
+    }
+    GemvArgs a = layer_args(h, T, idx, w, tbl);
+    a.x_bf16 = x_bf16;
+    a.x_resid = x_resid;
+    a.y = y;
+    return launch_gemv_layer(a, s, true, prof);
+}
+
 int run_forward(moe_ffn* h, const void* x, const int32_t* idx, const float* w,
                 const moe_expert_table* tbl, void* y, int T, cudaStream_t s)
 {
-    GemvArgs a = layer_args(h, T, idx, w, tbl);
-    a.x_bf16 = (const uint16_t*)x;
-    a.x_resid = nullptr;
-    a.y = y;
-    return cuda_rc(launch_gemv_layer(a, s, true, h->prof));
+    return cuda_rc(launch_layer(h, (const uint16_t*)x, nullptr, idx, w, tbl, y, T, s, h->prof));
 }
 
 }  // namespace
@@ -153,7 +183,8 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     h->cfg = *cfg;
     h->device = device;
     if (cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
-        gemv_init_device() != cudaSuccess || route_init_device() != cudaSuccess) {
+        gemv_init_device() != cudaSuccess || route_init_device() != cudaSuccess ||
+        group_init_device() != cudaSuccess) {
         delete h;
         return MOE_ERR_CUDA;
     }
@@ -161,6 +192,10 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     const int H = cfg->hidden, I = cfg->inter, k = cfg->topk;
     const bool e4m3 = cfg->act_mode == MOE_ACT_E4M3_UE8M0_128;
     GemvWorkspaceSizes g = gemv_workspace_sizes(T, k, H, I, h->sms, e4m3);
+    h->gemm_min_tokens = cfg->gemm_min_tokens > 0 ? cfg->gemm_min_tokens : kDefaultGemmMinTokens;
+    const bool grouped = T >= h->gemm_min_tokens;      // the expert-major path can be taken
+    GroupWorkspaceSizes gw{};
+    if (grouped) gw = group_workspace_sizes(T, k, cfg->num_experts, H, I, h->sms, e4m3);
 
     // one allocation, carved into aligned pieces
     size_t off = 0;
@@ -173,6 +208,12 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     size_t o_xq = take(g.xq), o_xsf = take(g.xsf), o_hq = take(g.hq), o_hsf = take(g.hsf);
     size_t o_pgu = take(g.part_gu * 8), o_pdn = take(g.part_dn * 8);
     size_t o_hraw = take(g.hraw), o_hpair = take(g.hpair);
+    size_t o_gsync = take(kGemvSyncInts * sizeof(int));
+    size_t o_gcnt = take(gw.counts), o_goff = take(gw.offsets), o_gperm = take(gw.perm);
+    size_t o_ginv = take(gw.inv), o_gbase = take(gw.gbase), o_ggrp = take(gw.groups);
+    size_t o_gxg = take(gw.xg), o_gxgsf = take(gw.xgsf), o_ghg = take(gw.hg), o_ghgsf = take(gw.hgsf);
+    size_t o_gobuf = take(gw.obuf), o_gpgu = take(gw.part_gu), o_gpdn = take(gw.part_dn);
+    size_t o_ghraw = take(gw.hraw), o_ghpair = take(gw.hpair);
     size_t o_xst = take((size_t)T * H * 2), o_ist = take((size_t)T * k * 4);
     size_t o_wst = take((size_t)T * k * 4), o_yst = take((size_t)T * H * 4);
     h->ws_bytes = off;
@@ -209,6 +250,35 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     a.act_e4m3 = e4m3;
     a.hraw = e4m3 ? (float*)(b + o_hraw) : nullptr;
     a.hpair = e4m3 ? (int*)(b + o_hpair) : nullptr;
+    GroupArgs& ga = h->gbase;
+    memset(&ga, 0, sizeof(ga));
+    ga.topk = k;
+    ga.E = cfg->num_experts;
+    ga.H = H;
+    ga.I = I;
+    ga.sms = h->sms;
+    ga.eps = 1e-6f;
+    ga.status = h->status;
+    ga.out_f32 = a.out_f32;
+    ga.act_e4m3 = e4m3;
+    if (grouped) {
+        ga.sync = (int*)(b + o_gsync);
+        ga.counts = (int32_t*)(b + o_gcnt);
+        ga.offsets = (int32_t*)(b + o_goff);
+        ga.perm = (int32_t*)(b + o_gperm);
+        ga.inv = (int32_t*)(b + o_ginv);
+        ga.gbase = (int32_t*)(b + o_gbase);
+        ga.groups = (GroupInfo*)(b + o_ggrp);
+        ga.xg = (uint8_t*)(b + o_gxg);
+        ga.xgsf = (uint8_t*)(b + o_gxgsf);
+        ga.hg = (uint8_t*)(b + o_ghg);
+        ga.hgsf = (uint8_t*)(b + o_ghgsf);
+        ga.obuf = (float*)(b + o_gobuf);
+        ga.part_gu = (uint64_t*)(b + o_gpgu);
+        ga.part_dn = (uint64_t*)(b + o_gpdn);
+        ga.hraw = e4m3 ? (float*)(b + o_ghraw) : nullptr;
+        ga.hpair = e4m3 ? (int*)(b + o_ghpair) : nullptr;
+    }
     h->x_stage = (uint16_t*)(b + o_xst);
     h->idx_stage = (int32_t*)(b + o_ist);
     h->w_stage = (float*)(b + o_wst);
@@ -281,7 +351,7 @@ int moe_ffn_route(moe_ffn_t h, const int32_t* topk_idx, int T, int32_t* counts, 
         return MOE_ERR_INVALID_ARG;
     if (h->cfg.num_experts > route_max_experts()) return MOE_ERR_UNSUPPORTED;
     DeviceGuard guard(h->device);
-    RouteArgs a{topk_idx, T * h->cfg.topk, h->cfg.num_experts, counts, offsets, perm, inv, h->status};
+    RouteArgs a{topk_idx, T * h->cfg.topk, h->cfg.num_experts, counts, offsets, perm, inv, h->status, nullptr, nullptr};
     cudaStream_t s = (cudaStream_t)stream;
     if (h->prof) h->prof->begin(kPhaseRoute, s);
     cudaError_t e = launch_route(a, s);
@@ -334,14 +404,10 @@ int moe_stack_forward(moe_ffn_t h, float* x, const moe_expert_table* tbls,
     cudaError_t e = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     cudaError_t le = cudaSuccess;
-    for (int l = 0; l < L && le == cudaSuccess; l++) {
-        GemvArgs a = layer_args(h, T, topk_idx + (size_t)l * T * h->cfg.topk,
-                                topk_w + (size_t)l * T * h->cfg.topk, &tbls[l]);
-        a.x_bf16 = nullptr;
-        a.x_resid = x;
-        a.y = nullptr;
-        le = launch_gemv_layer(a, h->cap_stream, true, nullptr);
-    }
+    for (int l = 0; l < L && le == cudaSuccess; l++)
+        le = launch_layer(h, nullptr, x, topk_idx + (size_t)l * T * h->cfg.topk,
+                          topk_w + (size_t)l * T * h->cfg.topk, &tbls[l], nullptr, T, h->cap_stream,
+                          nullptr);
     e = cudaStreamEndCapture(h->cap_stream, &graph);
     if (le != cudaSuccess || e != cudaSuccess) {
         if (graph) cudaGraphDestroy(graph);

@@ -1,0 +1,997 @@
+// group.cu -- expert-major ("grouped") path of one routed FP4 MoE layer, for
+// decode batches in which tokens share experts.
+//
+// Four launches per layer, chained with programmatic dependent launch (PDL):
+//   k_route    (route.cu) stable counting sort of the T*k slots by expert and
+//              the group table: each expert's sorted slots are cut into groups
+//              of up to kGroupTokens (8);
+//   k_gprep    x (bf16, or RMSNorm of the fp32 residual; in the E4M3 mode
+//              quantized per 128 first) -> 16 E2M1 pieces per element (see
+//              layout.h), written once per slot into its group's B operand;
+//   k_glayer   both projections in one persistent grid, one CTA per SM.  A job
+//              is (group, tile): 128 weight rows against the group's nt slots,
+//              one block-scaled MMA (kind::mxf4, M = 128, N = 16 nt, K = 64)
+//              per 64-K step, the nt slots' pieces being the N columns.  Jobs
+//              are ordered (expert, tile, group), so a weight tile leaves HBM
+//              once per expert and its further groups re-read it from L2 right
+//              away;
+//   k_gcombine y[t] = sum_k o[t, k] over the token's slots in k order (or
+//              x += that on a residual stream).
+//
+// B operand layout (group order): a slot at sorted position P keeps its pieces
+// at P * act_bytes(K); a group's slots are consecutive positions, and inside
+// the group unit u of K holds, per MMA m, the nt slots' 512-byte piece blocks
+// side by side -- byte offset  u * nt * 1024 + m * nt * 512 + i * 512  for slot
+// i of the group -- so the B rows of one MMA (16 per slot) are one contiguous
+// run with 256-byte row-group stride, and a run of units of one group is one
+// contiguous copy.  Scale atoms are per (group, unit): 512 bytes in the order
+// tcgen05.cp moves them, row n = 16 i + p (slot i, piece p) at byte
+// (n % 32) * 16 + (n / 32) * 4 + block.
+//
+// The kernel roles are those of the slot-major layer kernel (gemv.cu): a
+// weight producer thread filling a ring of shared-memory stages with
+// cp.async.bulk, an activation loader thread, here one MMA-issuing thread (each
+// MMA is N = 16 nt wide), and four epilogue warps that read the accumulator
+// with tcgen05.ld, sum the 16 piece columns of each slot, and finish a job:
+// gate/up -> h = w * silu(g) * u as pieces into the down projection's B
+// operand; down -> o of each slot.  A job split over several CTAs is finished
+// by the CTA holding its first unit, which adds the others' launch-tagged
+// partial sums in CTA order, so results are bitwise reproducible.  Every wait
+// is bounded (2 s); on expiry the kernel records the device-timeout status,
+// stops issuing, waits (bounded) for its copies in flight and frees its TMEM.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kNT = kGroupTokens;                            // slots per group
+constexpr int kGCU = 2;                                      // units per stage
+constexpr int kGStages = 6;
+constexpr int kGStageA = kGCU * kUnitCodeBytes;              // 16 KB of weights
+constexpr int kGStageSfa = kGCU * kUnitSfBytes;
+constexpr int kGStageB = kGCU * kNT * kUnitBBytes;           // up to 16 KB of pieces
+constexpr int kGStageSfb = kGCU * kUnitSfBytes;
+constexpr int kGOffSfa = kGStageA;
+constexpr int kGOffB = kGOffSfa + kGStageSfa;
+constexpr int kGOffSfb = kGOffB + kGStageB;
+constexpr int kGStageBytes = kGOffSfb + kGStageSfb;
+constexpr int kGTmemCols = 512;
+constexpr int kGAccCols = kNT * kPieces;                     // 128 fp32 columns per accumulator
+constexpr int kGSfCol0 = 2 * kGAccCols;                      // scale atoms after the two accumulators
+constexpr uint64_t kGWaitLimitNs = 2000000000ull;
+constexpr int kGWarpIssuer = 1;
+constexpr int kGWarpEpi0 = 2;                                // epilogue warps 2..5
+constexpr int kGWarpLoader = 6;
+constexpr int kGThreads = (kGWarpLoader + 1) * 32;
+constexpr int kGJobWindow = 32;
+
+static_assert(kGStageBytes % 1024 == 0, "stage alignment");
+static_assert(kGSfCol0 + kGStages * kGCU * 8 <= kGTmemCols, "tensor memory budget");
+static_assert(kGAccCols <= 256 && kGAccCols % 16 == 0, "MMA N");
+// CTAs of k_glayer wait on one another (the down projection needs every h):
+// two must never share an SM, so the shared memory asked for is more than
+// half of an SM's.
+constexpr size_t kGOneCtaPerSmSmem = 116 * 1024;
+
+struct GJob {
+    const uint8_t* code;    // weight tile, unit 0
+    const uint8_t* sf;
+    const uint8_t* B;       // the group's pieces, unit 0
+    const uint8_t* Bsf;     // the group's scale atoms, unit 0
+    int nt, p0, tile, g;    // slots, first sorted position, weight tile, group
+    bool ok;
+};
+
+struct GBSrc {
+    const uint8_t* B;       // nullptr: the stage multiplies nothing
+    const uint8_t* Bsf;
+    uint32_t nb, nsf;
+    int phase;
+};
+
+struct GSmem {
+    uint8_t stage[kGStages][kGStageBytes];
+    uint64_t full[kGStages];
+    uint64_t empty[kGStages];
+    uint64_t posted[kGStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    GBSrc bsrc[kGStages];
+    float comb[2][kNT][kTileRows];
+    GJob jobs[2][kGJobWindow];
+    uint32_t tmem;
+    int abort;
+};
+static_assert(sizeof(GSmem) <= 227 * 1024, "shared memory per CTA");
+
+// One projection's unit stream (host part; the job count is read on the device).
+struct GPlan {
+    int kgt, kg_half, ntiles;
+    size_t code_off, sf_off, tile_code_bytes, tile_sf_bytes;
+    size_t act_bytes;       // piece bytes of one slot over K
+    int phase;
+};
+
+// ----------------------------------------------------------------- pieces
+
+// Pieces of 64 consecutive elements (32-blocks blk0, blk0 + 1 of a unit; lane
+// l holds elements 2l, 2l + 1), computed once: byte[p] = the lane's E2M1 pair
+// of piece p, sc[p] = the piece's scale byte.  Same decomposition as the
+// slot-major path: the first scale is the least e with max|v| <= 6 * 2^e over
+// the 32-block, each next piece encodes the remainder 4x finer.
+struct Pieces64 {
+    uint8_t byte[kPieces];
+    uint8_t sc[kPieces];
+};
+
+__device__ __forceinline__ void make_pieces64(float v0, float v1, Pieces64& pc)
+{
+    float amax = fmaxf(fabsf(v0), fabsf(v1));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const int s0 = e2m1_scale_byte(amax);
+    float r0 = v0, r1 = v1;
+#pragma unroll
+    for (int p = 0; p < kPieces; p++) {
+        const int s = max(s0 - 2 * p, 1);
+        const float down = exp2i(127 - s), up = exp2i(s - 127);
+        const uint32_t byte = f32x2_to_e2m1x2(r0 * down, r1 * down);
+        const float2 d = e2m1x2_to_f32x2(byte);
+        r0 = fmaf(-d.x, up, r0);
+        r1 = fmaf(-d.y, up, r1);
+        pc.byte[p] = (uint8_t)byte;
+        pc.sc[p] = (uint8_t)s;
+    }
+}
+
+// Stores the pieces of slot i of a group: unit points at the group's unit
+// (codes), mstride = nt * 512 (distance between the unit's two MMAs), atom =
+// the group's scale atom of that unit; blk0 = the span's first 32-block
+// within the unit (0 or 2).
+__device__ __forceinline__ void store_pieces64(const Pieces64& pc, int lane, uint8_t* unit, int mstride,
+                                               uint8_t* atom, int i, int blk0)
+{
+    const int bu = blk0 + (lane >> 4);             // 32-block within the unit
+    const int ib = lane & 15;                      // byte within the block's row
+    uint8_t* rows = unit + (bu >> 1) * mstride + i * kMmaBBytes + (bu & 1) * 128 + ib;
+#pragma unroll
+    for (int p = 0; p < kPieces; p++) rows[(p >> 3) * 256 + (p & 7) * 16] = pc.byte[p];
+    if (ib == 0) {
+#pragma unroll
+        for (int p = 0; p < kPieces; p++) {
+            const int n = 16 * i + p;
+            atom[(n & 31) * 16 + (n >> 5) * 4 + bu] = pc.sc[p];
+        }
+    }
+}
+
+// Where slot position P's pieces of unit u (of a K with kgt units) go.
+struct GDst {
+    uint8_t* unit;
+    uint8_t* atom;
+    int mstride, i;
+};
+
+__device__ __forceinline__ GDst group_dst(const GroupArgs& a, int e, int P, int u, int kgt, size_t abytes,
+                                          uint8_t* codes, uint8_t* atoms)
+{
+    const int rel = P - a.offsets[e];
+    const int q = rel / kNT;
+    const int g = a.gbase[e] + q;
+    const int p0 = a.offsets[e] + q * kNT;
+    const int nt = min(kNT, a.counts[e] - q * kNT);
+    GDst d;
+    d.i = rel - q * kNT;
+    d.mstride = nt * kMmaBBytes;
+    d.unit = codes + (size_t)p0 * abytes + (size_t)u * nt * kUnitBBytes;
+    d.atom = atoms + ((size_t)g * kgt + u) * kUnitSfBytes;
+    return d;
+}
+
+// ------------------------------------------------------------------ k_gprep
+
+// grid (T, ceil(spans / 8)), 256 threads: one warp per 64 elements (bf16
+// mode) or per 128-element block (E4M3 mode); the pieces are made once and
+// stored for each of the token's slots.
+__global__ void __launch_bounds__(256) k_gprep(GroupArgs a)
+{
+    const int t = blockIdx.x;
+    const int H = a.H;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ float s_red[8];
+    __shared__ float s_den;
+    __shared__ int s_e[16], s_P[16];
+
+    pdl_wait();
+    pdl_trigger();
+    if (threadIdx.x < a.topk) {
+        const int j = t * a.topk + threadIdx.x;
+        const int P = a.inv[j];
+        s_P[threadIdx.x] = P;
+        s_e[threadIdx.x] = P >= 0 ? a.idx[j] : -1;
+    }
+    float den = 1.0f;
+    if (a.x_resid) {
+        // RMSNorm with unit weight: sum of squares in a fixed tree order
+        const float* xr = a.x_resid + (size_t)t * H;
+        float ss = 0.0f;
+        for (int i = threadIdx.x; i < H; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+        ss = warp_sum(ss);
+        if (lane == 0) s_red[warp] = ss;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float tot = 0.0f;
+            for (int w = 0; w < (int)(blockDim.x >> 5); w++) tot += s_red[w];
+            s_den = sqrtf(tot / (float)H + a.eps);
+        }
+        __syncthreads();
+        den = s_den;
+    } else {
+        __syncthreads();
+    }
+    const size_t abytes = act_bytes(H);
+    const int kgt = H / 128;
+    auto xval = [&](int i) {
+        return a.x_resid ? __bfloat162float(__float2bfloat16_rn(a.x_resid[(size_t)t * H + i] / den))
+                         : __uint_as_float((uint32_t)a.x_bf16[(size_t)t * H + i] << 16);
+    };
+    if (a.act_e4m3) {
+        // x quantized to E4M3 under one ue8m0 scale per 128 elements, then the
+        // dequantized values as pieces
+        const int b = blockIdx.y * (blockDim.x >> 5) + warp;      // 128-element block = unit
+        if (b >= H / 128) return;
+        float v[4];
+        for (int hh = 0; hh < 2; hh++)
+            for (int e = 0; e < 2; e++) v[2 * hh + e] = xval(b * 128 + hh * 64 + 2 * lane + e);
+        const float amax = warp_max(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+        const int s = ue8m0_for_amax_bits(amax);
+        for (int hh = 0; hh < 2; hh++) {
+            Pieces64 pc;
+            make_pieces64(e4m3_quant_dequant(v[2 * hh], s), e4m3_quant_dequant(v[2 * hh + 1], s), pc);
+            for (int kk = 0; kk < a.topk; kk++) {
+                if (s_P[kk] < 0) continue;
+                const GDst d = group_dst(a, s_e[kk], s_P[kk], b, kgt, abytes, a.xg, a.xgsf);
+                store_pieces64(pc, lane, d.unit, d.mstride, d.atom, d.i, 2 * hh);
+            }
+        }
+        return;
+    }
+    const int b = blockIdx.y * (blockDim.x >> 5) + warp;          // 64-element span
+    if (b >= H / 64) return;
+    Pieces64 pc;
+    make_pieces64(xval(b * 64 + 2 * lane), xval(b * 64 + 2 * lane + 1), pc);
+    for (int kk = 0; kk < a.topk; kk++) {
+        if (s_P[kk] < 0) continue;
+        const GDst d = group_dst(a, s_e[kk], s_P[kk], b / 2, kgt, abytes, a.xg, a.xgsf);
+        store_pieces64(pc, lane, d.unit, d.mstride, d.atom, d.i, 2 * (b & 1));
+    }
+}
+
+// ----------------------------------------------------------------- k_glayer
+
+// A CTA's part of one projection's unit stream: U units over the first
+// G = min(grid, U) CTAs (CTA c < G takes [c U / G, (c + 1) U / G), at least
+// one unit; the others none), so the CTAs between a split job's first and
+// last all hold part of it.
+struct GRange {
+    uint32_t u0, u1, j0, jlast;
+    int G;                  // CTAs that take part in this projection
+    bool empty;
+};
+
+__device__ __forceinline__ long long g_range_start(long long U, int G, int c) { return (long long)c * U / G; }
+
+__device__ __forceinline__ int g_cta_of_unit(long long U, int G, long long x)
+{
+    return (int)(((x + 1) * G - 1) / U);
+}
+
+__device__ __forceinline__ GRange g_cta_range(long long U, int grid, int kgt)
+{
+    GRange r;
+    const int G = (int)(U < grid ? U : grid);
+    const int c = (int)blockIdx.x < G ? (int)blockIdx.x : G;
+    r.G = G;
+    r.u0 = (uint32_t)(G > 0 ? g_range_start(U, G, c) : 0);
+    r.u1 = (uint32_t)(G > 0 ? g_range_start(U, G, c < G ? c + 1 : c) : 0);
+    r.empty = r.u1 == r.u0;
+    r.j0 = r.u0 / (uint32_t)kgt;
+    r.jlast = r.empty ? r.j0 : (r.u1 - 1) / (uint32_t)kgt;
+    return r;
+}
+
+// Walks a CTA's range in chunks of at most kGCU units that never cross a job;
+// every role sees the same sequence.
+struct GWalk {
+    uint32_t u, u1, kgt, job, kg;
+    __device__ GWalk(int kgt_, const GRange& r)
+    {
+        u = r.u0;
+        u1 = r.u1;
+        kgt = (uint32_t)kgt_;
+        job = r.j0;
+        kg = r.u0 - r.j0 * kgt;
+    }
+    __device__ uint32_t chunk() const { return min(min(kgt - kg, u1 - u), (uint32_t)kGCU); }
+    // advance past a chunk of n units; true at the end of a job or of the range
+    __device__ bool advance(uint32_t n, bool& next_job)
+    {
+        u += n;
+        kg += n;
+        next_job = false;
+        bool jend = (u == u1);
+        if (kg == kgt) {
+            kg = 0;
+            job++;
+            next_job = true;
+            jend = true;
+        }
+        return jend;
+    }
+};
+
+__device__ __forceinline__ int g_count_chunks(int kgt, const GRange& r)
+{
+    GWalk wk(kgt, r);
+    int n = 0;
+    while (wk.u < wk.u1) {
+        bool nj;
+        wk.advance(wk.chunk(), nj);
+        n++;
+    }
+    return n;
+}
+
+// Job j of a projection: jobs are ordered (expert, tile, group of the
+// expert); the expert's jobs are [ntiles gb, ntiles (gb + ng)), so j / ntiles
+// is one of its groups.
+template <int PHASE>
+__device__ GJob gjob_info(const GroupArgs& a, const GPlan& p, uint32_t job)
+{
+    GJob j;
+    const int gl = (int)(job / (uint32_t)p.ntiles);
+    const GroupInfo gi = a.groups[gl];
+    const uint32_t local = job - (uint32_t)gi.gb * (uint32_t)p.ntiles;
+    j.tile = (int)(local / (uint32_t)gi.ng);
+    const int g = gi.gb + (int)(local % (uint32_t)gi.ng);
+    const GroupInfo gg = g == gl ? gi : a.groups[g];
+    j.nt = gg.nt;
+    j.p0 = gg.p0;
+    j.g = g;
+    j.B = (PHASE == 0 ? a.xg : a.hg) + (size_t)gg.p0 * p.act_bytes;
+    j.Bsf = (PHASE == 0 ? a.xgsf : a.hgsf) + (size_t)g * p.kgt * kUnitSfBytes;
+    const uint8_t* cb = a.codes[gg.e];
+    const uint8_t* sb = a.scales[gg.e];
+    j.ok = cb && sb && ((reinterpret_cast<uintptr_t>(cb) | reinterpret_cast<uintptr_t>(sb)) & 15) == 0;
+    j.code = j.ok ? cb + p.code_off + (size_t)j.tile * p.tile_code_bytes : nullptr;
+    j.sf = j.ok ? sb + p.sf_off + (size_t)j.tile * p.tile_sf_bytes : nullptr;
+    return j;
+}
+
+template <int PHASE>
+__device__ __forceinline__ GJob gjob_at(const GroupArgs& a, const GPlan& p, const GRange& r, GSmem& sm,
+                                        uint32_t job)
+{
+    const uint32_t d = job - r.j0;
+    if (d < (uint32_t)kGJobWindow) return sm.jobs[PHASE][d];
+    const GJob j = gjob_info<PHASE>(a, p, job);
+    if (!j.ok) atomicOr(a.status, kStatusBadIndex);
+    return j;
+}
+
+__device__ __forceinline__ uint32_t g_ld_acquire_u32(const int* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint64_t g_ld_relaxed_u64(const uint64_t* p)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void g_st_relaxed_u64(uint64_t* p, uint64_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void g_set_abort(const GroupArgs& a, GSmem& sm)
+{
+    atomicOr(a.status, kStatusTimeout);
+    sm.abort = 1;
+}
+
+// Streams the weights of one projection's range into the ring and posts each
+// stage's activation source to the loader.  n: chunks so far (both phases).
+template <int PHASE>
+__device__ bool gproduce(const GroupArgs& a, const GPlan& p, const GRange& r, GSmem& sm, int& n)
+{
+    if (r.empty) return true;
+    GWalk wk(p.kgt, r);
+    GJob ji = gjob_at<PHASE>(a, p, r, sm, wk.job);
+    while (wk.u < wk.u1) {
+        const uint32_t nun = wk.chunk();
+        const bool has_half = p.kg_half && (wk.kg + nun == wk.kgt);
+        const uint32_t nfull = nun - (has_half ? 1u : 0u);
+        const uint32_t cb = nfull * kUnitCodeBytes + (has_half ? kMmaCodeBytes : 0);
+        const uint32_t sb = nun * kUnitSfBytes;
+        const uint32_t bb = (uint32_t)ji.nt * (nfull * kUnitBBytes + (has_half ? kMmaBBytes : 0));
+        const uint32_t bsb = nun * kUnitSfBytes;
+        const int s = n % kGStages;
+        if (n >= kGStages &&
+            !mbar_wait_or_abort(&sm.empty[s], ((n / kGStages) & 1) ^ 1, &sm.abort, kGWaitLimitNs)) {
+            g_set_abort(a, sm);
+            return false;
+        }
+        uint8_t* stg = sm.stage[s];
+        if (ji.ok) {
+            mbar_arrive_expect_tx(&sm.full[s], cb + sb + bb + bsb);
+            bulk_g2s(stg, ji.code + (size_t)wk.kg * kUnitCodeBytes, cb, &sm.full[s]);
+            bulk_g2s(stg + kGOffSfa, ji.sf + (size_t)wk.kg * kUnitSfBytes, sb, &sm.full[s]);
+            sm.bsrc[s] = GBSrc{ji.B + (size_t)wk.kg * ji.nt * kUnitBBytes, ji.Bsf + (size_t)wk.kg * kUnitSfBytes,
+                               bb, bsb, PHASE};
+        } else {
+            mbar_arrive(&sm.full[s]);      // an empty stage: nothing to multiply
+            sm.bsrc[s].B = nullptr;
+        }
+        mbar_arrive(&sm.posted[s]);        // release: bsrc is visible to the loader
+        bool nj;
+        wk.advance(nun, nj);
+        n++;
+        if (nj && wk.u < wk.u1) ji = gjob_at<PHASE>(a, p, r, sm, wk.job);
+    }
+    return true;
+}
+
+// Issues the activation copies of every posted stage, in order: x's pieces
+// after the previous kernel (PDL), h's once the grid-wide count of finished
+// h tiles reaches h_target.  A posted stage's copies are always issued, even
+// after a timeout, so that every transaction count completes.
+__device__ void gload_b(const GroupArgs& a, int nchunks, uint32_t h_target, GSmem& sm)
+{
+    bool pdl_done = false, h_done = false;
+    for (int n = 0; n < nchunks; n++) {
+        const int s = n % kGStages;
+        if (!mbar_wait_or_abort(&sm.posted[s], (n / kGStages) & 1, &sm.abort, kGWaitLimitNs)) {
+            g_set_abort(a, sm);
+            return;
+        }
+        const GBSrc q = sm.bsrc[s];
+        if (!q.B) continue;
+        if (!pdl_done) {
+            pdl_wait();
+            pdl_done = true;
+        }
+        if (q.phase == 1 && !h_done) {
+            bool ok = g_ld_acquire_u32(a.sync) >= h_target;
+            if (!ok) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!(ok = g_ld_acquire_u32(a.sync) >= h_target))
+                    if (*(volatile int*)&sm.abort || globaltimer_ns() - t0 > kGWaitLimitNs) break;
+            }
+            // h was written with generic stores; the copies read it through the async proxy
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            if (!ok) g_set_abort(a, sm);
+            h_done = true;
+        }
+        uint8_t* stg = sm.stage[s];
+        bulk_g2s(stg + kGOffB, q.B, q.nb, &sm.full[s]);
+        bulk_g2s(stg + kGOffSfb, q.Bsf, q.nsf, &sm.full[s]);
+    }
+}
+
+struct GIss {
+    int n, buf;
+    uint32_t use[2];
+    bool abort;
+};
+
+// The one MMA-issuing thread: per unit, the two scale atoms to TMEM and one
+// (or, for a half unit, no second) MMA of N = 16 nt per 64-K step.
+template <int PHASE>
+__device__ void gissue(const GroupArgs& a, const GPlan& p, const GRange& r, GSmem& sm, uint32_t tmem, GIss& is)
+{
+    if (r.empty) return;
+    GWalk wk(p.kgt, r);
+    GJob ji = gjob_at<PHASE>(a, p, r, sm, wk.job);
+    bool any = false;               // the accumulator holds this job's sum
+    bool job_start = true;
+    while (wk.u < wk.u1) {
+        const uint32_t nun = wk.chunk();
+        const int s = is.n % kGStages;
+        if (job_start) {
+            // the epilogue must have read this accumulator's previous job
+            if (!is.abort && is.use[is.buf] > 0 &&
+                !mbar_wait_or_abort(&sm.acc_empty[is.buf], (is.use[is.buf] - 1) & 1, &sm.abort, kGWaitLimitNs)) {
+                g_set_abort(a, sm);
+                is.abort = true;
+            }
+            job_start = false;
+        }
+        if (!is.abort && !mbar_wait_or_abort(&sm.full[s], (is.n / kGStages) & 1, &sm.abort, kGWaitLimitNs)) {
+            g_set_abort(a, sm);
+            is.abort = true;
+        }
+        if (!is.abort && ji.ok) {
+            tc_fence_after();
+            const uint8_t* st = sm.stage[s];
+            const uint32_t nt = (uint32_t)ji.nt;
+            const uint32_t idesc = mxf4_idesc(kTileRows, 16 * nt);
+            for (uint32_t ii = 0; ii < nun; ii++) {
+                const uint32_t col = tmem + kGSfCol0 + (uint32_t)(s * kGCU + ii) * 8;
+                tc_cp_sf(col, umma_desc(smem_u32(st + kGOffSfa + ii * kUnitSfBytes), 16, 128));
+                tc_cp_sf(col + 4, umma_desc(smem_u32(st + kGOffSfb + ii * kUnitSfBytes), 16, 128));
+                const bool half = p.kg_half && (wk.kg + ii == wk.kgt - 1);
+                for (uint32_t m = 0; m < (half ? 1u : 2u); m++) {
+                    const uint64_t ad =
+                        umma_desc(smem_u32(st + ii * kUnitCodeBytes + m * kMmaCodeBytes), 128, 256);
+                    const uint64_t bd = umma_desc(
+                        smem_u32(st + kGOffB + ii * nt * kUnitBBytes + m * nt * kMmaBBytes), 128, 256);
+                    tc_mma_mxf4(tmem + (uint32_t)is.buf * kGAccCols, ad, bd, mxf4_idesc_sf(idesc, 2 * m), col,
+                                col + 4, any ? 1u : 0u);
+                    any = true;
+                }
+            }
+        }
+        tc_commit(&sm.empty[s]);           // the stage is consumed once these MMAs are done
+        bool nj;
+        const bool jend = wk.advance(nun, nj);
+        is.n++;
+        if (nj && wk.u < wk.u1) ji = gjob_at<PHASE>(a, p, r, sm, wk.job);
+        if (jend) {
+            tc_commit(&sm.acc_full[is.buf]);   // the accumulator is final
+            is.use[is.buf]++;
+            is.buf ^= 1;
+            any = false;
+            job_start = true;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ epilogue
+
+// Gate/up job (group, tile), slot i -> the 64 values h = w * silu(g) * u of
+// that slot as pieces into the down projection's B operand, by one warp; then
+// the grid-wide count of finished h tiles grows by the tiles written.
+__device__ void gfinalize_gate_up(const GroupArgs& a, const GPlan& p, const GJob& jb, int i, const float* comb,
+                                  int lane)
+{
+    const int P = jb.p0 + i, tile = jb.tile;
+    const float w = a.w[a.perm[P]];
+    const float2 g = *reinterpret_cast<const float2*>(comb + 2 * lane);
+    const float2 u = *reinterpret_cast<const float2*>(comb + 64 + 2 * lane);
+    float h0 = silu(g.x) * u.x, h1 = silu(g.y) * u.y;
+    const size_t abytes = act_bytes(a.I);
+    const int kgt = (a.I + 127) / 128;
+    uint8_t* unit = a.hg + (size_t)jb.p0 * abytes + (size_t)(tile / 2) * jb.nt * kUnitBBytes;
+    uint8_t* atom = a.hgsf + ((size_t)jb.g * kgt + tile / 2) * kUnitSfBytes;
+    const int mstride = jb.nt * kMmaBBytes;
+    int done = 1;                         // h tiles whose pieces this call writes
+    if (a.act_e4m3) {
+        // h is quantized to E4M3 per 128 along I (tiles 2b, 2b + 1; a last block
+        // of 64 is one tile) before w; the second tile of a block to finish
+        // quantizes both, from the first one's raw h
+        const int blk = tile / 2, nblk = (p.ntiles + 1) / 2;
+        const bool pair = (tile | 1) < p.ntiles;
+        float o0 = 0.0f, o1 = 0.0f;
+        if (pair) {
+            float* mine = a.hraw + (size_t)P * a.I + (size_t)tile * 64 + 2 * lane;
+            mine[0] = h0;
+            mine[1] = h1;
+            __threadfence();
+            __syncwarp();
+            int old = 0;
+            if (lane == 0) old = atomicAdd(a.hpair + (size_t)P * nblk + blk, 1);
+            old = __shfl_sync(0xFFFFFFFFu, old, 0);
+            if (old == 0) return;         // the other tile finishes the block
+            __threadfence();
+            const float* other = a.hraw + (size_t)P * a.I + (size_t)(tile ^ 1) * 64 + 2 * lane;
+            o0 = __ldcg(other);
+            o1 = __ldcg(other + 1);
+            if (lane == 0) a.hpair[(size_t)P * nblk + blk] = 0;     // ready for the next launch
+            done = 2;
+        }
+        const float amax = warp_max(fmaxf(fmaxf(fabsf(h0), fabsf(h1)), fmaxf(fabsf(o0), fabsf(o1))));
+        const int s = ue8m0_for_amax_bits(amax);
+        h0 = e4m3_quant_dequant(h0, s);
+        h1 = e4m3_quant_dequant(h1, s);
+        if (pair) {
+            Pieces64 po;
+            make_pieces64(e4m3_quant_dequant(o0, s) * w, e4m3_quant_dequant(o1, s) * w, po);
+            store_pieces64(po, lane, unit, mstride, atom, i, 2 * ((tile ^ 1) & 1));
+        }
+    }
+    Pieces64 pc;
+    make_pieces64(h0 * w, h1 * w, pc);
+    store_pieces64(pc, lane, unit, mstride, atom, i, 2 * (tile & 1));
+    // the down projection reads these with bulk copies (async proxy), in other CTAs
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+        __threadfence();
+        atomicAdd(a.sync, done);
+    }
+}
+
+struct GEpi {
+    int buf, cb;
+    uint32_t use[2];
+    uint32_t tag;               // this launch's tag of the partial sums
+};
+
+// Partial sums (nt per row) of a split job from CTAs c..c1, added in CTA
+// order into acc; returns the first CTA not yet folded in.  With spin, waits
+// (bounded) for each; without, stops at the first whose entries are not all
+// there yet.
+__device__ __forceinline__ int gfold(const uint64_t* part, int c, int c1, int row, int nt, uint32_t tag, bool spin,
+                                     float (&acc)[kNT], bool* timed_out)
+{
+    uint64_t t0 = 0;
+    while (c <= c1) {
+        float v[kNT];
+        bool all = true;
+#pragma unroll
+        for (int i = 0; i < kNT; i++) {
+            v[i] = 0.0f;
+            if (i < nt && all) {
+                const uint64_t e = g_ld_relaxed_u64(part + ((size_t)c * kNT + i) * kTileRows + row);
+                if ((uint32_t)(e >> 32) == tag) v[i] = __uint_as_float((uint32_t)e);
+                else all = false;
+            }
+        }
+        if (all) {
+#pragma unroll
+            for (int i = 0; i < kNT; i++) acc[i] += v[i];
+            c++;
+            continue;
+        }
+        if (!spin) break;
+        if (t0 == 0) t0 = globaltimer_ns();
+        else if (globaltimer_ns() - t0 > kGWaitLimitNs) {
+            *timed_out = true;
+            break;
+        }
+    }
+    return c;
+}
+
+template <int PHASE>
+__device__ void gepilogue(const GroupArgs& a, const GPlan& p, const GRange& r, GSmem& sm, uint32_t tmem, long long U,
+                          int quad, int lane, GEpi& es)
+{
+    if (r.empty) return;
+    uint64_t* part = PHASE == 0 ? a.part_gu : a.part_dn;
+    const int row = quad * 32 + lane;                      // accumulator row of this thread
+    const int G = r.G;
+    GWalk wk(p.kgt, r);
+    GJob ji = gjob_at<PHASE>(a, p, r, sm, wk.job);
+    while (wk.u < wk.u1) {
+        const uint32_t job = wk.job;
+        const GJob cur = ji;
+        bool nj;
+        const bool jend = wk.advance(wk.chunk(), nj);
+        if (nj && wk.u < wk.u1) ji = gjob_at<PHASE>(a, p, r, sm, wk.job);
+        if (!jend) continue;
+
+        // --------------------------------------------- end of (this CTA's part of) a job
+        const long long js = (long long)job * p.kgt, je = js + p.kgt;
+        const bool owner = js >= r.u0;
+        const int c1 = owner && je > r.u1 ? g_cta_of_unit(U, G, je - 1) : (int)blockIdx.x;
+        const int nt = cur.nt;
+        float pacc[kNT];
+#pragma unroll
+        for (int i = 0; i < kNT; i++) pacc[i] = 0.0f;
+        bool late = false;
+        int cnext = blockIdx.x + 1;
+        if (c1 > (int)blockIdx.x)   // while the last MMAs run: the partials that are there already
+            cnext = gfold(part, cnext, c1, row, nt, es.tag, false, pacc, &late);
+
+        const int buf = es.buf;
+        const bool ready = !*(volatile int*)&sm.abort &&
+                           mbar_wait_or_abort(&sm.acc_full[buf], es.use[buf] & 1, &sm.abort, kGWaitLimitNs);
+        es.use[buf]++;
+        if (!ready) g_set_abort(a, sm);
+        tc_fence_after();
+        float v[kNT];
+#pragma unroll
+        for (int i = 0; i < kNT; i++) {
+            v[i] = 0.0f;
+            if (ready && cur.ok && i < nt) {
+                float acc[16];
+                tc_ld16(tmem + (uint32_t)buf * kGAccCols + (uint32_t)(i * kPieces) + ((uint32_t)(quad * 32) << 16),
+                        acc);
+#pragma unroll
+                for (int c = 0; c < kPieces; c++) v[i] += acc[c];
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);
+        es.buf ^= 1;
+
+        if (!owner) {
+            // a later part of a job owned by an earlier CTA
+#pragma unroll
+            for (int i = 0; i < kNT; i++)
+                if (i < nt)
+                    g_st_relaxed_u64(part + ((size_t)blockIdx.x * kNT + i) * kTileRows + row,
+                                     ((uint64_t)es.tag << 32) | __float_as_uint(v[i]));
+            continue;
+        }
+        if (cnext <= c1) {
+            const bool abort = *(volatile int*)&sm.abort;
+            gfold(part, cnext, c1, row, nt, es.tag, !abort, pacc, &late);
+            if (late) g_set_abort(a, sm);
+        }
+#pragma unroll
+        for (int i = 0; i < kNT; i++) v[i] += pacc[i];
+        if (PHASE == 0) {
+            float(*comb)[kTileRows] = sm.comb[es.cb];
+#pragma unroll
+            for (int i = 0; i < kNT; i++)
+                if (i < nt) comb[i][row] = v[i];
+            named_sync(1, 128);
+            for (int i = quad; i < nt; i += 4) gfinalize_gate_up(a, p, cur, i, comb[i], lane);
+            es.cb ^= 1;
+        } else {
+            // o of each slot: rows tile*128 .. +127 of the down output
+#pragma unroll
+            for (int i = 0; i < kNT; i++)
+                if (i < nt) a.obuf[(size_t)(cur.p0 + i) * a.H + (size_t)cur.tile * kTileRows + row] = v[i];
+        }
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+
+// One MoE layer on the expert-major path: the gate/up projection then the
+// down projection, in one persistent grid.  The job count comes from the
+// route kernel, finished before this grid starts (k_gprep lets it start only
+// after waiting for the route kernel).
+__global__ void __launch_bounds__(kGThreads, 1) k_glayer(GroupArgs a, GPlan p0, GPlan p1)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    GSmem& sm = *reinterpret_cast<GSmem*>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x;
+    const long long ngroups = a.gbase[a.E];
+    const long long U0 = ngroups * p0.ntiles * p0.kgt, U1 = ngroups * p1.ntiles * p1.kgt;
+    const GRange r0 = g_cta_range(U0, G, p0.kgt), r1 = g_cta_range(U1, G, p1.kgt);
+    const uint32_t h_target = (uint32_t)a.offsets[a.E] * (uint32_t)p0.ntiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGStages; s++) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 1);
+            mbar_init(&sm.posted[s], 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&sm.acc_full[b], 1);
+            mbar_init(&sm.acc_empty[b], 4);
+        }
+        mbar_init(&sm.drain, 1);
+        sm.abort = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        // resolve the CTA's first jobs of both projections in parallel
+        if (!r0.empty && r0.j0 + lane <= r0.jlast) {
+            const GJob j = gjob_info<0>(a, p0, r0.j0 + lane);
+            sm.jobs[0][lane] = j;
+            if (!j.ok) atomicOr(a.status, kStatusBadIndex);
+        }
+        if (!r1.empty && r1.j0 + lane <= r1.jlast) {
+            const GJob j = gjob_info<1>(a, p1, r1.j0 + lane);
+            sm.jobs[1][lane] = j;
+            if (!j.ok) atomicOr(a.status, kStatusBadIndex);
+        }
+    }
+    if (warp == kGWarpIssuer) tmem_alloc(&sm.tmem, kGTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_trigger();
+    const uint32_t tmem = sm.tmem;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int n = 0;
+            if (gproduce<0>(a, p0, r0, sm, n)) gproduce<1>(a, p1, r1, sm, n);
+            // no copy may still be in flight into this CTA's memory at exit
+            for (int m = n > kGStages ? n - kGStages : 0; m < n; m++)
+                mbar_wait_bounded(&sm.full[m % kGStages], (m / kGStages) & 1, kGWaitLimitNs);
+        }
+        return;
+    }
+    if (warp == kGWarpLoader) {
+        if (lane == 0) gload_b(a, g_count_chunks(p0.kgt, r0) + g_count_chunks(p1.kgt, r1), h_target, sm);
+        return;
+    }
+    if (warp == kGWarpIssuer) {
+        if (lane == 0) {
+            GIss is;
+            is.n = 0;
+            is.buf = 0;
+            is.use[0] = is.use[1] = 0;
+            is.abort = false;
+            gissue<0>(a, p0, r0, sm, tmem, is);
+            gissue<1>(a, p1, r1, sm, tmem, is);
+            // none of this thread's MMAs may be in flight when TMEM is freed
+            tc_commit(&sm.drain);
+            mbar_wait_bounded(&sm.drain, 0, kGWaitLimitNs);
+        }
+        __syncwarp();
+    } else {
+        pdl_wait();
+        GEpi es;
+        es.buf = 0;
+        es.cb = 0;
+        es.use[0] = es.use[1] = 0;
+        es.tag = 1u + (g_ld_acquire_u32(a.sync + 2) & 0x3FFFFFFFu);   // never 0, the cleared value
+        gepilogue<0>(a, p0, r0, sm, tmem, U0, warp & 3, lane, es);
+        gepilogue<1>(a, p1, r1, sm, tmem, U1, warp & 3, lane, es);
+        if (warp == kGWarpEpi0 && lane == 0) {
+            // the last CTA to finish resets the layer's counters for the next launch
+            __threadfence();
+            const int done = atomicAdd(a.sync + 1, 1);
+            if (done == G - 1) {
+                a.sync[0] = 0;
+                a.sync[1] = 0;
+                a.sync[2] += 1;      // the next launch tags its partial sums differently
+                __threadfence();
+            }
+        }
+    }
+    // the issuer and epilogue warps meet here before the tensor memory is released
+    tc_fence_before();
+    named_sync(2, 5 * 32);
+    tc_fence_after();
+    if (warp == kGWarpIssuer) tmem_dealloc(tmem, kGTmemCols);
+}
+
+// --------------------------------------------------------------- k_gcombine
+
+// grid (T), 256 threads: y[t] = sum over the token's slots, in k order, of the
+// down outputs (or x[t] += that).
+__global__ void __launch_bounds__(256) k_gcombine(GroupArgs a)
+{
+    const int t = blockIdx.x, H = a.H;
+    __shared__ int s_P[16];
+    pdl_wait();
+    pdl_trigger();
+    if (threadIdx.x < a.topk) s_P[threadIdx.x] = a.inv[t * a.topk + threadIdx.x];
+    __syncthreads();
+    for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
+        float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int kk = 0; kk < a.topk; kk++) {
+            const int P = s_P[kk];
+            if (P < 0) continue;
+            const float4 o = __ldcg(reinterpret_cast<const float4*>(a.obuf + (size_t)P * H + c));
+            s.x += o.x;
+            s.y += o.y;
+            s.z += o.z;
+            s.w += o.w;
+        }
+        const size_t o = (size_t)t * H + c;
+        if (a.x_resid) {
+            float4* xr = reinterpret_cast<float4*>(a.x_resid + o);
+            float4 x = *xr;
+            x.x += s.x;
+            x.y += s.y;
+            x.z += s.z;
+            x.w += s.w;
+            *xr = x;
+        } else if (a.out_f32) {
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.y) + o) = s;
+        } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(s.x, s.y), hi = __floats2bfloat162_rn(s.z, s.w);
+            uint2 v;
+            v.x = *reinterpret_cast<uint32_t*>(&lo);
+            v.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.y) + o) = v;
+        }
+    }
+}
+
+cudaError_t glaunch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, void** args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+GPlan gplan(const GroupArgs& a, int phase)
+{
+    GPlan p{};
+    const ExpertLayout E = make_expert_layout(a.H, a.I);
+    const MatLayout& L = phase == 0 ? E.gu : E.dn;
+    p.kgt = L.kgt();
+    p.kg_half = L.kg_half;
+    p.ntiles = L.tiles;
+    p.tile_code_bytes = L.tile_code_bytes();
+    p.tile_sf_bytes = L.tile_sf_bytes();
+    p.code_off = phase == 0 ? E.gu_code_off : E.dn_code_off;
+    p.sf_off = phase == 0 ? E.gu_sf_off : E.dn_sf_off;
+    p.act_bytes = act_bytes(phase == 0 ? a.H : a.I);
+    p.phase = phase;
+    return p;
+}
+
+size_t glayer_smem() { return sizeof(GSmem) > kGOneCtaPerSmSmem ? sizeof(GSmem) : kGOneCtaPerSmSmem; }
+
+}  // namespace
+
+GroupWorkspaceSizes group_workspace_sizes(int T, int topk, int E, int H, int I, int sms, bool e4m3)
+{
+    GroupWorkspaceSizes s{};
+    const size_t n = (size_t)T * topk;
+    const size_t G = (size_t)max_groups((int)n, E);
+    s.counts = (size_t)E * 4;
+    s.offsets = (size_t)(E + 1) * 4;
+    s.perm = n * 4;
+    s.inv = n * 4;
+    s.gbase = (size_t)(E + 1) * 4;
+    s.groups = G * sizeof(GroupInfo);
+    s.xg = n * act_bytes(H);
+    s.xgsf = G * (size_t)((H + 127) / 128) * kUnitSfBytes;
+    s.hg = n * act_bytes(I);
+    s.hgsf = G * (size_t)((I + 127) / 128) * kUnitSfBytes;
+    s.obuf = n * (size_t)H * 4;
+    s.part_gu = (size_t)sms * kNT * kTileRows * 8;
+    s.part_dn = s.part_gu;
+    s.hraw = e4m3 ? n * (size_t)I * 4 : 0;
+    s.hpair = e4m3 ? n * (size_t)((I + 127) / 128) * 4 : 0;
+    return s;
+}
+
+cudaError_t group_init_device()
+{
+    return cudaFuncSetAttribute((const void*)k_glayer, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)glayer_smem());
+}
+
+cudaError_t launch_group_layer(const GroupArgs& a0, cudaStream_t s, bool pdl, Profiler* prof)
+{
+    GroupArgs a = a0;
+    if (a.T == 0) return cudaSuccess;
+    const bool chain = pdl && !prof;
+    cudaError_t err;
+    RouteArgs ra{a.idx, a.T * a.topk, a.E, a.counts, a.offsets, a.perm, a.inv, a.status, a.gbase, a.groups};
+    if (prof) prof->begin(kPhaseRoute, s);
+    err = launch_route(ra, s, chain);
+    if (prof) prof->end(s);
+    if (err != cudaSuccess) return err;
+    void* args1[] = {&a};
+    {
+        const int spans = a.act_e4m3 ? a.H / 128 : a.H / 64;     // one warp each
+        if (prof) prof->begin(kPhasePrep, s);
+        err = glaunch((const void*)k_gprep, dim3(a.T, (spans + 7) / 8), dim3(256), 0, s, chain, args1);
+        if (prof) prof->end(s);
+        if (err != cudaSuccess) return err;
+    }
+    GPlan p0 = gplan(a, 0), p1 = gplan(a, 1);
+    void* args[] = {&a, &p0, &p1};
+    if (prof) prof->begin(kPhaseGateUp, s);
+    err = glaunch((const void*)k_glayer, dim3((unsigned)a.sms), dim3(kGThreads), glayer_smem(), s, chain, args);
+    if (prof) prof->end(s);
+    if (err != cudaSuccess) return err;
+    if (prof) prof->begin(kPhaseDown, s);
+    err = glaunch((const void*)k_gcombine, dim3(a.T), dim3(256), 0, s, chain, args1);
+    if (prof) prof->end(s);
+    return err;
+}
+
+}  // namespace moe

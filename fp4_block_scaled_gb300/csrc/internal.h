@@ -94,16 +94,83 @@ enum { kPhasePrep = 0, kPhaseGateUp = 1, kPhaseDown = 2, kPhaseRoute = 3, kPhase
 
 cudaError_t launch_gemv_layer(const GemvArgs& a, cudaStream_t s, bool pdl, Profiler* prof);
 
+// Slots per group of the expert-major path: a group is up to this many
+// consecutive sorted slots of one expert, multiplied as the N = 16 x slots
+// columns of one block-scaled MMA (N <= 128).
+constexpr int kGroupTokens = 8;
+
+// One group of the expert-major path.
+struct __align__(16) GroupInfo {
+    int e;          // expert
+    int p0;         // first sorted position (perm index) of its slots
+    int nt;         // slots, 1..kGroupTokens
+    int gb, ng;     // first group of the expert, groups of the expert
+    int pad[3];
+};
+
 // Token -> expert grouping (route.cu).
 struct RouteArgs {
     const int32_t* idx;     // [n] expert ids of the slots
     int n, E;
     int32_t *counts, *offsets, *perm, *inv;
     int* status;
+    // optional (nullptr: not made): group table of the expert-major path
+    int32_t* gbase;         // [E+1] first group of each expert; gbase[E] = groups
+    GroupInfo* groups;      // [max groups]
 };
+// Upper bound on the groups of n slots over E experts.
+inline int max_groups(int n, int E)
+{
+    const int used = n < E ? n : E;
+    const int g = (n + kGroupTokens - 1) / kGroupTokens + used;
+    return g < n ? g : n;
+}
+
+// Arguments of one MoE layer on the expert-major (grouped) path (group.cu).
+struct GroupArgs {
+    int T, topk, E, H, I;
+    int sms;
+    const uint16_t* x_bf16;
+    float* x_resid;
+    float eps;
+    const int32_t* idx;
+    const float* w;
+    const uint8_t* const* codes;
+    const uint8_t* const* scales;
+    // routing workspace (filled by the route kernel of the layer)
+    int32_t *counts, *offsets, *perm, *inv, *gbase;
+    GroupInfo* groups;
+    // B operands in group order: the pieces of slot at sorted position P start
+    // at P * act_bytes(K) (units of a group hold its nt slots side by side);
+    // scale atoms per (group, unit)
+    uint8_t* xg;            // [n][act_bytes(H)]
+    uint8_t* xgsf;          // [max groups][H/128][512]
+    uint8_t* hg;            // [n][act_bytes(I)]
+    uint8_t* hgsf;          // [max groups][ceil(I/128)][512]
+    float* obuf;            // [n][H] down-projection output per sorted slot
+    uint64_t* part_gu;      // [sms][kGroupTokens][128] tagged partial sums
+    uint64_t* part_dn;
+    int act_e4m3;
+    float* hraw;            // [n][I]
+    int* hpair;             // [n][ceil(I/128)]
+    int* sync;              // [3], as on the slot-major path (its own words)
+    int* status;
+    void* y;
+    int out_f32;
+};
+
+struct GroupWorkspaceSizes {
+    size_t counts, offsets, perm, inv, gbase, groups;    // bytes
+    size_t xg, xgsf, hg, hgsf, obuf, part_gu, part_dn, hraw, hpair;
+};
+GroupWorkspaceSizes group_workspace_sizes(int T, int topk, int E, int H, int I, int sms, bool e4m3);
+cudaError_t group_init_device();
+cudaError_t launch_group_layer(const GroupArgs& a, cudaStream_t s, bool pdl, Profiler* prof);
+// library default of moe_ffn_config.gemm_min_tokens
+constexpr int kDefaultGemmMinTokens = 16;
 int route_max_experts();
 cudaError_t route_init_device();
-cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, bool pdl = false);
 
 // E4M3 / ue8m0-per-128 activation quantizer (actquant.cu).
 struct ActQuantArgs {

@@ -10,6 +10,9 @@
 //      within an expert, so perm is unique and the result bit-exact.
 // Out-of-range ids are left out (inv = -1, status "bad index"); perm entries
 // past the number of valid slots are -1.
+// When asked for, the same pass also cuts each expert's sorted slots into
+// groups of up to kGroupTokens (the expert-major path's MMA columns): a second
+// exclusive scan, over ceil(count / kGroupTokens), numbers the groups.
 #include "common.cuh"
 #include "internal.h"
 
@@ -17,6 +20,34 @@ namespace moe {
 namespace {
 
 constexpr int kRouteThreads = 1024;
+
+// Exclusive prefix sum of v over the CTA (thread order); *total = the sum.
+// s_warp: one int per warp.  Every thread must call it.
+__device__ int block_exclusive_scan(int v, int* s_warp, int* total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    __syncthreads();                        // s_warp is free (earlier scans done)
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xFFFFFFFFu, w, o);
+            if (lane >= o) w += u;
+        }
+        if (lane < nw) s_warp[lane] = w;    // inclusive warp totals
+    }
+    __syncthreads();
+    *total = s_warp[nw - 1];
+    return incl - v + (warp ? s_warp[warp - 1] : 0);
+}
 
 __global__ void __launch_bounds__(kRouteThreads) k_route(RouteArgs a)
 {
@@ -37,41 +68,42 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteArgs a)
     }
     __syncthreads();
 
-    // exclusive scan over E: each thread owns a contiguous run of experts
+    // exclusive scans over E of the counts and of the group counts: each thread
+    // owns a contiguous run of experts
     const int per = (E + blockDim.x - 1) / blockDim.x;
     const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
-    int local = 0;
-    for (int e = e0; e < e1; e++) local += s_cur[e];
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += v;
+    int local = 0, lgrp = 0;
+    for (int e = e0; e < e1; e++) {
+        local += s_cur[e];
+        lgrp += (s_cur[e] + kGroupTokens - 1) / kGroupTokens;
     }
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const int nw = blockDim.x >> 5;
-        int v = lane < nw ? s_warp[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(0xFFFFFFFFu, v, o);
-            if (lane >= o) v += u;
-        }
-        if (lane < nw) s_warp[lane] = v;   // inclusive warp totals
-    }
-    __syncthreads();
-    int run = incl - local + (warp ? s_warp[warp - 1] : 0);   // exclusive start of my run
+    int total = 0, gtotal = 0;
+    int run = block_exclusive_scan(local, s_warp, &total);
+    int grun = block_exclusive_scan(lgrp, s_warp, &gtotal);
     for (int e = e0; e < e1; e++) {
         const int c = s_cur[e];
+        const int ng = (c + kGroupTokens - 1) / kGroupTokens;
         a.counts[e] = c;
         a.offsets[e] = run;
+        if (a.groups) {
+            a.gbase[e] = grun;
+            for (int q = 0; q < ng; q++) {
+                GroupInfo gi = {};
+                gi.e = e;
+                gi.p0 = run + q * kGroupTokens;
+                gi.nt = min(kGroupTokens, c - q * kGroupTokens);
+                gi.gb = grun;
+                gi.ng = ng;
+                a.groups[grun + q] = gi;
+            }
+        }
         s_cur[e] = run;                     // becomes the placement cursor
         run += c;
+        grun += ng;
     }
-    const int total = s_warp[(blockDim.x >> 5) - 1];
     if (tid == 0) {
         a.offsets[E] = total;
+        if (a.groups) a.gbase[E] = gtotal;
         if (s_bad) atomicOr(a.status, kStatusBadIndex);
     }
     __syncthreads();
@@ -116,7 +148,7 @@ cudaError_t route_init_device()
                                 route_max_experts() * (int)sizeof(int));
 }
 
-cudaError_t launch_route(const RouteArgs& a0, cudaStream_t s)
+cudaError_t launch_route(const RouteArgs& a0, cudaStream_t s, bool pdl)
 {
     RouteArgs a = a0;
     cudaLaunchConfig_t cfg = {};
@@ -124,6 +156,11 @@ cudaError_t launch_route(const RouteArgs& a0, cudaStream_t s)
     cfg.blockDim = dim3(kRouteThreads);
     cfg.dynamicSmemBytes = (size_t)a.E * sizeof(int);
     cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
     void* args[] = {&a};
     return cudaLaunchKernelExC(&cfg, (const void*)k_route, args);
 }

@@ -3,6 +3,7 @@ import numpy as np
 import torch
 
 import fp4_block_scaled_gb300 as moe
+import oracle
 import synth
 from fp4_block_scaled_gb300.experts import ExpertSet
 
@@ -51,3 +52,45 @@ def assert_close(y, ref, what=""):
 
 def bf16_to_f64(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16).astype(np.uint32).__lshift__(16).view(np.float32).astype(np.float64)
+
+
+class Layer:
+    """One layer's handle and device experts.  path: "slot" keeps every T on
+    the slot-major path, "group" sends every T to the expert-major path,
+    "auto" leaves the library default."""
+
+    def __init__(self, E, H, I, k, max_tokens=8, out=moe.MOE_OUT_F32, seed=0, layer=0, act=moe.MOE_ACT_BF16,
+                 path="slot"):
+        self.E, self.H, self.I, self.k = E, H, I, k
+        self.act = act
+        gmin = {"slot": max_tokens + 1, "group": 1, "auto": 0}[path]
+        self.cfg = moe.config(E, H, I, k, max_tokens, out_dtype=out, act_mode=act, gemm_min_tokens=gmin)
+        self.h = moe.moe_ffn_create(self.cfg, 0)
+        self.es = fill_layer(self.h, self.cfg, layer=layer, seed=seed)
+        self.seed, self.layer = seed, layer
+        self.out = out
+
+    def run(self, x_bits, idx, w):
+        T = x_bits.shape[0]
+        x = torch.from_numpy(x_bits.view(np.int16)).cuda()
+        it = torch.from_numpy(np.ascontiguousarray(idx, np.int32)).cuda()
+        wt = torch.from_numpy(np.ascontiguousarray(w, np.float32)).cuda()
+        dt = torch.float32 if self.out == moe.MOE_OUT_F32 else torch.bfloat16
+        y = torch.empty((T, self.H), dtype=dt, device="cuda")
+        moe.moe_ffn_forward(self.h, x, it, wt, self.es.table, y, T)
+        torch.cuda.synchronize()
+        return y
+
+    def oracle(self, x_bits, idx, w):
+        codes, scales = host_experts(self.H, self.I, idx.reshape(-1), layer=self.layer,
+                                     seed=self.seed, E=self.E)
+        act = oracle.ACT_E4M3_UE8M0_128 if self.act == moe.MOE_ACT_E4M3_UE8M0_128 else oracle.ACT_BF16
+        return oracle.moe_ffn(codes, scales, self.H, self.I, x_bits, idx, w, act_mode=act, nthreads=8)
+
+    def close(self):
+        moe.moe_ffn_destroy(self.h)
+
+
+def inputs(T, E, H, k, seed=0):
+    return (synth.activations_bf16(T, H, seed=seed), synth.routing_uniform(T, E, k, seed=seed),
+            synth.routing_weights(T, k, seed=seed))

@@ -7,7 +7,7 @@ import torch
 import fp4_block_scaled_gb300 as moe
 import oracle
 import synth
-from moe_setup import assert_close, bf16_to_f64, errors, fill_layer, host_experts
+from moe_setup import Layer, assert_close, bf16_to_f64, errors, fill_layer, host_experts, inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -21,42 +21,6 @@ def _cuda():
         pytest.skip("no CUDA device")
     moe.lib()
     yield
-
-
-class Layer:
-    def __init__(self, E, H, I, k, max_tokens=8, out=moe.MOE_OUT_F32, seed=0, layer=0, act=moe.MOE_ACT_BF16):
-        self.E, self.H, self.I, self.k = E, H, I, k
-        self.act = act
-        self.cfg = moe.config(E, H, I, k, max_tokens, out_dtype=out, act_mode=act)
-        self.h = moe.moe_ffn_create(self.cfg, 0)
-        self.es = fill_layer(self.h, self.cfg, layer=layer, seed=seed)
-        self.seed, self.layer = seed, layer
-        self.out = out
-
-    def run(self, x_bits, idx, w):
-        T = x_bits.shape[0]
-        x = torch.from_numpy(x_bits.view(np.int16)).cuda()
-        it = torch.from_numpy(np.ascontiguousarray(idx, np.int32)).cuda()
-        wt = torch.from_numpy(np.ascontiguousarray(w, np.float32)).cuda()
-        dt = torch.float32 if self.out == moe.MOE_OUT_F32 else torch.bfloat16
-        y = torch.empty((T, self.H), dtype=dt, device="cuda")
-        moe.moe_ffn_forward(self.h, x, it, wt, self.es.table, y, T)
-        torch.cuda.synchronize()
-        return y
-
-    def oracle(self, x_bits, idx, w):
-        codes, scales = host_experts(self.H, self.I, idx.reshape(-1), layer=self.layer,
-                                     seed=self.seed, E=self.E)
-        act = oracle.ACT_E4M3_UE8M0_128 if self.act == moe.MOE_ACT_E4M3_UE8M0_128 else oracle.ACT_BF16
-        return oracle.moe_ffn(codes, scales, self.H, self.I, x_bits, idx, w, act_mode=act, nthreads=8)
-
-    def close(self):
-        moe.moe_ffn_destroy(self.h)
-
-
-def inputs(T, E, H, k, seed=0):
-    return (synth.activations_bf16(T, H, seed=seed), synth.routing_uniform(T, E, k, seed=seed),
-            synth.routing_weights(T, k, seed=seed))
 
 
 def test_device_fill_matches_host_generator():
