@@ -145,16 +145,16 @@ def draw_routings(R, E, k, T, seed, dist="uniform", layer=0):
     return idx, w
 
 
-def traffic_record(kernel):
+def traffic_record(kernel, workload):
     """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
+    the current kernel source and on this workload's launch shape (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     rec = d.get(kernel)
-    if not rec:
+    if not rec or workload not in rec.get("workloads", []):
         return None
     src = os.path.join(ROOT, rec["source"])
     if not os.path.exists(src):
@@ -308,7 +308,11 @@ def run_ours(args, wl):
 
     E, H, I, k, T, L = wl["E"], wl["H"], wl["I"], wl["k"], wl["T"], wl["L"]
     act = moe.MOE_ACT_E4M3_UE8M0_128 if wl["act"] == "e4m3" else moe.MOE_ACT_BF16
-    cfg = moe.config(E, H, I, k, T, act_mode=act, out_dtype=moe.MOE_OUT_F32)
+    gmin = {"auto": 0, "slot": T + 1, "group": 1}[args.path]
+    cfg = moe.config(E, H, I, k, T, act_mode=act, out_dtype=moe.MOE_OUT_F32, gemm_min_tokens=gmin)
+    grouped = T >= (gmin or moe.DEFAULT_GEMM_MIN_TOKENS)
+    launches_per_layer = 4 if grouped else 2        # route, prep, layer, combine | prep, layer
+    kernel = "k_glayer" if grouped else "k_layer"
     h = moe.moe_ffn_create(cfg, local)
     nc, ns = synth.expert_sizes(H, I)
     tc = torch.empty(nc, dtype=torch.uint8, device="cuda")
@@ -426,9 +430,11 @@ def run_ours(args, wl):
     moe.moe_ffn_profile_enable(h, False)
     ly_ms = ms_ph[moe.MOE_PHASE_GATE_UP] / max(1, n_ph[moe.MOE_PHASE_GATE_UP])
     pr_ms = ms_ph[moe.MOE_PHASE_PREP] / max(1, n_ph[moe.MOE_PHASE_PREP])
+    ro_ms = ms_ph[moe.MOE_PHASE_ROUTE] / max(1, n_ph[moe.MOE_PHASE_ROUTE])
+    co_ms = ms_ph[moe.MOE_PHASE_DOWN] / max(1, n_ph[moe.MOE_PHASE_DOWN])
     ly_bytes = sum(distinct(i, 0) for i in range(nprof)) / nprof * expert_bytes(H, I) + act_io
     achieved = ly_bytes / (ly_ms / 1000.0) / 1e9
-    traffic = traffic_record("k_layer") if args.workload in ("layer_b1", "layer_b1_e64") else None
+    traffic = traffic_record(kernel, args.workload)
 
     # ---- end to end through the public API from host buffers: every step copies
     # its inputs in from pinned host memory and its result back
@@ -483,21 +489,23 @@ def run_ours(args, wl):
             "data": "synthetic",
             "config": {"workload": args.workload, "layers": L, "experts": E, "hidden": H, "inter": I,
                        "topk": k, "tokens_per_step": T, "routing": wl["dist"], "activations": wl["act"],
+                       "path": "expert-major (grouped)" if grouped else "slot-major",
                        "parallelism": f"replicas{world}",
                        "l2": f"inputs larger than L2: {resident:.1f} GB resident experts"
                              + (", consecutive steps share no expert" if T == 1 and L == 1 else ""),
                        "graph_chunk": chunk},
             "hbm_gbs": gbs_step, "hbm_frac": gbs_step / peak,
             "bytes_per_step": bytes_step,
-            "phase_us": {"prep": pr_ms * 1e3, "layer": ly_ms * 1e3},
-            "roofline": {"bound": "hbm", "kernel": "k_layer", "achieved": achieved,
+            "phase_us": {"route": ro_ms * 1e3, "prep": pr_ms * 1e3, "layer": ly_ms * 1e3,
+                         "combine": co_ms * 1e3},
+            "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved,
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes_per_launch": ly_bytes},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": T * H * 4},
-            "gpu_launches": 2 * K * L,
+            "gpu_launches": launches_per_layer * K * L,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -514,6 +522,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="layer_b1")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
+    ap.add_argument("--path", choices=["auto", "slot", "group"], default="auto",
+                    help="layer path: the library's choice for T, or forced slot-major / expert-major")
     args = ap.parse_args()
     wl = WORKLOADS[args.workload]
     if args.steps is None:

@@ -26,6 +26,7 @@ MOE_ACT_BF16 = 0
 MOE_ACT_E4M3_UE8M0_128 = 1
 MOE_OUT_BF16 = 0
 MOE_OUT_F32 = 1
+DEFAULT_GEMM_MIN_TOKENS = 16   # MOE_DEFAULT_GEMM_MIN_TOKENS
 
 EXPORTS = [
     "moe_ffn_packed_codes_bytes", "moe_ffn_packed_scales_bytes", "moe_ffn_create",

@@ -351,7 +351,7 @@ int moe_ffn_route(moe_ffn_t h, const int32_t* topk_idx, int T, int32_t* counts, 
         return MOE_ERR_INVALID_ARG;
     if (h->cfg.num_experts > route_max_experts()) return MOE_ERR_UNSUPPORTED;
     DeviceGuard guard(h->device);
-    RouteArgs a{topk_idx, T * h->cfg.topk, h->cfg.num_experts, counts, offsets, perm, inv, h->status, nullptr, nullptr};
+    RouteArgs a{topk_idx, T * h->cfg.topk, h->cfg.num_experts, counts, offsets, perm, inv, h->status, nullptr, nullptr, 1};
     cudaStream_t s = (cudaStream_t)stream;
     if (h->prof) h->prof->begin(kPhaseRoute, s);
     cudaError_t e = launch_route(a, s);

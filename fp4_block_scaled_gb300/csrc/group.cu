@@ -4,71 +4,102 @@
 // Four launches per layer, chained with programmatic dependent launch (PDL):
 //   k_route    (route.cu) stable counting sort of the T*k slots by expert and
 //              the group table: each expert's sorted slots are cut into groups
-//              of up to kGroupTokens (8);
+//              of up to S slots (S = 8 in the E4M3 mode, 4 in the bf16 mode);
 //   k_gprep    x (bf16, or RMSNorm of the fp32 residual; in the E4M3 mode
-//              quantized per 128 first) -> 16 E2M1 pieces per element (see
-//              layout.h), written once per slot into its group's B operand;
+//              quantized per 128 first) -> P E2M1 pieces per element (P = 8
+//              in the E4M3 mode, 16 in the bf16 mode; see below), written once
+//              per slot into its group's B operand;
 //   k_glayer   both projections in one persistent grid, one CTA per SM.  A job
 //              is (group, tile): 128 weight rows against the group's nt slots,
-//              one block-scaled MMA (kind::mxf4, M = 128, N = 16 nt, K = 64)
-//              per 64-K step, the nt slots' pieces being the N columns.  Jobs
-//              are ordered (expert, tile, group), so a weight tile leaves HBM
-//              once per expert and its further groups re-read it from L2 right
-//              away;
+//              block-scaled MMAs (kind::mxf4, M = 128, N = P nt <= 64, K = 64),
+//              the nt slots' pieces being the N columns.  Jobs are ordered
+//              (expert, tile, group), so a weight tile leaves HBM once per
+//              expert and its further groups re-read it from L2 right away;
 //   k_gcombine y[t] = sum_k o[t, k] over the token's slots in k order (or
 //              x += that on a residual stream).
 //
-// B operand layout (group order): a slot at sorted position P keeps its pieces
-// at P * act_bytes(K); a group's slots are consecutive positions, and inside
-// the group unit u of K holds, per MMA m, the nt slots' 512-byte piece blocks
-// side by side -- byte offset  u * nt * 1024 + m * nt * 512 + i * 512  for slot
-// i of the group -- so the B rows of one MMA (16 per slot) are one contiguous
-// run with 256-byte row-group stride, and a run of units of one group is one
-// contiguous copy.  Scale atoms are per (group, unit): 512 bytes in the order
-// tcgen05.cp moves them, row n = 16 i + p (slot i, piece p) at byte
-// (n % 32) * 16 + (n / 32) * 4 + block.
+// Pieces: v is carried as P E2M1 vectors with one ue8m0 scale per (piece,
+// 32-block), p_0 at the least scale 2^e0 with max|v| <= 6 2^e0, each next
+// piece encoding the remainder 4x finer, so an element is carried to within
+// 2^(e0 - 2P + 2): 2^-30 of the block scale 2^e0 for P = 16, 2^-14 for P = 8
+// (the E4M3 values have 4 significant bits; those within 2^10 of the block's
+// largest are carried exactly).
 //
-// The kernel roles are those of the slot-major layer kernel (gemv.cu): a
-// weight producer thread filling a ring of shared-memory stages with
-// cp.async.bulk, an activation loader thread, here one MMA-issuing thread (each
-// MMA is N = 16 nt wide), and four epilogue warps that read the accumulator
-// with tcgen05.ld, sum the 16 piece columns of each slot, and finish a job:
-// gate/up -> h = w * silu(g) * u as pieces into the down projection's B
-// operand; down -> o of each slot.  A job split over several CTAs is finished
-// by the CTA holding its first unit, which adds the others' launch-tagged
-// partial sums in CTA order, so results are bitwise reproducible.  Every wait
-// is bounded (2 s); on expiry the kernel records the device-timeout status,
-// stops issuing, waits (bounded) for its copies in flight and frees its TMEM.
+// B operand layout (group order): a slot at sorted position P keeps its pieces
+// at P * pb(K), pb(K) = 64 P bytes per 128-K unit (32 P for a last half unit);
+// a group's slots are consecutive positions, and inside the group, unit u of
+// K holds, per MMA m, the nt slots' (32 P)-byte piece blocks side by side --
+// byte offset  u nt 64P + m nt 32P + i 32P  for slot i -- so the B rows of one
+// MMA (P per slot) are one contiguous run with 256-byte row-group stride, and
+// a run of units of one group is one contiguous copy.  Scale atoms are per
+// (group, unit): 512 bytes in the order tcgen05.cp moves them, row n = P i + p
+// (slot i, piece p) at byte (n % 32) * 16 + (n / 32) * 4 + block.
+//
+// Roles of k_glayer (as in the slot-major layer kernel of gemv.cu): a weight
+// producer thread fills a ring of shared-memory stages (kGCU units each) with
+// cp.async.bulk; an activation loader thread fills a second, shallower ring
+// with the matching pieces; three MMA-issuing warps (one thread each issues at
+// most one tcgen05 instruction per ~150 cycles, several overlap) take one unit
+// of each stage into their own double-buffered accumulators; four epilogue
+// warps read them with tcgen05.ld, add the P piece columns of each slot and
+// the issuers in a fixed order, and finish a job: gate/up -> h = w silu(g) u
+// as pieces into the down projection's B operand; down -> o of each slot.  A
+// job split over several CTAs is finished by the CTA holding its first unit,
+// which adds the others' launch-tagged partial sums in CTA order, so results
+// are bitwise reproducible.  Every wait is bounded (2 s); on expiry the kernel
+// records the device-timeout status, stops issuing, waits (bounded) for its
+// copies in flight and frees its TMEM.
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
 namespace {
 
-constexpr int kNT = kGroupTokens;                            // slots per group
-constexpr int kGCU = 2;                                      // units per stage
-constexpr int kGStages = 6;
-constexpr int kGStageA = kGCU * kUnitCodeBytes;              // 16 KB of weights
-constexpr int kGStageSfa = kGCU * kUnitSfBytes;
-constexpr int kGStageB = kGCU * kNT * kUnitBBytes;           // up to 16 KB of pieces
-constexpr int kGStageSfb = kGCU * kUnitSfBytes;
-constexpr int kGOffSfa = kGStageA;
-constexpr int kGOffB = kGOffSfa + kGStageSfa;
-constexpr int kGOffSfb = kGOffB + kGStageB;
-constexpr int kGStageBytes = kGOffSfb + kGStageSfb;
+constexpr int kNT = kGroupTokens;                            // slots per group, at most
+constexpr int kGIssuers = 3;
+constexpr int kGCU = kGIssuers;                              // units per stage: one per issuer
+constexpr int kGStagesA = 5;                                 // weights (HBM): the deep ring
+constexpr int kGStagesB = 4;                                 // pieces (L2, issued later)
+constexpr int kGUnitB = 2 * kGroupN * 32;                    // B bytes of a unit at N = 64
+constexpr int kGOffSfa = kGCU * kUnitCodeBytes;              // 24 KB of weight codes, then their scale atoms
+constexpr int kGStageA = 26 * 1024;
+constexpr int kGOffSfb = kGCU * kGUnitB;                     // 12 KB of pieces, then their scale atoms
+constexpr int kGStageB = 14 * 1024;
 constexpr int kGTmemCols = 512;
-constexpr int kGAccCols = kNT * kPieces;                     // 128 fp32 columns per accumulator
-constexpr int kGSfCol0 = 2 * kGAccCols;                      // scale atoms after the two accumulators
+constexpr int kGAccCols = kGroupN;                           // 64 fp32 columns per accumulator
+constexpr int kGSfCol0 = kGIssuers * 2 * kGAccCols;          // scale atoms after the accumulators
 constexpr uint64_t kGWaitLimitNs = 2000000000ull;
-constexpr int kGWarpIssuer = 1;
-constexpr int kGWarpEpi0 = 2;                                // epilogue warps 2..5
-constexpr int kGWarpLoader = 6;
+constexpr int kGWarpEpi0 = 1 + kGIssuers;                    // epilogue warps 4..7
+constexpr int kGWarpLoader = kGWarpEpi0 + 4;
 constexpr int kGThreads = (kGWarpLoader + 1) * 32;
-constexpr int kGJobWindow = 32;
 
-static_assert(kGStageBytes % 1024 == 0, "stage alignment");
-static_assert(kGSfCol0 + kGStages * kGCU * 8 <= kGTmemCols, "tensor memory budget");
-static_assert(kGAccCols <= 256 && kGAccCols % 16 == 0, "MMA N");
+#ifdef MOE_G_TRACE
+// debug builds only: event timestamps of one CTA ([role][idx], ns) and per-CTA milestones
+}  // namespace
+__device__ long long g_gtrace[4][8192];
+__device__ long long g_gcta[8][1024];
+__device__ int g_gtrace_cta;
+namespace {
+#define G_TRACE(role, idx)                                                                               \
+    do {                                                                                                 \
+        if ((int)blockIdx.x == g_gtrace_cta && (idx) < 8192) g_gtrace[role][idx] = (long long)globaltimer_ns(); \
+    } while (0)
+#define G_CTA(slot) (g_gcta[slot][blockIdx.x] = (long long)globaltimer_ns())
+#else
+#define G_TRACE(role, idx) \
+    do {                   \
+    } while (0)
+#define G_CTA(slot) \
+    do {            \
+    } while (0)
+#endif
+
+static_assert(kGOffSfa + kGCU * kUnitSfBytes <= kGStageA && kGOffSfb + kGCU * kUnitSfBytes <= kGStageB,
+              "stage sizes");
+static_assert(kGStageA % 1024 == 0 && kGStageB % 1024 == 0, "stage alignment");
+static_assert(kGSfCol0 + kGStagesA * kGCU * 8 <= kGTmemCols, "tensor memory budget");
+static_assert(kGStagesB <= kGStagesA, "the activation ring is the shallower one");
+static_assert(kGroupN % 16 == 0 && kGroupN <= 256, "MMA N");
 // CTAs of k_glayer wait on one another (the down projection needs every h):
 // two must never share an SM, so the shared memory asked for is more than
 // half of an SM's.
@@ -91,16 +122,18 @@ struct GBSrc {
 };
 
 struct GSmem {
-    uint8_t stage[kGStages][kGStageBytes];
-    uint64_t full[kGStages];
-    uint64_t empty[kGStages];
-    uint64_t posted[kGStages];
+    uint8_t stageA[kGStagesA][kGStageA];
+    uint8_t stageB[kGStagesB][kGStageB];
+    uint64_t fullA[kGStagesA];   // the stage's weights landed
+    uint64_t emptyA[kGStagesA];  // the issuers are done with them
+    uint64_t posted[kGStagesA];  // the producer issued them and posted bsrc
+    uint64_t fullB[kGStagesB];   // the stage's pieces landed
+    uint64_t emptyB[kGStagesB];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
-    uint64_t drain;
-    GBSrc bsrc[kGStages];
+    uint64_t drain[kGIssuers];
+    GBSrc bsrc[kGStagesA];
     float comb[2][kNT][kTileRows];
-    GJob jobs[2][kGJobWindow];
     uint32_t tmem;
     int abort;
 };
@@ -111,22 +144,32 @@ struct GPlan {
     int kgt, kg_half, ntiles;
     size_t code_off, sf_off, tile_code_bytes, tile_sf_bytes;
     size_t act_bytes;       // piece bytes of one slot over K
+    int gs, np;             // slots per group (at most), pieces per slot
     int phase;
 };
 
+// Piece bytes of one slot over K with P pieces: 64 P per 128-K unit, 32 P for
+// a last half unit.
+__host__ __device__ inline size_t g_act_bytes(int K, int P)
+{
+    return (size_t)(K / 128) * 64 * P + (size_t)((K % 128) ? 32 * P : 0);
+}
+
 // ----------------------------------------------------------------- pieces
 
-// Pieces of 64 consecutive elements (32-blocks blk0, blk0 + 1 of a unit; lane
-// l holds elements 2l, 2l + 1), computed once: byte[p] = the lane's E2M1 pair
-// of piece p, sc[p] = the piece's scale byte.  Same decomposition as the
-// slot-major path: the first scale is the least e with max|v| <= 6 * 2^e over
-// the 32-block, each next piece encodes the remainder 4x finer.
+// P pieces of 64 consecutive elements (32-blocks blk0, blk0 + 1 of a unit;
+// lane l holds elements 2l, 2l + 1), computed once: byte[p] = the lane's E2M1
+// pair of piece p, sc[p] = the piece's scale byte.  The first scale is the
+// least e with max|v| <= 6 * 2^e over the 32-block (a half-warp), each next
+// piece encodes the remainder 4x finer; the remainders are exact in fp32.
+template <int P>
 struct Pieces64 {
-    uint8_t byte[kPieces];
-    uint8_t sc[kPieces];
+    uint8_t byte[P];
+    uint8_t sc[P];
 };
 
-__device__ __forceinline__ void make_pieces64(float v0, float v1, Pieces64& pc)
+template <int P>
+__device__ __forceinline__ void make_pieces64(float v0, float v1, Pieces64<P>& pc)
 {
     float amax = fmaxf(fabsf(v0), fabsf(v1));
 #pragma unroll
@@ -134,7 +177,7 @@ __device__ __forceinline__ void make_pieces64(float v0, float v1, Pieces64& pc)
     const int s0 = e2m1_scale_byte(amax);
     float r0 = v0, r1 = v1;
 #pragma unroll
-    for (int p = 0; p < kPieces; p++) {
+    for (int p = 0; p < P; p++) {
         const int s = max(s0 - 2 * p, 1);
         const float down = exp2i(127 - s), up = exp2i(s - 127);
         const uint32_t byte = f32x2_to_e2m1x2(r0 * down, r1 * down);
@@ -147,45 +190,50 @@ __device__ __forceinline__ void make_pieces64(float v0, float v1, Pieces64& pc)
 }
 
 // Stores the pieces of slot i of a group: unit points at the group's unit
-// (codes), mstride = nt * 512 (distance between the unit's two MMAs), atom =
+// (codes), mstride = nt * 32P (distance between the unit's two MMAs), atom =
 // the group's scale atom of that unit; blk0 = the span's first 32-block
-// within the unit (0 or 2).
-__device__ __forceinline__ void store_pieces64(const Pieces64& pc, int lane, uint8_t* unit, int mstride,
+// within the unit (0 or 2).  Rows n = P i + p: row group n / 8, row n % 8 of
+// a core matrix (16 bytes = one 32-block of two-element bytes).
+template <int P>
+__device__ __forceinline__ void store_pieces64(const Pieces64<P>& pc, int lane, uint8_t* unit, int mstride,
                                                uint8_t* atom, int i, int blk0)
 {
     const int bu = blk0 + (lane >> 4);             // 32-block within the unit
     const int ib = lane & 15;                      // byte within the block's row
-    uint8_t* rows = unit + (bu >> 1) * mstride + i * kMmaBBytes + (bu & 1) * 128 + ib;
+    uint8_t* rows = unit + (bu >> 1) * mstride + i * 32 * P + (bu & 1) * 128 + ib;
 #pragma unroll
-    for (int p = 0; p < kPieces; p++) rows[(p >> 3) * 256 + (p & 7) * 16] = pc.byte[p];
+    for (int p = 0; p < P; p++) rows[(p >> 3) * 256 + (p & 7) * 16] = pc.byte[p];
     if (ib == 0) {
 #pragma unroll
-        for (int p = 0; p < kPieces; p++) {
-            const int n = 16 * i + p;
+        for (int p = 0; p < P; p++) {
+            const int n = P * i + p;
             atom[(n & 31) * 16 + (n >> 5) * 4 + bu] = pc.sc[p];
         }
     }
 }
 
-// Where slot position P's pieces of unit u (of a K with kgt units) go.
+// Where slot position P's pieces of unit u (of a K with kgt units) go, with
+// groups of up to S = kGroupN / NP slots of NP pieces.
 struct GDst {
     uint8_t* unit;
     uint8_t* atom;
     int mstride, i;
 };
 
+template <int NP>
 __device__ __forceinline__ GDst group_dst(const GroupArgs& a, int e, int P, int u, int kgt, size_t abytes,
                                           uint8_t* codes, uint8_t* atoms)
 {
+    constexpr int S = kGroupN / NP;
     const int rel = P - a.offsets[e];
-    const int q = rel / kNT;
+    const int q = rel / S;
     const int g = a.gbase[e] + q;
-    const int p0 = a.offsets[e] + q * kNT;
-    const int nt = min(kNT, a.counts[e] - q * kNT);
+    const int p0 = a.offsets[e] + q * S;
+    const int nt = min(S, a.counts[e] - q * S);
     GDst d;
-    d.i = rel - q * kNT;
-    d.mstride = nt * kMmaBBytes;
-    d.unit = codes + (size_t)p0 * abytes + (size_t)u * nt * kUnitBBytes;
+    d.i = rel - q * S;
+    d.mstride = nt * 32 * NP;
+    d.unit = codes + (size_t)p0 * abytes + (size_t)u * nt * 64 * NP;
     d.atom = atoms + ((size_t)g * kgt + u) * kUnitSfBytes;
     return d;
 }
@@ -193,8 +241,8 @@ __device__ __forceinline__ GDst group_dst(const GroupArgs& a, int e, int P, int 
 // ------------------------------------------------------------------ k_gprep
 
 // grid (T, ceil(spans / 8)), 256 threads: one warp per 64 elements (bf16
-// mode) or per 128-element block (E4M3 mode); the pieces are made once and
-// stored for each of the token's slots.
+// mode, 16 pieces) or per 128-element block (E4M3 mode, 8 pieces); the
+// pieces are made once and stored for each of the token's slots.
 __global__ void __launch_bounds__(256) k_gprep(GroupArgs a)
 {
     const int t = blockIdx.x;
@@ -231,7 +279,6 @@ __global__ void __launch_bounds__(256) k_gprep(GroupArgs a)
     } else {
         __syncthreads();
     }
-    const size_t abytes = act_bytes(H);
     const int kgt = H / 128;
     auto xval = [&](int i) {
         return a.x_resid ? __bfloat162float(__float2bfloat16_rn(a.x_resid[(size_t)t * H + i] / den))
@@ -239,33 +286,35 @@ __global__ void __launch_bounds__(256) k_gprep(GroupArgs a)
     };
     if (a.act_e4m3) {
         // x quantized to E4M3 under one ue8m0 scale per 128 elements, then the
-        // dequantized values as pieces
+        // dequantized values as 8 pieces
         const int b = blockIdx.y * (blockDim.x >> 5) + warp;      // 128-element block = unit
         if (b >= H / 128) return;
+        const size_t abytes = g_act_bytes(H, 8);
         float v[4];
         for (int hh = 0; hh < 2; hh++)
             for (int e = 0; e < 2; e++) v[2 * hh + e] = xval(b * 128 + hh * 64 + 2 * lane + e);
         const float amax = warp_max(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
         const int s = ue8m0_for_amax_bits(amax);
         for (int hh = 0; hh < 2; hh++) {
-            Pieces64 pc;
-            make_pieces64(e4m3_quant_dequant(v[2 * hh], s), e4m3_quant_dequant(v[2 * hh + 1], s), pc);
+            Pieces64<8> pc;
+            make_pieces64<8>(e4m3_quant_dequant(v[2 * hh], s), e4m3_quant_dequant(v[2 * hh + 1], s), pc);
             for (int kk = 0; kk < a.topk; kk++) {
                 if (s_P[kk] < 0) continue;
-                const GDst d = group_dst(a, s_e[kk], s_P[kk], b, kgt, abytes, a.xg, a.xgsf);
-                store_pieces64(pc, lane, d.unit, d.mstride, d.atom, d.i, 2 * hh);
+                const GDst d = group_dst<8>(a, s_e[kk], s_P[kk], b, kgt, abytes, a.xg, a.xgsf);
+                store_pieces64<8>(pc, lane, d.unit, d.mstride, d.atom, d.i, 2 * hh);
             }
         }
         return;
     }
     const int b = blockIdx.y * (blockDim.x >> 5) + warp;          // 64-element span
     if (b >= H / 64) return;
-    Pieces64 pc;
-    make_pieces64(xval(b * 64 + 2 * lane), xval(b * 64 + 2 * lane + 1), pc);
+    const size_t abytes = g_act_bytes(H, 16);
+    Pieces64<16> pc;
+    make_pieces64<16>(xval(b * 64 + 2 * lane), xval(b * 64 + 2 * lane + 1), pc);
     for (int kk = 0; kk < a.topk; kk++) {
         if (s_P[kk] < 0) continue;
-        const GDst d = group_dst(a, s_e[kk], s_P[kk], b / 2, kgt, abytes, a.xg, a.xgsf);
-        store_pieces64(pc, lane, d.unit, d.mstride, d.atom, d.i, 2 * (b & 1));
+        const GDst d = group_dst<16>(a, s_e[kk], s_P[kk], b / 2, kgt, abytes, a.xg, a.xgsf);
+        store_pieces64<16>(pc, lane, d.unit, d.mstride, d.atom, d.i, 2 * (b & 1));
     }
 }
 
@@ -278,6 +327,7 @@ __global__ void __launch_bounds__(256) k_gprep(GroupArgs a)
 struct GRange {
     uint32_t u0, u1, j0, jlast;
     int G;                  // CTAs that take part in this projection
+    int ngroups;            // groups of the layer (from the route kernel)
     bool empty;
 };
 
@@ -288,9 +338,10 @@ __device__ __forceinline__ int g_cta_of_unit(long long U, int G, long long x)
     return (int)(((x + 1) * G - 1) / U);
 }
 
-__device__ __forceinline__ GRange g_cta_range(long long U, int grid, int kgt)
+__device__ __forceinline__ GRange g_cta_range(long long U, int grid, int kgt, int ngroups)
 {
     GRange r;
+    r.ngroups = ngroups;
     const int G = (int)(U < grid ? U : grid);
     const int c = (int)blockIdx.x < G ? (int)blockIdx.x : G;
     r.G = G;
@@ -332,54 +383,75 @@ struct GWalk {
     }
 };
 
+// Chunks of a CTA's range (as GWalk cuts it: never across a job, at most
+// kGCU units), in closed form.
 __device__ __forceinline__ int g_count_chunks(int kgt, const GRange& r)
 {
-    GWalk wk(kgt, r);
-    int n = 0;
-    while (wk.u < wk.u1) {
-        bool nj;
-        wk.advance(wk.chunk(), nj);
-        n++;
+    if (r.empty) return 0;
+    const uint32_t K = (uint32_t)kgt, CU = (uint32_t)kGCU;
+    const uint32_t fj = (r.u0 / K + 1) * K;            // end of the first job
+    if (r.u1 <= fj) return (int)((r.u1 - r.u0 + CU - 1) / CU);
+    const uint32_t whole = (r.u1 - fj) / K, rest = (r.u1 - fj) % K;
+    return (int)((fj - r.u0 + CU - 1) / CU + whole * ((K + CU - 1) / CU) + (rest + CU - 1) / CU);
+}
+
+// Walks the jobs of one projection in order.  Jobs are ordered (expert,
+// tile, group of the expert): expert e's jobs are [ntiles gb, ntiles (gb +
+// ng)), so job / ntiles is one of its groups.  Moving to the next job is
+// arithmetic; only an expert boundary reads the next expert's group record
+// and weight pointers.
+struct GCursor {
+    int tile, c;                 // weight tile, group within the expert
+    int gb, ng, cnt, p0e;        // the expert's first group, groups, slots, first sorted position
+    int ngroups, gs;
+    const uint8_t* cb;
+    const uint8_t* sb;
+    bool ok;
+
+    __device__ void enter(const GroupArgs& a, int gl)
+    {
+        const GroupInfo gi = a.groups[gl];
+        gb = gi.gb;
+        ng = gi.ng;
+        cnt = gi.cnt;
+        p0e = gi.p0 - (gl - gi.gb) * gs;
+        cb = a.codes[gi.e];
+        sb = a.scales[gi.e];
+        ok = cb && sb && ((reinterpret_cast<uintptr_t>(cb) | reinterpret_cast<uintptr_t>(sb)) & 15) == 0;
     }
-    return n;
-}
-
-// Job j of a projection: jobs are ordered (expert, tile, group of the
-// expert); the expert's jobs are [ntiles gb, ntiles (gb + ng)), so j / ntiles
-// is one of its groups.
-template <int PHASE>
-__device__ GJob gjob_info(const GroupArgs& a, const GPlan& p, uint32_t job)
-{
-    GJob j;
-    const int gl = (int)(job / (uint32_t)p.ntiles);
-    const GroupInfo gi = a.groups[gl];
-    const uint32_t local = job - (uint32_t)gi.gb * (uint32_t)p.ntiles;
-    j.tile = (int)(local / (uint32_t)gi.ng);
-    const int g = gi.gb + (int)(local % (uint32_t)gi.ng);
-    const GroupInfo gg = g == gl ? gi : a.groups[g];
-    j.nt = gg.nt;
-    j.p0 = gg.p0;
-    j.g = g;
-    j.B = (PHASE == 0 ? a.xg : a.hg) + (size_t)gg.p0 * p.act_bytes;
-    j.Bsf = (PHASE == 0 ? a.xgsf : a.hgsf) + (size_t)g * p.kgt * kUnitSfBytes;
-    const uint8_t* cb = a.codes[gg.e];
-    const uint8_t* sb = a.scales[gg.e];
-    j.ok = cb && sb && ((reinterpret_cast<uintptr_t>(cb) | reinterpret_cast<uintptr_t>(sb)) & 15) == 0;
-    j.code = j.ok ? cb + p.code_off + (size_t)j.tile * p.tile_code_bytes : nullptr;
-    j.sf = j.ok ? sb + p.sf_off + (size_t)j.tile * p.tile_sf_bytes : nullptr;
-    return j;
-}
-
-template <int PHASE>
-__device__ __forceinline__ GJob gjob_at(const GroupArgs& a, const GPlan& p, const GRange& r, GSmem& sm,
-                                        uint32_t job)
-{
-    const uint32_t d = job - r.j0;
-    if (d < (uint32_t)kGJobWindow) return sm.jobs[PHASE][d];
-    const GJob j = gjob_info<PHASE>(a, p, job);
-    if (!j.ok) atomicOr(a.status, kStatusBadIndex);
-    return j;
-}
+    __device__ void init(const GroupArgs& a, const GPlan& p, uint32_t job, int ngroups_)
+    {
+        ngroups = ngroups_;
+        gs = p.gs;
+        enter(a, (int)(job / (uint32_t)p.ntiles));
+        const uint32_t local = job - (uint32_t)gb * (uint32_t)p.ntiles;
+        tile = (int)(local / (uint32_t)ng);
+        c = (int)(local % (uint32_t)ng);
+    }
+    __device__ void next(const GroupArgs& a, const GPlan& p)
+    {
+        if (++c < ng) return;
+        c = 0;
+        if (++tile < p.ntiles) return;
+        tile = 0;
+        if (gb + ng < ngroups) enter(a, gb + ng);
+    }
+    template <int PHASE>
+    __device__ GJob job(const GroupArgs& a, const GPlan& p) const
+    {
+        GJob j;
+        j.tile = tile;
+        j.g = gb + c;
+        j.p0 = p0e + c * gs;
+        j.nt = min(gs, cnt - c * gs);
+        j.B = (PHASE == 0 ? a.xg : a.hg) + (size_t)j.p0 * p.act_bytes;
+        j.Bsf = (PHASE == 0 ? a.xgsf : a.hgsf) + (size_t)j.g * p.kgt * kUnitSfBytes;
+        j.ok = ok;
+        j.code = ok ? cb + p.code_off + (size_t)tile * p.tile_code_bytes : nullptr;
+        j.sf = ok ? sb + p.sf_off + (size_t)tile * p.tile_sf_bytes : nullptr;
+        return j;
+    }
+};
 
 __device__ __forceinline__ uint32_t g_ld_acquire_u32(const int* p)
 {
@@ -413,56 +485,71 @@ __device__ bool gproduce(const GroupArgs& a, const GPlan& p, const GRange& r, GS
 {
     if (r.empty) return true;
     GWalk wk(p.kgt, r);
-    GJob ji = gjob_at<PHASE>(a, p, r, sm, wk.job);
+    GCursor cur;
+    cur.init(a, p, wk.job, r.ngroups);
+    GJob ji = cur.job<PHASE>(a, p);
+    if (!ji.ok) atomicOr(a.status, kStatusBadIndex);
     while (wk.u < wk.u1) {
         const uint32_t nun = wk.chunk();
         const bool has_half = p.kg_half && (wk.kg + nun == wk.kgt);
         const uint32_t nfull = nun - (has_half ? 1u : 0u);
         const uint32_t cb = nfull * kUnitCodeBytes + (has_half ? kMmaCodeBytes : 0);
         const uint32_t sb = nun * kUnitSfBytes;
-        const uint32_t bb = (uint32_t)ji.nt * (nfull * kUnitBBytes + (has_half ? kMmaBBytes : 0));
+        const uint32_t ub = 64u * (uint32_t)p.np;                 // piece bytes of a slot per unit
+        const uint32_t bb = (uint32_t)ji.nt * (nfull * ub + (has_half ? ub / 2 : 0));
         const uint32_t bsb = nun * kUnitSfBytes;
-        const int s = n % kGStages;
-        if (n >= kGStages &&
-            !mbar_wait_or_abort(&sm.empty[s], ((n / kGStages) & 1) ^ 1, &sm.abort, kGWaitLimitNs)) {
+        const int s = n % kGStagesA;
+        if (n >= kGStagesA &&
+            !mbar_wait_or_abort(&sm.emptyA[s], ((n / kGStagesA) & 1) ^ 1, &sm.abort, kGWaitLimitNs)) {
             g_set_abort(a, sm);
             return false;
         }
-        uint8_t* stg = sm.stage[s];
+        uint8_t* stg = sm.stageA[s];
         if (ji.ok) {
-            mbar_arrive_expect_tx(&sm.full[s], cb + sb + bb + bsb);
-            bulk_g2s(stg, ji.code + (size_t)wk.kg * kUnitCodeBytes, cb, &sm.full[s]);
-            bulk_g2s(stg + kGOffSfa, ji.sf + (size_t)wk.kg * kUnitSfBytes, sb, &sm.full[s]);
-            sm.bsrc[s] = GBSrc{ji.B + (size_t)wk.kg * ji.nt * kUnitBBytes, ji.Bsf + (size_t)wk.kg * kUnitSfBytes,
-                               bb, bsb, PHASE};
+            mbar_arrive_expect_tx(&sm.fullA[s], cb + sb);
+            bulk_g2s(stg, ji.code + (size_t)wk.kg * kUnitCodeBytes, cb, &sm.fullA[s]);
+            bulk_g2s(stg + kGOffSfa, ji.sf + (size_t)wk.kg * kUnitSfBytes, sb, &sm.fullA[s]);
+            sm.bsrc[s] = GBSrc{ji.B + (size_t)wk.kg * ji.nt * ub, ji.Bsf + (size_t)wk.kg * kUnitSfBytes, bb, bsb,
+                               PHASE};
         } else {
-            mbar_arrive(&sm.full[s]);      // an empty stage: nothing to multiply
+            mbar_arrive(&sm.fullA[s]);     // an empty stage: nothing to multiply
             sm.bsrc[s].B = nullptr;
         }
         mbar_arrive(&sm.posted[s]);        // release: bsrc is visible to the loader
+        G_TRACE(0, n);
         bool nj;
         wk.advance(nun, nj);
         n++;
-        if (nj && wk.u < wk.u1) ji = gjob_at<PHASE>(a, p, r, sm, wk.job);
+        if (nj && wk.u < wk.u1) {
+            cur.next(a, p);
+            ji = cur.job<PHASE>(a, p);
+            if (!ji.ok) atomicOr(a.status, kStatusBadIndex);
+        }
     }
     return true;
 }
 
-// Issues the activation copies of every posted stage, in order: x's pieces
-// after the previous kernel (PDL), h's once the grid-wide count of finished
-// h tiles reaches h_target.  A posted stage's copies are always issued, even
-// after a timeout, so that every transaction count completes.
+// Issues the activation copies of every posted stage, in order, into the
+// activation ring: x's pieces after the previous kernel (PDL), h's once the
+// grid-wide count of finished h tiles reaches h_target.  Before exiting it
+// waits (bounded) for its own copies in flight.
 __device__ void gload_b(const GroupArgs& a, int nchunks, uint32_t h_target, GSmem& sm)
 {
     bool pdl_done = false, h_done = false;
-    for (int n = 0; n < nchunks; n++) {
-        const int s = n % kGStages;
-        if (!mbar_wait_or_abort(&sm.posted[s], (n / kGStages) & 1, &sm.abort, kGWaitLimitNs)) {
+    int n = 0;
+    for (; n < nchunks; n++) {
+        const int s = n % kGStagesA, sb = n % kGStagesB;
+        if (!mbar_wait_or_abort(&sm.posted[s], (n / kGStagesA) & 1, &sm.abort, kGWaitLimitNs) ||
+            (n >= kGStagesB &&
+             !mbar_wait_or_abort(&sm.emptyB[sb], ((n / kGStagesB) & 1) ^ 1, &sm.abort, kGWaitLimitNs))) {
             g_set_abort(a, sm);
-            return;
+            break;
         }
         const GBSrc q = sm.bsrc[s];
-        if (!q.B) continue;
+        if (!q.B) {
+            mbar_arrive(&sm.fullB[sb]);    // nothing to multiply in this stage
+            continue;
+        }
         if (!pdl_done) {
             pdl_wait();
             pdl_done = true;
@@ -474,15 +561,20 @@ __device__ void gload_b(const GroupArgs& a, int nchunks, uint32_t h_target, GSme
                 while (!(ok = g_ld_acquire_u32(a.sync) >= h_target))
                     if (*(volatile int*)&sm.abort || globaltimer_ns() - t0 > kGWaitLimitNs) break;
             }
+            G_CTA(7);
             // h was written with generic stores; the copies read it through the async proxy
             asm volatile("fence.proxy.async.global;" ::: "memory");
             if (!ok) g_set_abort(a, sm);
             h_done = true;
         }
-        uint8_t* stg = sm.stage[s];
-        bulk_g2s(stg + kGOffB, q.B, q.nb, &sm.full[s]);
-        bulk_g2s(stg + kGOffSfb, q.Bsf, q.nsf, &sm.full[s]);
+        uint8_t* stg = sm.stageB[sb];
+        mbar_arrive_expect_tx(&sm.fullB[sb], q.nb + q.nsf);
+        bulk_g2s(stg, q.B, q.nb, &sm.fullB[sb]);
+        bulk_g2s(stg + kGOffSfb, q.Bsf, q.nsf, &sm.fullB[sb]);
     }
+    // no copy may still be in flight into this CTA's memory at exit
+    for (int m = n > kGStagesB ? n - kGStagesB : 0; m < n; m++)
+        mbar_wait_bounded(&sm.fullB[m % kGStagesB], (m / kGStagesB) & 1, kGWaitLimitNs);
 }
 
 struct GIss {
@@ -491,19 +583,25 @@ struct GIss {
     bool abort;
 };
 
-// The one MMA-issuing thread: per unit, the two scale atoms to TMEM and one
-// (or, for a half unit, no second) MMA of N = 16 nt per 64-K step.
+// Issuer ii takes unit ii of every stage: its two scale atoms to TMEM, then
+// one MMA per 64-K step (two per unit, one for a half unit) of N = np nt
+// (rounded up to a multiple of 16; the extra columns are never read) into its
+// own double-buffered accumulator.
 template <int PHASE>
-__device__ void gissue(const GroupArgs& a, const GPlan& p, const GRange& r, GSmem& sm, uint32_t tmem, GIss& is)
+__device__ void gissue(const GroupArgs& a, const GPlan& p, const GRange& r, GSmem& sm, uint32_t tmem, int ii,
+                       GIss& is)
 {
     if (r.empty) return;
     GWalk wk(p.kgt, r);
-    GJob ji = gjob_at<PHASE>(a, p, r, sm, wk.job);
-    bool any = false;               // the accumulator holds this job's sum
+    GCursor cur;
+    cur.init(a, p, wk.job, r.ngroups);
+    GJob ji = cur.job<PHASE>(a, p);
+    bool any = false;               // this issuer's accumulator holds part of this job
     bool job_start = true;
+    const uint32_t ub = 64u * (uint32_t)p.np;
     while (wk.u < wk.u1) {
         const uint32_t nun = wk.chunk();
-        const int s = is.n % kGStages;
+        const int s = is.n % kGStagesA, sbi = is.n % kGStagesB;
         if (job_start) {
             // the epilogue must have read this accumulator's previous job
             if (!is.abort && is.use[is.buf] > 0 &&
@@ -513,38 +611,42 @@ __device__ void gissue(const GroupArgs& a, const GPlan& p, const GRange& r, GSme
             }
             job_start = false;
         }
-        if (!is.abort && !mbar_wait_or_abort(&sm.full[s], (is.n / kGStages) & 1, &sm.abort, kGWaitLimitNs)) {
+        if (!is.abort &&
+            (!mbar_wait_or_abort(&sm.fullA[s], (is.n / kGStagesA) & 1, &sm.abort, kGWaitLimitNs) ||
+             !mbar_wait_or_abort(&sm.fullB[sbi], (is.n / kGStagesB) & 1, &sm.abort, kGWaitLimitNs))) {
             g_set_abort(a, sm);
             is.abort = true;
         }
-        if (!is.abort && ji.ok) {
+        if (ii == 0) G_TRACE(1, is.n);
+        if (!is.abort && ji.ok && (uint32_t)ii < nun) {
             tc_fence_after();
-            const uint8_t* st = sm.stage[s];
+            const uint8_t* st = sm.stageA[s];
+            const uint8_t* sbs = sm.stageB[sbi];
             const uint32_t nt = (uint32_t)ji.nt;
-            const uint32_t idesc = mxf4_idesc(kTileRows, 16 * nt);
-            for (uint32_t ii = 0; ii < nun; ii++) {
-                const uint32_t col = tmem + kGSfCol0 + (uint32_t)(s * kGCU + ii) * 8;
-                tc_cp_sf(col, umma_desc(smem_u32(st + kGOffSfa + ii * kUnitSfBytes), 16, 128));
-                tc_cp_sf(col + 4, umma_desc(smem_u32(st + kGOffSfb + ii * kUnitSfBytes), 16, 128));
-                const bool half = p.kg_half && (wk.kg + ii == wk.kgt - 1);
-                for (uint32_t m = 0; m < (half ? 1u : 2u); m++) {
-                    const uint64_t ad =
-                        umma_desc(smem_u32(st + ii * kUnitCodeBytes + m * kMmaCodeBytes), 128, 256);
-                    const uint64_t bd = umma_desc(
-                        smem_u32(st + kGOffB + ii * nt * kUnitBBytes + m * nt * kMmaBBytes), 128, 256);
-                    tc_mma_mxf4(tmem + (uint32_t)is.buf * kGAccCols, ad, bd, mxf4_idesc_sf(idesc, 2 * m), col,
-                                col + 4, any ? 1u : 0u);
-                    any = true;
-                }
+            const uint32_t idesc = mxf4_idesc(kTileRows, ((uint32_t)p.np * nt + 15u) & ~15u);
+            const uint32_t col = tmem + kGSfCol0 + (uint32_t)(s * kGCU + ii) * 8;
+            tc_cp_sf(col, umma_desc(smem_u32(st + kGOffSfa + ii * kUnitSfBytes), 16, 128));
+            tc_cp_sf(col + 4, umma_desc(smem_u32(sbs + kGOffSfb + ii * kUnitSfBytes), 16, 128));
+            const bool half = p.kg_half && (wk.kg + (uint32_t)ii == wk.kgt - 1);
+            for (uint32_t m = 0; m < (half ? 1u : 2u); m++) {
+                const uint64_t ad = umma_desc(smem_u32(st + ii * kUnitCodeBytes + m * kMmaCodeBytes), 128, 256);
+                const uint64_t bd = umma_desc(smem_u32(sbs + ii * nt * ub + m * nt * (ub / 2)), 128, 256);
+                tc_mma_mxf4(tmem + (uint32_t)(ii * 2 + is.buf) * kGAccCols, ad, bd, mxf4_idesc_sf(idesc, 2 * m),
+                            col, col + 4, any ? 1u : 0u);
+                any = true;
             }
         }
-        tc_commit(&sm.empty[s]);           // the stage is consumed once these MMAs are done
+        tc_commit(&sm.emptyA[s]);          // this issuer's part of the stage is consumed
+        tc_commit(&sm.emptyB[sbi]);
         bool nj;
         const bool jend = wk.advance(nun, nj);
         is.n++;
-        if (nj && wk.u < wk.u1) ji = gjob_at<PHASE>(a, p, r, sm, wk.job);
+        if (nj && wk.u < wk.u1) {
+            cur.next(a, p);
+            ji = cur.job<PHASE>(a, p);
+        }
         if (jend) {
-            tc_commit(&sm.acc_full[is.buf]);   // the accumulator is final
+            tc_commit(&sm.acc_full[is.buf]);   // this issuer's accumulator is final
             is.use[is.buf]++;
             is.buf ^= 1;
             any = false;
@@ -556,8 +658,9 @@ __device__ void gissue(const GroupArgs& a, const GPlan& p, const GRange& r, GSme
 // ------------------------------------------------------------------ epilogue
 
 // Gate/up job (group, tile), slot i -> the 64 values h = w * silu(g) * u of
-// that slot as pieces into the down projection's B operand, by one warp; then
-// the grid-wide count of finished h tiles grows by the tiles written.
+// that slot as NP pieces into the down projection's B operand, by one warp;
+// then the grid-wide count of finished h tiles grows by the tiles written.
+template <int NP>
 __device__ void gfinalize_gate_up(const GroupArgs& a, const GPlan& p, const GJob& jb, int i, const float* comb,
                                   int lane)
 {
@@ -566,11 +669,11 @@ __device__ void gfinalize_gate_up(const GroupArgs& a, const GPlan& p, const GJob
     const float2 g = *reinterpret_cast<const float2*>(comb + 2 * lane);
     const float2 u = *reinterpret_cast<const float2*>(comb + 64 + 2 * lane);
     float h0 = silu(g.x) * u.x, h1 = silu(g.y) * u.y;
-    const size_t abytes = act_bytes(a.I);
+    const size_t abytes = g_act_bytes(a.I, NP);
     const int kgt = (a.I + 127) / 128;
-    uint8_t* unit = a.hg + (size_t)jb.p0 * abytes + (size_t)(tile / 2) * jb.nt * kUnitBBytes;
+    uint8_t* unit = a.hg + (size_t)jb.p0 * abytes + (size_t)(tile / 2) * jb.nt * 64 * NP;
     uint8_t* atom = a.hgsf + ((size_t)jb.g * kgt + tile / 2) * kUnitSfBytes;
-    const int mstride = jb.nt * kMmaBBytes;
+    const int mstride = jb.nt * 32 * NP;
     int done = 1;                         // h tiles whose pieces this call writes
     if (a.act_e4m3) {
         // h is quantized to E4M3 per 128 along I (tiles 2b, 2b + 1; a last block
@@ -601,14 +704,14 @@ __device__ void gfinalize_gate_up(const GroupArgs& a, const GPlan& p, const GJob
         h0 = e4m3_quant_dequant(h0, s);
         h1 = e4m3_quant_dequant(h1, s);
         if (pair) {
-            Pieces64 po;
-            make_pieces64(e4m3_quant_dequant(o0, s) * w, e4m3_quant_dequant(o1, s) * w, po);
-            store_pieces64(po, lane, unit, mstride, atom, i, 2 * ((tile ^ 1) & 1));
+            Pieces64<NP> po;
+            make_pieces64<NP>(e4m3_quant_dequant(o0, s) * w, e4m3_quant_dequant(o1, s) * w, po);
+            store_pieces64<NP>(po, lane, unit, mstride, atom, i, 2 * ((tile ^ 1) & 1));
         }
     }
-    Pieces64 pc;
-    make_pieces64(h0 * w, h1 * w, pc);
-    store_pieces64(pc, lane, unit, mstride, atom, i, 2 * (tile & 1));
+    Pieces64<NP> pc;
+    make_pieces64<NP>(h0 * w, h1 * w, pc);
+    store_pieces64<NP>(pc, lane, unit, mstride, atom, i, 2 * (tile & 1));
     // the down projection reads these with bulk copies (async proxy), in other CTAs
     asm volatile("fence.proxy.async.global;" ::: "memory");
     __syncwarp();
@@ -669,13 +772,21 @@ __device__ void gepilogue(const GroupArgs& a, const GPlan& p, const GRange& r, G
     const int row = quad * 32 + lane;                      // accumulator row of this thread
     const int G = r.G;
     GWalk wk(p.kgt, r);
-    GJob ji = gjob_at<PHASE>(a, p, r, sm, wk.job);
+    GCursor cs;
+    cs.init(a, p, wk.job, r.ngroups);
+    GJob ji = cs.job<PHASE>(a, p);
+    uint32_t mask = 0;                                     // issuers that accumulated into this job
     while (wk.u < wk.u1) {
         const uint32_t job = wk.job;
         const GJob cur = ji;
+        const uint32_t nun = wk.chunk();
+        if (cur.ok) mask |= (1u << nun) - 1u;
         bool nj;
-        const bool jend = wk.advance(wk.chunk(), nj);
-        if (nj && wk.u < wk.u1) ji = gjob_at<PHASE>(a, p, r, sm, wk.job);
+        const bool jend = wk.advance(nun, nj);
+        if (nj && wk.u < wk.u1) {
+            cs.next(a, p);
+            ji = cs.job<PHASE>(a, p);
+        }
         if (!jend) continue;
 
         // --------------------------------------------- end of (this CTA's part of) a job
@@ -699,16 +810,31 @@ __device__ void gepilogue(const GroupArgs& a, const GPlan& p, const GRange& r, G
         tc_fence_after();
         float v[kNT];
 #pragma unroll
-        for (int i = 0; i < kNT; i++) {
-            v[i] = 0.0f;
-            if (ready && cur.ok && i < nt) {
-                float acc[16];
-                tc_ld16(tmem + (uint32_t)buf * kGAccCols + (uint32_t)(i * kPieces) + ((uint32_t)(quad * 32) << 16),
-                        acc);
+        for (int i = 0; i < kNT; i++) v[i] = 0.0f;
+        if (ready) {
+            // slot i: the sum of its np piece columns, issuers in order
 #pragma unroll
-                for (int c = 0; c < kPieces; c++) v[i] += acc[c];
+            for (int ii = 0; ii < kGIssuers; ii++) {
+                if (!((mask >> ii) & 1u)) continue;
+                const uint32_t acc0 = tmem + (uint32_t)(ii * 2 + buf) * kGAccCols + ((uint32_t)(quad * 32) << 16);
+#pragma unroll
+                for (int i = 0; i < kNT; i++) {
+                    if (i >= nt) break;
+                    if (p.np == 8) {
+                        float acc[8];
+                        tc_ld8(acc0 + (uint32_t)(i * 8), acc);
+#pragma unroll
+                        for (int c = 0; c < 8; c++) v[i] += acc[c];
+                    } else {
+                        float acc[16];
+                        tc_ld16(acc0 + (uint32_t)(i * 16), acc);
+#pragma unroll
+                        for (int c = 0; c < 16; c++) v[i] += acc[c];
+                    }
+                }
             }
         }
+        mask = 0;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);
@@ -730,13 +856,18 @@ __device__ void gepilogue(const GroupArgs& a, const GPlan& p, const GRange& r, G
         }
 #pragma unroll
         for (int i = 0; i < kNT; i++) v[i] += pacc[i];
+        if (quad == 0 && lane == 0) G_TRACE(2, es.use[0] + es.use[1]);
         if (PHASE == 0) {
             float(*comb)[kTileRows] = sm.comb[es.cb];
 #pragma unroll
             for (int i = 0; i < kNT; i++)
                 if (i < nt) comb[i][row] = v[i];
             named_sync(1, 128);
-            for (int i = quad; i < nt; i += 4) gfinalize_gate_up(a, p, cur, i, comb[i], lane);
+            for (int i = quad; i < nt; i += 4) {
+                if (p.np == 8) gfinalize_gate_up<8>(a, p, cur, i, comb[i], lane);
+                else gfinalize_gate_up<16>(a, p, cur, i, comb[i], lane);
+            }
+            if (quad == 0 && lane == 0) G_TRACE(3, es.use[0] + es.use[1]);
             es.cb ^= 1;
         } else {
             // o of each slot: rows tile*128 .. +127 of the down output
@@ -761,37 +892,28 @@ __global__ void __launch_bounds__(kGThreads, 1) k_glayer(GroupArgs a, GPlan p0, 
     const int G = gridDim.x;
     const long long ngroups = a.gbase[a.E];
     const long long U0 = ngroups * p0.ntiles * p0.kgt, U1 = ngroups * p1.ntiles * p1.kgt;
-    const GRange r0 = g_cta_range(U0, G, p0.kgt), r1 = g_cta_range(U1, G, p1.kgt);
+    const GRange r0 = g_cta_range(U0, G, p0.kgt, (int)ngroups), r1 = g_cta_range(U1, G, p1.kgt, (int)ngroups);
     const uint32_t h_target = (uint32_t)a.offsets[a.E] * (uint32_t)p0.ntiles;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kGStages; s++) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], 1);
+        for (int s = 0; s < kGStagesA; s++) {
+            mbar_init(&sm.fullA[s], 1);
+            mbar_init(&sm.emptyA[s], kGIssuers);
             mbar_init(&sm.posted[s], 1);
         }
+        for (int s = 0; s < kGStagesB; s++) {
+            mbar_init(&sm.fullB[s], 1);
+            mbar_init(&sm.emptyB[s], kGIssuers);
+        }
         for (int b = 0; b < 2; b++) {
-            mbar_init(&sm.acc_full[b], 1);
+            mbar_init(&sm.acc_full[b], kGIssuers);
             mbar_init(&sm.acc_empty[b], 4);
         }
-        mbar_init(&sm.drain, 1);
+        for (int i = 0; i < kGIssuers; i++) mbar_init(&sm.drain[i], 1);
         sm.abort = 0;
         mbar_fence_init();
     }
-    if (warp == 0) {
-        // resolve the CTA's first jobs of both projections in parallel
-        if (!r0.empty && r0.j0 + lane <= r0.jlast) {
-            const GJob j = gjob_info<0>(a, p0, r0.j0 + lane);
-            sm.jobs[0][lane] = j;
-            if (!j.ok) atomicOr(a.status, kStatusBadIndex);
-        }
-        if (!r1.empty && r1.j0 + lane <= r1.jlast) {
-            const GJob j = gjob_info<1>(a, p1, r1.j0 + lane);
-            sm.jobs[1][lane] = j;
-            if (!j.ok) atomicOr(a.status, kStatusBadIndex);
-        }
-    }
-    if (warp == kGWarpIssuer) tmem_alloc(&sm.tmem, kGTmemCols);
+    if (warp == 1) tmem_alloc(&sm.tmem, kGTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -801,10 +923,14 @@ __global__ void __launch_bounds__(kGThreads, 1) k_glayer(GroupArgs a, GPlan p0, 
     if (warp == 0) {
         if (lane == 0) {
             int n = 0;
-            if (gproduce<0>(a, p0, r0, sm, n)) gproduce<1>(a, p1, r1, sm, n);
+            G_CTA(0);
+            const bool ok0 = gproduce<0>(a, p0, r0, sm, n);
+            G_CTA(1);
+            if (ok0) gproduce<1>(a, p1, r1, sm, n);
+            G_CTA(2);
             // no copy may still be in flight into this CTA's memory at exit
-            for (int m = n > kGStages ? n - kGStages : 0; m < n; m++)
-                mbar_wait_bounded(&sm.full[m % kGStages], (m / kGStages) & 1, kGWaitLimitNs);
+            for (int m = n > kGStagesA ? n - kGStagesA : 0; m < n; m++)
+                mbar_wait_bounded(&sm.fullA[m % kGStagesA], (m / kGStagesA) & 1, kGWaitLimitNs);
         }
         return;
     }
@@ -812,18 +938,20 @@ __global__ void __launch_bounds__(kGThreads, 1) k_glayer(GroupArgs a, GPlan p0, 
         if (lane == 0) gload_b(a, g_count_chunks(p0.kgt, r0) + g_count_chunks(p1.kgt, r1), h_target, sm);
         return;
     }
-    if (warp == kGWarpIssuer) {
+    if (warp < kGWarpEpi0) {
         if (lane == 0) {
             GIss is;
             is.n = 0;
             is.buf = 0;
             is.use[0] = is.use[1] = 0;
             is.abort = false;
-            gissue<0>(a, p0, r0, sm, tmem, is);
-            gissue<1>(a, p1, r1, sm, tmem, is);
+            gissue<0>(a, p0, r0, sm, tmem, warp - 1, is);
+            if (warp == 1) G_CTA(3);
+            gissue<1>(a, p1, r1, sm, tmem, warp - 1, is);
+            if (warp == 1) G_CTA(4);
             // none of this thread's MMAs may be in flight when TMEM is freed
-            tc_commit(&sm.drain);
-            mbar_wait_bounded(&sm.drain, 0, kGWaitLimitNs);
+            tc_commit(&sm.drain[warp - 1]);
+            mbar_wait_bounded(&sm.drain[warp - 1], 0, kGWaitLimitNs);
         }
         __syncwarp();
     } else {
@@ -834,7 +962,9 @@ __global__ void __launch_bounds__(kGThreads, 1) k_glayer(GroupArgs a, GPlan p0, 
         es.use[0] = es.use[1] = 0;
         es.tag = 1u + (g_ld_acquire_u32(a.sync + 2) & 0x3FFFFFFFu);   // never 0, the cleared value
         gepilogue<0>(a, p0, r0, sm, tmem, U0, warp & 3, lane, es);
+        if (warp == kGWarpEpi0 && lane == 0) G_CTA(5);
         gepilogue<1>(a, p1, r1, sm, tmem, U1, warp & 3, lane, es);
+        if (warp == kGWarpEpi0 && lane == 0) G_CTA(6);
         if (warp == kGWarpEpi0 && lane == 0) {
             // the last CTA to finish resets the layer's counters for the next launch
             __threadfence();
@@ -849,9 +979,9 @@ __global__ void __launch_bounds__(kGThreads, 1) k_glayer(GroupArgs a, GPlan p0, 
     }
     // the issuer and epilogue warps meet here before the tensor memory is released
     tc_fence_before();
-    named_sync(2, 5 * 32);
+    named_sync(2, (kGIssuers + 4) * 32);
     tc_fence_after();
-    if (warp == kGWarpIssuer) tmem_dealloc(tmem, kGTmemCols);
+    if (warp == 1) tmem_dealloc(tmem, kGTmemCols);
 }
 
 // --------------------------------------------------------------- k_gcombine
@@ -925,7 +1055,9 @@ GPlan gplan(const GroupArgs& a, int phase)
     p.tile_sf_bytes = L.tile_sf_bytes();
     p.code_off = phase == 0 ? E.gu_code_off : E.dn_code_off;
     p.sf_off = phase == 0 ? E.gu_sf_off : E.dn_sf_off;
-    p.act_bytes = act_bytes(phase == 0 ? a.H : a.I);
+    p.np = group_pieces(a.act_e4m3 != 0);
+    p.gs = group_slots(a.act_e4m3 != 0);
+    p.act_bytes = g_act_bytes(phase == 0 ? a.H : a.I, p.np);
     p.phase = phase;
     return p;
 }
@@ -938,7 +1070,7 @@ GroupWorkspaceSizes group_workspace_sizes(int T, int topk, int E, int H, int I, 
 {
     GroupWorkspaceSizes s{};
     const size_t n = (size_t)T * topk;
-    const size_t G = (size_t)max_groups((int)n, E);
+    const size_t G = (size_t)max_groups((int)n, E, group_slots(false));
     s.counts = (size_t)E * 4;
     s.offsets = (size_t)(E + 1) * 4;
     s.perm = n * 4;
@@ -969,7 +1101,9 @@ cudaError_t launch_group_layer(const GroupArgs& a0, cudaStream_t s, bool pdl, Pr
     if (a.T == 0) return cudaSuccess;
     const bool chain = pdl && !prof;
     cudaError_t err;
-    RouteArgs ra{a.idx, a.T * a.topk, a.E, a.counts, a.offsets, a.perm, a.inv, a.status, a.gbase, a.groups};
+    RouteArgs ra{a.idx,     a.T * a.topk, a.E,       a.counts, a.offsets,
+                 a.perm,    a.inv,        a.status,  a.gbase,  a.groups,
+                 group_slots(a.act_e4m3 != 0)};
     if (prof) prof->begin(kPhaseRoute, s);
     err = launch_route(ra, s, chain);
     if (prof) prof->end(s);

@@ -94,18 +94,23 @@ enum { kPhasePrep = 0, kPhaseGateUp = 1, kPhaseDown = 2, kPhaseRoute = 3, kPhase
 
 cudaError_t launch_gemv_layer(const GemvArgs& a, cudaStream_t s, bool pdl, Profiler* prof);
 
-// Slots per group of the expert-major path: a group is up to this many
-// consecutive sorted slots of one expert, multiplied as the N = 16 x slots
-// columns of one block-scaled MMA (N <= 128).
+// Slots per group of the expert-major path, at most: a group is up to this
+// many consecutive sorted slots of one expert, multiplied as the N = pieces x
+// slots columns of one block-scaled MMA (N <= 64: 8 slots of 8 pieces in the
+// E4M3 mode, 4 slots of 16 pieces in the bf16 mode).
 constexpr int kGroupTokens = 8;
+constexpr int kGroupN = 64;
+__host__ __device__ inline int group_pieces(bool e4m3) { return e4m3 ? 8 : 16; }
+__host__ __device__ inline int group_slots(bool e4m3) { return kGroupN / group_pieces(e4m3); }
 
 // One group of the expert-major path.
 struct __align__(16) GroupInfo {
     int e;          // expert
     int p0;         // first sorted position (perm index) of its slots
-    int nt;         // slots, 1..kGroupTokens
+    int nt;         // slots, 1..group size
     int gb, ng;     // first group of the expert, groups of the expert
-    int pad[3];
+    int cnt;        // slots of the expert
+    int pad[2];
 };
 
 // Token -> expert grouping (route.cu).
@@ -117,12 +122,13 @@ struct RouteArgs {
     // optional (nullptr: not made): group table of the expert-major path
     int32_t* gbase;         // [E+1] first group of each expert; gbase[E] = groups
     GroupInfo* groups;      // [max groups]
+    int group_size;         // slots per group, at most
 };
-// Upper bound on the groups of n slots over E experts.
-inline int max_groups(int n, int E)
+// Upper bound on the groups of n slots over E experts (groups of >= gs slots).
+inline int max_groups(int n, int E, int gs)
 {
     const int used = n < E ? n : E;
-    const int g = (n + kGroupTokens - 1) / kGroupTokens + used;
+    const int g = (n + gs - 1) / gs + used;
     return g < n ? g : n;
 }
 
@@ -141,8 +147,8 @@ struct GroupArgs {
     int32_t *counts, *offsets, *perm, *inv, *gbase;
     GroupInfo* groups;
     // B operands in group order: the pieces of slot at sorted position P start
-    // at P * act_bytes(K) (units of a group hold its nt slots side by side);
-    // scale atoms per (group, unit)
+    // at P * (bytes of one slot's pieces over K) (units of a group hold its nt
+    // slots side by side); scale atoms per (group, unit)
     uint8_t* xg;            // [n][act_bytes(H)]
     uint8_t* xgsf;          // [max groups][H/128][512]
     uint8_t* hg;            // [n][act_bytes(I)]
@@ -167,7 +173,7 @@ GroupWorkspaceSizes group_workspace_sizes(int T, int topk, int E, int H, int I, 
 cudaError_t group_init_device();
 cudaError_t launch_group_layer(const GroupArgs& a, cudaStream_t s, bool pdl, Profiler* prof);
 // library default of moe_ffn_config.gemm_min_tokens
-constexpr int kDefaultGemmMinTokens = 16;
+constexpr int kDefaultGemmMinTokens = MOE_DEFAULT_GEMM_MIN_TOKENS;
 int route_max_experts();
 cudaError_t route_init_device();
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, bool pdl = false);

@@ -11,8 +11,8 @@
 // Out-of-range ids are left out (inv = -1, status "bad index"); perm entries
 // past the number of valid slots are -1.
 // When asked for, the same pass also cuts each expert's sorted slots into
-// groups of up to kGroupTokens (the expert-major path's MMA columns): a second
-// exclusive scan, over ceil(count / kGroupTokens), numbers the groups.
+// groups of up to group_size slots (the expert-major path's MMA columns): a
+// second exclusive scan, over ceil(count / group_size), numbers the groups.
 #include "common.cuh"
 #include "internal.h"
 
@@ -72,17 +72,18 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteArgs a)
     // owns a contiguous run of experts
     const int per = (E + blockDim.x - 1) / blockDim.x;
     const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+    const int gs = a.groups ? a.group_size : 1;
     int local = 0, lgrp = 0;
     for (int e = e0; e < e1; e++) {
         local += s_cur[e];
-        lgrp += (s_cur[e] + kGroupTokens - 1) / kGroupTokens;
+        lgrp += (s_cur[e] + gs - 1) / gs;
     }
     int total = 0, gtotal = 0;
     int run = block_exclusive_scan(local, s_warp, &total);
     int grun = block_exclusive_scan(lgrp, s_warp, &gtotal);
     for (int e = e0; e < e1; e++) {
         const int c = s_cur[e];
-        const int ng = (c + kGroupTokens - 1) / kGroupTokens;
+        const int ng = (c + gs - 1) / gs;
         a.counts[e] = c;
         a.offsets[e] = run;
         if (a.groups) {
@@ -90,10 +91,11 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteArgs a)
             for (int q = 0; q < ng; q++) {
                 GroupInfo gi = {};
                 gi.e = e;
-                gi.p0 = run + q * kGroupTokens;
-                gi.nt = min(kGroupTokens, c - q * kGroupTokens);
+                gi.p0 = run + q * gs;
+                gi.nt = min(gs, c - q * gs);
                 gi.gb = grun;
                 gi.ng = ng;
+                gi.cnt = c;
                 a.groups[grun + q] = gi;
             }
         }

@@ -71,8 +71,18 @@ typedef struct {
     int act_mode;         /* MOE_ACT_*                                       */
     int out_dtype;        /* MOE_OUT_*                                       */
     int gemm_min_tokens;  /* T >= this uses the grouped (expert-major) path;
-                             0 selects the library default                   */
+                             0 selects MOE_DEFAULT_GEMM_MIN_TOKENS           */
 } moe_ffn_config;
+
+/* Below this many tokens a layer runs slot-major: each (token, expert) slot
+ * streams its expert's weights (batch 1 reads every chosen expert once; two
+ * launches per layer).  From it on, the layer runs expert-major: the slots are
+ * sorted by expert ([8GB] §提速之路：v1 到 v4, the per-expert token grouping)
+ * and each expert's weights are multiplied against up to 8 of its slots per
+ * tensor-core MMA, so an expert chosen by many tokens is streamed from HBM
+ * once per layer (four launches: route, prep, layer, combine).  Both paths
+ * compute the same function within the float tolerance. */
+#define MOE_DEFAULT_GEMM_MIN_TOKENS 16
 
 /* One layer's experts.  codes / scales are DEVICE arrays of E DEVICE pointers,
  * each to one expert's blob in the packed layout made by moe_ffn_pack_expert.
@@ -168,9 +178,11 @@ int moe_stack_forward(moe_ffn_t h, float* x, const moe_expert_table* tbls,
  * entry point is not traced.  Errors: INVALID_ARG, CUDA. */
 enum {
     MOE_PHASE_PREP = 0,      /* activation prep (and fused RMSNorm)         */
-    MOE_PHASE_GATE_UP = 1,   /* gate/up projections + SwiGLU                */
-    MOE_PHASE_DOWN = 2,      /* down projection + combine                   */
-    MOE_PHASE_ROUTE = 3,     /* token -> expert grouping                    */
+    MOE_PHASE_GATE_UP = 1,   /* the layer kernel: gate/up + SwiGLU + down
+                                (+ the combine on the slot-major path)      */
+    MOE_PHASE_DOWN = 2,      /* the combine kernel (expert-major path)      */
+    MOE_PHASE_ROUTE = 3,     /* token -> expert grouping (moe_ffn_route and
+                                the expert-major path's first kernel)       */
     MOE_PHASE_ACT_QUANT = 4, /* E4M3 activation quantizer                   */
     MOE_NUM_PHASES = 8
 };

@@ -64,3 +64,11 @@ def test_null_handle_and_strerror():
     for code in range(-6, 1):
         assert moe.strerror(code) and moe.strerror(code) != "unknown error code"
     assert moe.strerror(-99) == "unknown error code"
+
+
+def test_binding_constants_match_the_header():
+    import re
+
+    text = open(os.path.join(ROOT, "include", "moe_ffn.h"), encoding="utf-8").read()
+    m = re.search(r"#define MOE_DEFAULT_GEMM_MIN_TOKENS (\d+)", text)
+    assert m and int(m.group(1)) == moe.DEFAULT_GEMM_MIN_TOKENS
