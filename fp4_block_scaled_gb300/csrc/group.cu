@@ -134,6 +134,7 @@ struct GSmem {
     uint64_t drain[kGIssuers];
     GBSrc bsrc[kGStagesA];
     float comb[2][kNT][kTileRows];
+    float hstash[kNT][64];       // raw h of the first tile of a pair, per slot
     uint32_t tmem;
     int abort;
 };
@@ -395,13 +396,16 @@ __device__ __forceinline__ int g_count_chunks(int kgt, const GRange& r)
     return (int)((fj - r.u0 + CU - 1) / CU + whole * ((K + CU - 1) / CU) + (rest + CU - 1) / CU);
 }
 
-// Walks the jobs of one projection in order.  Jobs are ordered (expert,
-// tile, group of the expert): expert e's jobs are [ntiles gb, ntiles (gb +
-// ng)), so job / ntiles is one of its groups.  Moving to the next job is
-// arithmetic; only an expert boundary reads the next expert's group record
-// and weight pointers.
+// Walks the jobs of one projection in order.  Jobs are ordered (expert, tile
+// pair, group of the expert, tile of the pair): the two tiles 2b, 2b + 1 of a
+// group are adjacent jobs (the E4M3 mode quantizes h per 128 = two gate/up
+// tiles, so both halves usually meet in one CTA), and the groups of an expert
+// re-read a tile from L2 within two jobs.  Expert e's jobs are [ntiles gb,
+// ntiles (gb + ng)), so job / ntiles is one of its groups.  Moving to the next
+// job is arithmetic; only an expert boundary reads the next expert's group
+// record and weight pointers.
 struct GCursor {
-    int tile, c;                 // weight tile, group within the expert
+    int b, c, t;                 // tile pair, group within the expert, tile of the pair
     int gb, ng, cnt, p0e;        // the expert's first group, groups, slots, first sorted position
     int ngroups, gs;
     const uint8_t* cb;
@@ -425,30 +429,44 @@ struct GCursor {
         gs = p.gs;
         enter(a, (int)(job / (uint32_t)p.ntiles));
         const uint32_t local = job - (uint32_t)gb * (uint32_t)p.ntiles;
-        tile = (int)(local / (uint32_t)ng);
-        c = (int)(local % (uint32_t)ng);
+        const uint32_t paired = (uint32_t)(p.ntiles / 2) * 2u * (uint32_t)ng;   // jobs in full pairs
+        if (local < paired) {
+            b = (int)(local / (2u * (uint32_t)ng));
+            const uint32_t r = local % (2u * (uint32_t)ng);
+            c = (int)(r / 2);
+            t = (int)(r % 2);
+        } else {               // the last, single tile (odd tile count)
+            b = p.ntiles / 2;
+            c = (int)(local - paired);
+            t = 0;
+        }
     }
     __device__ void next(const GroupArgs& a, const GPlan& p)
     {
+        if (t == 0 && 2 * b + 1 < p.ntiles) {
+            t = 1;
+            return;
+        }
+        t = 0;
         if (++c < ng) return;
         c = 0;
-        if (++tile < p.ntiles) return;
-        tile = 0;
+        if (++b < (p.ntiles + 1) / 2) return;
+        b = 0;
         if (gb + ng < ngroups) enter(a, gb + ng);
     }
     template <int PHASE>
     __device__ GJob job(const GroupArgs& a, const GPlan& p) const
     {
         GJob j;
-        j.tile = tile;
+        j.tile = 2 * b + t;
         j.g = gb + c;
         j.p0 = p0e + c * gs;
         j.nt = min(gs, cnt - c * gs);
         j.B = (PHASE == 0 ? a.xg : a.hg) + (size_t)j.p0 * p.act_bytes;
         j.Bsf = (PHASE == 0 ? a.xgsf : a.hgsf) + (size_t)j.g * p.kgt * kUnitSfBytes;
         j.ok = ok;
-        j.code = ok ? cb + p.code_off + (size_t)tile * p.tile_code_bytes : nullptr;
-        j.sf = ok ? sb + p.sf_off + (size_t)tile * p.tile_sf_bytes : nullptr;
+        j.code = ok ? cb + p.code_off + (size_t)j.tile * p.tile_code_bytes : nullptr;
+        j.sf = ok ? sb + p.sf_off + (size_t)j.tile * p.tile_sf_bytes : nullptr;
         return j;
     }
 };
@@ -660,12 +678,15 @@ __device__ void gissue(const GroupArgs& a, const GPlan& p, const GRange& r, GSme
 // Gate/up job (group, tile), slot i -> the 64 values h = w * silu(g) * u of
 // that slot as NP pieces into the down projection's B operand, by one warp;
 // then the grid-wide count of finished h tiles grows by the tiles written.
+// In the E4M3 mode h is quantized per 128 (two tiles): local = 1 for the first
+// tile of a pair whose second tile this CTA finishes next (raw h goes to the
+// warp's stash), 2 for that second tile (the first one's h is in the stash),
+// 0 for a pair split between CTAs (met through global memory).
 template <int NP>
 __device__ void gfinalize_gate_up(const GroupArgs& a, const GPlan& p, const GJob& jb, int i, const float* comb,
-                                  int lane)
+                                  int lane, float* stash, int local)
 {
     const int P = jb.p0 + i, tile = jb.tile;
-    const float w = a.w[a.perm[P]];
     const float2 g = *reinterpret_cast<const float2*>(comb + 2 * lane);
     const float2 u = *reinterpret_cast<const float2*>(comb + 64 + 2 * lane);
     float h0 = silu(g.x) * u.x, h1 = silu(g.y) * u.y;
@@ -682,7 +703,16 @@ __device__ void gfinalize_gate_up(const GroupArgs& a, const GPlan& p, const GJob
         const int blk = tile / 2, nblk = (p.ntiles + 1) / 2;
         const bool pair = (tile | 1) < p.ntiles;
         float o0 = 0.0f, o1 = 0.0f;
-        if (pair) {
+        if (pair && local == 1) {
+            stash[2 * lane] = h0;
+            stash[2 * lane + 1] = h1;
+            return;
+        }
+        if (pair && local == 2) {
+            o0 = stash[2 * lane];
+            o1 = stash[2 * lane + 1];
+            done = 2;
+        } else if (pair) {
             float* mine = a.hraw + (size_t)P * a.I + (size_t)tile * 64 + 2 * lane;
             mine[0] = h0;
             mine[1] = h1;
@@ -704,11 +734,13 @@ __device__ void gfinalize_gate_up(const GroupArgs& a, const GPlan& p, const GJob
         h0 = e4m3_quant_dequant(h0, s);
         h1 = e4m3_quant_dequant(h1, s);
         if (pair) {
+            const float w = a.w[a.perm[P]];
             Pieces64<NP> po;
             make_pieces64<NP>(e4m3_quant_dequant(o0, s) * w, e4m3_quant_dequant(o1, s) * w, po);
             store_pieces64<NP>(po, lane, unit, mstride, atom, i, 2 * ((tile ^ 1) & 1));
         }
     }
+    const float w = a.w[a.perm[P]];
     Pieces64<NP> pc;
     make_pieces64<NP>(h0 * w, h1 * w, pc);
     store_pieces64<NP>(pc, lane, unit, mstride, atom, i, 2 * (tile & 1));
@@ -863,9 +895,14 @@ __device__ void gepilogue(const GroupArgs& a, const GPlan& p, const GRange& r, G
             for (int i = 0; i < kNT; i++)
                 if (i < nt) comb[i][row] = v[i];
             named_sync(1, 128);
+            int local = 0;      // E4M3 pair of tiles finished in this CTA (see gfinalize_gate_up)
+            if (a.act_e4m3 && (cur.tile | 1) < p.ntiles) {
+                const long long partner = (cur.tile & 1) ? (long long)job - 1 : (long long)job + 1;
+                if (g_cta_of_unit(U, G, partner * p.kgt) == (int)blockIdx.x) local = (cur.tile & 1) ? 2 : 1;
+            }
             for (int i = quad; i < nt; i += 4) {
-                if (p.np == 8) gfinalize_gate_up<8>(a, p, cur, i, comb[i], lane);
-                else gfinalize_gate_up<16>(a, p, cur, i, comb[i], lane);
+                if (p.np == 8) gfinalize_gate_up<8>(a, p, cur, i, comb[i], lane, sm.hstash[i], local);
+                else gfinalize_gate_up<16>(a, p, cur, i, comb[i], lane, sm.hstash[i], local);
             }
             if (quad == 0 && lane == 0) G_TRACE(3, es.use[0] + es.use[1]);
             es.cb ^= 1;
