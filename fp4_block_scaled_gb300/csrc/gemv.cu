@@ -84,7 +84,12 @@ constexpr int kSlotCache = 256;                              // routing weights 
 }  // namespace
 __device__ long long g_tc_trace[2][4][4096];
 __device__ long long g_tc_cta[8][1024];
+__device__ long long g_tc_fin[4][64];
 namespace {
+#define TC_FIN(step, idx)                                                                       \
+    do {                                                                                        \
+        if (blockIdx.x == 0 && lane == 0 && (idx) < 64) g_tc_fin[step][idx] = (long long)globaltimer_ns(); \
+    } while (0)
 #define TC_TRACE(ph, role, idx)                                                     \
     do {                                                                            \
         if (blockIdx.x == 0 && (idx) < 4096) g_tc_trace[ph][role][idx] = (long long)globaltimer_ns(); \
@@ -96,6 +101,9 @@ namespace {
     } while (0)
 #define TC_CTA(slot) \
     do {             \
+    } while (0)
+#define TC_FIN(step, idx) \
+    do {                  \
     } while (0)
 #endif
 
@@ -581,6 +589,7 @@ __device__ __forceinline__ void finalize_gate_up(const GemvArgs& a, const Stream
                                                  uint32_t group, const float* comb, int lane)
 {
     const int j = (int)(group / p.ntiles), tile = (int)(group % p.ntiles);
+    TC_FIN(0, group % 64);
     const float w = slot_weight(a, sm, j);
     const float2 g = *reinterpret_cast<const float2*>(comb + 2 * lane);
     const float2 u = *reinterpret_cast<const float2*>(comb + 64 + 2 * lane);
@@ -624,13 +633,15 @@ __device__ __forceinline__ void finalize_gate_up(const GemvArgs& a, const Stream
     uint8_t* Bunit = a.hq + (size_t)j * act_bytes(a.I) + (size_t)(tile / 2) * kUnitBBytes;
     uint8_t* Bsf = a.hsf + (size_t)j * act_sf_bytes(a.I) + (size_t)(tile / 2) * kUnitSfBytes;
     write_pieces64(h0 * w, h1 * w, lane, Bunit, Bsf, 2 * tile);
+    TC_FIN(1, group % 64);
     // the down projection reads these with bulk copies (async proxy), in other CTAs
     asm volatile("fence.proxy.async.global;" ::: "memory");
+    TC_FIN(2, group % 64);
     __syncwarp();
-    if (lane == 0) {
-        __threadfence();
-        atomicAdd(a.sync, done);
-    }
+    // release: the pieces (this warp's stores, ordered by the warp barrier) are
+    // visible before the count; the thread does not wait for the add
+    if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(a.sync), "r"(done) : "memory");
+    TC_FIN(3, group % 64);
 }
 
 struct EpiState {
@@ -771,6 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(GemvArgs a, StreamPlan p0
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     TcSmem& sm = *reinterpret_cast<TcSmem*>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) TC_CTA(7);
     const Range r0 = cta_range(p0), r1 = cta_range(p1);
     const uint32_t gu_groups = (uint32_t)(p0.U / ((long long)p0.kgt * p0.jobs_per_group));
 
@@ -948,8 +960,14 @@ GemvWorkspaceSizes gemv_workspace_sizes(int T, int topk, int H, int I, int sms, 
 
 cudaError_t gemv_init_device()
 {
-    return cudaFuncSetAttribute((const void*)k_layer, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)layer_smem());
+    cudaError_t e = cudaFuncSetAttribute((const void*)k_layer, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)layer_smem());
+    // k_prep asks for the same shared-memory carveout as k_layer, so that the
+    // SMs need no reconfiguration between the two kernels of a layer
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute((const void*)k_prep, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+    return e;
 }
 
 size_t gemv_stream_smem() { return layer_smem(); }

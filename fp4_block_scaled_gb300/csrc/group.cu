@@ -747,10 +747,9 @@ __device__ void gfinalize_gate_up(const GroupArgs& a, const GPlan& p, const GJob
     // the down projection reads these with bulk copies (async proxy), in other CTAs
     asm volatile("fence.proxy.async.global;" ::: "memory");
     __syncwarp();
-    if (lane == 0) {
-        __threadfence();
-        atomicAdd(a.sync, done);
-    }
+    // release: the pieces (this warp's stores, ordered by the warp barrier) are
+    // visible before the count; the thread does not wait for the add
+    if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(a.sync), "r"(done) : "memory");
 }
 
 struct GEpi {
