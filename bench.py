@@ -43,6 +43,9 @@ WORKLOADS = {
     # popularity), activations quantized to E4M3 with ue8m0 per 128
     "layer_b64": dict(E=384, H=4096, I=2880, k=6, T=64, L=1, act="e4m3", dist="uniform", steps=1000),
     "layer_b512": dict(E=384, H=4096, I=2880, k=6, T=512, L=1, act="e4m3", dist="zipf", steps=100),
+    # expert-major path with 64 resident experts (1.2 GB, above L2) at batch 16: 1-2
+    # slots per group as at batch 64; the size used for ncu captures of k_glayer
+    "layer_b16_e64": dict(E=64, H=4096, I=2880, k=6, T=16, L=1, act="e4m3", dist="uniform", steps=2000),
     # 40-layer stack of 128-expert layers (96 GB resident), residual + RMSNorm,
     # the whole step as one CUDA graph, at batch 1 and 32
     "stack_b1": dict(E=128, H=4096, I=2880, k=6, T=1, L=40, act="bf16", dist="uniform", steps=500),
@@ -145,9 +148,11 @@ def draw_routings(R, E, k, T, seed, dist="uniform", layer=0):
     return idx, w
 
 
-def traffic_record(kernel, workload):
+def traffic_record(kernel, workload, algorithmic_bytes):
     """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source and on this workload's launch shape (else None)."""
+    the current kernel source and on this workload's launch shape (else None):
+    the captured bytes, or the captured dram/algorithmic ratio times this
+    workload's algorithmic bytes per launch."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -160,7 +165,11 @@ def traffic_record(kernel, workload):
     if not os.path.exists(src):
         return None
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    return rec["dram_bytes_per_launch"] if sha == rec["source_sha256"] else None
+    if sha != rec["source_sha256"]:
+        return None
+    if "dram_bytes_per_algorithmic_byte" in rec:
+        return rec["dram_bytes_per_algorithmic_byte"] * algorithmic_bytes
+    return rec["dram_bytes_per_launch"]
 
 
 # --------------------------------------------------------------- CPU oracle
@@ -434,7 +443,7 @@ def run_ours(args, wl):
     co_ms = ms_ph[moe.MOE_PHASE_DOWN] / max(1, n_ph[moe.MOE_PHASE_DOWN])
     ly_bytes = sum(distinct(i, 0) for i in range(nprof)) / nprof * expert_bytes(H, I) + act_io
     achieved = ly_bytes / (ly_ms / 1000.0) / 1e9
-    traffic = traffic_record(kernel, args.workload)
+    traffic = traffic_record(kernel, args.workload, ly_bytes)
 
     # ---- end to end through the public API from host buffers: every step copies
     # its inputs in from pinned host memory and its result back
