@@ -207,6 +207,9 @@ __global__ void __launch_bounds__(256) k_prep(GemvArgs a)
     __shared__ float s_red[8];
     __shared__ float s_den;
 
+    // k_layer reads nothing this kernel or the previous layer writes before its
+    // own wait, so it may start (on the SMs the previous layer frees) right away
+    pdl_trigger();
     pdl_wait();
     float den = 1.0f;
     if (a.x_resid) {
@@ -225,7 +228,6 @@ __global__ void __launch_bounds__(256) k_prep(GemvArgs a)
         __syncthreads();
         den = s_den;
     }
-    pdl_trigger();
     if (a.act_e4m3) {
         // x quantized to E4M3 under one ue8m0 scale per 128 elements (lane l holds
         // elements 2l, 2l + 1 of each half), and the dequantized values as pieces
@@ -268,40 +270,52 @@ __global__ void __launch_bounds__(256) k_prep(GemvArgs a)
 
 // ----------------------------------------------------------------- k_layer
 
+// The slot j and weight tile of a job.
 template <int PHASE>
-__device__ __forceinline__ JobInfo job_info(const GemvArgs& a, const StreamPlan& p, long long job)
+__device__ __forceinline__ void job_slot(const GemvArgs& a, const StreamPlan& p, long long job, int& j, int& tile)
 {
-    JobInfo ji;
-    int j, t, tile;
-    if (PHASE == 0) {        // job = (slot, tile); B = pieces of the slot's token
+    if (PHASE == 0) {        // job = (slot, tile)
         j = (int)(job / p.ntiles);
         tile = (int)(job % p.ntiles);
-        t = j / a.topk;
-        ji.B = a.xq + (size_t)t * p.act_bytes;
-        ji.Bsf = a.xsf + (size_t)t * p.act_sf_bytes;
-    } else {                 // job = ((token, tile), slot); B = pieces of the slot's h
+    } else {                 // job = ((token, tile), slot)
         const long long grp = job / a.topk;
         const int kk = (int)(job % a.topk);
-        t = (int)(grp / p.ntiles);
+        const int t = (int)(grp / p.ntiles);
         tile = (int)(grp % p.ntiles);
         j = t * a.topk + kk;
+    }
+}
+
+// A job's weight and activation sources, given its slot's expert id e and that
+// expert's pointers (cb, sb; read only when e is in range).
+template <int PHASE>
+__device__ __forceinline__ JobInfo job_info_e(const GemvArgs& a, const StreamPlan& p, int j, int tile, int e,
+                                              const uint8_t* cb, const uint8_t* sb)
+{
+    JobInfo ji;
+    if (PHASE == 0) {        // B = pieces of the slot's token
+        const int t = j / a.topk;
+        ji.B = a.xq + (size_t)t * p.act_bytes;
+        ji.Bsf = a.xsf + (size_t)t * p.act_sf_bytes;
+    } else {                 // B = pieces of the slot's h
         ji.B = a.hq + (size_t)j * p.act_bytes;
         ji.Bsf = a.hsf + (size_t)j * p.act_sf_bytes;
     }
-    const int e = a.idx[j];
-    ji.ok = e >= 0 && e < a.E;
-    ji.code = nullptr;
-    ji.sf = nullptr;
-    if (ji.ok) {
-        const uint8_t* cb = a.codes[e];
-        const uint8_t* sb = a.scales[e];
-        ji.ok = cb && sb && ((reinterpret_cast<uintptr_t>(cb) | reinterpret_cast<uintptr_t>(sb)) & 15) == 0;
-        if (ji.ok) {
-            ji.code = cb + p.code_off + (size_t)tile * p.tile_code_bytes;
-            ji.sf = sb + p.sf_off + (size_t)tile * p.tile_sf_bytes;
-        }
-    }
+    ji.ok = e >= 0 && e < a.E && cb && sb &&
+            ((reinterpret_cast<uintptr_t>(cb) | reinterpret_cast<uintptr_t>(sb)) & 15) == 0;
+    ji.code = ji.ok ? cb + p.code_off + (size_t)tile * p.tile_code_bytes : nullptr;
+    ji.sf = ji.ok ? sb + p.sf_off + (size_t)tile * p.tile_sf_bytes : nullptr;
     return ji;
+}
+
+template <int PHASE>
+__device__ __forceinline__ JobInfo job_info(const GemvArgs& a, const StreamPlan& p, long long job)
+{
+    int j, tile;
+    job_slot<PHASE>(a, p, job, j, tile);
+    const int e = a.idx[j];
+    const bool in = e >= 0 && e < a.E;
+    return job_info_e<PHASE>(a, p, j, tile, e, in ? a.codes[e] : nullptr, in ? a.scales[e] : nullptr);
 }
 
 __device__ __forceinline__ long long range_start(const StreamPlan& p, int c)
@@ -801,14 +815,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(GemvArgs a, StreamPlan p0
         mbar_fence_init();
     }
     if (warp == 0) {
-        // resolve the CTA's first jobs of both projections (expert pointers) in parallel
-        if (r0.j0 + lane <= r0.jlast && lane < kJobWindow) {
-            const JobInfo ji = job_info<0>(a, p0, r0.j0 + lane);
+        // resolve the CTA's first jobs of both projections (expert pointers), one
+        // per lane and projection, the two projections' loads in flight together
+        const bool h0 = r0.j0 + lane <= r0.jlast && lane < kJobWindow;
+        const bool h1 = r1.j0 + lane <= r1.jlast && lane < kJobWindow;
+        int j0 = 0, t0 = 0, j1 = 0, t1 = 0;
+        if (h0) job_slot<0>(a, p0, r0.j0 + lane, j0, t0);
+        if (h1) job_slot<1>(a, p1, r1.j0 + lane, j1, t1);
+        const int e0 = h0 ? a.idx[j0] : -1, e1 = h1 ? a.idx[j1] : -1;
+        const bool in0 = e0 >= 0 && e0 < a.E, in1 = e1 >= 0 && e1 < a.E;
+        const uint8_t* cb0 = in0 ? a.codes[e0] : nullptr;
+        const uint8_t* sb0 = in0 ? a.scales[e0] : nullptr;
+        const uint8_t* cb1 = in1 ? a.codes[e1] : nullptr;
+        const uint8_t* sb1 = in1 ? a.scales[e1] : nullptr;
+        if (h0) {
+            const JobInfo ji = job_info_e<0>(a, p0, j0, t0, e0, cb0, sb0);
             sm.jobs[0][lane] = ji;
             if (!ji.ok) atomicOr(a.status, kStatusBadIndex);
         }
-        if (r1.j0 + lane <= r1.jlast && lane < kJobWindow) {
-            const JobInfo ji = job_info<1>(a, p1, r1.j0 + lane);
+        if (h1) {
+            const JobInfo ji = job_info_e<1>(a, p1, j1, t1, e1, cb1, sb1);
             sm.jobs[1][lane] = ji;
             if (!ji.ok) atomicOr(a.status, kStatusBadIndex);
         }
