@@ -369,6 +369,13 @@ __device__ __forceinline__ int e2m1_scale_byte(float amax)
     return s < 1 ? 1 : (s > 254 ? 254 : s);
 }
 
+// Arrive at named barrier `id` without waiting (the waiting side uses
+// named_sync with the same id and thread count).
+__device__ __forceinline__ void named_arrive(int id, int threads)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // Named barrier over the first `threads` threads of the CTA (id 1..15).
 __device__ __forceinline__ void named_sync(int id, int threads)
 {

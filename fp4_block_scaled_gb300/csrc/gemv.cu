@@ -13,25 +13,26 @@
 // A projection is a sequence of units -- one 128-K slice of one 128-row tile
 // of one expert matrix: 8 KB of E2M1 codes + a 512 B scale atom -- and each
 // CTA takes an equal contiguous range of it (stream-K split), so every SM
-// streams the same number of bytes.  Per CTA:
-//   warp 0 (one thread)  streams the weights: bulk-copies chunks of 4 units
+// streams the same number of bytes.  Per CTA (kCU = 5 units per stage, 4
+// stages):
+//   warp 0 (one thread)  streams the weights: bulk-copies chunks of kCU units
 //                        (codes + scale atoms) from HBM into a ring of
 //                        shared-memory stages (cp.async.bulk, mbarrier tx
-//                        counts), gate/up then down without a pause, and
-//                        prefetches the rest of its down range into L2 at the
-//                        boundary;
-//   warp 9 (one thread)  copies the matching activation pieces into each
+//                        counts), gate/up then down without a pause; nothing
+//                        is prefetched beyond the ring, so the gate/up tail and
+//                        the h hand-off do not queue behind down weights;
+//   last warp            copies the matching activation pieces into each
 //                        stage: x's once the previous kernel is done (PDL),
 //                        h's once every gate/up group of the grid has been
 //                        finalized (a grid-wide counter, bounded wait);
-//   warps 1-4            one MMA-issuing thread each (tcgen05 issue from a
-//                        single thread is serial; from several it overlaps):
+//   warps 1..kCU         one MMA-issuing thread each (one thread issues a
+//                        tcgen05 instruction per ~150 cycles; several overlap):
 //                        issuer i moves the scale atoms of unit i of every
 //                        stage to tensor memory (tcgen05.cp) and issues its
 //                        block-scaled MMAs (kind::mxf4, M = 128, N = 16, K = 64,
 //                        scale_vec 2X) into its own TMEM accumulator;
 //                        tcgen05.commit releases its part of the stage;
-//   warps 5-8            at the end of each reduction group read the issuers'
+//   4 epilogue warps     at the end of each reduction group read the issuers'
 //                        accumulators (tcgen05.ld), add the 16 piece columns
 //                        and the issuers in a fixed order, and finish the
 //                        group.  A group split over several CTAs is finished
@@ -39,6 +40,8 @@
 //                        last; the others leave launch-tagged partial sums
 //                        that it adds in CTA order (no fences or counters on
 //                        the way, and mostly read before its own sum is done).
+//                        The owned gate/up groups' h go to the four warps in
+//                        turn.
 // The tensor core does the E2M1 decoding, the per-(row, 32-block) scaling and
 // the fp32 accumulation; the CUDA cores only touch 128 values per group.
 // Results are bitwise reproducible on a given GPU.  Every wait is bounded
@@ -52,10 +55,10 @@ namespace {
 
 // units per chunk (stage) = MMA-issuing warps, and ring stages; build-time tunables
 #ifndef MOE_TC_CU
-#define MOE_TC_CU 4
+#define MOE_TC_CU 5
 #endif
 #ifndef MOE_TC_STAGES
-#define MOE_TC_STAGES 5
+#define MOE_TC_STAGES 4
 #endif
 constexpr int kCU = MOE_TC_CU;
 constexpr int kStageCodes = kCU * kUnitCodeBytes;            // 32 KB
@@ -83,7 +86,8 @@ constexpr int kSlotCache = 256;                              // routing weights 
 // and per-CTA milestones
 }  // namespace
 __device__ long long g_tc_trace[2][4][4096];
-__device__ long long g_tc_cta[8][1024];
+__device__ long long g_tc_cta[12][1024];
+__device__ long long g_tc_grp[5][1024];   // per gate/up group: acc ready, folded, barrier, fin start, fin end
 __device__ long long g_tc_fin[4][64];
 namespace {
 #define TC_FIN(step, idx)                                                                       \
@@ -95,6 +99,7 @@ namespace {
         if (blockIdx.x == 0 && (idx) < 4096) g_tc_trace[ph][role][idx] = (long long)globaltimer_ns(); \
     } while (0)
 #define TC_CTA(slot) (g_tc_cta[slot][blockIdx.x] = (long long)globaltimer_ns())
+#define TC_GRP(k, g) (g_tc_grp[k][(g) & 1023] = (long long)globaltimer_ns())
 #else
 #define TC_TRACE(ph, role, idx) \
     do {                        \
@@ -104,6 +109,9 @@ namespace {
     } while (0)
 #define TC_FIN(step, idx) \
     do {                  \
+    } while (0)
+#define TC_GRP(k, g) \
+    do {             \
     } while (0)
 #endif
 
@@ -141,7 +149,7 @@ struct TcSmem {
     uint64_t acc_empty[2];
     uint64_t drain[kIssuers];    // the issuers' last MMAs are done
     BSrc bsrc[kStages];
-    float comb[2][kTileRows];
+    float comb[4][kTileRows];    // gate/up sums of the last four owned groups
     float slot_w[kSlotCache];    // w of each slot, 0 where its expert index is invalid
     JobInfo jobs[2][kJobWindow]; // first jobs of the gate/up and down streams
     uint32_t tmem;
@@ -460,27 +468,6 @@ __device__ bool produce(const GemvArgs& a, const StreamPlan& p, const Range& r, 
     return true;
 }
 
-// The down weights beyond the first ring's worth go to L2 now, so that HBM
-// keeps streaming while the grid finishes h.
-__device__ void prefetch_down(const GemvArgs& a, const StreamPlan& p, const Range& r, TcSmem& sm)
-{
-    Walk wk(p, r);
-    const uint32_t kgt = wk.kgt;
-    JobInfo ji = job_at<1>(a, p, r, sm, wk.job);
-    for (int c = 0; wk.u < wk.u1; c++) {
-        const uint32_t nun = wk.chunk();
-        const bool has_half = p.kg_half && (wk.kg + nun == kgt);
-        const uint32_t cb = (nun - (has_half ? 1u : 0u)) * kUnitCodeBytes + (has_half ? kMmaCodeBytes : 0);
-        if (c >= kStages && ji.ok) {
-            prefetch_l2_bulk(ji.code + (size_t)wk.kg * kUnitCodeBytes, cb);
-            prefetch_l2_bulk(ji.sf + (size_t)wk.kg * kUnitSfBytes, nun * kUnitSfBytes);
-        }
-        bool nj;
-        wk.advance(nun, nj);
-        if (nj && wk.u < wk.u1) ji = job_at<1>(a, p, r, sm, wk.job);
-    }
-}
-
 // ------------------------------------------------------------------ loader
 
 // Issues the activation copies of every stage the producer posted, in order.
@@ -604,6 +591,8 @@ __device__ __forceinline__ void finalize_gate_up(const GemvArgs& a, const Stream
 {
     const int j = (int)(group / p.ntiles), tile = (int)(group % p.ntiles);
     TC_FIN(0, group % 64);
+    if (lane == 0) TC_CTA(8);
+    if (lane == 0) TC_GRP(3, group);
     const float w = slot_weight(a, sm, j);
     const float2 g = *reinterpret_cast<const float2*>(comb + 2 * lane);
     const float2 u = *reinterpret_cast<const float2*>(comb + 64 + 2 * lane);
@@ -656,6 +645,8 @@ __device__ __forceinline__ void finalize_gate_up(const GemvArgs& a, const Stream
     // visible before the count; the thread does not wait for the add
     if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(a.sync), "r"(done) : "memory");
     TC_FIN(3, group % 64);
+    if (lane == 0) TC_CTA(9);
+    if (lane == 0) TC_GRP(4, group);
 }
 
 struct EpiState {
@@ -736,6 +727,8 @@ __device__ void epilogue(const GemvArgs& a, const StreamPlan& p, const Range& r,
         const bool ready = !*(volatile int*)&sm.abort &&
                            mbar_wait_or_abort(&sm.acc_full[buf], es.use[buf] & 1, &sm.abort, kWaitLimitNs);
         if (et == 0) TC_TRACE(PHASE, 3, es.use[0] + es.use[1]);
+        if (PHASE == 0 && et == 0) TC_CTA(10);
+        if (PHASE == 0 && et == 0 && owner) TC_GRP(0, group);
         es.use[buf]++;
         if (!ready) set_abort(a, sm);
         tc_fence_after();
@@ -767,13 +760,26 @@ __device__ void epilogue(const GemvArgs& a, const StreamPlan& p, const Range& r,
             fold_partials(part, cnext, c1, row, es.tag, !abort, &pacc, &late);
             if (late) set_abort(a, sm);
         }
+        if (PHASE == 0 && et == 0) TC_CTA(11);
+        if (PHASE == 0 && et == 0) TC_GRP(1, group);
         v += pacc;
         if (PHASE == 0) {
+            // the owned groups' h go to the four epilogue warps in turn: the
+            // others only arrive at the group's barrier, so one warp's finalize
+            // overlaps the next groups' accumulator reads and finalizes.  Buffer
+            // and barrier cb are reused four groups later, when that warp has
+            // long finished (the issuers cannot pass it by more than the two
+            // accumulator buffers).
             float* comb = sm.comb[es.cb];
             comb[row] = v;
-            named_sync(1, 128);
-            if (et < 32) finalize_gate_up(a, p, sm, group, comb, lane);
-            es.cb ^= 1;
+            if (quad == es.cb) {
+                named_sync(3 + es.cb, 128);
+                if (lane == 0) TC_GRP(2, group);
+                finalize_gate_up(a, p, sm, group, comb, lane);
+            } else {
+                named_arrive(3 + es.cb, 128);
+            }
+            es.cb = (es.cb + 1) & 3;
         } else {
             // group = (token t, tile): 128 output rows, one per thread
             const int t = (int)(group / p.ntiles), tile = (int)(group % p.ntiles);
@@ -859,10 +865,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(GemvArgs a, StreamPlan p0
             int n = 0;
             const bool ok = produce<0>(a, p0, r0, sm, n);
             TC_CTA(2);
-            if (ok) {
-                prefetch_down(a, p1, r1, sm);
-                produce<1>(a, p1, r1, sm, n);
-            }
+            // the down weights follow at once into the ring; nothing more is
+            // prefetched, so that the gate/up tail and the h hand-off (the
+            // critical path) do not queue behind them in the memory system
+            if (ok) produce<1>(a, p1, r1, sm, n);
             // no copy may still be in flight into this CTA's memory at exit
             for (int m = n > kStages ? n - kStages : 0; m < n; m++)
                 mbar_wait_bounded(&sm.full[m % kStages], (m / kStages) & 1, kWaitLimitNs);
