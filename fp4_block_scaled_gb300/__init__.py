@@ -29,7 +29,7 @@ MOE_OUT_F32 = 1
 DEFAULT_GEMM_MIN_TOKENS = 16   # MOE_DEFAULT_GEMM_MIN_TOKENS
 
 EXPORTS = [
-    "moe_ffn_packed_codes_bytes", "moe_ffn_packed_scales_bytes", "moe_ffn_create",
+    "moe_ffn_packed_expert_bytes", "moe_ffn_create",
     "moe_ffn_pack_expert", "moe_ffn_forward", "moe_ffn_forward_host", "moe_ffn_route",
     "moe_ffn_act_quant", "moe_stack_forward", "moe_ffn_profile_enable", "moe_ffn_profile_read",
     "moe_ffn_status", "moe_ffn_strerror", "moe_ffn_destroy", "moe_ffn_forward_noalloc",
@@ -56,7 +56,7 @@ class moe_ffn_config(ctypes.Structure):
 
 
 class moe_expert_table(ctypes.Structure):
-    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+    _fields_ = [("experts", ctypes.c_void_p)]
 
 
 _lib = None
@@ -76,10 +76,9 @@ def lib() -> ctypes.CDLL:
         cfgp = ctypes.POINTER(moe_ffn_config)
         tblp = ctypes.POINTER(moe_expert_table)
         sig = {
-            "moe_ffn_packed_codes_bytes": (S, [cfgp]),
-            "moe_ffn_packed_scales_bytes": (S, [cfgp]),
+            "moe_ffn_packed_expert_bytes": (S, [cfgp]),
             "moe_ffn_create": (I, [ctypes.POINTER(P), cfgp, I]),
-            "moe_ffn_pack_expert": (I, [P, P, P, P, P, P]),
+            "moe_ffn_pack_expert": (I, [P, P, P, P, P]),
             "moe_ffn_forward": (I, [P, P, P, P, tblp, P, I, P]),
             "moe_ffn_forward_host": (I, [P, P, P, P, tblp, P, I, P]),
             "moe_ffn_route": (I, [P, P, I, P, P, P, P, P]),
@@ -140,12 +139,8 @@ def config(num_experts, hidden, inter, topk, max_tokens, act_mode=MOE_ACT_BF16,
                           gemm_min_tokens)
 
 
-def moe_ffn_packed_codes_bytes(cfg: moe_ffn_config) -> int:
-    return lib().moe_ffn_packed_codes_bytes(ctypes.byref(cfg))
-
-
-def moe_ffn_packed_scales_bytes(cfg: moe_ffn_config) -> int:
-    return lib().moe_ffn_packed_scales_bytes(ctypes.byref(cfg))
+def moe_ffn_packed_expert_bytes(cfg: moe_ffn_config) -> int:
+    return lib().moe_ffn_packed_expert_bytes(ctypes.byref(cfg))
 
 
 def moe_ffn_create(cfg: moe_ffn_config, device: int = 0) -> int:
@@ -154,15 +149,15 @@ def moe_ffn_create(cfg: moe_ffn_config, device: int = 0) -> int:
     return h.value
 
 
-def moe_ffn_pack_expert(h, canon_codes, canon_scales, packed_codes, packed_scales, stream=None):
-    _check(lib().moe_ffn_pack_expert(h, _p(canon_codes), _p(canon_scales), _p(packed_codes),
-                                     _p(packed_scales), _s(stream)), "moe_ffn_pack_expert")
+def moe_ffn_pack_expert(h, canon_codes, canon_scales, packed, stream=None):
+    _check(lib().moe_ffn_pack_expert(h, _p(canon_codes), _p(canon_scales), _p(packed), _s(stream)),
+           "moe_ffn_pack_expert")
 
 
-def expert_table(codes_ptrs, scales_ptrs) -> moe_expert_table:
-    """codes_ptrs / scales_ptrs: device arrays (e.g. torch int64 tensors on the
-    GPU) holding one device pointer per expert."""
-    return moe_expert_table(_p(codes_ptrs), _p(scales_ptrs))
+def expert_table(expert_ptrs) -> moe_expert_table:
+    """expert_ptrs: a device array (e.g. a torch int64 tensor on the GPU)
+    holding one device pointer per expert, each to a packed blob."""
+    return moe_expert_table(_p(expert_ptrs))
 
 
 def moe_ffn_forward(h, x, topk_idx, topk_w, table: moe_expert_table, y, T: int, stream=None):

@@ -18,7 +18,7 @@ struct StackGraph {
     const int32_t* idx;
     const float* w;
     int L, T;
-    std::vector<const void*> tables;  // codes/scales array pointers per layer
+    std::vector<const void*> tables;  // expert table array pointer per layer
     cudaGraphExec_t exec;
     unsigned long long last_use;
 };
@@ -92,8 +92,7 @@ GemvArgs layer_args(const moe_ffn* h, int T, const int32_t* idx, const float* w,
     a.T = T;
     a.idx = idx;
     a.w = w;
-    a.codes = tbl->codes;
-    a.scales = tbl->scales;
+    a.experts = tbl->experts;
     return a;
 }
 
@@ -103,9 +102,9 @@ int check_forward(const moe_ffn* h, const void* x, const int32_t* idx, const flo
     if (!h) return MOE_ERR_INVALID_ARG;
     if (T < 0 || T > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
-    if (!x || !idx || !w || !y || !tbl || !tbl->codes || !tbl->scales) return MOE_ERR_INVALID_ARG;
+    if (!x || !idx || !w || !y || !tbl || !tbl->experts) return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(y, 16) || !aligned(idx, 4) || !aligned(w, 4) ||
-        !aligned(tbl->codes, 8) || !aligned(tbl->scales, 8))
+        !aligned(tbl->experts, 8))
         return MOE_ERR_INVALID_ARG;
     if (x == y) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
@@ -118,8 +117,7 @@ GroupArgs group_args(const moe_ffn* h, int T, const int32_t* idx, const float* w
     a.T = T;
     a.idx = idx;
     a.w = w;
-    a.codes = tbl->codes;
-    a.scales = tbl->scales;
+    a.experts = tbl->experts;
     return a;
 }
 
@@ -155,16 +153,10 @@ int moe::check_config(const moe_ffn_config* cfg) { return check_cfg(cfg); }
 
 extern "C" {
 
-size_t moe_ffn_packed_codes_bytes(const moe_ffn_config* cfg)
+size_t moe_ffn_packed_expert_bytes(const moe_ffn_config* cfg)
 {
     if (check_cfg(cfg) != MOE_OK) return 0;
-    return make_expert_layout(cfg->hidden, cfg->inter).code_bytes;
-}
-
-size_t moe_ffn_packed_scales_bytes(const moe_ffn_config* cfg)
-{
-    if (check_cfg(cfg) != MOE_OK) return 0;
-    return make_expert_layout(cfg->hidden, cfg->inter).sf_bytes;
+    return make_expert_layout(cfg->hidden, cfg->inter).bytes;
 }
 
 int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
@@ -287,20 +279,19 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     return MOE_OK;
 }
 
-int moe_ffn_pack_expert(moe_ffn_t h, const void* canon_codes, const void* canon_scales,
-                        void* packed_codes, void* packed_scales, void* stream)
+int moe_ffn_pack_expert(moe_ffn_t h, const void* canon_codes, const void* canon_scales, void* packed,
+                        void* stream)
 {
-    if (!h || !canon_codes || !canon_scales || !packed_codes || !packed_scales)
-        return MOE_ERR_INVALID_ARG;
-    if (!aligned(canon_codes, 16) || !aligned(packed_codes, 16) || !aligned(packed_scales, 16))
-        return MOE_ERR_INVALID_ARG;
-    ExpertLayout L = make_expert_layout(h->cfg.hidden, h->cfg.inter);
+    if (!h || !canon_codes || !canon_scales || !packed) return MOE_ERR_INVALID_ARG;
+    if (!aligned(canon_codes, 16) || !aligned(packed, 16)) return MOE_ERR_INVALID_ARG;
+    const ExpertLayout L = make_expert_layout(h->cfg.hidden, h->cfg.inter);
+    const size_t nc = (size_t)3 * h->cfg.hidden * h->cfg.inter / 2, ns = nc / 16;
+    const char* pk = (const char*)packed;
     const char* cc = (const char*)canon_codes;
-    const char* pc = (const char*)packed_codes;
-    if (cc < pc + L.code_bytes && pc < cc + L.code_bytes) return MOE_ERR_INVALID_ARG;
+    const char* cs = (const char*)canon_scales;
+    if ((cc < pk + L.bytes && pk < cc + nc) || (cs < pk + L.bytes && pk < cs + ns)) return MOE_ERR_INVALID_ARG;
     DeviceGuard guard(h->device);
-    return cuda_rc(launch_pack_expert((const uint8_t*)canon_codes, (const uint8_t*)canon_scales,
-                                      (uint8_t*)packed_codes, (uint8_t*)packed_scales,
+    return cuda_rc(launch_pack_expert((const uint8_t*)canon_codes, (const uint8_t*)canon_scales, (uint8_t*)packed,
                                       h->cfg.hidden, h->cfg.inter, (cudaStream_t)stream));
 }
 
@@ -320,7 +311,7 @@ int moe_ffn_forward_host(moe_ffn_t h, const void* x_host, const int32_t* idx_hos
     if (!h) return MOE_ERR_INVALID_ARG;
     if (T < 0 || T > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
-    if (!x_host || !idx_host || !w_host || !y_host || !tbl || !tbl->codes || !tbl->scales)
+    if (!x_host || !idx_host || !w_host || !y_host || !tbl || !tbl->experts)
         return MOE_ERR_INVALID_ARG;
     DeviceGuard guard(h->device);
     cudaStream_t s = (cudaStream_t)stream;
@@ -382,15 +373,12 @@ int moe_stack_forward(moe_ffn_t h, float* x, const moe_expert_table* tbls,
     if (!x || !tbls || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(topk_idx, 4) || !aligned(topk_w, 4)) return MOE_ERR_INVALID_ARG;
     for (int l = 0; l < L; l++)
-        if (!tbls[l].codes || !tbls[l].scales) return MOE_ERR_INVALID_ARG;
+        if (!tbls[l].experts) return MOE_ERR_INVALID_ARG;
     DeviceGuard guard(h->device);
     cudaStream_t s = (cudaStream_t)stream;
 
-    std::vector<const void*> key(2 * (size_t)L);
-    for (int l = 0; l < L; l++) {
-        key[2 * l] = tbls[l].codes;
-        key[2 * l + 1] = tbls[l].scales;
-    }
+    std::vector<const void*> key((size_t)L);
+    for (int l = 0; l < L; l++) key[l] = tbls[l].experts;
     h->use_clock++;
     for (auto& gph : h->graphs) {
         if (gph.x == x && gph.idx == topk_idx && gph.w == topk_w && gph.L == L && gph.T == T &&

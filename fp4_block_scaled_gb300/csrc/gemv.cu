@@ -61,14 +61,12 @@ namespace {
 #define MOE_TC_STAGES 4
 #endif
 constexpr int kCU = MOE_TC_CU;
-constexpr int kStageCodes = kCU * kUnitCodeBytes;            // 32 KB
-constexpr int kStageSfa = kCU * kUnitSfBytes;                // 2 KB
-constexpr int kStageB = kCU * kUnitBBytes;                   // 4 KB
-constexpr int kStageSfb = kCU * kUnitSfBytes;                // 2 KB
-constexpr int kOffSfa = kStageCodes;
-constexpr int kOffB = kOffSfa + kStageSfa;
+constexpr int kStageA = kCU * kUnitBytes;                    // kCU units of weights: codes + scale atom each
+constexpr int kStageB = kCU * kUnitBBytes;                   // their activation pieces
+constexpr int kStageSfb = kCU * kUnitSfBytes;                // and the pieces' scale atoms
+constexpr int kOffB = kStageA;
 constexpr int kOffSfb = kOffB + kStageB;
-constexpr int kStageBytes = kOffSfb + kStageSfb;
+constexpr int kStageBytes = (kOffSfb + kStageSfb + 1023) / 1024 * 1024;
 constexpr int kStages = MOE_TC_STAGES;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 16;                                 // N = 16 fp32 columns
@@ -125,8 +123,7 @@ static_assert(kPieces == kAccCols && kBRows == kAccCols, "one accumulator column
 constexpr size_t kOneCtaPerSmSmem = 116 * 1024;
 
 struct JobInfo {
-    const uint8_t* code;    // unit 0 of this job's tile
-    const uint8_t* sf;
+    const uint8_t* w;       // unit 0 of this job's weight tile (codes + scale atom per unit)
     const uint8_t* B;       // activation pieces at unit 0
     const uint8_t* Bsf;
     bool ok;
@@ -164,7 +161,7 @@ struct StreamPlan {
     int kgt, kg_half;       // units per tile (incl. half unit), half flag
     int jobs_per_group;     // gate/up: 1 (slot, tile); down: topk slots of (token, tile)
     int ntiles;             // tiles per expert matrix
-    size_t code_off, sf_off, tile_code_bytes, tile_sf_bytes;
+    size_t off, tile_bytes; // the matrix in the expert blob, one tile
     size_t act_bytes, act_sf_bytes;    // per B vector
 };
 
@@ -295,10 +292,10 @@ __device__ __forceinline__ void job_slot(const GemvArgs& a, const StreamPlan& p,
 }
 
 // A job's weight and activation sources, given its slot's expert id e and that
-// expert's pointers (cb, sb; read only when e is in range).
+// expert's blob (read only when e is in range).
 template <int PHASE>
 __device__ __forceinline__ JobInfo job_info_e(const GemvArgs& a, const StreamPlan& p, int j, int tile, int e,
-                                              const uint8_t* cb, const uint8_t* sb)
+                                              const uint8_t* blob)
 {
     JobInfo ji;
     if (PHASE == 0) {        // B = pieces of the slot's token
@@ -309,10 +306,8 @@ __device__ __forceinline__ JobInfo job_info_e(const GemvArgs& a, const StreamPla
         ji.B = a.hq + (size_t)j * p.act_bytes;
         ji.Bsf = a.hsf + (size_t)j * p.act_sf_bytes;
     }
-    ji.ok = e >= 0 && e < a.E && cb && sb &&
-            ((reinterpret_cast<uintptr_t>(cb) | reinterpret_cast<uintptr_t>(sb)) & 15) == 0;
-    ji.code = ji.ok ? cb + p.code_off + (size_t)tile * p.tile_code_bytes : nullptr;
-    ji.sf = ji.ok ? sb + p.sf_off + (size_t)tile * p.tile_sf_bytes : nullptr;
+    ji.ok = e >= 0 && e < a.E && blob && (reinterpret_cast<uintptr_t>(blob) & 15) == 0;
+    ji.w = ji.ok ? blob + p.off + (size_t)tile * p.tile_bytes : nullptr;
     return ji;
 }
 
@@ -323,7 +318,7 @@ __device__ __forceinline__ JobInfo job_info(const GemvArgs& a, const StreamPlan&
     job_slot<PHASE>(a, p, job, j, tile);
     const int e = a.idx[j];
     const bool in = e >= 0 && e < a.E;
-    return job_info_e<PHASE>(a, p, j, tile, e, in ? a.codes[e] : nullptr, in ? a.scales[e] : nullptr);
+    return job_info_e<PHASE>(a, p, j, tile, e, in ? a.experts[e] : nullptr);
 }
 
 __device__ __forceinline__ long long range_start(const StreamPlan& p, int c)
@@ -438,8 +433,7 @@ __device__ bool produce(const GemvArgs& a, const StreamPlan& p, const Range& r, 
         const uint32_t nun = wk.chunk();
         const bool has_half = p.kg_half && (wk.kg + nun == kgt);
         const uint32_t nfull = nun - (has_half ? 1u : 0u);
-        const uint32_t cb = nfull * kUnitCodeBytes + (has_half ? kMmaCodeBytes : 0);
-        const uint32_t sb = nun * kUnitSfBytes;
+        const uint32_t wb = nfull * kUnitBytes + (has_half ? kHalfUnitBytes : 0);   // one copy
         const uint32_t bb = nfull * kUnitBBytes + (has_half ? kMmaBBytes : 0);
         const uint32_t bsb = nun * kUnitSfBytes;
         const int s = n % kStages;
@@ -449,9 +443,8 @@ __device__ bool produce(const GemvArgs& a, const StreamPlan& p, const Range& r, 
         }
         uint8_t* stg = sm.stage[s];
         if (ji.ok) {
-            mbar_arrive_expect_tx(&sm.full[s], cb + sb + bb + bsb);
-            bulk_g2s(stg, ji.code + (size_t)wk.kg * kUnitCodeBytes, cb, &sm.full[s]);
-            bulk_g2s(stg + kOffSfa, ji.sf + (size_t)wk.kg * kUnitSfBytes, sb, &sm.full[s]);
+            mbar_arrive_expect_tx(&sm.full[s], wb + bb + bsb);
+            bulk_g2s(stg, ji.w + (size_t)wk.kg * kUnitBytes, wb, &sm.full[s]);
             sm.bsrc[s] = BSrc{ji.B + (size_t)wk.kg * kUnitBBytes, ji.Bsf + (size_t)wk.kg * kUnitSfBytes, bb, bsb,
                               PHASE};
         } else {
@@ -548,11 +541,12 @@ __device__ void issue(const GemvArgs& a, const StreamPlan& p, const Range& r, Tc
             tc_fence_after();
             const uint8_t* st = sm.stage[s];
             const uint32_t col = tmem + kSfCol0 + (uint32_t)(s * kCU + ii) * 8;
-            tc_cp_sf(col, umma_desc(smem_u32(st + kOffSfa + ii * kUnitSfBytes), 16, 128));
-            tc_cp_sf(col + 4, umma_desc(smem_u32(st + kOffSfb + ii * kUnitSfBytes), 16, 128));
             const bool half = p.kg_half && (wk.kg + (uint32_t)ii == kgt - 1);
+            const uint8_t* unit = st + ii * kUnitBytes;            // codes, then the scale atom
+            tc_cp_sf(col, umma_desc(smem_u32(unit + (half ? kMmaCodeBytes : kUnitCodeBytes)), 16, 128));
+            tc_cp_sf(col + 4, umma_desc(smem_u32(st + kOffSfb + ii * kUnitSfBytes), 16, 128));
             for (int m = 0; m < (half ? 1 : 2); m++) {
-                const uint64_t ad = umma_desc(smem_u32(st + ii * kUnitCodeBytes + m * kMmaCodeBytes), 128, 256);
+                const uint64_t ad = umma_desc(smem_u32(unit + m * kMmaCodeBytes), 128, 256);
                 const uint64_t bd = umma_desc(smem_u32(st + kOffB + ii * kUnitBBytes + m * kMmaBBytes), 128, 256);
                 tc_mma_mxf4(tmem + (uint32_t)(ii * 2 + is.buf) * kAccCols, ad, bd, mxf4_idesc_sf(idesc, 2 * m), col,
                             col + 4, any ? 1u : 0u);
@@ -830,17 +824,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(GemvArgs a, StreamPlan p0
         if (h1) job_slot<1>(a, p1, r1.j0 + lane, j1, t1);
         const int e0 = h0 ? a.idx[j0] : -1, e1 = h1 ? a.idx[j1] : -1;
         const bool in0 = e0 >= 0 && e0 < a.E, in1 = e1 >= 0 && e1 < a.E;
-        const uint8_t* cb0 = in0 ? a.codes[e0] : nullptr;
-        const uint8_t* sb0 = in0 ? a.scales[e0] : nullptr;
-        const uint8_t* cb1 = in1 ? a.codes[e1] : nullptr;
-        const uint8_t* sb1 = in1 ? a.scales[e1] : nullptr;
+        const uint8_t* b0 = in0 ? a.experts[e0] : nullptr;
+        const uint8_t* b1 = in1 ? a.experts[e1] : nullptr;
         if (h0) {
-            const JobInfo ji = job_info_e<0>(a, p0, j0, t0, e0, cb0, sb0);
+            const JobInfo ji = job_info_e<0>(a, p0, j0, t0, e0, b0);
             sm.jobs[0][lane] = ji;
             if (!ji.ok) atomicOr(a.status, kStatusBadIndex);
         }
         if (h1) {
-            const JobInfo ji = job_info_e<1>(a, p1, j1, t1, e1, cb1, sb1);
+            const JobInfo ji = job_info_e<1>(a, p1, j1, t1, e1, b1);
             sm.jobs[1][lane] = ji;
             if (!ji.ok) atomicOr(a.status, kStatusBadIndex);
         }
@@ -951,20 +943,17 @@ StreamPlan make_plan(const GemvArgs& a, int phase)
     p.kgt = L.kgt();
     p.kg_half = L.kg_half;
     p.ntiles = L.tiles;
-    p.tile_code_bytes = L.tile_code_bytes();
-    p.tile_sf_bytes = L.tile_sf_bytes();
+    p.tile_bytes = L.tile_bytes();
     if (phase == 0) {
         p.U = (long long)a.T * a.topk * L.tiles * p.kgt;
         p.jobs_per_group = 1;
-        p.code_off = E.gu_code_off;
-        p.sf_off = E.gu_sf_off;
+        p.off = E.gu_off;
         p.act_bytes = act_bytes(a.H);
         p.act_sf_bytes = act_sf_bytes(a.H);
     } else {
         p.U = (long long)a.T * L.tiles * a.topk * p.kgt;
         p.jobs_per_group = a.topk;
-        p.code_off = E.dn_code_off;
-        p.sf_off = E.dn_sf_off;
+        p.off = E.dn_off;
         p.act_bytes = act_bytes(a.I);
         p.act_sf_bytes = act_sf_bytes(a.I);
     }

@@ -61,8 +61,7 @@ constexpr int kGCU = kGIssuers;                              // units per stage:
 constexpr int kGStagesA = 5;                                 // weights (HBM): the deep ring
 constexpr int kGStagesB = 4;                                 // pieces (L2, issued later)
 constexpr int kGUnitB = 2 * kGroupN * 32;                    // B bytes of a unit at N = 64
-constexpr int kGOffSfa = kGCU * kUnitCodeBytes;              // 24 KB of weight codes, then their scale atoms
-constexpr int kGStageA = 26 * 1024;
+constexpr int kGStageA = 26 * 1024;                          // kGCU units of weights (codes + scale atom each)
 constexpr int kGOffSfb = kGCU * kGUnitB;                     // 12 KB of pieces, then their scale atoms
 constexpr int kGStageB = 14 * 1024;
 constexpr int kGTmemCols = 512;
@@ -77,7 +76,7 @@ constexpr int kGThreads = (kGWarpLoader + 1) * 32;
 // debug builds only: event timestamps of one CTA ([role][idx], ns) and per-CTA milestones
 }  // namespace
 __device__ long long g_gtrace[4][8192];
-__device__ long long g_gcta[8][1024];
+__device__ long long g_gcta[16][1024];
 __device__ int g_gtrace_cta;
 namespace {
 #define G_TRACE(role, idx)                                                                               \
@@ -85,6 +84,9 @@ namespace {
         if ((int)blockIdx.x == g_gtrace_cta && (idx) < 8192) g_gtrace[role][idx] = (long long)globaltimer_ns(); \
     } while (0)
 #define G_CTA(slot) (g_gcta[slot][blockIdx.x] = (long long)globaltimer_ns())
+#define G_ACC(var, t0) ((var) += globaltimer_ns() - (t0))
+#define G_ADD(slot, var) (g_gcta[slot][blockIdx.x] += (long long)(var))
+#define G_NOW() globaltimer_ns()
 #else
 #define G_TRACE(role, idx) \
     do {                   \
@@ -92,10 +94,16 @@ namespace {
 #define G_CTA(slot) \
     do {            \
     } while (0)
+#define G_ACC(var, t0) \
+    do {               \
+    } while (0)
+#define G_ADD(slot, var) \
+    do {                 \
+    } while (0)
+#define G_NOW() 0ull
 #endif
 
-static_assert(kGOffSfa + kGCU * kUnitSfBytes <= kGStageA && kGOffSfb + kGCU * kUnitSfBytes <= kGStageB,
-              "stage sizes");
+static_assert(kGCU * kUnitBytes <= kGStageA && kGOffSfb + kGCU * kUnitSfBytes <= kGStageB, "stage sizes");
 static_assert(kGStageA % 1024 == 0 && kGStageB % 1024 == 0, "stage alignment");
 static_assert(kGSfCol0 + kGStagesA * kGCU * 8 <= kGTmemCols, "tensor memory budget");
 static_assert(kGStagesB <= kGStagesA, "the activation ring is the shallower one");
@@ -106,8 +114,7 @@ static_assert(kGroupN % 16 == 0 && kGroupN <= 256, "MMA N");
 constexpr size_t kGOneCtaPerSmSmem = 116 * 1024;
 
 struct GJob {
-    const uint8_t* code;    // weight tile, unit 0
-    const uint8_t* sf;
+    const uint8_t* w;       // weight tile, unit 0 (codes + scale atom per unit)
     const uint8_t* B;       // the group's pieces, unit 0
     const uint8_t* Bsf;     // the group's scale atoms, unit 0
     int nt, p0, tile, g;    // slots, first sorted position, weight tile, group
@@ -127,8 +134,8 @@ struct GSmem {
     uint64_t fullA[kGStagesA];   // the stage's weights landed
     uint64_t emptyA[kGStagesA];  // the issuers are done with them
     uint64_t posted[kGStagesA];  // the producer issued them and posted bsrc
-    uint64_t fullB[kGStagesB];   // the stage's pieces landed
-    uint64_t emptyB[kGStagesB];
+    uint64_t fullB[kGStagesB];   // the stage's pieces landed (the slot is free again once
+                                 // the weight stage of the chunk it held is empty)
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain[kGIssuers];
@@ -143,7 +150,7 @@ static_assert(sizeof(GSmem) <= 227 * 1024, "shared memory per CTA");
 // One projection's unit stream (host part; the job count is read on the device).
 struct GPlan {
     int kgt, kg_half, ntiles;
-    size_t code_off, sf_off, tile_code_bytes, tile_sf_bytes;
+    size_t off, tile_bytes; // the matrix in the expert blob, one tile
     size_t act_bytes;       // piece bytes of one slot over K
     int gs, np;             // slots per group (at most), pieces per slot
     int phase;
@@ -408,8 +415,7 @@ struct GCursor {
     int b, c, t;                 // tile pair, group within the expert, tile of the pair
     int gb, ng, cnt, p0e;        // the expert's first group, groups, slots, first sorted position
     int ngroups, gs;
-    const uint8_t* cb;
-    const uint8_t* sb;
+    const uint8_t* blob;         // the expert's packed blob
     bool ok;
 
     __device__ void enter(const GroupArgs& a, int gl)
@@ -419,9 +425,8 @@ struct GCursor {
         ng = gi.ng;
         cnt = gi.cnt;
         p0e = gi.p0 - (gl - gi.gb) * gs;
-        cb = a.codes[gi.e];
-        sb = a.scales[gi.e];
-        ok = cb && sb && ((reinterpret_cast<uintptr_t>(cb) | reinterpret_cast<uintptr_t>(sb)) & 15) == 0;
+        blob = a.experts[gi.e];
+        ok = blob && (reinterpret_cast<uintptr_t>(blob) & 15) == 0;
     }
     __device__ void init(const GroupArgs& a, const GPlan& p, uint32_t job, int ngroups_)
     {
@@ -465,8 +470,7 @@ struct GCursor {
         j.B = (PHASE == 0 ? a.xg : a.hg) + (size_t)j.p0 * p.act_bytes;
         j.Bsf = (PHASE == 0 ? a.xgsf : a.hgsf) + (size_t)j.g * p.kgt * kUnitSfBytes;
         j.ok = ok;
-        j.code = ok ? cb + p.code_off + (size_t)j.tile * p.tile_code_bytes : nullptr;
-        j.sf = ok ? sb + p.sf_off + (size_t)j.tile * p.tile_sf_bytes : nullptr;
+        j.w = ok ? blob + p.off + (size_t)j.tile * p.tile_bytes : nullptr;
         return j;
     }
 };
@@ -507,26 +511,27 @@ __device__ bool gproduce(const GroupArgs& a, const GPlan& p, const GRange& r, GS
     cur.init(a, p, wk.job, r.ngroups);
     GJob ji = cur.job<PHASE>(a, p);
     if (!ji.ok) atomicOr(a.status, kStatusBadIndex);
+    uint64_t w_e = 0;                          // debug builds: time spent waiting
     while (wk.u < wk.u1) {
         const uint32_t nun = wk.chunk();
         const bool has_half = p.kg_half && (wk.kg + nun == wk.kgt);
         const uint32_t nfull = nun - (has_half ? 1u : 0u);
-        const uint32_t cb = nfull * kUnitCodeBytes + (has_half ? kMmaCodeBytes : 0);
-        const uint32_t sb = nun * kUnitSfBytes;
+        const uint32_t wb = nfull * kUnitBytes + (has_half ? kHalfUnitBytes : 0);   // one copy
         const uint32_t ub = 64u * (uint32_t)p.np;                 // piece bytes of a slot per unit
         const uint32_t bb = (uint32_t)ji.nt * (nfull * ub + (has_half ? ub / 2 : 0));
         const uint32_t bsb = nun * kUnitSfBytes;
         const int s = n % kGStagesA;
+        const uint64_t tw = G_NOW();
         if (n >= kGStagesA &&
             !mbar_wait_or_abort(&sm.emptyA[s], ((n / kGStagesA) & 1) ^ 1, &sm.abort, kGWaitLimitNs)) {
             g_set_abort(a, sm);
             return false;
         }
+        G_ACC(w_e, tw);
         uint8_t* stg = sm.stageA[s];
         if (ji.ok) {
-            mbar_arrive_expect_tx(&sm.fullA[s], cb + sb);
-            bulk_g2s(stg, ji.code + (size_t)wk.kg * kUnitCodeBytes, cb, &sm.fullA[s]);
-            bulk_g2s(stg + kGOffSfa, ji.sf + (size_t)wk.kg * kUnitSfBytes, sb, &sm.fullA[s]);
+            mbar_arrive_expect_tx(&sm.fullA[s], wb);
+            bulk_g2s(stg, ji.w + (size_t)wk.kg * kUnitBytes, wb, &sm.fullA[s]);
             sm.bsrc[s] = GBSrc{ji.B + (size_t)wk.kg * ji.nt * ub, ji.Bsf + (size_t)wk.kg * kUnitSfBytes, bb, bsb,
                                PHASE};
         } else {
@@ -544,6 +549,8 @@ __device__ bool gproduce(const GroupArgs& a, const GPlan& p, const GRange& r, GS
             if (!ji.ok) atomicOr(a.status, kStatusBadIndex);
         }
     }
+    G_ADD(11, w_e);
+    (void)w_e;
     return true;
 }
 
@@ -557,9 +564,14 @@ __device__ void gload_b(const GroupArgs& a, int nchunks, uint32_t h_target, GSme
     int n = 0;
     for (; n < nchunks; n++) {
         const int s = n % kGStagesA, sb = n % kGStagesB;
+        // slot sb last held chunk n - kGStagesB: it is free once that chunk's
+        // weight stage is empty (all issuers committed it).  That barrier cannot
+        // be two phases ahead here: chunk n - kGStagesB + kGStagesA needs pieces
+        // this loop has not issued yet (kGStagesB <= kGStagesA).
+        const int m = n - kGStagesB;
         if (!mbar_wait_or_abort(&sm.posted[s], (n / kGStagesA) & 1, &sm.abort, kGWaitLimitNs) ||
-            (n >= kGStagesB &&
-             !mbar_wait_or_abort(&sm.emptyB[sb], ((n / kGStagesB) & 1) ^ 1, &sm.abort, kGWaitLimitNs))) {
+            (m >= 0 &&
+             !mbar_wait_or_abort(&sm.emptyA[m % kGStagesA], (m / kGStagesA) & 1, &sm.abort, kGWaitLimitNs))) {
             g_set_abort(a, sm);
             break;
         }
@@ -617,25 +629,35 @@ __device__ void gissue(const GroupArgs& a, const GPlan& p, const GRange& r, GSme
     bool any = false;               // this issuer's accumulator holds part of this job
     bool job_start = true;
     const uint32_t ub = 64u * (uint32_t)p.np;
+    uint64_t w_acc = 0, w_a = 0, w_b = 0, w_is = 0, w_all = 0;   // debug builds: time spent waiting / issuing
+    const uint64_t t_begin = G_NOW();
     while (wk.u < wk.u1) {
         const uint32_t nun = wk.chunk();
         const int s = is.n % kGStagesA, sbi = is.n % kGStagesB;
         if (job_start) {
             // the epilogue must have read this accumulator's previous job
+            const uint64_t tw = G_NOW();
             if (!is.abort && is.use[is.buf] > 0 &&
                 !mbar_wait_or_abort(&sm.acc_empty[is.buf], (is.use[is.buf] - 1) & 1, &sm.abort, kGWaitLimitNs)) {
                 g_set_abort(a, sm);
                 is.abort = true;
             }
+            G_ACC(w_acc, tw);
             job_start = false;
         }
-        if (!is.abort &&
-            (!mbar_wait_or_abort(&sm.fullA[s], (is.n / kGStagesA) & 1, &sm.abort, kGWaitLimitNs) ||
-             !mbar_wait_or_abort(&sm.fullB[sbi], (is.n / kGStagesB) & 1, &sm.abort, kGWaitLimitNs))) {
+        const uint64_t tw1 = G_NOW();
+        bool okA = is.abort || mbar_wait_or_abort(&sm.fullA[s], (is.n / kGStagesA) & 1, &sm.abort, kGWaitLimitNs);
+        G_ACC(w_a, tw1);
+        const uint64_t tw2 = G_NOW();
+        bool okB = is.abort || !okA ||
+                   mbar_wait_or_abort(&sm.fullB[sbi], (is.n / kGStagesB) & 1, &sm.abort, kGWaitLimitNs);
+        G_ACC(w_b, tw2);
+        if (!is.abort && (!okA || !okB)) {
             g_set_abort(a, sm);
             is.abort = true;
         }
         if (ii == 0) G_TRACE(1, is.n);
+        const uint64_t tis = G_NOW();
         if (!is.abort && ji.ok && (uint32_t)ii < nun) {
             tc_fence_after();
             const uint8_t* st = sm.stageA[s];
@@ -643,19 +665,20 @@ __device__ void gissue(const GroupArgs& a, const GPlan& p, const GRange& r, GSme
             const uint32_t nt = (uint32_t)ji.nt;
             const uint32_t idesc = mxf4_idesc(kTileRows, ((uint32_t)p.np * nt + 15u) & ~15u);
             const uint32_t col = tmem + kGSfCol0 + (uint32_t)(s * kGCU + ii) * 8;
-            tc_cp_sf(col, umma_desc(smem_u32(st + kGOffSfa + ii * kUnitSfBytes), 16, 128));
-            tc_cp_sf(col + 4, umma_desc(smem_u32(sbs + kGOffSfb + ii * kUnitSfBytes), 16, 128));
             const bool half = p.kg_half && (wk.kg + (uint32_t)ii == wk.kgt - 1);
+            const uint8_t* unit = st + ii * kUnitBytes;            // codes, then the scale atom
+            tc_cp_sf(col, umma_desc(smem_u32(unit + (half ? kMmaCodeBytes : kUnitCodeBytes)), 16, 128));
+            tc_cp_sf(col + 4, umma_desc(smem_u32(sbs + kGOffSfb + ii * kUnitSfBytes), 16, 128));
             for (uint32_t m = 0; m < (half ? 1u : 2u); m++) {
-                const uint64_t ad = umma_desc(smem_u32(st + ii * kUnitCodeBytes + m * kMmaCodeBytes), 128, 256);
+                const uint64_t ad = umma_desc(smem_u32(unit + m * kMmaCodeBytes), 128, 256);
                 const uint64_t bd = umma_desc(smem_u32(sbs + ii * nt * ub + m * nt * (ub / 2)), 128, 256);
                 tc_mma_mxf4(tmem + (uint32_t)(ii * 2 + is.buf) * kGAccCols, ad, bd, mxf4_idesc_sf(idesc, 2 * m),
                             col, col + 4, any ? 1u : 0u);
                 any = true;
             }
         }
-        tc_commit(&sm.emptyA[s]);          // this issuer's part of the stage is consumed
-        tc_commit(&sm.emptyB[sbi]);
+        tc_commit(&sm.emptyA[s]);          // this issuer's part of the stage (weights and pieces) is consumed
+        G_ACC(w_is, tis);
         bool nj;
         const bool jend = wk.advance(nun, nj);
         is.n++;
@@ -671,6 +694,20 @@ __device__ void gissue(const GroupArgs& a, const GPlan& p, const GRange& r, GSme
             job_start = true;
         }
     }
+    G_ACC(w_all, t_begin);
+    if (ii == 0) {
+        G_ADD(8, w_acc);
+        G_ADD(9, w_a);
+        G_ADD(10, w_b);
+        G_ADD(12, w_is);
+        G_ADD(13, w_all);
+    }
+    (void)w_acc;
+    (void)w_a;
+    (void)w_b;
+    (void)w_is;
+    (void)w_all;
+    (void)t_begin;
 }
 
 // ------------------------------------------------------------------ epilogue
@@ -937,10 +974,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_glayer(GroupArgs a, GPlan p0, 
             mbar_init(&sm.emptyA[s], kGIssuers);
             mbar_init(&sm.posted[s], 1);
         }
-        for (int s = 0; s < kGStagesB; s++) {
-            mbar_init(&sm.fullB[s], 1);
-            mbar_init(&sm.emptyB[s], kGIssuers);
-        }
+        for (int s = 0; s < kGStagesB; s++) mbar_init(&sm.fullB[s], 1);
         for (int b = 0; b < 2; b++) {
             mbar_init(&sm.acc_full[b], kGIssuers);
             mbar_init(&sm.acc_empty[b], 4);
@@ -1087,10 +1121,8 @@ GPlan gplan(const GroupArgs& a, int phase)
     p.kgt = L.kgt();
     p.kg_half = L.kg_half;
     p.ntiles = L.tiles;
-    p.tile_code_bytes = L.tile_code_bytes();
-    p.tile_sf_bytes = L.tile_sf_bytes();
-    p.code_off = phase == 0 ? E.gu_code_off : E.dn_code_off;
-    p.sf_off = phase == 0 ? E.gu_sf_off : E.dn_sf_off;
+    p.tile_bytes = L.tile_bytes();
+    p.off = phase == 0 ? E.gu_off : E.dn_off;
     p.np = group_pieces(a.act_e4m3 != 0);
     p.gs = group_slots(a.act_e4m3 != 0);
     p.act_bytes = g_act_bytes(phase == 0 ? a.H : a.I, p.np);

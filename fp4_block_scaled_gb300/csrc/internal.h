@@ -24,8 +24,7 @@ struct GemvArgs {
     float eps;
     const int32_t* idx;
     const float* w;
-    const uint8_t* const* codes;
-    const uint8_t* const* scales;
+    const uint8_t* const* experts;      // per expert: the packed blob (layout.h)
     // workspace
     uint8_t* xq;                        // [T][act_bytes(H)] activation pieces (B operand)
     uint8_t* xsf;                       // [T][act_sf_bytes(H)] their scale atoms
@@ -141,8 +140,7 @@ struct GroupArgs {
     float eps;
     const int32_t* idx;
     const float* w;
-    const uint8_t* const* codes;
-    const uint8_t* const* scales;
+    const uint8_t* const* experts;      // per expert: the packed blob (layout.h)
     // routing workspace (filled by the route kernel of the layer)
     int32_t *counts, *offsets, *perm, *inv, *gbase;
     GroupInfo* groups;
@@ -191,8 +189,7 @@ cudaError_t launch_act_quant(const ActQuantArgs& a, cudaStream_t s, bool pdl);
 // Host-side config validation shared by the entry points (api.cu).
 int check_config(const moe_ffn_config* cfg);
 
-cudaError_t launch_pack_expert(const uint8_t* canon_codes, const uint8_t* canon_scales,
-                               uint8_t* packed_codes, uint8_t* packed_scales, int H, int I,
-                               cudaStream_t s);
+cudaError_t launch_pack_expert(const uint8_t* canon_codes, const uint8_t* canon_scales, uint8_t* packed,
+                               int H, int I, cudaStream_t s);
 
 }  // namespace moe

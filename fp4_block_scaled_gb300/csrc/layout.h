@@ -7,18 +7,20 @@
 // units of 128 elements (two MMAs of K = 64, four ue8m0 blocks of 32), plus one
 // half unit of 64 when K % 128 == 64.
 //
-// Codes of a unit (8 KB; 4 KB for a half unit) are stored as the MMA reads
-// them from shared memory: per MMA m (4 KB), 16 row groups of 8 rows, each
-// holding two "core matrices" of 8 rows x 16 bytes (the two 32-element blocks
-// of that MMA's K range), i.e. offset = m*4096 + (row/8)*256 + c*128 +
-// (row%8)*16 for block 2m+c of the unit.  Scales of a unit are one 512-byte
-// atom: byte (row%32)*16 + (row/32)*4 + kb holds the scale of block kb of row
-// `row` -- the order in which tcgen05.cp moves 32 lanes x 128 bits into the
-// tensor memory for 128 rows.  A half unit's atom leaves bytes kb = 2, 3 at
-// 127 (scale 1, never read).  Tiles are stored one after another and units of
-// a tile are adjacent, so a run of units is one contiguous span of codes and
-// one of scales.  Codes are a pure permutation of the published layout; the
-// scales of a half unit are padded from 256 to 512 bytes.
+// A unit is its codes followed by its scale atom, so that one bulk copy moves
+// any run of units, codes and scales together:
+//   codes (8 KB; 4 KB for a half unit), stored as the MMA reads them from
+//   shared memory: per MMA m (4 KB), 16 row groups of 8 rows, each holding two
+//   "core matrices" of 8 rows x 16 bytes (the two 32-element blocks of that
+//   MMA's K range), i.e. offset = m*4096 + (row/8)*256 + c*128 + (row%8)*16
+//   for block 2m+c of the unit;
+//   then one 512-byte scale atom: byte (row%32)*16 + (row/32)*4 + kb holds the
+//   scale of block kb of row `row` -- the order in which tcgen05.cp moves 32
+//   lanes x 128 bits into the tensor memory for 128 rows.  A half unit's atom
+//   leaves bytes kb = 2, 3 at 127 (scale 1, never read).
+// Tiles are stored one after another, gate/up tiles first, in one blob per
+// expert.  The blob holds every code and scale byte of the published layout
+// once (a permutation), plus 256 padding bytes per half-unit atom.
 #pragma once
 #include <stddef.h>
 #include <stdint.h>
@@ -29,6 +31,8 @@ constexpr int kTileRows = 128;
 constexpr int kUnitCodeBytes = 8192;   // 128 rows x 128 E2M1 codes
 constexpr int kMmaCodeBytes = 4096;    // one MMA (K = 64)
 constexpr int kUnitSfBytes = 512;      // scale atom of a unit
+constexpr int kUnitBytes = kUnitCodeBytes + kUnitSfBytes;       // a full unit in the blob
+constexpr int kHalfUnitBytes = kMmaCodeBytes + kUnitSfBytes;    // a half unit in the blob
 
 struct MatLayout {
     int rows;      // matrix rows
@@ -37,11 +41,10 @@ struct MatLayout {
     int kg_full;   // k / 128
     int kg_half;   // 1 if k % 128 == 64
     __host__ __device__ int kgt() const { return kg_full + kg_half; }
-    __host__ __device__ size_t tile_code_bytes() const
+    __host__ __device__ size_t tile_bytes() const
     {
-        return (size_t)kg_full * kUnitCodeBytes + (size_t)kg_half * kMmaCodeBytes;
+        return (size_t)kg_full * kUnitBytes + (size_t)kg_half * kHalfUnitBytes;
     }
-    __host__ __device__ size_t tile_sf_bytes() const { return (size_t)kgt() * kUnitSfBytes; }
 };
 
 __host__ __device__ inline MatLayout make_layout(int rows, int k)
@@ -58,8 +61,7 @@ __host__ __device__ inline MatLayout make_layout(int rows, int k)
 struct ExpertLayout {
     MatLayout gu;   // 2*I rows (gate / up halves per tile), K = H
     MatLayout dn;   // H rows, K = I
-    size_t gu_code_off, dn_code_off, code_bytes;
-    size_t gu_sf_off, dn_sf_off, sf_bytes;
+    size_t gu_off, dn_off, bytes;
 };
 
 __host__ __device__ inline ExpertLayout make_expert_layout(int hidden, int inter)
@@ -67,12 +69,9 @@ __host__ __device__ inline ExpertLayout make_expert_layout(int hidden, int inter
     ExpertLayout L;
     L.gu = make_layout(2 * inter, hidden);
     L.dn = make_layout(hidden, inter);
-    L.gu_code_off = 0;
-    L.dn_code_off = (size_t)L.gu.tiles * L.gu.tile_code_bytes();
-    L.code_bytes = L.dn_code_off + (size_t)L.dn.tiles * L.dn.tile_code_bytes();
-    L.gu_sf_off = 0;
-    L.dn_sf_off = (size_t)L.gu.tiles * L.gu.tile_sf_bytes();
-    L.sf_bytes = L.dn_sf_off + (size_t)L.dn.tiles * L.dn.tile_sf_bytes();
+    L.gu_off = 0;
+    L.dn_off = (size_t)L.gu.tiles * L.gu.tile_bytes();
+    L.bytes = L.dn_off + (size_t)L.dn.tiles * L.dn.tile_bytes();
     return L;
 }
 

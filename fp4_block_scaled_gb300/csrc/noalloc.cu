@@ -81,7 +81,7 @@ extern "C" int moe_ffn_forward_noalloc(const moe_ffn_config* cfg, int device, co
     if (cfg->act_mode != MOE_ACT_BF16) return MOE_ERR_UNSUPPORTED;
     if (T < 0) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
-    if (!x || !topk_idx || !topk_w || !y || !tbl || !tbl->codes || !tbl->scales || x == y)
+    if (!x || !topk_idx || !topk_w || !y || !tbl || !tbl->experts || x == y)
         return MOE_ERR_INVALID_ARG;
     if (((uintptr_t)x | (uintptr_t)y) % 16 || ((uintptr_t)topk_idx | (uintptr_t)topk_w) % 4 ||
         ((uintptr_t)status) % 4)
@@ -134,8 +134,7 @@ extern "C" int moe_ffn_forward_noalloc(const moe_ffn_config* cfg, int device, co
     a.x_bf16 = (const uint16_t*)x;
     a.idx = topk_idx;
     a.w = topk_w;
-    a.codes = tbl->codes;
-    a.scales = tbl->scales;
+    a.experts = tbl->experts;
     a.xq = (uint8_t*)(b + o_xq);
     a.xsf = (uint8_t*)(b + o_xsf);
     a.hq = (uint8_t*)(b + o_hq);

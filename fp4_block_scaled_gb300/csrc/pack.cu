@@ -5,7 +5,7 @@
 // matrix order of layout.h, so that the decode kernels stream contiguous units
 // with bulk copies straight into the shared-memory layout the tensor-core MMA
 // reads, and the scale atoms straight into the form tcgen05.cp moves to the
-// tensor memory.
+// tensor memory; each unit's atom follows its codes in the one blob.
 #include "internal.h"
 
 namespace moe {
@@ -35,10 +35,10 @@ __device__ inline void canon_row(const SectionMap& s, int tile, int r, int k, co
     srow = s.scales + sbase + row * (k / 32);
 }
 
-// One thread per 16-byte chunk (one row x one 32-element block).
+// One thread per 16-byte chunk of codes (one row x one 32-element block).
 __global__ void pack_codes_kernel(SectionMap s, MatLayout L, uint8_t* out)
 {
-    const size_t per_tile = L.tile_code_bytes() / 16;
+    const size_t per_tile = ((size_t)L.kg_full * kUnitCodeBytes + (size_t)L.kg_half * kMmaCodeBytes) / 16;
     const size_t total = per_tile * L.tiles;
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t qi = (size_t)blockIdx.x * blockDim.x + threadIdx.x; qi < total; qi += stride) {
@@ -51,14 +51,15 @@ __global__ void pack_codes_kernel(SectionMap s, MatLayout L, uint8_t* out)
         const int block = kg * 4 + m * 2 + c;
         const uint8_t *crow, *srow;
         canon_row(s, tile, row, L.k, crow, srow);
-        reinterpret_cast<uint4*>(out)[qi] = *reinterpret_cast<const uint4*>(crow + (size_t)block * 16);
+        uint8_t* dst = out + (size_t)tile * L.tile_bytes() + (size_t)kg * kUnitBytes + (size_t)r * 16;
+        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(crow + (size_t)block * 16);
     }
 }
 
-// One thread per scale-atom byte.
+// One thread per scale-atom byte; a unit's atom follows its codes.
 __global__ void pack_scales_kernel(SectionMap s, MatLayout L, uint8_t* out)
 {
-    const size_t per_tile = L.tile_sf_bytes();
+    const size_t per_tile = (size_t)L.kgt() * kUnitSfBytes;
     const size_t total = per_tile * L.tiles;
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t bi = (size_t)blockIdx.x * blockDim.x + threadIdx.x; bi < total; bi += stride) {
@@ -67,13 +68,16 @@ __global__ void pack_scales_kernel(SectionMap s, MatLayout L, uint8_t* out)
         const int kg = q / kUnitSfBytes, b = q % kUnitSfBytes;
         const int row = b / 16 + 32 * ((b % 16) / 4);
         const int kb = b % 4;
-        if (kg == L.kg_full && kb >= 2) {      // padding of a half unit
-            out[bi] = 127;
+        const bool half = kg == L.kg_full;
+        uint8_t* dst = out + (size_t)tile * L.tile_bytes() + (size_t)kg * kUnitBytes +
+                       (half ? kMmaCodeBytes : kUnitCodeBytes) + b;
+        if (half && kb >= 2) {      // padding of a half unit
+            *dst = 127;
             continue;
         }
         const uint8_t *crow, *srow;
         canon_row(s, tile, row, L.k, crow, srow);
-        out[bi] = srow[kg * 4 + kb];
+        *dst = srow[kg * 4 + kb];
     }
 }
 
@@ -85,22 +89,22 @@ int grid_for(size_t n)
 
 }  // namespace
 
-cudaError_t launch_pack_expert(const uint8_t* cc, const uint8_t* cs, uint8_t* pc, uint8_t* ps,
-                               int H, int I, cudaStream_t st)
+cudaError_t launch_pack_expert(const uint8_t* cc, const uint8_t* cs, uint8_t* packed, int H, int I,
+                               cudaStream_t st)
 {
     ExpertLayout E = make_expert_layout(H, I);
     const size_t gu_c = (size_t)I * H / 2, gu_s = (size_t)I * H / 32;
     SectionMap gu{cc, cs, 1, gu_c, gu_s};
     SectionMap dn{cc + 2 * gu_c, cs + 2 * gu_s, 0, 0, 0};
     size_t n;
-    n = E.gu.tiles * E.gu.tile_code_bytes() / 16;
-    pack_codes_kernel<<<grid_for(n), 256, 0, st>>>(gu, E.gu, pc + E.gu_code_off);
-    n = E.dn.tiles * E.dn.tile_code_bytes() / 16;
-    pack_codes_kernel<<<grid_for(n), 256, 0, st>>>(dn, E.dn, pc + E.dn_code_off);
-    n = E.gu.tiles * E.gu.tile_sf_bytes();
-    pack_scales_kernel<<<grid_for(n), 256, 0, st>>>(gu, E.gu, ps + E.gu_sf_off);
-    n = E.dn.tiles * E.dn.tile_sf_bytes();
-    pack_scales_kernel<<<grid_for(n), 256, 0, st>>>(dn, E.dn, ps + E.dn_sf_off);
+    n = (size_t)E.gu.tiles * E.gu.kg_full * 512 + (size_t)E.gu.tiles * E.gu.kg_half * 256;
+    pack_codes_kernel<<<grid_for(n), 256, 0, st>>>(gu, E.gu, packed + E.gu_off);
+    n = (size_t)E.dn.tiles * E.dn.kg_full * 512 + (size_t)E.dn.tiles * E.dn.kg_half * 256;
+    pack_codes_kernel<<<grid_for(n), 256, 0, st>>>(dn, E.dn, packed + E.dn_off);
+    n = (size_t)E.gu.tiles * E.gu.kgt() * kUnitSfBytes;
+    pack_scales_kernel<<<grid_for(n), 256, 0, st>>>(gu, E.gu, packed + E.gu_off);
+    n = (size_t)E.dn.tiles * E.dn.kgt() * kUnitSfBytes;
+    pack_scales_kernel<<<grid_for(n), 256, 0, st>>>(dn, E.dn, packed + E.dn_off);
     return cudaGetLastError();
 }
 

@@ -1,7 +1,7 @@
-"""Device-resident expert sets: packed weight buffers and pointer tables.
+"""Device-resident expert sets: packed expert blobs and their pointer table.
 
-Holds the E packed experts of one layer in two device allocations (codes and
-scales, one fixed-size slot per expert) plus the two device arrays of expert
+Holds the E packed experts of one layer in one device allocation (one
+fixed-size slot per expert, 256-byte aligned) plus the device array of expert
 pointers that a moe_expert_table refers to.  torch provides the memory; the
 re-layout itself is moe_ffn_pack_expert.
 """
@@ -9,8 +9,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (config, expert_table, moe_ffn_packed_codes_bytes, moe_ffn_packed_scales_bytes,
-               moe_ffn_pack_expert)
+from . import config, expert_table, moe_ffn_packed_expert_bytes, moe_ffn_pack_expert
 
 
 class ExpertSet:
@@ -18,34 +17,24 @@ class ExpertSet:
         self.handle = handle
         self.cfg = cfg
         self.E = cfg.num_experts if num_experts is None else num_experts
-        self.code_bytes = moe_ffn_packed_codes_bytes(cfg)
-        self.scale_bytes = moe_ffn_packed_scales_bytes(cfg)
+        self.blob_bytes = moe_ffn_packed_expert_bytes(cfg)
         dev = torch.device("cuda", device)
         # slots padded to 256 bytes so every expert starts aligned
-        self.code_stride = (self.code_bytes + 255) // 256 * 256
-        self.scale_stride = (self.scale_bytes + 255) // 256 * 256
-        self.codes = torch.empty(self.E * self.code_stride, dtype=torch.uint8, device=dev)
-        self.scales = torch.empty(self.E * self.scale_stride, dtype=torch.uint8, device=dev)
-        cb, sb = self.codes.data_ptr(), self.scales.data_ptr()
-        self.code_ptrs = torch.tensor([cb + e * self.code_stride for e in range(self.E)],
-                                      dtype=torch.int64, device=dev)
-        self.scale_ptrs = torch.tensor([sb + e * self.scale_stride for e in range(self.E)],
-                                       dtype=torch.int64, device=dev)
-        self.table = expert_table(self.code_ptrs, self.scale_ptrs)
+        self.stride = (self.blob_bytes + 255) // 256 * 256
+        self.blobs = torch.empty(self.E * self.stride, dtype=torch.uint8, device=dev)
+        base = self.blobs.data_ptr()
+        self.ptrs = torch.tensor([base + e * self.stride for e in range(self.E)], dtype=torch.int64, device=dev)
+        self.table = expert_table(self.ptrs)
 
-    def code_slot(self, e: int) -> int:
-        return self.codes.data_ptr() + e * self.code_stride
-
-    def scale_slot(self, e: int) -> int:
-        return self.scales.data_ptr() + e * self.scale_stride
+    def slot(self, e: int) -> int:
+        return self.blobs.data_ptr() + e * self.stride
 
     def load(self, e: int, canon_codes, canon_scales, stream=None) -> None:
         """Pack one expert from the published layout (device buffers)."""
-        moe_ffn_pack_expert(self.handle, canon_codes, canon_scales, self.code_slot(e),
-                            self.scale_slot(e), stream)
+        moe_ffn_pack_expert(self.handle, canon_codes, canon_scales, self.slot(e), stream)
 
     def bytes(self) -> int:
-        return self.E * (self.code_bytes + self.scale_bytes)
+        return self.E * self.blob_bytes
 
 
 __all__ = ["ExpertSet", "config"]

@@ -84,20 +84,21 @@ typedef struct {
  * compute the same function within the float tolerance. */
 #define MOE_DEFAULT_GEMM_MIN_TOKENS 16
 
-/* One layer's experts.  codes / scales are DEVICE arrays of E DEVICE pointers,
- * each to one expert's blob in the packed layout made by moe_ffn_pack_expert.
- * A NULL entry is allowed for an expert that is never routed to. */
+/* One layer's experts.  experts is a DEVICE array of E DEVICE pointers, each
+ * to one expert's packed blob (moe_ffn_packed_expert_bytes bytes, 16-byte
+ * aligned) made by moe_ffn_pack_expert.  A NULL entry is allowed for an expert
+ * that is never routed to. */
 typedef struct {
-    const uint8_t* const* codes;
-    const uint8_t* const* scales;
+    const uint8_t* const* experts;
 } moe_expert_table;
 
-/* Bytes of one expert's packed codes (3*I*H/2) and packed scales (3*I*H/32):
- * the same sizes as the published layout ([8GB] §方案：不重写模型，只迁移其存储:
- * 17.7 MB of codes and 1.1 MB of scales at H = 4096, I = 2880).
- * Returns 0 for an invalid config. */
-size_t moe_ffn_packed_codes_bytes(const moe_ffn_config* cfg);
-size_t moe_ffn_packed_scales_bytes(const moe_ffn_config* cfg);
+/* Bytes of one expert's packed blob: every code and scale byte of the
+ * published layout ([8GB] §方案：不重写模型，只迁移其存储: 3*I*H/2 = 17.7 MB of
+ * codes and 3*I*H/32 = 1.1 MB of scales at H = 4096, I = 2880), re-laid out,
+ * plus 256 padding bytes per half-unit scale atom (H/128 of them when
+ * I % 128 == 64): 18,808,832 bytes at H = 4096, I = 2880.  Returns 0 for an
+ * invalid config. */
+size_t moe_ffn_packed_expert_bytes(const moe_ffn_config* cfg);
 
 /* Validate cfg, select `device`, allocate the workspace (sized from
  * max_tokens) and return a handle in *out.  Errors: INVALID_ARG (config),
@@ -110,10 +111,13 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device);
  *   canon_codes : gate [I][H/2] | up [I][H/2] | down [H][I/2]   (low nibble =
  *                 even element), canon_scales: gate [I][H/32] | up [I][H/32] |
  *                 down [H][I/32] (one ue8m0 byte per 32 weights of a row).
- * Output: packed_codes (moe_ffn_packed_codes_bytes) and packed_scales, device
- * memory, not overlapping the inputs.  A pure byte permutation. */
-int moe_ffn_pack_expert(moe_ffn_t h, const void* canon_codes, const void* canon_scales,
-                        void* packed_codes, void* packed_scales, void* stream);
+ * Output: packed (moe_ffn_packed_expert_bytes), device memory, 16-byte
+ * aligned, not overlapping the inputs: tiles of 128 rows, each a run of
+ * 128-wide K units, each unit its codes in the tensor-core operand order
+ * followed by its 512-byte scale atom, so that the kernels move a run of
+ * units, codes and scales together, with one bulk copy. */
+int moe_ffn_pack_expert(moe_ffn_t h, const void* canon_codes, const void* canon_scales, void* packed,
+                        void* stream);
 
 /* One MoE layer for T tokens (0 <= T <= max_tokens):
  *   x        device bf16 [T][H]

@@ -28,12 +28,12 @@ def test_library_exports_every_declared_symbol():
 def test_packed_sizes_equal_published_sizes():
     cfg = moe.config(384, 4096, 2880, 6, 1)
     nc, ns = synth.expert_sizes(4096, 2880)
-    assert moe.moe_ffn_packed_codes_bytes(cfg) == nc == 17694720
-    # scale atoms of the 64-wide half unit of each 128-row down tile are padded to 512 B
-    assert ns == 1105920
-    assert moe.moe_ffn_packed_scales_bytes(cfg) == ns + (4096 // 128) * 256
+    assert nc == 17694720 and ns == 1105920
+    # every published code and scale byte once; the scale atom of the 64-wide
+    # half unit of each 128-row down tile is padded from 256 to 512 bytes
+    assert moe.moe_ffn_packed_expert_bytes(cfg) == nc + ns + (4096 // 128) * 256 == 18808832
     cfg = moe.config(8, 256, 128, 2, 1)
-    assert moe.moe_ffn_packed_codes_bytes(cfg) == 3 * 256 * 128 // 2
+    assert moe.moe_ffn_packed_expert_bytes(cfg) == 3 * 256 * 128 // 2 + 3 * 256 * 128 // 32
 
 
 def test_invalid_configs_are_rejected_on_the_host():
@@ -49,7 +49,7 @@ def test_invalid_configs_are_rejected_on_the_host():
         moe.config(8, 4096, 2880, 6, 1, out_dtype=3),
     ]
     for c in bad:
-        assert moe.moe_ffn_packed_codes_bytes(c) == 0
+        assert moe.moe_ffn_packed_expert_bytes(c) == 0
     h = ctypes.c_void_p()
     assert moe.lib().moe_ffn_create(ctypes.byref(h), ctypes.byref(bad[0]), 0) == moe.MOE_ERR_INVALID_ARG
     assert moe.lib().moe_ffn_create(ctypes.byref(h), ctypes.byref(bad[3]), 0) == moe.MOE_ERR_UNSUPPORTED

@@ -35,11 +35,12 @@ def test_device_fill_matches_host_generator():
 
 
 def _pack_reference(codes, scales, H, I):
-    """Independent numpy statement of the packed layout (tiles of 128 rows,
-    units of 128 K, per MMA 16 row groups x 2 core matrices x 8 rows x 16 B;
-    one 512-byte scale atom per unit) used to check moe_ffn_pack_expert."""
+    """Independent numpy statement of the packed blob (tiles of 128 rows, units
+    of 128 K; per unit the codes, per MMA 16 row groups x 2 core matrices x 8
+    rows x 16 B, then one 512-byte scale atom) used to check
+    moe_ffn_pack_expert."""
     def section(cmat, smat, K, rows_of_tile, ntiles):
-        out_c, out_s = [], []
+        out = []
         kgf, half = K // 128, (K % 128) // 64
         for t in range(ntiles):
             rows = rows_of_tile(t)
@@ -49,13 +50,13 @@ def _pack_reference(codes, scales, H, I):
                         for c in range(2):
                             for r8 in range(8):
                                 b = kg * 4 + m * 2 + c
-                                out_c.append(cmat[rows[rg * 8 + r8], b * 16:b * 16 + 16])
+                                out.append(cmat[rows[rg * 8 + r8], b * 16:b * 16 + 16])
                 atom = np.full(512, 127, np.uint8)
                 for r in range(128):
                     for kb in range(2 if kg == kgf else 4):
                         atom[(r % 32) * 16 + (r // 32) * 4 + kb] = smat[rows[r], kg * 4 + kb]
-                out_s.append(atom)
-        return np.concatenate(out_c), np.concatenate(out_s)
+                out.append(atom)
+        return np.concatenate(out)
 
     gc, gs = I * H // 2, I * H // 32
     cg = codes[:gc].reshape(I, H // 2)
@@ -66,9 +67,9 @@ def _pack_reference(codes, scales, H, I):
     sd = scales[2 * gs:].reshape(H, I // 32)
     cgu = np.concatenate([cg, cu])            # rows 0..I-1 gate, I..2I-1 up
     sgu = np.concatenate([sg, su])
-    pc1, ps1 = section(cgu, sgu, H, lambda t: [64 * t + r for r in range(64)] + [I + 64 * t + r for r in range(64)], I // 64)
-    pc2, ps2 = section(cd, sd, I, lambda t: [128 * t + r for r in range(128)], H // 128)
-    return np.concatenate([pc1, pc2]), np.concatenate([ps1, ps2])
+    p1 = section(cgu, sgu, H, lambda t: [64 * t + r for r in range(64)] + [I + 64 * t + r for r in range(64)], I // 64)
+    p2 = section(cd, sd, I, lambda t: [128 * t + r for r in range(128)], H // 128)
+    return np.concatenate([p1, p2])
 
 
 @pytest.mark.parametrize("dims", [TINY, dict(E=2, H=256, I=192, k=1)])
@@ -79,11 +80,9 @@ def test_pack_is_the_documented_permutation(dims):
     try:
         es = fill_layer(h, cfg, experts=[1])
         codes, scales = synth.expert_canonical(H, I, 1)
-        rc, rs = _pack_reference(codes, scales, H, I)
-        got_c = es.codes[es.code_stride: es.code_stride + es.code_bytes].cpu().numpy()
-        got_s = es.scales[es.scale_stride: es.scale_stride + es.scale_bytes].cpu().numpy()
-        assert np.array_equal(got_c, rc)
-        assert np.array_equal(got_s, rs)
+        ref = _pack_reference(codes, scales, H, I)
+        got = es.blobs[es.stride: es.stride + es.blob_bytes].cpu().numpy()
+        assert np.array_equal(got, ref)
     finally:
         moe.moe_ffn_destroy(h)
 

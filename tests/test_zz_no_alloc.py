@@ -56,7 +56,7 @@ def test_noalloc_rejects_a_problem_larger_than_its_array():
     w = torch.zeros((T, k), dtype=torch.float32, device="cuda")
     y = torch.zeros((T, H), dtype=torch.float32, device="cuda")
     ptrs = torch.zeros(E, dtype=torch.int64, device="cuda")
-    table = moe.expert_table(ptrs, ptrs)
+    table = moe.expert_table(ptrs)
     with pytest.raises(moe.MoeError) as e:
         moe.moe_ffn_forward_noalloc(cfg, 0, x, idx, w, table, y, T)
     assert e.value.code == moe.MOE_ERR_UNSUPPORTED
