@@ -78,6 +78,10 @@ def lib() -> ctypes.CDLL:
         L.orc_rmsnorm_bf16.argtypes = [P, i32, dbl, P]
         L.orc_moe_stack.restype = i32
         L.orc_moe_stack.argtypes = [P, i32, P, i32, i32, P, P, i32, dbl, i32]
+        L.orc_router_logits.argtypes = [P, P, i32, i32, i32, P]
+        L.orc_router_logits.restype = None
+        L.orc_topk_softmax.argtypes = [P, i32, i32, i32, P, P]
+        L.orc_topk_softmax.restype = i32
         _lib = L
     return _lib
 
@@ -234,3 +238,26 @@ def moe_stack(layers, x, topk_idx, topk_w, act_mode: int = ACT_BF16, eps: float 
     if rc:
         raise ValueError(f"orc_moe_stack failed ({rc})")
     return x
+
+
+def router_logits(x_bf16, w_bf16) -> np.ndarray:
+    """fp64 logits [T][E] of bf16 activations x [T][H] and router weights W [E][H]."""
+    x = _c(x_bf16, np.uint16)
+    w = _c(w_bf16, np.uint16)
+    T, H = x.shape
+    E = w.shape[0]
+    assert w.shape[1] == H
+    out = np.zeros((T, E), np.float64)
+    lib().orc_router_logits(_ptr(x), _ptr(w), T, H, E, _ptr(out))
+    return out
+
+
+def topk_softmax(logits, k: int):
+    """(idx int32 [T][k], w float64 [T][k]) of the k largest logits per row."""
+    l = _c(logits, np.float64)
+    T, E = l.shape
+    idx = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float64)
+    rc = lib().orc_topk_softmax(_ptr(l), T, E, k, _ptr(idx), _ptr(w))
+    assert rc == 0, "orc_topk_softmax failed"
+    return idx, w

@@ -335,3 +335,54 @@ int orc_moe_stack(const orc_layer* layers, int L, double* x, int T, int topk,
     free(y);
     return err;
 }
+
+/* ---------------------------------------------------------------- router */
+
+/* logits[t][e] = sum over h of W[e][h] * x[t][h], every product and sum in
+ * fp64 (a bf16 x bf16 product is exact in fp64). */
+void orc_router_logits(const uint16_t* x_bf16, const uint16_t* w_bf16, int T, int H, int E, double* logits)
+{
+    for (int t = 0; t < T; t++)
+        for (int e = 0; e < E; e++) {
+            double acc = 0.0;
+            for (int h = 0; h < H; h++)
+                acc += orc_bf16_value(w_bf16[(size_t)e * H + h]) * orc_bf16_value(x_bf16[(size_t)t * H + h]);
+            logits[(size_t)t * E + e] = acc;
+        }
+}
+
+/* a ranks before b: larger logit first, NaN after every number, ties (and
+ * two NaNs) to the lower expert id */
+static int ranks_before(double va, int a, double vb, int b)
+{
+    const int na = isnan(va), nb = isnan(vb);
+    if (na != nb) return nb;
+    if (!na && va != vb) return va > vb;
+    return a < b;
+}
+
+/* Selection by k passes of "best remaining expert", then the softmax of the
+ * selected logits: w_i = exp(l_i - l_max) / sum_j exp(l_j - l_max). */
+int orc_topk_softmax(const double* logits, int T, int E, int k, int32_t* idx, double* w)
+{
+    if (k < 1 || k > E) return -1;
+    char* taken = (char*)malloc((size_t)E);
+    if (!taken) return -1;
+    for (int t = 0; t < T; t++) {
+        const double* l = logits + (size_t)t * E;
+        memset(taken, 0, (size_t)E);
+        for (int i = 0; i < k; i++) {
+            int best = -1;
+            for (int e = 0; e < E; e++)
+                if (!taken[e] && (best < 0 || ranks_before(l[e], e, l[best], best))) best = e;
+            taken[best] = 1;
+            idx[(size_t)t * k + i] = best;
+        }
+        const double lmax = l[idx[(size_t)t * k]];
+        double sum = 0.0;
+        for (int i = 0; i < k; i++) sum += exp(l[idx[(size_t)t * k + i]] - lmax);
+        for (int i = 0; i < k; i++) w[(size_t)t * k + i] = exp(l[idx[(size_t)t * k + i]] - lmax) / sum;
+    }
+    free(taken);
+    return 0;
+}

@@ -66,6 +66,15 @@ int orc_moe_stack(const orc_layer* layers, int L, double* x, int T, int topk,
                   const int32_t* topk_idx, const float* topk_w, int act_mode,
                   double eps, int nthreads);
 
+/* Router ahead of the path (the pages use a layer's router to pick its top-6
+ * experts, [8GB] §提速之路：v1 到 v4, v4; the gating function itself is not on
+ * the pages).  Reading: logits[t][e] = sum_h W[e][h] x[t][h] with W [E][H] and
+ * x [T][H] in bf16; the k experts with the largest logits are selected in
+ * descending order, ties to the lower expert id, a NaN logit below every
+ * number; their weights are the softmax of the selected logits. */
+void orc_router_logits(const uint16_t* x_bf16, const uint16_t* w_bf16, int T, int H, int E, double* logits);
+int orc_topk_softmax(const double* logits, int T, int E, int k, int32_t* idx, double* w);
+
 #ifdef __cplusplus
 }
 #endif

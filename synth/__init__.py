@@ -47,6 +47,7 @@ _C2 = np.uint64(0x94D049BB133111EB)
 # stream ids
 S_CODES, S_SCALES = 0, 1
 S_X, S_ROUTE, S_LOGIT = 0x10, 0x11, 0x12
+S_ROUTER_W = 0x13
 
 
 def mix64_int(z: int) -> int:
@@ -149,6 +150,13 @@ def activations_bf16(T: int, hidden: int, seed: int = 0, stream: int = S_X, n0: 
     """x ~ N(0,1) as bf16 bit patterns, shape [T, hidden]."""
     z = normals(seed, stream, T * hidden, n0)
     return f32_to_bf16_bits(z.astype(np.float32)).reshape(T, hidden)
+
+
+def router_weights_bf16(E: int, hidden: int, layer: int = 0, seed: int = 0) -> np.ndarray:
+    """Router weights W ~ N(0, 1/hidden) as bf16 bit patterns, shape [E, hidden]
+    (logits of unit-variance activations then have unit variance)."""
+    z = normals(seed, S_ROUTER_W + 0x100 * layer, E * hidden) / np.sqrt(hidden)
+    return f32_to_bf16_bits(z.astype(np.float32)).reshape(E, hidden)
 
 
 def activations_f32(T: int, hidden: int, seed: int = 0, stream: int = S_X, n0: int = 0) -> np.ndarray:

@@ -423,3 +423,52 @@ def test_stack_is_composition_of_layers():
         u = oracle.rmsnorm_bf16(x, 1e-6)
         x = x + oracle.moe_ffn(layers[l][0], layers[l][1], H, I, u, idx[l], w[l])
     assert np.array_equal(got, x)
+
+
+# ---- router ahead of the path: top-k of the router logits, softmax of the selected
+
+def _rank_brute_force(row, k):
+    """Expert ids ordered by (logit descending, id ascending), NaN last, by a
+    plain sort of (key, id) pairs."""
+    keys = [((1, 0.0) if np.isnan(v) else (0, -v), e) for e, v in enumerate(row)]
+    return [e for _, e in sorted(keys)][:k]
+
+
+def test_topk_selection_equals_a_sort_with_ties_and_nan():
+    rng = np.random.default_rng(11)
+    for E, k in ((40, 1), (40, 6), (40, 40), (384, 6)):
+        l = rng.choice([-2.0, -0.5, 0.0, 0.5, 1.0, 3.0], size=(30, E))     # many ties
+        l[3, 5] = np.nan
+        l[4, :] = np.nan
+        idx, w = oracle.topk_softmax(l, k)
+        for t in range(l.shape[0]):
+            assert list(idx[t]) == _rank_brute_force(l[t], k)
+
+
+def test_topk_softmax_closed_form_and_normalization():
+    rng = np.random.default_rng(12)
+    l = rng.standard_normal((50, 16))
+    idx, w = oracle.topk_softmax(l, 2)
+    d = l[np.arange(50), idx[:, 1]] - l[np.arange(50), idx[:, 0]]
+    assert np.allclose(w[:, 0], 1.0 / (1.0 + np.exp(d)), rtol=0, atol=1e-15)
+    idx, w = oracle.topk_softmax(l, 6)
+    assert np.allclose(w.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+    assert (np.diff(w, axis=1) <= 0).all()          # descending logits -> descending weights
+
+
+def test_router_logits_one_hot_zero_and_matmul():
+    E, H = 24, 256
+    W = synth.router_weights_bf16(E, H)
+    one = synth.f32_to_bf16_bits(np.float32([1.0]))[0]
+    for j in (0, 77, 255):
+        x = np.zeros((1, H), np.uint16)
+        x[0, j] = one
+        got = oracle.router_logits(x, W)[0]
+        assert np.array_equal(got, synth.bf16_bits_to_f32(W[:, j]).astype(np.float64))
+    z = oracle.router_logits(np.zeros((2, H), np.uint16), W)
+    assert not z.any()
+    idx, w = oracle.topk_softmax(z, 6)
+    assert (idx == np.arange(6)).all() and np.allclose(w, 1.0 / 6, rtol=0, atol=1e-16)
+    x = synth.activations_bf16(3, H, seed=4)
+    ref = synth.bf16_bits_to_f32(x).astype(np.float64) @ synth.bf16_bits_to_f32(W).astype(np.float64).T
+    assert np.allclose(oracle.router_logits(x, W), ref, rtol=1e-13, atol=1e-13)
