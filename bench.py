@@ -445,6 +445,25 @@ def run_ours(args, wl):
     achieved = ly_bytes / (ly_ms / 1000.0) / 1e9
     traffic = traffic_record(kernel, args.workload, ly_bytes)
 
+    # ---- the router ahead of the path (logits = W x, top-k, softmax): two
+    # launches, timed alone in profiling mode on the same stream
+    Wr = torch.from_numpy(synth.router_weights_bf16(E, H).view(np.int16)).cuda()
+    r_idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    r_w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    moe.moe_ffn_profile_enable(h, True)
+    nrt = 200
+    with torch.cuda.stream(stream):
+        for i in range(nrt):
+            moe.moe_router_topk(h, x_d[i % R], Wr, T, r_idx, r_w, stream=stream)
+    stream.synchronize()
+    ms_r, n_r = moe.moe_ffn_profile_read(h)
+    moe.moe_ffn_profile_enable(h, False)
+    r_us = ms_r[moe.MOE_PHASE_ROUTER] / max(1, n_r[moe.MOE_PHASE_ROUTER]) * 1e3
+    r_bytes = E * H * 2 + T * H * 2 + 2 * T * E * 4 + T * k * 8     # W, x, logits out and back, routing
+    router = {"kernels": "k_router_logits + k_router_select", "us": r_us, "algorithmic_bytes": r_bytes,
+              "gbs": r_bytes / (r_us * 1e-6) / 1e9, "frac_of_hbm": r_bytes / (r_us * 1e-6) / 1e9 / peak,
+              "launches": 2}
+
     # ---- end to end through the public API from host buffers: every step copies
     # its inputs in from pinned host memory and its result back
     ne2e = min(K, 2000 if T * L == 1 else 20)
@@ -511,6 +530,7 @@ def run_ours(args, wl):
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes_per_launch": ly_bytes},
+            "router": router,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": T * H * 4},

@@ -33,6 +33,7 @@ EXPORTS = [
     "moe_ffn_pack_expert", "moe_ffn_forward", "moe_ffn_forward_host", "moe_ffn_route",
     "moe_ffn_act_quant", "moe_stack_forward", "moe_ffn_profile_enable", "moe_ffn_profile_read",
     "moe_ffn_status", "moe_ffn_strerror", "moe_ffn_destroy", "moe_ffn_forward_noalloc",
+    "moe_router_topk", "moe_router_select",
 ]
 
 MOE_PHASE_PREP = 0
@@ -40,6 +41,7 @@ MOE_PHASE_GATE_UP = 1
 MOE_PHASE_DOWN = 2
 MOE_PHASE_ROUTE = 3
 MOE_PHASE_ACT_QUANT = 4
+MOE_PHASE_ROUTER = 5
 MOE_NUM_PHASES = 8
 
 
@@ -90,6 +92,8 @@ def lib() -> ctypes.CDLL:
             "moe_ffn_strerror": (ctypes.c_char_p, [I]),
             "moe_ffn_destroy": (None, [P]),
             "moe_ffn_forward_noalloc": (I, [cfgp, I, P, P, P, tblp, P, I, P, P]),
+            "moe_router_topk": (I, [P, P, P, I, P, P, P, P]),
+            "moe_router_select": (I, [P, P, I, P, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -215,3 +219,13 @@ def moe_ffn_forward_noalloc(cfg: moe_ffn_config, device: int, x, topk_idx, topk_
 
 def moe_ffn_destroy(h) -> None:
     lib().moe_ffn_destroy(h)
+
+
+def moe_router_topk(h, x, router_w, T: int, topk_idx, topk_w, logits=None, stream=None):
+    _check(lib().moe_router_topk(h, _p(x), _p(router_w), int(T), _p(logits), _p(topk_idx), _p(topk_w),
+                                 _s(stream)), "moe_router_topk")
+
+
+def moe_router_select(h, logits, T: int, topk_idx, topk_w, stream=None):
+    _check(lib().moe_router_select(h, _p(logits), int(T), _p(topk_idx), _p(topk_w), _s(stream)),
+           "moe_router_select")

@@ -43,6 +43,7 @@ struct moe_ffn {
     std::vector<StackGraph> graphs;
     unsigned long long use_clock;
     Profiler* prof;             // non-null while moe_ffn_profile_enable(h, 1)
+    float* rlogits;             // router logits scratch [max_tokens][E]
 };
 
 namespace {
@@ -176,7 +177,7 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     h->device = device;
     if (cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
         gemv_init_device() != cudaSuccess || route_init_device() != cudaSuccess ||
-        group_init_device() != cudaSuccess) {
+        group_init_device() != cudaSuccess || router_init_device() != cudaSuccess) {
         delete h;
         return MOE_ERR_CUDA;
     }
@@ -206,6 +207,7 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     size_t o_gxg = take(gw.xg), o_gxgsf = take(gw.xgsf), o_ghg = take(gw.hg), o_ghgsf = take(gw.hgsf);
     size_t o_gobuf = take(gw.obuf), o_gpgu = take(gw.part_gu), o_gpdn = take(gw.part_dn);
     size_t o_ghraw = take(gw.hraw), o_ghpair = take(gw.hpair);
+    size_t o_rlog = take((size_t)T * cfg->num_experts * 4);
     size_t o_xst = take((size_t)T * H * 2), o_ist = take((size_t)T * k * 4);
     size_t o_wst = take((size_t)T * k * 4), o_yst = take((size_t)T * H * 4);
     h->ws_bytes = off;
@@ -271,6 +273,7 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
         ga.hraw = e4m3 ? (float*)(b + o_ghraw) : nullptr;
         ga.hpair = e4m3 ? (int*)(b + o_ghpair) : nullptr;
     }
+    h->rlogits = (float*)(b + o_rlog);
     h->x_stage = (uint16_t*)(b + o_xst);
     h->idx_stage = (int32_t*)(b + o_ist);
     h->w_stage = (float*)(b + o_wst);
@@ -363,6 +366,41 @@ int moe_ffn_act_quant(moe_ffn_t h, const void* x, int rows, int n, uint8_t* code
     cudaError_t e = launch_act_quant(a, s, false);
     if (h->prof) h->prof->end(s);
     return cuda_rc(e);
+}
+
+int moe_router_topk(moe_ffn_t h, const void* x, const void* router_w, int T, float* logits,
+                    int32_t* topk_idx, float* topk_w, void* stream)
+{
+    if (!h || T < 0 || T > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !router_w || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(router_w, 16) || !aligned(logits, 4) || !aligned(topk_idx, 4) ||
+        !aligned(topk_w, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (h->cfg.num_experts > router_max_experts() || router_tokens_per_cta(h->cfg.hidden) == 0)
+        return MOE_ERR_UNSUPPORTED;
+    DeviceGuard guard(h->device);
+    RouterArgs a{(const uint16_t*)x, (const uint16_t*)router_w, logits ? logits : h->rlogits, topk_idx, topk_w,
+                 T, h->cfg.hidden, h->cfg.num_experts, h->cfg.topk, 0};
+    cudaStream_t s = (cudaStream_t)stream;
+    if (h->prof) h->prof->begin(kPhaseRouter, s);
+    cudaError_t e = launch_router_logits(a, s, !h->prof);
+    if (e == cudaSuccess) e = launch_router_select(a, s, !h->prof);
+    if (h->prof) h->prof->end(s);
+    return cuda_rc(e);
+}
+
+int moe_router_select(moe_ffn_t h, const float* logits, int T, int32_t* topk_idx, float* topk_w, void* stream)
+{
+    if (!h || T < 0 || T > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!logits || !topk_idx || !topk_w || !aligned(logits, 4) || !aligned(topk_idx, 4) || !aligned(topk_w, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (h->cfg.num_experts > router_max_experts()) return MOE_ERR_UNSUPPORTED;
+    DeviceGuard guard(h->device);
+    RouterArgs a{nullptr, nullptr, const_cast<float*>(logits), topk_idx, topk_w, T, h->cfg.hidden,
+                 h->cfg.num_experts, h->cfg.topk, 0};
+    return cuda_rc(launch_router_select(a, (cudaStream_t)stream, false));
 }
 
 int moe_stack_forward(moe_ffn_t h, float* x, const moe_expert_table* tbls,

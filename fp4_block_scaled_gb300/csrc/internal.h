@@ -89,7 +89,7 @@ struct Profiler {
 };
 
 enum { kPhasePrep = 0, kPhaseGateUp = 1, kPhaseDown = 2, kPhaseRoute = 3, kPhaseActQuant = 4,
-       kNumPhases = 8 };
+       kPhaseRouter = 5, kNumPhases = 8 };
 
 cudaError_t launch_gemv_layer(const GemvArgs& a, cudaStream_t s, bool pdl, Profiler* prof);
 
@@ -175,6 +175,22 @@ constexpr int kDefaultGemmMinTokens = MOE_DEFAULT_GEMM_MIN_TOKENS;
 int route_max_experts();
 cudaError_t route_init_device();
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, bool pdl = false);
+
+// Router ahead of the path (router.cu).
+struct RouterArgs {
+    const uint16_t* x;      // bf16 [T][H]
+    const uint16_t* w;      // bf16 [E][H] router weights
+    float* logits;          // fp32 [T][E]
+    int32_t* idx;           // [T][topk]
+    float* wout;            // [T][topk]
+    int T, H, E, topk;
+    int tpc;                // tokens per CTA of the logits kernel (set by the launcher)
+};
+int router_max_experts();
+int router_tokens_per_cta(int H);     // 0: H too large for the logits kernel
+cudaError_t router_init_device();
+cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t s, bool pdl);
+cudaError_t launch_router_select(const RouterArgs& a, cudaStream_t s, bool pdl);
 
 // E4M3 / ue8m0-per-128 activation quantizer (actquant.cu).
 struct ActQuantArgs {

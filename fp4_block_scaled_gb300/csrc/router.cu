@@ -1,0 +1,333 @@
+// router.cu -- the router ahead of the routed FFN: logits = W x for every
+// token, then each token's top-k experts and the softmax of their logits.
+//
+//   k_router_logits  grid (ceil(E / nw), ceil(T / tpc)), nw = 4 or 8 warps:
+//                    warp w owns expert row e = nw blockIdx.x + w; the CTA's
+//                    tpc <= 8 tokens sit in shared memory (bf16, fp32 for 8); each
+//                    lane loads its 16 chunks of 16 bytes of the row (8
+//                    weights each; a warp covers 4096 of H per pass) at once,
+//                    so a pass keeps the whole row in flight, and accumulates
+//                    the tpc dot products in fp32 (bf16 products are exact),
+//                    then a butterfly warp sum, so the result is
+//                    reproducible.
+//   k_router_select  one warp per token: the logits as order keys in
+//                    registers, k rounds of a warp arg-max under the order
+//                    "larger logit first, NaN after every number, ties to the
+//                    lower expert id" over the lanes' running bests, then the
+//                    softmax of the selected logits in fp32.
+// The token tile of k_router_logits is a template parameter (1..8) so that a
+// small batch runs small code (a fully unrolled 16-token body stalled on
+// instruction fetch).
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kRPerLane = 32;       // most logits per lane in k_router_select (E <= 1024)
+constexpr int kRChunks = 16;        // 16-byte weight chunks per lane per pass
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// dst[i] = f(src[i]) for i < n by the CTA's threads, eight loads in flight per
+// thread before the stores (a load-store pair per iteration would wait a full
+// memory round trip each).
+template <class F>
+__device__ __forceinline__ void stage_x(const uint4* src, int n, F store)
+{
+    for (int i0 = threadIdx.x; i0 < n; i0 += 8 * blockDim.x) {
+        uint4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            const int i = i0 + q * blockDim.x;
+            v[q] = i < n ? src[i] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            const int i = i0 + q * blockDim.x;
+            if (i < n) store(i, v[q]);
+        }
+    }
+}
+
+template <int TPC, int NW>
+__global__ void __launch_bounds__(NW * 32) k_router_logits(RouterArgs a)
+{
+    extern __shared__ __align__(16) uint4 s_x[];      // [TPC][H / 8]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H8 = a.H / 8;
+    const int t0 = blockIdx.y * TPC;
+    const int nt = min(TPC, a.T - t0);
+    const int e = blockIdx.x * NW + warp;
+    const uint4* wrow = reinterpret_cast<const uint4*>(a.w + (size_t)min(e, a.E - 1) * a.H);
+    float acc[TPC];
+#pragma unroll
+    for (int t = 0; t < TPC; t++) acc[t] = 0.0f;
+    auto dot = [&](const uint4 wq, int c) {
+        float wf[8];
+        bf16x8_to_f32(wq, wf);
+#pragma unroll
+        for (int t = 0; t < TPC; t++) {
+            if (t < nt) {
+                float xf[8];
+                bf16x8_to_f32(s_x[t * H8 + c], xf);
+#pragma unroll
+                for (int q = 0; q < 8; q++) acc[t] = fmaf(wf[q], xf[q], acc[t]);
+            }
+        }
+    };
+    if constexpr (TPC <= 4) {
+        // small batches are latency-bound: a whole pass of the row (a warp covers
+        // 4096 of H) in flight at once, issued before the wait for the previous
+        // kernel (the router weights are not written by earlier kernels)
+        uint4 wv[kRChunks];
+#pragma unroll
+        for (int i = 0; i < kRChunks; i++) {
+            const int c = lane + 32 * i;
+            wv[i] = c < H8 ? ldg_stream_v4(wrow + c) : make_uint4(0, 0, 0, 0);
+        }
+        pdl_wait();
+        pdl_trigger();
+        stage_x(reinterpret_cast<const uint4*>(a.x + (size_t)t0 * a.H), nt * H8,
+                [&](int i, const uint4 v) { s_x[i] = v; });
+        __syncthreads();
+        if (e >= a.E) return;
+        for (int c0 = 0; c0 < H8; c0 += 32 * kRChunks) {
+            if (c0 > 0) {
+#pragma unroll
+                for (int i = 0; i < kRChunks; i++) {
+                    const int c = c0 + lane + 32 * i;
+                    wv[i] = c < H8 ? ldg_stream_v4(wrow + c) : make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kRChunks; i++) {
+                const int c = c0 + lane + 32 * i;
+                if (c < H8) dot(wv[i], c);
+            }
+        }
+    } else {
+        // larger batches reuse each weight chunk for TPC tokens: x is staged as
+        // fp32 once per CTA ([TPC][H]) and the weights stream
+        float4* s_xf = reinterpret_cast<float4*>(s_x);
+        pdl_wait();
+        pdl_trigger();
+        stage_x(reinterpret_cast<const uint4*>(a.x + (size_t)t0 * a.H), nt * H8, [&](int i, const uint4 v) {
+            float f[8];
+            bf16x8_to_f32(v, f);
+            s_xf[2 * i] = make_float4(f[0], f[1], f[2], f[3]);
+            s_xf[2 * i + 1] = make_float4(f[4], f[5], f[6], f[7]);
+        });
+        __syncthreads();
+        if (e >= a.E) return;
+        constexpr int kDepth = 8;                 // weight chunks in flight per lane
+        for (int c0 = lane; c0 < H8; c0 += 32 * kDepth) {
+            uint4 wq[kDepth];
+#pragma unroll
+            for (int q = 0; q < kDepth; q++) {
+                const int c = c0 + 32 * q;
+                wq[q] = c < H8 ? ldg_stream_v4(wrow + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int q = 0; q < kDepth; q++) {
+            const int c = c0 + 32 * q;
+            if (c >= H8) break;
+            float wf[8];
+            bf16x8_to_f32(wq[q], wf);
+#pragma unroll
+            for (int t = 0; t < TPC; t++) {
+                if (t < nt) {
+                    const float4 x0 = s_xf[(t * H8 + c) * 2], x1 = s_xf[(t * H8 + c) * 2 + 1];
+                    acc[t] = fmaf(wf[0], x0.x, acc[t]);
+                    acc[t] = fmaf(wf[1], x0.y, acc[t]);
+                    acc[t] = fmaf(wf[2], x0.z, acc[t]);
+                    acc[t] = fmaf(wf[3], x0.w, acc[t]);
+                    acc[t] = fmaf(wf[4], x1.x, acc[t]);
+                    acc[t] = fmaf(wf[5], x1.y, acc[t]);
+                    acc[t] = fmaf(wf[6], x1.z, acc[t]);
+                    acc[t] = fmaf(wf[7], x1.w, acc[t]);
+                }
+            }
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < TPC; t++) {
+        if (t < nt) {
+            const float v = warp_sum(acc[t]);
+            if (lane == 0) a.logits[(size_t)(t0 + t) * a.E + e] = v;
+        }
+    }
+}
+
+// Order key of a logit: larger keys rank first; -0 and +0 tie; NaN ranks after
+// every number (key 1); key 0 is "taken" or "no expert".
+__device__ __forceinline__ uint32_t order_key(float v)
+{
+    if (isnan(v)) return 1u;
+    const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// grid ceil(T / 8), 256 threads: one warp per token.  Lane l holds the order
+// keys of experts l, l + 32, ... (R of them) in registers and its best
+// untaken one; a round takes the warp's best with two redux.sync (the largest
+// key, then the lowest id holding it), and only the winning lane picks its
+// next best.  Lane i keeps pick i for the softmax.
+template <int R>
+__global__ void __launch_bounds__(256) k_router_select(RouterArgs a)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    pdl_wait();
+    pdl_trigger();
+    if (t >= a.T) return;
+    const float* row = a.logits + (size_t)t * a.E;
+    float v[R];
+    uint32_t key[R];
+#pragma unroll
+    for (int j = 0; j < R; j++) {
+        const int e = lane + 32 * j;
+        v[j] = e < a.E ? row[e] : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < R; j++) key[j] = lane + 32 * j < a.E ? order_key(v[j]) : 0u;
+    uint32_t bk = 0;                                   // this lane's best: key, slot, value
+    int bj = 0;
+    float bv = 0.0f;
+    auto lane_best = [&]() {
+        bk = 0;
+        bj = 0;
+#pragma unroll
+        for (int j = 0; j < R; j++)                    // strict >: the lower id on equal keys
+            if (key[j] > bk) {
+                bk = key[j];
+                bj = j;
+                bv = v[j];
+            }
+    };
+    lane_best();
+    float mine = 0.0f;
+    int mine_e = 0;
+    for (int i = 0; i < a.topk; i++) {
+        const uint32_t gk = __reduce_max_sync(0xFFFFFFFFu, bk);
+        const int ge = (int)__reduce_min_sync(0xFFFFFFFFu, bk == gk ? (uint32_t)(lane + 32 * bj) : 0xFFFFFFFFu);
+        const float gv = __shfl_sync(0xFFFFFFFFu, bv, ge & 31);
+        if (lane == i) {
+            mine = gv;
+            mine_e = ge;
+        }
+        if ((ge & 31) == lane) {
+#pragma unroll
+            for (int j = 0; j < R; j++)
+                if (j == (ge >> 5)) key[j] = 0u;
+            lane_best();
+        }
+    }
+    const float m = __shfl_sync(0xFFFFFFFFu, mine, 0);
+    const float p = lane < a.topk ? expf(mine - m) : 0.0f;
+    float sum = p;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if (lane < a.topk) {
+        a.idx[(size_t)t * a.topk + lane] = mine_e;
+        a.wout[(size_t)t * a.topk + lane] = p / sum;
+    }
+}
+
+cudaError_t rlaunch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, void** args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+constexpr size_t kRSmemMax = 200 * 1024;
+
+}  // namespace
+
+int router_max_experts() { return 32 * kRPerLane; }
+
+// Largest token tile the logits kernel can hold for width H: tiles of up to 4
+// tokens keep x in bf16, of 8 in fp32.
+int router_tokens_per_cta(int H)
+{
+    if ((size_t)8 * H * 4 <= kRSmemMax) return 8;
+    if ((size_t)4 * H * 2 <= kRSmemMax) return 4;
+    if ((size_t)2 * H * 2 <= kRSmemMax) return 2;
+    return (size_t)H * 2 <= kRSmemMax ? 1 : 0;
+}
+
+cudaError_t router_init_device()
+{
+    const void* fns[] = {(const void*)k_router_logits<1, 4>, (const void*)k_router_logits<2, 4>,
+                         (const void*)k_router_logits<4, 4>, (const void*)k_router_logits<8, 8>};
+    cudaError_t e = cudaSuccess;
+    for (const void* f : fns) {
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmemMax);
+        // the same shared-memory carveout as the layer kernels: no SM reconfiguration between them
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
+    }
+    const void* sel[] = {(const void*)k_router_select<4>, (const void*)k_router_select<8>,
+                         (const void*)k_router_select<12>, (const void*)k_router_select<16>,
+                         (const void*)k_router_select<32>};
+    for (const void* f : sel)
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
+    return e;
+}
+
+cudaError_t launch_router_logits(const RouterArgs& a0, cudaStream_t s, bool pdl)
+{
+    RouterArgs a = a0;
+    if (a.T == 0) return cudaSuccess;
+    const int cap = router_tokens_per_cta(a.H);
+    int tpc = 8;
+    while (tpc > 1 && (tpc > cap || tpc / 2 >= a.T)) tpc /= 2;     // the smallest tile that holds T, within cap
+    a.tpc = tpc;
+    void* args[] = {&a};
+    const int nw = tpc <= 4 ? 4 : 8;          // small tiles: more CTAs pull the weights
+    const dim3 grid((a.E + nw - 1) / nw, (a.T + tpc - 1) / tpc);
+    const size_t smem = (size_t)tpc * a.H * (tpc > 4 ? 4 : 2);
+    const void* fn = tpc == 1   ? (const void*)k_router_logits<1, 4>
+                     : tpc == 2 ? (const void*)k_router_logits<2, 4>
+                     : tpc == 4 ? (const void*)k_router_logits<4, 4>
+                                : (const void*)k_router_logits<8, 8>;
+    return rlaunch(fn, grid, dim3(nw * 32), smem, s, pdl, args);
+}
+
+cudaError_t launch_router_select(const RouterArgs& a0, cudaStream_t s, bool pdl)
+{
+    RouterArgs a = a0;
+    if (a.T == 0) return cudaSuccess;
+    void* args[] = {&a};
+    const void* fn = a.E <= 128   ? (const void*)k_router_select<4>
+                     : a.E <= 256 ? (const void*)k_router_select<8>
+                     : a.E <= 384 ? (const void*)k_router_select<12>
+                     : a.E <= 512 ? (const void*)k_router_select<16>
+                                  : (const void*)k_router_select<32>;
+    return rlaunch(fn, dim3((a.T + 7) / 8), dim3(256), 0, s, pdl, args);
+}
+
+}  // namespace moe

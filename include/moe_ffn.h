@@ -159,6 +159,27 @@ int moe_ffn_route(moe_ffn_t h, const int32_t* topk_idx, int T, int32_t* counts,
 int moe_ffn_act_quant(moe_ffn_t h, const void* x, int rows, int n, uint8_t* codes,
                       uint8_t* scales, void* stream);
 
+/* The router ahead of the path (the pages pick each token's top-6 experts of a
+ * layer with that layer's router, [8GB] §提速之路：v1 到 v4, v4; the gating
+ * function is not on the pages).  Reading: for each token t,
+ *   logits[t][e] = sum_h router_w[e][h] * x[t][h]      (fp32 accumulation)
+ * the k = cfg.topk experts with the largest logits, in descending order (ties
+ * to the lower expert id; a NaN logit ranks after every number), and
+ *   topk_w[t][i] = exp(l_i - l_0) / sum_j exp(l_j - l_0)  over the selected.
+ *   x        device bf16 [T][H];  router_w device bf16 [E][H]
+ *   logits   optional device fp32 [T][E] output (NULL: kept in the workspace)
+ *   topk_idx device int32 [T][k], topk_w device fp32 [T][k] -- the routing
+ *            inputs of moe_ffn_forward.
+ * Two launches (logits, selection), deterministic.  UNSUPPORTED beyond 1024
+ * experts or H above 102,400. */
+int moe_router_topk(moe_ffn_t h, const void* x, const void* router_w, int T, float* logits,
+                    int32_t* topk_idx, float* topk_w, void* stream);
+
+/* The selection and softmax of moe_router_topk alone, from given device fp32
+ * logits [T][E] (bit-exact selection for given logits). */
+int moe_router_select(moe_ffn_t h, const float* logits, int T, int32_t* topk_idx, float* topk_w,
+                      void* stream);
+
 /* L-layer decode step on a residual stream ([A100] §然后又发现每 token 启动
  * 2000 次内核: RMSNorm and the MoE per layer, launched as a handful of
  * dispatches): for l = 0..L-1,
@@ -188,6 +209,7 @@ enum {
     MOE_PHASE_ROUTE = 3,     /* token -> expert grouping (moe_ffn_route and
                                 the expert-major path's first kernel)       */
     MOE_PHASE_ACT_QUANT = 4, /* E4M3 activation quantizer                   */
+    MOE_PHASE_ROUTER = 5,    /* router logits + top-k + softmax (moe_router_topk) */
     MOE_NUM_PHASES = 8
 };
 int moe_ffn_profile_enable(moe_ffn_t h, int on);

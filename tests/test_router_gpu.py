@@ -1,0 +1,108 @@
+"""GPU parity of the router ahead of the path (logits = W x, top-k with ties to
+the lower expert id, softmax of the selected logits) against the oracle,
+through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import fp4_block_scaled_gb300 as moe
+import oracle
+import synth
+from moe_setup import Layer, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    moe.lib()
+    yield
+
+
+def _handle(E, H, k, T):
+    return moe.moe_ffn_create(moe.config(E, H, 128, k, T), 0)
+
+
+def test_select_is_bit_exact_given_logits():
+    E, k, T = 384, 6, 37
+    rng = np.random.default_rng(21)
+    l = rng.choice(np.float32([-1.5, -0.25, 0.0, 0.75, 2.0]), size=(T, E)).astype(np.float32)   # many ties
+    l[:, 100] += rng.standard_normal(T).astype(np.float32)
+    l[3, 7] = np.nan
+    l[4, :] = np.nan
+    h = _handle(E, 256, k, T)
+    try:
+        ld = torch.from_numpy(l).cuda()
+        idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        moe.moe_router_select(h, ld, T, idx, w)
+        torch.cuda.synchronize()
+        ridx, rw = oracle.topk_softmax(l.astype(np.float64), k)
+        assert np.array_equal(idx.cpu().numpy(), ridx)
+        ok = ~np.isnan(rw).any(axis=1)
+        assert np.abs(w.cpu().numpy()[ok] - rw[ok]).max() <= 2e-6
+    finally:
+        moe.moe_ffn_destroy(h)
+
+
+@pytest.mark.parametrize("T", [1, 37, 64])
+def test_router_full_size_matches_oracle(T):
+    E, H, k = 384, 4096, 6
+    W = synth.router_weights_bf16(E, H, layer=1)
+    x = synth.activations_bf16(T, H, seed=30 + T)
+    h = _handle(E, H, k, T)
+    try:
+        wd = torch.from_numpy(W.view(np.int16)).cuda()
+        xd = torch.from_numpy(x.view(np.int16)).cuda()
+        logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+        idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        moe.moe_router_topk(h, xd, wd, T, idx, w, logits=logits)
+        torch.cuda.synchronize()
+        got_l = logits.cpu().numpy().astype(np.float64)
+        ref_l = oracle.router_logits(x, W)
+        err = np.abs(got_l - ref_l).max()
+        assert err <= 1e-5, f"router logits max|err| = {err:.3e}"
+        gi, gw = idx.cpu().numpy(), w.cpu().numpy()
+        # the selection is exactly the oracle's selection of the GPU's logits
+        ci, cw = oracle.topk_softmax(got_l, k)
+        assert np.array_equal(gi, ci)
+        assert np.abs(gw - cw).max() <= 2e-6
+        # and the oracle's own selection wherever its k-th / (k+1)-th margin is clear
+        ri, rw = oracle.topk_softmax(ref_l, k)
+        srt = -np.sort(-ref_l, axis=1)
+        clear = (srt[:, k - 1] - srt[:, k]) > 10 * err + 1e-7
+        assert clear.sum() >= T // 2
+        assert np.array_equal(gi[clear], ri[clear])
+        # the workspace path (no logits output) and a repeat give the same result
+        idx2 = torch.empty_like(idx)
+        w2 = torch.empty_like(w)
+        moe.moe_router_topk(h, xd, wd, T, idx2, w2)
+        torch.cuda.synchronize()
+        assert torch.equal(idx, idx2) and torch.equal(w.view(torch.int32), w2.view(torch.int32))
+    finally:
+        moe.moe_ffn_destroy(h)
+
+
+def test_router_then_layer_matches_oracle():
+    """Router on the device, its routing straight into the layer."""
+    E, H, I, k, T = 8, 256, 128, 2, 5
+    L = Layer(E=E, H=H, I=I, k=k, max_tokens=T)
+    try:
+        W = synth.router_weights_bf16(E, H, layer=2)
+        x = synth.activations_bf16(T, H, seed=41)
+        xd = torch.from_numpy(x.view(np.int16)).cuda()
+        idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        moe.moe_router_topk(L.h, xd, torch.from_numpy(W.view(np.int16)).cuda(), T, idx, w)
+        y = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        moe.moe_ffn_forward(L.h, xd, idx, w, L.es.table, y, T)
+        torch.cuda.synchronize()
+        ri, rw = oracle.topk_softmax(oracle.router_logits(x, W), k)
+        assert np.array_equal(idx.cpu().numpy(), ri)
+        ref = L.oracle(x, ri, rw.astype(np.float32))
+        assert_close(y.cpu().numpy(), ref, "router -> layer")
+    finally:
+        L.close()
