@@ -19,6 +19,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 
 ACT_BF16 = 0
 ACT_E4M3_UE8M0_128 = 1
+ACT_E2M1_UE8M0_32 = 2
 
 _lib = None
 
@@ -64,6 +65,12 @@ def lib() -> ctypes.CDLL:
         L.orc_ue8m0_for_amax.argtypes = [dbl]
         L.orc_act_quant_e4m3.restype = None
         L.orc_act_quant_e4m3.argtypes = [P, i32, i32, P, P]
+        L.orc_e2m1_rne.restype = i32
+        L.orc_e2m1_rne.argtypes = [dbl]
+        L.orc_ue8m0_for_amax_e2m1.restype = i32
+        L.orc_ue8m0_for_amax_e2m1.argtypes = [dbl]
+        L.orc_act_quant_e2m1.restype = None
+        L.orc_act_quant_e2m1.argtypes = [P, i32, i32, P, P]
         L.orc_silu.restype = dbl
         L.orc_silu.argtypes = [dbl]
         L.orc_matvec.restype = i32
@@ -143,6 +150,26 @@ def act_quant_e4m3(v, block: int = 128):
     codes = np.zeros(n, np.uint8)
     scales = np.zeros((n + block - 1) // block, np.uint8)
     lib().orc_act_quant_e4m3(_ptr(v), n, block, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def e2m1_rne(v: float) -> int:
+    """Nearest E2M1 code to v (ties to the even mantissa, saturating)."""
+    return int(lib().orc_e2m1_rne(float(v)))
+
+
+def ue8m0_for_amax_e2m1(amax: float) -> int:
+    """Scale byte k + 127 of an E2M1 block: the least k with amax <= 6 * 2^k."""
+    return int(lib().orc_ue8m0_for_amax_e2m1(float(amax)))
+
+
+def act_quant_e2m1(v, block: int = 32):
+    """Per-block E2M1 codes (one per byte) and ue8m0 scale bytes of v."""
+    v = _c(v, np.float64)
+    n = v.size
+    codes = np.zeros(n, np.uint8)
+    scales = np.zeros((n + block - 1) // block, np.uint8)
+    lib().orc_act_quant_e2m1(_ptr(v), n, block, _ptr(codes), _ptr(scales))
     return codes, scales
 
 

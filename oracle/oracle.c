@@ -141,6 +141,66 @@ void orc_act_quant_e4m3(const double* v, int n, int block, uint8_t* codes, uint8
     }
 }
 
+/* ------------------------------------------------ E2M1 activations (MXFP4) */
+
+/* Nearest E2M1 value to v (the grid 0, 0.5, 1, 1.5, 2, 3, 4, 6 and
+ * negatives), ties to the even mantissa bit, saturating to +-6; returned as
+ * the 4-bit code (sign in bit 3).  Reading (the sources give FP4 weights,
+ * [A100] §FP4の正体, not FP4 activations): activations are rounded the way a
+ * float is rounded to a narrower float, round-to-nearest-even. */
+int orc_e2m1_rne(double v)
+{
+    int sign = signbit(v) ? 8 : 0;
+    double a = fabs(v);
+    if (!(a == a)) return 0;
+    if (a >= 6.0) return 7 | sign;                              /* saturate */
+    int best = 0;
+    for (int c = 1; c < 8; c++) {
+        double d = fabs(orc_e2m1_value(c) - a), db = fabs(orc_e2m1_value(best) - a);
+        if (d < db || (d == db && (c & 1) == 0)) best = c;     /* tie: even mantissa (code bit 0) */
+    }
+    return best | sign;
+}
+
+/* Scale byte of an E2M1 activation block: 2^k with k the least integer such
+ * that amax <= 6 * 2^k (6 is E2M1's largest value), found by exact
+ * comparisons -- the ue8m0 convention of the model's activation quantizer
+ * ([8GB] §三个从不抛错的 Bug, 2: scales are ue8m0) with E2M1's range.
+ * Readings: amax = 0 gives k = 0; k is clamped to [-126, 127]; a non-finite
+ * amax gives the NaN byte 255. */
+int orc_ue8m0_for_amax_e2m1(double amax)
+{
+    if (!(amax == amax) || isinf(amax)) return 255;
+    if (amax == 0.0) return 127;
+    int e;
+    frexp(amax, &e);
+    int k = e - 3;
+    while (amax > ldexp(6.0, k)) k++;
+    while (amax <= ldexp(6.0, k - 1)) k--;
+    if (k < -126) k = -126;
+    if (k > 127) k = 127;
+    return k + 127;
+}
+
+/* Quantize v[0..n) in consecutive blocks of `block` elements (the last block
+ * may be shorter) to E2M1 codes (one per byte here) with one ue8m0 scale byte
+ * per block: code = nearest E2M1 to v * 2^-k. */
+void orc_act_quant_e2m1(const double* v, int n, int block, uint8_t* codes, uint8_t* scale_bytes)
+{
+    for (int b0 = 0, b = 0; b0 < n; b0 += block, b++) {
+        int nb = (n - b0 < block) ? n - b0 : block;
+        double amax = 0.0;
+        for (int i = 0; i < nb; i++) {
+            double a = fabs(v[b0 + i]);
+            if (a > amax || a != a) amax = a;
+        }
+        int s = orc_ue8m0_for_amax_e2m1(amax);
+        scale_bytes[b] = (uint8_t)s;
+        for (int i = 0; i < nb; i++)
+            codes[b0 + i] = (uint8_t)((s == 255) ? 0 : orc_e2m1_rne(ldexp(v[b0 + i], 127 - s)));
+    }
+}
+
 /* silu(g) = g * sigmoid(g) = g / (1 + e^-g). */
 double orc_silu(double g) { return g / (1.0 + exp(-g)); }
 
@@ -167,6 +227,17 @@ int orc_matvec(const uint8_t* codes, const uint8_t* scales, int rows, int k,
     return 0;
 }
 
+static void quant_dequant_e2m1(double* v, int n, int block)
+{
+    uint8_t* c = (uint8_t*)malloc((size_t)n);
+    uint8_t* s = (uint8_t*)malloc((size_t)(n + block - 1) / block);
+    orc_act_quant_e2m1(v, n, block, c, s);
+    for (int i = 0; i < n; i++)
+        v[i] = (s[i / block] == 255) ? NAN : orc_e2m1_value(c[i]) * orc_ue8m0_value(s[i / block]);
+    free(c);
+    free(s);
+}
+
 static void quant_dequant(double* v, int n, int block)
 {
     uint8_t* c = (uint8_t*)malloc((size_t)n);
@@ -179,7 +250,8 @@ static void quant_dequant(double* v, int n, int block)
 }
 
 /* One expert: o = Wd * (silu(Wg*x) (.) (Wu*x)).  In the E4M3 activation mode
- * x and h are first replaced by their per-128 E4M3/ue8m0 quantized values. */
+ * x and h are first replaced by their per-128 E4M3/ue8m0 quantized values, in
+ * the E2M1 mode by their per-32 E2M1/ue8m0 (MXFP4) quantized values. */
 int orc_expert_ffn(const uint8_t* codes, const uint8_t* scales, int hidden, int inter,
                    const double* x, int act_mode, double* o)
 {
@@ -190,12 +262,14 @@ int orc_expert_ffn(const uint8_t* codes, const uint8_t* scales, int hidden, int 
     double* u = (double*)malloc(sizeof(double) * I);
     memcpy(xin, x, sizeof(double) * H);
     if (act_mode == ORC_ACT_E4M3_UE8M0_128) quant_dequant(xin, H, 128);
+    if (act_mode == ORC_ACT_E2M1_UE8M0_32) quant_dequant_e2m1(xin, H, 32);
 
     size_t gu_codes = (size_t)I * H / 2, gu_scales = (size_t)I * H / 32;
     orc_matvec(codes, scales, I, H, xin, g);
     orc_matvec(codes + gu_codes, scales + gu_scales, I, H, xin, u);
     for (int i = 0; i < I; i++) g[i] = orc_silu(g[i]) * u[i];      /* g now holds h */
     if (act_mode == ORC_ACT_E4M3_UE8M0_128) quant_dequant(g, I, 128);
+    if (act_mode == ORC_ACT_E2M1_UE8M0_32) quant_dequant_e2m1(g, I, 32);
     orc_matvec(codes + 2 * gu_codes, scales + 2 * gu_scales, H, I, g, o);
     free(xin);
     free(g);

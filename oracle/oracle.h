@@ -31,7 +31,7 @@
 extern "C" {
 #endif
 
-enum { ORC_ACT_BF16 = 0, ORC_ACT_E4M3_UE8M0_128 = 1 };
+enum { ORC_ACT_BF16 = 0, ORC_ACT_E4M3_UE8M0_128 = 1, ORC_ACT_E2M1_UE8M0_32 = 2 };
 
 /* One layer's expert set: codes[e] / scales[e] point to the canonical blobs of
  * expert e (NULL allowed for experts that the routing never selects; selecting
@@ -50,6 +50,9 @@ double orc_e4m3_value(uint8_t code);
 uint8_t orc_e4m3_rne(double v);
 int orc_ue8m0_for_amax(double amax);
 void orc_act_quant_e4m3(const double* v, int n, int block, uint8_t* codes, uint8_t* scale_bytes);
+int orc_e2m1_rne(double v);
+int orc_ue8m0_for_amax_e2m1(double amax);
+void orc_act_quant_e2m1(const double* v, int n, int block, uint8_t* codes, uint8_t* scale_bytes);
 double orc_silu(double g);
 
 int orc_matvec(const uint8_t* codes, const uint8_t* scales, int rows, int k,

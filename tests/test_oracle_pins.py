@@ -185,6 +185,97 @@ def test_act_quant_scale_is_minimal_and_codes_fit():
                 assert codes[b * 128 + i] == _e4m3_brute(x / 2.0 ** k) or abs(x / 2.0 ** k) > 440
 
 
+# ------------------------------------------------ E2M1 activations (MXFP4)
+
+E2M1_GRID = np.array([e2m1_bitfield(c) for c in range(8)])     # 0, .5, 1, 1.5, 2, 3, 4, 6
+
+
+def _e2m1_brute(v):
+    """Nearest E2M1 code by brute force over the bit-field grid: ties to the
+    code whose mantissa bit is 0, magnitudes above 6 saturate."""
+    a = abs(v)
+    if a >= 6.0:
+        return 7 | (8 if math.copysign(1.0, v) < 0 else 0)
+    d = np.abs(E2M1_GRID - a)
+    best = [c for c in range(8) if d[c] == d.min()]
+    c = best[0] if len(best) == 1 else [b for b in best if b & 1 == 0][0]
+    return c | (8 if math.copysign(1.0, v) < 0 else 0)
+
+
+def _e2m1_qd_numpy(v, block=32):
+    """Independent MXFP4 quantize-dequantize: per block the least k with
+    amax <= 6 * 2^k (log2 then exact correction), vectorised nearest grid
+    value with ties to the even mantissa."""
+    out = np.empty_like(v)
+    for b0 in range(0, v.size, block):
+        blk = v[b0:b0 + block]
+        amax = np.abs(blk).max()
+        k = 0 if amax == 0 else math.ceil(math.log2(amax / 6.0))
+        while amax > 6.0 * 2.0 ** k:
+            k += 1
+        while amax != 0 and amax <= 6.0 * 2.0 ** (k - 1):
+            k -= 1
+        a = np.abs(blk) / 2.0 ** k
+        d = np.abs(a[:, None] - E2M1_GRID[None, :])
+        dmin = d.min(axis=1, keepdims=True)
+        cand = (d == dmin)
+        even = cand & ((np.arange(8) & 1) == 0)[None, :]
+        pick = np.where(even.any(axis=1), even.argmax(axis=1), cand.argmax(axis=1))
+        out[b0:b0 + block] = np.sign(blk) * E2M1_GRID[pick] * 2.0 ** k
+    return out
+
+
+def test_e2m1_rne_equals_brute_force_on_all_bf16():
+    bits = np.arange(65536, dtype=np.uint32)
+    vals = (bits << 16).view(np.float32).astype(np.float64)
+    finite = np.isfinite(vals)
+    for v in vals[finite]:
+        assert oracle.e2m1_rne(float(v)) == _e2m1_brute(float(v)), v
+
+
+def test_e2m1_rne_ties_and_saturation():
+    # the midpoints of the grid go to the even mantissa
+    for v, c in [(0.25, 0), (0.75, 2), (1.25, 2), (1.75, 4), (2.5, 4), (3.5, 6), (5.0, 6)]:
+        assert oracle.e2m1_rne(v) == c and oracle.e2m1_rne(-v) == c | 8
+    assert oracle.e2m1_rne(6.0) == 7 and oracle.e2m1_rne(1e30) == 7 and oracle.e2m1_rne(-7.0) == 15
+
+
+def test_ue8m0_for_amax_e2m1_boundaries():
+    assert oracle.ue8m0_for_amax_e2m1(0.0) == 127
+    for k in range(-40, 41):
+        edge = math.ldexp(6.0, k)
+        assert oracle.ue8m0_for_amax_e2m1(edge) == 127 + k
+        assert oracle.ue8m0_for_amax_e2m1(math.nextafter(edge, math.inf)) == 128 + k
+        assert oracle.ue8m0_for_amax_e2m1(math.ldexp(6.0, k - 1) * 1.0000001) == 127 + k
+    assert oracle.ue8m0_for_amax_e2m1(math.inf) == 255
+
+
+def test_act_quant_e2m1_scale_is_minimal_and_codes_are_nearest():
+    rng = np.random.default_rng(4)
+    for n in (1, 31, 64, 300, 2880):
+        v = rng.standard_normal(n) * 2.0 ** rng.integers(-20, 20)
+        codes, scales = oracle.act_quant_e2m1(v, 32)
+        for b, s in enumerate(scales):
+            blk = v[b * 32:(b + 1) * 32]
+            k = int(s) - 127
+            amax = np.abs(blk).max()
+            assert amax <= 6.0 * 2.0 ** k and amax > 6.0 * 2.0 ** (k - 1)
+            for i, x in enumerate(blk):
+                assert codes[b * 32 + i] == _e2m1_brute(x / 2.0 ** k)
+
+
+def test_act_quant_e2m1_fixed_points():
+    # a block of E2M1 values times 2^k (holding +-6 * 2^k) quantizes to itself
+    rng = np.random.default_rng(5)
+    for k in (-9, -1, 0, 3, 17):
+        c = rng.integers(0, 16, 32)
+        c[7] = 7
+        v = np.array([e2m1_bitfield(int(x)) for x in c]) * 2.0 ** k
+        codes, scales = oracle.act_quant_e2m1(v, 32)
+        assert scales[0] == 127 + k
+        assert np.array_equal(np.array([e2m1_bitfield(int(x)) for x in codes]) * 2.0 ** k, v)
+
+
 # --------------------------------------------------------------- SiLU
 
 def test_silu_closed_forms():
@@ -242,7 +333,7 @@ def test_matvec_equals_dense_matmul():
 def test_expert_ffn_zero_input_gives_exact_zero():
     H, I = 256, 128
     codes, scales = synth.expert_canonical(H, I, 0)
-    for mode in (oracle.ACT_BF16, oracle.ACT_E4M3_UE8M0_128):
+    for mode in (oracle.ACT_BF16, oracle.ACT_E4M3_UE8M0_128, oracle.ACT_E2M1_UE8M0_32):
         o = oracle.expert_ffn(codes, scales, H, I, np.zeros(H), mode)
         assert np.all(o == 0.0)
 
@@ -300,6 +391,20 @@ def test_expert_ffn_e4m3_mode_equals_dense_definition():
     # h crosses an fp32 rounding in the torch quantizer; allow rare rounding flips
     err = np.abs(got - ref).max() / np.sqrt(np.mean(ref ** 2))
     assert err < 1e-3
+
+
+def test_expert_ffn_e2m1_mode_equals_dense_definition():
+    H, I = 256, 128
+    codes, scales = synth.expert_canonical(H, I, 6)
+    Wg, Wu, Wd = split_expert(codes, scales, H, I)
+    x = synth.bf16_bits_to_f32(synth.activations_bf16(1, H, seed=8)[0]).astype(np.float64)
+    xq = _e2m1_qd_numpy(x)
+    g, u = Wg @ xq, Wu @ xq
+    ref = Wd @ _e2m1_qd_numpy(g / (1 + np.exp(-g)) * u)
+    got = oracle.expert_ffn(codes, scales, H, I, x, oracle.ACT_E2M1_UE8M0_32)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    # and the mode does quantize: it differs from the bf16 path
+    assert not np.allclose(got, oracle.expert_ffn(codes, scales, H, I, x), rtol=1e-3)
 
 
 def _tiny_layer(seed=0):
