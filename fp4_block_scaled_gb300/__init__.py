@@ -24,6 +24,7 @@ MOE_ERR_DEVICE_TIMEOUT = -6
 
 MOE_ACT_BF16 = 0
 MOE_ACT_E4M3_UE8M0_128 = 1
+MOE_ACT_E2M1_UE8M0_32 = 2
 MOE_OUT_BF16 = 0
 MOE_OUT_F32 = 1
 DEFAULT_GEMM_MIN_TOKENS = 16   # MOE_DEFAULT_GEMM_MIN_TOKENS

@@ -61,7 +61,8 @@ int check_cfg(const moe_ffn_config* c)
         c->max_tokens < 0)
         return MOE_ERR_INVALID_ARG;
     if (c->topk > 16 || c->topk > c->num_experts) return MOE_ERR_INVALID_ARG;
-    if (c->act_mode != MOE_ACT_BF16 && c->act_mode != MOE_ACT_E4M3_UE8M0_128)
+    if (c->act_mode != MOE_ACT_BF16 && c->act_mode != MOE_ACT_E4M3_UE8M0_128 &&
+        c->act_mode != MOE_ACT_E2M1_UE8M0_32)
         return MOE_ERR_INVALID_ARG;
     if (c->out_dtype != MOE_OUT_BF16 && c->out_dtype != MOE_OUT_F32) return MOE_ERR_INVALID_ARG;
     if (c->hidden % 128 || c->inter % 64) return MOE_ERR_UNSUPPORTED;
@@ -242,6 +243,7 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     a.status = h->status;
     a.out_f32 = cfg->out_dtype == MOE_OUT_F32;
     a.act_e4m3 = e4m3;
+    a.act_e2m1 = cfg->act_mode == MOE_ACT_E2M1_UE8M0_32;
     a.hraw = e4m3 ? (float*)(b + o_hraw) : nullptr;
     a.hpair = e4m3 ? (int*)(b + o_hpair) : nullptr;
     GroupArgs& ga = h->gbase;
@@ -255,6 +257,7 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     ga.status = h->status;
     ga.out_f32 = a.out_f32;
     ga.act_e4m3 = e4m3;
+    ga.act_e2m1 = a.act_e2m1;
     if (grouped) {
         ga.sync = (int*)(b + o_gsync);
         ga.counts = (int32_t*)(b + o_gcnt);

@@ -369,6 +369,22 @@ __device__ __forceinline__ int e2m1_scale_byte(float amax)
     return s < 1 ? 1 : (s > 254 ? 254 : s);
 }
 
+// Two elements of a 32-block held by the 16 lanes of a half-warp (lane l:
+// elements 2l, 2l + 1 of the block) quantized to E2M1 under the block's
+// ue8m0 scale -- the least 2^e with max|v| <= 6 * 2^e -- and taken back: a
+// round-to-nearest-even conversion of an exact scaling.  Every lane of the
+// warp takes part.
+__device__ __forceinline__ float2 e2m1_block_quant_dequant(float v0, float v1)
+{
+    float amax = fmaxf(fabsf(v0), fabsf(v1));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const int s = e2m1_scale_byte(amax);
+    const float down = exp2i(127 - s), up = exp2i(s - 127);
+    const float2 d = e2m1x2_to_f32x2(f32x2_to_e2m1x2(v0 * down, v1 * down));
+    return make_float2(d.x * up, d.y * up);
+}
+
 // Arrive at named barrier `id` without waiting (the waiting side uses
 // named_sync with the same id and thread count).
 __device__ __forceinline__ void named_arrive(int id, int threads)

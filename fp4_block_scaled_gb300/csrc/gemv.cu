@@ -268,6 +268,11 @@ __global__ void __launch_bounds__(256) k_prep(GemvArgs a)
         v0 = __uint_as_float((uint32_t)xb[0] << 16);
         v1 = __uint_as_float((uint32_t)xb[1] << 16);
     }
+    if (a.act_e2m1) {      // x quantized to E2M1 per 32 (carried exactly by the pieces)
+        const float2 q = e2m1_block_quant_dequant(v0, v1);
+        v0 = q.x;
+        v1 = q.y;
+    }
     uint8_t* Bunit = a.xq + (size_t)t * act_bytes(H) + (size_t)(b / 2) * kUnitBBytes;
     uint8_t* Bsf = a.xsf + (size_t)t * act_sf_bytes(H) + (size_t)(b / 2) * kUnitSfBytes;
     write_pieces64(v0, v1, lane, Bunit, Bsf, 2 * b);
@@ -592,6 +597,11 @@ __device__ __forceinline__ void finalize_gate_up(const GemvArgs& a, const Stream
     const float2 u = *reinterpret_cast<const float2*>(comb + 64 + 2 * lane);
     float h0 = silu(g.x) * u.x, h1 = silu(g.y) * u.y;
     int done = 1;                         // tiles of h whose pieces this call writes
+    if (a.act_e2m1) {                     // h quantized to E2M1 per 32 along I, before w
+        const float2 q = e2m1_block_quant_dequant(h0, h1);
+        h0 = q.x;
+        h1 = q.y;
+    }
     if (a.act_e4m3) {
         // h is quantized to E4M3 per 128 along I (tiles 2b, 2b + 1; a last block
         // of 64 is one tile), before w.  The second tile of a block to finish

@@ -163,6 +163,19 @@ __host__ __device__ inline size_t g_act_bytes(int K, int P)
     return (size_t)(K / 128) * 64 * P + (size_t)((K % 128) ? 32 * P : 0);
 }
 
+// B bytes of one 128-K unit of a group of nt slots of P pieces: per MMA
+// (K = 64) whole 8-row groups of 256 bytes, P nt rows (64 P nt bytes when 8
+// divides P; one row group for the one-piece E2M1 mode).
+__host__ __device__ inline uint32_t g_unit_b(int P, int nt) { return (uint32_t)((P * nt + 7) / 8) * 512u; }
+
+// The pieces of a group (first sorted position p0, group g) over K with kgt
+// units: slot-proportional when 8 divides P (pact = bytes per slot), else one
+// 512-byte unit per group and unit.
+__host__ __device__ inline uint8_t* g_group_b(uint8_t* base, int P, int p0, int g, int kgt, size_t pact)
+{
+    return P >= 8 ? base + (size_t)p0 * pact : base + (size_t)g * kgt * 512;
+}
+
 // ----------------------------------------------------------------- pieces
 
 // P pieces of 64 consecutive elements (32-blocks blk0, blk0 + 1 of a unit;
@@ -208,9 +221,12 @@ __device__ __forceinline__ void store_pieces64(const Pieces64<P>& pc, int lane, 
 {
     const int bu = blk0 + (lane >> 4);             // 32-block within the unit
     const int ib = lane & 15;                      // byte within the block's row
-    uint8_t* rows = unit + (bu >> 1) * mstride + i * 32 * P + (bu & 1) * 128 + ib;
+    uint8_t* rows = unit + (bu >> 1) * mstride + (bu & 1) * 128 + ib;
 #pragma unroll
-    for (int p = 0; p < P; p++) rows[(p >> 3) * 256 + (p & 7) * 16] = pc.byte[p];
+    for (int p = 0; p < P; p++) {
+        const int n = P * i + p;
+        rows[(n >> 3) * 256 + (n & 7) * 16] = pc.byte[p];
+    }
     if (ib == 0) {
 #pragma unroll
         for (int p = 0; p < P; p++) {
@@ -221,7 +237,7 @@ __device__ __forceinline__ void store_pieces64(const Pieces64<P>& pc, int lane, 
 }
 
 // Where slot position P's pieces of unit u (of a K with kgt units) go, with
-// groups of up to S = kGroupN / NP slots of NP pieces.
+// groups of up to S = min(kGroupN / NP, kGroupTokens) slots of NP pieces.
 struct GDst {
     uint8_t* unit;
     uint8_t* atom;
@@ -232,7 +248,7 @@ template <int NP>
 __device__ __forceinline__ GDst group_dst(const GroupArgs& a, int e, int P, int u, int kgt, size_t abytes,
                                           uint8_t* codes, uint8_t* atoms)
 {
-    constexpr int S = kGroupN / NP;
+    constexpr int S = kGroupN / NP < kGroupTokens ? kGroupN / NP : kGroupTokens;
     const int rel = P - a.offsets[e];
     const int q = rel / S;
     const int g = a.gbase[e] + q;
@@ -240,8 +256,8 @@ __device__ __forceinline__ GDst group_dst(const GroupArgs& a, int e, int P, int 
     const int nt = min(S, a.counts[e] - q * S);
     GDst d;
     d.i = rel - q * S;
-    d.mstride = nt * 32 * NP;
-    d.unit = codes + (size_t)p0 * abytes + (size_t)u * nt * 64 * NP;
+    d.mstride = (int)g_unit_b(NP, nt) / 2;
+    d.unit = g_group_b(codes, NP, p0, g, kgt, abytes) + (size_t)u * g_unit_b(NP, nt);
     d.atom = atoms + ((size_t)g * kgt + u) * kUnitSfBytes;
     return d;
 }
@@ -316,6 +332,19 @@ __global__ void __launch_bounds__(256) k_gprep(GroupArgs a)
     }
     const int b = blockIdx.y * (blockDim.x >> 5) + warp;          // 64-element span
     if (b >= H / 64) return;
+    if (a.act_e2m1) {
+        // the one piece of a 32-block is its E2M1 quantization: the scale is
+        // the least 2^e with max|x| <= 6 * 2^e, codes round to nearest even
+        const size_t abytes = g_act_bytes(H, 1);
+        Pieces64<1> pc;
+        make_pieces64<1>(xval(b * 64 + 2 * lane), xval(b * 64 + 2 * lane + 1), pc);
+        for (int kk = 0; kk < a.topk; kk++) {
+            if (s_P[kk] < 0) continue;
+            const GDst d = group_dst<1>(a, s_e[kk], s_P[kk], b / 2, kgt, abytes, a.xg, a.xgsf);
+            store_pieces64<1>(pc, lane, d.unit, d.mstride, d.atom, d.i, 2 * (b & 1));
+        }
+        return;
+    }
     const size_t abytes = g_act_bytes(H, 16);
     Pieces64<16> pc;
     make_pieces64<16>(xval(b * 64 + 2 * lane), xval(b * 64 + 2 * lane + 1), pc);
@@ -467,7 +496,7 @@ struct GCursor {
         j.g = gb + c;
         j.p0 = p0e + c * gs;
         j.nt = min(gs, cnt - c * gs);
-        j.B = (PHASE == 0 ? a.xg : a.hg) + (size_t)j.p0 * p.act_bytes;
+        j.B = g_group_b(PHASE == 0 ? a.xg : a.hg, p.np, j.p0, j.g, p.kgt, p.act_bytes);
         j.Bsf = (PHASE == 0 ? a.xgsf : a.hgsf) + (size_t)j.g * p.kgt * kUnitSfBytes;
         j.ok = ok;
         j.w = ok ? blob + p.off + (size_t)j.tile * p.tile_bytes : nullptr;
@@ -517,8 +546,8 @@ __device__ bool gproduce(const GroupArgs& a, const GPlan& p, const GRange& r, GS
         const bool has_half = p.kg_half && (wk.kg + nun == wk.kgt);
         const uint32_t nfull = nun - (has_half ? 1u : 0u);
         const uint32_t wb = nfull * kUnitBytes + (has_half ? kHalfUnitBytes : 0);   // one copy
-        const uint32_t ub = 64u * (uint32_t)p.np;                 // piece bytes of a slot per unit
-        const uint32_t bb = (uint32_t)ji.nt * (nfull * ub + (has_half ? ub / 2 : 0));
+        const uint32_t gub = g_unit_b(p.np, ji.nt);               // piece bytes of the group per unit
+        const uint32_t bb = nfull * gub + (has_half ? gub / 2 : 0);
         const uint32_t bsb = nun * kUnitSfBytes;
         const int s = n % kGStagesA;
         const uint64_t tw = G_NOW();
@@ -532,8 +561,7 @@ __device__ bool gproduce(const GroupArgs& a, const GPlan& p, const GRange& r, GS
         if (ji.ok) {
             mbar_arrive_expect_tx(&sm.fullA[s], wb);
             bulk_g2s(stg, ji.w + (size_t)wk.kg * kUnitBytes, wb, &sm.fullA[s]);
-            sm.bsrc[s] = GBSrc{ji.B + (size_t)wk.kg * ji.nt * ub, ji.Bsf + (size_t)wk.kg * kUnitSfBytes, bb, bsb,
-                               PHASE};
+            sm.bsrc[s] = GBSrc{ji.B + (size_t)wk.kg * gub, ji.Bsf + (size_t)wk.kg * kUnitSfBytes, bb, bsb, PHASE};
         } else {
             mbar_arrive(&sm.fullA[s]);     // an empty stage: nothing to multiply
             sm.bsrc[s].B = nullptr;
@@ -628,7 +656,6 @@ __device__ void gissue(const GroupArgs& a, const GPlan& p, const GRange& r, GSme
     GJob ji = cur.job<PHASE>(a, p);
     bool any = false;               // this issuer's accumulator holds part of this job
     bool job_start = true;
-    const uint32_t ub = 64u * (uint32_t)p.np;
     uint64_t w_acc = 0, w_a = 0, w_b = 0, w_is = 0, w_all = 0;   // debug builds: time spent waiting / issuing
     const uint64_t t_begin = G_NOW();
     while (wk.u < wk.u1) {
@@ -671,7 +698,8 @@ __device__ void gissue(const GroupArgs& a, const GPlan& p, const GRange& r, GSme
             tc_cp_sf(col + 4, umma_desc(smem_u32(sbs + kGOffSfb + ii * kUnitSfBytes), 16, 128));
             for (uint32_t m = 0; m < (half ? 1u : 2u); m++) {
                 const uint64_t ad = umma_desc(smem_u32(unit + m * kMmaCodeBytes), 128, 256);
-                const uint64_t bd = umma_desc(smem_u32(sbs + ii * nt * ub + m * nt * (ub / 2)), 128, 256);
+                const uint32_t gub = g_unit_b(p.np, (int)nt);
+                const uint64_t bd = umma_desc(smem_u32(sbs + ii * gub + m * (gub / 2)), 128, 256);
                 tc_mma_mxf4(tmem + (uint32_t)(ii * 2 + is.buf) * kGAccCols, ad, bd, mxf4_idesc_sf(idesc, 2 * m),
                             col, col + 4, any ? 1u : 0u);
                 any = true;
@@ -729,9 +757,9 @@ __device__ void gfinalize_gate_up(const GroupArgs& a, const GPlan& p, const GJob
     float h0 = silu(g.x) * u.x, h1 = silu(g.y) * u.y;
     const size_t abytes = g_act_bytes(a.I, NP);
     const int kgt = (a.I + 127) / 128;
-    uint8_t* unit = a.hg + (size_t)jb.p0 * abytes + (size_t)(tile / 2) * jb.nt * 64 * NP;
+    uint8_t* unit = g_group_b(a.hg, NP, jb.p0, jb.g, kgt, abytes) + (size_t)(tile / 2) * g_unit_b(NP, jb.nt);
     uint8_t* atom = a.hgsf + ((size_t)jb.g * kgt + tile / 2) * kUnitSfBytes;
-    const int mstride = jb.nt * 32 * NP;
+    const int mstride = (int)g_unit_b(NP, jb.nt) / 2;
     int done = 1;                         // h tiles whose pieces this call writes
     if (a.act_e4m3) {
         // h is quantized to E4M3 per 128 along I (tiles 2b, 2b + 1; a last block
@@ -777,7 +805,9 @@ __device__ void gfinalize_gate_up(const GroupArgs& a, const GPlan& p, const GJob
             store_pieces64<NP>(po, lane, unit, mstride, atom, i, 2 * ((tile ^ 1) & 1));
         }
     }
-    const float w = a.w[a.perm[P]];
+    // E2M1 mode: the one piece is h quantized per 32 (w scales the down output);
+    // otherwise w * h as pieces
+    const float w = a.act_e2m1 ? 1.0f : a.w[a.perm[P]];
     Pieces64<NP> pc;
     make_pieces64<NP>(h0 * w, h1 * w, pc);
     store_pieces64<NP>(pc, lane, unit, mstride, atom, i, 2 * (tile & 1));
@@ -886,6 +916,14 @@ __device__ void gepilogue(const GroupArgs& a, const GPlan& p, const GRange& r, G
                 if (!((mask >> ii) & 1u)) continue;
                 const uint32_t acc0 = tmem + (uint32_t)(ii * 2 + buf) * kGAccCols + ((uint32_t)(quad * 32) << 16);
 #pragma unroll
+                if (p.np == 1) {            // one column per slot
+                    float acc[8];
+                    tc_ld8(acc0, acc);
+#pragma unroll
+                    for (int i = 0; i < kNT; i++) v[i] += acc[i];
+                    continue;
+                }
+#pragma unroll
                 for (int i = 0; i < kNT; i++) {
                     if (i >= nt) break;
                     if (p.np == 8) {
@@ -938,6 +976,7 @@ __device__ void gepilogue(const GroupArgs& a, const GPlan& p, const GRange& r, G
             }
             for (int i = quad; i < nt; i += 4) {
                 if (p.np == 8) gfinalize_gate_up<8>(a, p, cur, i, comb[i], lane, sm.hstash[i], local);
+                else if (p.np == 1) gfinalize_gate_up<1>(a, p, cur, i, comb[i], lane, sm.hstash[i], local);
                 else gfinalize_gate_up<16>(a, p, cur, i, comb[i], lane, sm.hstash[i], local);
             }
             if (quad == 0 && lane == 0) G_TRACE(3, es.use[0] + es.use[1]);
@@ -1062,9 +1101,14 @@ __global__ void __launch_bounds__(256) k_gcombine(GroupArgs a)
 {
     const int t = blockIdx.x, H = a.H;
     __shared__ int s_P[16];
+    __shared__ float s_w[16];
     pdl_wait();
     pdl_trigger();
-    if (threadIdx.x < a.topk) s_P[threadIdx.x] = a.inv[t * a.topk + threadIdx.x];
+    if (threadIdx.x < a.topk) {
+        s_P[threadIdx.x] = a.inv[t * a.topk + threadIdx.x];
+        // the E2M1 mode applies the routing weight here (the other modes fold it into h)
+        s_w[threadIdx.x] = a.act_e2m1 ? a.w[t * a.topk + threadIdx.x] : 1.0f;
+    }
     __syncthreads();
     for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
         float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -1072,10 +1116,11 @@ __global__ void __launch_bounds__(256) k_gcombine(GroupArgs a)
             const int P = s_P[kk];
             if (P < 0) continue;
             const float4 o = __ldcg(reinterpret_cast<const float4*>(a.obuf + (size_t)P * H + c));
-            s.x += o.x;
-            s.y += o.y;
-            s.z += o.z;
-            s.w += o.w;
+            const float w = s_w[kk];
+            s.x = fmaf(w, o.x, s.x);
+            s.y = fmaf(w, o.y, s.y);
+            s.z = fmaf(w, o.z, s.z);
+            s.w = fmaf(w, o.w, s.w);
         }
         const size_t o = (size_t)t * H + c;
         if (a.x_resid) {
@@ -1123,8 +1168,8 @@ GPlan gplan(const GroupArgs& a, int phase)
     p.ntiles = L.tiles;
     p.tile_bytes = L.tile_bytes();
     p.off = phase == 0 ? E.gu_off : E.dn_off;
-    p.np = group_pieces(a.act_e4m3 != 0);
-    p.gs = group_slots(a.act_e4m3 != 0);
+    p.np = group_pieces(a.act_e4m3 != 0, a.act_e2m1 != 0);
+    p.gs = group_slots(a.act_e4m3 != 0, a.act_e2m1 != 0);
     p.act_bytes = g_act_bytes(phase == 0 ? a.H : a.I, p.np);
     p.phase = phase;
     return p;
@@ -1171,7 +1216,7 @@ cudaError_t launch_group_layer(const GroupArgs& a0, cudaStream_t s, bool pdl, Pr
     cudaError_t err;
     RouteArgs ra{a.idx,     a.T * a.topk, a.E,       a.counts, a.offsets,
                  a.perm,    a.inv,        a.status,  a.gbase,  a.groups,
-                 group_slots(a.act_e4m3 != 0)};
+                 group_slots(a.act_e4m3 != 0, a.act_e2m1 != 0)};
     if (prof) prof->begin(kPhaseRoute, s);
     err = launch_route(ra, s, chain);
     if (prof) prof->end(s);

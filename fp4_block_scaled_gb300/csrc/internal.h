@@ -36,6 +36,8 @@ struct GemvArgs {
     uint64_t* part_dn;                  // [sms][128]
     // E4M3 activation mode (x and h quantized to E4M3, one ue8m0 scale per 128)
     int act_e4m3;
+    // E2M1 activation mode (x and h quantized to E2M1, one ue8m0 scale per 32)
+    int act_e2m1;
     float* hraw;                        // [T*k][I] h before quantization
     int* hpair;                         // [T*k][ceil(I/128)] tiles of each 128-block of h done
     int* sync;                          // [3]: gate/up groups finished, CTAs finished (both
@@ -99,8 +101,14 @@ cudaError_t launch_gemv_layer(const GemvArgs& a, cudaStream_t s, bool pdl, Profi
 // E4M3 mode, 4 slots of 16 pieces in the bf16 mode).
 constexpr int kGroupTokens = 8;
 constexpr int kGroupN = 64;
-__host__ __device__ inline int group_pieces(bool e4m3) { return e4m3 ? 8 : 16; }
-__host__ __device__ inline int group_slots(bool e4m3) { return kGroupN / group_pieces(e4m3); }
+// pieces per slot of the expert-major path's activations, by mode (E2M1: the
+// quantized vector itself), and slots per group (at most kGroupTokens)
+__host__ __device__ inline int group_pieces(bool e4m3, bool e2m1 = false) { return e2m1 ? 1 : (e4m3 ? 8 : 16); }
+__host__ __device__ inline int group_slots(bool e4m3, bool e2m1 = false)
+{
+    const int s = kGroupN / group_pieces(e4m3, e2m1);
+    return s < kGroupTokens ? s : kGroupTokens;
+}
 
 // One group of the expert-major path.
 struct __align__(16) GroupInfo {
@@ -155,6 +163,7 @@ struct GroupArgs {
     uint64_t* part_gu;      // [sms][kGroupTokens][128] tagged partial sums
     uint64_t* part_dn;
     int act_e4m3;
+    int act_e2m1;           // one E2M1 piece per slot; w scales the down output
     float* hraw;            // [n][I]
     int* hpair;             // [n][ceil(I/128)]
     int* sync;              // [3], as on the slot-major path (its own words)

@@ -55,7 +55,14 @@ enum {
      * consecutive elements (the last block of h may be shorter) before each
      * projection; the scale is 2^k with k the least integer such that
      * amax <= 448 * 2^k, and codes round to nearest even, saturating. */
-    MOE_ACT_E4M3_UE8M0_128 = 1
+    MOE_ACT_E4M3_UE8M0_128 = 1,
+    /* x and h are quantized to FP4 E2M1 with one ue8m0 scale per 32
+     * consecutive elements (MXFP4) before each projection; the scale is 2^k
+     * with k the least integer such that amax <= 6 * 2^k, and codes round to
+     * nearest even, saturating.  On the expert-major path a slot's activation
+     * is then one E2M1 vector (the MMA's B operand is 4-bit, like the
+     * weights) and the routing weight scales the slot's down output. */
+    MOE_ACT_E2M1_UE8M0_32 = 2
 };
 
 enum { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 };

@@ -84,7 +84,8 @@ class Layer:
     def oracle(self, x_bits, idx, w):
         codes, scales = host_experts(self.H, self.I, idx.reshape(-1), layer=self.layer,
                                      seed=self.seed, E=self.E)
-        act = oracle.ACT_E4M3_UE8M0_128 if self.act == moe.MOE_ACT_E4M3_UE8M0_128 else oracle.ACT_BF16
+        act = {moe.MOE_ACT_E4M3_UE8M0_128: oracle.ACT_E4M3_UE8M0_128,
+               moe.MOE_ACT_E2M1_UE8M0_32: oracle.ACT_E2M1_UE8M0_32}.get(self.act, oracle.ACT_BF16)
         return oracle.moe_ffn(codes, scales, self.H, self.I, x_bits, idx, w, act_mode=act, nthreads=8)
 
     def close(self):
@@ -94,3 +95,66 @@ class Layer:
 def inputs(T, E, H, k, seed=0):
     return (synth.activations_bf16(T, H, seed=seed), synth.routing_uniform(T, E, k, seed=seed),
             synth.routing_weights(T, k, seed=seed))
+
+
+# ----------------------------------------------------- E2M1 activation mode
+
+E2M1_MIDPOINTS = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+
+
+def e2m1_flip_bound(H, I, E, x_bits, idx, w, layer=0, seed=0, delta=1e-4):
+    """How far y[t] may move (per output row) because h, computed in fp32 on
+    the GPU and in fp64 by the oracle, takes the other E2M1 code: every element
+    of h within delta (in units of its block scale) of a rounding midpoint, and
+    every element of a block whose maximum lies within a relative delta of a
+    scale boundary, may move by up to the largest E2M1 step (2 units, at the
+    larger candidate scale).  The fp32 h differs from the fp64 h by far less
+    than delta.  Returns (bound [T][H], number of such elements)."""
+    e2m1 = np.array([oracle.e2m1_value(c) for c in range(16)])
+    T, k = idx.shape
+    codes, scales = host_experts(H, I, idx.reshape(-1), layer=layer, seed=seed, E=E)
+    gc, gs = I * H // 2, I * H // 32
+    bound = np.zeros((T, H))
+    n_amb = 0
+    for t in range(T):
+        xf = (x_bits[t].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        xc, xs = oracle.act_quant_e2m1(xf, 32)
+        xq = e2m1[xc] * np.ldexp(1.0, np.repeat(xs.astype(np.int64), 32)[:H] - 127)
+        for j in range(k):
+            e = int(idx[t, j])
+            if e < 0 or e >= E:
+                continue
+            c, s = codes[e], scales[e]
+            g = oracle.matvec(c[:gc], s[:gs], I, H, xq)
+            u = oracle.matvec(c[gc:2 * gc], s[gs:2 * gs], I, H, xq)
+            h = g / (1.0 + np.exp(-g)) * u
+            dc = np.asarray(c[2 * gc:], np.uint8).reshape(H, I // 2)
+            ds = np.asarray(s[2 * gs:], np.uint8).reshape(H, I // 32)
+            for b0 in range(0, I, 32):
+                blk = h[b0:b0 + 32]
+                amax = float(np.abs(blk).max())
+                kk = oracle.ue8m0_for_amax_e2m1(amax) - 127
+                r = np.abs(blk) / 2.0 ** kk
+                near = np.abs(r[:, None] - E2M1_MIDPOINTS[None, :]).min(axis=1) < delta
+                edge = amax > 0 and (abs(amax / (6.0 * 2.0 ** (kk - 1)) - 1) < delta
+                                     or abs(amax / (6.0 * 2.0 ** kk) - 1) < delta)
+                amb = np.arange(32) if edge else np.nonzero(near)[0]
+                for i in amb:
+                    col_i = b0 + int(i)
+                    byte = dc[:, col_i // 2]
+                    nib = (byte >> 4) if col_i & 1 else (byte & 15)
+                    col = e2m1[nib] * np.ldexp(1.0, ds[:, col_i // 32].astype(np.int64) - 127)
+                    bound[t] += abs(float(w[t, j])) * np.abs(col) * 2.0 * 2.0 ** (kk + 1)
+                    n_amb += 1
+    return bound, n_amb
+
+
+def assert_close_e2m1(y, ref, bound, what=""):
+    """Within the usual tolerance once each row's possible code flips are
+    allowed for; cosine >= 0.9999."""
+    y = np.asarray(y, np.float64)
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    excess = np.abs(y - ref) - bound
+    rel = float(excess.max()) / rms
+    _, cos = errors(y, ref)
+    assert rel <= REL_MAX_ERR and cos >= 0.9999, f"{what}: max(|err| - flip bound)/rms={rel:.3e} cos={cos:.8f}"
