@@ -177,7 +177,7 @@ def traffic_record(kernel, workload, algorithmic_bytes):
 def _act_mode(wl):
     import oracle
 
-    return oracle.ACT_E4M3_UE8M0_128 if wl["act"] == "e4m3" else oracle.ACT_BF16
+    return {"e4m3": oracle.ACT_E4M3_UE8M0_128, "e2m1": oracle.ACT_E2M1_UE8M0_32}.get(wl["act"], oracle.ACT_BF16)
 
 
 def _oracle_token(wl, n, seed):
@@ -316,7 +316,7 @@ def run_ours(args, wl):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     E, H, I, k, T, L = wl["E"], wl["H"], wl["I"], wl["k"], wl["T"], wl["L"]
-    act = moe.MOE_ACT_E4M3_UE8M0_128 if wl["act"] == "e4m3" else moe.MOE_ACT_BF16
+    act = {"e4m3": moe.MOE_ACT_E4M3_UE8M0_128, "e2m1": moe.MOE_ACT_E2M1_UE8M0_32}.get(wl["act"], moe.MOE_ACT_BF16)
     gmin = {"auto": 0, "slot": T + 1, "group": 1}[args.path]
     cfg = moe.config(E, H, I, k, T, act_mode=act, out_dtype=moe.MOE_OUT_F32, gemm_min_tokens=gmin)
     grouped = T >= (gmin or moe.DEFAULT_GEMM_MIN_TOKENS)
@@ -513,7 +513,7 @@ def run_ours(args, wl):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "e4m3xe2m1->f32" if wl["act"] == "e4m3" else "f16xe2m1->f32",
+            "dtype": {"e4m3": "e4m3xe2m1->f32", "e2m1": "e2m1xe2m1->f32"}.get(wl["act"], "f16xe2m1->f32"),
             "data": "synthetic",
             "config": {"workload": args.workload, "layers": L, "experts": E, "hidden": H, "inter": I,
                        "topk": k, "tokens_per_step": T, "routing": wl["dist"], "activations": wl["act"],
@@ -553,8 +553,12 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
     ap.add_argument("--path", choices=["auto", "slot", "group"], default="auto",
                     help="layer path: the library's choice for T, or forced slot-major / expert-major")
+    ap.add_argument("--act", choices=["bf16", "e4m3", "e2m1"], default=None,
+                    help="activation numerics (default: the workload's)")
     args = ap.parse_args()
-    wl = WORKLOADS[args.workload]
+    wl = dict(WORKLOADS[args.workload])
+    if args.act:
+        wl["act"] = args.act
     if args.steps is None:
         args.steps = wl["steps"] if args.impl == "ours" else 10
     if args.warmup is None:

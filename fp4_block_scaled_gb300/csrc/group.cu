@@ -168,12 +168,15 @@ __host__ __device__ inline size_t g_act_bytes(int K, int P)
 // divides P; one row group for the one-piece E2M1 mode).
 __host__ __device__ inline uint32_t g_unit_b(int P, int nt) { return (uint32_t)((P * nt + 7) / 8) * 512u; }
 
-// The pieces of a group (first sorted position p0, group g) over K with kgt
-// units: slot-proportional when 8 divides P (pact = bytes per slot), else one
-// 512-byte unit per group and unit.
-__host__ __device__ inline uint8_t* g_group_b(uint8_t* base, int P, int p0, int g, int kgt, size_t pact)
+// The pieces of a group (first sorted position p0, group g; pact = piece
+// bytes of one slot over K): slot-proportional when 8 divides P, else a region
+// per group sized for a full group (its units are whole 8-row groups), which
+// is at most the 16-piece bytes of a slot, so the buffers sized per slot hold
+// it (there are no more groups than slots).
+__host__ __device__ inline uint8_t* g_group_b(uint8_t* base, int P, int p0, int g, size_t pact)
 {
-    return P >= 8 ? base + (size_t)p0 * pact : base + (size_t)g * kgt * 512;
+    const int S = kGroupN / P < kGroupTokens ? kGroupN / P : kGroupTokens;
+    return P >= 8 ? base + (size_t)p0 * pact : base + (size_t)g * pact * S;
 }
 
 // ----------------------------------------------------------------- pieces
@@ -257,7 +260,7 @@ __device__ __forceinline__ GDst group_dst(const GroupArgs& a, int e, int P, int 
     GDst d;
     d.i = rel - q * S;
     d.mstride = (int)g_unit_b(NP, nt) / 2;
-    d.unit = g_group_b(codes, NP, p0, g, kgt, abytes) + (size_t)u * g_unit_b(NP, nt);
+    d.unit = g_group_b(codes, NP, p0, g, abytes) + (size_t)u * g_unit_b(NP, nt);
     d.atom = atoms + ((size_t)g * kgt + u) * kUnitSfBytes;
     return d;
 }
@@ -496,7 +499,7 @@ struct GCursor {
         j.g = gb + c;
         j.p0 = p0e + c * gs;
         j.nt = min(gs, cnt - c * gs);
-        j.B = g_group_b(PHASE == 0 ? a.xg : a.hg, p.np, j.p0, j.g, p.kgt, p.act_bytes);
+        j.B = g_group_b(PHASE == 0 ? a.xg : a.hg, p.np, j.p0, j.g, p.act_bytes);
         j.Bsf = (PHASE == 0 ? a.xgsf : a.hgsf) + (size_t)j.g * p.kgt * kUnitSfBytes;
         j.ok = ok;
         j.w = ok ? blob + p.off + (size_t)j.tile * p.tile_bytes : nullptr;
@@ -757,7 +760,7 @@ __device__ void gfinalize_gate_up(const GroupArgs& a, const GPlan& p, const GJob
     float h0 = silu(g.x) * u.x, h1 = silu(g.y) * u.y;
     const size_t abytes = g_act_bytes(a.I, NP);
     const int kgt = (a.I + 127) / 128;
-    uint8_t* unit = g_group_b(a.hg, NP, jb.p0, jb.g, kgt, abytes) + (size_t)(tile / 2) * g_unit_b(NP, jb.nt);
+    uint8_t* unit = g_group_b(a.hg, NP, jb.p0, jb.g, abytes) + (size_t)(tile / 2) * g_unit_b(NP, jb.nt);
     uint8_t* atom = a.hgsf + ((size_t)jb.g * kgt + tile / 2) * kUnitSfBytes;
     const int mstride = (int)g_unit_b(NP, jb.nt) / 2;
     int done = 1;                         // h tiles whose pieces this call writes
@@ -917,8 +920,8 @@ __device__ void gepilogue(const GroupArgs& a, const GPlan& p, const GRange& r, G
                 const uint32_t acc0 = tmem + (uint32_t)(ii * 2 + buf) * kGAccCols + ((uint32_t)(quad * 32) << 16);
 #pragma unroll
                 if (p.np == 1) {            // one column per slot
-                    float acc[8];
-                    tc_ld8(acc0, acc);
+                    float acc[16];
+                    tc_ld16(acc0, acc);
 #pragma unroll
                     for (int i = 0; i < kNT; i++) v[i] += acc[i];
                     continue;

@@ -98,8 +98,9 @@ cudaError_t launch_gemv_layer(const GemvArgs& a, cudaStream_t s, bool pdl, Profi
 // Slots per group of the expert-major path, at most: a group is up to this
 // many consecutive sorted slots of one expert, multiplied as the N = pieces x
 // slots columns of one block-scaled MMA (N <= 64: 8 slots of 8 pieces in the
-// E4M3 mode, 4 slots of 16 pieces in the bf16 mode).
-constexpr int kGroupTokens = 8;
+// E4M3 mode, 4 slots of 16 pieces in the bf16 mode, 16 slots of one piece in
+// the E2M1 mode).
+constexpr int kGroupTokens = 16;
 constexpr int kGroupN = 64;
 // pieces per slot of the expert-major path's activations, by mode (E2M1: the
 // quantized vector itself), and slots per group (at most kGroupTokens)
