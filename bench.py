@@ -50,7 +50,16 @@ WORKLOADS = {
     # the whole step as one CUDA graph, at batch 1 and 32
     "stack_b1": dict(E=128, H=4096, I=2880, k=6, T=1, L=40, act="bf16", dist="uniform", steps=500),
     "stack_b32": dict(E=128, H=4096, I=2880, k=6, T=32, L=40, act="bf16", dist="uniform", steps=50),
+    # expert-sharing batching: pools of 256 sequences from 8 prompt clusters
+    # (alike prompts route alike), cut into batches of 32 by the planner
+    # (moe_batch_plan on the previous step's routing) or in arrival order; each
+    # step runs one batch's next-step routing through the 384-expert layer
+    "layer_b32_shared": dict(E=384, H=4096, I=2880, k=6, T=32, L=1, act="e4m3", dist="clustered_planned",
+                             steps=1000),
+    "layer_b32_arrival": dict(E=384, H=4096, I=2880, k=6, T=32, L=1, act="e4m3", dist="clustered_arrival",
+                              steps=1000),
 }
+SHARING_POOL, SHARING_CLUSTERS, SHARING_SIG_LAYERS = 256, 8, 8
 METRIC = "MoE expert-FFN decode tokens/s per layer-stack & HBM GB/s (% of GB300 roofline)"
 FALLBACK_HBM_GBS = 6800.0
 
@@ -135,7 +144,25 @@ def draw_routings(R, E, k, T, seed, dist="uniform", layer=0):
 
     idx = np.zeros((R, T, k), np.int32)
     prev = None
-    for r in range(R):
+    if dist.startswith("clustered"):
+        # batches of T from pools of alike-routing sequences: planned on the
+        # previous step's routing (SHARING_SIG_LAYERS layers), measured on the
+        # next step's routing of this layer
+        import fp4_block_scaled_gb300 as moe
+
+        per_pool = SHARING_POOL // T
+        for p in range((R + per_pool - 1) // per_pool):
+            r0, _ = synth.routing_clustered(SHARING_POOL, SHARING_SIG_LAYERS, E, k, SHARING_CLUSTERS,
+                                            seed=seed * 1000 + p, step=0)
+            r1, _ = synth.routing_clustered(SHARING_POOL, SHARING_SIG_LAYERS, E, k, SHARING_CLUSTERS,
+                                            seed=seed * 1000 + p, step=1)
+            order = (moe.moe_batch_plan(r0, E, T) if dist == "clustered_planned"
+                     else np.arange(SHARING_POOL, dtype=np.int32))
+            for b in range(per_pool):
+                r = p * per_pool + b
+                if r < R:
+                    idx[r] = r1[order[b * T:(b + 1) * T], layer % SHARING_SIG_LAYERS]
+    for r in range(R if not dist.startswith("clustered") else 0):
         st = synth.S_ROUTE + 1000 * (r + 1) + 7 * layer
         if dist == "zipf":
             cur = synth.routing_zipf(T, E, k, s=1.1, seed=seed, stream=st)
@@ -521,7 +548,9 @@ def run_ours(args, wl):
                        "parallelism": f"replicas{world}",
                        "l2": f"inputs larger than L2: {resident:.1f} GB resident experts"
                              + (", consecutive steps share no expert" if T == 1 and L == 1 else ""),
-                       "graph_chunk": chunk},
+                       "graph_chunk": chunk,
+                       "distinct_experts_per_layer_step": round(
+                           sum(distinct(i, l) for i in range(R) for l in range(L)) / (R * L), 2)},
             "hbm_gbs": gbs_step, "hbm_frac": gbs_step / peak,
             "bytes_per_step": bytes_step,
             "phase_us": {"route": ro_ms * 1e3, "prep": pr_ms * 1e3, "layer": ly_ms * 1e3,

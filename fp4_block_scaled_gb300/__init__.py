@@ -34,7 +34,7 @@ EXPORTS = [
     "moe_ffn_pack_expert", "moe_ffn_forward", "moe_ffn_forward_host", "moe_ffn_route",
     "moe_ffn_act_quant", "moe_stack_forward", "moe_ffn_profile_enable", "moe_ffn_profile_read",
     "moe_ffn_status", "moe_ffn_strerror", "moe_ffn_destroy", "moe_ffn_forward_noalloc",
-    "moe_router_topk", "moe_router_select",
+    "moe_router_topk", "moe_router_select", "moe_batch_plan", "moe_batch_distinct",
 ]
 
 MOE_PHASE_PREP = 0
@@ -95,6 +95,8 @@ def lib() -> ctypes.CDLL:
             "moe_ffn_forward_noalloc": (I, [cfgp, I, P, P, P, tblp, P, I, P, P]),
             "moe_router_topk": (I, [P, P, P, I, P, P, P, P]),
             "moe_router_select": (I, [P, P, I, P, P, P]),
+            "moe_batch_plan": (I, [P, I, I, I, I, I, P]),
+            "moe_batch_distinct": (I, [P, P, I, I, I, I, I, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -230,3 +232,40 @@ def moe_router_topk(h, x, router_w, T: int, topk_idx, topk_w, logits=None, strea
 def moe_router_select(h, logits, T: int, topk_idx, topk_w, stream=None):
     _check(lib().moe_router_select(h, _p(logits), int(T), _p(topk_idx), _p(topk_w), _s(stream)),
            "moe_router_select")
+
+
+def _host_i32(a, ndim):
+    import numpy as np
+
+    a = np.ascontiguousarray(a, dtype=np.int32)
+    if a.ndim != ndim:
+        raise ValueError(f"expected a {ndim}-d int32 array, got shape {a.shape}")
+    return a
+
+
+def moe_batch_plan(sig, E: int, B: int):
+    """Batch order of N sequences from their signatures sig [N][L][topk] (host
+    int32 expert ids, -1 for none): returns order [N] (host int32)."""
+    import numpy as np
+
+    sig = _host_i32(sig, 3)
+    N, L, k = sig.shape
+    order = np.empty(N, np.int32)
+    _check(lib().moe_batch_plan(sig.ctypes.data, N, L, k, int(E), int(B), order.ctypes.data), "moe_batch_plan")
+    return order
+
+
+def moe_batch_distinct(routing, order, E: int, B: int):
+    """Distinct experts per (batch, layer) [ceil(N/B)][L] of routing [N][L][topk]
+    cut into batches of B in the given order."""
+    import numpy as np
+
+    routing = _host_i32(routing, 3)
+    order = _host_i32(order, 1)
+    N, L, k = routing.shape
+    if order.size != N:
+        raise ValueError("order must hold N entries")
+    out = np.empty(((N + B - 1) // B, L), np.int32)
+    _check(lib().moe_batch_distinct(routing.ctypes.data, order.ctypes.data, N, L, k, int(E), int(B),
+                                    out.ctypes.data), "moe_batch_distinct")
+    return out

@@ -15,7 +15,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_ffn.so")
-SOURCES = ["api.cu", "gemv.cu", "group.cu", "pack.cu", "route.cu", "router.cu", "actquant.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "gemv.cu", "group.cu", "pack.cu", "route.cu", "router.cu", "actquant.cu", "noalloc.cu",
+           "sched.cpp"]
 HEADERS = ["common.cuh", "internal.h", "layout.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
@@ -53,7 +54,7 @@ def build(force: bool = False, verbose: bool = False, extra: list | None = None)
     extra = list(extra or [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

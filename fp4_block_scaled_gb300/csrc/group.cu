@@ -55,7 +55,7 @@
 namespace moe {
 namespace {
 
-constexpr int kNT = kGroupTokens;                            // slots per group, at most
+constexpr int kNT = kGroupTokens;                            // slots per group, at most (shared memory, partials)
 constexpr int kGIssuers = 3;
 constexpr int kGCU = kGIssuers;                              // units per stage: one per issuer
 constexpr int kGStagesA = 5;                                 // weights (HBM): the deep ring
@@ -832,25 +832,26 @@ struct GEpi {
 // order into acc; returns the first CTA not yet folded in.  With spin, waits
 // (bounded) for each; without, stops at the first whose entries are not all
 // there yet.
+template <int NT>
 __device__ __forceinline__ int gfold(const uint64_t* part, int c, int c1, int row, int nt, uint32_t tag, bool spin,
-                                     float (&acc)[kNT], bool* timed_out)
+                                     float (&acc)[NT], bool* timed_out)
 {
     uint64_t t0 = 0;
     while (c <= c1) {
-        float v[kNT];
+        float v[NT];
         bool all = true;
 #pragma unroll
-        for (int i = 0; i < kNT; i++) {
+        for (int i = 0; i < NT; i++) {
             v[i] = 0.0f;
             if (i < nt && all) {
-                const uint64_t e = g_ld_relaxed_u64(part + ((size_t)c * kNT + i) * kTileRows + row);
+                const uint64_t e = g_ld_relaxed_u64(part + ((size_t)c * NT + i) * kTileRows + row);
                 if ((uint32_t)(e >> 32) == tag) v[i] = __uint_as_float((uint32_t)e);
                 else all = false;
             }
         }
         if (all) {
 #pragma unroll
-            for (int i = 0; i < kNT; i++) acc[i] += v[i];
+            for (int i = 0; i < NT; i++) acc[i] += v[i];
             c++;
             continue;
         }
@@ -864,7 +865,7 @@ __device__ __forceinline__ int gfold(const uint64_t* part, int c, int c1, int ro
     return c;
 }
 
-template <int PHASE>
+template <int PHASE, int NT>
 __device__ void gepilogue(const GroupArgs& a, const GPlan& p, const GRange& r, GSmem& sm, uint32_t tmem, long long U,
                           int quad, int lane, GEpi& es)
 {
@@ -895,13 +896,13 @@ __device__ void gepilogue(const GroupArgs& a, const GPlan& p, const GRange& r, G
         const bool owner = js >= r.u0;
         const int c1 = owner && je > r.u1 ? g_cta_of_unit(U, G, je - 1) : (int)blockIdx.x;
         const int nt = cur.nt;
-        float pacc[kNT];
+        float pacc[NT];
 #pragma unroll
-        for (int i = 0; i < kNT; i++) pacc[i] = 0.0f;
+        for (int i = 0; i < NT; i++) pacc[i] = 0.0f;
         bool late = false;
         int cnext = blockIdx.x + 1;
         if (c1 > (int)blockIdx.x)   // while the last MMAs run: the partials that are there already
-            cnext = gfold(part, cnext, c1, row, nt, es.tag, false, pacc, &late);
+            cnext = gfold<NT>(part, cnext, c1, row, nt, es.tag, false, pacc, &late);
 
         const int buf = es.buf;
         const bool ready = !*(volatile int*)&sm.abort &&
@@ -909,9 +910,9 @@ __device__ void gepilogue(const GroupArgs& a, const GPlan& p, const GRange& r, G
         es.use[buf]++;
         if (!ready) g_set_abort(a, sm);
         tc_fence_after();
-        float v[kNT];
+        float v[NT];
 #pragma unroll
-        for (int i = 0; i < kNT; i++) v[i] = 0.0f;
+        for (int i = 0; i < NT; i++) v[i] = 0.0f;
         if (ready) {
             // slot i: the sum of its np piece columns, issuers in order
 #pragma unroll
@@ -923,11 +924,11 @@ __device__ void gepilogue(const GroupArgs& a, const GPlan& p, const GRange& r, G
                     float acc[16];
                     tc_ld16(acc0, acc);
 #pragma unroll
-                    for (int i = 0; i < kNT; i++) v[i] += acc[i];
+                    for (int i = 0; i < NT; i++) v[i] += acc[i];
                     continue;
                 }
 #pragma unroll
-                for (int i = 0; i < kNT; i++) {
+                for (int i = 0; i < NT; i++) {
                     if (i >= nt) break;
                     if (p.np == 8) {
                         float acc[8];
@@ -952,24 +953,24 @@ __device__ void gepilogue(const GroupArgs& a, const GPlan& p, const GRange& r, G
         if (!owner) {
             // a later part of a job owned by an earlier CTA
 #pragma unroll
-            for (int i = 0; i < kNT; i++)
+            for (int i = 0; i < NT; i++)
                 if (i < nt)
-                    g_st_relaxed_u64(part + ((size_t)blockIdx.x * kNT + i) * kTileRows + row,
+                    g_st_relaxed_u64(part + ((size_t)blockIdx.x * NT + i) * kTileRows + row,
                                      ((uint64_t)es.tag << 32) | __float_as_uint(v[i]));
             continue;
         }
         if (cnext <= c1) {
             const bool abort = *(volatile int*)&sm.abort;
-            gfold(part, cnext, c1, row, nt, es.tag, !abort, pacc, &late);
+            gfold<NT>(part, cnext, c1, row, nt, es.tag, !abort, pacc, &late);
             if (late) g_set_abort(a, sm);
         }
 #pragma unroll
-        for (int i = 0; i < kNT; i++) v[i] += pacc[i];
+        for (int i = 0; i < NT; i++) v[i] += pacc[i];
         if (quad == 0 && lane == 0) G_TRACE(2, es.use[0] + es.use[1]);
         if (PHASE == 0) {
             float(*comb)[kTileRows] = sm.comb[es.cb];
 #pragma unroll
-            for (int i = 0; i < kNT; i++)
+            for (int i = 0; i < NT; i++)
                 if (i < nt) comb[i][row] = v[i];
             named_sync(1, 128);
             int local = 0;      // E4M3 pair of tiles finished in this CTA (see gfinalize_gate_up)
@@ -987,7 +988,7 @@ __device__ void gepilogue(const GroupArgs& a, const GPlan& p, const GRange& r, G
         } else {
             // o of each slot: rows tile*128 .. +127 of the down output
 #pragma unroll
-            for (int i = 0; i < kNT; i++)
+            for (int i = 0; i < NT; i++)
                 if (i < nt) a.obuf[(size_t)(cur.p0 + i) * a.H + (size_t)cur.tile * kTileRows + row] = v[i];
         }
     }
@@ -999,6 +1000,7 @@ __device__ void gepilogue(const GroupArgs& a, const GPlan& p, const GRange& r, G
 // down projection, in one persistent grid.  The job count comes from the
 // route kernel, finished before this grid starts (k_gprep lets it start only
 // after waiting for the route kernel).
+template <int NT>
 __global__ void __launch_bounds__(kGThreads, 1) k_glayer(GroupArgs a, GPlan p0, GPlan p1)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1073,9 +1075,9 @@ __global__ void __launch_bounds__(kGThreads, 1) k_glayer(GroupArgs a, GPlan p0, 
         es.cb = 0;
         es.use[0] = es.use[1] = 0;
         es.tag = 1u + (g_ld_acquire_u32(a.sync + 2) & 0x3FFFFFFFu);   // never 0, the cleared value
-        gepilogue<0>(a, p0, r0, sm, tmem, U0, warp & 3, lane, es);
+        gepilogue<0, NT>(a, p0, r0, sm, tmem, U0, warp & 3, lane, es);
         if (warp == kGWarpEpi0 && lane == 0) G_CTA(5);
-        gepilogue<1>(a, p1, r1, sm, tmem, U1, warp & 3, lane, es);
+        gepilogue<1, NT>(a, p1, r1, sm, tmem, U1, warp & 3, lane, es);
         if (warp == kGWarpEpi0 && lane == 0) G_CTA(6);
         if (warp == kGWarpEpi0 && lane == 0) {
             // the last CTA to finish resets the layer's counters for the next launch
@@ -1207,8 +1209,12 @@ GroupWorkspaceSizes group_workspace_sizes(int T, int topk, int E, int H, int I, 
 
 cudaError_t group_init_device()
 {
-    return cudaFuncSetAttribute((const void*)k_glayer, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)glayer_smem());
+    cudaError_t e = cudaFuncSetAttribute((const void*)k_glayer<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)glayer_smem());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute((const void*)k_glayer<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)glayer_smem());
+    return e;
 }
 
 cudaError_t launch_group_layer(const GroupArgs& a0, cudaStream_t s, bool pdl, Profiler* prof)
@@ -1235,7 +1241,9 @@ cudaError_t launch_group_layer(const GroupArgs& a0, cudaStream_t s, bool pdl, Pr
     GPlan p0 = gplan(a, 0), p1 = gplan(a, 1);
     void* args[] = {&a, &p0, &p1};
     if (prof) prof->begin(kPhaseGateUp, s);
-    err = glaunch((const void*)k_glayer, dim3((unsigned)a.sms), dim3(kGThreads), glayer_smem(), s, chain, args);
+    // the epilogue is compiled for the mode's group size: 16 slots (E2M1) or at most 8
+    const void* fn = p0.gs > 8 ? (const void*)k_glayer<16> : (const void*)k_glayer<8>;
+    err = glaunch(fn, dim3((unsigned)a.sms), dim3(kGThreads), glayer_smem(), s, chain, args);
     if (prof) prof->end(s);
     if (err != cudaSuccess) return err;
     if (prof) prof->begin(kPhaseDown, s);

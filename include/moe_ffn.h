@@ -187,6 +187,28 @@ int moe_router_topk(moe_ffn_t h, const void* x, const void* router_w, int T, flo
 int moe_router_select(moe_ffn_t h, const float* logits, int T, int32_t* topk_idx, float* topk_w,
                       void* stream);
 
+/* Expert-sharing batch planner (host code; needs no GPU and no handle).
+ * Alike prompts route to alike experts, so batching alike sequences cuts the
+ * distinct experts a layer streams ([A100] §批处理不是「同时处理几个人」: 216 ->
+ * 156 in one layer; the pages give no algorithm).  Reading: a greedy cover --
+ * a batch starts from the lowest-numbered unplaced sequence and grows, until
+ * it holds B, by the unplaced sequence adding the fewest experts not yet in
+ * the batch summed over the layers (ties to the lower number).
+ *   sig    host int32 [N][L][topk]: each sequence's signature, its recent
+ *          top-k expert ids per layer (-1: none); ids in [-1, E)
+ *   order  host int32 [N] output: the sequences in batch order (batch b is
+ *          order[bB .. min((b+1)B, N)))
+ * Deterministic; O(N^2 L topk).  INVALID_ARG on a bad size or id. */
+int moe_batch_plan(const int32_t* sig, int N, int L, int topk, int E, int B, int32_t* order);
+
+/* The metric of the planner: the distinct experts each (batch, layer) touches
+ * when the sequences, in `order`, are cut into batches of B.
+ *   routing   host int32 [N][L][topk] (e.g. the next step's routing)
+ *   order     host int32 [N], a permutation of 0..N-1 (else INVALID_ARG)
+ *   distinct  host int32 [ceil(N/B)][L] output */
+int moe_batch_distinct(const int32_t* routing, const int32_t* order, int N, int L, int topk, int E, int B,
+                       int32_t* distinct);
+
 /* L-layer decode step on a residual stream ([A100] §然后又发现每 token 启动
  * 2000 次内核: RMSNorm and the MoE per layer, launched as a handful of
  * dispatches): for l = 0..L-1,

@@ -288,3 +288,57 @@ def topk_softmax(logits, k: int):
     rc = lib().orc_topk_softmax(_ptr(l), T, E, k, _ptr(idx), _ptr(w))
     assert rc == 0, "orc_topk_softmax failed"
     return idx, w
+
+
+# ------------------------------------------------ expert-sharing batching
+
+def batch_distinct(routing, order, B: int) -> np.ndarray:
+    """Distinct experts touched per (batch, layer) when the sequences, taken in
+    `order`, are cut into batches of B: |union of the batch's expert ids| with
+    -1 meaning none.  routing [N][L][k]; returns [ceil(N/B)][L]."""
+    routing = np.asarray(routing)
+    N, L, _ = routing.shape
+    nb = (N + B - 1) // B
+    out = np.zeros((nb, L), np.int64)
+    for b in range(nb):
+        members = [int(i) for i in order[b * B:(b + 1) * B]]
+        for l in range(L):
+            experts = set()
+            for i in members:
+                experts |= {int(e) for e in routing[i, l] if e >= 0}
+            out[b, l] = len(experts)
+    return out
+
+
+def batch_plan_greedy(sig, B: int) -> np.ndarray:
+    """The greedy expert-sharing plan, step by step: a batch starts from the
+    lowest-numbered sequence not yet placed; while it holds fewer than B, it
+    takes the unplaced sequence that adds the fewest experts not yet in the
+    batch, summed over the layers (the lowest number among equals).  Reading
+    (the pages report the effect -- 216 -> 156 distinct experts in a layer
+    when alike prompts share a batch -- and no algorithm)."""
+    sig = np.asarray(sig)
+    N, L, _ = sig.shape
+    rows = [[{int(e) for e in sig[i, l] if e >= 0} for l in range(L)] for i in range(N)]
+    placed = [False] * N
+    order = []
+    while len(order) < N:
+        seed = placed.index(False)
+        batch_sets = [set(s) for s in rows[seed]]
+        placed[seed] = True
+        order.append(seed)
+        size = 1
+        while size < B and len(order) < N:
+            best, best_cost = None, None
+            for i in range(N):
+                if placed[i]:
+                    continue
+                cost = sum(len(rows[i][l] - batch_sets[l]) for l in range(L))
+                if best_cost is None or cost < best_cost:
+                    best, best_cost = i, cost
+            placed[best] = True
+            order.append(best)
+            for l in range(L):
+                batch_sets[l] |= rows[best][l]
+            size += 1
+    return np.array(order, np.int32)

@@ -29,6 +29,11 @@ Recipes (all seed 0 unless a test says otherwise):
     top-k distinct experts (uniform without replacement); Zipf(s) routing
     draws expert e with probability proportional to (e + 1)^-s by inverse CDF.
   * topk_w: softmax (fp64) of top-k N(0,1) logits, stored as fp32.
+  * clustered routing (alike prompts route alike): sequence i belongs to
+    cluster (u64(i) >> 32) * C >> 32; cluster c has, per layer, a hot set of
+    `hot` distinct experts drawn uniformly; at decode step s each (sequence,
+    layer) draws k distinct experts, each draw from the hot set with
+    probability p_hot (uniform within it) and otherwise uniform over all E.
 """
 from __future__ import annotations
 
@@ -48,6 +53,7 @@ _C2 = np.uint64(0x94D049BB133111EB)
 S_CODES, S_SCALES = 0, 1
 S_X, S_ROUTE, S_LOGIT = 0x10, 0x11, 0x12
 S_ROUTER_W = 0x13
+S_CLUSTER, S_HOT, S_CROUTE = 0x14, 0x15, 0x16
 
 
 def mix64_int(z: int) -> int:
@@ -215,6 +221,40 @@ def routing_zipf(T: int, E: int, k: int, s: float = 1.1, seed: int = 0,
         return int(idx[t, j % ndraw])
 
     return _distinct_draws(draw, T, k, E)
+
+
+def routing_clustered(N: int, L: int, E: int, k: int, clusters: int = 8, hot: int = 32, p_hot: float = 0.6,
+                      seed: int = 0, step: int = 0):
+    """(routing [N][L][k] int32, cluster [N]) of N sequences at decode step
+    `step` under the clustered recipe; the clusters and their hot sets depend
+    on the seed only, so consecutive steps of a sequence route alike."""
+    cl = ((u64(seed, S_CLUSTER, 0, N) >> np.uint64(32)) * np.uint64(clusters)) >> np.uint64(32)
+    cl = cl.astype(np.int64)
+    ndraw = 256
+    hot_sets = {}
+
+    def hot_set(c, l):
+        if (c, l) not in hot_sets:
+            base = (c * L + l) * ndraw
+            hu = u64(seed, S_HOT, base, ndraw) >> np.uint64(32)
+            hot_sets[(c, l)] = _distinct_draws(lambda t, j: int((int(hu[j % ndraw]) * E) >> 32), 1, hot, E)[0]
+        return hot_sets[(c, l)]
+
+    out = np.zeros((N, L, k), np.int32)
+    for i in range(N):
+        for l in range(L):
+            hs = hot_set(int(cl[i]), l)
+            base = ((step * N + i) * L + l) * 2 * ndraw
+            uu = u64(seed, S_CROUTE, base, 2 * ndraw) >> np.uint64(32)
+
+            def draw(t, j, uu=uu, hs=hs):
+                a, b = int(uu[(2 * j) % (2 * ndraw)]), int(uu[(2 * j + 1) % (2 * ndraw)])
+                if a < int(p_hot * 2 ** 32):
+                    return int(hs[(b * len(hs)) >> 32])
+                return (b * E) >> 32
+
+            out[i, l] = _distinct_draws(draw, 1, k, E)[0]
+    return out, cl
 
 
 def routing_weights(T: int, k: int, seed: int = 0, stream: int = S_LOGIT, n0: int = 0) -> np.ndarray:
