@@ -60,6 +60,13 @@ WORKLOADS = {
                               steps=1000),
 }
 SHARING_POOL, SHARING_CLUSTERS, SHARING_SIG_LAYERS = 256, 8, 8
+# host-resident experts: the 384 experts of the layer in page-locked host memory,
+# 64 of them cached in HBM; consecutive steps share no expert, so every step
+# copies its 6 experts over NVLink-C2C unless a predictor prefetched them
+WORKLOADS["layer_b1_host"] = dict(E=384, H=4096, I=2880, k=6, T=1, L=1, act="bf16", dist="uniform", steps=300,
+                                  host=True, slots=64, guess=0.0)
+WORKLOADS["layer_b1_host_prefetch"] = dict(E=384, H=4096, I=2880, k=6, T=1, L=1, act="bf16", dist="uniform",
+                                           steps=300, host=True, slots=64, guess=0.8)
 METRIC = "MoE expert-FFN decode tokens/s per layer-stack & HBM GB/s (% of GB300 roofline)"
 FALLBACK_HBM_GBS = 6800.0
 
@@ -572,6 +579,147 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
+def run_host_experts(args, wl):
+    """One layer whose experts live in page-locked host memory, served by the
+    HBM expert cache (moe_expert_cache_*): per step fetch (copies of the misses
+    over NVLink-C2C), the layer, and -- with a predictor -- a prefetch of the
+    experts guessed for the next step (each of them right with probability
+    `guess`, else a random expert)."""
+    import numpy as np
+    import torch
+
+    import fp4_block_scaled_gb300 as moe
+    import synth
+    from fp4_block_scaled_gb300.experts import ExpertSet
+
+    if args.gpus != 1 or int(os.environ.get("WORLD_SIZE", "1")) != 1:
+        raise SystemExit("the host-resident workloads run on one GPU")
+    torch.cuda.set_device(0)
+    E, H, I, k, T = wl["E"], wl["H"], wl["I"], wl["k"], wl["T"]
+    cfg = moe.config(E, H, I, k, T, out_dtype=moe.MOE_OUT_F32)
+    h = moe.moe_ffn_create(cfg, 0)
+    stage = ExpertSet(h, cfg, num_experts=1)
+    host = torch.empty(E * stage.stride, dtype=torch.uint8, pin_memory=True)
+    nc, ns = synth.expert_sizes(H, I)
+    tc = torch.empty(nc, dtype=torch.uint8, device="cuda")
+    ts = torch.empty(ns, dtype=torch.uint8, device="cuda")
+    for e in range(E):
+        synth.device_fill_expert(tc.data_ptr(), ts.data_ptr(), H, I, e, layer=0, seed=0)
+        stage.load(0, tc, ts)
+        host[e * stage.stride:(e + 1) * stage.stride].copy_(stage.blobs)
+    torch.cuda.synchronize()
+    del tc, ts
+    c = moe.moe_expert_cache_create(cfg, 0, [host.data_ptr() + e * stage.stride for e in range(E)], wl["slots"])
+
+    K, W = args.steps, args.warmup
+    n = K + W + 1
+    idx_np, w_np = draw_routings(n, E, k, T, seed=0)
+    rng = np.random.default_rng(1)
+    guesses = []
+    for i in range(n):
+        g = idx_np[i].reshape(-1).copy()
+        for j in range(g.size):
+            if rng.random() >= wl["guess"]:
+                g[j] = rng.integers(0, E)
+        guesses.append(g)
+    x_np = synth.activations_bf16(n * T, H, seed=0).reshape(n, T, H)
+    idx_d = torch.from_numpy(idx_np).cuda()
+    w_d = torch.from_numpy(w_np).cuda()
+    x_d = torch.from_numpy(x_np.view(np.int16)).cuda()
+    y_d = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def step(i):
+        tbl = moe.moe_expert_cache_fetch(c, idx_np[i], stream)
+        moe.moe_ffn_forward(h, x_d[i], idx_d[i], w_d[i], tbl, y_d, T, stream)
+        if wl["guess"] > 0:
+            moe.moe_expert_cache_prefetch(c, guesses[i + 1], stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            step(i)
+    stream.synchronize()
+    h0, m0, b0 = moe.moe_expert_cache_stats(c)
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(W, W + K):
+            step(i)
+        ev1.record(stream)
+    stream.synchronize()
+    clocks = sampler.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    h1, m1, b1 = moe.moe_expert_cache_stats(c)
+    status = moe.moe_ffn_status(h, stream)
+    assert status == moe.MOE_OK, moe.strerror(status)
+    ms_step = ms_total / K
+    copied = b1 - b0
+    h2d_gbs = copied / (ms_total / 1000.0) / 1e9
+
+    # host -> device copy peak on this machine: one 1 GiB page-locked copy
+    big_h = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    big_d = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        big_d.copy_(big_h, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(4):
+        big_d.copy_(big_h, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    h2d_peak = 4 * (1 << 30) / (e0.elapsed_time(e1) / 1000.0) / 1e9
+    del big_h, big_d
+
+    # end to end from host buffers (inputs in, y out) with the cache
+    xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
+    ih = torch.from_numpy(idx_np).pin_memory()
+    wh = torch.from_numpy(w_np).pin_memory()
+    yh = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    ne2e = min(K, 100)
+    t0 = time.perf_counter()
+    for i in range(ne2e):
+        tbl = moe.moe_expert_cache_fetch(c, idx_np[i], stream)
+        moe.moe_ffn_forward_host(h, xh[i], ih[i], wh[i], tbl, yh, T, stream)
+        if wl["guess"] > 0:
+            moe.moe_expert_cache_prefetch(c, guesses[i + 1], stream)
+    e2e_value = T * ne2e / (time.perf_counter() - t0)
+
+    cpu = None
+    if not args.no_cpu:
+        v, thr, sample = cpu_sample(wl)
+        cpu = {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle", "sample": sample}
+    line = {
+        "metric": METRIC, "value": T * K / (ms_total / 1000.0), "unit": "tokens/s", "n_gpus": 1, "steps": K,
+        "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16xe2m1->f32", "data": "synthetic",
+        "config": {"workload": args.workload, "layers": 1, "experts": E, "hidden": H, "inter": I, "topk": k,
+                   "tokens_per_step": T, "routing": "uniform, consecutive steps share no expert",
+                   "activations": "bf16", "path": "slot-major", "parallelism": "replicas1",
+                   "experts_resident": f"page-locked host memory ({E * expert_bytes(H, I) / 1e9:.1f} GB), "
+                                       f"{wl['slots']} cached in HBM",
+                   "l2": "inputs larger than L2: every step copies its experts in"},
+        "host_experts": {"slots": wl["slots"], "prefetch_guess_accuracy": wl["guess"], "hits": h1 - h0,
+                         "misses": m1 - m0, "copied_gb": copied / 1e9, "h2d_gbs": h2d_gbs,
+                         "h2d_peak_gbs": h2d_peak, "h2d_frac": h2d_gbs / h2d_peak},
+        "roofline": {"bound": "h2d", "kernel": "host-to-device expert copies (copy engines)",
+                     "achieved": h2d_gbs, "peak": h2d_peak,
+                     "peak_kind": "measured in this run: 1 GiB page-locked host-to-device copies",
+                     "unit": "GB/s", "frac": h2d_gbs / h2d_peak, "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2 + 2 * T * k * 4,
+                "d2h_bytes_per_step": T * H * 4},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+    moe.moe_expert_cache_destroy(c)
+    moe.moe_ffn_destroy(h)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -596,6 +744,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args, wl)
+    elif wl.get("host"):
+        run_host_experts(args, wl)
     else:
         run_ours(args, wl)
 

@@ -35,6 +35,8 @@ EXPORTS = [
     "moe_ffn_act_quant", "moe_stack_forward", "moe_ffn_profile_enable", "moe_ffn_profile_read",
     "moe_ffn_status", "moe_ffn_strerror", "moe_ffn_destroy", "moe_ffn_forward_noalloc",
     "moe_router_topk", "moe_router_select", "moe_batch_plan", "moe_batch_distinct",
+    "moe_expert_cache_create", "moe_expert_cache_fetch", "moe_expert_cache_prefetch", "moe_expert_cache_slot",
+    "moe_expert_cache_stats", "moe_expert_cache_destroy",
 ]
 
 MOE_PHASE_PREP = 0
@@ -97,6 +99,13 @@ def lib() -> ctypes.CDLL:
             "moe_router_select": (I, [P, P, I, P, P, P]),
             "moe_batch_plan": (I, [P, I, I, I, I, I, P]),
             "moe_batch_distinct": (I, [P, P, I, I, I, I, I, P]),
+            "moe_expert_cache_create": (I, [cfgp, I, P, I, ctypes.POINTER(P)]),
+            "moe_expert_cache_fetch": (I, [P, P, I, P, tblp]),
+            "moe_expert_cache_prefetch": (I, [P, P, I, P]),
+            "moe_expert_cache_slot": (I, [P, I]),
+            "moe_expert_cache_stats": (I, [P, ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong),
+                                           ctypes.POINTER(ctypes.c_longlong)]),
+            "moe_expert_cache_destroy": (None, [P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -269,3 +278,48 @@ def moe_batch_distinct(routing, order, E: int, B: int):
     _check(lib().moe_batch_distinct(routing.ctypes.data, order.ctypes.data, N, L, k, int(E), int(B),
                                     out.ctypes.data), "moe_batch_distinct")
     return out
+
+
+# ------------------------------------------------------ host-resident experts
+
+def moe_expert_cache_create(cfg, device: int, host_ptrs, slots: int):
+    """Cache of `slots` device slots over experts whose packed blobs sit at the
+    host addresses host_ptrs [E] (page-locked)."""
+    arr = (ctypes.c_void_p * len(host_ptrs))(*[int(p) for p in host_ptrs])
+    out = ctypes.c_void_p()
+    _check(lib().moe_expert_cache_create(ctypes.byref(cfg), int(device), arr, int(slots), ctypes.byref(out)),
+           "moe_expert_cache_create")
+    return out.value
+
+
+def moe_expert_cache_fetch(c, ids, stream=None):
+    """Makes the experts of ids (host int32) resident; returns the layer's table."""
+    import numpy as np
+
+    ids = np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)
+    tbl = moe_expert_table()
+    _check(lib().moe_expert_cache_fetch(c, ids.ctypes.data, ids.size, _s(stream), ctypes.byref(tbl)),
+           "moe_expert_cache_fetch")
+    return tbl
+
+
+def moe_expert_cache_prefetch(c, ids, stream=None):
+    import numpy as np
+
+    ids = np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)
+    _check(lib().moe_expert_cache_prefetch(c, ids.ctypes.data, ids.size, _s(stream)), "moe_expert_cache_prefetch")
+
+
+def moe_expert_cache_slot(c, expert: int) -> int:
+    return int(lib().moe_expert_cache_slot(c, int(expert)))
+
+
+def moe_expert_cache_stats(c):
+    h, m, b = ctypes.c_longlong(), ctypes.c_longlong(), ctypes.c_longlong()
+    _check(lib().moe_expert_cache_stats(c, ctypes.byref(h), ctypes.byref(m), ctypes.byref(b)),
+           "moe_expert_cache_stats")
+    return h.value, m.value, b.value
+
+
+def moe_expert_cache_destroy(c) -> None:
+    lib().moe_expert_cache_destroy(c)

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_ffn.so")
 SOURCES = ["api.cu", "gemv.cu", "group.cu", "pack.cu", "route.cu", "router.cu", "actquant.cu", "noalloc.cu",
-           "sched.cpp"]
+           "sched.cpp", "cache.cpp"]
 HEADERS = ["common.cuh", "internal.h", "layout.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]

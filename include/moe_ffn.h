@@ -209,6 +209,38 @@ int moe_batch_plan(const int32_t* sig, int N, int L, int topk, int E, int B, int
 int moe_batch_distinct(const int32_t* routing, const int32_t* order, int N, int L, int topk, int E, int B,
                        int32_t* distinct);
 
+/* Host-resident experts with an HBM cache and prefetch ([8GB] §提速之路：v1 到
+ * v4 and [A100] §但 CPU 也没那么快 stream experts that do not fit on the GPU
+ * and hide the copies; here host memory sits behind NVLink-C2C).  Host code.
+ *   create   cfg: the layer's sizes; host_blobs: host array [E] of HOST
+ *            pointers (16-byte aligned, page-locked for asynchronous copies)
+ *            to packed expert blobs (moe_ffn_pack_expert's layout); slots:
+ *            expert-sized slots of device memory.  OOM if they do not fit.
+ *   fetch    ids: host int32 [n] expert ids (-1 ignored).  Makes them
+ *            resident: a miss takes the least recently used slot that the
+ *            request does not use (lowest slot on ties) and is copied there
+ *            on one of two internal copy streams; `stream` then waits for the
+ *            copies and receives the layer's table in *tbl (a device array of
+ *            E pointers, NULL for experts not resident) for launches on
+ *            `stream` until the next fetch.  INVALID_ARG if the request holds
+ *            more distinct experts than there are slots.
+ *   prefetch the same copies for experts expected next, without waiting;
+ *            slots the previous fetch returned stay intact until the work
+ *            enqueued on `stream` before this call is done.
+ * All calls of one cache must use one stream.  A slot is never overwritten
+ * while work enqueued before the call that evicts it may read it. */
+typedef struct moe_expert_cache_s* moe_expert_cache_t;
+int moe_expert_cache_create(const moe_ffn_config* cfg, int device, const void* const* host_blobs, int slots,
+                            moe_expert_cache_t* out);
+int moe_expert_cache_fetch(moe_expert_cache_t c, const int32_t* ids, int n, void* stream, moe_expert_table* tbl);
+int moe_expert_cache_prefetch(moe_expert_cache_t c, const int32_t* ids, int n, void* stream);
+/* The slot holding expert e, or -1. */
+int moe_expert_cache_slot(moe_expert_cache_t c, int expert);
+/* Fetch hits and misses so far, and bytes copied by fetches and prefetches. */
+int moe_expert_cache_stats(moe_expert_cache_t c, long long* hits, long long* misses, long long* bytes);
+/* Waits for the copies in flight and frees the cache. */
+void moe_expert_cache_destroy(moe_expert_cache_t c);
+
 /* L-layer decode step on a residual stream ([A100] §然后又发现每 token 启动
  * 2000 次内核: RMSNorm and the MoE per layer, launched as a handful of
  * dispatches): for l = 0..L-1,
