@@ -44,6 +44,7 @@ struct moe_ffn {
     unsigned long long use_clock;
     Profiler* prof;             // non-null while moe_ffn_profile_enable(h, 1)
     float* rlogits;             // router logits scratch [max_tokens][E]
+    float* rpart;               // router split-K partials [max splits][max_tokens][E] (batches above 8)
 };
 
 namespace {
@@ -209,6 +210,8 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     size_t o_gobuf = take(gw.obuf), o_gpgu = take(gw.part_gu), o_gpdn = take(gw.part_dn);
     size_t o_ghraw = take(gw.hraw), o_ghpair = take(gw.hpair);
     size_t o_rlog = take((size_t)T * cfg->num_experts * 4);
+    const size_t rpart_bytes = T > 8 ? (size_t)router_max_splits(H) * T * cfg->num_experts * 4 : 0;
+    size_t o_rpart = take(rpart_bytes);
     size_t o_xst = take((size_t)T * H * 2), o_ist = take((size_t)T * k * 4);
     size_t o_wst = take((size_t)T * k * 4), o_yst = take((size_t)T * H * 4);
     h->ws_bytes = off;
@@ -277,6 +280,7 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
         ga.hpair = e4m3 ? (int*)(b + o_ghpair) : nullptr;
     }
     h->rlogits = (float*)(b + o_rlog);
+    h->rpart = rpart_bytes ? (float*)(b + o_rpart) : nullptr;
     h->x_stage = (uint16_t*)(b + o_xst);
     h->idx_stage = (int32_t*)(b + o_ist);
     h->w_stage = (float*)(b + o_wst);
@@ -385,9 +389,14 @@ int moe_router_topk(moe_ffn_t h, const void* x, const void* router_w, int T, flo
     DeviceGuard guard(h->device);
     RouterArgs a{(const uint16_t*)x, (const uint16_t*)router_w, logits ? logits : h->rlogits, topk_idx, topk_w,
                  T, h->cfg.hidden, h->cfg.num_experts, h->cfg.topk, 0};
+    a.status = h->status;
+    // batches above 8 tokens: the tensor cores, in split-K partials that the
+    // selection adds up; smaller ones stream the weights on the CUDA cores
+    a.part = h->rpart;
+    a.nsplit = h->rpart ? router_mma_splits(T, h->cfg.hidden, h->cfg.num_experts) : 0;
     cudaStream_t s = (cudaStream_t)stream;
     if (h->prof) h->prof->begin(kPhaseRouter, s);
-    cudaError_t e = launch_router_logits(a, s, !h->prof);
+    cudaError_t e = a.nsplit ? launch_router_mma(a, s, !h->prof) : launch_router_logits(a, s, !h->prof);
     if (e == cudaSuccess) e = launch_router_select(a, s, !h->prof);
     if (h->prof) h->prof->end(s);
     return cuda_rc(e);

@@ -195,11 +195,22 @@ struct RouterArgs {
     float* wout;            // [T][topk]
     int T, H, E, topk;
     int tpc;                // tokens per CTA of the logits kernel (set by the launcher)
+    // tensor-core batch path: split-K partial logits [nsplit][T][E], summed in
+    // split order by the selection (nsplit = 0: the logits are in `logits`)
+    float* part;
+    int nsplit;
+    int* status;
 };
 int router_max_experts();
 int router_tokens_per_cta(int H);     // 0: H too large for the logits kernel
+// Splits of the tensor-core batch path for T tokens (0: the path does not
+// apply: T <= 8, or H not a multiple of 128); its partials need
+// router_max_splits(H) * T * E floats.
+int router_mma_splits(int T, int H, int E);
+int router_max_splits(int H);
 cudaError_t router_init_device();
 cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t s, bool pdl);
+cudaError_t launch_router_mma(const RouterArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_router_select(const RouterArgs& a, cudaStream_t s, bool pdl);
 
 // E4M3 / ue8m0-per-128 activation quantizer (actquant.cu).

@@ -192,13 +192,34 @@ __global__ void __launch_bounds__(256) k_router_select(RouterArgs a)
     pdl_wait();
     pdl_trigger();
     if (t >= a.T) return;
-    const float* row = a.logits + (size_t)t * a.E;
     float v[R];
     uint32_t key[R];
+    if (a.nsplit == 0) {
+        const float* row = a.logits + (size_t)t * a.E;
 #pragma unroll
-    for (int j = 0; j < R; j++) {
-        const int e = lane + 32 * j;
-        v[j] = e < a.E ? row[e] : 0.0f;
+        for (int j = 0; j < R; j++) {
+            const int e = lane + 32 * j;
+            v[j] = e < a.E ? row[e] : 0.0f;
+        }
+    } else {
+        // the tensor-core path's split-K partials, added in split order; the
+        // sums are the logits
+#pragma unroll
+        for (int j = 0; j < R; j++) v[j] = 0.0f;
+        for (int sp = 0; sp < a.nsplit; sp++) {
+            const float* row = a.part + ((size_t)sp * a.T + t) * a.E;
+#pragma unroll
+            for (int j = 0; j < R; j++) {
+                const int e = lane + 32 * j;
+                if (e < a.E) v[j] += __ldcg(row + e);
+            }
+        }
+        float* out = a.logits + (size_t)t * a.E;
+#pragma unroll
+        for (int j = 0; j < R; j++) {
+            const int e = lane + 32 * j;
+            if (e < a.E) out[e] = v[j];
+        }
     }
 #pragma unroll
     for (int j = 0; j < R; j++) key[j] = lane + 32 * j < a.E ? order_key(v[j]) : 0u;
@@ -245,6 +266,112 @@ __global__ void __launch_bounds__(256) k_router_select(RouterArgs a)
     }
 }
 
+// ------------------------------------------------ tensor-core batch path
+
+constexpr uint64_t kRWaitLimitNs = 2000000000ull;
+
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulate,
+// both operands K-major.
+__host__ __device__ constexpr uint32_t f16_bf16_idesc(uint32_t M, uint32_t N)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 16 bytes global -> shared, asynchronously; valid = false fills zeros (the
+// source address is then not read).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+
+// grid (ceil(E / 128), ceil(T / N), H / kr), 256 threads: the logits of 128
+// experts x N tokens over one K slice of kr, as kr / 16 tcgen05 MMAs (M = 128,
+// N, K = 16, bf16 in, fp32 in tensor memory) by one thread.  Both operands
+// are staged K-major without swizzle (per MMA: 8-row groups of 256 bytes, two
+// 8 x 16-byte core matrices along K), rows past E or T as zeros; the
+// accumulator goes to part[split][t][e].
+template <int N>
+__global__ void __launch_bounds__(256) k_router_mma(RouterArgs a, int kr)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tbase;
+    constexpr uint32_t kCols = N < 32 ? 32 : N;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e0 = blockIdx.x * 128, t0 = blockIdx.y * N, sp = blockIdx.z, k0 = sp * kr;
+    const int nm = kr / 16, cpr = kr / 8;          // MMAs; 16-byte chunks per row
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + (size_t)nm * 4096;
+    if (warp == 0) tmem_alloc(&tbase, kCols);
+    if (threadIdx.x == 32) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+    }
+    // the router weights are no previous kernel's output: staged before the wait
+    for (int i = threadIdx.x; i < 128 * cpr; i += 256) {
+        const int r = i / cpr, q = i % cpr, e = e0 + r;
+        const bool ok = e < a.E;
+        cp_async16(sA + (q >> 1) * 4096 + (r >> 3) * 256 + (q & 1) * 128 + (r & 7) * 16,
+                   a.w + (size_t)(ok ? e : 0) * a.H + k0 + 8 * q, ok);
+    }
+    pdl_wait();
+    pdl_trigger();
+    for (int i = threadIdx.x; i < N * cpr; i += 256) {
+        const int r = i / cpr, q = i % cpr, t = t0 + r;
+        const bool ok = t < a.T;
+        cp_async16(sB + (q >> 1) * (N * 32) + (r >> 3) * 256 + (q & 1) * 128 + (r & 7) * 16,
+                   a.x + (size_t)(ok ? t : 0) * a.H + k0 + 8 * q, ok);
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    // the copies wrote through the generic proxy; the tensor core reads through the async one
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tbase;
+    if (threadIdx.x == 0) {
+        const uint32_t idesc = f16_bf16_idesc(128, N);
+        for (int m = 0; m < nm; m++)
+            tc_mma_f16(tmem, umma_desc(smem_u32(sA + m * 4096), 128, 256),
+                       umma_desc(smem_u32(sB + (size_t)m * N * 32), 128, 256), idesc, m > 0 ? 1u : 0u);
+        tc_commit(&bar);
+    }
+    bool done = mbar_wait_bounded(&bar, 0, kRWaitLimitNs);
+    if (!done) {
+        if (threadIdx.x == 0 && a.status) atomicOr(a.status, kStatusTimeout);
+        done = mbar_wait_bounded(&bar, 0, kRWaitLimitNs);     // the MMAs must be over before the free
+    }
+    tc_fence_after();
+    if (warp < 4 && done) {
+        const int e = e0 + warp * 32 + lane;
+#pragma unroll 1
+        for (int c0 = 0; c0 < N; c0 += 16) {
+            float v[16];
+            tc_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                const int t = t0 + c0 + j;
+                if (t < a.T && e < a.E) a.part[((size_t)sp * a.T + t) * a.E + e] = v[j];
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kCols);
+}
+
 cudaError_t rlaunch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, void** args)
 {
     cudaLaunchConfig_t cfg = {};
@@ -276,6 +403,32 @@ int router_tokens_per_cta(int H)
     return (size_t)H * 2 <= kRSmemMax ? 1 : 0;
 }
 
+namespace {
+
+int mma_tile_n(int T)
+{
+    int n = 16;
+    while (n < T && n < 256) n *= 2;
+    return n;
+}
+
+size_t mma_smem(int N, int kr) { return (size_t)(kr / 16) * (4096 + (size_t)N * 32); }
+
+}  // namespace
+
+int router_max_splits(int H) { return H % 128 == 0 ? H / 128 : 0; }
+
+int router_mma_splits(int T, int H, int E)
+{
+    if (T <= 8 || H % 128 != 0 || E <= 0) return 0;
+    const int N = mma_tile_n(T);
+    const long long tiles = (long long)((E + 127) / 128) * ((T + N - 1) / N);
+    // K slices of 256 where that still gives about 96 CTAs (fewer partials to
+    // add), else of 128
+    const int kr = (H % 256 == 0 && tiles * (H / 256) >= 96 && mma_smem(N, 256) <= kRSmemMax) ? 256 : 128;
+    return H / kr;
+}
+
 cudaError_t router_init_device()
 {
     const void* fns[] = {(const void*)k_router_logits<1, 4>, (const void*)k_router_logits<2, 4>,
@@ -295,7 +448,35 @@ cudaError_t router_init_device()
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
+    const void* mma[] = {(const void*)k_router_mma<16>, (const void*)k_router_mma<32>, (const void*)k_router_mma<64>,
+                         (const void*)k_router_mma<128>, (const void*)k_router_mma<256>};
+    for (const void* f : mma) {
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmemMax);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
+    }
     return e;
+}
+
+// The logits of T > 8 tokens on the tensor cores, as a.nsplit K slices of
+// partial sums in a.part (router_mma_splits(T, H, E) of them).
+cudaError_t launch_router_mma(const RouterArgs& a0, cudaStream_t s, bool pdl)
+{
+    RouterArgs a = a0;
+    if (a.T == 0) return cudaSuccess;
+    if (a.nsplit <= 0 || a.H % a.nsplit != 0 || !a.part) return cudaErrorInvalidValue;
+    const int N = mma_tile_n(a.T), kr = a.H / a.nsplit;
+    if (kr % 128 != 0 || mma_smem(N, kr) > kRSmemMax) return cudaErrorInvalidValue;
+    int krv = kr;
+    void* args[] = {&a, &krv};
+    const dim3 grid((a.E + 127) / 128, (a.T + N - 1) / N, a.nsplit);
+    const void* fn = N == 16    ? (const void*)k_router_mma<16>
+                     : N == 32  ? (const void*)k_router_mma<32>
+                     : N == 64  ? (const void*)k_router_mma<64>
+                     : N == 128 ? (const void*)k_router_mma<128>
+                                : (const void*)k_router_mma<256>;
+    return rlaunch(fn, grid, dim3(256), mma_smem(N, kr), s, pdl, args);
 }
 
 cudaError_t launch_router_logits(const RouterArgs& a0, cudaStream_t s, bool pdl)
