@@ -329,6 +329,26 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------- ranks
+
+def max_over_ranks(v, dist, device):
+    """The largest v over the ranks: a replicated job takes as long as its
+    slowest rank (dist: torch.distributed, or None for one rank)."""
+    if dist is None:
+        return float(v)
+    import torch
+
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world, tokens_per_step, steps, ms_total):
+    """Tokens per second of `world` independent replicas that each ran `steps`
+    steps of `tokens_per_step` tokens within ms_total (the slowest rank's time)."""
+    return world * tokens_per_step * steps / (ms_total / 1000.0)
+
+
 # --------------------------------------------------------------- GPU arm
 
 def run_ours(args, wl):
@@ -444,12 +464,9 @@ def run_ours(args, wl):
     clocks = sampler.stop()
     barrier()
     ms_total = ev0.elapsed_time(ev1)
-    if dist is not None:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dist, "cuda")
     ms_step = ms_total / K
-    value = world * T * K / (ms_total / 1000.0)
+    value = replica_throughput(world, T, K, ms_total)
 
     # algorithmic bytes: distinct experts per layer per step x bytes per expert + activations
     def distinct(i, l):
