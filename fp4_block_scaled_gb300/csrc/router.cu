@@ -206,13 +206,24 @@ __global__ void __launch_bounds__(256) k_router_select(RouterArgs a)
         // sums are the logits
 #pragma unroll
         for (int j = 0; j < R; j++) v[j] = 0.0f;
-        for (int sp = 0; sp < a.nsplit; sp++) {
-            const float* row = a.part + ((size_t)sp * a.T + t) * a.E;
+        // four splits' loads in flight at once, added in split order
+        constexpr int kQ = R <= 16 ? 4 : 2;
+        for (int sp0 = 0; sp0 < a.nsplit; sp0 += kQ) {
+            float q[kQ][R];
 #pragma unroll
-            for (int j = 0; j < R; j++) {
-                const int e = lane + 32 * j;
-                if (e < a.E) v[j] += __ldcg(row + e);
+            for (int u = 0; u < kQ; u++) {
+                const float* row = a.part + ((size_t)(sp0 + u) * a.T + t) * a.E;
+#pragma unroll
+                for (int j = 0; j < R; j++) {
+                    const int e = lane + 32 * j;
+                    q[u][j] = (sp0 + u < a.nsplit && e < a.E) ? __ldcg(row + e) : 0.0f;
+                }
             }
+#pragma unroll
+            for (int u = 0; u < kQ; u++)
+#pragma unroll
+                for (int j = 0; j < R; j++)
+                    if (sp0 + u < a.nsplit) v[j] += q[u][j];
         }
         float* out = a.logits + (size_t)t * a.E;
 #pragma unroll
@@ -319,17 +330,21 @@ __global__ void __launch_bounds__(256) k_router_mma(RouterArgs a, int kr)
         mbar_init(&bar, 1);
         mbar_fence_init();
     }
+    // A warp copies 8 rows x 4 chunks at a time (lane: row lane % 8, chunk
+    // lane / 8): each quarter-warp writes 8 rows of one core matrix, 8
+    // different bank groups, and each row's 4 chunks are 64 contiguous bytes.
+    const int q4 = cpr / 4;                        // power of two
     // the router weights are no previous kernel's output: staged before the wait
-    for (int i = threadIdx.x; i < 128 * cpr; i += 256) {
-        const int r = i / cpr, q = i % cpr, e = e0 + r;
+    for (int it = warp; it < 16 * q4; it += 8) {
+        const int r = (it / q4) * 8 + (lane & 7), q = (it % q4) * 4 + (lane >> 3), e = e0 + r;
         const bool ok = e < a.E;
         cp_async16(sA + (q >> 1) * 4096 + (r >> 3) * 256 + (q & 1) * 128 + (r & 7) * 16,
                    a.w + (size_t)(ok ? e : 0) * a.H + k0 + 8 * q, ok);
     }
     pdl_wait();
     pdl_trigger();
-    for (int i = threadIdx.x; i < N * cpr; i += 256) {
-        const int r = i / cpr, q = i % cpr, t = t0 + r;
+    for (int it = warp; it < (N / 8) * q4; it += 8) {
+        const int r = (it / q4) * 8 + (lane & 7), q = (it % q4) * 4 + (lane >> 3), t = t0 + r;
         const bool ok = t < a.T;
         cp_async16(sB + (q >> 1) * (N * 32) + (r >> 3) * 256 + (q & 1) * 128 + (r & 7) * 16,
                    a.x + (size_t)(ok ? t : 0) * a.H + k0 + 8 * q, ok);
