@@ -152,6 +152,10 @@ struct TcSmem {
     uint32_t tmem;
     int abort;
     int last;
+    // finished gate/up groups of this CTA: (count << 32) | h tiles written,
+    // added at CTA scope by the finalizing warps; the loader thread makes them
+    // grid-visible (it alone waits for the release at GPU scope)
+    unsigned long long fin_word;
 };
 
 // Host-computed description of one projection's unit stream.
@@ -454,7 +458,7 @@ __device__ bool produce(const GemvArgs& a, const StreamPlan& p, const Range& r, 
                               PHASE};
         } else {
             mbar_arrive(&sm.full[s]);      // an empty stage: nothing to multiply
-            sm.bsrc[s].B = nullptr;
+            sm.bsrc[s] = BSrc{nullptr, nullptr, 0, 0, PHASE};
         }
         mbar_arrive(&sm.posted[s]);        // release: bsrc is visible to the loader
         TC_TRACE(PHASE, 0, n);
@@ -472,9 +476,44 @@ __device__ bool produce(const GemvArgs& a, const StreamPlan& p, const Range& r, 
 // x's pieces wait for the previous kernel (PDL); h's for the grid-wide count
 // of finalized gate/up groups.  Once a stage is posted its copies are always
 // issued, even after a timeout, so that every transaction count completes.
-__device__ void load_b(const GemvArgs& a, int nchunks, uint32_t gu_groups, TcSmem& sm)
+__device__ __forceinline__ unsigned long long ld_acquire_cta_u64(const unsigned long long* p)
 {
-    bool pdl_done = false, h_done = false;
+    unsigned long long v;
+    asm volatile("ld.acquire.cta.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+// Makes this CTA's `owned` finished gate/up groups grid-visible, as they come:
+// each increment of the CTA-scope word is added to the grid-wide count with a
+// GPU-scope release (cumulative over the finalizing warps' stores, which it
+// acquired).  Bounded; false on timeout or abort.
+__device__ bool publish_own_groups(const GemvArgs& a, TcSmem& sm, uint32_t owned)
+{
+    uint32_t cnt = 0, pub = 0;
+    uint64_t t0 = 0;
+    while (cnt < owned) {
+        const unsigned long long w = ld_acquire_cta_u64(&sm.fin_word);
+        const uint32_t c = (uint32_t)(w >> 32), d = (uint32_t)w;
+        if (d > pub) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(a.sync), "r"(d - pub) : "memory");
+            pub = d;
+        }
+        if (c > cnt) {
+            cnt = c;
+            t0 = 0;
+            continue;
+        }
+        if (*(volatile int*)&sm.abort) return false;
+        if (t0 == 0) t0 = globaltimer_ns();
+        else if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+__device__ void load_b(const GemvArgs& a, int nchunks, uint32_t gu_groups, uint32_t owned, TcSmem& sm)
+{
+    bool pdl_done = false, h_done = false, published = false;
     for (int n = 0; n < nchunks; n++) {
         const int s = n % kStages;
         if (!mbar_wait_or_abort(&sm.posted[s], (n / kStages) & 1, &sm.abort, kWaitLimitNs)) {
@@ -482,6 +521,12 @@ __device__ void load_b(const GemvArgs& a, int nchunks, uint32_t gu_groups, TcSme
             return;
         }
         const BSrc q = sm.bsrc[s];
+        if (q.phase == 1 && !published) {
+            // every CTA's finished gate/up groups must reach the grid-wide count,
+            // also when its own down stages multiply nothing
+            if (!publish_own_groups(a, sm, owned)) set_abort(a, sm);
+            published = true;
+        }
         if (!q.B) continue;
         if (!pdl_done) {
             pdl_wait();
@@ -504,6 +549,7 @@ __device__ void load_b(const GemvArgs& a, int nchunks, uint32_t gu_groups, TcSme
         bulk_g2s(stg + kOffB, q.B, q.nb, &sm.full[s]);
         bulk_g2s(stg + kOffSfb, q.Bsf, q.nsf, &sm.full[s]);
     }
+    if (!published && !publish_own_groups(a, sm, owned)) set_abort(a, sm);
 }
 
 // ------------------------------------------------------------------ MMA issue
@@ -585,7 +631,15 @@ __device__ __forceinline__ float slot_weight(const GemvArgs& a, const TcSmem& sm
 
 // Gate/up group (slot j, tile) -> the 64 values h = w_j * silu(g) * u, as
 // pieces, by one warp; then one more finished group on the grid-wide count.
-__device__ __forceinline__ void finalize_gate_up(const GemvArgs& a, const StreamPlan& p, const TcSmem& sm,
+__device__ __forceinline__ void fin_signal(TcSmem& sm, int lane, uint32_t done)
+{
+    if (lane == 0)
+        asm volatile("red.release.cta.shared::cta.add.u64 [%0], %1;" ::"r"(smem_u32(&sm.fin_word)),
+                     "l"((1ull << 32) | (unsigned long long)done)
+                     : "memory");
+}
+
+__device__ __forceinline__ void finalize_gate_up(const GemvArgs& a, const StreamPlan& p, TcSmem& sm,
                                                  uint32_t group, const float* comb, int lane)
 {
     const int j = (int)(group / p.ntiles), tile = (int)(group % p.ntiles);
@@ -618,7 +672,10 @@ __device__ __forceinline__ void finalize_gate_up(const GemvArgs& a, const Stream
             int old = 0;
             if (lane == 0) old = atomicAdd(a.hpair + (size_t)j * nblk + blk, 1);
             old = __shfl_sync(0xFFFFFFFFu, old, 0);
-            if (old == 0) return;         // the other tile finishes the block
+            if (old == 0) {               // the other tile finishes the block
+                fin_signal(sm, lane, 0);
+                return;
+            }
             __threadfence();
             const float* other = a.hraw + (size_t)j * a.I + (size_t)(tile ^ 1) * 64 + 2 * lane;
             o0 = __ldcg(other);
@@ -645,9 +702,10 @@ __device__ __forceinline__ void finalize_gate_up(const GemvArgs& a, const Stream
     asm volatile("fence.proxy.async.global;" ::: "memory");
     TC_FIN(2, group % 64);
     __syncwarp();
-    // release: the pieces (this warp's stores, ordered by the warp barrier) are
-    // visible before the count; the thread does not wait for the add
-    if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(a.sync), "r"(done) : "memory");
+    // the pieces (this warp's stores, ordered by the warp barrier) go to the
+    // loader thread with a CTA-scope release; its GPU-scope release of the
+    // count covers them, and this warp goes back to the epilogue at once
+    fin_signal(sm, lane, (uint32_t)done);
     TC_FIN(3, group % 64);
     if (lane == 0) TC_CTA(9);
     if (lane == 0) TC_GRP(4, group);
@@ -822,6 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(GemvArgs a, StreamPlan p0
         }
         for (int i = 0; i < kIssuers; i++) mbar_init(&sm.drain[i], 1);
         sm.abort = 0;
+        sm.fin_word = 0;
         mbar_fence_init();
     }
     if (warp == 0) {
@@ -878,7 +937,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(GemvArgs a, StreamPlan p0
         return;
     }
     if (warp == kWarpLoader) {
-        if (lane == 0) load_b(a, count_chunks(p0, r0) + count_chunks(p1, r1), gu_groups, sm);
+        // gate/up groups whose first unit is in this CTA's range: it finalizes them
+        const uint32_t owned = (r0.u1 + p0.kgt - 1) / (uint32_t)p0.kgt - (r0.u0 + p0.kgt - 1) / (uint32_t)p0.kgt;
+        if (lane == 0) load_b(a, count_chunks(p0, r0) + count_chunks(p1, r1), gu_groups, owned, sm);
         return;
     }
     if (warp < kWarpEpi0) {
