@@ -182,6 +182,17 @@ def draw_routings(R, E, k, T, seed, dist="uniform", layer=0):
     return idx, w
 
 
+def source_fingerprint(path):
+    """sha256 of a C/CUDA source without its comments and whitespace: the code
+    the counters were taken on (a comment edit does not invalidate them)."""
+    import re
+
+    text = open(path, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return hashlib.sha256(re.sub(r"\s+", "", text).encode()).hexdigest()
+
+
 def traffic_record(kernel, workload, algorithmic_bytes):
     """dram bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source and on this workload's launch shape (else None):
@@ -198,8 +209,7 @@ def traffic_record(kernel, workload, algorithmic_bytes):
     src = os.path.join(ROOT, rec["source"])
     if not os.path.exists(src):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    if sha != rec["source_sha256"]:
+    if source_fingerprint(src) != rec.get("source_fingerprint"):
         return None
     if "dram_bytes_per_algorithmic_byte" in rec:
         return rec["dram_bytes_per_algorithmic_byte"] * algorithmic_bytes

@@ -24,7 +24,10 @@
 //   last warp            copies the matching activation pieces into each
 //                        stage: x's once the previous kernel is done (PDL),
 //                        h's once every gate/up group of the grid has been
-//                        finalized (a grid-wide counter, bounded wait);
+//                        finalized (a grid-wide counter, bounded wait); before
+//                        that wait it makes its own CTA's finished groups
+//                        grid-visible (the finalizing warps hand them over at
+//                        CTA scope and go on);
 //   warps 1..kCU         one MMA-issuing thread each (one thread issues a
 //                        tcgen05 instruction per ~150 cycles; several overlap):
 //                        issuer i moves the scale atoms of unit i of every
@@ -630,7 +633,8 @@ __device__ __forceinline__ float slot_weight(const GemvArgs& a, const TcSmem& sm
 }
 
 // Gate/up group (slot j, tile) -> the 64 values h = w_j * silu(g) * u, as
-// pieces, by one warp; then one more finished group on the grid-wide count.
+// pieces, by one warp; then the group goes to the loader thread, which adds it
+// to the grid-wide count.
 __device__ __forceinline__ void fin_signal(TcSmem& sm, int lane, uint32_t done)
 {
     if (lane == 0)
