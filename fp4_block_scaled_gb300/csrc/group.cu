@@ -292,7 +292,19 @@ __global__ void __launch_bounds__(256) k_gprep(GroupArgs a)
         // RMSNorm with unit weight: sum of squares in a fixed tree order
         const float* xr = a.x_resid + (size_t)t * H;
         float ss = 0.0f;
-        for (int i = threadIdx.x; i < H; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+        // eight loads in flight per thread, then added in the same order as
+        // one element at a time (i = tid, tid + blockDim, ...)
+        for (int i0 = threadIdx.x; i0 < H; i0 += 8 * (int)blockDim.x) {
+            float v[8];
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                const int i = i0 + q * (int)blockDim.x;
+                v[q] = i < H ? __ldcg(xr + i) : 0.0f;
+            }
+#pragma unroll
+            for (int q = 0; q < 8; q++)
+                if (i0 + q * (int)blockDim.x < H) ss = fmaf(v[q], v[q], ss);
+        }
         ss = warp_sum(ss);
         if (lane == 0) s_red[warp] = ss;
         __syncthreads();
