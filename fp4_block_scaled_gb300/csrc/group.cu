@@ -248,15 +248,15 @@ struct GDst {
 };
 
 template <int NP>
-__device__ __forceinline__ GDst group_dst(const GroupArgs& a, int e, int P, int u, int kgt, size_t abytes,
+__device__ __forceinline__ GDst group_dst(int off, int gbase, int count, int P, int u, int kgt, size_t abytes,
                                           uint8_t* codes, uint8_t* atoms)
 {
     constexpr int S = kGroupN / NP < kGroupTokens ? kGroupN / NP : kGroupTokens;
-    const int rel = P - a.offsets[e];
+    const int rel = P - off;              // off, gbase, count: the expert's offsets / gbase / counts
     const int q = rel / S;
-    const int g = a.gbase[e] + q;
-    const int p0 = a.offsets[e] + q * S;
-    const int nt = min(S, a.counts[e] - q * S);
+    const int g = gbase + q;
+    const int p0 = off + q * S;
+    const int nt = min(S, count - q * S);
     GDst d;
     d.i = rel - q * S;
     d.mstride = (int)g_unit_b(NP, nt) / 2;
@@ -277,15 +277,22 @@ __global__ void __launch_bounds__(256) k_gprep(GroupArgs a)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ float s_red[8];
     __shared__ float s_den;
-    __shared__ int s_e[16], s_P[16];
+    __shared__ int s_e[16], s_P[16], s_off[16], s_gb[16], s_cnt[16];
 
     pdl_wait();
     pdl_trigger();
     if (threadIdx.x < a.topk) {
+        // the token's slots: their sorted positions and experts, then each
+        // expert's group table entries (two round trips, not one per slot later)
         const int j = t * a.topk + threadIdx.x;
         const int P = a.inv[j];
-        s_P[threadIdx.x] = P;
-        s_e[threadIdx.x] = P >= 0 ? a.idx[j] : -1;
+        const int e = a.idx[j];
+        const bool ok = P >= 0 && e >= 0 && e < a.E;
+        s_P[threadIdx.x] = ok ? P : -1;
+        s_e[threadIdx.x] = ok ? e : -1;
+        s_off[threadIdx.x] = ok ? a.offsets[e] : 0;
+        s_gb[threadIdx.x] = ok ? a.gbase[e] : 0;
+        s_cnt[threadIdx.x] = ok ? a.counts[e] : 0;
     }
     float den = 1.0f;
     if (a.x_resid) {
@@ -339,7 +346,7 @@ __global__ void __launch_bounds__(256) k_gprep(GroupArgs a)
             make_pieces64<8>(e4m3_quant_dequant(v[2 * hh], s), e4m3_quant_dequant(v[2 * hh + 1], s), pc);
             for (int kk = 0; kk < a.topk; kk++) {
                 if (s_P[kk] < 0) continue;
-                const GDst d = group_dst<8>(a, s_e[kk], s_P[kk], b, kgt, abytes, a.xg, a.xgsf);
+                const GDst d = group_dst<8>(s_off[kk], s_gb[kk], s_cnt[kk], s_P[kk], b, kgt, abytes, a.xg, a.xgsf);
                 store_pieces64<8>(pc, lane, d.unit, d.mstride, d.atom, d.i, 2 * hh);
             }
         }
@@ -355,7 +362,7 @@ __global__ void __launch_bounds__(256) k_gprep(GroupArgs a)
         make_pieces64<1>(xval(b * 64 + 2 * lane), xval(b * 64 + 2 * lane + 1), pc);
         for (int kk = 0; kk < a.topk; kk++) {
             if (s_P[kk] < 0) continue;
-            const GDst d = group_dst<1>(a, s_e[kk], s_P[kk], b / 2, kgt, abytes, a.xg, a.xgsf);
+            const GDst d = group_dst<1>(s_off[kk], s_gb[kk], s_cnt[kk], s_P[kk], b / 2, kgt, abytes, a.xg, a.xgsf);
             store_pieces64<1>(pc, lane, d.unit, d.mstride, d.atom, d.i, 2 * (b & 1));
         }
         return;
@@ -365,7 +372,7 @@ __global__ void __launch_bounds__(256) k_gprep(GroupArgs a)
     make_pieces64<16>(xval(b * 64 + 2 * lane), xval(b * 64 + 2 * lane + 1), pc);
     for (int kk = 0; kk < a.topk; kk++) {
         if (s_P[kk] < 0) continue;
-        const GDst d = group_dst<16>(a, s_e[kk], s_P[kk], b / 2, kgt, abytes, a.xg, a.xgsf);
+        const GDst d = group_dst<16>(s_off[kk], s_gb[kk], s_cnt[kk], s_P[kk], b / 2, kgt, abytes, a.xg, a.xgsf);
         store_pieces64<16>(pc, lane, d.unit, d.mstride, d.atom, d.i, 2 * (b & 1));
     }
 }
@@ -1128,26 +1135,34 @@ __global__ void __launch_bounds__(256) k_gcombine(GroupArgs a)
     }
     __syncthreads();
     for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
-        float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        for (int kk = 0; kk < a.topk; kk++) {
-            const int P = s_P[kk];
-            if (P < 0) continue;
-            const float4 o = __ldcg(reinterpret_cast<const float4*>(a.obuf + (size_t)P * H + c));
-            const float w = s_w[kk];
-            s.x = fmaf(w, o.x, s.x);
-            s.y = fmaf(w, o.y, s.y);
-            s.z = fmaf(w, o.z, s.z);
-            s.w = fmaf(w, o.w, s.w);
-        }
+        // every slot's output (and the residual) loaded first (topk <= 16),
+        // then added in k order
         const size_t o = (size_t)t * H + c;
+        float4 ov[16];
+#pragma unroll
+        for (int kk = 0; kk < 16; kk++) {
+            const int P = kk < a.topk ? s_P[kk] : -1;
+            ov[kk] = P >= 0 ? __ldcg(reinterpret_cast<const float4*>(a.obuf + (size_t)P * H + c))
+                            : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+        float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (a.x_resid) x = *reinterpret_cast<const float4*>(a.x_resid + o);
+        float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int kk = 0; kk < 16; kk++) {
+            if (kk >= a.topk || s_P[kk] < 0) continue;
+            const float w = s_w[kk];
+            s.x = fmaf(w, ov[kk].x, s.x);
+            s.y = fmaf(w, ov[kk].y, s.y);
+            s.z = fmaf(w, ov[kk].z, s.z);
+            s.w = fmaf(w, ov[kk].w, s.w);
+        }
         if (a.x_resid) {
-            float4* xr = reinterpret_cast<float4*>(a.x_resid + o);
-            float4 x = *xr;
             x.x += s.x;
             x.y += s.y;
             x.z += s.z;
             x.w += s.w;
-            *xr = x;
+            *reinterpret_cast<float4*>(a.x_resid + o) = x;
         } else if (a.out_f32) {
             *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.y) + o) = s;
         } else {

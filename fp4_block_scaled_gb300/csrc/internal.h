@@ -131,6 +131,7 @@ struct RouteArgs {
     int32_t* gbase;         // [E+1] first group of each expert; gbase[E] = groups
     GroupInfo* groups;      // [max groups]
     int group_size;         // slots per group, at most
+    int split;              // set by the launcher: parallel placement (32 x E counters fit)
 };
 // Upper bound on the groups of n slots over E experts (groups of >= gs slots).
 inline int max_groups(int n, int E, int gs)

@@ -20,6 +20,7 @@ namespace moe {
 namespace {
 
 constexpr int kRouteThreads = 1024;
+constexpr size_t kRouteSplitSmem = 200 * 1024;
 
 // Exclusive prefix sum of v over the CTA (thread order); *total = the sum.
 // s_warp: one int per warp.  Every thread must call it.
@@ -61,6 +62,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteArgs a)
     for (int e = tid; e < E; e += blockDim.x) s_cur[e] = 0;
     if (tid == 0) s_bad = 0;
     __syncthreads();
+#pragma unroll 4
     for (int j = tid; j < n; j += blockDim.x) {
         const int e = a.idx[j];
         if (e >= 0 && e < E) atomicAdd(&s_cur[e], 1);
@@ -110,27 +112,70 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteArgs a)
     }
     __syncthreads();
 
-    // stable placement, one warp, slots in order
-    if (warp == 0) {
-        for (int base = 0; base < n; base += 32) {
+    // stable placement: pos(j) = offsets[e_j] + (slots before j with expert
+    // e_j).  With room for 32 x E counters in shared memory, warp w takes the
+    // w-th contiguous segment of the slots: it counts its segment per expert,
+    // an exclusive scan over the warps per expert gives its start cursors,
+    // then it places its segment in order (32 slots at a time, ranks within a
+    // chunk by match).  Otherwise one warp walks all slots.
+    const int nw = blockDim.x >> 5;
+    const bool split = a.split != 0;
+    int* s_seg = s_cur + E;                                      // [32][E] when split
+    const int seg = split ? (n + nw - 1) / nw : n;
+    const int w_lo = split ? min(n, warp * seg) : 0, w_hi = split ? min(n, w_lo + seg) : n;
+    int* cur = split ? s_seg + (size_t)warp * E : s_cur;     // this warp's cursors
+    if (split) {
+        for (int i = tid; i < nw * E; i += blockDim.x) s_seg[i] = 0;
+        __syncthreads();
+        for (int j = w_lo + lane; j < w_hi; j += 32) {
+            const int e = a.idx[j];
+            if (e >= 0 && e < E) atomicAdd(&cur[e], 1);
+        }
+        __syncthreads();
+        for (int e = tid; e < E; e += blockDim.x) {
+            int c = s_cur[e];                                   // the expert's offset
+            for (int w = 0; w < nw; w++) {
+                int* pw = s_seg + (size_t)w * E + e;
+                const int cnt = *pw;
+                *pw = c;
+                c += cnt;
+            }
+        }
+        __syncthreads();
+    }
+    if (split || warp == 0) {
+        constexpr int kBatch = 8;                               // ids of 8 chunks per round trip
+        int ev[kBatch];
+        for (int base = w_lo; base < w_hi; base += 32) {
+            const int q = ((base - w_lo) >> 5) % kBatch;
+            if (q == 0) {
+#pragma unroll
+                for (int b = 0; b < kBatch; b++) {
+                    const int jj = base + 32 * b + lane;
+                    ev[b] = jj < w_hi ? a.idx[jj] : -1;
+                }
+            }
             const int j = base + lane;
-            const int e = j < n ? a.idx[j] : -1;
-            const bool valid = j < n && e >= 0 && e < E;
+            int e = -1;
+#pragma unroll
+            for (int b = 0; b < kBatch; b++)
+                if (b == q) e = ev[b];
+            const bool valid = j < w_hi && e >= 0 && e < E;
             const int key = valid ? e : E + lane;          // invalid lanes match nobody
             const unsigned mask = __match_any_sync(0xFFFFFFFFu, key);
             const int leader = __ffs(mask) - 1;
             const int rank = __popc(mask & ((1u << lane) - 1u));
             int start = 0;
             if (valid && lane == leader) {
-                start = s_cur[e];
-                s_cur[e] = start + __popc(mask);
+                start = cur[e];
+                cur[e] = start + __popc(mask);
             }
             start = __shfl_sync(0xFFFFFFFFu, start, leader);
             if (valid) {
                 const int pos = start + rank;
                 a.perm[pos] = j;
                 a.inv[j] = pos;
-            } else if (j < n) {
+            } else if (j < w_hi) {
                 a.inv[j] = -1;
             }
             __syncwarp();
@@ -146,8 +191,9 @@ int route_max_experts() { return 32768; }
 
 cudaError_t route_init_device()
 {
+    const size_t need = (size_t)route_max_experts() * sizeof(int);
     return cudaFuncSetAttribute((const void*)k_route, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                route_max_experts() * (int)sizeof(int));
+                                (int)(need > kRouteSplitSmem ? need : kRouteSplitSmem));
 }
 
 cudaError_t launch_route(const RouteArgs& a0, cudaStream_t s, bool pdl)
@@ -156,7 +202,10 @@ cudaError_t launch_route(const RouteArgs& a0, cudaStream_t s, bool pdl)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1);
     cfg.blockDim = dim3(kRouteThreads);
-    cfg.dynamicSmemBytes = (size_t)a.E * sizeof(int);
+    // E cursors, and 32 x E per-warp counters for the parallel placement when
+    // they fit
+    a.split = (size_t)33 * a.E * sizeof(int) <= kRouteSplitSmem ? 1 : 0;
+    cfg.dynamicSmemBytes = (size_t)(a.split ? 33 : 1) * a.E * sizeof(int);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
