@@ -150,6 +150,7 @@ struct TcSmem {
     uint64_t drain[kIssuers];    // the issuers' last MMAs are done
     BSrc bsrc[kStages];
     float comb[4][kTileRows];    // gate/up sums of the last four owned groups
+    uint4 tr[4][32];             // per epilogue warp: the pieces' byte transpose
     float slot_w[kSlotCache];    // w of each slot, 0 where its expert index is invalid
     JobInfo jobs[2][kJobWindow]; // first jobs of the gate/up and down streams
     uint32_t tmem;
@@ -184,17 +185,20 @@ struct StreamPlan {
 // so the 16 pieces carry every element to within 2^(e_0 - 30) while only the
 // first scale needs a reduction across lanes.
 // Bunit: the unit's B codes, Bsf: its scale atom.
+// The half-warp's 16 x 16 bytes (lane: its byte of each piece) are transposed
+// through `scratch` (32 x 16 bytes, this warp's) so that each lane stores one
+// 16-byte row -- piece i of its block -- and one scale byte.
 __device__ __forceinline__ void write_pieces64(float v0, float v1, int lane, uint8_t* Bunit, uint8_t* Bsf,
-                                               int blk0)
+                                               int blk0, uint4* scratch)
 {
     const int bu = (blk0 & 3) + (lane >> 4);       // block within the unit
     const int i = lane & 15;                       // byte within the block's row
-    uint8_t* rows = Bunit + (bu >> 1) * kMmaBBytes + (bu & 1) * 128 + i;
     float amax = fmaxf(fabsf(v0), fabsf(v1));
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
     const int s0 = e2m1_scale_byte(amax);
     float r0 = v0, r1 = v1;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};              // byte p: this lane's pair of piece p
 #pragma unroll
     for (int p = 0; p < kPieces; p++) {
         const int s = max(s0 - 2 * p, 1);
@@ -203,9 +207,20 @@ __device__ __forceinline__ void write_pieces64(float v0, float v1, int lane, uin
         const float2 d = e2m1x2_to_f32x2(byte);
         r0 = fmaf(-d.x, up, r0);
         r1 = fmaf(-d.y, up, r1);
-        rows[(p >> 3) * 256 + (p & 7) * 16] = (uint8_t)byte;
-        if (i == 0) Bsf[p * 16 + bu] = (uint8_t)s;
+        w[p >> 2] |= (byte & 0xFFu) << (8 * (p & 3));
     }
+    scratch[lane] = make_uint4(w[0], w[1], w[2], w[3]);
+    __syncwarp();
+    const uint8_t* sb = reinterpret_cast<const uint8_t*>(scratch + (lane & 16));   // this half-warp's lanes
+    uint32_t row[4];
+#pragma unroll
+    for (int q = 0; q < 4; q++)
+        row[q] = (uint32_t)sb[(4 * q) * 16 + i] | ((uint32_t)sb[(4 * q + 1) * 16 + i] << 8) |
+                 ((uint32_t)sb[(4 * q + 2) * 16 + i] << 16) | ((uint32_t)sb[(4 * q + 3) * 16 + i] << 24);
+    __syncwarp();                                  // scratch free again
+    uint8_t* dst = Bunit + (bu >> 1) * kMmaBBytes + (bu & 1) * 128 + (i >> 3) * 256 + (i & 7) * 16;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(row[0], row[1], row[2], row[3]);
+    Bsf[i * 16 + bu] = (uint8_t)max(s0 - 2 * i, 1);
 }
 
 // ------------------------------------------------------------------ k_prep
@@ -218,6 +233,7 @@ __global__ void __launch_bounds__(256) k_prep(GemvArgs a)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ float s_red[8];
     __shared__ float s_den;
+    __shared__ uint4 s_tr[8][32];          // per warp: the pieces' byte transpose
 
     // k_layer reads nothing this kernel or the previous layer writes before its
     // own wait, so it may start (on the SMs the previous layer frees) right away
@@ -270,7 +286,7 @@ __global__ void __launch_bounds__(256) k_prep(GemvArgs a)
             uint8_t* Bunit = a.xq + (size_t)t * act_bytes(H) + (size_t)b * kUnitBBytes;
             uint8_t* Bsf = a.xsf + (size_t)t * act_sf_bytes(H) + (size_t)b * kUnitSfBytes;
             write_pieces64(e4m3_quant_dequant(v[2 * hh], s), e4m3_quant_dequant(v[2 * hh + 1], s), lane, Bunit,
-                           Bsf, 2 * hh);
+                           Bsf, 2 * hh, s_tr[warp]);
         }
         return;
     }
@@ -294,7 +310,7 @@ __global__ void __launch_bounds__(256) k_prep(GemvArgs a)
     }
     uint8_t* Bunit = a.xq + (size_t)t * act_bytes(H) + (size_t)(b / 2) * kUnitBBytes;
     uint8_t* Bsf = a.xsf + (size_t)t * act_sf_bytes(H) + (size_t)(b / 2) * kUnitSfBytes;
-    write_pieces64(v0, v1, lane, Bunit, Bsf, 2 * b);
+    write_pieces64(v0, v1, lane, Bunit, Bsf, 2 * b, s_tr[warp]);
 }
 
 // ----------------------------------------------------------------- k_layer
@@ -656,7 +672,7 @@ __device__ __forceinline__ void fin_signal(TcSmem& sm, int lane, uint32_t done)
 }
 
 __device__ __forceinline__ void finalize_gate_up(const GemvArgs& a, const StreamPlan& p, TcSmem& sm,
-                                                 uint32_t group, const float* comb, int lane)
+                                                 uint32_t group, const float* comb, int lane, int tr_warp)
 {
     const int j = (int)(group / p.ntiles), tile = (int)(group % p.ntiles);
     TC_FIN(0, group % 64);
@@ -707,12 +723,13 @@ __device__ __forceinline__ void finalize_gate_up(const GemvArgs& a, const Stream
             const int ot = tile ^ 1;
             uint8_t* Bunit = a.hq + (size_t)j * act_bytes(a.I) + (size_t)(ot / 2) * kUnitBBytes;
             uint8_t* Bsf = a.hsf + (size_t)j * act_sf_bytes(a.I) + (size_t)(ot / 2) * kUnitSfBytes;
-            write_pieces64(e4m3_quant_dequant(o0, s) * w, e4m3_quant_dequant(o1, s) * w, lane, Bunit, Bsf, 2 * ot);
+            write_pieces64(e4m3_quant_dequant(o0, s) * w, e4m3_quant_dequant(o1, s) * w, lane, Bunit, Bsf, 2 * ot,
+                           sm.tr[tr_warp]);
         }
     }
     uint8_t* Bunit = a.hq + (size_t)j * act_bytes(a.I) + (size_t)(tile / 2) * kUnitBBytes;
     uint8_t* Bsf = a.hsf + (size_t)j * act_sf_bytes(a.I) + (size_t)(tile / 2) * kUnitSfBytes;
-    write_pieces64(h0 * w, h1 * w, lane, Bunit, Bsf, 2 * tile);
+    write_pieces64(h0 * w, h1 * w, lane, Bunit, Bsf, 2 * tile, sm.tr[tr_warp]);
     TC_FIN(1, group % 64);
     // the down projection reads these with bulk copies (async proxy), in other CTAs
     asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -853,7 +870,7 @@ __device__ void epilogue(const GemvArgs& a, const StreamPlan& p, const Range& r,
             if (quad == es.cb) {
                 named_sync(3 + es.cb, 128);
                 if (lane == 0) TC_GRP(2, group);
-                finalize_gate_up(a, p, sm, group, comb, lane);
+                finalize_gate_up(a, p, sm, group, comb, lane, quad);
             } else {
                 named_arrive(3 + es.cb, 128);
             }
