@@ -142,6 +142,7 @@ struct GSmem {
     GBSrc bsrc[kGStagesA];
     float comb[2][kNT][kTileRows];
     float hstash[kNT][64];       // raw h of the first tile of a pair, per slot
+    uint4 tr[4][32];             // per epilogue warp: the pieces' byte transpose
     uint32_t tmem;
     int abort;
 };
@@ -239,6 +240,59 @@ __device__ __forceinline__ void store_pieces64(const Pieces64<P>& pc, int lane, 
     }
 }
 
+// A lane's share of its half-warp's pieces after a transpose through shared
+// memory (P = 8 or 16): with 16 pieces row ib (16 bytes: piece ib of the
+// half-warp's 16 lanes), with 8 half `ib % 2` of row ib / 2 (8 bytes).
+template <int P>
+struct PieceRow {
+    uint32_t w[P / 4];
+    int s0;                 // the first piece's scale byte
+};
+
+template <int P>
+__device__ __forceinline__ PieceRow<P> transpose_pieces(const Pieces64<P>& pc, int lane, uint4* scratch)
+{
+    static_assert(P == 8 || P == 16, "row transpose for 8 or 16 pieces");
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int p = 0; p < P; p++) w[p >> 2] |= (uint32_t)pc.byte[p] << (8 * (p & 3));
+    scratch[lane] = make_uint4(w[0], w[1], w[2], w[3]);
+    __syncwarp();
+    const uint8_t* sb = reinterpret_cast<const uint8_t*>(scratch + (lane & 16));
+    const int ib = lane & 15;
+    const int p = P == 16 ? ib : ib >> 1, k0 = P == 16 ? 0 : 8 * (ib & 1);
+    PieceRow<P> r;
+#pragma unroll
+    for (int q = 0; q < P / 4; q++)
+        r.w[q] = (uint32_t)sb[(k0 + 4 * q) * 16 + p] | ((uint32_t)sb[(k0 + 4 * q + 1) * 16 + p] << 8) |
+                 ((uint32_t)sb[(k0 + 4 * q + 2) * 16 + p] << 16) | ((uint32_t)sb[(k0 + 4 * q + 3) * 16 + p] << 24);
+    r.s0 = pc.sc[0];
+    __syncwarp();
+    return r;
+}
+
+// The transposed pieces of slot i of a group (as store_pieces64): one 16- or
+// 8-byte store and at most one scale byte per lane.
+template <int P>
+__device__ __forceinline__ void store_piece_rows(const PieceRow<P>& r, int lane, uint8_t* unit, int mstride,
+                                                 uint8_t* atom, int i, int blk0)
+{
+    const int bu = blk0 + (lane >> 4);
+    const int ib = lane & 15;
+    uint8_t* rows = unit + (bu >> 1) * mstride + (bu & 1) * 128;
+    if (P == 16) {
+        const int n = 16 * i + ib;
+        *reinterpret_cast<uint4*>(rows + (n >> 3) * 256 + (n & 7) * 16) = make_uint4(r.w[0], r.w[1], r.w[2], r.w[3]);
+    } else {
+        const int n = 8 * i + (ib >> 1);
+        *reinterpret_cast<uint2*>(rows + (n >> 3) * 256 + (n & 7) * 16 + 8 * (ib & 1)) = make_uint2(r.w[0], r.w[1]);
+    }
+    if (ib < P) {
+        const int n = P * i + ib;
+        atom[(n & 31) * 16 + (n >> 5) * 4 + bu] = (uint8_t)max(r.s0 - 2 * ib, 1);
+    }
+}
+
 // Where slot position P's pieces of unit u (of a K with kgt units) go, with
 // groups of up to S = min(kGroupN / NP, kGroupTokens) slots of NP pieces.
 struct GDst {
@@ -278,6 +332,7 @@ __global__ void __launch_bounds__(256) k_gprep(GroupArgs a)
     __shared__ float s_red[8];
     __shared__ float s_den;
     __shared__ int s_e[16], s_P[16], s_off[16], s_gb[16], s_cnt[16];
+    __shared__ uint4 s_tr[8][32];          // per warp: the pieces' byte transpose
 
     pdl_wait();
     pdl_trigger();
@@ -344,10 +399,11 @@ __global__ void __launch_bounds__(256) k_gprep(GroupArgs a)
         for (int hh = 0; hh < 2; hh++) {
             Pieces64<8> pc;
             make_pieces64<8>(e4m3_quant_dequant(v[2 * hh], s), e4m3_quant_dequant(v[2 * hh + 1], s), pc);
+            const PieceRow<8> pr = transpose_pieces<8>(pc, lane, s_tr[warp]);
             for (int kk = 0; kk < a.topk; kk++) {
                 if (s_P[kk] < 0) continue;
                 const GDst d = group_dst<8>(s_off[kk], s_gb[kk], s_cnt[kk], s_P[kk], b, kgt, abytes, a.xg, a.xgsf);
-                store_pieces64<8>(pc, lane, d.unit, d.mstride, d.atom, d.i, 2 * hh);
+                store_piece_rows<8>(pr, lane, d.unit, d.mstride, d.atom, d.i, 2 * hh);
             }
         }
         return;
@@ -370,10 +426,11 @@ __global__ void __launch_bounds__(256) k_gprep(GroupArgs a)
     const size_t abytes = g_act_bytes(H, 16);
     Pieces64<16> pc;
     make_pieces64<16>(xval(b * 64 + 2 * lane), xval(b * 64 + 2 * lane + 1), pc);
+    const PieceRow<16> pr = transpose_pieces<16>(pc, lane, s_tr[warp]);
     for (int kk = 0; kk < a.topk; kk++) {
         if (s_P[kk] < 0) continue;
         const GDst d = group_dst<16>(s_off[kk], s_gb[kk], s_cnt[kk], s_P[kk], b / 2, kgt, abytes, a.xg, a.xgsf);
-        store_pieces64<16>(pc, lane, d.unit, d.mstride, d.atom, d.i, 2 * (b & 1));
+        store_piece_rows<16>(pr, lane, d.unit, d.mstride, d.atom, d.i, 2 * (b & 1));
     }
 }
 
@@ -769,9 +826,23 @@ __device__ void gissue(const GroupArgs& a, const GPlan& p, const GRange& r, GSme
 // tile of a pair whose second tile this CTA finishes next (raw h goes to the
 // warp's stash), 2 for that second tile (the first one's h is in the stash),
 // 0 for a pair split between CTAs (met through global memory).
+// The pieces of one slot: transposed into 16- or 8-byte rows (8, 16 pieces) or
+// stored as they are (one piece: a byte per lane, already contiguous).
+template <int NP>
+__device__ __forceinline__ void put_pieces(const Pieces64<NP>& pc, int lane, uint8_t* unit, int mstride,
+                                           uint8_t* atom, int i, int blk0, uint4* scratch)
+{
+    if constexpr (NP == 1) {
+        store_pieces64<1>(pc, lane, unit, mstride, atom, i, blk0);
+    } else {
+        const PieceRow<NP> pr = transpose_pieces<NP>(pc, lane, scratch);
+        store_piece_rows<NP>(pr, lane, unit, mstride, atom, i, blk0);
+    }
+}
+
 template <int NP>
 __device__ void gfinalize_gate_up(const GroupArgs& a, const GPlan& p, const GJob& jb, int i, const float* comb,
-                                  int lane, float* stash, int local)
+                                  int lane, float* stash, int local, uint4* scratch)
 {
     const int P = jb.p0 + i, tile = jb.tile;
     const float2 g = *reinterpret_cast<const float2*>(comb + 2 * lane);
@@ -824,7 +895,7 @@ __device__ void gfinalize_gate_up(const GroupArgs& a, const GPlan& p, const GJob
             const float w = a.w[a.perm[P]];
             Pieces64<NP> po;
             make_pieces64<NP>(e4m3_quant_dequant(o0, s) * w, e4m3_quant_dequant(o1, s) * w, po);
-            store_pieces64<NP>(po, lane, unit, mstride, atom, i, 2 * ((tile ^ 1) & 1));
+            put_pieces<NP>(po, lane, unit, mstride, atom, i, 2 * ((tile ^ 1) & 1), scratch);
         }
     }
     // E2M1 mode: the one piece is h quantized per 32 (w scales the down output);
@@ -832,7 +903,7 @@ __device__ void gfinalize_gate_up(const GroupArgs& a, const GPlan& p, const GJob
     const float w = a.act_e2m1 ? 1.0f : a.w[a.perm[P]];
     Pieces64<NP> pc;
     make_pieces64<NP>(h0 * w, h1 * w, pc);
-    store_pieces64<NP>(pc, lane, unit, mstride, atom, i, 2 * (tile & 1));
+    put_pieces<NP>(pc, lane, unit, mstride, atom, i, 2 * (tile & 1), scratch);
     // the down projection reads these with bulk copies (async proxy), in other CTAs
     asm volatile("fence.proxy.async.global;" ::: "memory");
     __syncwarp();
@@ -998,9 +1069,10 @@ __device__ void gepilogue(const GroupArgs& a, const GPlan& p, const GRange& r, G
                 if (g_cta_of_unit(U, G, partner * p.kgt) == (int)blockIdx.x) local = (cur.tile & 1) ? 2 : 1;
             }
             for (int i = quad; i < nt; i += 4) {
-                if (p.np == 8) gfinalize_gate_up<8>(a, p, cur, i, comb[i], lane, sm.hstash[i], local);
-                else if (p.np == 1) gfinalize_gate_up<1>(a, p, cur, i, comb[i], lane, sm.hstash[i], local);
-                else gfinalize_gate_up<16>(a, p, cur, i, comb[i], lane, sm.hstash[i], local);
+                if (p.np == 8) gfinalize_gate_up<8>(a, p, cur, i, comb[i], lane, sm.hstash[i], local, sm.tr[quad]);
+                else if (p.np == 1)
+                    gfinalize_gate_up<1>(a, p, cur, i, comb[i], lane, sm.hstash[i], local, sm.tr[quad]);
+                else gfinalize_gate_up<16>(a, p, cur, i, comb[i], lane, sm.hstash[i], local, sm.tr[quad]);
             }
             if (quad == 0 && lane == 0) G_TRACE(3, es.use[0] + es.use[1]);
             es.cb ^= 1;
