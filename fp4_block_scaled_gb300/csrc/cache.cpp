@@ -9,9 +9,10 @@
 //
 //   fetch(ids)     makes the experts of `ids` resident: a miss takes the least
 //                  recently used slot that the request does not use, and its
-//                  blob is copied there on one of two copy streams (two copies
-//                  in flight; a slot's copies always take the same stream, so
-//                  they stay in order); the caller's stream waits for the copies and
+//                  blob is copied there; the copies of a request go round-robin
+//                  over kCopyStreams copy streams (several in flight), and a
+//                  copy into a slot waits for the slot's previous fill, so a
+//                  slot's fills stay in order; the caller's stream waits for the copies and
 //                  then receives the layer's expert table (a device array of
 //                  E pointers, NULL for experts not resident), written in
 //                  stream order from a ring of page-locked staging buffers.
@@ -31,6 +32,10 @@
 
 #include "../../include/moe_ffn.h"
 
+namespace {
+constexpr int kCopyStreams = 4;
+}
+
 struct moe_expert_cache_s {
     int device = 0;
     int E = 0, slots = 0;
@@ -41,11 +46,13 @@ struct moe_expert_cache_s {
     std::vector<int> expert_in;                // slot -> expert or -1
     std::vector<long long> last_use;           // slot -> request stamp
     std::vector<cudaEvent_t> released;         // slot -> free once this event completes
+    std::vector<cudaEvent_t> filled;           // slot -> its last fill is done once this completes
     std::vector<char> ever_used;
     std::vector<int> prev_slots;               // slots of the previous request
     long long clock = 0;
-    cudaStream_t copy[2] = {nullptr, nullptr};
-    cudaEvent_t copied[2] = {nullptr, nullptr};
+    cudaStream_t copy[kCopyStreams] = {};
+    cudaEvent_t copied[kCopyStreams] = {};
+    int next_copy = 0;
     // the layer tables: one device array of E pointers, rewritten in stream
     // order; its host staging buffers form a ring guarded by events
     const uint8_t** dtable = nullptr;
@@ -79,7 +86,9 @@ void destroy_cache(moe_expert_cache_s* c)
     Guard g(c->device);
     for (cudaEvent_t e : c->released)
         if (e) cudaEventDestroy(e);
-    for (int i = 0; i < 2; i++) {
+    for (cudaEvent_t e : c->filled)
+        if (e) cudaEventDestroy(e);
+    for (int i = 0; i < kCopyStreams; i++) {
         if (c->copy[i]) cudaStreamDestroy(c->copy[i]);
         if (c->copied[i]) cudaEventDestroy(c->copied[i]);
     }
@@ -151,13 +160,19 @@ int make_resident(moe_expert_cache_s* c, const int32_t* ids, int n, bool count, 
         in_req[victim] = 1;
         if (count) c->misses++;
         c->bytes += (long long)c->blob;
-        cudaStream_t cs = c->copy[victim & 1];
+        cudaStream_t cs = c->copy[c->next_copy];
+        c->next_copy = (c->next_copy + 1) % kCopyStreams;
         cudaError_t err = cudaSuccess;
-        if (c->ever_used[victim]) err = cudaStreamWaitEvent(cs, c->released[victim], 0);
+        if (c->ever_used[victim]) {
+            // after the work that may read the slot, and after its previous fill
+            err = cudaStreamWaitEvent(cs, c->released[victim], 0);
+            if (err == cudaSuccess) err = cudaStreamWaitEvent(cs, c->filled[victim], 0);
+        }
         c->ever_used[victim] = 1;
         if (err == cudaSuccess)
             err = cudaMemcpyAsync(c->dev + (size_t)victim * c->stride, c->host[e], c->blob, cudaMemcpyHostToDevice,
                                   cs);
+        if (err == cudaSuccess) err = cudaEventRecord(c->filled[victim], cs);
         if (err != cudaSuccess) return MOE_ERR_CUDA;
         if (req_slots) req_slots->push_back(victim);
     }
@@ -186,15 +201,18 @@ extern "C" int moe_expert_cache_create(const moe_ffn_config* cfg, int device, co
     c->expert_in.assign((size_t)slots, -1);
     c->last_use.assign((size_t)slots, 0);
     c->released.assign((size_t)slots, nullptr);
+    c->filled.assign((size_t)slots, nullptr);
     c->ever_used.assign((size_t)slots, 0);
     bool ok = cudaMalloc(&c->dev, c->stride * (size_t)slots) == cudaSuccess;
     ok = ok && cudaMalloc(&c->dtable, sizeof(void*) * (size_t)c->E) == cudaSuccess;
-    for (int i = 0; ok && i < 2; i++) {
+    for (int i = 0; ok && i < kCopyStreams; i++) {
         ok = cudaStreamCreateWithFlags(&c->copy[i], cudaStreamNonBlocking) == cudaSuccess;
         ok = ok && cudaEventCreateWithFlags(&c->copied[i], cudaEventDisableTiming) == cudaSuccess;
     }
-    for (int s = 0; ok && s < slots; s++)
+    for (int s = 0; ok && s < slots; s++) {
         ok = cudaEventCreateWithFlags(&c->released[s], cudaEventDisableTiming) == cudaSuccess;
+        ok = ok && cudaEventCreateWithFlags(&c->filled[s], cudaEventDisableTiming) == cudaSuccess;
+    }
     for (int i = 0; ok && i < moe_expert_cache_s::kRing; i++) {
         ok = cudaMallocHost((void**)&c->stage[i], sizeof(void*) * (size_t)c->E) == cudaSuccess;
         ok = ok && cudaEventCreateWithFlags(&c->stage_ev[i], cudaEventDisableTiming) == cudaSuccess;
@@ -221,7 +239,7 @@ extern "C" int moe_expert_cache_fetch(moe_expert_cache_t c, const int32_t* ids, 
     if (rc != MOE_OK) return rc;
     // the caller's stream waits for this request's copies (and earlier ones on
     // the same copy streams, which may be prefetches of these experts)
-    for (int q = 0; q < 2; q++) {
+    for (int q = 0; q < kCopyStreams; q++) {
         if (cudaEventRecord(c->copied[q], c->copy[q]) != cudaSuccess) return MOE_ERR_CUDA;
         if (cudaStreamWaitEvent(s, c->copied[q], 0) != cudaSuccess) return MOE_ERR_CUDA;
     }
@@ -272,7 +290,7 @@ extern "C" void moe_expert_cache_destroy(moe_expert_cache_t c)
     if (!c) return;
     {
         Guard g(c->device);
-        for (int q = 0; q < 2; q++)
+        for (int q = 0; q < kCopyStreams; q++)
             if (c->copy[q]) cudaStreamSynchronize(c->copy[q]);
     }
     destroy_cache(c);

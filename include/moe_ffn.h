@@ -221,7 +221,7 @@ int moe_batch_distinct(const int32_t* routing, const int32_t* order, int N, int 
  *   fetch    ids: host int32 [n] expert ids (-1 ignored).  Makes them
  *            resident: a miss takes the least recently used slot that the
  *            request does not use (lowest slot on ties) and is copied there
- *            on one of two internal copy streams; `stream` then waits for the
+ *            on one of four internal copy streams (round-robin); `stream` then waits for the
  *            copies and receives the layer's table in *tbl (a device array of
  *            E pointers, NULL for experts not resident) for launches on
  *            `stream` until the next fetch.  INVALID_ARG if the request holds
