@@ -3,6 +3,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <new>
 #include <vector>
 
@@ -23,6 +24,16 @@ struct StackGraph {
     unsigned long long last_use;
 };
 
+// The whole of one moe_ffn_forward_host call as a graph: one host-to-device
+// copy of the packed inputs, the layer's kernels, one device-to-host copy of y,
+// between page-locked staging buffers of the handle.
+struct HostGraph {
+    int T;
+    const void* experts;
+    cudaGraphExec_t exec;
+    unsigned long long last_use;
+};
+
 }  // namespace
 
 struct moe_ffn {
@@ -35,10 +46,10 @@ struct moe_ffn {
     GroupArgs gbase;            // the same for the expert-major path
     int gemm_min_tokens;        // T >= this takes the expert-major path
     int* status;
-    uint16_t* x_stage;          // staging for moe_ffn_forward_host
-    int32_t* idx_stage;
-    float* w_stage;
+    uint8_t* in_stage;          // device staging for moe_ffn_forward_host: x | idx | w, packed per T
     void* y_stage;
+    uint8_t* host_stage;        // page-locked: the packed inputs, then y (allocated on first use)
+    std::vector<HostGraph> hgraphs;
     cudaStream_t cap_stream;    // private stream used only for graph capture
     std::vector<StackGraph> graphs;
     unsigned long long use_clock;
@@ -54,6 +65,15 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Packed inputs of moe_ffn_forward_host for T tokens: x (bf16 [T][H]) at 0,
+// topk_idx at idx_off(T), topk_w at w_off(T), each 16-byte aligned.
+size_t host_idx_off(int T, int H) { return align_up((size_t)T * H * 2, 16); }
+size_t host_w_off(int T, int H, int k) { return host_idx_off(T, H) + align_up((size_t)T * k * 4, 16); }
+size_t host_in_bytes(int T, int H, int k) { return host_w_off(T, H, k) + (size_t)T * k * 4; }
+// Above this many bytes of x and y, moe_ffn_forward_host copies straight from
+// and to the caller's buffers instead of through its page-locked staging.
+constexpr size_t kHostStageMax = 128 * 1024;
 
 int check_cfg(const moe_ffn_config* c)
 {
@@ -212,8 +232,7 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     size_t o_rlog = take((size_t)T * cfg->num_experts * 4);
     const size_t rpart_bytes = T > 8 ? (size_t)router_max_splits(H) * T * cfg->num_experts * 4 : 0;
     size_t o_rpart = take(rpart_bytes);
-    size_t o_xst = take((size_t)T * H * 2), o_ist = take((size_t)T * k * 4);
-    size_t o_wst = take((size_t)T * k * 4), o_yst = take((size_t)T * H * 4);
+    size_t o_inst = take(host_in_bytes(T, H, k)), o_yst = take((size_t)T * H * 4);
     h->ws_bytes = off;
     if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -281,9 +300,7 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     }
     h->rlogits = (float*)(b + o_rlog);
     h->rpart = rpart_bytes ? (float*)(b + o_rpart) : nullptr;
-    h->x_stage = (uint16_t*)(b + o_xst);
-    h->idx_stage = (int32_t*)(b + o_ist);
-    h->w_stage = (float*)(b + o_wst);
+    h->in_stage = (uint8_t*)(b + o_inst);
     h->y_stage = (void*)(b + o_yst);
     *out = h;
     return MOE_OK;
@@ -325,20 +342,88 @@ int moe_ffn_forward_host(moe_ffn_t h, const void* x_host, const int32_t* idx_hos
         return MOE_ERR_INVALID_ARG;
     DeviceGuard guard(h->device);
     cudaStream_t s = (cudaStream_t)stream;
-    const int H = h->cfg.hidden, k = h->cfg.topk;
-    size_t ybytes = (size_t)T * H * (h->cfg.out_dtype == MOE_OUT_F32 ? 4 : 2);
-    cudaError_t e;
-    e = cudaMemcpyAsync(h->x_stage, x_host, (size_t)T * H * 2, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(h->idx_stage, idx_host, (size_t)T * k * 4, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(h->w_stage, w_host, (size_t)T * k * 4, cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    int rc = run_forward(h, h->x_stage, h->idx_stage, h->w_stage, tbl, h->y_stage, T, s);
-    if (rc) return rc;
-    e = cudaMemcpyAsync(y_host, h->y_stage, ybytes, cudaMemcpyDeviceToHost, s);
+    const int H = h->cfg.hidden, k = h->cfg.topk, Tmax = h->cfg.max_tokens;
+    const size_t ybytes = (size_t)T * H * (h->cfg.out_dtype == MOE_OUT_F32 ? 4 : 2);
+    const size_t io = host_idx_off(T, H), wo = host_w_off(T, H, k), nin = host_in_bytes(T, H, k);
+    const size_t ytok = (size_t)H * (h->cfg.out_dtype == MOE_OUT_F32 ? 4 : 2);
+    const int Tst = (int)std::min<size_t>((size_t)Tmax, kHostStageMax / ((size_t)H * 2 + ytok));  // largest staged T
+    const size_t yo = align_up(host_in_bytes(Tst, H, k), 256);
+    const int32_t* idx_d = (const int32_t*)(h->in_stage + io);
+    const float* w_d = (const float*)(h->in_stage + wo);
+    cudaError_t e = cudaSuccess;
+    if ((size_t)T * H * 2 + ybytes > kHostStageMax) {
+        // large batches: three copies straight from the caller's buffers and one
+        // back (host-side staging copies would cost more than the launches saved)
+        e = cudaMemcpyAsync(h->in_stage, x_host, (size_t)T * H * 2, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaMemcpyAsync((void*)idx_d, idx_host, (size_t)T * k * 4, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaMemcpyAsync((void*)w_d, w_host, (size_t)T * k * 4, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        int rc = run_forward(h, h->in_stage, idx_d, w_d, tbl, h->y_stage, T, s);
+        if (rc) return rc;
+        e = cudaMemcpyAsync(y_host, h->y_stage, ybytes, cudaMemcpyDeviceToHost, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        return cuda_rc(e);
+    }
+    if (!h->host_stage) {
+        void* p = nullptr;
+        if (cudaHostAlloc(&p, yo + (size_t)Tst * ytok, cudaHostAllocDefault) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_OOM;
+        }
+        h->host_stage = (uint8_t*)p;
+    }
+    uint8_t* hs = h->host_stage;
+    // the previous call waited for its stream, so the staging buffers are free
+    memcpy(hs, x_host, (size_t)T * H * 2);
+    memcpy(hs + io, idx_host, (size_t)T * k * 4);
+    memcpy(hs + wo, w_host, (size_t)T * k * 4);
+    if (h->prof) {  // profiling times each launch on its own: no graph
+        e = cudaMemcpyAsync(h->in_stage, hs, nin, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        int rc = run_forward(h, h->in_stage, idx_d, w_d, tbl, h->y_stage, T, s);
+        if (rc) return rc;
+        e = cudaMemcpyAsync(hs + yo, h->y_stage, ybytes, cudaMemcpyDeviceToHost, s);
+    } else {
+        h->use_clock++;
+        HostGraph* g = nullptr;
+        for (auto& c : h->hgraphs)
+            if (c.T == T && c.experts == tbl->experts) g = &c;
+        if (!g) {
+            cudaGraph_t graph = nullptr;
+            e = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal);
+            if (e != cudaSuccess) return MOE_ERR_CUDA;
+            cudaError_t le = cudaMemcpyAsync(h->in_stage, hs, nin, cudaMemcpyHostToDevice, h->cap_stream);
+            int rc = MOE_OK;
+            if (le == cudaSuccess) rc = run_forward(h, h->in_stage, idx_d, w_d, tbl, h->y_stage, T, h->cap_stream);
+            if (le == cudaSuccess && rc == MOE_OK)
+                le = cudaMemcpyAsync(hs + yo, h->y_stage, ybytes, cudaMemcpyDeviceToHost, h->cap_stream);
+            e = cudaStreamEndCapture(h->cap_stream, &graph);
+            if (le != cudaSuccess || rc != MOE_OK || e != cudaSuccess) {
+                if (graph) cudaGraphDestroy(graph);
+                cudaGetLastError();
+                return rc != MOE_OK ? rc : MOE_ERR_CUDA;
+            }
+            cudaGraphExec_t exec = nullptr;
+            e = cudaGraphInstantiate(&exec, graph, 0);
+            cudaGraphDestroy(graph);
+            if (e != cudaSuccess) return MOE_ERR_CUDA;
+            if (h->hgraphs.size() >= 8) {  // evict the least recently used graph
+                size_t v = 0;
+                for (size_t i = 1; i < h->hgraphs.size(); i++)
+                    if (h->hgraphs[i].last_use < h->hgraphs[v].last_use) v = i;
+                cudaGraphExecDestroy(h->hgraphs[v].exec);
+                h->hgraphs.erase(h->hgraphs.begin() + (long)v);
+            }
+            h->hgraphs.push_back(HostGraph{T, tbl->experts, exec, 0});
+            g = &h->hgraphs.back();
+        }
+        g->last_use = h->use_clock;
+        e = cudaGraphLaunch(g->exec, s);
+    }
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    return cuda_rc(e);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    memcpy(y_host, hs + yo, ybytes);
+    return MOE_OK;
 }
 
 int moe_ffn_route(moe_ffn_t h, const int32_t* topk_idx, int T, int32_t* counts, int32_t* offsets,
@@ -542,6 +627,8 @@ void moe_ffn_destroy(moe_ffn_t h)
     if (!h) return;
     DeviceGuard guard(h->device);
     for (auto& g : h->graphs) cudaGraphExecDestroy(g.exec);
+    for (auto& g : h->hgraphs) cudaGraphExecDestroy(g.exec);
+    if (h->host_stage) cudaFreeHost(h->host_stage);
     delete h->prof;
     if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
     cudaFree(h->ws);

@@ -184,16 +184,28 @@ def test_out_of_range_expert_contributes_zero_and_sets_status():
         L.close()
 
 
-def test_forward_host_equals_forward():
-    L = Layer(**TINY)
+@pytest.mark.parametrize("shape", ["tiny", "wide"])
+@pytest.mark.parametrize("out", [moe.MOE_OUT_F32, moe.MOE_OUT_BF16])
+def test_forward_host_equals_forward(out, shape):
+    """The host-buffer call equals the device call on both paths, over
+    repeated calls with new inputs, several T and profiling mode.  Small
+    batches go through the staging buffer and a graph per (T, table)
+    (replayed and re-keyed here); with hidden 4096 the batches of 20 and 24
+    take the direct copies."""
+    cfg = TINY if shape == "tiny" else dict(E=8, H=4096, I=128, k=2)
+    L = Layer(**cfg, max_tokens=24, out=out, path="auto")
     try:
-        T = 3
-        x, idx, w = inputs(T, TINY["E"], TINY["H"], TINY["k"], seed=2)
-        y_dev = L.run(x, idx, w).cpu().numpy()
-        y_host = np.zeros((T, TINY["H"]), np.float32)
-        moe.moe_ffn_forward_host(L.h, x.ctypes.data, idx.ctypes.data, w.ctypes.data, L.es.table,
-                                 y_host.ctypes.data, T)
-        assert np.array_equal(y_dev, y_host)
+        for step, T in enumerate([3, 1, 3, 20, 1, 24, 3]):
+            x, idx, w = inputs(T, cfg["E"], cfg["H"], cfg["k"], seed=40 + step)
+            y_dev = L.run(x, idx, w).cpu()
+            y_dev = (y_dev.view(torch.int16) if out == moe.MOE_OUT_BF16 else y_dev).numpy()
+            y_host = np.zeros((T, cfg["H"]), np.float32 if out == moe.MOE_OUT_F32 else np.int16)
+            moe.moe_ffn_profile_enable(L.h, step == 4)
+            moe.moe_ffn_forward_host(L.h, x.ctypes.data, idx.ctypes.data, w.ctypes.data, L.es.table,
+                                     y_host.ctypes.data, T)
+            assert np.array_equal(y_dev, y_host), f"step {step}, T {T}"
+        moe.moe_ffn_profile_enable(L.h, False)
+        assert moe.moe_ffn_status(L.h) == moe.MOE_OK
     finally:
         L.close()
 
