@@ -24,9 +24,9 @@ struct StackGraph {
     unsigned long long last_use;
 };
 
-// The whole of one moe_ffn_forward_host call as a graph: one host-to-device
-// copy of the packed inputs, the layer's kernels, one device-to-host copy of y,
-// between page-locked staging buffers of the handle.
+// The layer's kernels of one small-batch moe_ffn_forward_host call as a graph,
+// reading their inputs from and writing y to the handle's mapped page-locked
+// staging buffer.
 struct HostGraph {
     int T;
     const void* experts;
@@ -48,7 +48,8 @@ struct moe_ffn {
     int* status;
     uint8_t* in_stage;          // device staging for moe_ffn_forward_host: x | idx | w, packed per T
     void* y_stage;
-    uint8_t* host_stage;        // page-locked: the packed inputs, then y (allocated on first use)
+    uint8_t* host_stage;        // page-locked, mapped: the packed inputs, then y (allocated on first use)
+    uint8_t* host_stage_dev;    // its device address
     std::vector<HostGraph> hgraphs;
     cudaStream_t cap_stream;    // private stream used only for graph capture
     std::vector<StackGraph> graphs;
@@ -344,7 +345,7 @@ int moe_ffn_forward_host(moe_ffn_t h, const void* x_host, const int32_t* idx_hos
     cudaStream_t s = (cudaStream_t)stream;
     const int H = h->cfg.hidden, k = h->cfg.topk, Tmax = h->cfg.max_tokens;
     const size_t ybytes = (size_t)T * H * (h->cfg.out_dtype == MOE_OUT_F32 ? 4 : 2);
-    const size_t io = host_idx_off(T, H), wo = host_w_off(T, H, k), nin = host_in_bytes(T, H, k);
+    const size_t io = host_idx_off(T, H), wo = host_w_off(T, H, k);
     const size_t ytok = (size_t)H * (h->cfg.out_dtype == MOE_OUT_F32 ? 4 : 2);
     const int Tst = (int)std::min<size_t>((size_t)Tmax, kHostStageMax / ((size_t)H * 2 + ytok));  // largest staged T
     const size_t yo = align_up(host_in_bytes(Tst, H, k), 256);
@@ -366,23 +367,33 @@ int moe_ffn_forward_host(moe_ffn_t h, const void* x_host, const int32_t* idx_hos
     }
     if (!h->host_stage) {
         void* p = nullptr;
-        if (cudaHostAlloc(&p, yo + (size_t)Tst * ytok, cudaHostAllocDefault) != cudaSuccess) {
+        void* d = nullptr;
+        if (cudaHostAlloc(&p, yo + (size_t)Tst * ytok, cudaHostAllocMapped) != cudaSuccess) {
             cudaGetLastError();
             return MOE_ERR_OOM;
         }
+        if (cudaHostGetDevicePointer(&d, p, 0) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFreeHost(p);
+            return MOE_ERR_CUDA;
+        }
         h->host_stage = (uint8_t*)p;
+        h->host_stage_dev = (uint8_t*)d;
     }
     uint8_t* hs = h->host_stage;
-    // the previous call waited for its stream, so the staging buffers are free
+    uint8_t* hd = h->host_stage_dev;
+    // the previous call waited for its stream, so the staging buffer is free
     memcpy(hs, x_host, (size_t)T * H * 2);
     memcpy(hs + io, idx_host, (size_t)T * k * 4);
     memcpy(hs + wo, w_host, (size_t)T * k * 4);
+    // the kernels read x, topk_idx, topk_w from the mapped staging buffer and
+    // write y into it: the bytes cross the host link inside the kernels' own
+    // loads and stores, with no copy of their own
+    const int32_t* idx_m = (const int32_t*)(hd + io);
+    const float* w_m = (const float*)(hd + wo);
     if (h->prof) {  // profiling times each launch on its own: no graph
-        e = cudaMemcpyAsync(h->in_stage, hs, nin, cudaMemcpyHostToDevice, s);
-        if (e != cudaSuccess) return MOE_ERR_CUDA;
-        int rc = run_forward(h, h->in_stage, idx_d, w_d, tbl, h->y_stage, T, s);
+        int rc = run_forward(h, hd, idx_m, w_m, tbl, hd + yo, T, s);
         if (rc) return rc;
-        e = cudaMemcpyAsync(hs + yo, h->y_stage, ybytes, cudaMemcpyDeviceToHost, s);
     } else {
         h->use_clock++;
         HostGraph* g = nullptr;
@@ -392,13 +403,9 @@ int moe_ffn_forward_host(moe_ffn_t h, const void* x_host, const int32_t* idx_hos
             cudaGraph_t graph = nullptr;
             e = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal);
             if (e != cudaSuccess) return MOE_ERR_CUDA;
-            cudaError_t le = cudaMemcpyAsync(h->in_stage, hs, nin, cudaMemcpyHostToDevice, h->cap_stream);
-            int rc = MOE_OK;
-            if (le == cudaSuccess) rc = run_forward(h, h->in_stage, idx_d, w_d, tbl, h->y_stage, T, h->cap_stream);
-            if (le == cudaSuccess && rc == MOE_OK)
-                le = cudaMemcpyAsync(hs + yo, h->y_stage, ybytes, cudaMemcpyDeviceToHost, h->cap_stream);
+            const int rc = run_forward(h, hd, idx_m, w_m, tbl, hd + yo, T, h->cap_stream);
             e = cudaStreamEndCapture(h->cap_stream, &graph);
-            if (le != cudaSuccess || rc != MOE_OK || e != cudaSuccess) {
+            if (rc != MOE_OK || e != cudaSuccess) {
                 if (graph) cudaGraphDestroy(graph);
                 cudaGetLastError();
                 return rc != MOE_OK ? rc : MOE_ERR_CUDA;

@@ -140,15 +140,16 @@ int moe_ffn_forward(moe_ffn_t h, const void* x, const int32_t* topk_idx, const f
 /* moe_ffn_forward with HOST x / topk_idx / topk_w / y (any host memory; the
  * call waits for `stream` before it returns).  Small batches (x and y
  * together at most 128 KB): the inputs are packed into a page-locked staging
- * buffer of the handle (allocated on the first such call), which reaches the
- * device in ONE copy; that copy, the layer's kernels and the copy of y back
- * into the staging buffer run as one CUDA graph on `stream` (captured on the
- * first call for each (T, tbl->experts) pair, at most 8 kept; launched one by
- * one while profiling is enabled), then y is copied out.  Larger batches: x,
- * topk_idx and topk_w are copied straight from the caller's buffers (pinned
- * memory makes these copies DMA-only) and y straight back.  The expert table
- * stays in device memory.  Returns MOE_ERR_OOM if the staging buffer cannot
- * be allocated. */
+ * buffer of the handle that is mapped into the device's address space
+ * (allocated on the first such call); the layer's kernels read x, topk_idx and
+ * topk_w from it and write y into it over the host link, with no copy
+ * operations, run as one CUDA graph on `stream` (captured on the first call
+ * for each (T, tbl->experts) pair, at most 8 kept; launched one by one while
+ * profiling is enabled); then y is copied out on the host.  Larger batches:
+ * x, topk_idx and topk_w are copied straight from the caller's buffers into
+ * device memory (pinned memory makes these copies DMA-only) and y straight
+ * back.  The expert table stays in device memory.  Returns MOE_ERR_OOM if the
+ * staging buffer cannot be allocated. */
 int moe_ffn_forward_host(moe_ffn_t h, const void* x_host, const int32_t* topk_idx_host,
                          const float* topk_w_host, const moe_expert_table* tbl, void* y_host,
                          int T, void* stream);
