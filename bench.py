@@ -506,8 +506,8 @@ def run_ours(args, wl):
     achieved = ly_bytes / (ly_ms / 1000.0) / 1e9
     traffic = traffic_record(kernel, args.workload, ly_bytes)
 
-    # ---- the router ahead of the path (logits = W x, top-k, softmax): two
-    # launches per call; timed (a) back to back in a CUDA graph of nrg calls,
+    # ---- the router ahead of the path (logits = W x, top-k, softmax): one
+    # launch per call up to 8 tokens, two above; timed (a) back to back in a CUDA graph of nrg calls,
     # as a decode step would run it, and (b) alone, events around each call
     Wr = torch.from_numpy(synth.router_weights_bf16(E, H).view(np.int16)).cuda()
     r_idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
@@ -544,11 +544,12 @@ def run_ours(args, wl):
     moe.moe_ffn_profile_enable(h, False)
     r_us = ms_r[moe.MOE_PHASE_ROUTER] / max(1, n_r[moe.MOE_PHASE_ROUTER]) * 1e3
     r_bytes = E * H * 2 + T * H * 2 + 2 * T * E * 4 + T * k * 8     # W, x, logits out and back, routing
-    router = {"kernels": ("k_router_logits" if T <= 8 else "k_router_mma") + " + k_router_select",
+    router = {"kernels": "k_router_logits (selection in its last CTA per token tile)" if T <= 8
+              else "k_router_mma + k_router_select",
               "us": r_us_graph, "us_alone": r_us, "algorithmic_bytes": r_bytes,
               "gbs": r_bytes / (r_us_graph * 1e-6) / 1e9,
               "frac_of_hbm": r_bytes / (r_us_graph * 1e-6) / 1e9 / peak,
-              "launches": 2, "timing": f"us: per call, {nrg} calls back to back in a CUDA graph, each on its "
+              "launches": 1 if T <= 8 else 2, "timing": f"us: per call, {nrg} calls back to back in a CUDA graph, each on its "
                                        "own router matrix (256 MB in all, > L2); us_alone: events around "
                                        "each call, one matrix"}
 

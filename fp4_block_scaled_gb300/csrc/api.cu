@@ -57,6 +57,7 @@ struct moe_ffn {
     Profiler* prof;             // non-null while moe_ffn_profile_enable(h, 1)
     float* rlogits;             // router logits scratch [max_tokens][E]
     float* rpart;               // router split-K partials [max splits][max_tokens][E] (batches above 8)
+    int* rtickets;              // router: finished CTAs per token tile [max_tokens], zero between calls
 };
 
 namespace {
@@ -230,7 +231,7 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     size_t o_gxg = take(gw.xg), o_gxgsf = take(gw.xgsf), o_ghg = take(gw.hg), o_ghgsf = take(gw.hgsf);
     size_t o_gobuf = take(gw.obuf), o_gpgu = take(gw.part_gu), o_gpdn = take(gw.part_dn);
     size_t o_ghraw = take(gw.hraw), o_ghpair = take(gw.hpair);
-    size_t o_rlog = take((size_t)T * cfg->num_experts * 4);
+    size_t o_rlog = take((size_t)T * cfg->num_experts * 4), o_rtk = take((size_t)T * sizeof(int));
     const size_t rpart_bytes = T > 8 ? (size_t)router_max_splits(H) * T * cfg->num_experts * 4 : 0;
     size_t o_rpart = take(rpart_bytes);
     size_t o_inst = take(host_in_bytes(T, H, k)), o_yst = take((size_t)T * H * 4);
@@ -300,6 +301,7 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
         ga.hpair = e4m3 ? (int*)(b + o_ghpair) : nullptr;
     }
     h->rlogits = (float*)(b + o_rlog);
+    h->rtickets = (int*)(b + o_rtk);
     h->rpart = rpart_bytes ? (float*)(b + o_rpart) : nullptr;
     h->in_stage = (uint8_t*)(b + o_inst);
     h->y_stage = (void*)(b + o_yst);
@@ -488,8 +490,14 @@ int moe_router_topk(moe_ffn_t h, const void* x, const void* router_w, int T, flo
     a.nsplit = h->rpart ? router_mma_splits(T, h->cfg.hidden, h->cfg.num_experts) : 0;
     cudaStream_t s = (cudaStream_t)stream;
     if (h->prof) h->prof->begin(kPhaseRouter, s);
-    cudaError_t e = a.nsplit ? launch_router_mma(a, s, !h->prof) : launch_router_logits(a, s, !h->prof);
-    if (e == cudaSuccess) e = launch_router_select(a, s, !h->prof);
+    cudaError_t e;
+    if (a.nsplit) {
+        e = launch_router_mma(a, s, !h->prof);
+        if (e == cudaSuccess) e = launch_router_select(a, s, !h->prof);
+    } else {  // one launch: the logits kernel's last CTA per token tile selects
+        a.tickets = h->rtickets;
+        e = launch_router_logits(a, s, !h->prof);
+    }
     if (h->prof) h->prof->end(s);
     return cuda_rc(e);
 }

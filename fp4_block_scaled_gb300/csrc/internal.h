@@ -201,6 +201,9 @@ struct RouterArgs {
     float* part;
     int nsplit;
     int* status;
+    // non-null: k_router_logits also selects (the last CTA of each token tile,
+    // counted here; [ceil(T / tpc)] ints, zero between launches)
+    int* tickets;
 };
 int router_max_experts();
 int router_tokens_per_cta(int H);     // 0: H too large for the logits kernel

@@ -9,7 +9,9 @@
 //                    so a pass keeps the whole row in flight, and accumulates
 //                    the tpc dot products in fp32 (bf16 products are exact),
 //                    then a butterfly warp sum, so the result is
-//                    reproducible.
+//                    reproducible.  Given a ticket counter per token tile,
+//                    the last CTA of the tile to finish also runs the
+//                    selection below for its tokens: one launch per call.
 //   k_router_select  one warp per token: the logits as order keys in
 //                    registers, k rounds of a warp arg-max under the order
 //                    "larger logit first, NaN after every number, ties to the
@@ -60,116 +62,6 @@ __device__ __forceinline__ void stage_x(const uint4* src, int n, F store)
     }
 }
 
-template <int TPC, int NW>
-__global__ void __launch_bounds__(NW * 32) k_router_logits(RouterArgs a)
-{
-    extern __shared__ __align__(16) uint4 s_x[];      // [TPC][H / 8]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int H8 = a.H / 8;
-    const int t0 = blockIdx.y * TPC;
-    const int nt = min(TPC, a.T - t0);
-    const int e = blockIdx.x * NW + warp;
-    const uint4* wrow = reinterpret_cast<const uint4*>(a.w + (size_t)min(e, a.E - 1) * a.H);
-    float acc[TPC];
-#pragma unroll
-    for (int t = 0; t < TPC; t++) acc[t] = 0.0f;
-    auto dot = [&](const uint4 wq, int c) {
-        float wf[8];
-        bf16x8_to_f32(wq, wf);
-#pragma unroll
-        for (int t = 0; t < TPC; t++) {
-            if (t < nt) {
-                float xf[8];
-                bf16x8_to_f32(s_x[t * H8 + c], xf);
-#pragma unroll
-                for (int q = 0; q < 8; q++) acc[t] = fmaf(wf[q], xf[q], acc[t]);
-            }
-        }
-    };
-    if constexpr (TPC <= 4) {
-        // small batches are latency-bound: a whole pass of the row (a warp covers
-        // 4096 of H) in flight at once, issued before the wait for the previous
-        // kernel (the router weights are not written by earlier kernels)
-        uint4 wv[kRChunks];
-#pragma unroll
-        for (int i = 0; i < kRChunks; i++) {
-            const int c = lane + 32 * i;
-            wv[i] = c < H8 ? ldg_stream_v4(wrow + c) : make_uint4(0, 0, 0, 0);
-        }
-        pdl_wait();
-        pdl_trigger();
-        stage_x(reinterpret_cast<const uint4*>(a.x + (size_t)t0 * a.H), nt * H8,
-                [&](int i, const uint4 v) { s_x[i] = v; });
-        __syncthreads();
-        if (e >= a.E) return;
-        for (int c0 = 0; c0 < H8; c0 += 32 * kRChunks) {
-            if (c0 > 0) {
-#pragma unroll
-                for (int i = 0; i < kRChunks; i++) {
-                    const int c = c0 + lane + 32 * i;
-                    wv[i] = c < H8 ? ldg_stream_v4(wrow + c) : make_uint4(0, 0, 0, 0);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < kRChunks; i++) {
-                const int c = c0 + lane + 32 * i;
-                if (c < H8) dot(wv[i], c);
-            }
-        }
-    } else {
-        // larger batches reuse each weight chunk for TPC tokens: x is staged as
-        // fp32 once per CTA ([TPC][H]) and the weights stream
-        float4* s_xf = reinterpret_cast<float4*>(s_x);
-        pdl_wait();
-        pdl_trigger();
-        stage_x(reinterpret_cast<const uint4*>(a.x + (size_t)t0 * a.H), nt * H8, [&](int i, const uint4 v) {
-            float f[8];
-            bf16x8_to_f32(v, f);
-            s_xf[2 * i] = make_float4(f[0], f[1], f[2], f[3]);
-            s_xf[2 * i + 1] = make_float4(f[4], f[5], f[6], f[7]);
-        });
-        __syncthreads();
-        if (e >= a.E) return;
-        constexpr int kDepth = 8;                 // weight chunks in flight per lane
-        for (int c0 = lane; c0 < H8; c0 += 32 * kDepth) {
-            uint4 wq[kDepth];
-#pragma unroll
-            for (int q = 0; q < kDepth; q++) {
-                const int c = c0 + 32 * q;
-                wq[q] = c < H8 ? ldg_stream_v4(wrow + c) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int q = 0; q < kDepth; q++) {
-            const int c = c0 + 32 * q;
-            if (c >= H8) break;
-            float wf[8];
-            bf16x8_to_f32(wq[q], wf);
-#pragma unroll
-            for (int t = 0; t < TPC; t++) {
-                if (t < nt) {
-                    const float4 x0 = s_xf[(t * H8 + c) * 2], x1 = s_xf[(t * H8 + c) * 2 + 1];
-                    acc[t] = fmaf(wf[0], x0.x, acc[t]);
-                    acc[t] = fmaf(wf[1], x0.y, acc[t]);
-                    acc[t] = fmaf(wf[2], x0.z, acc[t]);
-                    acc[t] = fmaf(wf[3], x0.w, acc[t]);
-                    acc[t] = fmaf(wf[4], x1.x, acc[t]);
-                    acc[t] = fmaf(wf[5], x1.y, acc[t]);
-                    acc[t] = fmaf(wf[6], x1.z, acc[t]);
-                    acc[t] = fmaf(wf[7], x1.w, acc[t]);
-                }
-            }
-            }
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < TPC; t++) {
-        if (t < nt) {
-            const float v = warp_sum(acc[t]);
-            if (lane == 0) a.logits[(size_t)(t0 + t) * a.E + e] = v;
-        }
-    }
-}
-
 // Order key of a logit: larger keys rank first; -0 and +0 tie; NaN ranks after
 // every number (key 1); key 0 is "taken" or "no expert".
 __device__ __forceinline__ uint32_t order_key(float v)
@@ -179,19 +71,15 @@ __device__ __forceinline__ uint32_t order_key(float v)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// grid ceil(T / 8), 256 threads: one warp per token.  Lane l holds the order
-// keys of experts l, l + 32, ... (R of them) in registers and its best
-// untaken one; a round takes the warp's best with two redux.sync (the largest
-// key, then the lowest id holding it), and only the winning lane picks its
-// next best.  Lane i keeps pick i for the softmax.
+// One warp selects token t's top-k.  Lane l holds the order keys of experts
+// l, l + 32, ... (R of them) in registers and its best untaken one; a round
+// takes the warp's best with two redux.sync (the largest key, then the lowest
+// id holding it), and only the winning lane picks its next best.  Lane i keeps
+// pick i for the softmax.  The logits are read through L2 (other CTAs of the
+// same grid may have written them).
 template <int R>
-__global__ void __launch_bounds__(256) k_router_select(RouterArgs a)
+__device__ __forceinline__ void select_token(const RouterArgs& a, int t, int lane)
 {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + warp;
-    pdl_wait();
-    pdl_trigger();
-    if (t >= a.T) return;
     float v[R];
     uint32_t key[R];
     if (a.nsplit == 0) {
@@ -199,7 +87,7 @@ __global__ void __launch_bounds__(256) k_router_select(RouterArgs a)
 #pragma unroll
         for (int j = 0; j < R; j++) {
             const int e = lane + 32 * j;
-            v[j] = e < a.E ? row[e] : 0.0f;
+            v[j] = e < a.E ? __ldcg(row + e) : 0.0f;
         }
     } else {
         // the tensor-core path's split-K partials, added in split order; the
@@ -275,6 +163,151 @@ __global__ void __launch_bounds__(256) k_router_select(RouterArgs a)
         a.idx[(size_t)t * a.topk + lane] = mine_e;
         a.wout[(size_t)t * a.topk + lane] = p / sum;
     }
+}
+
+__device__ __forceinline__ void select_token_any(const RouterArgs& a, int t, int lane)
+{
+    if (a.E <= 128) select_token<4>(a, t, lane);
+    else if (a.E <= 256) select_token<8>(a, t, lane);
+    else if (a.E <= 384) select_token<12>(a, t, lane);
+    else if (a.E <= 512) select_token<16>(a, t, lane);
+    else select_token<32>(a, t, lane);
+}
+
+// grid ceil(T / 8), 256 threads: one warp per token.
+template <int R>
+__global__ void __launch_bounds__(256) k_router_select(RouterArgs a)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    pdl_wait();
+    pdl_trigger();
+    if (t >= a.T) return;
+    select_token<R>(a, t, lane);
+}
+
+template <int TPC, int NW>
+__global__ void __launch_bounds__(NW * 32) k_router_logits(RouterArgs a)
+{
+    extern __shared__ __align__(16) uint4 s_x[];      // [TPC][H / 8]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H8 = a.H / 8;
+    const int t0 = blockIdx.y * TPC;
+    const int nt = min(TPC, a.T - t0);
+    const int e = blockIdx.x * NW + warp;
+    const uint4* wrow = reinterpret_cast<const uint4*>(a.w + (size_t)min(e, a.E - 1) * a.H);
+    float acc[TPC];
+#pragma unroll
+    for (int t = 0; t < TPC; t++) acc[t] = 0.0f;
+    auto dot = [&](const uint4 wq, int c) {
+        float wf[8];
+        bf16x8_to_f32(wq, wf);
+#pragma unroll
+        for (int t = 0; t < TPC; t++) {
+            if (t < nt) {
+                float xf[8];
+                bf16x8_to_f32(s_x[t * H8 + c], xf);
+#pragma unroll
+                for (int q = 0; q < 8; q++) acc[t] = fmaf(wf[q], xf[q], acc[t]);
+            }
+        }
+    };
+    if constexpr (TPC <= 4) {
+        // small batches are latency-bound: a whole pass of the row (a warp covers
+        // 4096 of H) in flight at once, issued before the wait for the previous
+        // kernel (the router weights are not written by earlier kernels)
+        uint4 wv[kRChunks];
+#pragma unroll
+        for (int i = 0; i < kRChunks; i++) {
+            const int c = lane + 32 * i;
+            wv[i] = c < H8 ? ldg_stream_v4(wrow + c) : make_uint4(0, 0, 0, 0);
+        }
+        pdl_wait();
+        pdl_trigger();
+        stage_x(reinterpret_cast<const uint4*>(a.x + (size_t)t0 * a.H), nt * H8,
+                [&](int i, const uint4 v) { s_x[i] = v; });
+        __syncthreads();
+        const bool live = e < a.E;     // warps past E stay for the selection below
+        for (int c0 = 0; live && c0 < H8; c0 += 32 * kRChunks) {
+            if (c0 > 0) {
+#pragma unroll
+                for (int i = 0; i < kRChunks; i++) {
+                    const int c = c0 + lane + 32 * i;
+                    wv[i] = c < H8 ? ldg_stream_v4(wrow + c) : make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kRChunks; i++) {
+                const int c = c0 + lane + 32 * i;
+                if (c < H8) dot(wv[i], c);
+            }
+        }
+    } else {
+        // larger batches reuse each weight chunk for TPC tokens: x is staged as
+        // fp32 once per CTA ([TPC][H]) and the weights stream
+        float4* s_xf = reinterpret_cast<float4*>(s_x);
+        pdl_wait();
+        pdl_trigger();
+        stage_x(reinterpret_cast<const uint4*>(a.x + (size_t)t0 * a.H), nt * H8, [&](int i, const uint4 v) {
+            float f[8];
+            bf16x8_to_f32(v, f);
+            s_xf[2 * i] = make_float4(f[0], f[1], f[2], f[3]);
+            s_xf[2 * i + 1] = make_float4(f[4], f[5], f[6], f[7]);
+        });
+        __syncthreads();
+        const bool live = e < a.E;     // warps past E stay for the selection below
+        constexpr int kDepth = 8;                 // weight chunks in flight per lane
+        for (int c0 = lane; live && c0 < H8; c0 += 32 * kDepth) {
+            uint4 wq[kDepth];
+#pragma unroll
+            for (int q = 0; q < kDepth; q++) {
+                const int c = c0 + 32 * q;
+                wq[q] = c < H8 ? ldg_stream_v4(wrow + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int q = 0; q < kDepth; q++) {
+            const int c = c0 + 32 * q;
+            if (c >= H8) break;
+            float wf[8];
+            bf16x8_to_f32(wq[q], wf);
+#pragma unroll
+            for (int t = 0; t < TPC; t++) {
+                if (t < nt) {
+                    const float4 x0 = s_xf[(t * H8 + c) * 2], x1 = s_xf[(t * H8 + c) * 2 + 1];
+                    acc[t] = fmaf(wf[0], x0.x, acc[t]);
+                    acc[t] = fmaf(wf[1], x0.y, acc[t]);
+                    acc[t] = fmaf(wf[2], x0.z, acc[t]);
+                    acc[t] = fmaf(wf[3], x0.w, acc[t]);
+                    acc[t] = fmaf(wf[4], x1.x, acc[t]);
+                    acc[t] = fmaf(wf[5], x1.y, acc[t]);
+                    acc[t] = fmaf(wf[6], x1.z, acc[t]);
+                    acc[t] = fmaf(wf[7], x1.w, acc[t]);
+                }
+            }
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < TPC; t++) {
+        if (t < nt) {
+            const float v = warp_sum(acc[t]);
+            if (lane == 0 && e < a.E) a.logits[(size_t)(t0 + t) * a.E + e] = v;
+        }
+    }
+    if (!a.tickets) return;
+    // the last CTA of this token tile to finish selects its tokens' top-k: the
+    // logits are made visible before the ticket is taken, and the counter is
+    // cleared for the next launch (whose CTAs take tickets only after this
+    // grid has completed, behind their griddepcontrol.wait)
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(a.tickets + blockIdx.y, 1) == (int)gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (warp < nt) select_token_any(a, t0 + warp, lane);
+    if (threadIdx.x == 0) a.tickets[blockIdx.y] = 0;
 }
 
 // ------------------------------------------------ tensor-core batch path

@@ -108,3 +108,33 @@ def test_router_then_layer_matches_oracle():
         assert_close(y.cpu().numpy(), ref, "router -> layer")
     finally:
         L.close()
+
+
+@pytest.mark.parametrize("E", [130, 384, 1000])
+def test_single_launch_router_repeats_and_ragged_expert_rows(E):
+    """At T <= 8 one launch computes the logits and, in the last CTA of each
+    token tile, the selection (a per-tile counter cleared by that CTA): many
+    calls in a row on one handle, T varying, E not a multiple of the CTA's
+    warps (idle warps in the last CTA), each equal to the oracle's selection
+    of the GPU's logits."""
+    H, k = 512, 6
+    W = synth.router_weights_bf16(E, H, layer=2)
+    h = _handle(E, H, k, 8)
+    try:
+        wd = torch.from_numpy(W.view(np.int16)).cuda()
+        for step, T in enumerate([1, 3, 8, 2, 1, 5, 8, 4]):
+            x = synth.activations_bf16(T, H, seed=70 + step)
+            xd = torch.from_numpy(x.view(np.int16)).cuda()
+            logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+            idx = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+            w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+            moe.moe_router_topk(h, xd, wd, T, idx, w, logits=logits)
+            torch.cuda.synchronize()
+            got_l = logits.cpu().numpy().astype(np.float64)
+            assert np.abs(got_l - oracle.router_logits(x, W)).max() <= 1e-5
+            ci, cw = oracle.topk_softmax(got_l, k)
+            assert np.array_equal(idx.cpu().numpy(), ci), f"step {step}, T {T}"
+            assert np.abs(w.cpu().numpy() - cw).max() <= 2e-6
+        assert moe.moe_ffn_status(h) == moe.MOE_OK
+    finally:
+        moe.moe_ffn_destroy(h)
