@@ -939,7 +939,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(GemvArgs a, StreamPlan p0
             if (!ji.ok) atomicOr(a.status, kStatusBadIndex);
         }
     } else {
-        // routing weights of the slots (inputs of the layer, not of the previous kernel)
+        // routing weights of the slots: inputs of the call, complete before its
+        // first kernel may start (their producers let dependents launch only at
+        // completion), so they are read before griddepcontrol.wait
         const int slots = min(a.T * a.topk, kSlotCache);
         for (int j = threadIdx.x - 32; j < slots; j += kThreads - 32) {
             const int e = a.idx[j];

@@ -12,6 +12,9 @@
 //                    reproducible.  Given a ticket counter per token tile,
 //                    the last CTA of the tile to finish also runs the
 //                    selection below for its tokens: one launch per call.
+// A kernel that writes topk_idx / topk_w never lets its dependents launch early
+// (no griddepcontrol.launch_dependents): the layer's kernels resolve expert
+// pointers from topk_idx before their own griddepcontrol.wait.
 //   k_router_select  one warp per token: the logits as order keys in
 //                    registers, k rounds of a warp arg-max under the order
 //                    "larger logit first, NaN after every number, ties to the
@@ -181,7 +184,8 @@ __global__ void __launch_bounds__(256) k_router_select(RouterArgs a)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     pdl_wait();
-    pdl_trigger();
+    // no early launch_dependents: the next kernel may read topk_idx / topk_w
+    // before its own griddepcontrol.wait, so it starts only once they are written
     if (t >= a.T) return;
     select_token<R>(a, t, lane);
 }
@@ -223,7 +227,7 @@ __global__ void __launch_bounds__(NW * 32) k_router_logits(RouterArgs a)
             wv[i] = c < H8 ? ldg_stream_v4(wrow + c) : make_uint4(0, 0, 0, 0);
         }
         pdl_wait();
-        pdl_trigger();
+        if (!a.tickets) pdl_trigger();     // selecting here: dependents start at completion
         stage_x(reinterpret_cast<const uint4*>(a.x + (size_t)t0 * a.H), nt * H8,
                 [&](int i, const uint4 v) { s_x[i] = v; });
         __syncthreads();
@@ -247,7 +251,7 @@ __global__ void __launch_bounds__(NW * 32) k_router_logits(RouterArgs a)
         // fp32 once per CTA ([TPC][H]) and the weights stream
         float4* s_xf = reinterpret_cast<float4*>(s_x);
         pdl_wait();
-        pdl_trigger();
+        if (!a.tickets) pdl_trigger();     // selecting here: dependents start at completion
         stage_x(reinterpret_cast<const uint4*>(a.x + (size_t)t0 * a.H), nt * H8, [&](int i, const uint4 v) {
             float f[8];
             bf16x8_to_f32(v, f);

@@ -133,7 +133,13 @@ int moe_ffn_pack_expert(moe_ffn_t h, const void* canon_codes, const void* canon_
  *   tbl      host struct of device pointer arrays (see moe_expert_table)
  *   y        device [T][H], bf16 or fp32 per cfg.out_dtype; y must not alias x
  * y[t] = sum_{k} topk_w[t,k] * FFN_{topk_idx[t,k]}(x[t]).  Deterministic:
- * repeated calls give bitwise identical y. */
+ * repeated calls give bitwise identical y.  The layer's first kernels read
+ * topk_idx, topk_w and the expert table before they wait for the stream's
+ * previous kernel (programmatic dependent launch), so these must be written by
+ * stream work that completes before a dependent launch may begin: an ordinary
+ * kernel or copy, or moe_router_topk / moe_router_select (which let the next
+ * launch start only once their outputs are written) -- not by a kernel that
+ * lets dependents launch early. */
 int moe_ffn_forward(moe_ffn_t h, const void* x, const int32_t* topk_idx, const float* topk_w,
                     const moe_expert_table* tbl, void* y, int T, void* stream);
 

@@ -138,3 +138,41 @@ def test_single_launch_router_repeats_and_ragged_expert_rows(E):
         assert moe.moe_ffn_status(h) == moe.MOE_OK
     finally:
         moe.moe_ffn_destroy(h)
+
+
+@pytest.mark.parametrize("T", [1, 4, 20])
+def test_router_feeds_layer_on_one_stream_without_waits(T):
+    """Router then layer, step after step on one stream with no host wait, the
+    routing buffers reused: the layer's first kernels read topk_idx before
+    their griddepcontrol.wait, so the router must let them start only after
+    it has written it.  Each step's y equals a later, synchronized forward of
+    the same step's routing, bit for bit."""
+    E, H, I, k = 16, 4096, 2880, 6
+    L = Layer(E=E, H=H, I=I, k=k, max_tokens=T, path="auto")
+    s = torch.cuda.Stream()
+    try:
+        Wd = torch.from_numpy(synth.router_weights_bf16(E, H, layer=3).view(np.int16)).cuda()
+        idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        steps = 6
+        xs = [torch.from_numpy(synth.activations_bf16(T, H, seed=90 + i).view(np.int16)).cuda() for i in range(steps)]
+        ys = [torch.empty((T, H), dtype=torch.float32, device="cuda") for _ in range(steps)]
+        idx_s = [torch.empty_like(idx) for _ in range(steps)]
+        w_s = [torch.empty_like(w) for _ in range(steps)]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            for i in range(steps):
+                moe.moe_router_topk(L.h, xs[i], Wd, T, idx, w, stream=s)
+                moe.moe_ffn_forward(L.h, xs[i], idx, w, L.es.table, ys[i], T, s)
+                idx_s[i].copy_(idx)
+                w_s[i].copy_(w)
+        s.synchronize()
+        for i in range(steps):
+            y_ref = torch.empty_like(ys[i])
+            moe.moe_ffn_forward(L.h, xs[i], idx_s[i], w_s[i], L.es.table, y_ref, T)
+            torch.cuda.synchronize()
+            assert torch.equal(ys[i].view(torch.int32), y_ref.view(torch.int32)), f"step {i}"
+        assert len({tuple(t.cpu().numpy().ravel()) for t in idx_s}) > 1       # the routing did change
+        assert moe.moe_ffn_status(L.h) == moe.MOE_OK
+    finally:
+        L.close()
