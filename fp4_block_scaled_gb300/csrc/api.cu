@@ -34,6 +34,21 @@ struct HostGraph {
     unsigned long long last_use;
 };
 
+// A handle keeps at most this many cached graphs of each kind; the least
+// recently used one makes room for a new one.
+constexpr size_t kMaxGraphs = 8;
+
+template <class G>
+void evict_lru_graph(std::vector<G>& graphs)
+{
+    if (graphs.size() < kMaxGraphs) return;
+    size_t v = 0;
+    for (size_t i = 1; i < graphs.size(); i++)
+        if (graphs[i].last_use < graphs[v].last_use) v = i;
+    cudaGraphExecDestroy(graphs[v].exec);
+    graphs.erase(graphs.begin() + (long)v);
+}
+
 }  // namespace
 
 struct moe_ffn {
@@ -416,13 +431,7 @@ int moe_ffn_forward_host(moe_ffn_t h, const void* x_host, const int32_t* idx_hos
             e = cudaGraphInstantiate(&exec, graph, 0);
             cudaGraphDestroy(graph);
             if (e != cudaSuccess) return MOE_ERR_CUDA;
-            if (h->hgraphs.size() >= 8) {  // evict the least recently used graph
-                size_t v = 0;
-                for (size_t i = 1; i < h->hgraphs.size(); i++)
-                    if (h->hgraphs[i].last_use < h->hgraphs[v].last_use) v = i;
-                cudaGraphExecDestroy(h->hgraphs[v].exec);
-                h->hgraphs.erase(h->hgraphs.begin() + (long)v);
-            }
+            evict_lru_graph(h->hgraphs);
             h->hgraphs.push_back(HostGraph{T, tbl->experts, exec, 0});
             g = &h->hgraphs.back();
         }
@@ -556,13 +565,7 @@ int moe_stack_forward(moe_ffn_t h, float* x, const moe_expert_table* tbls,
     e = cudaGraphInstantiate(&exec, graph, 0);
     cudaGraphDestroy(graph);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    if (h->graphs.size() >= 8) {  // evict the least recently used graph
-        size_t v = 0;
-        for (size_t i = 1; i < h->graphs.size(); i++)
-            if (h->graphs[i].last_use < h->graphs[v].last_use) v = i;
-        cudaGraphExecDestroy(h->graphs[v].exec);
-        h->graphs.erase(h->graphs.begin() + (long)v);
-    }
+    evict_lru_graph(h->graphs);
     h->graphs.push_back(StackGraph{x, topk_idx, topk_w, L, T, key, exec, h->use_clock});
     return cuda_rc(cudaGraphLaunch(exec, s));
 }
