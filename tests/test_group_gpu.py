@@ -166,3 +166,20 @@ def test_full_size_batch64_e4m3_grouped_all_tokens():
         assert np.array_equal(y, L.run(x, idx, w).cpu().numpy())
     finally:
         L.close()
+
+
+@pytest.mark.parametrize("path,T", [("slot", 1), ("slot", 5), ("group", 3), ("group", 20)])
+@pytest.mark.parametrize("E,k", [(1, 1), (8, 8)])
+@pytest.mark.parametrize("act", [moe.MOE_ACT_BF16, E4M3])
+def test_degenerate_routing_shapes(E, k, path, T, act):
+    """A single expert chosen by every token (E = k = 1: one group of all the
+    slots on the expert-major path), and every expert chosen by every token
+    (k = E = 8): both paths against the oracle."""
+    L = Layer(E=E, H=256, I=128, k=k, max_tokens=24, act=act, path=path)
+    try:
+        x, idx, w = inputs(T, E, 256, k, seed=300 + 10 * E + T)
+        assert sorted(idx[0].tolist()) == list(range(E)) if k == E else True
+        assert_close(L.run(x, idx, w).cpu().numpy(), L.oracle(x, idx, w), f"E={E} k={k} {path} T={T} act={act}")
+        assert moe.moe_ffn_status(L.h) == moe.MOE_OK
+    finally:
+        L.close()
