@@ -184,16 +184,17 @@ def test_out_of_range_expert_contributes_zero_and_sets_status():
         L.close()
 
 
+@pytest.mark.parametrize("act", [moe.MOE_ACT_BF16, moe.MOE_ACT_E4M3_UE8M0_128, moe.MOE_ACT_E2M1_UE8M0_32])
 @pytest.mark.parametrize("shape", ["tiny", "wide"])
 @pytest.mark.parametrize("out", [moe.MOE_OUT_F32, moe.MOE_OUT_BF16])
-def test_forward_host_equals_forward(out, shape):
+def test_forward_host_equals_forward(out, shape, act):
     """The host-buffer call equals the device call on both paths, over
     repeated calls with new inputs, several T and profiling mode.  Small
     batches go through the staging buffer and a graph per (T, table)
     (replayed and re-keyed here); with hidden 4096 the batches of 20 and 24
     take the direct copies."""
     cfg = TINY if shape == "tiny" else dict(E=8, H=4096, I=128, k=2)
-    L = Layer(**cfg, max_tokens=24, out=out, path="auto")
+    L = Layer(**cfg, max_tokens=24, out=out, path="auto", act=act)
     try:
         for step, T in enumerate([3, 1, 3, 20, 1, 24, 3]):
             x, idx, w = inputs(T, cfg["E"], cfg["H"], cfg["k"], seed=40 + step)
