@@ -193,9 +193,10 @@ def source_fingerprint(path):
     return hashlib.sha256(re.sub(r"\s+", "", text).encode()).hexdigest()
 
 
-def traffic_record(kernel, workload, algorithmic_bytes):
+def traffic_record(kernel, workload, act, algorithmic_bytes):
     """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source and on this workload's launch shape (else None):
+    the current kernel source, on this workload's launch shape and in this
+    activation mode (else None):
     the captured bytes, or the captured dram/algorithmic ratio times this
     workload's algorithmic bytes per launch."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -204,7 +205,7 @@ def traffic_record(kernel, workload, algorithmic_bytes):
     with open(p) as f:
         d = json.load(f)
     rec = d.get(kernel)
-    if not rec or workload not in rec.get("workloads", []):
+    if not rec or workload not in rec.get("workloads", []) or act != rec.get("activations"):
         return None
     src = os.path.join(ROOT, rec["source"])
     if not os.path.exists(src):
@@ -504,7 +505,7 @@ def run_ours(args, wl):
     co_ms = ms_ph[moe.MOE_PHASE_DOWN] / max(1, n_ph[moe.MOE_PHASE_DOWN])
     ly_bytes = sum(distinct(i, 0) for i in range(nprof)) / nprof * expert_bytes(H, I) + act_io
     achieved = ly_bytes / (ly_ms / 1000.0) / 1e9
-    traffic = traffic_record(kernel, args.workload, ly_bytes)
+    traffic = traffic_record(kernel, args.workload, wl["act"], ly_bytes)
 
     # ---- the router ahead of the path (logits = W x, top-k, softmax): one
     # launch per call up to 8 tokens, two above; timed (a) back to back in a CUDA graph of nrg calls,
