@@ -36,7 +36,7 @@ EXPORTS = [
     "moe_ffn_status", "moe_ffn_strerror", "moe_ffn_destroy", "moe_ffn_forward_noalloc",
     "moe_router_topk", "moe_router_select", "moe_batch_plan", "moe_batch_distinct",
     "moe_expert_cache_create", "moe_expert_cache_fetch", "moe_expert_cache_prefetch", "moe_expert_cache_slot",
-    "moe_expert_cache_stats", "moe_expert_cache_destroy",
+    "moe_expert_cache_stats", "moe_expert_cache_destroy", "moe_ffn_test_set_wait", "moe_ffn_test_fail_allocs",
 ]
 
 MOE_PHASE_PREP = 0
@@ -106,6 +106,8 @@ def lib() -> ctypes.CDLL:
             "moe_expert_cache_stats": (I, [P, ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong),
                                            ctypes.POINTER(ctypes.c_longlong)]),
             "moe_expert_cache_destroy": (None, [P]),
+            "moe_ffn_test_set_wait": (I, [P, ctypes.c_ulonglong, I]),
+            "moe_ffn_test_fail_allocs": (None, [I]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -227,6 +229,17 @@ def moe_ffn_forward_noalloc(cfg: moe_ffn_config, device: int, x, topk_idx, topk_
     _check(lib().moe_ffn_forward_noalloc(ctypes.byref(cfg), int(device), _p(x), _p(topk_idx),
                                          _p(topk_w), ctypes.byref(table), _p(y), int(T),
                                          _p(status), _s(stream)), "moe_ffn_forward_noalloc")
+
+
+def moe_ffn_test_set_wait(h, wait_ns: int, withhold: bool) -> None:
+    """Test hook: bounded-wait limit of the slot-major kernel and the withheld
+    partial sums that make its waits run out (see include/moe_ffn.h)."""
+    _check(lib().moe_ffn_test_set_wait(h, int(wait_ns), 1 if withhold else 0), "moe_ffn_test_set_wait")
+
+
+def moe_ffn_test_fail_allocs(n: int) -> None:
+    """Test hook: the library's next n allocations fail as if out of memory."""
+    lib().moe_ffn_test_fail_allocs(int(n))
 
 
 def moe_ffn_destroy(h) -> None:

@@ -4,6 +4,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <new>
 #include <vector>
 
@@ -191,6 +192,36 @@ int run_forward(moe_ffn* h, const void* x, const int32_t* idx, const float* w,
 
 int moe::check_config(const moe_ffn_config* cfg) { return check_cfg(cfg); }
 
+namespace {
+std::atomic<int> g_fail_allocs{0};    // test hook: this many allocations still to fail
+
+bool fail_this_alloc()
+{
+    int n = g_fail_allocs.load();
+    while (n > 0)
+        if (g_fail_allocs.compare_exchange_weak(n, n - 1)) return true;
+    return false;
+}
+}  // namespace
+
+cudaError_t moe::lib_malloc(void** p, size_t bytes)
+{
+    if (fail_this_alloc()) {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMalloc(p, bytes);
+}
+
+cudaError_t moe::lib_host_alloc(void** p, size_t bytes, unsigned flags)
+{
+    if (fail_this_alloc()) {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaHostAlloc(p, bytes, flags);
+}
+
 extern "C" {
 
 size_t moe_ffn_packed_expert_bytes(const moe_ffn_config* cfg)
@@ -251,7 +282,7 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     size_t o_rpart = take(rpart_bytes);
     size_t o_inst = take(host_in_bytes(T, H, k)), o_yst = take((size_t)T * H * 4);
     h->ws_bytes = off;
-    if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
+    if (lib_malloc(&h->ws, h->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
         delete h;
         return MOE_ERR_OOM;
@@ -385,7 +416,7 @@ int moe_ffn_forward_host(moe_ffn_t h, const void* x_host, const int32_t* idx_hos
     if (!h->host_stage) {
         void* p = nullptr;
         void* d = nullptr;
-        if (cudaHostAlloc(&p, yo + (size_t)Tst * ytok, cudaHostAllocMapped) != cudaSuccess) {
+        if (lib_host_alloc(&p, yo + (size_t)Tst * ytok, cudaHostAllocMapped) != cudaSuccess) {
             cudaGetLastError();
             return MOE_ERR_OOM;
         }
@@ -568,6 +599,16 @@ int moe_stack_forward(moe_ffn_t h, float* x, const moe_expert_table* tbls,
     evict_lru_graph(h->graphs);
     h->graphs.push_back(StackGraph{x, topk_idx, topk_w, L, T, key, exec, h->use_clock});
     return cuda_rc(cudaGraphLaunch(exec, s));
+}
+
+void moe_ffn_test_fail_allocs(int n) { g_fail_allocs.store(n > 0 ? n : 0); }
+
+int moe_ffn_test_set_wait(moe_ffn_t h, unsigned long long wait_ns, int withhold)
+{
+    if (!h) return MOE_ERR_INVALID_ARG;
+    h->base.wait_ns = wait_ns;
+    h->base.debug_withhold = withhold ? 1 : 0;
+    return MOE_OK;
 }
 
 int moe_ffn_status(moe_ffn_t h, void* stream)

@@ -31,6 +31,7 @@
 #include <vector>
 
 #include "../../include/moe_ffn.h"
+#include "internal.h"
 
 namespace {
 constexpr int kCopyStreams = 4;
@@ -203,8 +204,8 @@ extern "C" int moe_expert_cache_create(const moe_ffn_config* cfg, int device, co
     c->released.assign((size_t)slots, nullptr);
     c->filled.assign((size_t)slots, nullptr);
     c->ever_used.assign((size_t)slots, 0);
-    bool ok = cudaMalloc(&c->dev, c->stride * (size_t)slots) == cudaSuccess;
-    ok = ok && cudaMalloc(&c->dtable, sizeof(void*) * (size_t)c->E) == cudaSuccess;
+    bool ok = moe::lib_malloc((void**)&c->dev, c->stride * (size_t)slots) == cudaSuccess;
+    ok = ok && moe::lib_malloc((void**)&c->dtable, sizeof(void*) * (size_t)c->E) == cudaSuccess;
     for (int i = 0; ok && i < kCopyStreams; i++) {
         ok = cudaStreamCreateWithFlags(&c->copy[i], cudaStreamNonBlocking) == cudaSuccess;
         ok = ok && cudaEventCreateWithFlags(&c->copied[i], cudaEventDisableTiming) == cudaSuccess;
@@ -214,7 +215,7 @@ extern "C" int moe_expert_cache_create(const moe_ffn_config* cfg, int device, co
         ok = ok && cudaEventCreateWithFlags(&c->filled[s], cudaEventDisableTiming) == cudaSuccess;
     }
     for (int i = 0; ok && i < moe_expert_cache_s::kRing; i++) {
-        ok = cudaMallocHost((void**)&c->stage[i], sizeof(void*) * (size_t)c->E) == cudaSuccess;
+        ok = moe::lib_host_alloc((void**)&c->stage[i], sizeof(void*) * (size_t)c->E, cudaHostAllocDefault) == cudaSuccess;
         ok = ok && cudaEventCreateWithFlags(&c->stage_ev[i], cudaEventDisableTiming) == cudaSuccess;
         if (ok) ok = cudaEventRecord(c->stage_ev[i], 0) == cudaSuccess;
     }

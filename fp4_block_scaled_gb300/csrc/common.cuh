@@ -7,31 +7,6 @@
 
 namespace moe {
 
-// Four bytes of a word, each holding two E2M1 codes (low nibble = even
-// element), to four f16x2 registers (low half = low nibble).  The hardware
-// conversion is exact: every E2M1 value is an f16 value.
-__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&o)[4])
-{
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-        : "r"(w));
-}
-
-// D += A(16x16, f16) * B(16x8, f16), fp32 accumulate.
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                          uint32_t a3, uint32_t b0, uint32_t b1)
-{
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // Streaming read-only loads: weights are read once per call, so keep them out of L1.
 __device__ __forceinline__ uint4 ldg_stream_v4(const void* p)
 {
@@ -42,42 +17,8 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* p)
     return r;
 }
 
-__device__ __forceinline__ uint2 ldg_stream_v2(const void* p)
-{
-    uint2 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
-                 : "=r"(r.x), "=r"(r.y)
-                 : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t ldg_stream_u32(const void* p)
-{
-    uint32_t r;
-    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
-    return r;
-}
-
-// ue8m0 byte -> 2^(s-127) as fp32 by placing s in the exponent field.  Exact
-// for s in 1..254; s = 0 (2^-127, below the fp32 normal range) gives 0 and
-// s = 255 (NaN) gives +inf, which still poisons the result.
-__device__ __forceinline__ float ue8m0_f32(uint32_t s) { return __uint_as_float(s << 23); }
-
-__device__ __forceinline__ uint32_t byte_of(uint32_t w, int i) { return (w >> (8 * i)) & 0xFFu; }
-
 // 2^e as fp32 for e in [-126, 127].
 __device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
-
-// Exponent a such that amax * 2^-a lies in [2^14, 2^15): f16 then holds the
-// block's largest element with full precision and cannot overflow.
-__device__ __forceinline__ int f16_block_exponent(float amax)
-{
-    uint32_t b = __float_as_uint(amax);
-    int e = (int)((b >> 23) & 0xFF) - 127;
-    if (amax == 0.0f || e == 128) return 0;  // zero block, or inf/NaN (propagates)
-    int a = e - 14;
-    return a < -110 ? -110 : (a > 110 ? 110 : a);
-}
 
 __device__ __forceinline__ float warp_max(float v)
 {
@@ -98,11 +39,6 @@ __device__ __forceinline__ float warp_sum(float v)
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
 // ---------------------------------------------------------------- mbarrier / bulk copy
@@ -111,6 +47,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
+
+// Deadlines of the bounded waits count SM clock cycles (a per-SM counter that
+// costs nothing to read), at 2 cycles per nanosecond: a wait gives up after
+// its limit at 2 GHz and proportionally later at lower clocks.
+__device__ __forceinline__ uint64_t wait_clock() { return (uint64_t)clock64(); }
+__device__ __forceinline__ uint64_t wait_cycles(uint64_t ns) { return 2 * ns; }
 
 __device__ __forceinline__ uint64_t globaltimer_ns()
 {
@@ -136,6 +78,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// Adds tx bytes to the current phase of `bar` without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -154,14 +102,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended in hardware for up to
+// hint_ns while the phase is not complete (it resumes as soon as it
+// completes), so that waiting threads leave the issue slots to working warps.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kWaitSleepNs = 2000;   // suspend-time hint of one try in the bounded waits
+
 // Wait for the phase of `bar` with the given parity to complete, for at most
 // limit_ns of wall time.  Returns false if it gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (globaltimer_ns() - t0 > limit_ns) return false;
+    const uint64_t t0 = wait_clock(), lim = wait_cycles(limit_ns);
+#ifdef MOE_WAIT_BACKOFF
+    while (!mbar_try_wait(bar, parity)) {
+        __nanosleep(64);
+        if (wait_clock() - t0 > lim) return false;
+    }
+#else
+    while (!mbar_try_wait_sleep(bar, parity, kWaitSleepNs))
+        if (wait_clock() - t0 > lim) return false;
+#endif
     return true;
 }
 
@@ -170,9 +143,16 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
                                                    uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (*(const volatile int*)abort || globaltimer_ns() - t0 > limit_ns) return false;
+    const uint64_t t0 = wait_clock(), lim = wait_cycles(limit_ns);
+#ifdef MOE_WAIT_BACKOFF
+    while (!mbar_try_wait(bar, parity)) {
+        __nanosleep(64);
+        if (*(const volatile int*)abort || wait_clock() - t0 > lim) return false;
+    }
+#else
+    while (!mbar_try_wait_sleep(bar, parity, kWaitSleepNs))
+        if (*(const volatile int*)abort || wait_clock() - t0 > lim) return false;
+#endif
     return true;
 }
 
@@ -270,6 +250,56 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16])
 #pragma unroll
     for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
+
+// Warp-collective, without waiting: 64 / 16 consecutive 32-bit TMEM columns
+// of this warp's 32 lanes into raw registers; tc_wait_ld() completes every
+// load issued so far (the registers may not be read before it).
+__device__ __forceinline__ void tc_ld64_nowait(uint32_t taddr, uint32_t (&r)[64])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,"
+        "%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tc_ld16_nowait(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Marks registers a non-waiting TMEM load wrote as read only after
+// tc_wait_ld(): each passes through an empty volatile asm placed after it, so
+// the compiler cannot move a use above the wait.
+template <int N>
+__device__ __forceinline__ void tc_ld_fence_regs(uint32_t (&r)[N])
+{
+#pragma unroll
+    for (int i = 0; i < N; i++) asm volatile("" : "+r"(r[i]));
+}
+
+// Warp-collective: one 32-bit TMEM column of this warp's 32 lanes from r;
+// tc_wait_st() completes the stores issued so far.
+__device__ __forceinline__ void tc_st1(uint32_t taddr, float v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(__float_as_uint(v)) : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Warp-collective: 8 consecutive 32-bit TMEM columns of this warp's 32 lanes.
 __device__ __forceinline__ void tc_ld8(uint32_t taddr, float (&v)[8])

@@ -75,7 +75,7 @@ constexpr int kTmemCols = 512;
 constexpr int kAccCols = 16;                                 // N = 16 fp32 columns
 constexpr int kIssuers = kCU;                                // MMA-issuing warps, one unit of a stage each
 constexpr int kSfCol0 = kIssuers * 2 * kAccCols;             // scale atoms after the accumulators
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 constexpr int kWarpEpi0 = 1 + kIssuers;                      // first of the 4 epilogue warps
 constexpr int kWarpLoader = kWarpEpi0 + 4;                   // activation copies
 constexpr int kThreads = (kWarpLoader + 1) * 32;
@@ -124,6 +124,10 @@ static_assert(kPieces == kAccCols && kBRows == kAccCols, "one accumulator column
 // tensor-memory allocation: the dynamic shared memory asked for is at least
 // more than half of an SM's.
 constexpr size_t kOneCtaPerSmSmem = 116 * 1024;
+// activation numerics, one instance of the layer kernel each (each instance
+// holds only its own mode's code, which keeps the kernel small: its code
+// competes for the instruction caches with the weight stream)
+enum : int { kModeBf16 = 0, kModeE4m3 = 1, kModeE2m1 = 2 };
 
 struct JobInfo {
     const uint8_t* w;       // unit 0 of this job's weight tile (codes + scale atom per unit)
@@ -210,6 +214,43 @@ __device__ __forceinline__ void write_pieces64(float v0, float v1, int lane, uin
         w[p >> 2] |= (byte & 0xFFu) << (8 * (p & 3));
     }
     scratch[lane] = make_uint4(w[0], w[1], w[2], w[3]);
+    __syncwarp();
+    const uint8_t* sb = reinterpret_cast<const uint8_t*>(scratch + (lane & 16));   // this half-warp's lanes
+    uint32_t row[4];
+#pragma unroll
+    for (int q = 0; q < 4; q++)
+        row[q] = (uint32_t)sb[(4 * q) * 16 + i] | ((uint32_t)sb[(4 * q + 1) * 16 + i] << 8) |
+                 ((uint32_t)sb[(4 * q + 2) * 16 + i] << 16) | ((uint32_t)sb[(4 * q + 3) * 16 + i] << 24);
+    __syncwarp();                                  // scratch free again
+    uint8_t* dst = Bunit + (bu >> 1) * kMmaBBytes + (bu & 1) * 128 + (i >> 3) * 256 + (i & 7) * 16;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(row[0], row[1], row[2], row[3]);
+    Bsf[i * 16 + bu] = (uint8_t)max(s0 - 2 * i, 1);
+}
+
+// write_pieces64 with the piece loop rolled: the layer kernel's copy has to
+// stay small, since its code competes for the instruction caches with the
+// weight stream (each piece byte goes to the transpose buffer as it comes).
+__device__ __forceinline__ void write_pieces64_small(float v0, float v1, int lane, uint8_t* Bunit, uint8_t* Bsf,
+                                                     int blk0, uint4* scratch)
+{
+    const int bu = (blk0 & 3) + (lane >> 4);
+    const int i = lane & 15;
+    float amax = fmaxf(fabsf(v0), fabsf(v1));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const int s0 = e2m1_scale_byte(amax);
+    float r0 = v0, r1 = v1;
+    uint8_t* mine = reinterpret_cast<uint8_t*>(scratch + lane);
+#pragma unroll 1
+    for (int p = 0; p < kPieces; p++) {
+        const int s = max(s0 - 2 * p, 1);
+        const float down = exp2i(127 - s), up = exp2i(s - 127);
+        const uint32_t byte = f32x2_to_e2m1x2(r0 * down, r1 * down);
+        const float2 d = e2m1x2_to_f32x2(byte);
+        r0 = fmaf(-d.x, up, r0);
+        r1 = fmaf(-d.y, up, r1);
+        mine[p] = (uint8_t)byte;
+    }
     __syncwarp();
     const uint8_t* sb = reinterpret_cast<const uint8_t*>(scratch + (lane & 16));   // this half-warp's lanes
     uint32_t row[4];
@@ -314,6 +355,9 @@ __global__ void __launch_bounds__(256) k_prep(GemvArgs a)
 }
 
 // ----------------------------------------------------------------- k_layer
+
+// Limit of every bounded wait of the launch.
+__device__ __forceinline__ uint64_t wait_limit(const GemvArgs& a) { return a.wait_ns ? a.wait_ns : kDefaultWaitNs; }
 
 // The slot j and weight tile of a job.
 template <int PHASE>
@@ -477,7 +521,7 @@ __device__ bool produce(const GemvArgs& a, const StreamPlan& p, const Range& r, 
         const uint32_t bb = nfull * kUnitBBytes + (has_half ? kMmaBBytes : 0);
         const uint32_t bsb = nun * kUnitSfBytes;
         const int s = n % kStages;
-        if (n >= kStages && !mbar_wait_or_abort(&sm.empty[s], ((n / kStages) & 1) ^ 1, &sm.abort, kWaitLimitNs)) {
+        if (n >= kStages && !mbar_wait_or_abort(&sm.empty[s], ((n / kStages) & 1) ^ 1, &sm.abort, wait_limit(a))) {
             set_abort(a, sm);
             return false;
         }
@@ -522,10 +566,12 @@ __device__ bool publish_own_groups(const GemvArgs& a, TcSmem& sm, uint32_t owned
 {
     uint32_t cnt = 0, pub = 0;
     uint64_t t0 = 0;
+    // test hook: the first CTA keeps its groups back, so the others' waits run out
+    const bool withhold = a.debug_withhold && blockIdx.x == 0;
     while (cnt < owned) {
         const unsigned long long w = ld_acquire_cta_u64(&sm.fin_word);
         const uint32_t c = (uint32_t)(w >> 32), d = (uint32_t)w;
-        if (d > pub) {
+        if (d > pub && !withhold) {
             asm volatile("fence.proxy.async.global;" ::: "memory");
             asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(a.sync), "r"(d - pub) : "memory");
             pub = d;
@@ -536,8 +582,8 @@ __device__ bool publish_own_groups(const GemvArgs& a, TcSmem& sm, uint32_t owned
             continue;
         }
         if (*(volatile int*)&sm.abort) return false;
-        if (t0 == 0) t0 = globaltimer_ns();
-        else if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (t0 == 0) t0 = wait_clock();
+        else if (wait_clock() - t0 > wait_cycles(wait_limit(a))) return false;
     }
     return true;
 }
@@ -547,7 +593,7 @@ __device__ void load_b(const GemvArgs& a, int nchunks, uint32_t gu_groups, uint3
     bool pdl_done = false, h_done = false, published = false;
     for (int n = 0; n < nchunks; n++) {
         const int s = n % kStages;
-        if (!mbar_wait_or_abort(&sm.posted[s], (n / kStages) & 1, &sm.abort, kWaitLimitNs)) {
+        if (!mbar_wait_or_abort(&sm.posted[s], (n / kStages) & 1, &sm.abort, wait_limit(a))) {
             set_abort(a, sm);
             return;
         }
@@ -566,9 +612,9 @@ __device__ void load_b(const GemvArgs& a, int nchunks, uint32_t gu_groups, uint3
         if (q.phase == 1 && !h_done) {
             bool ok = ld_acquire_u32(a.sync) >= gu_groups;
             if (!ok) {
-                const uint64_t t0 = globaltimer_ns();
+                const uint64_t t0 = wait_clock();
                 while (!(ok = ld_acquire_u32(a.sync) >= gu_groups))
-                    if (*(volatile int*)&sm.abort || globaltimer_ns() - t0 > kWaitLimitNs) break;
+                    if (*(volatile int*)&sm.abort || wait_clock() - t0 > wait_cycles(wait_limit(a))) break;
             }
             TC_CTA(3);
             // h was written with generic stores; the copies read it through the async proxy
@@ -608,13 +654,13 @@ __device__ void issue(const GemvArgs& a, const StreamPlan& p, const Range& r, Tc
         if (group_start) {
             // the epilogue must have read this accumulator's previous group
             if (!is.abort && is.use[is.buf] > 0 &&
-                !mbar_wait_or_abort(&sm.acc_empty[is.buf], (is.use[is.buf] - 1) & 1, &sm.abort, kWaitLimitNs)) {
+                !mbar_wait_or_abort(&sm.acc_empty[is.buf], (is.use[is.buf] - 1) & 1, &sm.abort, wait_limit(a))) {
                 set_abort(a, sm);
                 is.abort = true;
             }
             group_start = false;
         }
-        if (!is.abort && !mbar_wait_or_abort(&sm.full[s], (is.n / kStages) & 1, &sm.abort, kWaitLimitNs)) {
+        if (!is.abort && !mbar_wait_or_abort(&sm.full[s], (is.n / kStages) & 1, &sm.abort, wait_limit(a))) {
             set_abort(a, sm);
             is.abort = true;
         }
@@ -671,6 +717,7 @@ __device__ __forceinline__ void fin_signal(TcSmem& sm, int lane, uint32_t done)
                      : "memory");
 }
 
+template <int MODE>
 __device__ __forceinline__ void finalize_gate_up(const GemvArgs& a, const StreamPlan& p, TcSmem& sm,
                                                  uint32_t group, const float* comb, int lane, int tr_warp)
 {
@@ -683,12 +730,12 @@ __device__ __forceinline__ void finalize_gate_up(const GemvArgs& a, const Stream
     const float2 u = *reinterpret_cast<const float2*>(comb + 64 + 2 * lane);
     float h0 = silu(g.x) * u.x, h1 = silu(g.y) * u.y;
     int done = 1;                         // tiles of h whose pieces this call writes
-    if (a.act_e2m1) {                     // h quantized to E2M1 per 32 along I, before w
+    if (MODE == kModeE2m1) {                     // h quantized to E2M1 per 32 along I, before w
         const float2 q = e2m1_block_quant_dequant(h0, h1);
         h0 = q.x;
         h1 = q.y;
     }
-    if (a.act_e4m3) {
+    if (MODE == kModeE4m3) {
         // h is quantized to E4M3 per 128 along I (tiles 2b, 2b + 1; a last block
         // of 64 is one tile), before w.  The second tile of a block to finish
         // quantizes both, from the first one's raw h.
@@ -723,13 +770,13 @@ __device__ __forceinline__ void finalize_gate_up(const GemvArgs& a, const Stream
             const int ot = tile ^ 1;
             uint8_t* Bunit = a.hq + (size_t)j * act_bytes(a.I) + (size_t)(ot / 2) * kUnitBBytes;
             uint8_t* Bsf = a.hsf + (size_t)j * act_sf_bytes(a.I) + (size_t)(ot / 2) * kUnitSfBytes;
-            write_pieces64(e4m3_quant_dequant(o0, s) * w, e4m3_quant_dequant(o1, s) * w, lane, Bunit, Bsf, 2 * ot,
+            write_pieces64_small(e4m3_quant_dequant(o0, s) * w, e4m3_quant_dequant(o1, s) * w, lane, Bunit, Bsf, 2 * ot,
                            sm.tr[tr_warp]);
         }
     }
     uint8_t* Bunit = a.hq + (size_t)j * act_bytes(a.I) + (size_t)(tile / 2) * kUnitBBytes;
     uint8_t* Bsf = a.hsf + (size_t)j * act_sf_bytes(a.I) + (size_t)(tile / 2) * kUnitSfBytes;
-    write_pieces64(h0 * w, h1 * w, lane, Bunit, Bsf, 2 * tile, sm.tr[tr_warp]);
+    write_pieces64_small(h0 * w, h1 * w, lane, Bunit, Bsf, 2 * tile, sm.tr[tr_warp]);
     TC_FIN(1, group % 64);
     // the down projection reads these with bulk copies (async proxy), in other CTAs
     asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -766,7 +813,7 @@ __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v)
 // order into *acc; returns the first CTA not yet folded in.  With spin, waits
 // (bounded) for each; without, stops at the first that is not there yet.
 __device__ __forceinline__ int fold_partials(const uint64_t* part, int c, int c1, int row, uint32_t tag,
-                                             bool spin, float* acc, bool* timed_out)
+                                             bool spin, float* acc, bool* timed_out, uint64_t limit)
 {
     uint64_t t0 = 0;
     while (c <= c1) {
@@ -777,8 +824,8 @@ __device__ __forceinline__ int fold_partials(const uint64_t* part, int c, int c1
             continue;
         }
         if (!spin) break;
-        if (t0 == 0) t0 = globaltimer_ns();
-        else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (t0 == 0) t0 = wait_clock();
+        else if (wait_clock() - t0 > wait_cycles(limit)) {
             *timed_out = true;
             break;
         }
@@ -786,7 +833,7 @@ __device__ __forceinline__ int fold_partials(const uint64_t* part, int c, int c1
     return c;
 }
 
-template <int PHASE>
+template <int PHASE, int MODE>
 __device__ void epilogue(const GemvArgs& a, const StreamPlan& p, const Range& r, TcSmem& sm, uint32_t tmem,
                          int quad, int lane, int et, EpiState& es)
 {
@@ -816,11 +863,11 @@ __device__ void epilogue(const GemvArgs& a, const StreamPlan& p, const Range& r,
         bool late = false;
         int cnext = blockIdx.x + 1;
         if (c1 > (int)blockIdx.x)   // while the last MMAs run: the partials that are there already
-            cnext = fold_partials(part, cnext, c1, row, es.tag, false, &pacc, &late);
+            cnext = fold_partials(part, cnext, c1, row, es.tag, false, &pacc, &late, wait_limit(a));
 
         const int buf = es.buf;
         const bool ready = !*(volatile int*)&sm.abort &&
-                           mbar_wait_or_abort(&sm.acc_full[buf], es.use[buf] & 1, &sm.abort, kWaitLimitNs);
+                           mbar_wait_or_abort(&sm.acc_full[buf], es.use[buf] & 1, &sm.abort, wait_limit(a));
         if (et == 0) TC_TRACE(PHASE, 3, es.use[0] + es.use[1]);
         if (PHASE == 0 && et == 0) TC_CTA(10);
         if (PHASE == 0 && et == 0 && owner) TC_GRP(0, group);
@@ -852,7 +899,7 @@ __device__ void epilogue(const GemvArgs& a, const StreamPlan& p, const Range& r,
         }
         if (cnext <= c1) {
             const bool abort = *(volatile int*)&sm.abort;
-            fold_partials(part, cnext, c1, row, es.tag, !abort, &pacc, &late);
+            fold_partials(part, cnext, c1, row, es.tag, !abort, &pacc, &late, wait_limit(a));
             if (late) set_abort(a, sm);
         }
         if (PHASE == 0 && et == 0) TC_CTA(11);
@@ -870,7 +917,7 @@ __device__ void epilogue(const GemvArgs& a, const StreamPlan& p, const Range& r,
             if (quad == es.cb) {
                 named_sync(3 + es.cb, 128);
                 if (lane == 0) TC_GRP(2, group);
-                finalize_gate_up(a, p, sm, group, comb, lane, quad);
+                finalize_gate_up<MODE>(a, p, sm, group, comb, lane, quad);
             } else {
                 named_arrive(3 + es.cb, 128);
             }
@@ -892,6 +939,7 @@ __device__ void epilogue(const GemvArgs& a, const StreamPlan& p, const Range& r,
 // persistent grid.  The producer streams the down weights right after the
 // gate/up weights; only the copies of h wait until the last h piece is
 // written.
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) k_layer(GemvArgs a, StreamPlan p0, StreamPlan p1)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -967,7 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(GemvArgs a, StreamPlan p0
             if (ok) produce<1>(a, p1, r1, sm, n);
             // no copy may still be in flight into this CTA's memory at exit
             for (int m = n > kStages ? n - kStages : 0; m < n; m++)
-                mbar_wait_bounded(&sm.full[m % kStages], (m / kStages) & 1, kWaitLimitNs);
+                mbar_wait_bounded(&sm.full[m % kStages], (m / kStages) & 1, wait_limit(a));
         }
         return;
     }
@@ -990,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(GemvArgs a, StreamPlan p0
             // none of this thread's MMAs may be in flight when TMEM is freed (after
             // an abort the epilogue no longer waits for the accumulators)
             tc_commit(&sm.drain[warp - 1]);
-            mbar_wait_bounded(&sm.drain[warp - 1], 0, kWaitLimitNs);
+            mbar_wait_bounded(&sm.drain[warp - 1], 0, wait_limit(a));
         }
         __syncwarp();
     } else {
@@ -1001,9 +1049,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(GemvArgs a, StreamPlan p0
         es.cb = 0;
         es.use[0] = es.use[1] = 0;
         es.tag = 1u + (ld_acquire_u32(a.sync + 2) & 0x3FFFFFFFu);   // never 0, the cleared value
-        epilogue<0>(a, p0, r0, sm, tmem, warp & 3, lane, et, es);
+        epilogue<0, MODE>(a, p0, r0, sm, tmem, warp & 3, lane, et, es);
         if (et == 0) TC_CTA(5);
-        epilogue<1>(a, p1, r1, sm, tmem, warp & 3, lane, et, es);
+        epilogue<1, MODE>(a, p1, r1, sm, tmem, warp & 3, lane, et, es);
         if (et == 0) TC_CTA(6);
         if (et == 0) {
             // the last CTA to finish resets the layer's counters for the next launch
@@ -1087,8 +1135,10 @@ GemvWorkspaceSizes gemv_workspace_sizes(int T, int topk, int H, int I, int sms, 
 
 cudaError_t gemv_init_device()
 {
-    cudaError_t e = cudaFuncSetAttribute((const void*)k_layer, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)layer_smem());
+    cudaError_t e = cudaSuccess;
+    for (const void* fn : {(const void*)k_layer<kModeBf16>, (const void*)k_layer<kModeE4m3>,
+                           (const void*)k_layer<kModeE2m1>})
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)layer_smem());
     // k_prep asks for the same shared-memory carveout as k_layer, so that the
     // SMs need no reconfiguration between the two kernels of a layer
     if (e == cudaSuccess)
@@ -1119,7 +1169,9 @@ cudaError_t launch_gemv_layer(const GemvArgs& a0, cudaStream_t s, bool pdl, Prof
     p0.G = p1.G = (int)G;     // every CTA has units of both projections
     void* args[] = {&a, &p0, &p1};
     if (prof) prof->begin(kPhaseGateUp, s);
-    err = launch_ex((const void*)k_layer, dim3((unsigned)G), dim3(kThreads), layer_smem(), s, pdl && !prof, args);
+    const void* fn = a.act_e4m3 ? (const void*)k_layer<kModeE4m3>
+                     : a.act_e2m1 ? (const void*)k_layer<kModeE2m1> : (const void*)k_layer<kModeBf16>;
+    err = launch_ex(fn, dim3((unsigned)G), dim3(kThreads), layer_smem(), s, pdl && !prof, args);
     if (prof) prof->end(s);
     return err;
 }

@@ -694,9 +694,9 @@ __device__ void gload_b(const GroupArgs& a, int nchunks, uint32_t h_target, GSme
         if (q.phase == 1 && !h_done) {
             bool ok = g_ld_acquire_u32(a.sync) >= h_target;
             if (!ok) {
-                const uint64_t t0 = globaltimer_ns();
+                const uint64_t t0 = wait_clock();
                 while (!(ok = g_ld_acquire_u32(a.sync) >= h_target))
-                    if (*(volatile int*)&sm.abort || globaltimer_ns() - t0 > kGWaitLimitNs) break;
+                    if (*(volatile int*)&sm.abort || wait_clock() - t0 > wait_cycles(kGWaitLimitNs)) break;
             }
             G_CTA(7);
             // h was written with generic stores; the copies read it through the async proxy
@@ -946,8 +946,8 @@ __device__ __forceinline__ int gfold(const uint64_t* part, int c, int c1, int ro
             continue;
         }
         if (!spin) break;
-        if (t0 == 0) t0 = globaltimer_ns();
-        else if (globaltimer_ns() - t0 > kGWaitLimitNs) {
+        if (t0 == 0) t0 = wait_clock();
+        else if (wait_clock() - t0 > wait_cycles(kGWaitLimitNs)) {
             *timed_out = true;
             break;
         }

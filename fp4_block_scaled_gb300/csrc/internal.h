@@ -44,6 +44,8 @@ struct GemvArgs {
                                         // zero between launches: the last CTA resets them),
                                         // launches so far (the partials' tag)
     int* status;
+    unsigned long long wait_ns;         // limit of every bounded wait in the kernels (0: 2 s)
+    int debug_withhold;                 // test hook: CTA 0 never reports its finished gate/up groups
     // output (forward): y [T][H] fp32 or bf16
     void* y;
     int out_f32;
@@ -58,6 +60,11 @@ struct GemvWorkspaceSizes {
 constexpr int kGemvSyncInts = 3;
 GemvWorkspaceSizes gemv_workspace_sizes(int T, int topk, int H, int I, int sms, bool e4m3);
 cudaError_t gemv_init_device();   // per device, before the first launch
+
+// Every device and page-locked allocation of the library goes through these,
+// so that a test can make them fail (moe_ffn_test_fail_allocs).
+cudaError_t lib_malloc(void** p, size_t bytes);
+cudaError_t lib_host_alloc(void** p, size_t bytes, unsigned flags);
 size_t gemv_stream_smem();
 
 // Optional per-phase event recorder (moe_ffn_profile_*); nullptr = off.

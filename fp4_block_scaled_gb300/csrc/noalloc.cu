@@ -13,14 +13,19 @@
 // g_scratch is a static __device__ array: every GPU that loads this library
 // holds its kNoAllocScratchBytes until the process exits, and all calls share
 // it.  In host code the name g_scratch is only a host-side stand-in for the
-// symbol, not a device address; its device address is obtained once per
-// device with cudaGetSymbolAddress (with that device current) and passed to
-// the kernels.  That set-up runs during the first call on each device, so the
-// first call on a device should come before any stream capture.  Each call
-// clears the counters that must start at zero (cudaMemsetAsync on the call's
-// stream), but the array keeps the rest of the previous call's contents, and
-// two calls whose work overlaps on the GPU (different streams, or different
-// threads without ordering) race on it.
+// symbol, not a device address; its device address is obtained with
+// cudaGetSymbolAddress, with the device current, and passed to the kernels.
+// The first call on a device also sets the kernels' shared-memory limits, so
+// it should come before any stream capture; later calls look the address up
+// again and redo that set-up if it changed (a device reset makes a new
+// context, with a new copy of the array).  Each call clears the counters that
+// must start at zero (cudaMemsetAsync on the call's stream); the rest keeps
+// the previous call's contents, and two calls whose work overlaps on the GPU
+// (different streams, or different threads without ordering) race on it.  The
+// launch-tagged partial sums sit at fixed offsets, in areas sized for the
+// largest SM count, so they only ever hold tagged words (whose tags, counting
+// launches, never repeat) or the array's initial zeros, whatever the shapes of
+// earlier calls.
 #include <cuda_runtime.h>
 #include <string.h>
 
@@ -32,38 +37,42 @@ using namespace moe;
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = 4u << 20;   // 4 MiB
+constexpr size_t kNoAllocScratchBytes = 4u << 20;   // 4 MiB in all:
+constexpr size_t kSyncBytes = 256;                      // status word and counters
+constexpr int kMaxSms = 256;
+constexpr size_t kPartBytes = (size_t)kMaxSms * 128 * 8; // one area of tagged partial sums
+constexpr size_t kOffPartGu = kSyncBytes;
+constexpr size_t kOffPartDn = kOffPartGu + kPartBytes;
+constexpr size_t kOffRest = kOffPartDn + kPartBytes;    // then the activation and h pieces
 constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_scratch[kNoAllocScratchBytes];
 
 struct DeviceScratch {
-    void* ptr = nullptr;   // device address of g_scratch on that device
+    void* ptr = nullptr;   // device address of g_scratch in that device's current context
     int sms = 0;
-    bool ready = false;
 };
 
 DeviceScratch g_devices[kMaxDevices];
 std::mutex g_setup_mutex;
 
-// Once per device, with the device current: resolve g_scratch's address and
-// prepare the kernels' shared-memory limits.
-int setup_device(int device, DeviceScratch** out)
+// With the device current: g_scratch's address, and (first call, or a new
+// context since) the kernels' shared-memory limits.
+int setup_device(int device, DeviceScratch* out)
 {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     DeviceScratch& d = g_devices[device];
-    if (!d.ready) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_scratch) != cudaSuccess || !ptr) return MOE_ERR_CUDA;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_scratch) != cudaSuccess || !ptr) return MOE_ERR_CUDA;
+    if (ptr != d.ptr) {
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
             return MOE_ERR_CUDA;
         if (gemv_init_device() != cudaSuccess) return MOE_ERR_CUDA;
         d.ptr = ptr;
         d.sms = sms;
-        d.ready = true;
     }
-    *out = &d;
+    *out = d;
     return MOE_OK;
 }
 
@@ -98,29 +107,30 @@ extern "C" int moe_ffn_forward_noalloc(const moe_ffn_config* cfg, int device, co
         ~Restore() { if (prev >= 0 && prev != dev) cudaSetDevice(prev); }
     } restore{prev, device};
 
-    DeviceScratch* d = nullptr;
+    DeviceScratch d;
     rc = setup_device(device, &d);
     if (rc) return rc;
+    if (d.sms > kMaxSms) return MOE_ERR_UNSUPPORTED;
 
-    // carve the scratch: status and counters first (cleared every call, except
-    // the launch count that tags the partial sums), then the rest
+    // fixed areas first (status and counters, cleared every call except the
+    // launch count that tags the partial sums; the two areas of tagged partial
+    // sums), then the activation and h pieces
     const int H = cfg->hidden, I = cfg->inter, k = cfg->topk;
-    const GemvWorkspaceSizes g = gemv_workspace_sizes(T, k, H, I, d->sms, false);
-    size_t off = 0;
+    const GemvWorkspaceSizes g = gemv_workspace_sizes(T, k, H, I, d.sms, false);
+    size_t off = kOffRest;
     auto take = [&](size_t bytes) {
         size_t o = off;
         off = align_up(off + bytes, 256);
         return o;
     };
-    const size_t o_status = take(sizeof(int)), o_sync = take(kGemvSyncInts * sizeof(int));
-    const size_t zero_bytes = o_sync + 2 * sizeof(int);
     const size_t o_xq = take(g.xq), o_xsf = take(g.xsf), o_hq = take(g.hq), o_hsf = take(g.hsf);
-    const size_t o_pgu = take(g.part_gu * 8), o_pdn = take(g.part_dn * 8);
     if (off > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;   // problem too large for the array
 
     cudaStream_t s = (cudaStream_t)stream;
-    char* b = (char*)d->ptr;
-    if (cudaMemsetAsync(b, 0, zero_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+    char* b = (char*)d.ptr;
+    int* status_w = (int*)b;
+    int* sync_w = status_w + 1;
+    if (cudaMemsetAsync(b, 0, 3 * sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;   // status, sync[0..1]
 
     GemvArgs a;
     memset(&a, 0, sizeof(a));
@@ -129,7 +139,7 @@ extern "C" int moe_ffn_forward_noalloc(const moe_ffn_config* cfg, int device, co
     a.E = cfg->num_experts;
     a.H = H;
     a.I = I;
-    a.sms = d->sms;
+    a.sms = d.sms;
     a.eps = 1e-6f;
     a.x_bf16 = (const uint16_t*)x;
     a.idx = topk_idx;
@@ -139,10 +149,10 @@ extern "C" int moe_ffn_forward_noalloc(const moe_ffn_config* cfg, int device, co
     a.xsf = (uint8_t*)(b + o_xsf);
     a.hq = (uint8_t*)(b + o_hq);
     a.hsf = (uint8_t*)(b + o_hsf);
-    a.part_gu = (uint64_t*)(b + o_pgu);
-    a.part_dn = (uint64_t*)(b + o_pdn);
-    a.sync = (int*)(b + o_sync);
-    a.status = status ? status : (int*)(b + o_status);
+    a.part_gu = (uint64_t*)(b + kOffPartGu);
+    a.part_dn = (uint64_t*)(b + kOffPartDn);
+    a.sync = sync_w;
+    a.status = status ? status : status_w;
     a.y = y;
     a.out_f32 = cfg->out_dtype == MOE_OUT_F32;
     return launch_gemv_layer(a, s, true, nullptr) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

@@ -314,11 +314,31 @@ int moe_ffn_profile_read(moe_ffn_t h, double* ms, int* launches);
  * `stream`; the array otherwise keeps the previous call's contents, and calls
  * whose work overlaps on the GPU race on it, so calls must be ordered on one
  * stream.  The first call on a device resolves the array's device address and
- * sets kernel attributes; make that first call before any stream capture. */
+ * sets kernel attributes; make that first call before any stream capture.
+ * Calls look the address up again and redo that set-up when it changed (a
+ * device reset made a new context). */
 int moe_ffn_forward_noalloc(const moe_ffn_config* cfg, int device, const void* x,
                             const int32_t* topk_idx, const float* topk_w,
                             const moe_expert_table* tbl, void* y, int T, int* status,
                             void* stream);
+
+/* Test hooks for the failure paths.  The sources have no counterpart of
+ * these; they exist so that tests can drive the error handling without a GPU
+ * fault, trap or hang.
+ *
+ * moe_ffn_test_set_wait: later calls on h run the slot-major layer kernel
+ * with every bounded device-side wait giving up after wait_ns nanoseconds
+ * (at 2 GHz SM clock; 0: the default, 2 s), and with withhold != 0 its first
+ * CTA never reports its finished gate/up groups, so that the other CTAs' waits
+ * for the whole of h run out: the call completes, y is incomplete, and
+ * moe_ffn_status returns MOE_ERR_DEVICE_TIMEOUT.  Graphs the handle captured earlier keep the
+ * settings they were captured with.  Errors: INVALID_ARG.
+ *
+ * moe_ffn_test_fail_allocs: the next n device or page-locked allocations the
+ * library makes (any handle, cache or staging buffer) fail as if out of
+ * memory; n = 0 clears.  The calls that make them return MOE_ERR_OOM. */
+int moe_ffn_test_set_wait(moe_ffn_t h, unsigned long long wait_ns, int withhold);
+void moe_ffn_test_fail_allocs(int n);
 
 /* Wait for `stream`, then return and clear the sticky device status:
  * MOE_OK, MOE_ERR_BAD_INDEX or MOE_ERR_DEVICE_TIMEOUT (or MOE_ERR_CUDA if the

@@ -2,8 +2,6 @@
 oracle's metric and greedy pinned against hand counts, closed forms and a
 known optimum; the library bit-exact against the oracle; the benefit on
 synthetic clustered routing (alike sequences route alike)."""
-import itertools
-
 import numpy as np
 import pytest
 
@@ -63,19 +61,53 @@ def test_greedy_recovers_disjoint_clusters():
     assert np.array_equal(oracle.batch_distinct(sig, order, B), np.array(union))
 
 
-def test_greedy_never_worse_than_brute_force_bound_on_tiny_cases():
-    """On 6 sequences in batches of 3 the greedy's total is between the
-    optimum over all partitions (brute force) and the worst one."""
-    rng = np.random.default_rng(2)
-    for trial in range(20):
-        sig = rng.integers(0, 8, size=(6, 2, 2))
-        totals = []
-        for first in itertools.combinations(range(1, 6), 2):
-            a = [0, *first]
-            b = [i for i in range(6) if i not in a]
-            totals.append(oracle.batch_distinct(sig, a + b, 3).sum())
-        g = oracle.batch_distinct(sig, oracle.batch_plan_greedy(sig, 3), 3).sum()
-        assert min(totals) <= g <= max(totals)
+# Hand-worked plans.  Each case is built so that one plausible misreading of
+# the greedy rule gives a different order than the rule itself: a batch
+# starts from the lowest-numbered unplaced sequence; the next member is the
+# unplaced sequence adding the fewest experts not yet in the batch, counted
+# per layer and summed over the layers; ties go to the lower number.
+HAND_PLANS = [
+    # tie-break: from seed 0 {0,1}, sequences 2 {0,5} and 3 {1,6} both add one
+    # expert (1 adds two); the lower number, 2, joins.  (Ties to the higher
+    # number would give 0 3 1 2.)
+    ("ties go to the lower number", [[[0, 1]], [[2, 3]], [[0, 5]], [[1, 6]]], 2, [0, 2, 1, 3]),
+    # per-layer sets: sequence 1 routes to {2} then {1}, sequence 2 to {1}
+    # then {3}.  Counted per layer, 1 adds two experts and 2 adds one, so 2
+    # joins; pooling the ids of all layers into one set would make 1 add
+    # nothing and join first (0 1 2).
+    ("experts are counted per layer", [[[1], [2]], [[2], [1]], [[1], [3]]], 2, [0, 2, 1]),
+    # summed over layers: 1 adds {2,3} in layer 0 and nothing in layer 1 (sum
+    # 2, largest layer 2); 2 adds {4} and {12} (sum 2, largest layer 1).  The
+    # sums tie and the lower number, 1, joins; taking the largest layer's count
+    # instead would pick 2.
+    ("costs are summed over the layers", [[[0, 1], [10, 11]], [[2, 3], [10, 11]], [[0, 4], [10, 12]]], 3, [0, 1, 2]),
+    # the second batch starts from the lowest unplaced sequence (2), not from
+    # the best remaining pair: 1 and 3 share {2,3}, but 1 already sits in the
+    # first batch, so the greedy pays 4 + 4 where 0 2 | 1 3 would pay 4 + 2.
+    ("each batch starts from the lowest unplaced number", [[[0, 1]], [[2, 3]], [[4, 5]], [[2, 3]]], 2, [0, 1, 2, 3]),
+    # growth uses the batch's union so far, not the seed alone: after 0 {0,1}
+    # takes 1 {0,2} (adds 1; 2 {3,4} and 3 {2,5} add 2), sequence 3 adds only
+    # {5} to {0,1,2} while 2 adds {3,4}, so 3 joins before 2.
+    ("growth counts against the batch so far", [[[0, 1]], [[0, 2]], [[3, 4]], [[2, 5]]], 3, [0, 1, 3, 2]),
+    # -1 is no expert: 2 {9,-1} adds one expert, 1 {9,10} two, so 2 joins
+    # (counting -1 as an expert would tie them and take 1)
+    ("-1 is no expert", [[[7, 8]], [[9, 10]], [[9, -1]]], 2, [0, 2, 1]),
+    # a repeated id adds once: 2 {9,9} adds one expert, 1 {9,10} two
+    ("a repeated id counts once", [[[7, 8]], [[9, 10]], [[9, 9]]], 2, [0, 2, 1]),
+]
+
+
+@pytest.mark.parametrize("what,sig,B,order", HAND_PLANS, ids=[h[0] for h in HAND_PLANS])
+def test_greedy_hand_worked_plans(what, sig, B, order):
+    assert oracle.batch_plan_greedy(np.array(sig), B).tolist() == order, what
+
+
+@pytest.mark.parametrize("what,sig,B,order", HAND_PLANS, ids=[h[0] for h in HAND_PLANS])
+def test_library_greedy_hand_worked_plans(what, sig, B, order):
+    _lib_or_skip()
+    sig = np.array(sig, np.int32)
+    E = int(sig.max()) + 1
+    assert moe.moe_batch_plan(sig, E, B).tolist() == order, what
 
 
 # ------------------------------------------------- library vs the oracle
