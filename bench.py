@@ -1,11 +1,13 @@
 """Benchmark: routed FP4 MoE expert-FFN decode on one GB300 (or N replicas).
 
-Workload (default `layer_b1`): one MoE layer with 384 resident experts
-(H=4096, I=2880, FP4 E2M1 + ue8m0 per 32, 7.2 GB), top-6 routing, decode batch
-1.  Each step is one moe_ffn_forward call for a fresh token; routings are
-pre-drawn so that consecutive steps share no expert (every step streams its 6
-experts, 112.8 MB, from HBM: inputs far larger than L2).  Steps are replayed
-from CUDA graphs of up to 500 calls.
+Workload (default `stack_b1`, the metric's configuration): a decode step of a
+40-layer MoE stack at batch 1 -- each layer 128 resident experts (H=4096,
+I=2880, FP4 E2M1 + ue8m0 per 32; 96 GB for the stack), top-6 routing drawn per
+layer, residual + RMSNorm per layer, the whole step one CUDA graph
+(moe_stack_forward).  `layer_b1` is one layer with 384 resident experts (7.2
+GB), a fresh token per step, consecutive steps sharing no expert (every step
+streams its 6 experts, 112.8 MB, from HBM: inputs far larger than L2),
+replayed from CUDA graphs of up to 500 calls.
 
 Other workloads (`--workload`): the same layer at batch 64 (uniform routing)
 and 512 (Zipf expert popularity) with E4M3 activations, and a 40-layer stack
@@ -34,7 +36,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOADS = {
-    # one MoE layer, decode batch 1 (the default: the headline workload)
+    # one MoE layer, decode batch 1 (the per-layer headline)
     "layer_b1": dict(E=384, H=4096, I=2880, k=6, T=1, L=1, act="bf16", dist="uniform", steps=20000),
     # same step (6 experts streamed per token) with 64 resident experts (1.2 GB,
     # still far above L2): the size used for ncu captures
@@ -46,7 +48,8 @@ WORKLOADS = {
     # expert-major path with 64 resident experts (1.2 GB, above L2) at batch 16: 1-2
     # slots per group as at batch 64; the size used for ncu captures of k_glayer
     "layer_b16_e64": dict(E=64, H=4096, I=2880, k=6, T=16, L=1, act="e4m3", dist="uniform", steps=2000),
-    # 40-layer stack of 128-expert layers (96 GB resident), residual + RMSNorm,
+    # 40-layer stack of 128-expert layers (96 GB resident), residual + RMSNorm (stack_b1:
+    # the default, the metric's configuration),
     # the whole step as one CUDA graph, at batch 1 and 32
     "stack_b1": dict(E=128, H=4096, I=2880, k=6, T=1, L=40, act="bf16", dist="uniform", steps=500),
     "stack_b32": dict(E=128, H=4096, I=2880, k=6, T=32, L=40, act="bf16", dist="uniform", steps=50),
@@ -504,7 +507,42 @@ def run_ours(args, wl):
     ro_ms = ms_ph[moe.MOE_PHASE_ROUTE] / max(1, n_ph[moe.MOE_PHASE_ROUTE])
     co_ms = ms_ph[moe.MOE_PHASE_DOWN] / max(1, n_ph[moe.MOE_PHASE_DOWN])
     ly_bytes = sum(distinct(i, 0) for i in range(nprof)) / nprof * expert_bytes(H, I) + act_io
-    achieved = ly_bytes / (ly_ms / 1000.0) / 1e9
+    # the same kernel inside a step: on the slot-major path, a CUDA graph of
+    # layer-kernel launches back to back (measurement mode: the layer kernel
+    # alone, on the pieces of the last full call; each launch overlaps the
+    # previous one's tail as programmatic dependent launch lets it, as in a
+    # step), the routings cycling as in the timed steps.  The profiling events
+    # above separate the launches (no overlap), so they read longer.
+    ly_graph_ms = None
+    if not grouped:
+        nlg = 200 if T == 1 else 20
+        with torch.cuda.stream(stream):
+            moe.moe_ffn_forward(h, x_d[0], idx_d[0, 0], w_d[0, 0], sets[0].table, yp, T, stream)
+        stream.synchronize()
+        moe.moe_ffn_profile_layer_only(h, True)
+        # launch i: routing (i / L) mod R of layer i mod L (a stack's layers have
+        # weights of their own, so no two consecutive launches share an expert)
+        lg = [((i // L) % R, i % L) for i in range(nlg)]
+        g_l = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_l, stream=stream):
+            for r_, l_ in lg:
+                moe.moe_ffn_forward(h, x_d[0], idx_d[r_, l_], w_d[r_, l_], sets[l_].table, yp, T, stream)
+        moe.moe_ffn_profile_layer_only(h, False)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g_l.replay()
+            evl0, evl1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            evl0.record(stream)
+            for _ in range(5):
+                g_l.replay()
+            evl1.record(stream)
+        stream.synchronize()
+        ly_graph_ms = evl0.elapsed_time(evl1) / (5 * nlg)
+        del g_l
+        lg_bytes = sum(distinct(r_, l_) for r_, l_ in lg) / nlg * expert_bytes(H, I) + act_io
+        achieved = lg_bytes / (ly_graph_ms / 1000.0) / 1e9
+    else:
+        achieved = ly_bytes / (ly_ms / 1000.0) / 1e9
     traffic = traffic_record(kernel, args.workload, wl["act"], ly_bytes)
 
     # ---- the router ahead of the path (logits = W x, top-k, softmax): one
@@ -609,7 +647,7 @@ def run_ours(args, wl):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None,
-            "dtype": {"e4m3": "e4m3xe2m1->f32", "e2m1": "e2m1xe2m1->f32"}.get(wl["act"], "f16xe2m1->f32"),
+            "dtype": {"e4m3": "e4m3xe2m1->f32", "e2m1": "e2m1xe2m1->f32"}.get(wl["act"], "bf16xe2m1->f32"),
             "data": "synthetic",
             "config": {"workload": args.workload, "layers": L, "experts": E, "hidden": H, "inter": I,
                        "topk": k, "tokens_per_step": T, "routing": wl["dist"], "activations": wl["act"],
@@ -621,13 +659,19 @@ def run_ours(args, wl):
                        "distinct_experts_per_layer_step": round(
                            sum(distinct(i, l) for i in range(R) for l in range(L)) / (R * L), 2)},
             "hbm_gbs": gbs_step, "hbm_frac": gbs_step / peak,
+            "per_layer": {"us": ms_step / L * 1e3, "tokens_s": value * L} if L > 1 else None,
             "bytes_per_step": bytes_step,
             "phase_us": {"route": ro_ms * 1e3, "prep": pr_ms * 1e3, "layer": ly_ms * 1e3,
                          "combine": co_ms * 1e3},
             "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved,
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "algorithmic_bytes_per_launch": ly_bytes},
+                         "algorithmic_bytes_per_launch": ly_bytes,
+                         "timing": ("in a CUDA graph of layer-kernel launches back to back, "
+                                    f"{ly_graph_ms * 1e3:.2f} us per launch; with events around each launch "
+                                    f"(launches separated) {ly_ms * 1e3:.2f} us")
+                         if ly_graph_ms is not None else
+                         f"events around each launch (launches separated): {ly_ms * 1e3:.2f} us"},
             "router": router,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -757,7 +801,7 @@ def run_host_experts(args, wl):
     line = {
         "metric": METRIC, "value": T * K / (ms_total / 1000.0), "unit": "tokens/s", "n_gpus": 1, "steps": K,
         "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16xe2m1->f32", "data": "synthetic",
+        "dtype": "bf16xe2m1->f32", "data": "synthetic",
         "config": {"workload": args.workload, "layers": 1, "experts": E, "hidden": H, "inter": I, "topk": k,
                    "tokens_per_step": T, "routing": "uniform, consecutive steps share no expert",
                    "activations": "bf16", "path": "slot-major", "parallelism": "replicas1",
@@ -788,7 +832,7 @@ def main():
     ap.add_argument("--steps", type=int, default=None, help="timed steps (default: per workload)")
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="layer_b1")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="stack_b1")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
     ap.add_argument("--path", choices=["auto", "slot", "group"], default="auto",
                     help="layer path: the library's choice for T, or forced slot-major / expert-major")

@@ -37,6 +37,7 @@ EXPORTS = [
     "moe_router_topk", "moe_router_select", "moe_batch_plan", "moe_batch_distinct",
     "moe_expert_cache_create", "moe_expert_cache_fetch", "moe_expert_cache_prefetch", "moe_expert_cache_slot",
     "moe_expert_cache_stats", "moe_expert_cache_destroy", "moe_ffn_test_set_wait", "moe_ffn_test_fail_allocs",
+    "moe_ffn_profile_layer_only",
 ]
 
 MOE_PHASE_PREP = 0
@@ -108,6 +109,7 @@ def lib() -> ctypes.CDLL:
             "moe_expert_cache_destroy": (None, [P]),
             "moe_ffn_test_set_wait": (I, [P, ctypes.c_ulonglong, I]),
             "moe_ffn_test_fail_allocs": (None, [I]),
+            "moe_ffn_profile_layer_only": (I, [P, I]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -215,6 +217,12 @@ def moe_ffn_profile_read(h):
     n = (ctypes.c_int * MOE_NUM_PHASES)()
     _check(lib().moe_ffn_profile_read(h, ms, n), "moe_ffn_profile_read")
     return list(ms), list(n)
+
+
+def moe_ffn_profile_layer_only(h, on: bool = True) -> None:
+    """Measurement mode: slot-major forwards launch the layer kernel alone,
+    reusing the last full call's activation pieces (see include/moe_ffn.h)."""
+    _check(lib().moe_ffn_profile_layer_only(h, 1 if on else 0), "moe_ffn_profile_layer_only")
 
 
 def moe_ffn_status(h, stream=None) -> int:

@@ -601,6 +601,13 @@ int moe_stack_forward(moe_ffn_t h, float* x, const moe_expert_table* tbls,
     return cuda_rc(cudaGraphLaunch(exec, s));
 }
 
+int moe_ffn_profile_layer_only(moe_ffn_t h, int on)
+{
+    if (!h) return MOE_ERR_INVALID_ARG;
+    h->base.skip_prep = on ? 1 : 0;
+    return MOE_OK;
+}
+
 void moe_ffn_test_fail_allocs(int n) { g_fail_allocs.store(n > 0 ? n : 0); }
 
 int moe_ffn_test_set_wait(moe_ffn_t h, unsigned long long wait_ns, int withhold)

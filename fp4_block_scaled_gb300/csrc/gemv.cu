@@ -1154,7 +1154,7 @@ cudaError_t launch_gemv_layer(const GemvArgs& a0, cudaStream_t s, bool pdl, Prof
     GemvArgs a = a0;
     if (a.T == 0) return cudaSuccess;
     cudaError_t err;
-    {
+    if (!a.skip_prep) {
         void* args[] = {&a};
         if (prof) prof->begin(kPhasePrep, s);
         const int spans = a.act_e4m3 ? a.H / 128 : a.H / 64;      // one warp each

@@ -46,6 +46,8 @@ struct GemvArgs {
     int* status;
     unsigned long long wait_ns;         // limit of every bounded wait in the kernels (0: 2 s)
     int debug_withhold;                 // test hook: CTA 0 never reports its finished gate/up groups
+    int skip_prep;                      // measurement mode: launch the layer kernel alone (the
+                                        // activation pieces of the previous call are reused)
     // output (forward): y [T][H] fp32 or bf16
     void* y;
     int out_f32;

@@ -292,6 +292,18 @@ enum {
 int moe_ffn_profile_enable(moe_ffn_t h, int on);
 int moe_ffn_profile_read(moe_ffn_t h, double* ms, int* launches);
 
+/* Measurement mode of the slot-major path (the sources have no counterpart;
+ * it serves timing): while on, moe_ffn_forward calls that take the
+ * slot-major path launch only the layer kernel, which reuses the activation
+ * pieces that the last full call left in the handle's workspace -- its
+ * output is the layer applied to that call's x with this call's routing and
+ * experts.  A CUDA graph of such calls, back to back, measures the layer
+ * kernel's duration as it runs inside a step (each launch overlapping the
+ * previous one's tail, as programmatic dependent launch allows), which the
+ * profiling events above cannot (they separate the launches).  The expert-
+ * major path and moe_stack_forward are not affected.  Errors: INVALID_ARG. */
+int moe_ffn_profile_layer_only(moe_ffn_t h, int on);
+
 /* moe_ffn_forward without a handle and without allocating.  The sources have
  * no counterpart of this call; it serves callers that may not allocate device
  * memory on their call path -- hosts that own every device allocation and give

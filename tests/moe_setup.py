@@ -149,6 +149,49 @@ def e2m1_flip_bound(H, I, E, x_bits, idx, w, layer=0, seed=0, delta=1e-4):
     return bound, n_amb
 
 
+def e4m3_flip_candidates(H, I, E, x_bits, idx, layer=0, seed=0, delta=1e-4):
+    """How many elements of h could round to the other E4M3 neighbour on the
+    GPU (fp32 h) than in the oracle (fp64 h): elements of the oracle's h whose
+    scaled value lies within delta (relative to the local grid step) of a
+    midpoint between adjacent E4M3 values, plus whole 128-blocks (64 for the
+    last) whose maximum lies within a relative delta of a scale boundary
+    448 * 2^k.  Each such flip moves y by about 1e-3 rms.  Returns (count,
+    elements of h examined)."""
+    pos = np.unique([oracle.e4m3_value(c) for c in range(127)])
+    mids = (pos[1:] + pos[:-1]) / 2.0
+    steps = pos[1:] - pos[:-1]
+    T, k = idx.shape
+    codes, scales = host_experts(H, I, idx.reshape(-1), layer=layer, seed=seed, E=E)
+    gc, gs = I * H // 2, I * H // 32
+    n, total = 0, 0
+    for t in range(T):
+        xf = (x_bits[t].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        xc, xsc = oracle.act_quant_e4m3(xf, 128)
+        xq = np.array([oracle.e4m3_value(int(c)) for c in xc]) * np.ldexp(
+            1.0, np.repeat(xsc.astype(np.int64), 128)[:H] - 127)
+        for j in range(k):
+            e = int(idx[t, j])
+            c, sc = codes[e], scales[e]
+            g = oracle.matvec(c[:gc], sc[:gs], I, H, xq)
+            u = oracle.matvec(c[gc:2 * gc], sc[gs:2 * gs], I, H, xq)
+            hv = g / (1.0 + np.exp(-g)) * u
+            for b0 in range(0, I, 128):
+                blk = hv[b0:b0 + 128]
+                amax = float(np.abs(blk).max())
+                kk = oracle.ue8m0_for_amax(amax) - 127
+                total += blk.size
+                if amax > 0 and (abs(amax / (448.0 * 2.0 ** kk) - 1) < delta
+                                 or abs(amax / (448.0 * 2.0 ** (kk - 1)) - 1) < delta):
+                    n += blk.size
+                    continue
+                r = np.abs(blk) / 2.0 ** kk
+                pos_i = np.clip(np.searchsorted(mids, r), 1, len(mids) - 1)
+                d = np.minimum(np.abs(r - mids[pos_i - 1]) / steps[pos_i - 1],
+                               np.abs(r - mids[pos_i]) / steps[pos_i])
+                n += int((d < delta).sum())
+    return n, total
+
+
 def assert_close_e2m1(y, ref, bound, what=""):
     """Within the usual tolerance once each row's possible code flips are
     allowed for; cosine >= 0.9999."""

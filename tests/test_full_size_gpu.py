@@ -73,6 +73,56 @@ STACK_REL_MAX_ERR = 5e-2
 STACK_MIN_COS = 0.9999
 
 
+def test_stack_40_layers_batch1_every_layer():
+    """40 layers of 128 experts (96 GB resident), one token: the slot-major
+    path with the RMSNorm fused into its prep kernel at H = 4096, one cached
+    graph -- the benchmarked decode step.  Every layer is checked on the GPU's
+    own residual at the layer tolerance, then the free-running result."""
+    E, T, L = 128, 1, 40
+    cfg = moe.config(E, H, I, K, T)
+    h = moe.moe_ffn_create(cfg, 0)
+    sets = []
+    try:
+        sets = [fill_layer(h, cfg, layer=l) for l in range(L)]
+        idx = np.stack([synth.routing_uniform(T, E, K, seed=300 + l) for l in range(L)])
+        w = np.stack([synth.routing_weights(T, K, seed=300 + l) for l in range(L)])
+        x0 = synth.activations_f32(T, H, seed=11)
+        x = torch.from_numpy(x0.copy()).cuda()
+        it, wt = torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda()
+        moe.moe_stack_forward(h, x, [s.table for s in sets], it, wt, L, T)
+        torch.cuda.synchronize()
+        assert moe.moe_ffn_status(h) == moe.MOE_OK
+        xs = x.cpu().numpy()
+        assert np.isfinite(xs).all()
+        xl = torch.from_numpy(x0.copy()).cuda()
+        res = [x0]
+        for l in range(L):
+            moe.moe_stack_forward(h, xl, [sets[l].table], it[l], wt[l], 1, T)
+            res.append(xl.cpu().numpy())
+        assert np.array_equal(res[-1], xs)          # the graph is exactly these launches
+        layers = []
+        for l in range(L):
+            c, sc = host_experts(H, I, idx[l, 0], layer=l, E=E)
+            layers.append((c, sc, H, I))
+        for l in range(L):
+            xin = res[l].astype(np.float64)
+            ref = oracle.moe_stack([layers[l]], xin, idx[l:l + 1], w[l:l + 1], nthreads=THREADS)
+            assert_close(res[l + 1] - xin, ref - xin, f"batch-1 stack layer {l}")
+        ref = oracle.moe_stack(layers, x0.astype(np.float64), idx, w, nthreads=THREADS)
+        rel, cos = errors(xs, ref)
+        assert rel <= STACK_REL_MAX_ERR and cos >= STACK_MIN_COS, \
+            f"40-layer batch-1 stack: max|err|/rms={rel:.3e} cos={cos:.8f}"
+        # the whole step again: bit-identical
+        x2 = torch.from_numpy(x0.copy()).cuda()
+        moe.moe_stack_forward(h, x2, [s.table for s in sets], it, wt, L, T)
+        torch.cuda.synchronize()
+        assert np.array_equal(x2.cpu().numpy(), xs)
+    finally:
+        del sets
+        moe.moe_ffn_destroy(h)
+        torch.cuda.empty_cache()
+
+
 def test_stack_40_layers_batch32_sampled_token():
     """40 layers of 128 experts (96 GB resident), 32 tokens, one cached graph."""
     E, T, L = 128, 32, 40
