@@ -61,6 +61,11 @@ WORKLOADS = {
                              steps=1000),
     "layer_b32_arrival": dict(E=384, H=4096, I=2880, k=6, T=32, L=1, act="e4m3", dist="clustered_arrival",
                               steps=1000),
+    # a compute-bound shape of the same formats: 8 experts, each chosen by all
+    # 2048 tokens (M = 2048 rows per expert), E4M3 activations x E2M1 weights --
+    # 1.16 TFLOP a step against 150 MB of weights, far right of the ridge point
+    "gemm_e8_b2048": dict(E=8, H=4096, I=2880, k=8, T=2048, L=1, act="e4m3", dist="uniform", steps=20,
+                          bound="tensor"),
 }
 SHARING_POOL, SHARING_CLUSTERS, SHARING_SIG_LAYERS = 256, 8, 8
 # host-resident experts: the 384 experts of the layer in page-locked host memory,
@@ -81,6 +86,21 @@ def peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+# dense tensor rates relative to bf16 (nominal per-GPU figures: bf16 2.25,
+# fp8 / kind::mxf8f6f4 4.5, fp4 / kind::mxf4 13.5 PFLOP/s)
+FP8_PER_BF16, FP4_PER_BF16 = 2.0, 6.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def tensor_peak_bf16():
+    """Measured dense bf16 TFLOP/s (burst: a kernel timed alone) and its kind."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def cores():
@@ -388,9 +408,15 @@ def run_ours(args, wl):
     gmin = {"auto": 0, "slot": T + 1, "group": 1}[args.path]
     cfg = moe.config(E, H, I, k, T, act_mode=act, out_dtype=moe.MOE_OUT_F32, gemm_min_tokens=gmin)
     grouped = T >= (gmin or moe.DEFAULT_GEMM_MIN_TOKENS)
-    launches_per_layer = 4 if grouped else 2        # route, prep, layer, combine | prep, layer
-    kernel = "k_glayer" if grouped else "k_layer"
+    # the E4M3 expert-major path's MMA: as asked, or the library's choice (auto)
+    f8 = grouped and wl["act"] == "e4m3" and (args.mma == "f8" or (args.mma == "auto" and T * k >= 128 * E))
+    # route, prep, layer, combine | route, prep, gate/up, h quantizer, down, combine | prep, layer
+    launches_per_layer = (6 if f8 else 4) if grouped else 2
+    kernel = ("k_f8gemm" if f8 else "k_glayer") if grouped else "k_layer"
     h = moe.moe_ffn_create(cfg, local)
+    if grouped and wl["act"] == "e4m3":
+        moe.moe_ffn_set_mma_kind(h, {"auto": moe.MOE_MMA_AUTO, "pieces": moe.MOE_MMA_MXF4_PIECES,
+                                     "f8": moe.MOE_MMA_MXF8F6F4}[args.mma])
     nc, ns = synth.expert_sizes(H, I)
     tc = torch.empty(nc, dtype=torch.uint8, device="cuda")
     ts = torch.empty(ns, dtype=torch.uint8, device="cuda")
@@ -502,7 +528,8 @@ def run_ours(args, wl):
     stream.synchronize()
     ms_ph, n_ph = moe.moe_ffn_profile_read(h)
     moe.moe_ffn_profile_enable(h, False)
-    ly_ms = ms_ph[moe.MOE_PHASE_GATE_UP] / max(1, n_ph[moe.MOE_PHASE_GATE_UP])
+    # the layer's MMA kernel time per forward (the kind::mxf8f6f4 path: its two launches)
+    ly_ms = ms_ph[moe.MOE_PHASE_GATE_UP] / max(1, n_ph[moe.MOE_PHASE_GATE_UP] // (2 if f8 else 1))
     pr_ms = ms_ph[moe.MOE_PHASE_PREP] / max(1, n_ph[moe.MOE_PHASE_PREP])
     ro_ms = ms_ph[moe.MOE_PHASE_ROUTE] / max(1, n_ph[moe.MOE_PHASE_ROUTE])
     co_ms = ms_ph[moe.MOE_PHASE_DOWN] / max(1, n_ph[moe.MOE_PHASE_DOWN])
@@ -544,6 +571,22 @@ def run_ours(args, wl):
     else:
         achieved = ly_bytes / (ly_ms / 1000.0) / 1e9
     traffic = traffic_record(kernel, args.workload, wl["act"], ly_bytes)
+    tensor = None
+    if wl.get("bound") == "tensor":
+        # the two projections' MMA flops per forward over the layer kernels' time,
+        # against the dense rate of the MMA's kind (E4M3 x E2M1: kind::mxf8f6f4,
+        # the fp8 rate; E2M1 x E2M1: kind::mxf4, the fp4 rate), derived from the
+        # measured bf16 rate by the nominal ratios
+        flops = 2.0 * T * k * 3 * H * I
+        bf16, bf16_kind = tensor_peak_bf16()
+        tf = flops / (ly_ms / 1000.0) / 1e12
+        rate = FP4_PER_BF16 if wl["act"] == "e2m1" else FP8_PER_BF16
+        tensor = {"bound": "tensor", "kernel": kernel, "achieved": tf, "peak": bf16 * rate,
+                  "peak_kind": f"{bf16_kind} bf16 {bf16:.1f} TFLOP/s x {rate:g} (nominal ratio of the MMA kind)",
+                  "unit": "TFLOP/s", "frac": tf / (bf16 * rate),
+                  "frac_of_fp4_peak": tf / (bf16 * FP4_PER_BF16),
+                  "flops_per_launch": flops, "traffic": None,
+                  "timing": f"events around each launch (launches separated): {ly_ms * 1e3:.2f} us per forward"}
 
     # ---- the router ahead of the path (logits = W x, top-k, softmax): one
     # launch per call up to 8 tokens, two above; timed (a) back to back in a CUDA graph of nrg calls,
@@ -651,7 +694,8 @@ def run_ours(args, wl):
             "data": "synthetic",
             "config": {"workload": args.workload, "layers": L, "experts": E, "hidden": H, "inter": I,
                        "topk": k, "tokens_per_step": T, "routing": wl["dist"], "activations": wl["act"],
-                       "path": "expert-major (grouped)" if grouped else "slot-major",
+                       "path": ("expert-major, kind::mxf8f6f4" if f8 else "expert-major (grouped)")
+                       if grouped else "slot-major",
                        "parallelism": f"replicas{world}",
                        "l2": f"inputs larger than L2: {resident:.1f} GB resident experts"
                              + (", consecutive steps share no expert" if T == 1 and L == 1 else ""),
@@ -663,7 +707,7 @@ def run_ours(args, wl):
             "bytes_per_step": bytes_step,
             "phase_us": {"route": ro_ms * 1e3, "prep": pr_ms * 1e3, "layer": ly_ms * 1e3,
                          "combine": co_ms * 1e3},
-            "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved,
+            "roofline": tensor if tensor is not None else {"bound": "hbm", "kernel": kernel, "achieved": achieved,
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes_per_launch": ly_bytes,
@@ -838,6 +882,9 @@ def main():
                     help="layer path: the library's choice for T, or forced slot-major / expert-major")
     ap.add_argument("--act", choices=["bf16", "e4m3", "e2m1"], default=None,
                     help="activation numerics (default: the workload's)")
+    ap.add_argument("--mma", choices=["auto", "pieces", "f8"], default="auto",
+                    help="E4M3 expert-major path: the library's choice (auto), kind::mxf8f6f4 (f8) or "
+                         "kind::mxf4 with E2M1 pieces")
     args = ap.parse_args()
     wl = dict(WORKLOADS[args.workload])
     if args.act:

@@ -37,8 +37,14 @@ EXPORTS = [
     "moe_router_topk", "moe_router_select", "moe_batch_plan", "moe_batch_distinct",
     "moe_expert_cache_create", "moe_expert_cache_fetch", "moe_expert_cache_prefetch", "moe_expert_cache_slot",
     "moe_expert_cache_stats", "moe_expert_cache_destroy", "moe_ffn_test_set_wait", "moe_ffn_test_fail_allocs",
+    "moe_ffn_test_copy_h",
+    "moe_ffn_set_mma_kind",
     "moe_ffn_profile_layer_only",
 ]
+
+MOE_MMA_AUTO = 0
+MOE_MMA_MXF4_PIECES = 1
+MOE_MMA_MXF8F6F4 = 2
 
 MOE_PHASE_PREP = 0
 MOE_PHASE_GATE_UP = 1
@@ -109,6 +115,8 @@ def lib() -> ctypes.CDLL:
             "moe_expert_cache_destroy": (None, [P]),
             "moe_ffn_test_set_wait": (I, [P, ctypes.c_ulonglong, I]),
             "moe_ffn_test_fail_allocs": (None, [I]),
+            "moe_ffn_test_copy_h": (I, [P, P, P, I, P]),
+            "moe_ffn_set_mma_kind": (I, [P, I]),
             "moe_ffn_profile_layer_only": (I, [P, I]),
         }
         for name, (res, args) in sig.items():
@@ -225,6 +233,11 @@ def moe_ffn_profile_layer_only(h, on: bool = True) -> None:
     _check(lib().moe_ffn_profile_layer_only(h, 1 if on else 0), "moe_ffn_profile_layer_only")
 
 
+def moe_ffn_set_mma_kind(h, kind: int) -> None:
+    """The expert-major path's MMA in the E4M3 mode (MOE_MMA_*)."""
+    _check(lib().moe_ffn_set_mma_kind(h, int(kind)), "moe_ffn_set_mma_kind")
+
+
 def moe_ffn_status(h, stream=None) -> int:
     """Returns the (cleared) sticky device status code; does not raise."""
     return lib().moe_ffn_status(h, _s(stream))
@@ -237,6 +250,17 @@ def moe_ffn_forward_noalloc(cfg: moe_ffn_config, device: int, x, topk_idx, topk_
     _check(lib().moe_ffn_forward_noalloc(ctypes.byref(cfg), int(device), _p(x), _p(topk_idx),
                                          _p(topk_w), ctypes.byref(table), _p(y), int(T),
                                          _p(status), _s(stream)), "moe_ffn_forward_noalloc")
+
+
+def moe_ffn_test_copy_h(h, n: int, inter: int, stream=None):
+    """Test hook: (h [n][inter] fp32, perm [n] int32) of the last kind::mxf8f6f4
+    expert-major call, as device tensors (see include/moe_ffn.h)."""
+    import torch
+
+    hd = torch.empty((n, inter), dtype=torch.float32, device="cuda")
+    pd = torch.empty(n, dtype=torch.int32, device="cuda")
+    _check(lib().moe_ffn_test_copy_h(h, hd.data_ptr(), pd.data_ptr(), int(n), _s(stream)), "moe_ffn_test_copy_h")
+    return hd, pd
 
 
 def moe_ffn_test_set_wait(h, wait_ns: int, withhold: bool) -> None:

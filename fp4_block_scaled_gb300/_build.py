@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_ffn.so")
-SOURCES = ["api.cu", "gemv.cu", "group.cu", "pack.cu", "route.cu", "router.cu", "actquant.cu", "noalloc.cu",
+SOURCES = ["api.cu", "gemv.cu", "group.cu", "gemm8.cu", "pack.cu", "route.cu", "router.cu", "actquant.cu", "noalloc.cu",
            "sched.cpp", "cache.cpp"]
 HEADERS = ["common.cuh", "internal.h", "layout.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -61,6 +61,7 @@ struct moe_ffn {
     GemvArgs base;              // workspace pointers, problem sizes (slot-major path)
     GroupArgs gbase;            // the same for the expert-major path
     int gemm_min_tokens;        // T >= this takes the expert-major path
+    int mma_kind;               // MOE_MMA_*: the expert-major path's MMA in the E4M3 mode
     int* status;
     uint8_t* in_stage;          // device staging for moe_ffn_forward_host: x | idx | w, packed per T
     void* y_stage;
@@ -166,18 +167,25 @@ GroupArgs group_args(const moe_ffn* h, int T, const int32_t* idx, const float* w
 // (x_bf16 == nullptr) the residual x_resid += moe(rmsnorm(x_resid)).
 cudaError_t launch_layer(const moe_ffn* h, const uint16_t* x_bf16, float* x_resid, const int32_t* idx,
                          const float* w, const moe_expert_table* tbl, void* y, int T, cudaStream_t s,
-                         Profiler* prof)
+                         Profiler* prof, bool ssq_in = false)
 {
     if (T >= h->gemm_min_tokens) {
         GroupArgs a = group_args(h, T, idx, w, tbl);
         a.x_bf16 = x_bf16;
         a.x_resid = x_resid;
         a.y = y;
+        // E4M3: kind::mxf8f6f4 where asked for, and by default where experts hold
+        // many slots on average (the tensor-bound shapes; on HBM-bound decode
+        // batches the pieces path streams the weights faster)
+        if (a.act_e4m3 && (h->mma_kind == MOE_MMA_MXF8F6F4 ||
+                           (h->mma_kind == MOE_MMA_AUTO && (long long)T * a.topk >= 128LL * a.E)))
+            return launch_f8_layer(a, s, true, prof);
         return launch_group_layer(a, s, true, prof);
     }
     GemvArgs a = layer_args(h, T, idx, w, tbl);
     a.x_bf16 = x_bf16;
     a.x_resid = x_resid;
+    a.ssq_in = ssq_in ? 1 : 0;
     a.y = y;
     return launch_gemv_layer(a, s, true, prof);
 }
@@ -247,7 +255,8 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     h->device = device;
     if (cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
         gemv_init_device() != cudaSuccess || route_init_device() != cudaSuccess ||
-        group_init_device() != cudaSuccess || router_init_device() != cudaSuccess) {
+        group_init_device() != cudaSuccess || f8_init_device() != cudaSuccess ||
+        router_init_device() != cudaSuccess) {
         delete h;
         return MOE_ERR_CUDA;
     }
@@ -259,6 +268,9 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     const bool grouped = T >= h->gemm_min_tokens;      // the expert-major path can be taken
     GroupWorkspaceSizes gw{};
     if (grouped) gw = group_workspace_sizes(T, k, cfg->num_experts, H, I, h->sms, e4m3);
+    F8WorkspaceSizes fw{};
+    if (grouped && e4m3) fw = f8_workspace_sizes(T, k, cfg->num_experts, H, I);
+    h->mma_kind = MOE_MMA_AUTO;
 
     // one allocation, carved into aligned pieces
     size_t off = 0;
@@ -270,13 +282,14 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     size_t o_status = take(sizeof(int)), o_sync = take(kGemvSyncInts * sizeof(int));
     size_t o_xq = take(g.xq), o_xsf = take(g.xsf), o_hq = take(g.hq), o_hsf = take(g.hsf);
     size_t o_pgu = take(g.part_gu * 8), o_pdn = take(g.part_dn * 8);
-    size_t o_hraw = take(g.hraw), o_hpair = take(g.hpair);
+    size_t o_hraw = take(g.hraw), o_hpair = take(g.hpair), o_ssq = take(g.ssq);
     size_t o_gsync = take(kGemvSyncInts * sizeof(int));
     size_t o_gcnt = take(gw.counts), o_goff = take(gw.offsets), o_gperm = take(gw.perm);
     size_t o_ginv = take(gw.inv), o_gbase = take(gw.gbase), o_ggrp = take(gw.groups);
     size_t o_gxg = take(gw.xg), o_gxgsf = take(gw.xgsf), o_ghg = take(gw.hg), o_ghgsf = take(gw.hgsf);
     size_t o_gobuf = take(gw.obuf), o_gpgu = take(gw.part_gu), o_gpdn = take(gw.part_dn);
     size_t o_ghraw = take(gw.hraw), o_ghpair = take(gw.hpair);
+    size_t o_fxb = take(fw.xb8), o_fxbsf = take(fw.xb8sf), o_fhb = take(fw.hb8), o_fhbsf = take(fw.hb8sf);
     size_t o_rlog = take((size_t)T * cfg->num_experts * 4), o_rtk = take((size_t)T * sizeof(int));
     const size_t rpart_bytes = T > 8 ? (size_t)router_max_splits(H) * T * cfg->num_experts * 4 : 0;
     size_t o_rpart = take(rpart_bytes);
@@ -316,6 +329,7 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     a.act_e2m1 = cfg->act_mode == MOE_ACT_E2M1_UE8M0_32;
     a.hraw = e4m3 ? (float*)(b + o_hraw) : nullptr;
     a.hpair = e4m3 ? (int*)(b + o_hpair) : nullptr;
+    a.ssq = (float*)(b + o_ssq);
     GroupArgs& ga = h->gbase;
     memset(&ga, 0, sizeof(ga));
     ga.topk = k;
@@ -345,6 +359,12 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
         ga.part_dn = (uint64_t*)(b + o_gpdn);
         ga.hraw = e4m3 ? (float*)(b + o_ghraw) : nullptr;
         ga.hpair = e4m3 ? (int*)(b + o_ghpair) : nullptr;
+        if (e4m3) {
+            ga.xb8 = (uint8_t*)(b + o_fxb);
+            ga.xb8sf = (uint8_t*)(b + o_fxbsf);
+            ga.hb8 = (uint8_t*)(b + o_fhb);
+            ga.hb8sf = (uint8_t*)(b + o_fhbsf);
+        }
     }
     h->rlogits = (float*)(b + o_rlog);
     h->rtickets = (int*)(b + o_rtk);
@@ -585,7 +605,7 @@ int moe_stack_forward(moe_ffn_t h, float* x, const moe_expert_table* tbls,
     for (int l = 0; l < L && le == cudaSuccess; l++)
         le = launch_layer(h, nullptr, x, topk_idx + (size_t)l * T * h->cfg.topk,
                           topk_w + (size_t)l * T * h->cfg.topk, &tbls[l], nullptr, T, h->cap_stream,
-                          nullptr);
+                          nullptr, l > 0);     // each layer leaves the next one its RMSNorm partials
     e = cudaStreamEndCapture(h->cap_stream, &graph);
     if (le != cudaSuccess || e != cudaSuccess) {
         if (graph) cudaGraphDestroy(graph);
@@ -608,7 +628,29 @@ int moe_ffn_profile_layer_only(moe_ffn_t h, int on)
     return MOE_OK;
 }
 
+int moe_ffn_set_mma_kind(moe_ffn_t h, int kind)
+{
+    if (!h || (kind != MOE_MMA_AUTO && kind != MOE_MMA_MXF4_PIECES && kind != MOE_MMA_MXF8F6F4))
+        return MOE_ERR_INVALID_ARG;
+    h->mma_kind = kind;
+    return MOE_OK;
+}
+
 void moe_ffn_test_fail_allocs(int n) { g_fail_allocs.store(n > 0 ? n : 0); }
+
+int moe_ffn_test_copy_h(moe_ffn_t h, float* h_dst, int32_t* perm_dst, int n, void* stream)
+{
+    if (!h || !h->gbase.hraw || !h->gbase.xb8 || !h_dst || !perm_dst || n < 0 ||
+        (long long)n > (long long)h->cfg.max_tokens * h->cfg.topk)
+        return MOE_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t hb = (size_t)n * h->cfg.inter * sizeof(float);
+    if (cudaMemcpyAsync(h_dst, h->gbase.hraw, hb, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(perm_dst, h->gbase.perm, (size_t)n * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
 
 int moe_ffn_test_set_wait(moe_ffn_t h, unsigned long long wait_ns, int withhold)
 {

@@ -41,6 +41,38 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
+// RMSNorm (unit weight) denominator sqrt(mean(x^2) + eps) of one row of H
+// floats, by the whole CTA (every thread calls it; at most 32 warps): the sum
+// of squares in a fixed order -- eight loads in flight per thread, added as
+// one element at a time (i = tid, tid + blockDim, ...), then the warps' sums
+// in warp order.  s_red: 33 floats of shared memory.
+__device__ __forceinline__ float block_rms_den(const float* xr, int H, float eps, float* s_red)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float ss = 0.0f;
+    for (int i0 = threadIdx.x; i0 < H; i0 += 8 * (int)blockDim.x) {
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            const int i = i0 + q * (int)blockDim.x;
+            v[q] = i < H ? __ldcg(xr + i) : 0.0f;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; q++)
+            if (i0 + q * (int)blockDim.x < H) ss = fmaf(v[q], v[q], ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) s_red[warp] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float tot = 0.0f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); w++) tot += s_red[w];
+        s_red[32] = sqrtf(tot / (float)H + eps);
+    }
+    __syncthreads();
+    return s_red[32];
+}
+
 // ---------------------------------------------------------------- mbarrier / bulk copy
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)

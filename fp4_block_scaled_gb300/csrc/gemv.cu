@@ -266,14 +266,15 @@ __device__ __forceinline__ void write_pieces64_small(float v0, float v1, int lan
 
 // ------------------------------------------------------------------ k_prep
 
+constexpr int kPrepParts = 1024;
+
 // grid (T, ceil(H/64 / 8)), 256 threads: one warp per 64 elements.
 __global__ void __launch_bounds__(256) k_prep(GemvArgs a)
 {
     const int t = blockIdx.x;
     const int H = a.H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __shared__ float s_red[8];
-    __shared__ float s_den;
+    __shared__ float s_part[kPrepParts];   // the RMSNorm's partial sums of squares, per 32 rows
     __shared__ uint4 s_tr[8][32];          // per warp: the pieces' byte transpose
 
     // k_layer reads nothing this kernel or the previous layer writes before its
@@ -282,32 +283,40 @@ __global__ void __launch_bounds__(256) k_prep(GemvArgs a)
     pdl_wait();
     float den = 1.0f;
     if (a.x_resid) {
-        // RMSNorm with unit weight: sum of squares in a fixed tree order
-        const float* xr = a.x_resid + (size_t)t * H;
+        // RMSNorm with unit weight.  The sum of squares in one fixed order: per
+        // 32 rows a butterfly sum of the squares (lane l: row 32 g + l), then the
+        // H / 32 partials added lane-strided in index order and a butterfly sum
+        // -- the order in which a stack's layer leaves them for the next one
+        // (ssq_in: read instead of the row, 128 floats instead of 4096)
+        const int ng = H / 32, nw = (int)(blockDim.x >> 5);
         float ss = 0.0f;
-        // eight loads in flight per thread, then added in the same order as
-        // one element at a time (i = tid, tid + blockDim, ...)
-        for (int i0 = threadIdx.x; i0 < H; i0 += 8 * (int)blockDim.x) {
-            float v[8];
+        if (a.ssq_in) {
+            const float* part = a.ssq + (size_t)t * ng;
+            for (int q = lane; q < ng; q += 32) ss += __ldcg(part + q);
+        } else {
+            const float* xr = a.x_resid + (size_t)t * H;
+            for (int g0 = 0; g0 < ng; g0 += kPrepParts) {
+                const int gn = min(kPrepParts, ng - g0);
+                // warp w: groups w, w + nw, ..., eight loads in flight
+                for (int q0 = warp; q0 < gn; q0 += 8 * nw) {
+                    float v[8];
 #pragma unroll
-            for (int q = 0; q < 8; q++) {
-                const int i = i0 + q * (int)blockDim.x;
-                v[q] = i < H ? __ldcg(xr + i) : 0.0f;
+                    for (int k = 0; k < 8; k++) {
+                        const int q = q0 + nw * k;
+                        v[k] = q < gn ? __ldcg(xr + (size_t)(g0 + q) * 32 + lane) : 0.0f;
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; k++) {
+                        const float p = warp_sum(__fmul_rn(v[k], v[k]));
+                        if (q0 + nw * k < gn && lane == 0) s_part[q0 + nw * k] = p;
+                    }
+                }
+                __syncthreads();
+                for (int q = lane; q < gn; q += 32) ss += s_part[q];
+                __syncthreads();
             }
-#pragma unroll
-            for (int q = 0; q < 8; q++)
-                if (i0 + q * (int)blockDim.x < H) ss = fmaf(v[q], v[q], ss);
         }
-        ss = warp_sum(ss);
-        if (lane == 0) s_red[warp] = ss;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float tot = 0.0f;
-            for (int w = 0; w < (int)(blockDim.x >> 5); w++) tot += s_red[w];
-            s_den = sqrtf(tot / (float)H + a.eps);
-        }
-        __syncthreads();
-        den = s_den;
+        den = sqrtf(warp_sum(ss) / (float)H + a.eps);
     }
     if (a.act_e4m3) {
         // x quantized to E4M3 under one ue8m0 scale per 128 elements (lane l holds
@@ -926,8 +935,13 @@ __device__ void epilogue(const GemvArgs& a, const StreamPlan& p, const Range& r,
             // group = (token t, tile): 128 output rows, one per thread
             const int t = (int)(group / p.ntiles), tile = (int)(group % p.ntiles);
             const size_t o = (size_t)t * a.H + (size_t)tile * kTileRows + row;
-            if (a.x_resid) a.x_resid[o] += v;
-            else if (a.out_f32) reinterpret_cast<float*>(a.y)[o] = v;
+            if (a.x_resid) {
+                const float xn = a.x_resid[o] + v;
+                a.x_resid[o] = xn;
+                // the next layer's RMSNorm: this warp's 32 rows' sum of squares
+                const float ss = warp_sum(__fmul_rn(xn, xn));
+                if (lane == 0) a.ssq[(size_t)t * (a.H / 32) + tile * 4 + quad] = ss;
+            } else if (a.out_f32) reinterpret_cast<float*>(a.y)[o] = v;
             else reinterpret_cast<__nv_bfloat16*>(a.y)[o] = __float2bfloat16_rn(v);
         }
     }
@@ -1130,6 +1144,7 @@ GemvWorkspaceSizes gemv_workspace_sizes(int T, int topk, int H, int I, int sms, 
     s.part_dn = (size_t)sms * kTileRows;
     s.hraw = e4m3 ? slots * I * sizeof(float) : 0;
     s.hpair = e4m3 ? slots * (size_t)((I + 127) / 128) * sizeof(int) : 0;
+    s.ssq = (size_t)T * (H / 32) * sizeof(float);
     return s;
 }
 

@@ -329,8 +329,7 @@ __global__ void __launch_bounds__(256) k_gprep(GroupArgs a)
     const int t = blockIdx.x;
     const int H = a.H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __shared__ float s_red[8];
-    __shared__ float s_den;
+    __shared__ float s_red[33];
     __shared__ int s_e[16], s_P[16], s_off[16], s_gb[16], s_cnt[16];
     __shared__ uint4 s_tr[8][32];          // per warp: the pieces' byte transpose
 
@@ -349,37 +348,8 @@ __global__ void __launch_bounds__(256) k_gprep(GroupArgs a)
         s_gb[threadIdx.x] = ok ? a.gbase[e] : 0;
         s_cnt[threadIdx.x] = ok ? a.counts[e] : 0;
     }
-    float den = 1.0f;
-    if (a.x_resid) {
-        // RMSNorm with unit weight: sum of squares in a fixed tree order
-        const float* xr = a.x_resid + (size_t)t * H;
-        float ss = 0.0f;
-        // eight loads in flight per thread, then added in the same order as
-        // one element at a time (i = tid, tid + blockDim, ...)
-        for (int i0 = threadIdx.x; i0 < H; i0 += 8 * (int)blockDim.x) {
-            float v[8];
-#pragma unroll
-            for (int q = 0; q < 8; q++) {
-                const int i = i0 + q * (int)blockDim.x;
-                v[q] = i < H ? __ldcg(xr + i) : 0.0f;
-            }
-#pragma unroll
-            for (int q = 0; q < 8; q++)
-                if (i0 + q * (int)blockDim.x < H) ss = fmaf(v[q], v[q], ss);
-        }
-        ss = warp_sum(ss);
-        if (lane == 0) s_red[warp] = ss;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float tot = 0.0f;
-            for (int w = 0; w < (int)(blockDim.x >> 5); w++) tot += s_red[w];
-            s_den = sqrtf(tot / (float)H + a.eps);
-        }
-        __syncthreads();
-        den = s_den;
-    } else {
-        __syncthreads();
-    }
+    const float den = a.x_resid ? block_rms_den(a.x_resid + (size_t)t * H, H, a.eps, s_red) : 1.0f;
+    __syncthreads();
     const int kgt = H / 128;
     auto xval = [&](int i) {
         return a.x_resid ? __bfloat162float(__float2bfloat16_rn(a.x_resid[(size_t)t * H + i] / den))
@@ -1202,8 +1172,9 @@ __global__ void __launch_bounds__(256) k_gcombine(GroupArgs a)
     pdl_trigger();
     if (threadIdx.x < a.topk) {
         s_P[threadIdx.x] = a.inv[t * a.topk + threadIdx.x];
-        // the E2M1 mode applies the routing weight here (the other modes fold it into h)
-        s_w[threadIdx.x] = a.act_e2m1 ? a.w[t * a.topk + threadIdx.x] : 1.0f;
+        // the E2M1 mode and the kind::mxf8f6f4 path apply the routing weight
+        // here (the piece modes fold it into h)
+        s_w[threadIdx.x] = (a.act_e2m1 || a.o_unweighted) ? a.w[t * a.topk + threadIdx.x] : 1.0f;
     }
     __syncthreads();
     for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
@@ -1346,9 +1317,16 @@ cudaError_t launch_group_layer(const GroupArgs& a0, cudaStream_t s, bool pdl, Pr
     if (prof) prof->end(s);
     if (err != cudaSuccess) return err;
     if (prof) prof->begin(kPhaseDown, s);
-    err = glaunch((const void*)k_gcombine, dim3(a.T), dim3(256), 0, s, chain, args1);
+    err = launch_group_combine(a, s, chain);
     if (prof) prof->end(s);
     return err;
+}
+
+cudaError_t launch_group_combine(const GroupArgs& a0, cudaStream_t s, bool pdl)
+{
+    GroupArgs a = a0;
+    void* args[] = {&a};
+    return glaunch((const void*)k_gcombine, dim3(a.T), dim3(256), 0, s, pdl, args);
 }
 
 }  // namespace moe

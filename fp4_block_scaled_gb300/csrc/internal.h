@@ -48,6 +48,11 @@ struct GemvArgs {
     int debug_withhold;                 // test hook: CTA 0 never reports its finished gate/up groups
     int skip_prep;                      // measurement mode: launch the layer kernel alone (the
                                         // activation pieces of the previous call are reused)
+    // residual stream: per token, the sum of squares of each 32 rows of x that
+    // the layer's down projection wrote ([T][H / 32]); ssq_in: the previous
+    // layer left them for this layer's x (its RMSNorm reads them, not x)
+    float* ssq;
+    int ssq_in;
     // output (forward): y [T][H] fp32 or bf16
     void* y;
     int out_f32;
@@ -58,6 +63,7 @@ struct GemvArgs {
 struct GemvWorkspaceSizes {
     size_t xq, xsf, hq, hsf, part_gu, part_dn;
     size_t hraw, hpair;                 // bytes, E4M3 activation mode only
+    size_t ssq;                         // bytes
 };
 constexpr int kGemvSyncInts = 3;
 GemvWorkspaceSizes gemv_workspace_sizes(int T, int topk, int H, int I, int sms, bool e4m3);
@@ -181,6 +187,14 @@ struct GroupArgs {
     int* status;
     void* y;
     int out_f32;
+    // kind::mxf8f6f4 path (gemm8.cu): E4M3 rows of x and h per group, and
+    // their scale atoms (two per group and 128-K unit)
+    uint8_t* xb8;
+    uint8_t* xb8sf;
+    uint8_t* hb8;
+    uint8_t* hb8sf;
+    int o_unweighted;       // obuf holds unweighted down outputs: the combine applies w
+    int f8_gs;              // slots per group of the kind::mxf8f6f4 launch (set by its launcher)
 };
 
 struct GroupWorkspaceSizes {
@@ -190,6 +204,20 @@ struct GroupWorkspaceSizes {
 GroupWorkspaceSizes group_workspace_sizes(int T, int topk, int E, int H, int I, int sms, bool e4m3);
 cudaError_t group_init_device();
 cudaError_t launch_group_layer(const GroupArgs& a, cudaStream_t s, bool pdl, Profiler* prof);
+// y[t] = sum over the token's slots of w * obuf (or x += that), group.cu
+cudaError_t launch_group_combine(const GroupArgs& a, cudaStream_t s, bool pdl);
+
+// The expert-major path with E4M3 activations multiplied directly
+// (tcgen05.mma kind::mxf8f6f4, gemm8.cu): groups of up to kF8GroupSlots slots
+// of one expert, one MMA column per slot.
+constexpr int kF8GroupSlots = 240;         // groups of the form for tensor-bound shapes
+constexpr int kF8GroupSlotsNarrow = 64;    // ... and for HBM-bound decode batches
+struct F8WorkspaceSizes {
+    size_t xb8, xb8sf, hb8, hb8sf;      // bytes
+};
+F8WorkspaceSizes f8_workspace_sizes(int T, int topk, int E, int H, int I);
+cudaError_t f8_init_device();
+cudaError_t launch_f8_layer(const GroupArgs& a, cudaStream_t s, bool pdl, Profiler* prof);
 // library default of moe_ffn_config.gemm_min_tokens
 constexpr int kDefaultGemmMinTokens = MOE_DEFAULT_GEMM_MIN_TOKENS;
 int route_max_experts();

@@ -281,16 +281,36 @@ int moe_stack_forward(moe_ffn_t h, float* x, const moe_expert_table* tbls,
 enum {
     MOE_PHASE_PREP = 0,      /* activation prep (and fused RMSNorm)         */
     MOE_PHASE_GATE_UP = 1,   /* the layer kernel: gate/up + SwiGLU + down
-                                (+ the combine on the slot-major path)      */
+                                (+ the combine on the slot-major path); on
+                                the kind::mxf8f6f4 expert-major path its two
+                                launches, gate/up and down                  */
     MOE_PHASE_DOWN = 2,      /* the combine kernel (expert-major path)      */
     MOE_PHASE_ROUTE = 3,     /* token -> expert grouping (moe_ffn_route and
                                 the expert-major path's first kernel)       */
-    MOE_PHASE_ACT_QUANT = 4, /* E4M3 activation quantizer                   */
+    MOE_PHASE_ACT_QUANT = 4, /* E4M3 activation quantizer (and h's, on the
+                                kind::mxf8f6f4 expert-major path)           */
     MOE_PHASE_ROUTER = 5,    /* router logits + top-k + softmax (moe_router_topk) */
     MOE_NUM_PHASES = 8
 };
 int moe_ffn_profile_enable(moe_ffn_t h, int on);
 int moe_ffn_profile_read(moe_ffn_t h, double* ms, int* launches);
+
+/* The tensor-core operation of the expert-major path in the E4M3 mode
+ * (MOE_ACT_E4M3_UE8M0_128).  MOE_MMA_MXF8F6F4: tcgen05.mma kind::mxf8f6f4,
+ * the E2M1 weights times the E4M3 activations as they are, one slot per MMA
+ * column, groups of up to 240 slots of an expert where T * topk >= 128 * E
+ * (else up to 64), six launches (route, prep, gate/up, h quantizer, down,
+ * combine).  MOE_MMA_MXF4_PIECES: kind::mxf4, each E4M3 value carried as 8
+ * E2M1 pieces, groups of up to 8 slots.  MOE_MMA_AUTO (the default): the
+ * first where T * topk >= 128 * E (tensor-bound shapes, where it is several
+ * times faster), else the second (HBM-bound decode batches, where it streams
+ * the weights faster).  Both compute the same function within the float
+ * tolerance ([8GB] §三个从不抛错的 Bug, item 2, fixes the E4M3 +
+ * ue8m0-per-128 activation format; the pages leave the MMA to the build).
+ * The bf16 and E2M1 modes and the slot-major path are not affected.
+ * Errors: INVALID_ARG. */
+enum { MOE_MMA_AUTO = 0, MOE_MMA_MXF4_PIECES = 1, MOE_MMA_MXF8F6F4 = 2 };
+int moe_ffn_set_mma_kind(moe_ffn_t h, int kind);
 
 /* Measurement mode of the slot-major path (the sources have no counterpart;
  * it serves timing): while on, moe_ffn_forward calls that take the
@@ -348,8 +368,17 @@ int moe_ffn_forward_noalloc(const moe_ffn_config* cfg, int device, const void* x
  *
  * moe_ffn_test_fail_allocs: the next n device or page-locked allocations the
  * library makes (any handle, cache or staging buffer) fail as if out of
- * memory; n = 0 clears.  The calls that make them return MOE_ERR_OOM. */
+ * memory; n = 0 clears.  The calls that make them return MOE_ERR_OOM.
+ *
+ * moe_ffn_test_copy_h: after an expert-major call in the E4M3 mode on the
+ * kind::mxf8f6f4 path, copies (enqueued on `stream`, device to device) the
+ * fp32 h = silu(g) u of each of the call's first n sorted slots, before its
+ * E4M3 quantization, into h_dst ([n][inter] floats) and the slot order into
+ * perm_dst ([n] int32: sorted position -> slot t * topk + k), so that a test
+ * can check h itself and the down projection on the GPU's own quantized h.
+ * Errors: INVALID_ARG (no such workspace on this handle, n out of range). */
 int moe_ffn_test_set_wait(moe_ffn_t h, unsigned long long wait_ns, int withhold);
+int moe_ffn_test_copy_h(moe_ffn_t h, float* h_dst, int32_t* perm_dst, int n, void* stream);
 void moe_ffn_test_fail_allocs(int n);
 
 /* Wait for `stream`, then return and clear the sticky device status:

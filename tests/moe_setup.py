@@ -60,12 +60,14 @@ class Layer:
     "auto" leaves the library default."""
 
     def __init__(self, E, H, I, k, max_tokens=8, out=moe.MOE_OUT_F32, seed=0, layer=0, act=moe.MOE_ACT_BF16,
-                 path="slot"):
+                 path="slot", mma=None):
         self.E, self.H, self.I, self.k = E, H, I, k
         self.act = act
         gmin = {"slot": max_tokens + 1, "group": 1, "auto": 0}[path]
         self.cfg = moe.config(E, H, I, k, max_tokens, out_dtype=out, act_mode=act, gemm_min_tokens=gmin)
         self.h = moe.moe_ffn_create(self.cfg, 0)
+        if mma is not None:
+            moe.moe_ffn_set_mma_kind(self.h, mma)
         self.es = fill_layer(self.h, self.cfg, layer=layer, seed=seed)
         self.seed, self.layer = seed, layer
         self.out = out
@@ -190,6 +192,127 @@ def e4m3_flip_candidates(H, I, E, x_bits, idx, layer=0, seed=0, delta=1e-4):
                                np.abs(r - mids[pos_i]) / steps[pos_i])
                 n += int((d < delta).sum())
     return n, total
+
+
+def e4m3_flip_bound(H, I, E, x_bits, idx, w, layer=0, seed=0, delta=1e-4):
+    """How far y[t] may move (per output row) because an element of h,
+    computed in fp32 on the GPU and in fp64 by the oracle, takes the other E4M3
+    neighbour: each element of the oracle's h within delta (relative to the
+    local grid step) of a midpoint moves by that step; every element of a
+    128-block (64 for the last) whose maximum lies within a relative delta of a
+    scale boundary 448 * 2^k by up to the largest E4M3 step at the larger
+    candidate scale.  Each moves y by w times its down column.  Returns
+    (bound [T][H], number of such elements)."""
+    e2m1 = np.array([oracle.e2m1_value(c) for c in range(16)])
+    pos = np.unique([oracle.e4m3_value(c) for c in range(127)])
+    mids = (pos[1:] + pos[:-1]) / 2.0
+    steps = pos[1:] - pos[:-1]
+    T, k = idx.shape
+    codes, scales = host_experts(H, I, idx.reshape(-1), layer=layer, seed=seed, E=E)
+    gc, gs = I * H // 2, I * H // 32
+    bound = np.zeros((T, H))
+    n_amb = 0
+    for t in range(T):
+        xf = (x_bits[t].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        xc, xsc = oracle.act_quant_e4m3(xf, 128)
+        xq = np.array([oracle.e4m3_value(int(c)) for c in xc]) * np.ldexp(
+            1.0, np.repeat(xsc.astype(np.int64), 128)[:H] - 127)
+        for j in range(k):
+            e = int(idx[t, j])
+            if e < 0 or e >= E:
+                continue
+            c, sc = codes[e], scales[e]
+            g = oracle.matvec(c[:gc], sc[:gs], I, H, xq)
+            u = oracle.matvec(c[gc:2 * gc], sc[gs:2 * gs], I, H, xq)
+            hv = g / (1.0 + np.exp(-g)) * u
+            dc = np.asarray(c[2 * gc:], np.uint8).reshape(H, I // 2)
+            ds = np.asarray(sc[2 * gs:], np.uint8).reshape(H, I // 32)
+            for b0 in range(0, I, 128):
+                blk = hv[b0:b0 + 128]
+                amax = float(np.abs(blk).max())
+                kk = oracle.ue8m0_for_amax(amax) - 127
+                if amax > 0 and (abs(amax / (448.0 * 2.0 ** kk) - 1) < delta
+                                 or abs(amax / (448.0 * 2.0 ** (kk - 1)) - 1) < delta):
+                    amb = [(i, float(steps.max()) * 2.0 ** (kk + 1)) for i in range(blk.size)]
+                else:
+                    r = np.abs(blk) / 2.0 ** kk
+                    pi = np.clip(np.searchsorted(mids, r), 1, len(mids) - 1)
+                    d_lo = np.abs(r - mids[pi - 1]) / steps[pi - 1]
+                    d_hi = np.abs(r - mids[pi]) / steps[pi]
+                    st = np.where(d_lo < d_hi, steps[pi - 1], steps[pi])
+                    amb = [(int(i), float(st[i]) * 2.0 ** kk) for i in np.nonzero(np.minimum(d_lo, d_hi) < delta)[0]]
+                for i, step in amb:
+                    ci = b0 + i
+                    byte = dc[:, ci // 2]
+                    nib = (byte >> 4) if ci & 1 else (byte & 15)
+                    col = e2m1[nib] * np.ldexp(1.0, ds[:, ci // 32].astype(np.int64) - 127)
+                    bound[t] += abs(float(w[t, j])) * np.abs(col) * step
+                    n_amb += 1
+    return bound, n_amb
+
+
+def assert_close_e4m3(y, ref, layer_args, what=""):
+    """The float tolerance, or -- when it fails -- the tolerance once each row's
+    possible E4M3 flips of h are allowed for (e4m3_flip_bound over
+    layer_args = (H, I, E, x_bits, idx, w[, layer, seed])); cosine >= 0.99999."""
+    rel, cos = errors(y, ref)
+    if rel <= REL_MAX_ERR and cos >= MIN_COS:
+        return
+    bound, n = e4m3_flip_bound(*layer_args)
+    y = np.asarray(y, np.float64)
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    excess = float((np.abs(y - ref) - bound).max()) / rms
+    assert excess <= REL_MAX_ERR and cos >= MIN_COS, \
+        f"{what}: max|err|/rms={rel:.3e}, beyond the bound of {n} possible h flips {excess:.3e}, cos={cos:.8f}"
+
+
+def check_f8_h_and_down(handle, H, I, E, x_bits, idx, w, y, tokens=None, layer=0, seed=0, what=""):
+    """For a call on the kind::mxf8f6f4 expert-major path: (1) the GPU's fp32
+    h of each slot of the given tokens against the oracle's fp64 h (max |diff|
+    <= 1e-5 max|h| per slot); (2) y against the oracle's down projection and
+    combine of the GPU's own E4M3-quantized h (the oracle's quantizer on the
+    GPU's h; max|err| <= 1e-5 rms, so every difference from the plain oracle
+    is an E4M3 rounding decision of h).  Returns (flips, elements): the
+    elements of h whose E4M3 code or block scale differs between the GPU's h
+    and the oracle's."""
+    import torch
+
+    T, k = idx.shape
+    tokens = range(T) if tokens is None else list(tokens)
+    n = T * k
+    hd, pd = moe.moe_ffn_test_copy_h(handle, n, I)
+    torch.cuda.synchronize()
+    hg, perm = hd.cpu().numpy().astype(np.float64), pd.cpu().numpy()
+    pos_of = {int(perm[P]): P for P in range(n) if perm[P] >= 0}
+    e4 = np.array([oracle.e4m3_value(c) for c in range(256)])
+    codes, scales = host_experts(H, I, idx.reshape(-1), layer=layer, seed=seed, E=E)
+    gc, gs = I * H // 2, I * H // 32
+
+    def deq(c, sc, n_):
+        return e4[c] * np.ldexp(1.0, np.repeat(sc.astype(np.int64), 128)[:n_] - 127)
+
+    flips = total = 0
+    for t in tokens:
+        xf = (x_bits[t].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        xq = deq(*oracle.act_quant_e4m3(xf, 128), H)
+        y2 = np.zeros(H)
+        for j in range(k):
+            e = int(idx[t, j])
+            P = pos_of[t * k + j]
+            c, sc = codes[e], scales[e]
+            g = oracle.matvec(c[:gc], sc[:gs], I, H, xq)
+            u = oracle.matvec(c[gc:2 * gc], sc[gs:2 * gs], I, H, xq)
+            h = g / (1.0 + np.exp(-g)) * u
+            d = float(np.abs(hg[P] - h).max())
+            assert d <= 1e-5 * float(np.abs(h).max()), f"{what}: h of token {t} slot {j}: max|diff| {d:.3e}"
+            cg, sg = oracle.act_quant_e4m3(hg[P], 128)
+            co, so = oracle.act_quant_e4m3(h, 128)
+            flips += int(((cg != co) | (np.repeat(sg, 128)[:I] != np.repeat(so, 128)[:I])).sum())
+            total += I
+            y2 += float(w[t, j]) * oracle.matvec(c[2 * gc:], sc[2 * gs:], H, I, deq(cg, sg, I))
+        rel, _ = errors(np.asarray(y[t:t + 1], np.float64), y2[None, :])
+        assert rel <= 1e-5, f"{what}: token {t}: y vs down(GPU h): max|err|/rms={rel:.3e}"
+    return flips, total
 
 
 def assert_close_e2m1(y, ref, bound, what=""):

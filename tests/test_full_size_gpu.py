@@ -11,7 +11,7 @@ import torch
 import fp4_block_scaled_gb300 as moe
 import oracle
 import synth
-from moe_setup import assert_close, errors, fill_layer, host_experts
+from moe_setup import assert_close, check_f8_h_and_down, errors, fill_layer, host_experts
 
 pytestmark = pytest.mark.gpu
 
@@ -28,11 +28,14 @@ def _cuda():
     torch.cuda.empty_cache()
 
 
-def test_layer_batch512_zipf_e4m3_sampled_tokens():
-    """384 experts, 512 tokens with Zipf(1.1) expert popularity, E4M3 activations."""
+@pytest.mark.parametrize("mma", [moe.MOE_MMA_MXF8F6F4, moe.MOE_MMA_MXF4_PIECES])
+def test_layer_batch512_zipf_e4m3_sampled_tokens(mma):
+    """384 experts, 512 tokens with Zipf(1.1) expert popularity, E4M3 activations,
+    on both tensor-core operations of the expert-major path."""
     E, T = 384, 512
     cfg = moe.config(E, H, I, K, T, act_mode=moe.MOE_ACT_E4M3_UE8M0_128, out_dtype=moe.MOE_OUT_F32)
     h = moe.moe_ffn_create(cfg, 0)
+    moe.moe_ffn_set_mma_kind(h, mma)
     try:
         es = fill_layer(h, cfg)
         x = synth.activations_bf16(T, H, seed=5)
@@ -49,11 +52,16 @@ def test_layer_batch512_zipf_e4m3_sampled_tokens():
         # popular expert (whose slots are spread over the most units)
         hot = int(np.bincount(idx.reshape(-1), minlength=E).argmax())
         t_hot = int(np.nonzero((idx == hot).any(axis=1))[0][-1])
-        for t in sorted({0, 1, T // 2, T - 1, t_hot}):
+        sample = sorted({0, 1, T // 2, T - 1, t_hot})
+        for t in sample:
             codes, scales = host_experts(H, I, idx[t], E=E)
             ref = oracle.moe_ffn(codes, scales, H, I, x[t:t + 1], idx[t:t + 1], w[t:t + 1],
                                  act_mode=oracle.ACT_E4M3_UE8M0_128, nthreads=THREADS)
             assert_close(y1[t:t + 1], ref, f"T=512 zipf e4m3 token {t}")
+        if mma == moe.MOE_MMA_MXF8F6F4:
+            # h of the sampled tokens' slots, and the down step on the GPU's own quantized h
+            flips, total = check_f8_h_and_down(h, H, I, E, x, idx, w, y1, tokens=sample, what="T=512 zipf")
+            print(f"E4M3 rounding decisions of h that differ from the oracle's: {flips} of {total}")
         # the whole batch again: bit-identical
         moe.moe_ffn_forward(h, xd, it, wt, es.table, y, T)
         torch.cuda.synchronize()
@@ -170,3 +178,38 @@ def test_stack_40_layers_batch32_sampled_token():
         del sets
         moe.moe_ffn_destroy(h)
         torch.cuda.empty_cache()
+
+
+def test_compute_bound_shape_8_experts_2048_tokens_sampled():
+    """The tensor-bound shape of the benchmark: 8 experts, each chosen by all
+    2048 tokens (top-8 of 8), E4M3 activations on kind::mxf8f6f4 with groups of
+    240 slots; sampled tokens against the oracle, h and the down step on the
+    GPU's own quantized h, and a bit-identical repeat."""
+    E, T, k = 8, 2048, 8
+    cfg = moe.config(E, H, I, k, T, act_mode=moe.MOE_ACT_E4M3_UE8M0_128, out_dtype=moe.MOE_OUT_F32)
+    h = moe.moe_ffn_create(cfg, 0)
+    try:
+        es = fill_layer(h, cfg)
+        x = synth.activations_bf16(T, H, seed=12)
+        idx = synth.routing_uniform(T, E, k, seed=12)
+        w = synth.routing_weights(T, k, seed=12)
+        xd = torch.from_numpy(x.view(np.int16)).cuda()
+        it, wt = torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda()
+        y = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        moe.moe_ffn_forward(h, xd, it, wt, es.table, y, T)
+        torch.cuda.synchronize()
+        y1 = y.cpu().numpy()
+        assert moe.moe_ffn_status(h) == moe.MOE_OK
+        sample = [0, 239, 240, 1000, T - 1]          # group edges of the first expert's slots
+        codes, scales = host_experts(H, I, np.arange(E), E=E)
+        for t in sample:
+            ref = oracle.moe_ffn(codes, scales, H, I, x[t:t + 1], idx[t:t + 1], w[t:t + 1],
+                                 act_mode=oracle.ACT_E4M3_UE8M0_128, nthreads=THREADS)
+            assert_close(y1[t:t + 1], ref, f"E=8 T=2048 token {t}")
+        flips, total = check_f8_h_and_down(h, H, I, E, x, idx, w, y1, tokens=sample, what="E=8 T=2048")
+        print(f"E4M3 rounding decisions of h that differ from the oracle's: {flips} of {total}")
+        moe.moe_ffn_forward(h, xd, it, wt, es.table, y, T)
+        torch.cuda.synchronize()
+        assert np.array_equal(y.cpu().numpy(), y1)
+    finally:
+        moe.moe_ffn_destroy(h)
