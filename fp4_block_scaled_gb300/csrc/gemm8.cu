@@ -62,6 +62,21 @@
 #include "internal.h"
 
 namespace moe {
+
+#ifdef MOE_F8_TRACE
+// debug builds only: per CTA, the issuer's cycles spent waiting for each
+// dependency and issuing ([0] expanded weights, [1] activation rows, [2] scale
+// slot, [3] accumulator, [4] issuing, [5] units)
+__device__ unsigned long long g_f8_trace[6][1024];
+#define F8_ACC(k, t0) (g_f8_trace[k][blockIdx.x] += (unsigned long long)(clock64() - (t0)))
+#define F8_NOW() clock64()
+#else
+#define F8_NOW() 0ll
+#define F8_ACC(k, t0) \
+    do {              \
+    } while (0)
+#endif
+
 namespace {
 
 constexpr int kF8Cap = 150 * 1024;                    // the unit ring: packed weights + activation rows
@@ -506,10 +521,12 @@ __device__ void f8_issue(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int nj
         // the epilogue has read this accumulator's previous job (every issuer
         // waits, also one without units in this job, so that none can arrive
         // for a later job before this one's phase is complete)
+        long long tw = F8_NOW();
         if (!mbar_wait_or_abort(&sm.acc_empty[buf], ((jl >> 1) & 1) ^ 1, &sm.abort, kF8WaitNs)) {
             abort = true;
             break;
         }
+        F8_ACC(3, tw);
         bool first = true;
         for (int u = 0; u < p.kgt; u++, c++) {
             const F8Unit U = f8_unit(p, jb, u);
@@ -517,11 +534,18 @@ __device__ void f8_issue(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int nj
             if ((int)(c % NI) != ii) continue;
             const uint32_t sp = c % kF8Pad;
             const uint32_t reuse = (uint32_t)(NI * Tm::kSlots);      // the scale slot's previous unit
-            bool ok = mbar_wait_or_abort(&sm.pad_ready[sp], (c / kF8Pad) & 1, &sm.abort, kF8WaitNs) &&
-                      mbar_wait_or_abort(&sm.full_b[c % kF8D], (c / kF8D) & 1, &sm.abort, kF8WaitNs);
+            tw = F8_NOW();
+            bool ok = mbar_wait_or_abort(&sm.pad_ready[sp], (c / kF8Pad) & 1, &sm.abort, kF8WaitNs);
+            F8_ACC(0, tw);
+            tw = F8_NOW();
+            ok = ok && mbar_wait_or_abort(&sm.full_b[c % kF8D], (c / kF8D) & 1, &sm.abort, kF8WaitNs);
+            F8_ACC(1, tw);
+            tw = F8_NOW();
             if (ok && c >= reuse)
                 ok = mbar_wait_or_abort(&sm.unit_free[(c - reuse) % kF8D], ((c - reuse) / kF8D) & 1, &sm.abort,
                                         kF8WaitNs);
+            F8_ACC(2, tw);
+            tw = F8_NOW();
             if (!ok) {
                 abort = true;
                 break;
@@ -545,6 +569,10 @@ __device__ void f8_issue(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int nj
                 first = false;
             }
             tc_commit(&sm.unit_free[c % kF8D]);
+            F8_ACC(4, tw);
+#ifdef MOE_F8_TRACE
+            g_f8_trace[5][blockIdx.x]++;
+#endif
         }
         if (abort) break;
         tc_commit(&sm.acc_full[buf]);
@@ -792,3 +820,14 @@ cudaError_t launch_f8_layer(const GroupArgs& a0, cudaStream_t s, bool pdl, Profi
 }
 
 }  // namespace moe
+
+#ifdef MOE_F8_TRACE
+// debug builds only: the issuer's wait and issue cycles per CTA (cleared after the read)
+extern "C" int moe_debug_f8_trace(unsigned long long* dst, size_t bytes)
+{
+    const size_t n = bytes < sizeof(moe::g_f8_trace) ? bytes : sizeof(moe::g_f8_trace);
+    if (cudaMemcpyFromSymbol(dst, moe::g_f8_trace, n) != cudaSuccess) return 1;
+    static unsigned long long zero[6][1024];
+    return cudaMemcpyToSymbol(moe::g_f8_trace, zero, sizeof(zero)) == cudaSuccess ? 0 : 1;
+}
+#endif
