@@ -408,13 +408,15 @@ def run_ours(args, wl):
     gmin = {"auto": 0, "slot": T + 1, "group": 1}[args.path]
     cfg = moe.config(E, H, I, k, T, act_mode=act, out_dtype=moe.MOE_OUT_F32, gemm_min_tokens=gmin)
     grouped = T >= (gmin or moe.DEFAULT_GEMM_MIN_TOKENS)
-    # the E4M3 expert-major path's MMA: as asked, or the library's choice (auto)
-    f8 = grouped and wl["act"] == "e4m3" and (args.mma == "f8" or (args.mma == "auto" and T * k >= 128 * E))
+    # the quantized modes' expert-major form (E4M3: kind::mxf8f6f4, E2M1:
+    # kind::mxf4, activations as they are): as asked, or the library's choice (auto)
+    f8 = (grouped and wl["act"] in ("e4m3", "e2m1")
+          and (args.mma == "f8" or (args.mma == "auto" and T * k >= 128 * E)))
     # route, prep, layer, combine | route, prep, gate/up, h quantizer, down, combine | prep, layer
     launches_per_layer = (6 if f8 else 4) if grouped else 2
     kernel = ("k_f8gemm" if f8 else "k_glayer") if grouped else "k_layer"
     h = moe.moe_ffn_create(cfg, local)
-    if grouped and wl["act"] == "e4m3":
+    if grouped and wl["act"] in ("e4m3", "e2m1"):
         moe.moe_ffn_set_mma_kind(h, {"auto": moe.MOE_MMA_AUTO, "pieces": moe.MOE_MMA_MXF4_PIECES,
                                      "f8": moe.MOE_MMA_MXF8F6F4}[args.mma])
     nc, ns = synth.expert_sizes(H, I)
@@ -883,8 +885,8 @@ def main():
     ap.add_argument("--act", choices=["bf16", "e4m3", "e2m1"], default=None,
                     help="activation numerics (default: the workload's)")
     ap.add_argument("--mma", choices=["auto", "pieces", "f8"], default="auto",
-                    help="E4M3 expert-major path: the library's choice (auto), kind::mxf8f6f4 (f8) or "
-                         "kind::mxf4 with E2M1 pieces")
+                    help="quantized modes' expert-major form: the library's choice (auto), the activations "
+                         "as they are (f8: kind::mxf8f6f4 for E4M3, kind::mxf4 for E2M1) or E2M1 pieces")
     args = ap.parse_args()
     wl = dict(WORKLOADS[args.workload])
     if args.act:

@@ -177,8 +177,10 @@ cudaError_t launch_layer(const moe_ffn* h, const uint16_t* x_bf16, float* x_resi
         // E4M3: kind::mxf8f6f4 where asked for, and by default where experts hold
         // many slots on average (the tensor-bound shapes; on HBM-bound decode
         // batches the pieces path streams the weights faster)
-        if (a.act_e4m3 && (h->mma_kind == MOE_MMA_MXF8F6F4 ||
-                           (h->mma_kind == MOE_MMA_AUTO && (long long)T * a.topk >= 128LL * a.E)))
+        // (the E2M1 mode likewise: its activation rows as they are, kind::mxf4)
+        if ((a.act_e4m3 || a.act_e2m1) &&
+            (h->mma_kind == MOE_MMA_MXF8F6F4 ||
+             (h->mma_kind == MOE_MMA_AUTO && (long long)T * a.topk >= 128LL * a.E)))
             return launch_f8_layer(a, s, true, prof);
         return launch_group_layer(a, s, true, prof);
     }
@@ -268,8 +270,10 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     const bool grouped = T >= h->gemm_min_tokens;      // the expert-major path can be taken
     GroupWorkspaceSizes gw{};
     if (grouped) gw = group_workspace_sizes(T, k, cfg->num_experts, H, I, h->sms, e4m3);
+    const bool e2m1 = cfg->act_mode == MOE_ACT_E2M1_UE8M0_32;
     F8WorkspaceSizes fw{};
-    if (grouped && e4m3) fw = f8_workspace_sizes(T, k, cfg->num_experts, H, I);
+    if (grouped && (e4m3 || e2m1)) fw = f8_workspace_sizes(T, k, cfg->num_experts, H, I);
+    const size_t f4_hraw = grouped && e2m1 ? (size_t)T * k * I * sizeof(float) : 0;   // h of the direct form
     h->mma_kind = MOE_MMA_AUTO;
 
     // one allocation, carved into aligned pieces
@@ -290,6 +294,7 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
     size_t o_gobuf = take(gw.obuf), o_gpgu = take(gw.part_gu), o_gpdn = take(gw.part_dn);
     size_t o_ghraw = take(gw.hraw), o_ghpair = take(gw.hpair);
     size_t o_fxb = take(fw.xb8), o_fxbsf = take(fw.xb8sf), o_fhb = take(fw.hb8), o_fhbsf = take(fw.hb8sf);
+    size_t o_f4hraw = take(f4_hraw);
     size_t o_rlog = take((size_t)T * cfg->num_experts * 4), o_rtk = take((size_t)T * sizeof(int));
     const size_t rpart_bytes = T > 8 ? (size_t)router_max_splits(H) * T * cfg->num_experts * 4 : 0;
     size_t o_rpart = take(rpart_bytes);
@@ -359,12 +364,13 @@ int moe_ffn_create(moe_ffn_t* out, const moe_ffn_config* cfg, int device)
         ga.part_dn = (uint64_t*)(b + o_gpdn);
         ga.hraw = e4m3 ? (float*)(b + o_ghraw) : nullptr;
         ga.hpair = e4m3 ? (int*)(b + o_ghpair) : nullptr;
-        if (e4m3) {
+        if (e4m3 || e2m1) {
             ga.xb8 = (uint8_t*)(b + o_fxb);
             ga.xb8sf = (uint8_t*)(b + o_fxbsf);
             ga.hb8 = (uint8_t*)(b + o_fhb);
             ga.hb8sf = (uint8_t*)(b + o_fhbsf);
         }
+        if (e2m1) ga.hraw = (float*)(b + o_f4hraw);
     }
     h->rlogits = (float*)(b + o_rlog);
     h->rtickets = (int*)(b + o_rtk);

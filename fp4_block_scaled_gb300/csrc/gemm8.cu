@@ -135,6 +135,7 @@ struct F8Plan {
     int kgt;              // 128-K units (a last half unit included)
     int half;             // 1: the last unit is a half unit (K % 128 == 64)
     int K;                // reduction length
+    int bunit;            // bytes of one B row per 128-K unit: 128 (E4M3), 64 (E2M1)
     size_t tile_bytes;    // bytes of a tile in the blob
     size_t mat_off;       // the projection's offset in the blob
 };
@@ -166,7 +167,7 @@ __device__ __forceinline__ F8Job f8_job(const GroupArgs& a, const F8Plan& p, int
     const uint8_t* blob = a.experts[e];
     J.ok = blob != nullptr && (reinterpret_cast<uintptr_t>(blob) & 15) == 0;
     J.a = blob + p.mat_off + (size_t)J.tile * p.tile_bytes;
-    J.b = (PHASE == 0 ? a.xb8 : a.hb8) + f8_group_rows(p0, g) * (size_t)p.K;
+    J.b = (PHASE == 0 ? a.xb8 : a.hb8) + f8_group_rows(p0, g) * (size_t)p.K * p.bunit / 128;
     J.bsf = (PHASE == 0 ? a.xb8sf : a.hb8sf) + (size_t)g * p.kgt * (2 * kUnitSfBytes);
     return J;
 }
@@ -183,7 +184,7 @@ __device__ __forceinline__ F8Unit f8_unit(const F8Plan& p, const F8Job& jb, int 
     F8Unit U;
     U.half = p.half && u == p.kgt - 1;
     U.abytes = U.half ? kHalfUnitBytes : kUnitBytes;
-    U.bbytes = (uint32_t)jb.nb * (U.half ? 64u : 128u);
+    U.bbytes = (uint32_t)jb.nb * (uint32_t)(U.half ? p.bunit / 2 : p.bunit);
     U.sbytes = jb.nb > 128 ? 2 * kUnitSfBytes : kUnitSfBytes;
     U.size = (U.abytes + U.bbytes + U.sbytes + 127u) & ~127u;
     return U;
@@ -295,6 +296,39 @@ __device__ __forceinline__ void f8_store_row(uint8_t* unit, uint8_t* atoms, int 
             (uint32_t)s * 0x01010101u;
 }
 
+// E2M1 rows (the E2M1 activation mode; kind::mxf4): a lane's four elements
+// 4 lane .. 4 lane + 3 of a 128-element unit (lanes 8 b .. 8 b + 7 hold its
+// 32-block b) under the block's ue8m0 byte -- the least 2^e with max |v| <=
+// 6 * 2^e, the E2M1 activation rule -- rounded to nearest even, as two bytes
+// (element 2i in the low nibble of byte i); s: the block's scale byte.
+__device__ __forceinline__ uint32_t f4_codes4(const float (&v)[4], int& s)
+{
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    s = e2m1_scale_byte(amax);
+    const float down = exp2i(127 - s);
+    return f32x2_to_e2m1x2(v[0] * down, v[1] * down) | (f32x2_to_e2m1x2(v[2] * down, v[3] * down) << 8);
+}
+
+// Stores a lane's two code bytes of row i of a group's unit (nb rows; per
+// 64-K MMA m, the kind::mxf4 K-major layout: core matrices of 8 rows x 16 B)
+// and, from lane 0, the row's four block scale bytes into the unit's atoms.
+// Every lane of the warp takes part.
+__device__ __forceinline__ void f4_store_row(uint8_t* unit, uint8_t* atoms, int nb, int i, int lane, bool in,
+                                             uint32_t codes, int s)
+{
+    const int kb = lane >> 3;
+    if (in)
+        *reinterpret_cast<uint16_t*>(unit + (size_t)(kb >> 1) * nb * 32 + (i >> 3) * 256 + (kb & 1) * 128 +
+                                     (i & 7) * 16 + (lane & 7) * 2) = (uint16_t)codes;
+    const uint32_t s0 = (uint32_t)__shfl_sync(0xFFFFFFFFu, s, 0), s1 = (uint32_t)__shfl_sync(0xFFFFFFFFu, s, 8);
+    const uint32_t s2 = (uint32_t)__shfl_sync(0xFFFFFFFFu, s, 16), s3 = (uint32_t)__shfl_sync(0xFFFFFFFFu, s, 24);
+    if (lane == 0)
+        *reinterpret_cast<uint32_t*>(atoms + (i >> 7) * kUnitSfBytes + (i & 31) * 16 + ((i & 127) >> 5) * 4) =
+            s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+}
+
 // Where sorted slot P's rows go: its group, its row in the group, the
 // group's first slot and rows of the MMA (from the route kernel's output).
 struct F8Slot {
@@ -345,6 +379,18 @@ __global__ void __launch_bounds__(256) k_f8prep(GroupArgs a)
         v[q] = a.x_resid ? __bfloat162float(__float2bfloat16_rn(a.x_resid[i] / den))
                          : __uint_as_float((uint32_t)a.x_bf16[i] << 16);
     }
+    if (a.act_e2m1) {
+        int s;
+        const uint32_t codes = f4_codes4(v, s);
+        for (int kk = 0; kk < a.topk; kk++) {
+            if (!s_ok[kk]) continue;
+            const F8Slot sl = s_sl[kk];
+            uint8_t* unit = a.xb8 + f8_group_rows(sl.p0, sl.g) * (H / 2) + (size_t)b * sl.nb * 64;
+            uint8_t* atoms = a.xb8sf + ((size_t)sl.g * (H / 128) + b) * (2 * kUnitSfBytes);
+            f4_store_row(unit, atoms, sl.nb, sl.i, lane, true, codes, s);
+        }
+        return;
+    }
     const int s = f8_block_scale(v);
     const uint32_t codes = f8_codes4(v, s);
     for (int kk = 0; kk < a.topk; kk++) {
@@ -380,10 +426,17 @@ __global__ void __launch_bounds__(256) k_f8hquant(GroupArgs a)
         v[2] = h.z;
         v[3] = h.w;
     }
+    uint8_t* atoms = a.hb8sf + ((size_t)sl.g * kgt + u) * (2 * kUnitSfBytes);
+    if (a.act_e2m1) {
+        int s;
+        const uint32_t codes = f4_codes4(v, s);
+        uint8_t* unit = a.hb8 + f8_group_rows(sl.p0, sl.g) * (I / 2) + (size_t)u * sl.nb * 64;
+        f4_store_row(unit, atoms, sl.nb, sl.i, lane, in, codes, s);
+        return;
+    }
     const int s = f8_block_scale(v);
     const uint32_t codes = f8_codes4(v, s);
     uint8_t* unit = a.hb8 + f8_group_rows(sl.p0, sl.g) * I + (size_t)u * sl.nb * 128;
-    uint8_t* atoms = a.hb8sf + ((size_t)sl.g * kgt + u) * (2 * kUnitSfBytes);
     f8_store_row(unit, atoms, sl.nb, sl.i, lane, in, codes, s);
 }
 
@@ -445,7 +498,7 @@ __device__ void f8_produce_b(const GroupArgs& a, const F8Plan& p, F8Smem& sm, in
             if (jb.ok) {
                 uint8_t* dst = sm.ring + st % kF8Cap + U.abytes;
                 mbar_arrive_expect_tx(bar, U.bbytes + U.sbytes);
-                bulk_g2s(dst, jb.b + (size_t)u * jb.nb * 128, U.bbytes, bar);
+                bulk_g2s(dst, jb.b + (size_t)u * jb.nb * p.bunit, U.bbytes, bar);
                 bulk_g2s(dst + U.bbytes, jb.bsf + (size_t)u * (2 * kUnitSfBytes), U.sbytes, bar);
             } else {
                 mbar_arrive(bar);
@@ -508,7 +561,7 @@ __device__ void f8_expand(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int n
 // unit's span of the ring and its expanded-weight stage are freed by the
 // commit after them, the accumulator handed to the epilogue (count NI) after
 // the job's last unit.
-template <int PHASE, int NI>
+template <int PHASE, int NI, int KIND>
 __device__ void f8_issue(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int njobs, uint32_t tmem, int ii)
 {
     using Tm = F8Tm<NI>;
@@ -535,7 +588,9 @@ __device__ void f8_issue(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int nj
             const uint32_t sp = c % kF8Pad;
             const uint32_t reuse = (uint32_t)(NI * Tm::kSlots);      // the scale slot's previous unit
             tw = F8_NOW();
-            bool ok = mbar_wait_or_abort(&sm.pad_ready[sp], (c / kF8Pad) & 1, &sm.abort, kF8WaitNs);
+            // kind::mxf8f6f4: the expanded weights; kind::mxf4: the packed ones in the ring
+            bool ok = KIND == 0 ? mbar_wait_or_abort(&sm.pad_ready[sp], (c / kF8Pad) & 1, &sm.abort, kF8WaitNs)
+                                : mbar_wait_or_abort(&sm.full_a[c % kF8D], (c / kF8D) & 1, &sm.abort, kF8WaitNs);
             F8_ACC(0, tw);
             tw = F8_NOW();
             ok = ok && mbar_wait_or_abort(&sm.full_b[c % kF8D], (c / kF8D) & 1, &sm.abort, kF8WaitNs);
@@ -552,19 +607,37 @@ __device__ void f8_issue(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int nj
             }
             tc_fence_after();
             if (jb.ok) {
-                const uint8_t* pa = sm.pad[sp];
                 const uint8_t* pb = sm.ring + st % kF8Cap + U.abytes;
                 const uint32_t sf = tmem + Tm::sf(ii, c);
-                tc_cp_sf(sf, umma_desc(smem_u32(pa + kF8PadBytes), 16, 128));
-                tc_cp_sf(sf + 4, umma_desc(smem_u32(pb + U.bbytes), 16, 128));
-                if (jb.nb > 128) tc_cp_sf(sf + 8, umma_desc(smem_u32(pb + U.bbytes + kUnitSfBytes), 16, 128));
                 const uint32_t acc = tmem + Tm::acc(ii, buf);
-                const int steps = U.half ? 2 : 4;
-                for (int kb = 0; kb < steps; kb++) {
-                    const uint64_t ad = umma_desc(smem_u32(pa + kb * 4096), 128, 256);
-                    const uint64_t bd = umma_desc(smem_u32(pb + kb * jb.nb * 32), 128, 256);
-                    tc_mma_mxf8f6f4(acc, ad, bd, f8_idesc((uint32_t)jb.nb, (uint32_t)kb), sf, sf + 4,
-                                    (!first || kb) ? 1u : 0u);
+                if (KIND == 0) {
+                    // E2M1 weights (expanded) x E4M3 rows: K = 32 per MMA, scale byte kb
+                    const uint8_t* pa = sm.pad[sp];
+                    tc_cp_sf(sf, umma_desc(smem_u32(pa + kF8PadBytes), 16, 128));
+                    tc_cp_sf(sf + 4, umma_desc(smem_u32(pb + U.bbytes), 16, 128));
+                    if (jb.nb > 128) tc_cp_sf(sf + 8, umma_desc(smem_u32(pb + U.bbytes + kUnitSfBytes), 16, 128));
+                    const int steps = U.half ? 2 : 4;
+                    for (int kb = 0; kb < steps; kb++) {
+                        const uint64_t ad = umma_desc(smem_u32(pa + kb * 4096), 128, 256);
+                        const uint64_t bd = umma_desc(smem_u32(pb + kb * jb.nb * 32), 128, 256);
+                        tc_mma_mxf8f6f4(acc, ad, bd, f8_idesc((uint32_t)jb.nb, (uint32_t)kb), sf, sf + 4,
+                                        (!first || kb) ? 1u : 0u);
+                    }
+                } else {
+                    // E2M1 weights (packed, as the blob holds them) x E2M1 rows: K = 64
+                    // per MMA, scale bytes 2m, 2m + 1
+                    const uint8_t* pa = sm.ring + st % kF8Cap;
+                    tc_cp_sf(sf, umma_desc(smem_u32(pa + (U.half ? kMmaCodeBytes : kUnitCodeBytes)), 16, 128));
+                    tc_cp_sf(sf + 4, umma_desc(smem_u32(pb + U.bbytes), 16, 128));
+                    if (jb.nb > 128) tc_cp_sf(sf + 8, umma_desc(smem_u32(pb + U.bbytes + kUnitSfBytes), 16, 128));
+                    const uint32_t idesc = mxf4_idesc(kTileRows, (uint32_t)jb.nb);
+                    const int steps = U.half ? 1 : 2;
+                    for (int m = 0; m < steps; m++) {
+                        const uint64_t ad = umma_desc(smem_u32(pa + m * kMmaCodeBytes), 128, 256);
+                        const uint64_t bd = umma_desc(smem_u32(pb + m * jb.nb * 32), 128, 256);
+                        tc_mma_mxf4(acc, ad, bd, mxf4_idesc_sf(idesc, 2u * (uint32_t)m), sf, sf + 4,
+                                    (!first || m) ? 1u : 0u);
+                    }
                 }
                 first = false;
             }
@@ -659,7 +732,7 @@ __device__ void f8_epilogue(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int
     }
 }
 
-template <int PHASE, int NI>
+template <int PHASE, int NI, int KIND>
 __global__ void __launch_bounds__(kF8Threads, 1) k_f8gemm(GroupArgs a, F8Plan p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -699,12 +772,13 @@ __global__ void __launch_bounds__(kF8Threads, 1) k_f8gemm(GroupArgs a, F8Plan p)
         return;
     }
     if (warp >= kF8WarpExp0 && warp < kF8WarpEpi0) {
-        f8_expand<PHASE>(a, p, sm, njobs, threadIdx.x - kF8WarpExp0 * 32);
+        // kind::mxf4 multiplies the packed weights where they landed
+        if (KIND == 0) f8_expand<PHASE>(a, p, sm, njobs, threadIdx.x - kF8WarpExp0 * 32);
         return;
     }
     if (warp < kF8WarpExp0) {
         const int ii = warp - kF8WarpMma0;
-        if (ii < NI && lane == 0) f8_issue<PHASE, NI>(a, p, sm, njobs, tmem, ii);
+        if (ii < NI && lane == 0) f8_issue<PHASE, NI, KIND>(a, p, sm, njobs, tmem, ii);
         __syncwarp();
     } else {
         f8_epilogue<PHASE, NI>(a, p, sm, njobs, tmem, warp & 3, lane);
@@ -725,6 +799,7 @@ F8Plan f8plan(const GroupArgs& a, int phase)
     p.kgt = m.kgt();
     p.half = m.kg_half;
     p.K = m.k;
+    p.bunit = a.act_e2m1 ? 64 : 128;
     p.tile_bytes = m.tile_bytes();
     p.mat_off = phase ? L.dn_off : L.gu_off;
     return p;
@@ -764,8 +839,9 @@ F8WorkspaceSizes f8_workspace_sizes(int T, int topk, int E, int H, int I)
 cudaError_t f8_init_device()
 {
     cudaError_t e = cudaSuccess;
-    for (const void* fn : {(const void*)k_f8gemm<0, 1>, (const void*)k_f8gemm<1, 1>, (const void*)k_f8gemm<0, 3>,
-                           (const void*)k_f8gemm<1, 3>})
+    for (const void* fn : {(const void*)k_f8gemm<0, 1, 0>, (const void*)k_f8gemm<1, 1, 0>,
+                           (const void*)k_f8gemm<0, 3, 0>, (const void*)k_f8gemm<1, 3, 0>,
+                           (const void*)k_f8gemm<0, 1, 1>, (const void*)k_f8gemm<1, 1, 1>})
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)f8_smem());
     return e;
@@ -780,7 +856,8 @@ cudaError_t launch_f8_layer(const GroupArgs& a0, cudaStream_t s, bool pdl, Profi
     // many slots on average (the MMAs are large: tensor-bound shapes), else
     // groups of up to 64 and three issuers (HBM-bound decode batches, where one
     // thread could not issue the small MMAs as fast as the weights arrive)
-    const bool wide = (long long)a.T * a.topk >= 128LL * a.E;
+    // (the E2M1 mode, kind::mxf4, has the wide form only)
+    const bool wide = a.act_e2m1 || (long long)a.T * a.topk >= 128LL * a.E;
     a.f8_gs = wide ? kF8GroupSlots : kF8GroupSlotsNarrow;
     const bool chain = pdl && !prof;
     cudaError_t err;
@@ -798,8 +875,13 @@ cudaError_t launch_f8_layer(const GroupArgs& a0, cudaStream_t s, bool pdl, Profi
     F8Plan p0 = f8plan(a, 0), p1 = f8plan(a, 1);
     void* args_gu[] = {&a, &p0};
     if (prof) prof->begin(kPhaseGateUp, s);
-    err = f8launch(wide ? (const void*)k_f8gemm<0, 1> : (const void*)k_f8gemm<0, 3>, dim3((unsigned)a.sms),
-                   dim3(kF8Threads), f8_smem(), s, chain, args_gu);
+    const void* gu = a.act_e2m1 ? (const void*)k_f8gemm<0, 1, 1>
+                     : wide        ? (const void*)k_f8gemm<0, 1, 0>
+                                   : (const void*)k_f8gemm<0, 3, 0>;
+    const void* dn = a.act_e2m1 ? (const void*)k_f8gemm<1, 1, 1>
+                     : wide        ? (const void*)k_f8gemm<1, 1, 0>
+                                   : (const void*)k_f8gemm<1, 3, 0>;
+    err = f8launch(gu, dim3((unsigned)a.sms), dim3(kF8Threads), f8_smem(), s, chain, args_gu);
     if (prof) prof->end(s);
     if (err != cudaSuccess) return err;
     const long long hw = (long long)a.T * a.topk * ((a.I + 127) / 128);
@@ -809,8 +891,7 @@ cudaError_t launch_f8_layer(const GroupArgs& a0, cudaStream_t s, bool pdl, Profi
     if (err != cudaSuccess) return err;
     void* args_dn[] = {&a, &p1};
     if (prof) prof->begin(kPhaseGateUp, s);     // the layer's MMA kernels, both projections
-    err = f8launch(wide ? (const void*)k_f8gemm<1, 1> : (const void*)k_f8gemm<1, 3>, dim3((unsigned)a.sms),
-                   dim3(kF8Threads), f8_smem(), s, chain, args_dn);
+    err = f8launch(dn, dim3((unsigned)a.sms), dim3(kF8Threads), f8_smem(), s, chain, args_dn);
     if (prof) prof->end(s);
     if (err != cudaSuccess) return err;
     if (prof) prof->begin(kPhaseDown, s);

@@ -295,20 +295,25 @@ enum {
 int moe_ffn_profile_enable(moe_ffn_t h, int on);
 int moe_ffn_profile_read(moe_ffn_t h, double* ms, int* launches);
 
-/* The tensor-core operation of the expert-major path in the E4M3 mode
- * (MOE_ACT_E4M3_UE8M0_128).  MOE_MMA_MXF8F6F4: tcgen05.mma kind::mxf8f6f4,
- * the E2M1 weights times the E4M3 activations as they are, one slot per MMA
- * column, groups of up to 240 slots of an expert where T * topk >= 128 * E
- * (else up to 64), six launches (route, prep, gate/up, h quantizer, down,
- * combine).  MOE_MMA_MXF4_PIECES: kind::mxf4, each E4M3 value carried as 8
- * E2M1 pieces, groups of up to 8 slots.  MOE_MMA_AUTO (the default): the
- * first where T * topk >= 128 * E (tensor-bound shapes, where it is several
- * times faster), else the second (HBM-bound decode batches, where it streams
- * the weights faster).  Both compute the same function within the float
- * tolerance ([8GB] §三个从不抛错的 Bug, item 2, fixes the E4M3 +
- * ue8m0-per-128 activation format; the pages leave the MMA to the build).
- * The bf16 and E2M1 modes and the slot-major path are not affected.
- * Errors: INVALID_ARG. */
+/* The tensor-core operation of the expert-major path for quantized
+ * activations.
+ *   MOE_MMA_MXF8F6F4 ("direct"): the activations as they are, one slot per MMA
+ *     column -- E4M3 mode (MOE_ACT_E4M3_UE8M0_128): tcgen05.mma
+ *     kind::mxf8f6f4, the E2M1 weights times the E4M3 rows, groups of up to
+ *     240 slots of an expert where T * topk >= 128 * E, else up to 64; E2M1
+ *     mode (MOE_ACT_E2M1_UE8M0_32): kind::mxf4, the E2M1 weights as the blob
+ *     holds them times the E2M1 rows (FP4 on both sides), groups of up to
+ *     240.  Six launches (route, prep, gate/up, h quantizer, down, combine).
+ *   MOE_MMA_MXF4_PIECES: kind::mxf4 with the activations carried as E2M1
+ *     pieces (8 per E4M3 value, groups of up to 8 slots; 1 per E2M1 value,
+ *     groups of up to 16).
+ *   MOE_MMA_AUTO (the default): direct where T * topk >= 128 * E
+ *     (tensor-bound shapes, where it is several times faster), else pieces
+ *     (HBM-bound decode batches, where that streams the weights faster).
+ * All compute the same function within the float tolerance ([8GB] §三个从不抛错的
+ * Bug, item 2, fixes the E4M3 + ue8m0-per-128 activation format; the pages
+ * leave the MMA to the build).  The bf16 mode and the slot-major path are not
+ * affected.  Errors: INVALID_ARG. */
 enum { MOE_MMA_AUTO = 0, MOE_MMA_MXF4_PIECES = 1, MOE_MMA_MXF8F6F4 = 2 };
 int moe_ffn_set_mma_kind(moe_ffn_t h, int kind);
 

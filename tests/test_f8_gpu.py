@@ -12,11 +12,13 @@ import torch
 import fp4_block_scaled_gb300 as moe
 import oracle
 import synth
-from moe_setup import Layer, assert_close, assert_close_e4m3, check_f8_h_and_down, e4m3_flip_candidates, host_experts, inputs
+from moe_setup import (Layer, assert_close, assert_close_e2m1, assert_close_e4m3, check_f8_h_and_down,
+                       e2m1_flip_bound, e4m3_flip_candidates, host_experts, inputs)
 
 pytestmark = pytest.mark.gpu
 
 E4M3 = moe.MOE_ACT_E4M3_UE8M0_128
+E2M1 = moe.MOE_ACT_E2M1_UE8M0_32
 F8 = moe.MOE_MMA_MXF8F6F4
 
 
@@ -128,3 +130,41 @@ def test_f8_stack_fused_rmsnorm_matches_oracle():
     finally:
         del sets
         moe.moe_ffn_destroy(h)
+
+
+@pytest.mark.parametrize("E,H,I,k,T", [
+    (8, 256, 128, 2, 16),        # gate/up K = 256: two units; N = 16
+    (8, 256, 448, 2, 40),        # down K = 448: a 64-wide last unit (one K = 64 MMA)
+    (4, 256, 192, 2, 300),       # N up to 160: two scale atoms
+    (16, 1024, 448, 6, 64),
+])
+def test_mxf4_direct_e2m1_matches_oracle(E, H, I, k, T):
+    """The E2M1 activation mode on the same direct form, kind::mxf4: E2M1 weights
+    as the blob holds them times the E2M1 rows of x and h (one per slot),
+    against the oracle's E2M1 mode with its bound for h's E2M1 rounding flips."""
+    L = Layer(E, H, I, k, max_tokens=T, act=E2M1, path="group", mma=F8)
+    try:
+        x, idx, w = inputs(T, E, H, k, seed=90 + T)
+        y = L.run(x, idx, w).cpu().numpy()
+        assert moe.moe_ffn_status(L.h) == moe.MOE_OK
+        bound, n = e2m1_flip_bound(H, I, E, x, idx, w)
+        assert_close_e2m1(y, L.oracle(x, idx, w), bound, f"mxf4 direct E={E} H={H} I={I} T={T} ({n} flips allowed)")
+        assert np.array_equal(L.run(x, idx, w).cpu().numpy(), y)
+    finally:
+        L.close()
+
+
+def test_mxf4_direct_and_pieces_agree_e2m1():
+    """Both E2M1-mode forms (direct and one piece per value) against the oracle."""
+    E, H, I, k, T = 16, 1024, 448, 6, 24
+    Ld = Layer(E, H, I, k, max_tokens=T, act=E2M1, path="group", mma=F8)
+    Lp = Layer(E, H, I, k, max_tokens=T, act=E2M1, path="group", mma=moe.MOE_MMA_MXF4_PIECES)
+    try:
+        x, idx, w = inputs(T, E, H, k, seed=13)
+        bound, _ = e2m1_flip_bound(H, I, E, x, idx, w)
+        ref = Ld.oracle(x, idx, w)
+        assert_close_e2m1(Ld.run(x, idx, w).cpu().numpy(), ref, bound, "direct")
+        assert_close_e2m1(Lp.run(x, idx, w).cpu().numpy(), ref, bound, "pieces")
+    finally:
+        Ld.close()
+        Lp.close()

@@ -11,7 +11,8 @@ import torch
 import fp4_block_scaled_gb300 as moe
 import oracle
 import synth
-from moe_setup import assert_close, check_f8_h_and_down, errors, fill_layer, host_experts
+from moe_setup import (assert_close, assert_close_e2m1, check_f8_h_and_down, e2m1_flip_bound, errors, fill_layer,
+                       host_experts)
 
 pytestmark = pytest.mark.gpu
 
@@ -180,13 +181,17 @@ def test_stack_40_layers_batch32_sampled_token():
         torch.cuda.empty_cache()
 
 
-def test_compute_bound_shape_8_experts_2048_tokens_sampled():
+@pytest.mark.parametrize("act", [moe.MOE_ACT_E4M3_UE8M0_128, moe.MOE_ACT_E2M1_UE8M0_32])
+def test_compute_bound_shape_8_experts_2048_tokens_sampled(act):
     """The tensor-bound shape of the benchmark: 8 experts, each chosen by all
-    2048 tokens (top-8 of 8), E4M3 activations on kind::mxf8f6f4 with groups of
-    240 slots; sampled tokens against the oracle, h and the down step on the
-    GPU's own quantized h, and a bit-identical repeat."""
+    2048 tokens (top-8 of 8), groups of 240 slots on the direct form: E4M3
+    activations on kind::mxf8f6f4 (with h and the down step on the GPU's own
+    quantized h checked), E2M1 activations on kind::mxf4 (with the bound for
+    h's E2M1 rounding flips); sampled tokens against the oracle and a
+    bit-identical repeat."""
     E, T, k = 8, 2048, 8
-    cfg = moe.config(E, H, I, k, T, act_mode=moe.MOE_ACT_E4M3_UE8M0_128, out_dtype=moe.MOE_OUT_F32)
+    e4m3 = act == moe.MOE_ACT_E4M3_UE8M0_128
+    cfg = moe.config(E, H, I, k, T, act_mode=act, out_dtype=moe.MOE_OUT_F32)
     h = moe.moe_ffn_create(cfg, 0)
     try:
         es = fill_layer(h, cfg)
@@ -202,12 +207,18 @@ def test_compute_bound_shape_8_experts_2048_tokens_sampled():
         assert moe.moe_ffn_status(h) == moe.MOE_OK
         sample = [0, 239, 240, 1000, T - 1]          # group edges of the first expert's slots
         codes, scales = host_experts(H, I, np.arange(E), E=E)
+        mode = oracle.ACT_E4M3_UE8M0_128 if e4m3 else oracle.ACT_E2M1_UE8M0_32
         for t in sample:
-            ref = oracle.moe_ffn(codes, scales, H, I, x[t:t + 1], idx[t:t + 1], w[t:t + 1],
-                                 act_mode=oracle.ACT_E4M3_UE8M0_128, nthreads=THREADS)
-            assert_close(y1[t:t + 1], ref, f"E=8 T=2048 token {t}")
-        flips, total = check_f8_h_and_down(h, H, I, E, x, idx, w, y1, tokens=sample, what="E=8 T=2048")
-        print(f"E4M3 rounding decisions of h that differ from the oracle's: {flips} of {total}")
+            ref = oracle.moe_ffn(codes, scales, H, I, x[t:t + 1], idx[t:t + 1], w[t:t + 1], act_mode=mode,
+                                 nthreads=THREADS)
+            if e4m3:
+                assert_close(y1[t:t + 1], ref, f"E=8 T=2048 token {t}")
+            else:
+                bound, _ = e2m1_flip_bound(H, I, E, x[t:t + 1], idx[t:t + 1], w[t:t + 1])
+                assert_close_e2m1(y1[t:t + 1], ref, bound, f"E=8 T=2048 E2M1 token {t}")
+        if e4m3:
+            flips, total = check_f8_h_and_down(h, H, I, E, x, idx, w, y1, tokens=sample, what="E=8 T=2048")
+            print(f"E4M3 rounding decisions of h that differ from the oracle's: {flips} of {total}")
         moe.moe_ffn_forward(h, xd, it, wt, es.table, y, T)
         torch.cuda.synchronize()
         assert np.array_equal(y.cpu().numpy(), y1)
