@@ -206,14 +206,27 @@ def draw_routings(R, E, k, T, seed, dist="uniform", layer=0):
 
 
 def source_fingerprint(path):
-    """sha256 of a C/CUDA source without its comments and whitespace: the code
-    the counters were taken on (a comment edit does not invalidate them)."""
+    """sha256 of a C/CUDA source, and of the in-tree headers it includes
+    (recursively), without comments and whitespace: the code the counters
+    were taken on (a comment edit does not invalidate them)."""
     import re
 
-    text = open(path, encoding="utf-8").read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    text = re.sub(r"//[^\n]*", "", text)
-    return hashlib.sha256(re.sub(r"\s+", "", text).encode()).hexdigest()
+    seen, parts = set(), []
+
+    def add(p):
+        p = os.path.normpath(p)
+        if p in seen or not os.path.exists(p):
+            return
+        seen.add(p)
+        text = open(p, encoding="utf-8").read()
+        for inc in re.findall(r'^\s*#\s*include\s+"([^"]+)"', text, flags=re.M):
+            add(os.path.join(os.path.dirname(p), inc))
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        parts.append(re.sub(r"\s+", "", text))
+
+    add(path)
+    return hashlib.sha256("".join(parts).encode()).hexdigest()
 
 
 def traffic_record(kernel, workload, act, algorithmic_bytes):

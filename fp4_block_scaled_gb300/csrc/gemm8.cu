@@ -4,7 +4,7 @@
 // activation rows as operand B, one ue8m0 scale per 32 along K on both sides
 // (the activations' per-128 scale repeated in each of its four 32-blocks).
 // A slot is one MMA column, so a group holds up to kF8GroupSlots slots of one
-// expert and a weight tile leaves HBM once per group of up to 240 tokens.
+// expert and a weight tile leaves HBM once per group of up to 224 tokens.
 //
 // Launches, chained with programmatic dependent launch:
 //   k_route    (route.cu) the T*k slots sorted by expert, cut into groups of
@@ -28,7 +28,7 @@
 // per 32-K step kb, the no-swizzle K-major layout of the MMA:
 //   kb * nb * 32 + (row / 8) * 256 + half * 128 + (row % 8) * 16
 // (16 codes per 16-byte row, half 0/1 = codes 0-15 / 16-31 of the step).
-// Scale atoms per (group, unit): two of 512 bytes (rows 0-127, 128-239) in
+// Scale atoms per (group, unit): two of 512 bytes (rows 0-127, 128-255) in
 // the order tcgen05.cp moves them, byte (row % 32) * 16 + (row % 128 / 32) * 4
 // + kb.
 //
@@ -36,7 +36,7 @@
 // layout.h: codes + scale atom, one bulk copy) followed by the group's
 // activation rows of that unit and their scale atoms -- in which each unit
 // takes a contiguous span sized to its group (a few KB of rows for a group of
-// a few slots, 30 KB for 240), so that small groups keep many units in flight
+// a few slots, 28 KB for 224), so that small groups keep many units in flight
 // while HBM latency is covered; and four stages of expanded weights: four
 // warps rewrite each unit's codes into the form kind::mxf8f6f4 reads E2M1 in
 // (16 codes in 8 bytes, then 8 bytes of padding, per 16-byte row of a core
@@ -50,11 +50,14 @@
 //   warp 1  activation producer: the unit's rows and scale atoms beside them
 //           (both producers replay the same span order and wait for the
 //           spans they overwrite to be consumed);
-//   warp 2  MMA issuer: per unit, the two scale sets to TMEM (tcgen05.cp)
-//           and one MMA per 32-K step into one of two accumulators;
-//   warps 3-6  expanders: packed weights -> an expanded-weight stage;
-//   warps 7-10 epilogue: tcgen05.ld of the finished accumulator, SwiGLU or
-//           the per-slot store.
+//   warps 2-4  MMA issuers (two in the wide form, three in the narrow one),
+//           one thread each, taking alternate units of every job: per unit,
+//           the scale sets to TMEM (tcgen05.cp) and one MMA per 32-K step
+//           into the issuer's own accumulator;
+//   warps 5-8  expanders (kind::mxf8f6f4): packed weights -> an
+//           expanded-weight stage;
+//   warps 9-12 epilogue: tcgen05.ld of the issuers' accumulators, added in
+//           issuer order, then SwiGLU or the per-slot store.
 // Every wait is bounded (2 s): on expiry the kernel records the device-timeout
 // status, stops, waits (bounded) for its copies and MMAs in flight and frees
 // its TMEM.
@@ -64,11 +67,14 @@
 namespace moe {
 
 #ifdef MOE_F8_TRACE
-// debug builds only: per CTA, the issuer's cycles spent waiting for each
+// debug builds only: per CTA, the issuers' cycles spent waiting for each
 // dependency and issuing ([0] expanded weights, [1] activation rows, [2] scale
-// slot, [3] accumulator, [4] issuing, [5] units)
-__device__ unsigned long long g_f8_trace[6][1024];
-#define F8_ACC(k, t0) (g_f8_trace[k][blockIdx.x] += (unsigned long long)(clock64() - (t0)))
+// slot, [3] accumulator, [4] issuing, [5] units), and the first epilogue
+// warp's cycles waiting for a finished accumulator [6], reading it out [7],
+// and within that: TMEM loads [8], gate/up exchange, SwiGLU and stores [11],
+// the pair's closing barrier [12], down stores [13]
+__device__ unsigned long long g_f8_trace[14][1024];
+#define F8_ACC(k, t0) atomicAdd(&g_f8_trace[k][blockIdx.x], (unsigned long long)(clock64() - (t0)))
 #define F8_NOW() clock64()
 #else
 #define F8_NOW() 0ll
@@ -91,28 +97,36 @@ constexpr int kF8WarpProdA = 0, kF8WarpProdB = 1, kF8WarpMma0 = 2;
 constexpr int kF8WarpExp0 = kF8WarpMma0 + kF8MaxIssuers, kF8WarpEpi0 = kF8WarpExp0 + 4;
 constexpr int kF8Threads = (kF8WarpEpi0 + 4) * 32;
 
-static_assert(kF8GroupSlots % 16 == 0 && kF8GroupSlots <= 240 && kF8GroupSlotsNarrow <= 64, "MMA N and TMEM");
+static_assert(kF8GroupSlots % 16 == 0 && kF8GroupSlots <= 224 && kF8GroupSlotsNarrow <= 64, "MMA N and TMEM");
 static_assert(kF8Cap % 128 == 0 && kF8PadStage % 128 == 0, "alignment");
 static_assert(kUnitBytes + kF8GroupSlots * 128 + 2 * kUnitSfBytes <= kF8Cap, "a unit fits the ring");
 
-// Tensor memory of the two forms (NI = MMA-issuing threads):
-//   NI = 1 (groups of up to 240 slots): accumulator b at column 256 b; the
-//     scale columns of unit c right after accumulator c % 2 (A 4, B 8);
-//   NI = 3 (groups of up to 64): issuer i's accumulator b at 64 (2 i + b),
-//     columns 0-383; its scale slots s = 0..4 at 384 + 8 (5 i + s) (A 4, B 4).
-// Issuer i takes the units c with c % NI == i; a scale slot is reused once the
-// unit it held (NI * slots units earlier) has been multiplied.
+// Tensor memory of the two forms (NI = MMA-issuing threads; issuer i takes
+// the units c with c % NI == i of every job into an accumulator of its own,
+// and the epilogue adds the NI accumulators in issuer order):
+//   NI = 2 (groups of up to kF8GroupSlots = 224 slots): issuer i's single
+//     accumulator at column 256 i; its scale slots s = 0, 1 right after it, at
+//     256 i + 224 + 12 s (A 4, B 8);
+//   NI = 3 (groups of up to 64): issuer i's accumulators b = 0, 1 at
+//     64 (2 i + b), columns 0-383; its scale slots s = 0..4 at 384 + 8 (5 i + s)
+//     (A 4, B 4).
+// A scale slot is reused once the unit it held (NI * slots units earlier) has
+// been multiplied.  With one accumulator per issuer the next job's MMAs wait
+// for the epilogue to have read the last one's.
 template <int NI>
 struct F8Tm {
-    static constexpr int kSlots = NI == 1 ? 2 : 5;
-    __device__ static uint32_t acc(int i, uint32_t b) { return NI == 1 ? b * 256u : 64u * (2u * (uint32_t)i + b); }
+    static_assert(NI == 2 || NI == 3, "the two forms");
+    static constexpr int kSlots = NI == 2 ? 2 : 5;
+    static constexpr uint32_t kBufs = NI == 2 ? 1 : 2;
+    __device__ static uint32_t acc(int i, uint32_t b) { return NI == 2 ? 256u * (uint32_t)i : 64u * (2u * (uint32_t)i + b); }
     __device__ static uint32_t sf(int i, uint32_t c)
     {
-        return NI == 1 ? (c & 1u) * 256u + (uint32_t)kF8GroupSlots
-                       : 384u + 8u * (uint32_t)(kSlots * i + (int)((c / NI) % kSlots));
+        const uint32_t s = (c / NI) % kSlots;
+        return NI == 2 ? 256u * (uint32_t)i + (uint32_t)kF8GroupSlots + 12u * s
+                       : 384u + 8u * (uint32_t)(kSlots * i) + 8u * s;
     }
 };
-static_assert(384 + 8 * 5 * kF8MaxIssuers <= kF8TmemCols && kF8GroupSlots + 12 <= 256, "TMEM budget");
+static_assert(384 + 8 * 5 * kF8MaxIssuers <= kF8TmemCols && kF8GroupSlots + 2 * 12 <= 256, "TMEM budget");
 
 // A unit's place in the ring: its packed weights (codes + scale atom, one
 // bulk copy from the blob) at the start, then the group's activation rows of
@@ -570,12 +584,12 @@ __device__ void f8_issue(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int nj
     bool abort = false;
     for (int j = blockIdx.x; j < njobs && !abort; j += gridDim.x, jl++) {
         const F8Job jb = f8_job<PHASE>(a, p, j);
-        const uint32_t buf = jl & 1;
+        const uint32_t buf = jl % Tm::kBufs;
         // the epilogue has read this accumulator's previous job (every issuer
         // waits, also one without units in this job, so that none can arrive
         // for a later job before this one's phase is complete)
         long long tw = F8_NOW();
-        if (!mbar_wait_or_abort(&sm.acc_empty[buf], ((jl >> 1) & 1) ^ 1, &sm.abort, kF8WaitNs)) {
+        if (!mbar_wait_or_abort(&sm.acc_empty[buf], ((jl / Tm::kBufs) & 1) ^ 1, &sm.abort, kF8WaitNs)) {
             abort = true;
             break;
         }
@@ -644,7 +658,7 @@ __device__ void f8_issue(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int nj
             tc_commit(&sm.unit_free[c % kF8D]);
             F8_ACC(4, tw);
 #ifdef MOE_F8_TRACE
-            g_f8_trace[5][blockIdx.x]++;
+            atomicAdd(&g_f8_trace[5][blockIdx.x], 1ull);
 #endif
         }
         if (abort) break;
@@ -671,64 +685,98 @@ __device__ void f8_epilogue(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int
     uint32_t jl = 0;
     for (int j = blockIdx.x; j < njobs; j += gridDim.x, jl++) {
         const F8Job jb = f8_job<PHASE>(a, p, j);
-        const uint32_t buf = jl & 1;
-        if (!mbar_wait_or_abort(&sm.acc_full[buf], (jl >> 1) & 1, &sm.abort, kF8WaitNs)) {
+        const uint32_t buf = jl % Tm::kBufs;
+        long long tw = F8_NOW();
+        if (!mbar_wait_or_abort(&sm.acc_full[buf], (jl / Tm::kBufs) & 1, &sm.abort, kF8WaitNs)) {
             f8_set_abort(a, sm);
             return;
         }
+        if (q == 0 && lane == 0) F8_ACC(6, tw);
+        tw = F8_NOW();
         tc_fence_after();
         // issuer i holds part of this job if one of its units c = jl kgt + u has c % NI == i
         const uint32_t c0 = jl * (uint32_t)p.kgt;
+        const uint32_t lq = (uint32_t)(32 * q) << 16;
+        auto holds = [&](int ii) {
+            return !((uint32_t)p.kgt < (uint32_t)NI && (uint32_t)((ii - (int)(c0 % NI) + NI) % NI) >= (uint32_t)p.kgt);
+        };
         for (int n0 = 0; n0 < jb.nt; n0 += 32) {
             const int ncol = min(32, jb.nt - n0);
             float v[32];
+            long long tc = F8_NOW();
 #pragma unroll
             for (int i = 0; i < 32; i++) v[i] = 0.0f;
             if (jb.ok) {
+                // the first two issuers' columns loaded together (16 at a time),
+                // then added in issuer order
+                const bool h0 = holds(0), h1 = holds(1);
 #pragma unroll
-                for (int ii = 0; ii < NI; ii++) {
-                    if ((uint32_t)p.kgt < (uint32_t)NI && (uint32_t)((ii - (int)(c0 % NI) + NI) % NI) >= (uint32_t)p.kgt)
-                        continue;
+                for (int hh = 0; hh < 32; hh += 16) {
+                    uint32_t r0[16], r1[16];
+                    if (h0) tc_ld16_nowait(tmem + lq + Tm::acc(0, buf) + (uint32_t)(n0 + hh), r0);
+                    if (h1) tc_ld16_nowait(tmem + lq + Tm::acc(1, buf) + (uint32_t)(n0 + hh), r1);
+                    tc_wait_ld();
+                    tc_ld_fence_regs<16>(r0);
+                    tc_ld_fence_regs<16>(r1);
+#pragma unroll
+                    for (int i = 0; i < 16; i++) {
+                        if (h0) v[hh + i] += __uint_as_float(r0[i]);
+                        if (h1) v[hh + i] += __uint_as_float(r1[i]);
+                    }
+                }
+#pragma unroll
+                for (int ii = 2; ii < NI; ii++) {
+                    if (!holds(ii)) continue;
                     uint32_t r[32];
-                    tc_ld32_nowait(tmem + ((uint32_t)(32 * q) << 16) + Tm::acc(ii, buf) + (uint32_t)n0, r);
+                    tc_ld32_nowait(tmem + lq + Tm::acc(ii, buf) + (uint32_t)n0, r);
                     tc_wait_ld();
                     tc_ld_fence_regs<32>(r);
 #pragma unroll
                     for (int i = 0; i < 32; i++) v[i] += __uint_as_float(r[i]);
                 }
             }
+            if (q == 0 && lane == 0) F8_ACC(8, tc);
+            tc = F8_NOW();
             if (PHASE == 0) {
                 // gate warp q and up warp q + 2 hold the same 32 outputs: the gate
                 // warp hands over its slots 16-31, the up warp its slots 0-15, and
-                // each makes h for 16 slots
-                const int pair = q & 1;
-                float* hrow = a.hraw + (size_t)(jb.p0 + n0) * a.I + (size_t)jb.tile * 64 + 32 * pair + lane;
+                // each makes h for 16 slots (all 16 products first, so that their
+                // exponentials and quotients overlap, then the stores)
+                const int pair = q & 1, base = q >= 2 ? 16 : 0;
+                float* hrow = a.hraw + (size_t)(jb.p0 + n0 + base) * a.I + (size_t)jb.tile * 64 + 32 * pair + lane;
+                float hv[16];
                 if (q >= 2) {
 #pragma unroll
                     for (int i = 0; i < 16; i++) sm.xch[pair][i][lane] = v[i];
                     named_sync(2 + pair, 64);
 #pragma unroll
-                    for (int i = 16; i < 32; i++)
-                        if (i < ncol) hrow[(size_t)i * a.I] = silu(sm.xch[pair][i][lane]) * v[i];
+                    for (int i = 0; i < 16; i++) hv[i] = silu(sm.xch[pair][16 + i][lane]) * v[16 + i];
                 } else {
 #pragma unroll
                     for (int i = 16; i < 32; i++) sm.xch[pair][i][lane] = v[i];
                     named_sync(2 + pair, 64);
 #pragma unroll
-                    for (int i = 0; i < 16; i++)
-                        if (i < ncol) hrow[(size_t)i * a.I] = silu(v[i]) * sm.xch[pair][i][lane];
+                    for (int i = 0; i < 16; i++) hv[i] = silu(v[i]) * sm.xch[pair][i][lane];
                 }
+#pragma unroll
+                for (int i = 0; i < 16; i++)
+                    if (base + i < ncol) hrow[(size_t)i * a.I] = hv[i];
+                if (q == 0 && lane == 0) F8_ACC(11, tc);
+                tc = F8_NOW();
                 named_sync(2 + pair, 64);
+                if (q == 0 && lane == 0) F8_ACC(12, tc);
             } else {
                 float* orow = a.obuf + (size_t)(jb.p0 + n0) * a.H + (size_t)jb.tile * kTileRows + 32 * q + lane;
 #pragma unroll
                 for (int i = 0; i < 32; i++)
                     if (i < ncol) orow[(size_t)i * a.H] = v[i];
+                if (q == 0 && lane == 0) F8_ACC(13, tc);
             }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);
+        if (q == 0 && lane == 0) F8_ACC(7, tw);
     }
 }
 
@@ -839,9 +887,9 @@ F8WorkspaceSizes f8_workspace_sizes(int T, int topk, int E, int H, int I)
 cudaError_t f8_init_device()
 {
     cudaError_t e = cudaSuccess;
-    for (const void* fn : {(const void*)k_f8gemm<0, 1, 0>, (const void*)k_f8gemm<1, 1, 0>,
+    for (const void* fn : {(const void*)k_f8gemm<0, 2, 0>, (const void*)k_f8gemm<1, 2, 0>,
                            (const void*)k_f8gemm<0, 3, 0>, (const void*)k_f8gemm<1, 3, 0>,
-                           (const void*)k_f8gemm<0, 1, 1>, (const void*)k_f8gemm<1, 1, 1>})
+                           (const void*)k_f8gemm<0, 2, 1>, (const void*)k_f8gemm<1, 2, 1>})
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)f8_smem());
     return e;
@@ -852,10 +900,12 @@ cudaError_t launch_f8_layer(const GroupArgs& a0, cudaStream_t s, bool pdl, Profi
     GroupArgs a = a0;
     if (a.T == 0) return cudaSuccess;
     a.o_unweighted = 1;                       // the combine applies the routing weights
-    // the form: groups of up to 240 slots and one issuer where experts hold
-    // many slots on average (the MMAs are large: tensor-bound shapes), else
-    // groups of up to 64 and three issuers (HBM-bound decode batches, where one
-    // thread could not issue the small MMAs as fast as the weights arrive)
+    // the form: groups of up to 224 slots and two issuers where experts hold
+    // many slots on average (the MMAs are large: tensor-bound shapes; one
+    // thread issues a block-scaled MMA every ~125 cycles whatever its N, and
+    // two keep the tensor pipe busy at N = 224), else groups of up to 64 and
+    // three issuers (HBM-bound decode batches, where one thread could not issue
+    // the small MMAs as fast as the weights arrive)
     // (the E2M1 mode, kind::mxf4, has the wide form only)
     const bool wide = a.act_e2m1 || (long long)a.T * a.topk >= 128LL * a.E;
     a.f8_gs = wide ? kF8GroupSlots : kF8GroupSlotsNarrow;
@@ -875,11 +925,11 @@ cudaError_t launch_f8_layer(const GroupArgs& a0, cudaStream_t s, bool pdl, Profi
     F8Plan p0 = f8plan(a, 0), p1 = f8plan(a, 1);
     void* args_gu[] = {&a, &p0};
     if (prof) prof->begin(kPhaseGateUp, s);
-    const void* gu = a.act_e2m1 ? (const void*)k_f8gemm<0, 1, 1>
-                     : wide        ? (const void*)k_f8gemm<0, 1, 0>
+    const void* gu = a.act_e2m1 ? (const void*)k_f8gemm<0, 2, 1>
+                     : wide        ? (const void*)k_f8gemm<0, 2, 0>
                                    : (const void*)k_f8gemm<0, 3, 0>;
-    const void* dn = a.act_e2m1 ? (const void*)k_f8gemm<1, 1, 1>
-                     : wide        ? (const void*)k_f8gemm<1, 1, 0>
+    const void* dn = a.act_e2m1 ? (const void*)k_f8gemm<1, 2, 1>
+                     : wide        ? (const void*)k_f8gemm<1, 2, 0>
                                    : (const void*)k_f8gemm<1, 3, 0>;
     err = f8launch(gu, dim3((unsigned)a.sms), dim3(kF8Threads), f8_smem(), s, chain, args_gu);
     if (prof) prof->end(s);
@@ -908,7 +958,7 @@ extern "C" int moe_debug_f8_trace(unsigned long long* dst, size_t bytes)
 {
     const size_t n = bytes < sizeof(moe::g_f8_trace) ? bytes : sizeof(moe::g_f8_trace);
     if (cudaMemcpyFromSymbol(dst, moe::g_f8_trace, n) != cudaSuccess) return 1;
-    static unsigned long long zero[6][1024];
+    static unsigned long long zero[14][1024];
     return cudaMemcpyToSymbol(moe::g_f8_trace, zero, sizeof(zero)) == cudaSuccess ? 0 : 1;
 }
 #endif

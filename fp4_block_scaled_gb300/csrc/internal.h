@@ -210,7 +210,7 @@ cudaError_t launch_group_combine(const GroupArgs& a, cudaStream_t s, bool pdl);
 // The expert-major path with E4M3 activations multiplied directly
 // (tcgen05.mma kind::mxf8f6f4, gemm8.cu): groups of up to kF8GroupSlots slots
 // of one expert, one MMA column per slot.
-constexpr int kF8GroupSlots = 240;         // groups of the form for tensor-bound shapes
+constexpr int kF8GroupSlots = 224;         // groups of the form for tensor-bound shapes
 constexpr int kF8GroupSlotsNarrow = 64;    // ... and for HBM-bound decode batches
 struct F8WorkspaceSizes {
     size_t xb8, xb8sf, hb8, hb8sf;      // bytes

@@ -1,7 +1,7 @@
 """GPU parity of the expert-major path's kind::mxf8f6f4 form (E4M3
 activations times E2M1 weights on the tensor core, one slot per MMA column,
-groups of up to 240 slots) against the CPU oracle's E4M3 mode, through the C
-ABI.  Shapes span the MMA's N range (16 to 240 columns, one and two scale
+groups of up to 224 slots) against the CPU oracle's E4M3 mode, through the C
+ABI.  Shapes span the MMA's N range (16 to 224 columns, one and two scale
 atoms), experts cut into several groups, a down projection with a 64-wide
 last K unit, and the stack's fused RMSNorm.  Float outputs: max|err| <=
 2e-3 * rms(ref), cosine >= 0.99999."""
@@ -57,7 +57,7 @@ def test_f8_layer_matches_oracle(E, H, I, k, T):
 
 def test_f8_experts_over_several_groups():
     """Two experts, both chosen by every one of 600 tokens: 600 slots each,
-    cut into groups of 240, 240 and 120 (N = 240, 240, 128)."""
+    cut into groups of 224, 224 and 152 (N = 224, 224, 160)."""
     E, H, I, k, T = 2, 256, 128, 2, 600
     L = Layer(E, H, I, k, max_tokens=T, act=E4M3, path="group", mma=F8)
     try:
