@@ -50,14 +50,19 @@
 //   warp 1  activation producer: the unit's rows and scale atoms beside them
 //           (both producers replay the same span order and wait for the
 //           spans they overwrite to be consumed);
-//   warps 2-4  MMA issuers (two in the wide form, three in the narrow one),
-//           one thread each, taking alternate units of every job: per unit,
-//           the scale sets to TMEM (tcgen05.cp) and one MMA per 32-K step
-//           into the issuer's own accumulator;
+//   warps 2-4  wide form: warp 2 the MMA issuer (one thread; per unit one
+//           MMA per 32-K step over all the group's rows, into the job's
+//           double-buffered accumulator) and warp 4 the scale stager (one
+//           thread; per unit the scale atoms to TMEM by tcgen05.cp, committed
+//           to the issuer's barrier), since one thread issues a tcgen05
+//           instruction only every ~120 cycles; narrow form: three issuers,
+//           one thread each, taking alternate units of every job, each with
+//           its own scale copies and accumulators;
 //   warps 5-8  expanders (kind::mxf8f6f4): packed weights -> an
 //           expanded-weight stage;
-//   warps 9-12 epilogue: tcgen05.ld of the issuers' accumulators, added in
-//           issuer order, then SwiGLU or the per-slot store.
+//   warps 9-12 epilogue: tcgen05.ld of the job's accumulator (the narrow
+//           form: the issuers' accumulators, added in issuer order), then
+//           SwiGLU or the per-slot store.
 // Every wait is bounded (2 s): on expiry the kernel records the device-timeout
 // status, stops, waits (bounded) for its copies and MMAs in flight and frees
 // its TMEM.
@@ -72,8 +77,11 @@ namespace moe {
 // slot, [3] accumulator, [4] issuing, [5] units), and the first epilogue
 // warp's cycles waiting for a finished accumulator [6], reading it out [7],
 // and within that: TMEM loads [8], gate/up exchange, SwiGLU and stores [11],
-// the pair's closing barrier [12], down stores [13]
-__device__ unsigned long long g_f8_trace[14][1024];
+// the pair's closing barrier [12], down stores [13]; the wide form's scale
+// stager waiting for the expanded weights [14] and the activation rows [15],
+// and issuing [16]; the first expander thread waiting for the packed weights
+// [17] and for the stage to be free [18], and expanding [19]
+__device__ unsigned long long g_f8_trace[20][1024];
 #define F8_ACC(k, t0) atomicAdd(&g_f8_trace[k][blockIdx.x], (unsigned long long)(clock64() - (t0)))
 #define F8_NOW() clock64()
 #else
@@ -101,32 +109,34 @@ static_assert(kF8GroupSlots % 16 == 0 && kF8GroupSlots <= 224 && kF8GroupSlotsNa
 static_assert(kF8Cap % 128 == 0 && kF8PadStage % 128 == 0, "alignment");
 static_assert(kUnitBytes + kF8GroupSlots * 128 + 2 * kUnitSfBytes <= kF8Cap, "a unit fits the ring");
 
-// Tensor memory of the two forms (NI = MMA-issuing threads; issuer i takes
-// the units c with c % NI == i of every job into an accumulator of its own,
-// and the epilogue adds the NI accumulators in issuer order):
-//   NI = 2 (groups of up to kF8GroupSlots = 224 slots): issuer i's single
-//     accumulator at column 256 i; its scale slots s = 0, 1 right after it, at
-//     256 i + 224 + 12 s (A 4, B 8);
-//   NI = 3 (groups of up to 64): issuer i's accumulators b = 0, 1 at
-//     64 (2 i + b), columns 0-383; its scale slots s = 0..4 at 384 + 8 (5 i + s)
-//     (A 4, B 4).
-// A scale slot is reused once the unit it held (NI * slots units earlier) has
-// been multiplied.  With one accumulator per issuer the next job's MMAs wait
-// for the epilogue to have read the last one's.
+// Tensor memory of the two forms (NI = MMA-issuing threads):
+//   NI = 1 (groups of up to kF8GroupSlots = 224 slots): the accumulator of a
+//     job at column 256 b (b = 0, 1: double-buffered); the scale slot of unit
+//     c, s = c % 4 (the unit's expanded-weight stage), at
+//     256 (s % 2) + 224 + 12 (s / 2) (A 4, B 8), filled by the scale stager;
+//   NI = 3 (groups of up to 64): issuer i takes the units c with c % 3 == i
+//     of every job into accumulators of its own, b = 0, 1 at 64 (2 i + b),
+//     columns 0-383, added by the epilogue in issuer order; its scale slots
+//     s = 0..4 at 384 + 8 (5 i + s) (A 4, B 4), which it fills itself.
+// A scale slot is reused once the unit it held has been multiplied.
 template <int NI>
 struct F8Tm {
-    static_assert(NI == 2 || NI == 3, "the two forms");
-    static constexpr int kSlots = NI == 2 ? 2 : 5;
-    static constexpr uint32_t kBufs = NI == 2 ? 1 : 2;
-    __device__ static uint32_t acc(int i, uint32_t b) { return NI == 2 ? 256u * (uint32_t)i : 64u * (2u * (uint32_t)i + b); }
+    static_assert(NI == 1 || NI == 3, "the two forms");
+    static constexpr bool kWide = NI == 1;
+    static constexpr int kSlots = kWide ? 4 : 5;
+    static constexpr int kAccs = kWide ? 1 : NI;         // accumulators the epilogue adds
+    __device__ static uint32_t acc(int i, uint32_t b) { return kWide ? 256u * b : 64u * (2u * (uint32_t)i + b); }
     __device__ static uint32_t sf(int i, uint32_t c)
     {
-        const uint32_t s = (c / NI) % kSlots;
-        return NI == 2 ? 256u * (uint32_t)i + (uint32_t)kF8GroupSlots + 12u * s
-                       : 384u + 8u * (uint32_t)(kSlots * i) + 8u * s;
+        if (kWide) {
+            const uint32_t s = c % kSlots;
+            return 256u * (s & 1u) + (uint32_t)kF8GroupSlots + 12u * (s >> 1);
+        }
+        return 384u + 8u * (uint32_t)(kSlots * i) + 8u * ((c / NI) % kSlots);
     }
 };
 static_assert(384 + 8 * 5 * kF8MaxIssuers <= kF8TmemCols && kF8GroupSlots + 2 * 12 <= 256, "TMEM budget");
+static_assert(kF8Pad == 4, "the wide form's scale slots follow the expanded-weight stages");
 
 // A unit's place in the ring: its packed weights (codes + scale atom, one
 // bulk copy from the blob) at the start, then the group's activation rows of
@@ -137,7 +147,7 @@ struct F8Smem {
     uint8_t pad[kF8Pad][kF8PadStage];   // expanded weights, then the unit's A atom
     float xch[2][32][32];               // epilogue: up values of 32 rows x 32 slots, per warp pair
     uint64_t full_a[kF8D], full_b[kF8D], unit_free[kF8D];
-    uint64_t pad_ready[kF8Pad];
+    uint64_t pad_ready[kF8Pad], sf_ready[kF8Pad];
     uint64_t acc_full[2], acc_empty[2], drain[kF8MaxIssuers];
     uint32_t tmem;
     int abort;
@@ -541,9 +551,15 @@ __device__ void f8_expand(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int n
             const uint32_t sp = c % kF8Pad;
             // the stage's previous unit (c - kF8Pad) must have been multiplied
             const uint32_t prev = c - kF8Pad;
-            if (!mbar_wait_or_abort(&sm.full_a[c % kF8D], (c / kF8D) & 1, &sm.abort, kF8WaitNs) ||
-                (c >= (uint32_t)kF8Pad &&
-                 !mbar_wait_or_abort(&sm.unit_free[prev % kF8D], (prev / kF8D) & 1, &sm.abort, kF8WaitNs))) {
+            long long tw = F8_NOW();
+            bool ok = mbar_wait_or_abort(&sm.full_a[c % kF8D], (c / kF8D) & 1, &sm.abort, kF8WaitNs);
+            if (et == 0) F8_ACC(17, tw);
+            tw = F8_NOW();
+            ok = ok && (c < (uint32_t)kF8Pad ||
+                        mbar_wait_or_abort(&sm.unit_free[prev % kF8D], (prev / kF8D) & 1, &sm.abort, kF8WaitNs));
+            if (et == 0) F8_ACC(18, tw);
+            tw = F8_NOW();
+            if (!ok) {
                 f8_set_abort(a, sm);
                 return;
             }
@@ -566,30 +582,169 @@ __device__ void f8_expand(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int n
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.pad_ready[sp]);
+            if (et == 0) F8_ACC(19, tw);
         }
     }
 }
 
-// MMA issuer i (one thread of NI): per unit c with c % NI == i, the scale
-// sets of A and B to TMEM, then one MMA per 32-K step into its accumulator; a
-// unit's span of the ring and its expanded-weight stage are freed by the
-// commit after them, the accumulator handed to the epilogue (count NI) after
-// the job's last unit.
-template <int PHASE, int NI, int KIND>
-__device__ void f8_issue(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int njobs, uint32_t tmem, int ii)
+// Scale stager of the wide form (one thread): per unit, once its weights are
+// expanded (kind::mxf8f6f4) or have landed (kind::mxf4; the scale slot's
+// previous unit multiplied) and its activation rows are in, the unit's A
+// scale atom and the group's B atoms to the unit's scale slot (tcgen05.cp),
+// committed to sf_ready: the issuers then wait once per unit and only issue
+// MMAs (one thread issues a tcgen05 instruction every ~110 cycles).
+template <int PHASE, int KIND>
+__device__ void f8_stage_sf(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int njobs, uint32_t tmem)
 {
+    using Tm = F8Tm<1>;
+    F8Ring ring;
+    uint32_t c = 0;
+    bool ok = true;
+    for (int j = blockIdx.x; ok && j < njobs; j += gridDim.x) {
+        const F8Job jb = f8_job<PHASE>(a, p, j);
+        for (int u = 0; u < p.kgt; u++, c++) {
+            const F8Unit U = f8_unit(p, jb, u);
+            const uint64_t st = ring.take(U.size);
+            const uint32_t sp = c % kF8Pad;
+            long long tw = F8_NOW();
+            if (KIND == 0) {
+                ok = mbar_wait_or_abort(&sm.pad_ready[sp], (c / kF8Pad) & 1, &sm.abort, kF8WaitNs);
+            } else {
+                ok = mbar_wait_or_abort(&sm.full_a[c % kF8D], (c / kF8D) & 1, &sm.abort, kF8WaitNs);
+                const uint32_t prev = c - kF8Pad;
+                if (ok && c >= (uint32_t)kF8Pad)
+                    ok = mbar_wait_or_abort(&sm.unit_free[prev % kF8D], (prev / kF8D) & 1, &sm.abort, kF8WaitNs);
+            }
+            F8_ACC(14, tw);
+            tw = F8_NOW();
+            ok = ok && mbar_wait_or_abort(&sm.full_b[c % kF8D], (c / kF8D) & 1, &sm.abort, kF8WaitNs);
+            F8_ACC(15, tw);
+            tw = F8_NOW();
+            if (!ok) break;
+            tc_fence_after();
+            if (jb.ok) {
+                const uint8_t* ring_u = sm.ring + st % kF8Cap;
+                const uint8_t* pb = ring_u + U.abytes;
+                const uint8_t* atom_a = KIND == 0 ? sm.pad[sp] + kF8PadBytes
+                                                  : ring_u + (U.half ? kMmaCodeBytes : kUnitCodeBytes);
+                const uint32_t sf = tmem + Tm::sf(0, c);
+                tc_cp_sf(sf, umma_desc(smem_u32(atom_a), 16, 128));
+                tc_cp_sf(sf + 4, umma_desc(smem_u32(pb + U.bbytes), 16, 128));
+                if (jb.nb > 128) tc_cp_sf(sf + 8, umma_desc(smem_u32(pb + U.bbytes + kUnitSfBytes), 16, 128));
+            }
+            tc_commit(&sm.sf_ready[sp]);
+            F8_ACC(16, tw);
+        }
+    }
+    if (!ok) f8_set_abort(a, sm);
+    tc_commit(&sm.drain[2]);
+    mbar_wait_bounded(&sm.drain[2], 0, kF8WaitNs);
+}
+
+// MMA issuer of the wide form (one thread): per unit, once its scale slot is
+// filled, one MMA per 32-K step (kind::mxf8f6f4; 64-K steps for kind::mxf4)
+// over all the group's rows of B into the job's accumulator; the unit's span
+// of the ring, its expanded-weight stage and its scale slot are freed by the
+// commit after them, the accumulator handed to the epilogue after the job's
+// last unit.
+template <int PHASE, int KIND>
+__device__ void f8_issue_wide(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int njobs, uint32_t tmem)
+{
+    using Tm = F8Tm<1>;
+    F8Ring ring;
+    uint32_t c = 0, jl = 0;
+    bool abort = false;
+    for (int j = blockIdx.x; j < njobs && !abort; j += gridDim.x, jl++) {
+        const F8Job jb = f8_job<PHASE>(a, p, j);
+        const uint32_t buf = jl & 1;
+        long long tw = F8_NOW();
+        if (!mbar_wait_or_abort(&sm.acc_empty[buf], ((jl >> 1) & 1) ^ 1, &sm.abort, kF8WaitNs)) {
+            abort = true;
+            break;
+        }
+        F8_ACC(3, tw);
+        const int n = jb.nb;
+        const uint32_t acc = tmem + Tm::acc(0, buf);
+        bool first = true;
+        for (int u = 0; u < p.kgt; u++, c++) {
+            const F8Unit U = f8_unit(p, jb, u);
+            const uint64_t st = ring.take(U.size);
+            const uint32_t sp = c % kF8Pad;
+            tw = F8_NOW();
+            if (!mbar_wait_or_abort(&sm.sf_ready[sp], (c / kF8Pad) & 1, &sm.abort, kF8WaitNs)) {
+                abort = true;
+                break;
+            }
+            F8_ACC(0, tw);
+            tw = F8_NOW();
+            tc_fence_after();
+            if (jb.ok) {
+                const uint8_t* pb = sm.ring + st % kF8Cap + U.abytes;
+                // B's scale atoms: rows 0-127 at sf + 4, rows 128- at sf + 8 (the MMA
+                // over all the rows reads both)
+                const uint32_t sf = tmem + Tm::sf(0, c), sfb = sf + 4;
+                if (KIND == 0) {
+                    // E2M1 weights (expanded) x E4M3 rows: K = 32 per MMA, scale byte kb
+                    const uint8_t* pa = sm.pad[sp];
+                    const int steps = U.half ? 2 : 4;
+                    for (int kb = 0; kb < steps; kb++) {
+                        const uint64_t ad = umma_desc(smem_u32(pa + kb * 4096), 128, 256);
+                        const uint64_t bd = umma_desc(smem_u32(pb + kb * jb.nb * 32), 128, 256);
+                        tc_mma_mxf8f6f4(acc, ad, bd, f8_idesc((uint32_t)n, (uint32_t)kb), sf, sfb,
+                                        (!first || kb) ? 1u : 0u);
+                    }
+                } else {
+                    // E2M1 weights (packed, as the blob holds them) x E2M1 rows: K = 64
+                    // per MMA, scale bytes 2m, 2m + 1
+                    const uint8_t* pa = sm.ring + st % kF8Cap;
+                    const uint32_t idesc = mxf4_idesc(kTileRows, (uint32_t)n);
+                    const int steps = U.half ? 1 : 2;
+                    for (int m = 0; m < steps; m++) {
+                        const uint64_t ad = umma_desc(smem_u32(pa + m * kMmaCodeBytes), 128, 256);
+                        const uint64_t bd = umma_desc(smem_u32(pb + m * jb.nb * 32), 128, 256);
+                        tc_mma_mxf4(acc, ad, bd, mxf4_idesc_sf(idesc, 2u * (uint32_t)m), sf, sfb,
+                                    (!first || m) ? 1u : 0u);
+                    }
+                }
+                first = false;
+            }
+            tc_commit(&sm.unit_free[c % kF8D]);
+            F8_ACC(4, tw);
+#ifdef MOE_F8_TRACE
+            atomicAdd(&g_f8_trace[5][blockIdx.x], 1ull);
+#endif
+        }
+        if (abort) break;
+        tc_commit(&sm.acc_full[buf]);
+    }
+    if (abort) f8_set_abort(a, sm);
+    // none of this thread's tensor-core operations may be in flight when the
+    // TMEM is freed or the CTA exits
+    tc_commit(&sm.drain[0]);
+    mbar_wait_bounded(&sm.drain[0], 0, kF8WaitNs);
+}
+
+// MMA issuer i of the narrow form (one thread of three): per unit c with
+// c % 3 == i, the scale sets of A and B to its own scale slot, then one MMA
+// per 32-K step into its accumulator; a unit's span of the ring and its
+// expanded-weight stage are freed by the commit after them, the accumulator
+// handed to the epilogue (count 3) after the job's last unit.
+template <int PHASE, int KIND>
+__device__ void f8_issue_narrow(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int njobs, uint32_t tmem, int ii)
+{
+    constexpr int NI = 3;
     using Tm = F8Tm<NI>;
     F8Ring ring;
     uint32_t c = 0, jl = 0;
     bool abort = false;
     for (int j = blockIdx.x; j < njobs && !abort; j += gridDim.x, jl++) {
         const F8Job jb = f8_job<PHASE>(a, p, j);
-        const uint32_t buf = jl % Tm::kBufs;
+        const uint32_t buf = jl & 1;
         // the epilogue has read this accumulator's previous job (every issuer
         // waits, also one without units in this job, so that none can arrive
         // for a later job before this one's phase is complete)
         long long tw = F8_NOW();
-        if (!mbar_wait_or_abort(&sm.acc_empty[buf], ((jl / Tm::kBufs) & 1) ^ 1, &sm.abort, kF8WaitNs)) {
+        if (!mbar_wait_or_abort(&sm.acc_empty[buf], ((jl >> 1) & 1) ^ 1, &sm.abort, kF8WaitNs)) {
             abort = true;
             break;
         }
@@ -625,11 +780,9 @@ __device__ void f8_issue(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int nj
                 const uint32_t sf = tmem + Tm::sf(ii, c);
                 const uint32_t acc = tmem + Tm::acc(ii, buf);
                 if (KIND == 0) {
-                    // E2M1 weights (expanded) x E4M3 rows: K = 32 per MMA, scale byte kb
                     const uint8_t* pa = sm.pad[sp];
                     tc_cp_sf(sf, umma_desc(smem_u32(pa + kF8PadBytes), 16, 128));
                     tc_cp_sf(sf + 4, umma_desc(smem_u32(pb + U.bbytes), 16, 128));
-                    if (jb.nb > 128) tc_cp_sf(sf + 8, umma_desc(smem_u32(pb + U.bbytes + kUnitSfBytes), 16, 128));
                     const int steps = U.half ? 2 : 4;
                     for (int kb = 0; kb < steps; kb++) {
                         const uint64_t ad = umma_desc(smem_u32(pa + kb * 4096), 128, 256);
@@ -638,12 +791,9 @@ __device__ void f8_issue(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int nj
                                         (!first || kb) ? 1u : 0u);
                     }
                 } else {
-                    // E2M1 weights (packed, as the blob holds them) x E2M1 rows: K = 64
-                    // per MMA, scale bytes 2m, 2m + 1
                     const uint8_t* pa = sm.ring + st % kF8Cap;
                     tc_cp_sf(sf, umma_desc(smem_u32(pa + (U.half ? kMmaCodeBytes : kUnitCodeBytes)), 16, 128));
                     tc_cp_sf(sf + 4, umma_desc(smem_u32(pb + U.bbytes), 16, 128));
-                    if (jb.nb > 128) tc_cp_sf(sf + 8, umma_desc(smem_u32(pb + U.bbytes + kUnitSfBytes), 16, 128));
                     const uint32_t idesc = mxf4_idesc(kTileRows, (uint32_t)jb.nb);
                     const int steps = U.half ? 1 : 2;
                     for (int m = 0; m < steps; m++) {
@@ -665,8 +815,6 @@ __device__ void f8_issue(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int nj
         tc_commit(&sm.acc_full[buf]);
     }
     if (abort) f8_set_abort(a, sm);
-    // none of this thread's tensor-core operations may be in flight when the
-    // TMEM is freed or the CTA exits
     tc_commit(&sm.drain[ii]);
     mbar_wait_bounded(&sm.drain[ii], 0, kF8WaitNs);
 }
@@ -685,9 +833,9 @@ __device__ void f8_epilogue(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int
     uint32_t jl = 0;
     for (int j = blockIdx.x; j < njobs; j += gridDim.x, jl++) {
         const F8Job jb = f8_job<PHASE>(a, p, j);
-        const uint32_t buf = jl % Tm::kBufs;
+        const uint32_t buf = jl & 1;
         long long tw = F8_NOW();
-        if (!mbar_wait_or_abort(&sm.acc_full[buf], (jl / Tm::kBufs) & 1, &sm.abort, kF8WaitNs)) {
+        if (!mbar_wait_or_abort(&sm.acc_full[buf], (jl >> 1) & 1, &sm.abort, kF8WaitNs)) {
             f8_set_abort(a, sm);
             return;
         }
@@ -706,26 +854,16 @@ __device__ void f8_epilogue(const GroupArgs& a, const F8Plan& p, F8Smem& sm, int
             long long tc = F8_NOW();
 #pragma unroll
             for (int i = 0; i < 32; i++) v[i] = 0.0f;
-            if (jb.ok) {
-                // the first two issuers' columns loaded together (16 at a time),
-                // then added in issuer order
-                const bool h0 = holds(0), h1 = holds(1);
+            if (jb.ok && Tm::kAccs == 1) {
+                uint32_t r[32];
+                tc_ld32_nowait(tmem + lq + Tm::acc(0, buf) + (uint32_t)n0, r);
+                tc_wait_ld();
+                tc_ld_fence_regs<32>(r);
 #pragma unroll
-                for (int hh = 0; hh < 32; hh += 16) {
-                    uint32_t r0[16], r1[16];
-                    if (h0) tc_ld16_nowait(tmem + lq + Tm::acc(0, buf) + (uint32_t)(n0 + hh), r0);
-                    if (h1) tc_ld16_nowait(tmem + lq + Tm::acc(1, buf) + (uint32_t)(n0 + hh), r1);
-                    tc_wait_ld();
-                    tc_ld_fence_regs<16>(r0);
-                    tc_ld_fence_regs<16>(r1);
+                for (int i = 0; i < 32; i++) v[i] += __uint_as_float(r[i]);
+            } else if (jb.ok) {
 #pragma unroll
-                    for (int i = 0; i < 16; i++) {
-                        if (h0) v[hh + i] += __uint_as_float(r0[i]);
-                        if (h1) v[hh + i] += __uint_as_float(r1[i]);
-                    }
-                }
-#pragma unroll
-                for (int ii = 2; ii < NI; ii++) {
+                for (int ii = 0; ii < NI; ii++) {
                     if (!holds(ii)) continue;
                     uint32_t r[32];
                     tc_ld32_nowait(tmem + lq + Tm::acc(ii, buf) + (uint32_t)n0, r);
@@ -792,7 +930,10 @@ __global__ void __launch_bounds__(kF8Threads, 1) k_f8gemm(GroupArgs a, F8Plan p)
             mbar_init(&sm.full_b[s], 1);
             mbar_init(&sm.unit_free[s], 1);
         }
-        for (int s = 0; s < kF8Pad; s++) mbar_init(&sm.pad_ready[s], 4);
+        for (int s = 0; s < kF8Pad; s++) {
+            mbar_init(&sm.pad_ready[s], 4);
+            mbar_init(&sm.sf_ready[s], 1);
+        }
         for (int b = 0; b < 2; b++) {
             mbar_init(&sm.acc_full[b], NI);
             mbar_init(&sm.acc_empty[b], 4);
@@ -826,7 +967,14 @@ __global__ void __launch_bounds__(kF8Threads, 1) k_f8gemm(GroupArgs a, F8Plan p)
     }
     if (warp < kF8WarpExp0) {
         const int ii = warp - kF8WarpMma0;
-        if (ii < NI && lane == 0) f8_issue<PHASE, NI, KIND>(a, p, sm, njobs, tmem, ii);
+        if (lane == 0) {
+            if (NI == 1) {
+                if (ii == 0) f8_issue_wide<PHASE, KIND>(a, p, sm, njobs, tmem);
+                else if (ii == 2) f8_stage_sf<PHASE, KIND>(a, p, sm, njobs, tmem);
+            } else {
+                f8_issue_narrow<PHASE, KIND>(a, p, sm, njobs, tmem, ii);
+            }
+        }
         __syncwarp();
     } else {
         f8_epilogue<PHASE, NI>(a, p, sm, njobs, tmem, warp & 3, lane);
@@ -887,9 +1035,9 @@ F8WorkspaceSizes f8_workspace_sizes(int T, int topk, int E, int H, int I)
 cudaError_t f8_init_device()
 {
     cudaError_t e = cudaSuccess;
-    for (const void* fn : {(const void*)k_f8gemm<0, 2, 0>, (const void*)k_f8gemm<1, 2, 0>,
+    for (const void* fn : {(const void*)k_f8gemm<0, 1, 0>, (const void*)k_f8gemm<1, 1, 0>,
                            (const void*)k_f8gemm<0, 3, 0>, (const void*)k_f8gemm<1, 3, 0>,
-                           (const void*)k_f8gemm<0, 2, 1>, (const void*)k_f8gemm<1, 2, 1>})
+                           (const void*)k_f8gemm<0, 1, 1>, (const void*)k_f8gemm<1, 1, 1>})
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)f8_smem());
     return e;
@@ -900,12 +1048,11 @@ cudaError_t launch_f8_layer(const GroupArgs& a0, cudaStream_t s, bool pdl, Profi
     GroupArgs a = a0;
     if (a.T == 0) return cudaSuccess;
     a.o_unweighted = 1;                       // the combine applies the routing weights
-    // the form: groups of up to 224 slots and two issuers where experts hold
-    // many slots on average (the MMAs are large: tensor-bound shapes; one
-    // thread issues a block-scaled MMA every ~125 cycles whatever its N, and
-    // two keep the tensor pipe busy at N = 224), else groups of up to 64 and
-    // three issuers (HBM-bound decode batches, where one thread could not issue
-    // the small MMAs as fast as the weights arrive)
+    // the form: groups of up to 224 slots, one issuer and a scale stager where
+    // experts hold many slots on average (the MMAs are large: tensor-bound
+    // shapes), else groups of up to 64 and three issuers (HBM-bound decode
+    // batches, where one thread could not issue the small MMAs as fast as the
+    // weights arrive)
     // (the E2M1 mode, kind::mxf4, has the wide form only)
     const bool wide = a.act_e2m1 || (long long)a.T * a.topk >= 128LL * a.E;
     a.f8_gs = wide ? kF8GroupSlots : kF8GroupSlotsNarrow;
@@ -925,11 +1072,11 @@ cudaError_t launch_f8_layer(const GroupArgs& a0, cudaStream_t s, bool pdl, Profi
     F8Plan p0 = f8plan(a, 0), p1 = f8plan(a, 1);
     void* args_gu[] = {&a, &p0};
     if (prof) prof->begin(kPhaseGateUp, s);
-    const void* gu = a.act_e2m1 ? (const void*)k_f8gemm<0, 2, 1>
-                     : wide        ? (const void*)k_f8gemm<0, 2, 0>
+    const void* gu = a.act_e2m1 ? (const void*)k_f8gemm<0, 1, 1>
+                     : wide        ? (const void*)k_f8gemm<0, 1, 0>
                                    : (const void*)k_f8gemm<0, 3, 0>;
-    const void* dn = a.act_e2m1 ? (const void*)k_f8gemm<1, 2, 1>
-                     : wide        ? (const void*)k_f8gemm<1, 2, 0>
+    const void* dn = a.act_e2m1 ? (const void*)k_f8gemm<1, 1, 1>
+                     : wide        ? (const void*)k_f8gemm<1, 1, 0>
                                    : (const void*)k_f8gemm<1, 3, 0>;
     err = f8launch(gu, dim3((unsigned)a.sms), dim3(kF8Threads), f8_smem(), s, chain, args_gu);
     if (prof) prof->end(s);
@@ -958,7 +1105,7 @@ extern "C" int moe_debug_f8_trace(unsigned long long* dst, size_t bytes)
 {
     const size_t n = bytes < sizeof(moe::g_f8_trace) ? bytes : sizeof(moe::g_f8_trace);
     if (cudaMemcpyFromSymbol(dst, moe::g_f8_trace, n) != cudaSuccess) return 1;
-    static unsigned long long zero[14][1024];
+    static unsigned long long zero[20][1024];
     return cudaMemcpyToSymbol(moe::g_f8_trace, zero, sizeof(zero)) == cudaSuccess ? 0 : 1;
 }
 #endif
