@@ -1192,3 +1192,15 @@ cudaError_t launch_gemv_layer(const GemvArgs& a0, cudaStream_t s, bool pdl, Prof
 }
 
 }  // namespace moe
+
+#ifdef MOE_TC_TRACE
+// debug builds only: the per-CTA milestones of the last layer launch (ns,
+// globaltimer), cleared after the read
+extern "C" int moe_debug_layer_trace(long long* dst, size_t bytes)
+{
+    const size_t n = bytes < sizeof(moe::g_tc_cta) ? bytes : sizeof(moe::g_tc_cta);
+    if (cudaMemcpyFromSymbol(dst, moe::g_tc_cta, n) != cudaSuccess) return 1;
+    static long long zero[12][1024];
+    return cudaMemcpyToSymbol(moe::g_tc_cta, zero, sizeof(zero)) == cudaSuccess ? 0 : 1;
+}
+#endif
