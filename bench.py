@@ -641,14 +641,60 @@ def run_ours(args, wl):
     moe.moe_ffn_profile_enable(h, False)
     r_us = ms_r[moe.MOE_PHASE_ROUTER] / max(1, n_r[moe.MOE_PHASE_ROUTER]) * 1e3
     r_bytes = E * H * 2 + T * H * 2 + 2 * T * E * 4 + T * k * 8     # W, x, logits out and back, routing
-    router = {"kernels": "k_router_logits (selection in its last CTA per token tile)" if T <= 8
+    # (c) inside a decode step: 40 layers of (router -> layer on the router's
+    # routing), each layer with router weights of its own, against the same 40
+    # layer calls on the pre-drawn routings, both one CUDA graph; the difference
+    # per layer is what the router adds to a step (its launch and weight loads
+    # overlap the previous layer's kernel as programmatic dependent launch allows)
+    r_in_step = None
+    if T <= 8:
+        nl = 40
+        Wl = torch.randn((nl, E, H), generator=gen, device="cuda").to(torch.bfloat16).view(torch.int16)
+        ri = torch.empty((nl, T, k), dtype=torch.int32, device="cuda")
+        rw = torch.empty((nl, T, k), dtype=torch.float32, device="cuda")
+        yl = torch.empty((T, H), dtype=torch.float32, device="cuda")
+
+        def step_graph(mode):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(nl):
+                    l_ = i % L
+                    if mode == "router":      # the router call, then the layer call on its routing
+                        moe.moe_router_topk(h, x_d[i % R], Wl[i], T, ri[i], rw[i], stream=stream)
+                        moe.moe_ffn_forward(h, x_d[i % R], ri[i], rw[i], sets[l_].table, yl, T, stream)
+                    else:
+                        moe.moe_ffn_forward(h, x_d[i % R], idx_d[i % R, l_], w_d[i % R, l_], sets[l_].table, yl,
+                                            T, stream)
+            return g
+
+        times = []
+        for mode in ("none", "router"):
+            g = step_graph(mode)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    g.replay()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(10):
+                    g.replay()
+                e1.record(stream)
+            stream.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3 / (10 * nl))
+            del g
+        r_in_step = times[1] - times[0]
+        del Wl
+    router = {"kernels": ("k_router_cluster (one thread-block cluster: logits, then the selection in its first CTA)"
+                          if T == 1 and E <= 256 else
+                          "k_router_logits (selection in its last CTA per token tile)") if T <= 8
               else "k_router_mma + k_router_select",
-              "us": r_us_graph, "us_alone": r_us, "algorithmic_bytes": r_bytes,
+              "us": r_us_graph, "us_alone": r_us, "us_in_step": r_in_step, "algorithmic_bytes": r_bytes,
               "gbs": r_bytes / (r_us_graph * 1e-6) / 1e9,
               "frac_of_hbm": r_bytes / (r_us_graph * 1e-6) / 1e9 / peak,
               "launches": 1 if T <= 8 else 2, "timing": f"us: per call, {nrg} calls back to back in a CUDA graph, each on its "
                                        "own router matrix (256 MB in all, > L2); us_alone: events around "
-                                       "each call, one matrix"}
+                                       "each call, one matrix; us_in_step: per layer, a graph of 40 "
+                                       "(moe_router_topk -> moe_ffn_forward on its routing) pairs less a graph "
+                                       "of the same 40 layers on pre-drawn routings"}
 
     # ---- end to end through the public API from host buffers: every step copies
     # its inputs in from pinned host memory and its result back

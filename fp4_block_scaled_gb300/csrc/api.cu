@@ -560,6 +560,9 @@ int moe_router_topk(moe_ffn_t h, const void* x, const void* router_w, int T, flo
     if (a.nsplit) {
         e = launch_router_mma(a, s, !h->prof);
         if (e == cudaSuccess) e = launch_router_select(a, s, !h->prof);
+    } else if (router_cluster_fits(T, h->cfg.num_experts, h->cfg.hidden)) {
+        // one token: one cluster computes the logits and selects
+        e = launch_router_cluster(a, s, !h->prof);
     } else {  // one launch: the logits kernel's last CTA per token tile selects
         a.tickets = h->rtickets;
         e = launch_router_logits(a, s, !h->prof);

@@ -253,6 +253,10 @@ cudaError_t router_init_device();
 cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_router_mma(const RouterArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_router_select(const RouterArgs& a, cudaStream_t s, bool pdl);
+// one token on one thread-block cluster (logits and selection in one launch,
+// no global round trip between them), where the device and the shape allow it
+bool router_cluster_fits(int T, int E, int H);
+cudaError_t launch_router_cluster(const RouterArgs& a, cudaStream_t s, bool pdl);
 
 // E4M3 / ue8m0-per-128 activation quantizer (actquant.cu).
 struct ActQuantArgs {

@@ -27,156 +27,13 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "rsel.cuh"
 
 namespace moe {
+using namespace rsel;
 namespace {
 
 constexpr int kRPerLane = 32;       // most logits per lane in k_router_select (E <= 1024)
-constexpr int kRChunks = 16;        // 16-byte weight chunks per lane per pass
-
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8])
-{
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-}
-
-// dst[i] = f(src[i]) for i < n by the CTA's threads, eight loads in flight per
-// thread before the stores (a load-store pair per iteration would wait a full
-// memory round trip each).
-template <class F>
-__device__ __forceinline__ void stage_x(const uint4* src, int n, F store)
-{
-    for (int i0 = threadIdx.x; i0 < n; i0 += 8 * blockDim.x) {
-        uint4 v[8];
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            const int i = i0 + q * blockDim.x;
-            v[q] = i < n ? src[i] : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            const int i = i0 + q * blockDim.x;
-            if (i < n) store(i, v[q]);
-        }
-    }
-}
-
-// Order key of a logit: larger keys rank first; -0 and +0 tie; NaN ranks after
-// every number (key 1); key 0 is "taken" or "no expert".
-__device__ __forceinline__ uint32_t order_key(float v)
-{
-    if (isnan(v)) return 1u;
-    const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// One warp selects token t's top-k.  Lane l holds the order keys of experts
-// l, l + 32, ... (R of them) in registers and its best untaken one; a round
-// takes the warp's best with two redux.sync (the largest key, then the lowest
-// id holding it), and only the winning lane picks its next best.  Lane i keeps
-// pick i for the softmax.  The logits are read through L2 (other CTAs of the
-// same grid may have written them).
-template <int R>
-__device__ __forceinline__ void select_token(const RouterArgs& a, int t, int lane)
-{
-    float v[R];
-    uint32_t key[R];
-    if (a.nsplit == 0) {
-        const float* row = a.logits + (size_t)t * a.E;
-#pragma unroll
-        for (int j = 0; j < R; j++) {
-            const int e = lane + 32 * j;
-            v[j] = e < a.E ? __ldcg(row + e) : 0.0f;
-        }
-    } else {
-        // the tensor-core path's split-K partials, added in split order; the
-        // sums are the logits
-#pragma unroll
-        for (int j = 0; j < R; j++) v[j] = 0.0f;
-        // four splits' loads in flight at once, added in split order
-        constexpr int kQ = R <= 16 ? 4 : 2;
-        for (int sp0 = 0; sp0 < a.nsplit; sp0 += kQ) {
-            float q[kQ][R];
-#pragma unroll
-            for (int u = 0; u < kQ; u++) {
-                const float* row = a.part + ((size_t)(sp0 + u) * a.T + t) * a.E;
-#pragma unroll
-                for (int j = 0; j < R; j++) {
-                    const int e = lane + 32 * j;
-                    q[u][j] = (sp0 + u < a.nsplit && e < a.E) ? __ldcg(row + e) : 0.0f;
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kQ; u++)
-#pragma unroll
-                for (int j = 0; j < R; j++)
-                    if (sp0 + u < a.nsplit) v[j] += q[u][j];
-        }
-        float* out = a.logits + (size_t)t * a.E;
-#pragma unroll
-        for (int j = 0; j < R; j++) {
-            const int e = lane + 32 * j;
-            if (e < a.E) out[e] = v[j];
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < R; j++) key[j] = lane + 32 * j < a.E ? order_key(v[j]) : 0u;
-    uint32_t bk = 0;                                   // this lane's best: key, slot, value
-    int bj = 0;
-    float bv = 0.0f;
-    auto lane_best = [&]() {
-        bk = 0;
-        bj = 0;
-#pragma unroll
-        for (int j = 0; j < R; j++)                    // strict >: the lower id on equal keys
-            if (key[j] > bk) {
-                bk = key[j];
-                bj = j;
-                bv = v[j];
-            }
-    };
-    lane_best();
-    float mine = 0.0f;
-    int mine_e = 0;
-    for (int i = 0; i < a.topk; i++) {
-        const uint32_t gk = __reduce_max_sync(0xFFFFFFFFu, bk);
-        const int ge = (int)__reduce_min_sync(0xFFFFFFFFu, bk == gk ? (uint32_t)(lane + 32 * bj) : 0xFFFFFFFFu);
-        const float gv = __shfl_sync(0xFFFFFFFFu, bv, ge & 31);
-        if (lane == i) {
-            mine = gv;
-            mine_e = ge;
-        }
-        if ((ge & 31) == lane) {
-#pragma unroll
-            for (int j = 0; j < R; j++)
-                if (j == (ge >> 5)) key[j] = 0u;
-            lane_best();
-        }
-    }
-    const float m = __shfl_sync(0xFFFFFFFFu, mine, 0);
-    const float p = lane < a.topk ? expf(mine - m) : 0.0f;
-    float sum = p;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-    if (lane < a.topk) {
-        a.idx[(size_t)t * a.topk + lane] = mine_e;
-        a.wout[(size_t)t * a.topk + lane] = p / sum;
-    }
-}
-
-__device__ __forceinline__ void select_token_any(const RouterArgs& a, int t, int lane)
-{
-    if (a.E <= 128) select_token<4>(a, t, lane);
-    else if (a.E <= 256) select_token<8>(a, t, lane);
-    else if (a.E <= 384) select_token<12>(a, t, lane);
-    else if (a.E <= 512) select_token<16>(a, t, lane);
-    else select_token<32>(a, t, lane);
-}
-
 // grid ceil(T / 8), 256 threads: one warp per token.
 template <int R>
 __global__ void __launch_bounds__(256) k_router_select(RouterArgs a)
@@ -314,6 +171,43 @@ __global__ void __launch_bounds__(NW * 32) k_router_logits(RouterArgs a)
     if (threadIdx.x == 0) a.tickets[blockIdx.y] = 0;
 }
 
+// ------------------------------------------------ one token, one cluster
+
+// grid = one cluster of C CTAs, NW warps each, for one token: warp w of CTA
+// r owns expert row e = NW r + w and computes its logit exactly as
+// k_router_logits does for a one-token tile (the lane's whole share of the row
+// loaded before the wait for the previous kernel, the same order of products
+// and the same butterfly sum); each logit goes to global memory and into the
+// first CTA's shared memory, and after one cluster barrier that CTA's first
+// warp selects -- no ticket, fence or global round trip between the logits and
+// the selection.
+template <int NW>
+__global__ void __launch_bounds__(NW * 32) k_router_cluster(RouterArgs a)
+{
+    extern __shared__ __align__(16) uint4 s_x[];      // [H / 8] x (bf16), then [E] logits (the first CTA's)
+    float* s_logit = reinterpret_cast<float*>(s_x + a.H / 8);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int e = (int)rank * NW + warp;
+    uint4 wv[kRChunks];
+    row_load(a, e, lane, wv);
+    pdl_wait();
+    stage_x(reinterpret_cast<const uint4*>(a.x), a.H / 8, [&](int i, const uint4 v) { s_x[i] = v; });
+    __syncthreads();
+    if (e < a.E) {
+        const float v = row_dot(a, e, lane, wv, s_x);
+        if (lane == 0) {
+            a.logits[e] = v;
+            st_cluster_f32(&s_logit[e], 0, v);
+        }
+    }
+    cluster_barrier();
+    if (rank == 0 && warp == 0) {
+        if (a.E <= 128) select_token<4>(a, 0, lane, s_logit);
+        else select_token<8>(a, 0, lane, s_logit);
+    }
+}
+
 // ------------------------------------------------ tensor-core batch path
 
 constexpr uint64_t kRWaitLimitNs = 2000000000ull;
@@ -441,6 +335,10 @@ cudaError_t rlaunch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStre
 
 constexpr size_t kRSmemMax = 200 * 1024;
 
+// CTAs per cluster of k_router_cluster on this device (0: not available),
+// set by router_init_device
+int g_cluster_ctas = 0;
+
 }  // namespace
 
 int router_max_experts() { return 32 * kRPerLane; }
@@ -500,6 +398,43 @@ cudaError_t router_init_device()
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
+    // the one-token cluster kernel: 16 CTAs where the device allows that size, else 8
+    g_cluster_ctas = 0;
+    const void* clu[] = {(const void*)k_router_cluster<4>, (const void*)k_router_cluster<8>,
+                         (const void*)k_router_cluster<16>};
+    bool allow16 = true;
+    for (const void* f : clu) {
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
+        if (cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+            (void)cudaGetLastError();
+            allow16 = false;
+        }
+    }
+    if (e == cudaSuccess) {
+        for (int cs : {16, 8}) {
+            if (cs == 16 && !allow16) continue;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(cs);
+            cfg.blockDim = dim3(16 * 32);
+            cfg.dynamicSmemBytes = 64 * 1024;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = cs;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, (const void*)k_router_cluster<16>, &cfg) == cudaSuccess && n > 0) {
+                g_cluster_ctas = cs;
+                break;
+            }
+            (void)cudaGetLastError();
+        }
+    }
     const void* mma[] = {(const void*)k_router_mma<16>, (const void*)k_router_mma<32>, (const void*)k_router_mma<64>,
                          (const void*)k_router_mma<128>, (const void*)k_router_mma<256>};
     for (const void* f : mma) {
@@ -548,6 +483,39 @@ cudaError_t launch_router_logits(const RouterArgs& a0, cudaStream_t s, bool pdl)
                      : tpc == 4 ? (const void*)k_router_logits<4, 4>
                                 : (const void*)k_router_logits<8, 8>;
     return rlaunch(fn, grid, dim3(nw * 32), smem, s, pdl, args);
+}
+
+bool router_cluster_fits(int T, int E, int H)
+{
+    return T == 1 && g_cluster_ctas > 0 && E >= 1 && E <= g_cluster_ctas * 16 && E <= 256 && H % 8 == 0 &&
+           (size_t)H * 2 + (size_t)E * 4 <= 64 * 1024;
+}
+
+cudaError_t launch_router_cluster(const RouterArgs& a0, cudaStream_t s, bool pdl)
+{
+    RouterArgs a = a0;
+    if (!router_cluster_fits(a.T, a.E, a.H)) return cudaErrorInvalidValue;
+    const int cs = g_cluster_ctas;
+    const int per = (a.E + cs - 1) / cs;                 // rows per CTA
+    const int nw = per <= 4 ? 4 : per <= 8 ? 8 : 16;
+    const void* fn = nw == 4 ? (const void*)k_router_cluster<4>
+                     : nw == 8 ? (const void*)k_router_cluster<8> : (const void*)k_router_cluster<16>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cs);
+    cfg.blockDim = dim3((unsigned)nw * 32);
+    cfg.dynamicSmemBytes = (size_t)a.H * 2 + (size_t)a.E * 4;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    void* args[] = {&a};
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 cudaError_t launch_router_select(const RouterArgs& a0, cudaStream_t s, bool pdl)

@@ -191,10 +191,15 @@ int moe_ffn_act_quant(moe_ffn_t h, const void* x, int rows, int n, uint8_t* code
  *   logits   optional device fp32 [T][E] output (NULL: kept in the workspace)
  *   topk_idx device int32 [T][k], topk_w device fp32 [T][k] -- the routing
  *            inputs of moe_ffn_forward.
- * Two launches (logits, selection), deterministic.  Up to 8 tokens the
- * logits stream the weights on the CUDA cores; above 8 (H a multiple of 128)
- * they are tcgen05 bf16 MMAs in split-K partial sums, added by the selection
- * in a fixed order.  UNSUPPORTED beyond 1024 experts or H above 102,400. */
+ * Deterministic.  One token with E <= 256: one launch of one thread-block
+ * cluster (a warp per expert row; the selection in the cluster's first CTA,
+ * from the logits gathered in its shared memory), where the device runs
+ * clusters of 8 or 16 CTAs.  Up to 8 tokens otherwise: one launch, the logits
+ * streaming the weights on the CUDA cores and the last CTA of each token tile
+ * selecting.  Above 8 tokens (H a multiple of 128): tcgen05 bf16 MMAs in
+ * split-K partial sums, then a selection launch that adds them in a fixed
+ * order.  Every path gives the same logits for a one-token call.
+ * UNSUPPORTED beyond 1024 experts or H above 102,400. */
 int moe_router_topk(moe_ffn_t h, const void* x, const void* router_w, int T, float* logits,
                     int32_t* topk_idx, float* topk_w, void* stream);
 

@@ -110,6 +110,36 @@ def test_router_then_layer_matches_oracle():
         L.close()
 
 
+@pytest.mark.parametrize("E", [64, 128, 200, 256])
+def test_one_token_cluster_router_matches_oracle(E):
+    """A single token with up to 256 experts: one thread-block cluster computes
+    the logits (one warp per expert row) and its first CTA selects from them in
+    shared memory; logits within 1e-5 of the oracle's, the selection exactly
+    the oracle's selection of the GPU's logits, twelve calls in a row on one
+    handle (fresh inputs each time) all equal to it."""
+    H, k = 4096, 6
+    W = synth.router_weights_bf16(E, H, layer=4)
+    h = _handle(E, H, k, 1)
+    try:
+        wd = torch.from_numpy(W.view(np.int16)).cuda()
+        for step in range(12):
+            x = synth.activations_bf16(1, H, seed=90 + step)
+            xd = torch.from_numpy(x.view(np.int16)).cuda()
+            logits = torch.empty((1, E), dtype=torch.float32, device="cuda")
+            idx = torch.full((1, k), -7, dtype=torch.int32, device="cuda")
+            w = torch.empty((1, k), dtype=torch.float32, device="cuda")
+            moe.moe_router_topk(h, xd, wd, 1, idx, w, logits=logits)
+            torch.cuda.synchronize()
+            got_l = logits.cpu().numpy().astype(np.float64)
+            assert np.abs(got_l - oracle.router_logits(x, W)).max() <= 1e-5
+            ci, cw = oracle.topk_softmax(got_l, k)
+            assert np.array_equal(idx.cpu().numpy(), ci), f"step {step}"
+            assert np.abs(w.cpu().numpy() - cw).max() <= 2e-6
+        assert moe.moe_ffn_status(h) == moe.MOE_OK
+    finally:
+        moe.moe_ffn_destroy(h)
+
+
 @pytest.mark.parametrize("E", [130, 384, 1000])
 def test_single_launch_router_repeats_and_ragged_expert_rows(E):
     """At T <= 8 one launch computes the logits and, in the last CTA of each
@@ -176,3 +206,4 @@ def test_router_feeds_layer_on_one_stream_without_waits(T):
         assert moe.moe_ffn_status(L.h) == moe.MOE_OK
     finally:
         L.close()
+
