@@ -38,7 +38,7 @@ EXPORTS = [
     "moe_expert_cache_create", "moe_expert_cache_fetch", "moe_expert_cache_prefetch", "moe_expert_cache_slot",
     "moe_expert_cache_stats", "moe_expert_cache_destroy", "moe_ffn_test_set_wait", "moe_ffn_test_fail_allocs",
     "moe_ffn_test_copy_h",
-    "moe_ffn_set_mma_kind",
+    "moe_ffn_set_mma_kind", "moe_ffn_set_routing_wait",
     "moe_ffn_profile_layer_only",
 ]
 
@@ -117,6 +117,7 @@ def lib() -> ctypes.CDLL:
             "moe_ffn_test_fail_allocs": (None, [I]),
             "moe_ffn_test_copy_h": (I, [P, P, P, I, P]),
             "moe_ffn_set_mma_kind": (I, [P, I]),
+            "moe_ffn_set_routing_wait": (I, [P, I]),
             "moe_ffn_profile_layer_only": (I, [P, I]),
         }
         for name, (res, args) in sig.items():
@@ -236,6 +237,11 @@ def moe_ffn_profile_layer_only(h, on: bool = True) -> None:
 def moe_ffn_set_mma_kind(h, kind: int) -> None:
     """The expert-major path's MMA in the E4M3 mode (MOE_MMA_*)."""
     _check(lib().moe_ffn_set_mma_kind(h, int(kind)), "moe_ffn_set_mma_kind")
+
+
+def moe_ffn_set_routing_wait(h, on: int) -> None:
+    """1: the layer's kernels read the routing only after their dependency wait."""
+    _check(lib().moe_ffn_set_routing_wait(h, int(on)), "moe_ffn_set_routing_wait")
 
 
 def moe_ffn_status(h, stream=None) -> int:

@@ -637,12 +637,36 @@ int moe_ffn_profile_layer_only(moe_ffn_t h, int on)
     return MOE_OK;
 }
 
+// The cached graphs hold the kernel arguments of the settings they were
+// captured with: a settings change drops them (after the device is done with
+// them), and the next calls capture new ones.
+static int drop_graphs(moe_ffn* h)
+{
+    if (h->graphs.empty() && h->hgraphs.empty()) return MOE_OK;
+    DeviceGuard guard(h->device);
+    if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+    for (auto& g : h->graphs) cudaGraphExecDestroy(g.exec);
+    for (auto& g : h->hgraphs) cudaGraphExecDestroy(g.exec);
+    h->graphs.clear();
+    h->hgraphs.clear();
+    return MOE_OK;
+}
+
+int moe_ffn_set_routing_wait(moe_ffn_t h, int on)
+{
+    if (!h || (on != 0 && on != 1)) return MOE_ERR_INVALID_ARG;
+    if (h->base.routing_after_wait == on) return MOE_OK;
+    h->base.routing_after_wait = on;
+    return drop_graphs(h);
+}
+
 int moe_ffn_set_mma_kind(moe_ffn_t h, int kind)
 {
     if (!h || (kind != MOE_MMA_AUTO && kind != MOE_MMA_MXF4_PIECES && kind != MOE_MMA_MXF8F6F4))
         return MOE_ERR_INVALID_ARG;
+    if (h->mma_kind == kind) return MOE_OK;
     h->mma_kind = kind;
-    return MOE_OK;
+    return drop_graphs(h);
 }
 
 void moe_ffn_test_fail_allocs(int n) { g_fail_allocs.store(n > 0 ? n : 0); }

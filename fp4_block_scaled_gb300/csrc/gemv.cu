@@ -994,6 +994,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(GemvArgs a, StreamPlan p0
         sm.fin_word = 0;
         mbar_fence_init();
     }
+    // a caller whose routing comes from a kernel that releases its dependents
+    // early asks for the routing to be read after the dependency wait
+    if (a.routing_after_wait) pdl_wait();
     if (warp == 0) {
         // resolve the CTA's first jobs of both projections (expert pointers), one
         // per lane and projection, the two projections' loads in flight together

@@ -48,6 +48,8 @@ struct GemvArgs {
     int debug_withhold;                 // test hook: CTA 0 never reports its finished gate/up groups
     int skip_prep;                      // measurement mode: launch the layer kernel alone (the
                                         // activation pieces of the previous call are reused)
+    int routing_after_wait;             // read idx, w and the expert table only after the
+                                        // dependency wait (their writer may release early)
     // residual stream: per token, the sum of squares of each 32 rows of x that
     // the layer's down projection wrote ([T][H / 32]); ssq_in: the previous
     // layer left them for this layer's x (its RMSNorm reads them, not x)

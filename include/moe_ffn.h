@@ -139,9 +139,21 @@ int moe_ffn_pack_expert(moe_ffn_t h, const void* canon_codes, const void* canon_
  * stream work that completes before a dependent launch may begin: an ordinary
  * kernel or copy, or moe_router_topk / moe_router_select (which let the next
  * launch start only once their outputs are written) -- not by a kernel that
- * lets dependents launch early. */
+ * lets dependents launch early, unless moe_ffn_set_routing_wait(h, 1) is set. */
 int moe_ffn_forward(moe_ffn_t h, const void* x, const int32_t* topk_idx, const float* topk_w,
                     const moe_expert_table* tbl, void* y, int T, void* stream);
+
+/* on = 1: the layer's kernels read topk_idx, topk_w and the expert table only
+ * after they have waited for the stream's previous kernel, so those inputs may
+ * come from a kernel that lets its dependents launch early (programmatic
+ * dependent launch) and writes them afterwards.  The weight stream then starts
+ * only once that kernel has completed (at batch 1 the layer loses the overlap
+ * with the previous kernel's tail).  on = 0 (the default): as documented at
+ * moe_ffn_forward.  Applies to moe_ffn_forward, moe_ffn_forward_host and
+ * moe_stack_forward on this handle; results are identical either way.  A
+ * change drops the handle's cached graphs (after waiting for the device), so
+ * the next calls capture new ones.  Errors: INVALID_ARG, CUDA. */
+int moe_ffn_set_routing_wait(moe_ffn_t h, int on);
 
 /* moe_ffn_forward with HOST x / topk_idx / topk_w / y (any host memory; the
  * call waits for `stream` before it returns).  Small batches (x and y
@@ -305,10 +317,11 @@ int moe_ffn_profile_read(moe_ffn_t h, double* ms, int* launches);
  *   MOE_MMA_MXF8F6F4 ("direct"): the activations as they are, one slot per MMA
  *     column -- E4M3 mode (MOE_ACT_E4M3_UE8M0_128): tcgen05.mma
  *     kind::mxf8f6f4, the E2M1 weights times the E4M3 rows, groups of up to
- *     240 slots of an expert where T * topk >= 128 * E, else up to 64; E2M1
- *     mode (MOE_ACT_E2M1_UE8M0_32): kind::mxf4, the E2M1 weights as the blob
- *     holds them times the E2M1 rows (FP4 on both sides), groups of up to
- *     240.  Six launches (route, prep, gate/up, h quantizer, down, combine).
+ *     224 slots of an expert (one MMA issuer and a scale-copy thread) where
+ *     T * topk >= 128 * E, else up to 64 (three issuers); E2M1 mode
+ *     (MOE_ACT_E2M1_UE8M0_32): kind::mxf4, the E2M1 weights as the blob holds
+ *     them times the E2M1 rows (FP4 on both sides), groups of up to 224.  Six
+ *     launches (route, prep, gate/up, h quantizer, down, combine).
  *   MOE_MMA_MXF4_PIECES: kind::mxf4 with the activations carried as E2M1
  *     pieces (8 per E4M3 value, groups of up to 8 slots; 1 per E2M1 value,
  *     groups of up to 16).
@@ -318,7 +331,8 @@ int moe_ffn_profile_read(moe_ffn_t h, double* ms, int* launches);
  * All compute the same function within the float tolerance ([8GB] §三个从不抛错的
  * Bug, item 2, fixes the E4M3 + ue8m0-per-128 activation format; the pages
  * leave the MMA to the build).  The bf16 mode and the slot-major path are not
- * affected.  Errors: INVALID_ARG. */
+ * affected.  A change drops the handle's cached graphs (after waiting for the
+ * device).  Errors: INVALID_ARG, CUDA. */
 enum { MOE_MMA_AUTO = 0, MOE_MMA_MXF4_PIECES = 1, MOE_MMA_MXF8F6F4 = 2 };
 int moe_ffn_set_mma_kind(moe_ffn_t h, int kind);
 

@@ -207,3 +207,61 @@ def test_router_feeds_layer_on_one_stream_without_waits(T):
     finally:
         L.close()
 
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_routing_wait_gives_identical_results(T):
+    """moe_ffn_set_routing_wait(h, 1) (the routing read after the layer's
+    dependency wait) changes no bit: a forward and a 3-layer stack with the
+    setting on equal the same calls with it off (the cached stack graph is
+    dropped and captured again at each change), and router -> layer chained on
+    one stream without host waits stays equal to the synchronized forwards."""
+    E, H, I, k, L = 16, 4096, 2880, 6, 3
+    lay = Layer(E=E, H=H, I=I, k=k, max_tokens=T)
+    try:
+        x = synth.activations_bf16(T, H, seed=140 + T)
+        idx = synth.routing_uniform(T, E, k, seed=140 + T)
+        w = synth.routing_weights(T, k, seed=140 + T)
+        y_off = lay.run(x, idx, w)
+        moe.moe_ffn_set_routing_wait(lay.h, 1)
+        y_on = lay.run(x, idx, w)
+        assert torch.equal(y_off.view(torch.int32), y_on.view(torch.int32))
+        # a stack of L layers (the handle's experts in every layer), on then off
+        it = torch.from_numpy(np.stack([synth.routing_uniform(T, E, k, seed=150 + l) for l in range(L)])).cuda()
+        wt = torch.from_numpy(np.stack([synth.routing_weights(T, k, seed=150 + l) for l in range(L)])).cuda()
+        x0 = torch.from_numpy(synth.activations_f32(T, H, seed=160)).cuda()
+        outs = []
+        for on in (1, 0, 1):
+            moe.moe_ffn_set_routing_wait(lay.h, on)
+            xs = x0.clone()
+            moe.moe_stack_forward(lay.h, xs, [lay.es.table] * L, it, wt, L, T)
+            torch.cuda.synchronize()
+            outs.append(xs)
+        assert torch.equal(outs[0].view(torch.int32), outs[1].view(torch.int32))
+        assert torch.equal(outs[0].view(torch.int32), outs[2].view(torch.int32))
+        # router -> layer chained with the setting on
+        moe.moe_ffn_set_routing_wait(lay.h, 1)
+        Wd = torch.from_numpy(synth.router_weights_bf16(E, H, layer=5).view(np.int16)).cuda()
+        s = torch.cuda.Stream()
+        ri = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        rw = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        xs_ = [torch.from_numpy(synth.activations_bf16(T, H, seed=170 + i).view(np.int16)).cuda() for i in range(4)]
+        ys = [torch.empty((T, H), dtype=torch.float32, device="cuda") for _ in range(4)]
+        ri_s = [torch.empty_like(ri) for _ in range(4)]
+        rw_s = [torch.empty_like(rw) for _ in range(4)]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            for i in range(4):
+                moe.moe_router_topk(lay.h, xs_[i], Wd, T, ri, rw, stream=s)
+                moe.moe_ffn_forward(lay.h, xs_[i], ri, rw, lay.es.table, ys[i], T, s)
+                ri_s[i].copy_(ri)
+                rw_s[i].copy_(rw)
+        s.synchronize()
+        for i in range(4):
+            yr = torch.empty((T, H), dtype=torch.float32, device="cuda")
+            moe.moe_ffn_forward(lay.h, xs_[i], ri_s[i], rw_s[i], lay.es.table, yr, T)
+            torch.cuda.synchronize()
+            assert torch.equal(ys[i].view(torch.int32), yr.view(torch.int32)), f"step {i}"
+        assert moe.moe_ffn_status(lay.h) == moe.MOE_OK
+    finally:
+        lay.close()
