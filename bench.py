@@ -714,22 +714,20 @@ def run_ours(args, wl):
             moe.moe_ffn_forward_host(h, xp[i], ip[i], wp[i], tb0, yp, T, sp)
         h2d = T * H * 2 + 2 * T * k * 4
     else:
-        xin = torch.empty((T, H), dtype=torch.int16, device="cuda")
-        idev = torch.empty((L, T, k), dtype=torch.int32, device="cuda")
-        wdev = torch.empty((L, T, k), dtype=torch.float32, device="cuda")
-        xf = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        # the residual of each step in host memory (fp32, updated in place by the
+        # call), reset from the step's input before every call
         tables = [es.table for es in sets]
+        x32 = (x_np.view(np.uint16).astype(np.uint32) << 16).view(np.float32)      # bf16 -> fp32, exact
+        xw = torch.empty((T, H), dtype=torch.float32).pin_memory()
+        xw_np = xw.numpy()
+        ih_np = [np.ascontiguousarray(idx_np[i]) for i in range(R)]
+        wh_np = [np.ascontiguousarray(w_np[i]) for i in range(R)]
+        xwp, sp = xw.data_ptr(), stream.cuda_stream
 
         def e2e_step(i):
-            with torch.cuda.stream(stream):
-                xin.copy_(xh[i], non_blocking=True)
-                idev.copy_(ih[i], non_blocking=True)
-                wdev.copy_(wh[i], non_blocking=True)
-                xf.copy_(xin.view(torch.bfloat16))
-                moe.moe_stack_forward(h, xf, tables, idev, wdev, L, T, stream)
-                yh.copy_(xf, non_blocking=True)
-            stream.synchronize()
-        h2d = T * H * 2 + 2 * L * T * k * 4
+            np.copyto(xw_np, x32[i])
+            moe.moe_stack_forward_host(h, xwp, tables, ih_np[i].ctypes.data, wh_np[i].ctypes.data, L, T, sp)
+        h2d = T * H * 4 + 2 * L * T * k * 4
     for i in range(3):
         e2e_step(i % R)
     t0 = time.perf_counter()

@@ -32,7 +32,8 @@ DEFAULT_GEMM_MIN_TOKENS = 16   # MOE_DEFAULT_GEMM_MIN_TOKENS
 EXPORTS = [
     "moe_ffn_packed_expert_bytes", "moe_ffn_create",
     "moe_ffn_pack_expert", "moe_ffn_forward", "moe_ffn_forward_host", "moe_ffn_route",
-    "moe_ffn_act_quant", "moe_stack_forward", "moe_ffn_profile_enable", "moe_ffn_profile_read",
+    "moe_ffn_act_quant", "moe_stack_forward", "moe_stack_forward_host", "moe_ffn_profile_enable",
+    "moe_ffn_profile_read",
     "moe_ffn_status", "moe_ffn_strerror", "moe_ffn_destroy", "moe_ffn_forward_noalloc",
     "moe_router_topk", "moe_router_select", "moe_batch_plan", "moe_batch_distinct",
     "moe_expert_cache_create", "moe_expert_cache_fetch", "moe_expert_cache_prefetch", "moe_expert_cache_slot",
@@ -96,6 +97,7 @@ def lib() -> ctypes.CDLL:
             "moe_ffn_route": (I, [P, P, I, P, P, P, P, P]),
             "moe_ffn_act_quant": (I, [P, P, I, I, P, P, P]),
             "moe_stack_forward": (I, [P, P, tblp, P, P, I, I, P]),
+            "moe_stack_forward_host": (I, [P, P, tblp, P, P, I, I, P]),
             "moe_ffn_profile_enable": (I, [P, I]),
             "moe_ffn_profile_read": (I, [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I)]),
             "moe_ffn_status": (I, [P, P]),
@@ -214,6 +216,15 @@ def moe_stack_forward(h, x, tables, topk_idx, topk_w, L: int, T: int, stream=Non
     arr = (moe_expert_table * len(tables))(*tables)
     _check(lib().moe_stack_forward(h, _p(x), arr, _p(topk_idx), _p(topk_w), int(L), int(T),
                                    _s(stream)), "moe_stack_forward")
+
+
+def moe_stack_forward_host(h, x_host, tables, topk_idx_host, topk_w_host, L: int, T: int, stream=None):
+    """Host buffers (CPU tensors or ints holding host addresses): x fp32 [T][H]
+    updated in place, topk_idx int32 / topk_w fp32 [L][T][k]; waits for the
+    stream.  tables: a sequence of moe_expert_table, one per layer."""
+    arr = (moe_expert_table * len(tables))(*tables)
+    _check(lib().moe_stack_forward_host(h, _p(x_host), arr, _p(topk_idx_host), _p(topk_w_host), int(L), int(T),
+                                        _s(stream)), "moe_stack_forward_host")
 
 
 def moe_ffn_profile_enable(h, on: bool = True) -> None:

@@ -52,6 +52,22 @@ void evict_lru_graph(std::vector<G>& graphs)
 
 }  // namespace
 
+// n 16-byte words from src to dst (the host-buffer stack call's staging copies,
+// mapped host memory <-> device memory)
+__global__ void k_stage_copy(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n)
+{
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
+static cudaError_t launch_stage_copy(const void* src, void* dst, size_t bytes, cudaStream_t s)
+{
+    const size_t n = bytes / 16;
+    const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, 64);
+    k_stage_copy<<<blocks, 256, 0, s>>>((const uint4*)src, (uint4*)dst, n);
+    return cudaGetLastError();
+}
+
 struct moe_ffn {
     moe_ffn_config cfg;
     int device;
@@ -70,6 +86,13 @@ struct moe_ffn {
     std::vector<HostGraph> hgraphs;
     cudaStream_t cap_stream;    // private stream used only for graph capture
     std::vector<StackGraph> graphs;
+    // moe_stack_forward_host: page-locked mapped staging (x | idx | w) and its
+    // device copy, grown on demand, and the graphs of the whole call
+    uint8_t* sstage;
+    uint8_t* sstage_dev;
+    uint8_t* sdev;
+    size_t scap;
+    std::vector<StackGraph> sgraphs;
     unsigned long long use_clock;
     Profiler* prof;             // non-null while moe_ffn_profile_enable(h, 1)
     float* rlogits;             // router logits scratch [max_tokens][E]
@@ -630,6 +653,97 @@ int moe_stack_forward(moe_ffn_t h, float* x, const moe_expert_table* tbls,
     return cuda_rc(cudaGraphLaunch(exec, s));
 }
 
+int moe_stack_forward_host(moe_ffn_t h, float* x_host, const moe_expert_table* tbls,
+                           const int32_t* topk_idx_host, const float* topk_w_host, int L, int T, void* stream)
+{
+    if (!h || L < 0 || T < 0 || T > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+    if (L == 0 || T == 0) return MOE_OK;
+    if (!x_host || !tbls || !topk_idx_host || !topk_w_host) return MOE_ERR_INVALID_ARG;
+    for (int l = 0; l < L; l++)
+        if (!tbls[l].experts) return MOE_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    cudaStream_t s = (cudaStream_t)stream;
+    const int H = h->cfg.hidden, k = h->cfg.topk;
+    const size_t xb = (size_t)T * H * 4, rb = (size_t)L * T * k * 4;
+    const size_t io = align_up(xb, 256), wo = io + align_up(rb, 256), total = wo + align_up(rb, 256);
+    if (total > h->scap) {
+        // grow: the previous call waited for its stream, so the old buffers are idle;
+        // graphs that name them go with them
+        for (auto& g : h->sgraphs) cudaGraphExecDestroy(g.exec);
+        h->sgraphs.clear();
+        if (h->sstage) cudaFreeHost(h->sstage);
+        if (h->sdev) cudaFree(h->sdev);
+        h->sstage = h->sstage_dev = h->sdev = nullptr;
+        h->scap = 0;
+        void* p = nullptr;
+        void* d = nullptr;
+        void* dv = nullptr;
+        if (lib_host_alloc(&p, total, cudaHostAllocMapped) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_OOM;
+        }
+        if (lib_malloc(&dv, total) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFreeHost(p);
+            return MOE_ERR_OOM;
+        }
+        if (cudaHostGetDevicePointer(&d, p, 0) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFreeHost(p);
+            cudaFree(dv);
+            return MOE_ERR_CUDA;
+        }
+        h->sstage = (uint8_t*)p;
+        h->sstage_dev = (uint8_t*)d;
+        h->sdev = (uint8_t*)dv;
+        h->scap = total;
+    }
+    memcpy(h->sstage, x_host, xb);
+    memcpy(h->sstage + io, topk_idx_host, rb);
+    memcpy(h->sstage + wo, topk_w_host, rb);
+    float* xd = (float*)h->sdev;
+    const int32_t* id = (const int32_t*)(h->sdev + io);
+    const float* wd = (const float*)(h->sdev + wo);
+    std::vector<const void*> key((size_t)L);
+    for (int l = 0; l < L; l++) key[l] = tbls[l].experts;
+    h->use_clock++;
+    StackGraph* g = nullptr;
+    for (auto& c : h->sgraphs)
+        if (c.L == L && c.T == T && c.tables == key) g = &c;
+    cudaError_t e = cudaSuccess;
+    if (!g) {
+        // one graph for the whole call: the inputs from the mapped staging buffer
+        // into device memory (one copy kernel), the L layers, x back
+        cudaGraph_t graph = nullptr;
+        e = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        cudaError_t le = launch_stage_copy(h->sstage_dev, h->sdev, total, h->cap_stream);
+        for (int l = 0; l < L && le == cudaSuccess; l++)
+            le = launch_layer(h, nullptr, xd, id + (size_t)l * T * k, wd + (size_t)l * T * k, &tbls[l], nullptr, T,
+                              h->cap_stream, nullptr, l > 0);
+        if (le == cudaSuccess) le = launch_stage_copy(h->sdev, h->sstage_dev, align_up(xb, 16), h->cap_stream);
+        e = cudaStreamEndCapture(h->cap_stream, &graph);
+        if (le != cudaSuccess || e != cudaSuccess) {
+            if (graph) cudaGraphDestroy(graph);
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+        cudaGraphExec_t exec = nullptr;
+        e = cudaGraphInstantiate(&exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        evict_lru_graph(h->sgraphs);
+        h->sgraphs.push_back(StackGraph{xd, id, wd, L, T, key, exec, 0});
+        g = &h->sgraphs.back();
+    }
+    g->last_use = h->use_clock;
+    e = cudaGraphLaunch(g->exec, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    memcpy(x_host, h->sstage, xb);
+    return MOE_OK;
+}
+
 int moe_ffn_profile_layer_only(moe_ffn_t h, int on)
 {
     if (!h) return MOE_ERR_INVALID_ARG;
@@ -642,13 +756,15 @@ int moe_ffn_profile_layer_only(moe_ffn_t h, int on)
 // them), and the next calls capture new ones.
 static int drop_graphs(moe_ffn* h)
 {
-    if (h->graphs.empty() && h->hgraphs.empty()) return MOE_OK;
+    if (h->graphs.empty() && h->hgraphs.empty() && h->sgraphs.empty()) return MOE_OK;
     DeviceGuard guard(h->device);
     if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
     for (auto& g : h->graphs) cudaGraphExecDestroy(g.exec);
     for (auto& g : h->hgraphs) cudaGraphExecDestroy(g.exec);
+    for (auto& g : h->sgraphs) cudaGraphExecDestroy(g.exec);
     h->graphs.clear();
     h->hgraphs.clear();
+    h->sgraphs.clear();
     return MOE_OK;
 }
 
@@ -769,7 +885,10 @@ void moe_ffn_destroy(moe_ffn_t h)
     DeviceGuard guard(h->device);
     for (auto& g : h->graphs) cudaGraphExecDestroy(g.exec);
     for (auto& g : h->hgraphs) cudaGraphExecDestroy(g.exec);
+    for (auto& g : h->sgraphs) cudaGraphExecDestroy(g.exec);
     if (h->host_stage) cudaFreeHost(h->host_stage);
+    if (h->sstage) cudaFreeHost(h->sstage);
+    if (h->sdev) cudaFree(h->sdev);
     delete h->prof;
     if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
     cudaFree(h->ws);

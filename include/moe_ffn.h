@@ -288,6 +288,18 @@ int moe_stack_forward(moe_ffn_t h, float* x, const moe_expert_table* tbls,
                       const int32_t* topk_idx, const float* topk_w, int L, int T,
                       void* stream);
 
+/* moe_stack_forward with HOST x (fp32 [T][H], updated in place), topk_idx and
+ * topk_w (int32 / fp32 [L][T][k]); the call waits for `stream` before it
+ * returns.  The inputs are packed into a page-locked staging buffer of the
+ * handle that is mapped into the device's address space (grown on demand),
+ * and one CUDA graph per (T, L, expert tables) copies them into device memory
+ * with one kernel, runs the L layers and copies x back into the staging
+ * buffer, from which it is copied out on the host.  Results equal
+ * moe_stack_forward's bit for bit.  Returns MOE_ERR_OOM if the staging
+ * buffers cannot be allocated. */
+int moe_stack_forward_host(moe_ffn_t h, float* x_host, const moe_expert_table* tbls,
+                           const int32_t* topk_idx_host, const float* topk_w_host, int L, int T, void* stream);
+
 /* Per-kernel timing, a tracing aid.  While enabled, forward calls record a
  * CUDA event pair around each of their kernel launches on the call's stream
  * (this also stops a kernel's prologue from overlapping the previous kernel).
