@@ -168,3 +168,44 @@ def test_mxf4_direct_and_pieces_agree_e2m1():
     finally:
         Ld.close()
         Lp.close()
+
+
+def test_mma_kind_change_replaces_the_cached_stack_graph():
+    """The stack's cached graph holds the MMA kind it was captured with: after
+    moe_ffn_set_mma_kind the same call (same pointers) runs the new kind, bit
+    for bit what a fresh handle set to that kind computes, and switching back
+    gives the first result again."""
+    E, H, I, k, T, NL = 8, 256, 448, 2, 48, 3
+    cfg = moe.config(E, H, I, k, T, act_mode=E4M3, gemm_min_tokens=1)
+    from moe_setup import fill_layer
+    h = moe.moe_ffn_create(cfg, 0)
+    h2 = moe.moe_ffn_create(cfg, 0)
+    try:
+        sets = [fill_layer(h, cfg, layer=l) for l in range(NL)]
+        idx = torch.from_numpy(np.stack([synth.routing_uniform(T, E, k, seed=500 + l) for l in range(NL)])).cuda()
+        w = torch.from_numpy(np.stack([synth.routing_weights(T, k, seed=500 + l) for l in range(NL)])).cuda()
+        x0 = torch.from_numpy(synth.activations_f32(T, H, seed=22)).cuda()
+        x = torch.empty_like(x0)
+        tables = [s.table for s in sets]
+
+        def run(hh):
+            x.copy_(x0)
+            moe.moe_stack_forward(hh, x, tables, idx, w, NL, T)
+            torch.cuda.synchronize()
+            return x.clone()
+
+        moe.moe_ffn_set_mma_kind(h, F8)
+        y_f8 = run(h)
+        moe.moe_ffn_set_mma_kind(h, moe.MOE_MMA_MXF4_PIECES)
+        y_pc = run(h)
+        moe.moe_ffn_set_mma_kind(h2, moe.MOE_MMA_MXF4_PIECES)
+        y_pc_ref = run(h2)
+        moe.moe_ffn_set_mma_kind(h, F8)
+        y_f8_again = run(h)
+        assert torch.equal(y_pc.view(torch.int32), y_pc_ref.view(torch.int32))
+        assert torch.equal(y_f8.view(torch.int32), y_f8_again.view(torch.int32))
+        assert not torch.equal(y_f8.view(torch.int32), y_pc.view(torch.int32))   # the two kinds differ in rounding
+        assert moe.moe_ffn_status(h) == moe.MOE_OK
+    finally:
+        moe.moe_ffn_destroy(h)
+        moe.moe_ffn_destroy(h2)
