@@ -616,21 +616,30 @@ def run_ours(args, wl):
     with torch.cuda.stream(stream):
         moe.moe_router_topk(h, x_d[0], Wr, T, r_idx, r_w, stream=stream)     # warm-up outside capture
     stream.synchronize()
-    g_r = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_r, stream=stream):
-        for i in range(nrg):
-            moe.moe_router_topk(h, x_d[i % R], Wrs[i], T, r_idx, r_w, stream=stream)
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            g_r.replay()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(10):
-            g_r.replay()
-        ev1.record(stream)
-    stream.synchronize()
-    r_us_graph = ev0.elapsed_time(ev1) * 1e3 / (10 * nrg)
-    del g_r, Wrs
+    def router_graph_us():
+        g_r = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_r, stream=stream):
+            for i in range(nrg):
+                moe.moe_router_topk(h, x_d[i % R], Wrs[i], T, r_idx, r_w, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g_r.replay()
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            for _ in range(10):
+                g_r.replay()
+            ev1.record(stream)
+        stream.synchronize()
+        return ev0.elapsed_time(ev1) * 1e3 / (10 * nrg)
+
+    r_us_graph = router_graph_us()
+    # (d) with the handle's layer kernels reading the routing after their
+    # dependency wait (moe_ffn_set_routing_wait), the router lets the next
+    # launch start at once
+    moe.moe_ffn_set_routing_wait(h, 1)
+    r_us_graph_rel = router_graph_us()
+    moe.moe_ffn_set_routing_wait(h, 0)
+    del Wrs
     moe.moe_ffn_profile_enable(h, True)
     nrt = 200
     with torch.cuda.stream(stream):
@@ -646,7 +655,7 @@ def run_ours(args, wl):
     # layer calls on the pre-drawn routings, both one CUDA graph; the difference
     # per layer is what the router adds to a step (its launch and weight loads
     # overlap the previous layer's kernel as programmatic dependent launch allows)
-    r_in_step = None
+    r_in_step = r_in_step_rel = None
     if T <= 8:
         nl = 40
         Wl = torch.randn((nl, E, H), generator=gen, device="cuda").to(torch.bfloat16).view(torch.int16)
@@ -668,8 +677,9 @@ def run_ours(args, wl):
             return g
 
         times = []
-        for mode in ("none", "router"):
-            g = step_graph(mode)
+        for mode in ("none", "router", "router_rel"):
+            moe.moe_ffn_set_routing_wait(h, 1 if mode == "router_rel" else 0)
+            g = step_graph("router" if mode == "router_rel" else mode)
             with torch.cuda.stream(stream):
                 for _ in range(3):
                     g.replay()
@@ -682,19 +692,25 @@ def run_ours(args, wl):
             times.append(e0.elapsed_time(e1) * 1e3 / (10 * nl))
             del g
         r_in_step = times[1] - times[0]
+        r_in_step_rel = times[2] - times[0]
+        moe.moe_ffn_set_routing_wait(h, 0)
         del Wl
     router = {"kernels": ("k_router_cluster (one thread-block cluster: logits, then the selection in its first CTA)"
                           if T == 1 and E <= 256 else
                           "k_router_logits (selection in its last CTA per token tile)") if T <= 8
               else "k_router_mma + k_router_select",
-              "us": r_us_graph, "us_alone": r_us, "us_in_step": r_in_step, "algorithmic_bytes": r_bytes,
+              "us": r_us_graph, "us_alone": r_us, "us_in_step": r_in_step,
+              "routing_wait": {"us": r_us_graph_rel, "us_in_step": r_in_step_rel},
+              "algorithmic_bytes": r_bytes,
               "gbs": r_bytes / (r_us_graph * 1e-6) / 1e9,
               "frac_of_hbm": r_bytes / (r_us_graph * 1e-6) / 1e9 / peak,
               "launches": 1 if T <= 8 else 2, "timing": f"us: per call, {nrg} calls back to back in a CUDA graph, each on its "
                                        "own router matrix (256 MB in all, > L2); us_alone: events around "
                                        "each call, one matrix; us_in_step: per layer, a graph of 40 "
                                        "(moe_router_topk -> moe_ffn_forward on its routing) pairs less a graph "
-                                       "of the same 40 layers on pre-drawn routings"}
+                                       "of the same 40 layers on pre-drawn routings; routing_wait: the same two "
+                                       "with moe_ffn_set_routing_wait(h, 1) (the layer reads the routing after its "
+                                       "dependency wait, so the router releases the next launch at once)"}
 
     # ---- end to end through the public API from host buffers: every step copies
     # its inputs in from pinned host memory and its result back

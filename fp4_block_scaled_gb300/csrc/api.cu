@@ -573,6 +573,7 @@ int moe_router_topk(moe_ffn_t h, const void* x, const void* router_w, int T, flo
     RouterArgs a{(const uint16_t*)x, (const uint16_t*)router_w, logits ? logits : h->rlogits, topk_idx, topk_w,
                  T, h->cfg.hidden, h->cfg.num_experts, h->cfg.topk, 0};
     a.status = h->status;
+    a.release_early = h->base.routing_after_wait;
     // batches above 8 tokens: the tensor cores, in split-K partials that the
     // selection adds up; smaller ones stream the weights on the CUDA cores
     a.part = h->rpart;

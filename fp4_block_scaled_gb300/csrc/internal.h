@@ -243,6 +243,9 @@ struct RouterArgs {
     // non-null: k_router_logits also selects (the last CTA of each token tile,
     // counted here; [ceil(T / tpc)] ints, zero between launches)
     int* tickets;
+    // the handle's layer kernels read the routing only after their dependency
+    // wait, so the router kernels may let the next launch start at once
+    int release_early;
 };
 int router_max_experts();
 int router_tokens_per_cta(int H);     // 0: H too large for the logits kernel

@@ -41,8 +41,10 @@ __global__ void __launch_bounds__(256) k_router_select(RouterArgs a)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     pdl_wait();
-    // no early launch_dependents: the next kernel may read topk_idx / topk_w
-    // before its own griddepcontrol.wait, so it starts only once they are written
+    // no early launch_dependents (unless the handle's layer reads the routing
+    // after its own wait): the next kernel may read topk_idx / topk_w before its
+    // griddepcontrol.wait, so it starts only once they are written
+    if (a.release_early) pdl_trigger();
     if (t >= a.T) return;
     select_token<R>(a, t, lane);
 }
@@ -84,7 +86,7 @@ __global__ void __launch_bounds__(NW * 32) k_router_logits(RouterArgs a)
             wv[i] = c < H8 ? ldg_stream_v4(wrow + c) : make_uint4(0, 0, 0, 0);
         }
         pdl_wait();
-        if (!a.tickets) pdl_trigger();     // selecting here: dependents start at completion
+        if (!a.tickets || a.release_early) pdl_trigger();     // selecting here: dependents start at completion
         stage_x(reinterpret_cast<const uint4*>(a.x + (size_t)t0 * a.H), nt * H8,
                 [&](int i, const uint4 v) { s_x[i] = v; });
         __syncthreads();
@@ -108,7 +110,7 @@ __global__ void __launch_bounds__(NW * 32) k_router_logits(RouterArgs a)
         // fp32 once per CTA ([TPC][H]) and the weights stream
         float4* s_xf = reinterpret_cast<float4*>(s_x);
         pdl_wait();
-        if (!a.tickets) pdl_trigger();     // selecting here: dependents start at completion
+        if (!a.tickets || a.release_early) pdl_trigger();     // selecting here: dependents start at completion
         stage_x(reinterpret_cast<const uint4*>(a.x + (size_t)t0 * a.H), nt * H8, [&](int i, const uint4 v) {
             float f[8];
             bf16x8_to_f32(v, f);
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(NW * 32) k_router_cluster(RouterArgs a)
     const int e = (int)rank * NW + warp;
     uint4 wv[kRChunks];
     row_load(a, e, lane, wv);
+    if (a.release_early) pdl_trigger();
     pdl_wait();
     stage_x(reinterpret_cast<const uint4*>(a.x), a.H / 8, [&](int i, const uint4 v) { s_x[i] = v; });
     __syncthreads();

@@ -150,9 +150,11 @@ int moe_ffn_forward(moe_ffn_t h, const void* x, const int32_t* topk_idx, const f
  * only once that kernel has completed (at batch 1 the layer loses the overlap
  * with the previous kernel's tail).  on = 0 (the default): as documented at
  * moe_ffn_forward.  Applies to moe_ffn_forward, moe_ffn_forward_host and
- * moe_stack_forward on this handle; results are identical either way.  A
- * change drops the handle's cached graphs (after waiting for the device), so
- * the next calls capture new ones.  Errors: INVALID_ARG, CUDA. */
+ * moe_stack_forward on this handle; results are identical either way.  With
+ * it on, moe_router_topk on this handle lets the next launch start at once
+ * (before its outputs are written): only kernels that wait before reading them
+ * may follow it.  A change drops the handle's cached graphs (after waiting for
+ * the device), so the next calls capture new ones.  Errors: INVALID_ARG, CUDA. */
 int moe_ffn_set_routing_wait(moe_ffn_t h, int on);
 
 /* moe_ffn_forward with HOST x / topk_idx / topk_w / y (any host memory; the

@@ -209,13 +209,15 @@ def test_router_feeds_layer_on_one_stream_without_waits(T):
 
 
 
-@pytest.mark.parametrize("T", [1, 4])
+@pytest.mark.parametrize("T", [1, 4, 20])
 def test_routing_wait_gives_identical_results(T):
     """moe_ffn_set_routing_wait(h, 1) (the routing read after the layer's
     dependency wait) changes no bit: a forward and a 3-layer stack with the
     setting on equal the same calls with it off (the cached stack graph is
     dropped and captured again at each change), and router -> layer chained on
-    one stream without host waits stays equal to the synchronized forwards."""
+    one stream without host waits (the router now letting the layer start at
+    once, one launch at T <= 8, logits + selection above) stays equal to the
+    synchronized forwards."""
     E, H, I, k, L = 16, 4096, 2880, 6, 3
     lay = Layer(E=E, H=H, I=I, k=k, max_tokens=T)
     try:
